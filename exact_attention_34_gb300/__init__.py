@@ -1,0 +1,216 @@
+"""Python binding of the GB300 exact-attention C-ABI library (``libattn.so``).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind ``include/attn.h``.  PyTorch supplies device memory and streams.
+The functions named like the C entry points (``attn_fwd``, ``attn_bwd``, ...)
+take torch tensors, read the sizes off their shapes and raise ``AttnError`` on
+any status other than ``ATTN_OK``.  ``forward`` / ``backward`` / ``decode``
+are conveniences that allocate the outputs with torch first.
+
+There is no fallback: if ``libattn.so`` is missing or fails to load, importing
+the functions raises.  Build it with ``exact_attention_34_gb300.build.build()``
+(or ``__graft_entry__.build()``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_WORKSPACE = 3
+ATTN_ERR_CUDA = 4
+ATTN_ERR_DEVICE = 5
+
+ATTN_BF16 = 0
+ATTN_FP32 = 1
+
+_DT = {torch.bfloat16: ATTN_BF16, torch.float32: ATTN_FP32}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}: {detail}")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load libattn.so once (raises if it is not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is not built; run exact_attention_34_gb300.build.build()")
+    L = ctypes.CDLL(_LIB_PATH)
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    sig = {
+        "attn_status_string": (ctypes.c_char_p, [I]),
+        "attn_last_error": (ctypes.c_char_p, []),
+        "attn_fwd": (I, [P, P, P, P, P, I, I, I, I, I, I, F, I, P, I, P]),
+        "attn_bwd_preprocess": (I, [P, P, P, I, I, I, I, I, P]),
+        "attn_bwd_workspace_size": (S, [I, I, I, I, I, I]),
+        "attn_bwd": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, I, I, P, S, P]),
+        "attn_decode_num_splits": (I, [I, I, I, I, I, I]),
+        "attn_decode_splitkv": (I, [P, P, P, P, P, I, I, I, I, I, I, F, I, P, I, I, P]),
+        "attn_decode_combine": (I, [P, P, P, P, I, I, I, I, I, I, P]),
+        "attn_decode_workspace_size": (S, [I, I, I, I, I]),
+        "attn_device_status": (I, [ctypes.POINTER(I), ctypes.POINTER(I), I]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+EXPORTED = (
+    "attn_status_string", "attn_last_error", "attn_fwd", "attn_bwd_preprocess", "attn_bwd_workspace_size",
+    "attn_bwd", "attn_decode_num_splits", "attn_decode_splitkv", "attn_decode_combine",
+    "attn_decode_workspace_size", "attn_device_status",
+)
+
+
+def status_string(s: int) -> str:
+    return lib().attn_status_string(int(s)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != ATTN_OK:
+        raise AttnError(status, where, lib().attn_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype(t) -> int:
+    if t.dtype not in _DT:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return _DT[t.dtype]
+
+
+def _dims(q, k):
+    B, Lq, Hq, d = q.shape
+    Lkv, Hkv = k.shape[1], k.shape[2]
+    return B, Lq, Lkv, Hq, Hkv, d
+
+
+def _scale(scale, d):
+    return 1.0 / math.sqrt(d) if scale is None else float(scale)
+
+
+# ---- entry points with the C names -------------------------------------------
+
+def attn_fwd(q, k, v, o, lse, scale=None, causal=False, kv_lens=None, stream=None):
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    _check(lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Lq, Lkv, Hq, Hkv, d,
+                          _scale(scale, d), int(bool(causal)), _ptr(kv_lens), _dtype(q), _stream(stream)),
+           "attn_fwd")
+
+
+def attn_bwd_preprocess(o, dout, delta, stream=None):
+    B, Lq, Hq, d = o.shape
+    _check(lib().attn_bwd_preprocess(_ptr(o), _ptr(dout), _ptr(delta), B, Lq, Hq, d, _dtype(o), _stream(stream)),
+           "attn_bwd_preprocess")
+
+
+def attn_bwd_workspace_size(B, Lq, Hq, d, deterministic=True, dtype=torch.bfloat16) -> int:
+    return int(lib().attn_bwd_workspace_size(B, Lq, Hq, d, int(bool(deterministic)), _DT[dtype]))
+
+
+def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, scale=None, causal=False, kv_lens=None,
+             deterministic=True, stream=None):
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                          B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d), int(bool(causal)), _ptr(kv_lens), _dtype(q),
+                          int(bool(deterministic)), _ptr(workspace), ws_bytes, _stream(stream)),
+           "attn_bwd")
+
+
+def attn_decode_num_splits(B, Lq, Lkv, Hq, Hkv, d) -> int:
+    return int(lib().attn_decode_num_splits(B, Lq, Lkv, Hq, Hkv, d))
+
+
+def attn_decode_splitkv(q, k_cache, v_cache, o_part, lse_part, num_splits, scale=None, causal=False,
+                        kv_lens=None, stream=None):
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k_cache)
+    _check(lib().attn_decode_splitkv(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o_part), _ptr(lse_part), B, Lq,
+                                     Lkv, Hq, Hkv, d, _scale(scale, d), int(bool(causal)), _ptr(kv_lens),
+                                     int(num_splits), _dtype(q), _stream(stream)),
+           "attn_decode_splitkv")
+
+
+def attn_decode_combine(o_part, lse_part, o, lse, stream=None):
+    B, Hq, S, Lq, d = o_part.shape
+    _check(lib().attn_decode_combine(_ptr(o_part), _ptr(lse_part), _ptr(o), _ptr(lse), B, Lq, Hq, d, S, _dtype(o),
+                                     _stream(stream)),
+           "attn_decode_combine")
+
+
+def attn_decode_workspace_size(B, Lq, Hq, d, num_splits) -> int:
+    return int(lib().attn_decode_workspace_size(B, Lq, Hq, d, num_splits))
+
+
+def attn_device_status(reset=True):
+    code, site = ctypes.c_int(0), ctypes.c_int(0)
+    st = lib().attn_device_status(ctypes.byref(code), ctypes.byref(site), int(bool(reset)))
+    return st, code.value, site.value
+
+
+# ---- conveniences that allocate outputs with torch ------------------------------
+
+def forward(q, k, v, scale=None, causal=False, kv_lens=None, stream=None):
+    """(o, lse) for q [B,Lq,Hq,d], k/v [B,Lkv,Hkv,d] on the GPU."""
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, Lq, device=q.device, dtype=torch.float32)
+    attn_fwd(q, k, v, o, lse, scale, causal, kv_lens, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_lens=None, deterministic=True, stream=None):
+    """(dq, dk, dv) given the forward's o and lse."""
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    nbytes = attn_bwd_workspace_size(B, Lq, Hq, d, deterministic, q.dtype)
+    ws = torch.empty(max(nbytes, 256), device=q.device, dtype=torch.uint8)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, ws, scale, causal, kv_lens, deterministic, stream)
+    return dq, dk, dv
+
+
+def decode(q, k_cache, v_cache, scale=None, causal=False, kv_lens=None, num_splits=0, stream=None,
+           return_partials=False):
+    """Split-KV decode + log-sum-exp combine: (o, lse) [and the partials]."""
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k_cache)
+    S = num_splits if num_splits > 0 else attn_decode_num_splits(B, Lq, Lkv, Hq, Hkv, d)
+    o_part = torch.empty(B, Hq, S, Lq, d, device=q.device, dtype=torch.float32)
+    lse_part = torch.empty(B, Hq, S, Lq, device=q.device, dtype=torch.float32)
+    attn_decode_splitkv(q, k_cache, v_cache, o_part, lse_part, S, scale, causal, kv_lens, stream)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, Lq, device=q.device, dtype=torch.float32)
+    attn_decode_combine(o_part, lse_part, o, lse, stream)
+    if return_partials:
+        return o, lse, o_part, lse_part
+    return o, lse

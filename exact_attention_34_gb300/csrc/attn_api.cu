@@ -1,0 +1,344 @@
+// C-ABI layer: argument validation, TMA descriptor construction, workspace
+// sizing and kernel dispatch.  Everything is checked on the host before a
+// launch; nothing here allocates device memory or synchronises (except
+// attn_device_status, which is documented to).
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <initializer_list>
+#include <utility>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "attn_internal.h"
+
+namespace attn {
+
+// Device-side status word (one per device the library is used on).
+__device__ DeviceStatus g_status;
+
+namespace {
+
+thread_local char t_last_error[512] = "";
+
+attn_status fail(attn_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+attn_status fail(attn_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+attn_status ok() {
+  t_last_error[0] = '\0';
+  return ATTN_OK;
+}
+
+attn_status from_cuda(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return ok();
+  if (e == cudaErrorNotSupported) return fail(ATTN_ERR_UNSUPPORTED, "%s: not supported by this build", what);
+  return fail(ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+DeviceStatus* g_status_ptr[kMaxDevices] = {};
+std::mutex g_status_mu;
+
+// Device address of g_status for the current device (looked up once per device).
+DeviceStatus* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_status_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<DeviceStatus*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Shape/pointer checks common to the forward, backward and decode.
+attn_status check_problem(int B, int Lq, int Lkv, int Hq, int Hkv, int d, float scale, int causal,
+                          attn_dtype dtype) {
+  if (B <= 0 || Lq <= 0 || Lkv <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0)
+    return fail(ATTN_ERR_INVALID_ARG, "sizes must be positive (B=%d Lq=%d Lkv=%d Hq=%d Hkv=%d d=%d)", B, Lq, Lkv,
+                Hq, Hkv, d);
+  if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+  if (!(std::isfinite(scale) && scale > 0.f)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP32) return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head_dim %d not supported (64 or 128)", d);
+  // 32-bit index headroom for per-row offsets (elements of one tensor)
+  const double big = static_cast<double>(B) * Lq * Hq * d;
+  const double bigk = static_cast<double>(B) * Lkv * Hkv * d;
+  if (big >= 9.0e15 || bigk >= 9.0e15) return fail(ATTN_ERR_INVALID_ARG, "tensor too large");
+  if (Lq > (1 << 30) || Lkv > (1 << 30)) return fail(ATTN_ERR_INVALID_ARG, "sequence too long");
+  return ATTN_OK;
+}
+
+attn_status need_ptrs(std::initializer_list<std::pair<const void*, const char*>> ptrs) {
+  for (auto& pr : ptrs) {
+    if (pr.first == nullptr) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", pr.second);
+    if (!aligned16(pr.first)) return fail(ATTN_ERR_INVALID_ARG, "%s is not 16-byte aligned", pr.second);
+  }
+  return ATTN_OK;
+}
+
+Problem make_problem(int B, int Lq, int Lkv, int Hq, int Hkv, int d, float scale, int causal, const int32_t* kl) {
+  Problem p;
+  p.B = B;
+  p.Lq = Lq;
+  p.Lkv = Lkv;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.d = d;
+  p.G = Hq / Hkv;
+  p.causal = causal;
+  p.scale = scale;
+  p.kv_lens = kl;
+  return p;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+bool make_bshd_tmap(CUtensorMap* map, const void* base, bool bf16, int B, int L, int H, int d, int box_inner,
+                    int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t es = bf16 ? 2 : 4;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(H) * d * es, static_cast<cuuint64_t>(d) * es,
+                           static_cast<cuuint64_t>(L) * H * d * es};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int device_sm_count() {
+  static int cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_DEVICE: return "ATTN_ERR_DEVICE";
+  }
+  return "ATTN_ERR_UNKNOWN";
+}
+
+const char* attn_last_error(void) { return t_last_error; }
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Lq, int Lkv,
+                     int Hq, int Hkv, int d, float scale, int causal, const int32_t* kv_lens, attn_dtype dtype,
+                     attn_stream_t stream) {
+  attn_status s = check_problem(B, Lq, Lkv, Hq, Hkv, d, scale, causal, dtype);
+  if (s != ATTN_OK) return s;
+  s = need_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}});
+  if (s != ATTN_OK) return s;
+  if (kv_lens != nullptr && (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "kv_lens is not 4-byte aligned");
+  FwdArgs a;
+  a.pb = make_problem(B, Lq, Lkv, Hq, Hkv, d, scale, causal, kv_lens);
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  DeviceStatus* st = status_ptr();
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = dtype == ATTN_BF16 ? launch_fwd_bf16(a, st, cs) : launch_fwd_f32(a, st, cs);
+  return from_cuda(e, "attn_fwd launch");
+}
+
+attn_status attn_bwd_preprocess(const void* o, const void* dout, float* delta, int B, int Lq, int Hq, int d,
+                                attn_dtype dtype, attn_stream_t stream) {
+  attn_status s = check_problem(B, Lq, Lq, Hq, Hq, d, 1.0f, 0, dtype);
+  if (s != ATTN_OK) return s;
+  s = need_ptrs({{o, "o"}, {dout, "dout"}, {delta, "delta"}});
+  if (s != ATTN_OK) return s;
+  cudaError_t e = launch_bwd_preprocess(o, dout, delta, nullptr, B, Lq, Hq, d, dtype == ATTN_BF16,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  return from_cuda(e, "attn_bwd_preprocess launch");
+}
+
+size_t attn_bwd_workspace_size(int B, int Lq, int Hq, int d, int deterministic, attn_dtype dtype) {
+  (void)dtype;
+  if (B <= 0 || Lq <= 0 || Hq <= 0 || d <= 0) return 0;
+  size_t bytes = align256(static_cast<size_t>(B) * Hq * Lq * sizeof(float));
+  if (!deterministic) bytes += align256(static_cast<size_t>(B) * Lq * Hq * d * sizeof(float));
+  return bytes;
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, int B, int Lq, int Lkv, int Hq, int Hkv, int d, float scale,
+                     int causal, const int32_t* kv_lens, attn_dtype dtype, int deterministic, void* workspace,
+                     size_t workspace_bytes, attn_stream_t stream) {
+  attn_status s = check_problem(B, Lq, Lkv, Hq, Hkv, d, scale, causal, dtype);
+  if (s != ATTN_OK) return s;
+  s = need_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}, {dout, "dout"}, {dq, "dq"}, {dk, "dk"},
+                 {dv, "dv"}});
+  if (s != ATTN_OK) return s;
+  if (kv_lens != nullptr && (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "kv_lens is not 4-byte aligned");
+  if (deterministic != 0 && deterministic != 1) return fail(ATTN_ERR_INVALID_ARG, "deterministic must be 0 or 1");
+  const size_t need = attn_bwd_workspace_size(B, Lq, Hq, d, deterministic, dtype);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                workspace == nullptr ? static_cast<size_t>(0) : workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(ATTN_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  BwdArgs a;
+  a.pb = make_problem(B, Lq, Lkv, Hq, Hkv, d, scale, causal, kv_lens);
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.dout = dout;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.delta = static_cast<float*>(workspace);
+  a.dq_acc = deterministic ? nullptr
+                           : reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                      align256(static_cast<size_t>(B) * Hq * Lq * sizeof(float)));
+  a.deterministic = deterministic;
+  DeviceStatus* st = status_ptr();
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = dtype == ATTN_BF16 ? launch_bwd_bf16(a, st, cs) : launch_bwd_f32(a, st, cs);
+  return from_cuda(e, "attn_bwd launch");
+}
+
+int attn_decode_num_splits(int B, int Lq, int Lkv, int Hq, int Hkv, int d) {
+  (void)d;
+  if (B <= 0 || Lq <= 0 || Lkv <= 0 || Hq <= 0 || Hkv <= 0) return 1;
+  // Enough (batch, KV head, split) programs to fill every SM about 4 times
+  // over while each split keeps at least 2 KV tiles; the lengths themselves
+  // live on the device, so the choice uses Lkv only.
+  const int max_splits = std::max(1, (Lkv + 255) / 256);
+  const long want = 4L * device_sm_count();
+  long s = (want + static_cast<long>(B) * Hkv - 1) / (static_cast<long>(B) * Hkv);
+  if (s < 1) s = 1;
+  if (s > max_splits) s = max_splits;
+  if (s > 1024) s = 1024;
+  (void)Hq;
+  return static_cast<int>(s);
+}
+
+size_t attn_decode_workspace_size(int B, int Lq, int Hq, int d, int num_splits) {
+  if (B <= 0 || Lq <= 0 || Hq <= 0 || d <= 0 || num_splits <= 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * Hq * num_splits * Lq;
+  return align256(rows * d * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+attn_status attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, float* o_part,
+                                float* lse_part, int B, int Lq, int Lkv, int Hq, int Hkv, int d, float scale,
+                                int causal, const int32_t* kv_lens, int num_splits, attn_dtype dtype,
+                                attn_stream_t stream) {
+  attn_status s = check_problem(B, Lq, Lkv, Hq, Hkv, d, scale, causal, dtype);
+  if (s != ATTN_OK) return s;
+  s = need_ptrs({{q, "q"}, {k_cache, "k_cache"}, {v_cache, "v_cache"}, {o_part, "o_part"}, {lse_part, "lse_part"}});
+  if (s != ATTN_OK) return s;
+  if (kv_lens != nullptr && (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
+    return fail(ATTN_ERR_INVALID_ARG, "kv_lens is not 4-byte aligned");
+  if (num_splits < 0) return fail(ATTN_ERR_INVALID_ARG, "num_splits must be >= 0");
+  if (num_splits == 0) num_splits = attn_decode_num_splits(B, Lq, Lkv, Hq, Hkv, d);
+  const int G = Hq / Hkv;
+  if (static_cast<long>(G) * Lq > 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "decode packs G*Lq = %ld rows into one 128-row tile (at most 128)",
+                static_cast<long>(G) * Lq);
+  const int per = (Lkv + num_splits - 1) / num_splits;
+  DecodeArgs a;
+  a.pb = make_problem(B, Lq, Lkv, Hq, Hkv, d, scale, causal, kv_lens);
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.num_splits = num_splits;
+  a.chunk = 128 * ((per + 127) / 128);
+  DeviceStatus* st = status_ptr();
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = dtype == ATTN_BF16 ? launch_decode_bf16(a, st, cs) : launch_decode_f32(a, st, cs);
+  return from_cuda(e, "attn_decode_splitkv launch");
+}
+
+attn_status attn_decode_combine(const float* o_part, const float* lse_part, void* o, float* lse, int B, int Lq,
+                                int Hq, int d, int num_splits, attn_dtype dtype, attn_stream_t stream) {
+  attn_status s = check_problem(B, Lq, Lq, Hq, Hq, d, 1.0f, 0, dtype);
+  if (s != ATTN_OK) return s;
+  s = need_ptrs({{o_part, "o_part"}, {lse_part, "lse_part"}, {o, "o"}, {lse, "lse"}});
+  if (s != ATTN_OK) return s;
+  if (num_splits <= 0) return fail(ATTN_ERR_INVALID_ARG, "num_splits must be > 0");
+  cudaError_t e = launch_decode_combine(o_part, lse_part, o, lse, B, Lq, Hq, d, num_splits, dtype == ATTN_BF16,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  return from_cuda(e, "attn_decode_combine launch");
+}
+
+attn_status attn_device_status(int* code, int* site, int reset) {
+  DeviceStatus* p = status_ptr();
+  if (p == nullptr) return fail(ATTN_ERR_CUDA, "cannot resolve the device status word");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return from_cuda(e, "attn_device_status synchronize");
+  DeviceStatus h;
+  e = cudaMemcpy(&h, p, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return from_cuda(e, "attn_device_status read");
+  if (code) *code = h.code;
+  if (site) *site = h.site;
+  if (reset) {
+    DeviceStatus z = {0, 0, 0};
+    e = cudaMemcpy(p, &z, sizeof(z), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return from_cuda(e, "attn_device_status reset");
+  }
+  if (h.code != 0) return fail(ATTN_ERR_DEVICE, "device status code %d at site %d (block %d)", h.code, h.site, h.block);
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// Internal interface between the C-ABI layer (attn_api.cu) and the kernel
+// translation units.  Not installed; the public ABI is include/attn.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sm103_ptx.cuh"
+
+namespace attn {
+
+// Problem description shared by every kernel family.  All pointers are device
+// pointers; sizes are validated by the ABI layer before a launch.
+struct Problem {
+  int B, Lq, Lkv, Hq, Hkv, d, G;
+  int causal;
+  float scale;             // softmax scale (> 0)
+  const int32_t* kv_lens;  // [B] or nullptr
+};
+
+// ---- forward ---------------------------------------------------------------
+struct FwdArgs {
+  Problem pb;
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+};
+cudaError_t launch_fwd_bf16(const FwdArgs& a, DeviceStatus* st, cudaStream_t s);
+cudaError_t launch_fwd_f32(const FwdArgs& a, DeviceStatus* st, cudaStream_t s);
+
+// ---- backward --------------------------------------------------------------
+struct BwdArgs {
+  Problem pb;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const float* lse;
+  const void* dout;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* delta;  // workspace [B, Hq, Lq]
+  float* dq_acc; // workspace [B, Lq, Hq, d] (atomic variant only)
+  int deterministic;
+};
+cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* delta, float* dq_acc, int B, int Lq, int Hq,
+                                  int d, int is_bf16, cudaStream_t s);
+cudaError_t launch_bwd_bf16(const BwdArgs& a, DeviceStatus* st, cudaStream_t s);
+cudaError_t launch_bwd_f32(const BwdArgs& a, DeviceStatus* st, cudaStream_t s);
+
+// ---- split-KV decode ---------------------------------------------------------
+struct DecodeArgs {
+  Problem pb;
+  const void* q;
+  const void* k;
+  const void* v;
+  float* o_part;
+  float* lse_part;
+  int num_splits;
+  int chunk;  // keys per split, a multiple of 128
+};
+cudaError_t launch_decode_bf16(const DecodeArgs& a, DeviceStatus* st, cudaStream_t s);
+cudaError_t launch_decode_f32(const DecodeArgs& a, DeviceStatus* st, cudaStream_t s);
+cudaError_t launch_decode_combine(const float* o_part, const float* lse_part, void* o, float* lse, int B, int Lq,
+                                  int Hq, int d, int num_splits, int is_bf16, cudaStream_t s);
+
+// ---- host helpers (attn_api.cu) ---------------------------------------------
+// Tiled TMA descriptor over a [B, L, H, d] tensor: dims (d, L, H, B), box
+// (box_inner, box_rows, 1, 1), 128-byte swizzle, zero fill out of bounds.
+bool make_bshd_tmap(CUtensorMap* map, const void* base, bool bf16, int B, int L, int H, int d, int box_inner,
+                    int box_rows);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace attn

@@ -1,0 +1,366 @@
+// Forward attention, bf16, head_dim 64/128, on the sm_103a tensor cores.
+//
+// Method (probjax "Attention performance", sections "When to use which" and
+// "Memory"): exact softmax attention computed tile by tile with an online
+// softmax, so memory stays linear in the sequence length; the output and the
+// per-row log-sum-exp are the residuals of the backward.  The softmax is
+// evaluated in base 2: t = s * scale * log2(e), P = 2^(t - m), and
+// LSE = ln(2) * (m + log2(l)).
+//
+// One CTA owns two 128-row query tiles (A and B) of one (batch, head) and
+// streams the K/V tiles of the head's KV head (GQA: h / G) through a ring of
+// shared-memory slots filled by TMA.  Warp roles:
+//   warps 0-3  softmax of tile A (thread = query row = TMEM lane)
+//   warps 4-7  softmax of tile B
+//   warp  8    TMA producer (one lane)
+//   warp  9    tcgen05.mma issuer (one lane); owns the TMEM allocation
+// TMEM (512 columns): S_A [0,128) S_B [128,256) O_A [256,256+d) O_B [384,384+d).
+// P (bf16) is written over the first 64 columns of its S tile and is the A
+// operand of O += P V straight from TMEM.  The MMA issue order per KV tile j is
+//   PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+// so each softmax group has the other tile's two MMAs to hide behind, and
+// S_X(j+1) is issued after the PV_X(j) that reads the P stored in S_X's
+// columns (tcgen05.mma ops of one thread execute in issue order).  O is
+// rescaled lazily: only when a row's running maximum grows by more than
+// 2^8 (kRescaleThreshold), done by the softmax warps in TMEM.
+#include "attn_internal.h"
+
+namespace attn {
+namespace {
+
+constexpr int kBM = 128;  // rows per query tile (= TMEM lanes)
+constexpr int kBN = 128;  // keys per KV tile
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kQTileBytes = kBM * D * 2;     // one query tile, bf16
+  static constexpr int kSlotBytes = kBN * D * 2;      // one K or V tile
+  static constexpr int kBoxBytes = 128 * 64 * 2;      // one TMA box (128 rows x 64 cols)
+  static constexpr int kSlots = (D == 128) ? 4 : 8;   // ring depth
+  static constexpr int kOffSlots = 2 * kQTileBytes;
+  static constexpr int kOffBars = kOffSlots + kSlots * kSlotBytes;
+  static constexpr int kNumBars = 2 * kSlots + 7;
+  static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;  // + alignment slack
+  static constexpr int kThreads = 320;
+};
+
+struct FwdKParams {
+  void* o;
+  float* lse;
+  const int32_t* kv_lens;
+  int Lq, Lkv, Hq, Hkv, G, causal, n_qblocks;
+  float scale_log2;
+  DeviceStatus* status;
+};
+
+// Number of key columns row i may attend to: keys [0, limit) are valid.
+__device__ __forceinline__ int key_limit(int i, int Lq, int kvl, int causal) {
+  if (!causal) return kvl;
+  return min(kvl, i + 1 + kvl - Lq);
+}
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdKParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* sQ = smem;  // tile A at 0, tile B at kQTileBytes
+  uint8_t* sSlots = smem + C::kOffSlots;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::kSlots;
+  uint64_t* q_full = bars + 2 * C::kSlots;
+  uint64_t* s_full = q_full + 1;  // [2]
+  uint64_t* p_full = q_full + 3;  // [2]
+  uint64_t* o_full = q_full + 5;  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  const int qb = p.causal ? (p.n_qblocks - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const int hq = blockIdx.y, b = blockIdx.z;
+  const int hkv = hq / p.G;
+  int kvl = p.Lkv;
+  if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
+
+  // KV tiles each query tile needs (the limit grows with the row index).
+  auto tiles_for = [&](int x) {
+    const int row0 = qb * 2 * kBM + x * kBM;
+    if (row0 >= p.Lq) return 0;
+    const int last = min(row0 + kBM - 1, p.Lq - 1);
+    const int lim = key_limit(last, p.Lq, kvl, p.causal);
+    return lim > 0 ? (lim + kBN - 1) / kBN : 0;
+  };
+  const int n_a = tiles_for(0), n_b = tiles_for(1);
+  const int n = max(n_a, n_b);
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(q_full, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 128);
+      mbar_init(&o_full[x], 1);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      uint32_t qbytes = (n_a > 0 ? C::kQTileBytes : 0) + (n_b > 0 ? C::kQTileBytes : 0);
+      mbar_arrive_expect_tx(q_full, qbytes);
+      for (int x = 0; x < 2; ++x) {
+        if ((x == 0 ? n_a : n_b) == 0) continue;
+        const int row0 = qb * 2 * kBM + x * kBM;
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_4d(sQ + x * C::kQTileBytes + h * C::kBoxBytes, &tm_q, q_full, h * 64, row0, hq, b);
+      }
+      for (int j = 0; j < n; ++j) {
+        bool ok = true;
+        for (int t = 0; t < 2 && ok; ++t) {
+          const int ld = 2 * j + t, s = ld % C::kSlots, r = ld / C::kSlots;
+          if (r > 0) ok = mbar_wait(&empty[s], (r - 1) & 1, abort_flag, p.status, 1);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&full[s], C::kSlotBytes);
+          uint8_t* dst = sSlots + s * C::kSlotBytes;
+          for (int h = 0; h < D / 64; ++h)
+            tma_load_4d(dst + h * C::kBoxBytes, t == 0 ? &tm_k : &tm_v, &full[s], h * 64, j * kBN, hkv, b);
+        }
+        if (!ok) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n > 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);  // Q (K-major) x K^T (K-major)
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);    // P (TMEM) x V (MN-major)
+      const uint32_t q_addr = smem_u32(sQ);
+      const uint32_t slot_addr = smem_u32(sSlots);
+      // S_x = Q_x K^T : 16-wide k-steps along d; each 64-column half of d is its own TMA box.
+      auto issue_s = [&](int x, int kslot) {
+        const uint32_t qa = q_addr + x * C::kQTileBytes;
+        const uint32_t ka = slot_addr + kslot * C::kSlotBytes;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * C::kBoxBytes + (k & 3) * 32;
+          mma_ss(tbase + x * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_s, k > 0);
+        }
+      };
+      // O_x (+)= P_x V : 16-key k-steps; P advances 8 TMEM columns, V 16 rows (2 KB).
+      auto issue_pv = [&](int x, int vslot, int acc) {
+        const uint32_t va = slot_addr + vslot * C::kSlotBytes;
+#pragma unroll
+        for (int k = 0; k < kBN / 16; ++k) {
+          mma_ts(tbase + 256 + x * 128, tbase + x * 128 + k * 8, sdesc_sw128(va + k * 2048, C::kBoxBytes, 1024),
+                 idesc_o, (acc || k > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.status, 2);
+      if (ok) ok = mbar_wait(&full[0], 0, abort_flag, p.status, 3);
+      if (ok) {
+        tc_fence_after();
+        if (n_a > 0) { issue_s(0, 0); mma_commit(&s_full[0]); }
+        if (n_b > 0) { issue_s(1, 0); mma_commit(&s_full[1]); }
+        mma_commit(&empty[0]);
+      }
+      for (int j = 0; j < n && ok; ++j) {
+        const int vl = 2 * j + 1, vs = vl % C::kSlots;
+        const int kl = 2 * j + 2, ks = kl % C::kSlots;
+        const bool has_next = j + 1 < n;
+        ok = mbar_wait(&full[vs], (vl / C::kSlots) & 1, abort_flag, p.status, 4);
+        if (!ok) break;
+        tc_fence_after();
+        if (j < n_a) {
+          ok = mbar_wait(&p_full[0], j & 1, abort_flag, p.status, 5);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(0, vs, j > 0);
+          if (j == n_a - 1) mma_commit(&o_full[0]);
+        }
+        if (has_next) {
+          ok = mbar_wait(&full[ks], (kl / C::kSlots) & 1, abort_flag, p.status, 6);
+          if (!ok) break;
+          tc_fence_after();
+          if (j + 1 < n_a) { issue_s(0, ks); mma_commit(&s_full[0]); }
+        }
+        if (j < n_b) {
+          ok = mbar_wait(&p_full[1], j & 1, abort_flag, p.status, 7);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(1, vs, j > 0);
+          if (j == n_b - 1) mma_commit(&o_full[1]);
+        }
+        mma_commit(&empty[vs]);
+        if (has_next) {
+          if (j + 1 < n_b) { issue_s(1, ks); mma_commit(&s_full[1]); }
+          mma_commit(&empty[ks]);
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int x = warp >> 2, wq = warp & 3;
+    const int row = qb * 2 * kBM + x * kBM + wq * 32 + lane;
+    const int n_x = x == 0 ? n_a : n_b;
+    const uint32_t t_lane = tbase + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t s_addr = t_lane + x * 128;
+    const uint32_t o_addr = t_lane + 256 + x * 128;
+    const int lim = row < p.Lq ? key_limit(row, p.Lq, kvl, p.causal) : 0;
+    const float sl2 = p.scale_log2;
+    float m_used = -INFINITY, l_sum = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_x; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], j & 1, abort_flag, p.status, 8));
+      if (!ok) break;
+      tc_fence_after();
+      float s[kBN];
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(s_addr + c * 32, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+      }
+      const int col0 = j * kBN;
+      if (col0 + kBN > lim) {
+#pragma unroll
+        for (int i = 0; i < kBN; ++i)
+          if (col0 + i >= lim) s[i] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, s[i]);
+      const float m_tile = mx * sl2;  // scale > 0, so the max commutes with the scaling
+      const bool grow = m_tile > m_used + kRescaleThreshold;
+      const float m_new = grow ? m_tile : m_used;
+      const float alpha = grow ? ex2_approx(m_used - m_new) : 1.0f;
+      l_sum *= alpha;
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(o_addr + c * 32, r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st32(o_addr + c * 32, r);
+        }
+      }
+      m_used = m_new;
+      const float mb = (m_used == -INFINITY) ? 0.f : m_used;
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, -mb));
+          const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, -mb));
+          l_sum += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(s_addr + c * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full[x]);
+    }
+    // epilogue: O / l -> bf16, LSE
+    if (ok && n_x > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_full[x], 0, abort_flag, p.status, 9));
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
+                            ((static_cast<size_t>(b) * p.Lq + row) * p.Hq + hq) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        if (n_x > 0) {
+          tmem_ld32(o_addr + c * 32, r);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
+        if (row < p.Lq) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+      if (row < p.Lq) {
+        p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Lq + row] =
+            l_sum > 0.f ? (m_used + lg2_approx(l_sum)) * kLn2 : -INFINITY;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_bf16_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  const Problem& pb = a.pb;
+  CUtensorMap tq, tk, tv;
+  if (!make_bshd_tmap(&tq, a.q, true, pb.B, pb.Lq, pb.Hq, D, 64, kBM)) return cudaErrorInvalidValue;
+  if (!make_bshd_tmap(&tk, a.k, true, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
+  if (!make_bshd_tmap(&tv, a.v, true, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  FwdKParams kp;
+  kp.o = a.o;
+  kp.lse = a.lse;
+  kp.kv_lens = pb.kv_lens;
+  kp.Lq = pb.Lq;
+  kp.Lkv = pb.Lkv;
+  kp.Hq = pb.Hq;
+  kp.Hkv = pb.Hkv;
+  kp.G = pb.G;
+  kp.causal = pb.causal;
+  kp.n_qblocks = (pb.Lq + 2 * kBM - 1) / (2 * kBM);
+  kp.scale_log2 = pb.scale * kLog2e;
+  kp.status = st;
+  dim3 grid(kp.n_qblocks, pb.Hq, pb.B);
+  fwd_bf16_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16(const FwdArgs& a, DeviceStatus* st, cudaStream_t s) {
+  if (a.pb.d == 64) return launch_fwd_bf16_d<64>(a, st, s);
+  return launch_fwd_bf16_d<128>(a, st, s);
+}
+
+}  // namespace attn

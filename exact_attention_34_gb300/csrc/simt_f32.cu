@@ -1,0 +1,527 @@
+// float32 attention in true fp32 arithmetic on the CUDA cores (FFMA).
+//
+// The pages run fp32 attention with TF32 matmuls and note it costs about three
+// decimal digits ("GPU and CPU performance", section "Methodology", TF32);
+// these kernels keep full fp32 products so float32 inputs match the exact
+// result to ~1e-6.  Same method as the tensor-core path: tiled exact
+// attention with an online softmax in base 2 (forward, also used for the
+// split-KV partials), a delta = rowsum(dO * O) preprocess, and a two-pass
+// backward (dK/dV per KV tile, then dQ per query tile) or a single pass with
+// float32 atomic dQ accumulation ("Attention performance", section "When to
+// use which", backward pass).
+//
+// Tiles are 64 x 64; 256 threads form a 16 x 16 grid.  Thread (ty, tx) owns
+// tile rows 4*ty .. 4*ty+3 and the tile columns tx, tx+16, tx+32, tx+48 (and
+// head-dim columns tx + 16*e), so shared-memory rows padded by one float are
+// read without bank conflicts.
+#include "attn_internal.h"
+
+namespace attn {
+namespace {
+
+constexpr int kT = 64;    // tile rows and columns
+constexpr int kPad = 1;   // shared-memory row padding (floats)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ int key_limit(int i, int Lq, int kvl, int causal) {
+  if (!causal) return kvl;
+  return min(kvl, i + 1 + kvl - Lq);
+}
+
+__device__ __forceinline__ int seq_len_of(const int32_t* kv_lens, int b, int Lkv) {
+  return kv_lens == nullptr ? Lkv : min(max(kv_lens[b], 0), Lkv);
+}
+
+// Copy `rows` x D floats of a [., L, H, D] tensor (rows l0.. of head h) into a
+// padded shared tile; rows past L are zero-filled.
+template <int D>
+__device__ __forceinline__ void load_tile(float* __restrict__ dst, const float* __restrict__ src, int b, int l0,
+                                          int h, int L, int H) {
+  constexpr int kW = D / 4;  // float4 per row
+  for (int idx = threadIdx.x; idx < kT * kW; idx += blockDim.x) {
+    const int r = idx / kW, c4 = idx % kW;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (l0 + r < L) v = *reinterpret_cast<const float4*>(src + ((static_cast<size_t>(b) * L + l0 + r) * H + h) * D + c4 * 4);
+    float* d = dst + r * (D + kPad) + c4 * 4;
+    d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+  }
+}
+
+// acc[a][c] = sum_k A[4*ty + a][k] * Bm[tx + 16*c][k]   (both padded, D wide)
+template <int D>
+__device__ __forceinline__ void tile_dot(const float* __restrict__ A, const float* __restrict__ Bm, int ty, int tx,
+                                         float (&acc)[4][4]) {
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
+#pragma unroll 4
+  for (int k = 0; k < D; ++k) {
+    float av[4], bv[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) av[a] = A[(4 * ty + a) * (D + kPad) + k];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) bv[c] = Bm[(tx + 16 * c) * (D + kPad) + k];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[a][c] = fmaf(av[a], bv[c], acc[a][c]);
+  }
+}
+
+// out[a][e] += sum_j P[4*ty + a][j] * M[j][tx + 16*e]  (P is kT x kT padded, M is kT x D padded)
+template <int D>
+__device__ __forceinline__ void tile_pv(const float* __restrict__ P, const float* __restrict__ M, int ty, int tx,
+                                        float (&out)[4][D / 16]) {
+#pragma unroll 4
+  for (int j = 0; j < kT; ++j) {
+    float pv[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) pv[a] = P[(4 * ty + a) * (kT + kPad) + j];
+#pragma unroll
+    for (int e = 0; e < D / 16; ++e) {
+      const float m = M[j * (D + kPad) + tx + 16 * e];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) out[a][e] = fmaf(pv[a], m, out[a][e]);
+    }
+  }
+}
+
+// out[a][e] += sum_j P[j][4*ty + a] * M[j][tx + 16*e]  (transposed P)
+template <int D>
+__device__ __forceinline__ void tile_ptv(const float* __restrict__ P, const float* __restrict__ M, int ty, int tx,
+                                         float (&out)[4][D / 16]) {
+#pragma unroll 4
+  for (int j = 0; j < kT; ++j) {
+    float pv[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) pv[a] = P[j * (kT + kPad) + 4 * ty + a];
+#pragma unroll
+    for (int e = 0; e < D / 16; ++e) {
+      const float m = M[j * (D + kPad) + tx + 16 * e];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) out[a][e] = fmaf(pv[a], m, out[a][e]);
+    }
+  }
+}
+
+__device__ __forceinline__ float row_reduce_max(float v) {
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+__device__ __forceinline__ float row_reduce_sum(float v) {
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+struct F32FwdParams {
+  const float* q;
+  const float* k;
+  const float* v;
+  float* o;          // final mode: [B, Lq, Hq, D]
+  float* lse;        // final mode: [B, Hq, Lq]
+  float* o_part;     // partial mode: [B, Hq, S, Lq, D]
+  float* lse_part;   // partial mode: [B, Hq, S, Lq]
+  const int32_t* kv_lens;
+  int B, Lq, Lkv, Hq, Hkv, G, causal, num_splits, chunk;
+  float scale_log2;
+};
+
+// grid (ceil(Lq/64), Hq, B * num_splits).  num_splits == 1 and o != nullptr:
+// ordinary forward; otherwise split s covers keys [s*chunk, (s+1)*chunk).
+template <int D>
+__global__ void __launch_bounds__(256) f32_fwd_kernel(const F32FwdParams p) {
+  extern __shared__ float sm[];
+  float* Qs = sm;
+  float* Ks = Qs + kT * (D + kPad);
+  float* Vs = Ks + kT * (D + kPad);
+  float* Ps = Vs + kT * (D + kPad);
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int q0 = blockIdx.x * kT, h = blockIdx.y;
+  const int b = blockIdx.z % p.B, split = blockIdx.z / p.B;
+  const int hk = h / p.G;
+  const int kvl = seq_len_of(p.kv_lens, b, p.Lkv);
+  const int k_lo = split * p.chunk;
+  const int k_hi = min(kvl, k_lo + p.chunk);
+  const int last_row = min(q0 + kT - 1, p.Lq - 1);
+  const int hi_all = min(k_hi, key_limit(last_row, p.Lq, kvl, p.causal));
+
+  load_tile<D>(Qs, p.q, b, q0, h, p.Lq, p.Hq);
+  float m[4], l[4], acc[4][D / 16];
+  int lim[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    m[a] = -INFINITY;
+    l[a] = 0.f;
+    const int i = q0 + 4 * ty + a;
+    lim[a] = i < p.Lq ? min(k_hi, key_limit(i, p.Lq, kvl, p.causal)) : 0;
+#pragma unroll
+    for (int e = 0; e < D / 16; ++e) acc[a][e] = 0.f;
+  }
+  for (int j0 = k_lo; j0 < hi_all; j0 += kT) {
+    __syncthreads();
+    load_tile<D>(Ks, p.k, b, j0, hk, p.Lkv, p.Hkv);
+    load_tile<D>(Vs, p.v, b, j0, hk, p.Lkv, p.Hkv);
+    __syncthreads();
+    float s[4][4];
+    tile_dot<D>(Qs, Ks, ty, tx, s);
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int j = j0 + tx + 16 * c;
+        s[a][c] = (j < lim[a]) ? s[a][c] * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, s[a][c]);
+      }
+      mx = row_reduce_max(mx);
+      const float m_new = fmaxf(m[a], mx);
+      const float mb = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ex2_approx(m[a] - mb);
+      m[a] = m_new;
+      float ls = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float pv = ex2_approx(s[a][c] - mb);
+        ls += pv;
+        Ps[(4 * ty + a) * (kT + kPad) + tx + 16 * c] = pv;
+      }
+      l[a] = l[a] * alpha + row_reduce_sum(ls);
+#pragma unroll
+      for (int e = 0; e < D / 16; ++e) acc[a][e] *= alpha;
+    }
+    __syncthreads();
+    tile_pv<D>(Ps, Vs, ty, tx, acc);
+  }
+  const bool partial = p.o == nullptr;
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int i = q0 + 4 * ty + a;
+    if (i >= p.Lq) continue;
+    const float inv = l[a] > 0.f ? 1.0f / l[a] : 0.f;
+    const float lse_v = l[a] > 0.f ? (m[a] + log2f(l[a])) * kLn2 : -INFINITY;
+    float* orow;
+    if (!partial) {
+      orow = p.o + ((static_cast<size_t>(b) * p.Lq + i) * p.Hq + h) * D;
+      if (tx == 0) p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Lq + i] = lse_v;
+    } else {
+      const size_t r = ((static_cast<size_t>(b) * p.Hq + h) * p.num_splits + split) * p.Lq + i;
+      orow = p.o_part + r * D;
+      if (tx == 0) p.lse_part[r] = lse_v;
+    }
+#pragma unroll
+    for (int e = 0; e < D / 16; ++e) orow[tx + 16 * e] = acc[a][e] * inv;
+  }
+}
+
+struct F32BwdParams {
+  const float* q;
+  const float* k;
+  const float* v;
+  const float* lse;
+  const float* dout;
+  const float* delta;
+  float* dq;
+  float* dk;
+  float* dv;
+  float* dq_acc;  // atomic variant: [B, Lq, Hq, D] (unscaled)
+  const int32_t* kv_lens;
+  int B, Lq, Lkv, Hq, Hkv, G, causal;
+  float scale, scale_log2;
+};
+
+// Recompute P and dS for one (query tile, key tile) pair in "key-major" form:
+// element [a][c] is key 4*ty + a (of the key tile) and query tx + 16*c.
+template <int D>
+__device__ __forceinline__ void kt_probs(const float* Ks, const float* Vs, const float* Qs, const float* dOs,
+                                         const float* lse2_s, const float* delta_s, const int* lim_s, int j0, int ty,
+                                         int tx, float scale_log2, float (&P)[4][4], float (&dS)[4][4]) {
+  float s[4][4], dp[4][4];
+  tile_dot<D>(Ks, Qs, ty, tx, s);
+  tile_dot<D>(Vs, dOs, ty, tx, dp);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int qi = tx + 16 * c;
+    const float l2 = lse2_s[qi];
+    const int lim = lim_s[qi];
+    const float dl = delta_s[qi];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int j = j0 + 4 * ty + a;
+      const float pv = (j < lim) ? ex2_approx(fmaf(s[a][c], scale_log2, -l2)) : 0.f;
+      P[a][c] = pv;
+      dS[a][c] = pv * (dp[a][c] - dl);
+    }
+  }
+}
+
+// dK/dV for one 64-key tile of one KV head, summed over the G query heads and
+// every query tile that sees it (fixed order: deterministic).  In the atomic
+// variant it also adds dS K into the float32 dQ accumulator.
+template <int D>
+__global__ void __launch_bounds__(256) f32_bwd_dkdv_kernel(const F32BwdParams p) {
+  extern __shared__ float sm[];
+  float* Ks = sm;
+  float* Vs = Ks + kT * (D + kPad);
+  float* Qs = Vs + kT * (D + kPad);
+  float* dOs = Qs + kT * (D + kPad);
+  float* Pt = dOs + kT * (D + kPad);  // [key][query]
+  float* dSt = Pt + kT * (kT + kPad);
+  float* lse2_s = dSt + kT * (kT + kPad);
+  float* delta_s = lse2_s + kT;
+  int* lim_s = reinterpret_cast<int*>(delta_s + kT);
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int j0 = blockIdx.x * kT, hk = blockIdx.y, b = blockIdx.z;
+  const int kvl = seq_len_of(p.kv_lens, b, p.Lkv);
+  float dk[4][D / 16], dv[4][D / 16];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int e = 0; e < D / 16; ++e) dk[a][e] = dv[a][e] = 0.f;
+  if (j0 < kvl) {
+    load_tile<D>(Ks, p.k, b, j0, hk, p.Lkv, p.Hkv);
+    load_tile<D>(Vs, p.v, b, j0, hk, p.Lkv, p.Hkv);
+    const int q_first = p.causal ? max(0, j0 + p.Lq - kvl) : 0;
+    for (int g = 0; g < p.G; ++g) {
+      const int h = hk * p.G + g;
+      for (int q0 = (q_first / kT) * kT; q0 < p.Lq; q0 += kT) {
+        __syncthreads();
+        load_tile<D>(Qs, p.q, b, q0, h, p.Lq, p.Hq);
+        load_tile<D>(dOs, p.dout, b, q0, h, p.Lq, p.Hq);
+        if (threadIdx.x < kT) {
+          const int i = q0 + threadIdx.x;
+          const bool in = i < p.Lq;
+          const float ls = in ? p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Lq + i] : -INFINITY;
+          lse2_s[threadIdx.x] = ls * kLog2e;
+          delta_s[threadIdx.x] = in ? p.delta[(static_cast<size_t>(b) * p.Hq + h) * p.Lq + i] : 0.f;
+          lim_s[threadIdx.x] = (in && ls != -INFINITY) ? key_limit(i, p.Lq, kvl, p.causal) : 0;
+        }
+        __syncthreads();
+        float P[4][4], dS[4][4];
+        kt_probs<D>(Ks, Vs, Qs, dOs, lse2_s, delta_s, lim_s, j0, ty, tx, p.scale_log2, P, dS);
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            Pt[(4 * ty + a) * (kT + kPad) + tx + 16 * c] = P[a][c];
+            dSt[(4 * ty + a) * (kT + kPad) + tx + 16 * c] = dS[a][c];
+          }
+        __syncthreads();
+        tile_pv<D>(Pt, dOs, ty, tx, dv);
+        tile_pv<D>(dSt, Qs, ty, tx, dk);
+        if (p.dq_acc != nullptr) {
+          // dQacc[query 4*ty + a][tx + 16e] += sum_key dS^T[key][query] K[key][...]
+          float dq[4][D / 16];
+#pragma unroll
+          for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int e = 0; e < D / 16; ++e) dq[a][e] = 0.f;
+          tile_ptv<D>(dSt, Ks, ty, tx, dq);
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            const int i = q0 + 4 * ty + a;
+            if (i >= p.Lq) continue;
+            float* dst = p.dq_acc + ((static_cast<size_t>(b) * p.Lq + i) * p.Hq + h) * D;
+#pragma unroll
+            for (int e = 0; e < D / 16; ++e) atomicAdd(dst + tx + 16 * e, dq[a][e]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int j = j0 + 4 * ty + a;
+    if (j >= p.Lkv) continue;
+    const size_t off = ((static_cast<size_t>(b) * p.Lkv + j) * p.Hkv + hk) * D;
+#pragma unroll
+    for (int e = 0; e < D / 16; ++e) {
+      p.dk[off + tx + 16 * e] = dk[a][e] * p.scale;
+      p.dv[off + tx + 16 * e] = dv[a][e];
+    }
+  }
+}
+
+// dQ for one 64-row query tile: loops over the key tiles it sees.
+template <int D>
+__global__ void __launch_bounds__(256) f32_bwd_dq_kernel(const F32BwdParams p) {
+  extern __shared__ float sm[];
+  float* Qs = sm;
+  float* dOs = Qs + kT * (D + kPad);
+  float* Ks = dOs + kT * (D + kPad);
+  float* Vs = Ks + kT * (D + kPad);
+  float* dSs = Vs + kT * (D + kPad);  // [query][key]
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int q0 = blockIdx.x * kT, h = blockIdx.y, b = blockIdx.z;
+  const int hk = h / p.G;
+  const int kvl = seq_len_of(p.kv_lens, b, p.Lkv);
+  load_tile<D>(Qs, p.q, b, q0, h, p.Lq, p.Hq);
+  load_tile<D>(dOs, p.dout, b, q0, h, p.Lq, p.Hq);
+  float l2[4], dl[4];
+  int lim[4];
+  float acc[4][D / 16];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int i = q0 + 4 * ty + a;
+    const bool in = i < p.Lq;
+    const float ls = in ? p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Lq + i] : -INFINITY;
+    l2[a] = ls * kLog2e;
+    dl[a] = in ? p.delta[(static_cast<size_t>(b) * p.Hq + h) * p.Lq + i] : 0.f;
+    lim[a] = (in && ls != -INFINITY) ? key_limit(i, p.Lq, kvl, p.causal) : 0;
+#pragma unroll
+    for (int e = 0; e < D / 16; ++e) acc[a][e] = 0.f;
+  }
+  const int last_row = min(q0 + kT - 1, p.Lq - 1);
+  const int hi_all = key_limit(last_row, p.Lq, kvl, p.causal);
+  for (int j0 = 0; j0 < hi_all; j0 += kT) {
+    __syncthreads();
+    load_tile<D>(Ks, p.k, b, j0, hk, p.Lkv, p.Hkv);
+    load_tile<D>(Vs, p.v, b, j0, hk, p.Lkv, p.Hkv);
+    __syncthreads();
+    float s[4][4], dp[4][4];
+    tile_dot<D>(Qs, Ks, ty, tx, s);
+    tile_dot<D>(dOs, Vs, ty, tx, dp);
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int j = j0 + tx + 16 * c;
+        const float pv = (j < lim[a]) ? ex2_approx(fmaf(s[a][c], p.scale_log2, -l2[a])) : 0.f;
+        dSs[(4 * ty + a) * (kT + kPad) + tx + 16 * c] = pv * (dp[a][c] - dl[a]);
+      }
+    __syncthreads();
+    tile_pv<D>(dSs, Ks, ty, tx, acc);
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int i = q0 + 4 * ty + a;
+    if (i >= p.Lq) continue;
+    float* dst = p.dq + ((static_cast<size_t>(b) * p.Lq + i) * p.Hq + h) * D;
+#pragma unroll
+    for (int e = 0; e < D / 16; ++e) dst[tx + 16 * e] = acc[a][e] * p.scale;
+  }
+}
+
+// dq = scale * dq_acc  (atomic variant, float32 output)
+__global__ void f32_dq_convert_kernel(const float* __restrict__ acc, float* __restrict__ dq, long n, float scale) {
+  const long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) dq[i] = acc[i] * scale;
+}
+
+template <int D>
+constexpr int fwd_smem() {
+  return (3 * kT * (D + kPad) + kT * (kT + kPad)) * 4;
+}
+template <int D>
+constexpr int dkdv_smem() {
+  return (4 * kT * (D + kPad) + 2 * kT * (kT + kPad) + 3 * kT) * 4;
+}
+template <int D>
+constexpr int dq_smem() {
+  return (4 * kT * (D + kPad) + kT * (kT + kPad)) * 4;
+}
+
+template <int D>
+cudaError_t run_fwd(const F32FwdParams& p, int splits, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(f32_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd_smem<D>());
+  if (e != cudaSuccess) return e;
+  dim3 grid((p.Lq + kT - 1) / kT, p.Hq, p.B * splits);
+  f32_fwd_kernel<D><<<grid, 256, fwd_smem<D>(), s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t run_bwd(const F32BwdParams& p, bool atomic_dq, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(f32_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       dkdv_smem<D>());
+  if (e != cudaSuccess) return e;
+  dim3 g1((p.Lkv + kT - 1) / kT, p.Hkv, p.B);
+  f32_bwd_dkdv_kernel<D><<<g1, 256, dkdv_smem<D>(), s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (atomic_dq) {
+    const long n = static_cast<long>(p.B) * p.Lq * p.Hq * D;
+    f32_dq_convert_kernel<<<static_cast<int>((n + 255) / 256), 256, 0, s>>>(p.dq_acc, p.dq, n, p.scale);
+    return cudaGetLastError();
+  }
+  e = cudaFuncSetAttribute(f32_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem<D>());
+  if (e != cudaSuccess) return e;
+  dim3 g2((p.Lq + kT - 1) / kT, p.Hq, p.B);
+  f32_bwd_dq_kernel<D><<<g2, 256, dq_smem<D>(), s>>>(p);
+  return cudaGetLastError();
+}
+
+F32FwdParams fwd_params(const Problem& pb, const void* q, const void* k, const void* v) {
+  F32FwdParams p{};
+  p.q = static_cast<const float*>(q);
+  p.k = static_cast<const float*>(k);
+  p.v = static_cast<const float*>(v);
+  p.kv_lens = pb.kv_lens;
+  p.B = pb.B;
+  p.Lq = pb.Lq;
+  p.Lkv = pb.Lkv;
+  p.Hq = pb.Hq;
+  p.Hkv = pb.Hkv;
+  p.G = pb.G;
+  p.causal = pb.causal;
+  p.scale_log2 = pb.scale * kLog2e;
+  return p;
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_f32(const FwdArgs& a, DeviceStatus* st, cudaStream_t s) {
+  (void)st;
+  F32FwdParams p = fwd_params(a.pb, a.q, a.k, a.v);
+  p.o = static_cast<float*>(a.o);
+  p.lse = a.lse;
+  p.num_splits = 1;
+  p.chunk = a.pb.Lkv;
+  return a.pb.d == 64 ? run_fwd<64>(p, 1, s) : run_fwd<128>(p, 1, s);
+}
+
+cudaError_t launch_decode_f32(const DecodeArgs& a, DeviceStatus* st, cudaStream_t s) {
+  (void)st;
+  F32FwdParams p = fwd_params(a.pb, a.q, a.k, a.v);
+  p.o_part = a.o_part;
+  p.lse_part = a.lse_part;
+  p.num_splits = a.num_splits;
+  p.chunk = a.chunk;
+  return a.pb.d == 64 ? run_fwd<64>(p, a.num_splits, s) : run_fwd<128>(p, a.num_splits, s);
+}
+
+cudaError_t launch_bwd_f32(const BwdArgs& a, DeviceStatus* st, cudaStream_t s) {
+  (void)st;
+  const Problem& pb = a.pb;
+  cudaError_t e = launch_bwd_preprocess(a.o, a.dout, a.delta, a.deterministic ? nullptr : a.dq_acc, pb.B, pb.Lq,
+                                        pb.Hq, pb.d, 0, s);
+  if (e != cudaSuccess) return e;
+  F32BwdParams p{};
+  p.q = static_cast<const float*>(a.q);
+  p.k = static_cast<const float*>(a.k);
+  p.v = static_cast<const float*>(a.v);
+  p.lse = a.lse;
+  p.dout = static_cast<const float*>(a.dout);
+  p.delta = a.delta;
+  p.dq = static_cast<float*>(a.dq);
+  p.dk = static_cast<float*>(a.dk);
+  p.dv = static_cast<float*>(a.dv);
+  p.dq_acc = a.deterministic ? nullptr : a.dq_acc;
+  p.kv_lens = pb.kv_lens;
+  p.B = pb.B;
+  p.Lq = pb.Lq;
+  p.Lkv = pb.Lkv;
+  p.Hq = pb.Hq;
+  p.Hkv = pb.Hkv;
+  p.G = pb.G;
+  p.causal = pb.causal;
+  p.scale = pb.scale;
+  p.scale_log2 = pb.scale * kLog2e;
+  return pb.d == 64 ? run_bwd<64>(p, !a.deterministic, s) : run_bwd<128>(p, !a.deterministic, s);
+}
+
+}  // namespace attn

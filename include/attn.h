@@ -1,0 +1,166 @@
+/*
+ * attn.h -- C ABI of a GB300 (sm_103a) exact scaled-dot-product attention
+ * library: forward, backward (dQ, dK, dV) and split-KV decode.
+ *
+ * What it computes (probjax benchmark pages, "Attention performance"):
+ *   O = softmax(scale * Q K^T) V over the valid keys of each query row, and
+ *   the per-row natural log-sum-exp LSE that the backward recomputes from
+ *   (sections "Attention performance" and "Memory": the kernels keep the
+ *   output and the log-sum-exp as residuals).
+ *
+ * Tensor layout (section "Attention performance": inputs are
+ * [batch, seq, heads, head_dim]):
+ *   q, o, dout, dq   [B, Lq,  Hq,  d]   dense, d innermost
+ *   k, v, dk, dv     [B, Lkv, Hkv, d]   dense, d innermost
+ *   lse, delta       [B, Hq, Lq]        float32
+ * GQA ("Grouped-query attention and decoding"): Hq = G * Hkv and query head h
+ * reads KV head h / G directly; K and V are never repeated.
+ *
+ * Valid keys.  With kvl[b] = kv_lens[b] clamped into [0, Lkv] (Lkv when
+ * kv_lens is NULL), key j is valid for query row i of batch b iff
+ *   j < kvl[b]                          (KVLenMask, "H100 (Hopper)",
+ *                                         section "Mosaic GPU")
+ *   and, when causal, j <= i + kvl[b] - Lq   (causal aligned to the bottom
+ *                                         right; equal-length causal j <= i)
+ * A row without a valid key has O = 0, LSE = -inf and dQ = 0; keys at or past
+ * kvl[b] get dK = dV = 0 (same section).
+ *
+ * Conventions for every call:
+ *   - The caller allocates every buffer and owns the stream; the library never
+ *     allocates, frees or synchronises.  Calls are asynchronous on `stream`
+ *     (NULL = the legacy default stream).  Pointers named here are device
+ *     pointers unless stated otherwise.
+ *   - Every tensor pointer must be 16-byte aligned and, for bf16, every row
+ *     stride (Hq*d, Hkv*d elements) is then a multiple of 16 bytes.
+ *   - Arguments are validated on the host before anything is launched; a bad
+ *     argument returns an error code and launches nothing.  Values that live
+ *     on the device (kv_lens) cannot be checked there and are clamped into
+ *     [0, Lkv] by the kernels.
+ *   - dtype ATTN_BF16: q/k/v/o/dout/dq/dk/dv are bf16; ATTN_FP32: all float32.
+ *     lse, delta, partials and workspaces are always float32.
+ *   - head_dim d must be 64 or 128.
+ *   - Calls are thread-safe: no mutable global state is shared between calls
+ *     (tensor-map descriptors are built per call and passed by value).
+ */
+#ifndef GB300_ATTN_H
+#define GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without pulling in CUDA headers. */
+typedef struct CUstream_st* attn_stream_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* bad size, NULL or misaligned pointer, Hq % Hkv != 0 */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid call this build cannot compute exactly (e.g. d) */
+  ATTN_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the size query says */
+  ATTN_ERR_CUDA = 4,        /* a CUDA runtime/driver call or kernel launch failed */
+  ATTN_ERR_DEVICE = 5       /* a kernel reported a device-side fault (see attn_device_status) */
+} attn_status;
+
+typedef enum { ATTN_BF16 = 0, ATTN_FP32 = 1 } attn_dtype;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* attn_status_string(attn_status s);
+
+/* Detail message of the last error returned on the calling thread ("" if none). */
+const char* attn_last_error(void);
+
+/*
+ * Forward.  Writes o [B,Lq,Hq,d] (dtype) and lse [B,Hq,Lq] (float32, natural
+ * log, -inf on rows without a valid key).  scale is the softmax scale (pass
+ * 1/sqrt(d) for the standard one; any finite value is accepted).  kv_lens is
+ * a device int32 [B] or NULL.  causal is 0 or 1.
+ * Fused, memory-linear tiled kernel with online softmax ("Attention
+ * performance", section "When to use which": memory grows linearly in T).
+ */
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Lq, int Lkv,
+                     int Hq, int Hkv, int d, float scale, int causal, const int32_t* kv_lens, attn_dtype dtype,
+                     attn_stream_t stream);
+
+/*
+ * Backward preprocess: delta[b,h,i] = sum_c dout[b,i,h,c] * o[b,i,h,c] in
+ * float32 ([B,Hq,Lq]).  attn_bwd runs it itself; it is exported so the step
+ * can be checked and timed on its own.
+ */
+attn_status attn_bwd_preprocess(const void* o, const void* dout, float* delta, int B, int Lq, int Hq, int d,
+                                attn_dtype dtype, attn_stream_t stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs.  deterministic = 1: the two-pass
+ * backward (a dK/dV kernel per KV block, then a separate dQ kernel; bitwise
+ * reproducible), workspace = delta.  deterministic = 0: the single-pass
+ * backward with dQ accumulated by float32 atomic adds (order not
+ * reproducible), workspace = delta + a float32 dQ buffer [B,Lq,Hq,d]
+ * ("Attention performance", section "When to use which", backward pass).
+ */
+size_t attn_bwd_workspace_size(int B, int Lq, int Hq, int d, int deterministic, attn_dtype dtype);
+
+/*
+ * Backward: given the forward's o and lse and the output gradient dout,
+ * writes dq [B,Lq,Hq,d], dk and dv [B,Lkv,Hkv,d] (dtype).  For GQA, dk/dv sum
+ * over the G query heads of each KV head.  workspace must be 256-byte aligned
+ * and at least attn_bwd_workspace_size(...) bytes; its contents on entry do
+ * not matter.
+ */
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, int B, int Lq, int Lkv, int Hq, int Hkv, int d, float scale,
+                     int causal, const int32_t* kv_lens, attn_dtype dtype, int deterministic, void* workspace,
+                     size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * Split-KV decode for few queries over a long KV cache ("Attention
+ * performance", section "Grouped-query attention and decoding"): the keys are
+ * split across programs, the G query heads of a KV head (times the Lq rows)
+ * are packed into one tile, and the partial results are combined by their
+ * log-sum-exp.
+ *
+ * Partition: with C = 128 * ceil(ceil(Lkv / num_splits) / 128), split s of
+ * batch b covers keys [s*C, min((s+1)*C, kvl[b])) and is empty when
+ * s*C >= kvl[b].  Supported for Lq * (Hq / Hkv) <= 128.
+ *
+ * attn_decode_splitkv writes, per split, the attention over the split's valid
+ * keys, normalised within the split:
+ *   o_part   float32 [B, Hq, num_splits, Lq, d]
+ *   lse_part float32 [B, Hq, num_splits, Lq]   (-inf, with o_part = 0, where
+ *                                               the row has no valid key in it)
+ * num_splits = 0 picks attn_decode_num_splits(...).  The same num_splits must
+ * be passed to attn_decode_combine.
+ */
+int attn_decode_num_splits(int B, int Lq, int Lkv, int Hq, int Hkv, int d);
+attn_status attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, float* o_part,
+                                float* lse_part, int B, int Lq, int Lkv, int Hq, int Hkv, int d, float scale,
+                                int causal, const int32_t* kv_lens, int num_splits, attn_dtype dtype,
+                                attn_stream_t stream);
+
+/*
+ * Log-sum-exp combine: lse = log sum_s exp(lse_part_s) and
+ * o = sum_s exp(lse_part_s - lse) o_part_s, cast to dtype; rows whose splits
+ * are all empty get o = 0 and lse = -inf.  o [B,Lq,Hq,d], lse [B,Hq,Lq].
+ */
+attn_status attn_decode_combine(const float* o_part, const float* lse_part, void* o, float* lse, int B, int Lq,
+                                int Hq, int d, int num_splits, attn_dtype dtype, attn_stream_t stream);
+
+/* Bytes of o_part plus lse_part for a decode call (num_splits > 0). */
+size_t attn_decode_workspace_size(int B, int Lq, int Hq, int d, int num_splits);
+
+/*
+ * Device-side status of the current device: kernels never trap; a pipeline
+ * wait that runs out of time (2 s) records a code and a site here and the
+ * kernel ends early.  Synchronises the device.  Writes code/site (host
+ * pointers, nullable) and clears the status when reset != 0.  Returns
+ * ATTN_ERR_DEVICE when a code was set, ATTN_OK otherwise.
+ */
+attn_status attn_device_status(int* code, int* site, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300_ATTN_H */
