@@ -124,6 +124,13 @@ Problem make_problem(int B, int Lq, int Lkv, int Hq, int Hkv, int d, float scale
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+int lq_padded(int Lq) { return (Lq + 127) / 128 * 128; }
+
+// bytes of one [B, Hq, Lq_pad] float32 row-statistics array of the backward
+size_t bwd_rowstat_bytes(int B, int Lq, int Hq) {
+  return align256(static_cast<size_t>(B) * Hq * lq_padded(Lq) * sizeof(float));
+}
+
 }  // namespace
 
 bool make_bshd_tmap(CUtensorMap* map, const void* base, bool bf16, int B, int L, int H, int d, int box_inner,
@@ -203,15 +210,27 @@ attn_status attn_bwd_preprocess(const void* o, const void* dout, float* delta, i
   if (s != ATTN_OK) return s;
   s = need_ptrs({{o, "o"}, {dout, "dout"}, {delta, "delta"}});
   if (s != ATTN_OK) return s;
-  cudaError_t e = launch_bwd_preprocess(o, dout, delta, nullptr, B, Lq, Hq, d, dtype == ATTN_BF16,
-                                        reinterpret_cast<cudaStream_t>(stream));
+  PreprocessArgs pa;
+  pa.o = o;
+  pa.dout = dout;
+  pa.lse = nullptr;
+  pa.delta = delta;
+  pa.lse2 = nullptr;
+  pa.dq_acc = nullptr;
+  pa.B = B;
+  pa.Lq = Lq;
+  pa.Lq_pad = Lq;
+  pa.Hq = Hq;
+  pa.d = d;
+  pa.is_bf16 = dtype == ATTN_BF16;
+  cudaError_t e = launch_bwd_preprocess(pa, reinterpret_cast<cudaStream_t>(stream));
   return from_cuda(e, "attn_bwd_preprocess launch");
 }
 
 size_t attn_bwd_workspace_size(int B, int Lq, int Hq, int d, int deterministic, attn_dtype dtype) {
   (void)dtype;
   if (B <= 0 || Lq <= 0 || Hq <= 0 || d <= 0) return 0;
-  size_t bytes = align256(static_cast<size_t>(B) * Hq * Lq * sizeof(float));
+  size_t bytes = 2 * bwd_rowstat_bytes(B, Lq, Hq);  // delta and lse2, padded rows
   if (!deterministic) bytes += align256(static_cast<size_t>(B) * Lq * Hq * d * sizeof(float));
   return bytes;
 }
@@ -245,10 +264,11 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
+  const size_t rs = bwd_rowstat_bytes(B, Lq, Hq);
   a.delta = static_cast<float*>(workspace);
-  a.dq_acc = deterministic ? nullptr
-                           : reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                                      align256(static_cast<size_t>(B) * Hq * Lq * sizeof(float)));
+  a.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + rs);
+  a.dq_acc = deterministic ? nullptr : reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * rs);
+  a.Lq_pad = lq_padded(Lq);
   a.deterministic = deterministic;
   DeviceStatus* st = status_ptr();
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);

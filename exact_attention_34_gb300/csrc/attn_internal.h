@@ -43,12 +43,25 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
-  float* delta;  // workspace [B, Hq, Lq]
-  float* dq_acc; // workspace [B, Lq, Hq, d] (atomic variant only)
+  float* delta;   // workspace [B, Hq, Lq_pad]
+  float* lse2;    // workspace [B, Hq, Lq_pad]: lse * log2(e), +inf on empty and pad rows
+  float* dq_acc;  // workspace [B, Lq, Hq, d] (atomic variant only)
+  int Lq_pad;     // Lq rounded up to a multiple of 128
   int deterministic;
 };
-cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* delta, float* dq_acc, int B, int Lq, int Hq,
-                                  int d, int is_bf16, cudaStream_t s);
+
+// delta = rowsum(dO * O) in the padded [B, Hq, Lq_pad] layout; optional lse2,
+// pad-row fill and dQ-accumulator zeroing (see small_kernels.cu).
+struct PreprocessArgs {
+  const void* o;
+  const void* dout;
+  const float* lse;  // needed when lse2 != nullptr
+  float* delta;
+  float* lse2;       // nullable
+  float* dq_acc;     // nullable
+  int B, Lq, Lq_pad, Hq, d, is_bf16;
+};
+cudaError_t launch_bwd_preprocess(const PreprocessArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_bf16(const BwdArgs& a, DeviceStatus* st, cudaStream_t s);
 cudaError_t launch_bwd_f32(const BwdArgs& a, DeviceStatus* st, cudaStream_t s);
 

@@ -1,0 +1,702 @@
+// Backward attention, bf16, head_dim 64/128, on the sm_103a tensor cores.
+//
+// Method (probjax "Attention performance", section "When to use which",
+// backward pass): the probabilities are recomputed from the forward's
+// log-sum-exp, P = 2^(s * scale * log2(e) - lse * log2(e)), with
+//   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - delta),  delta = rowsum(dO * O),
+//   dQ = scale * dS K,  dK = scale * dS^T Q.
+// Two variants, as on the pages:
+//   * two-pass, deterministic: a dK/dV kernel per KV tile, then a separate dQ
+//     kernel per query tile; every sum runs in a fixed order, so the result
+//     is bitwise reproducible;
+//   * single pass: the dK/dV kernel also adds dS K into a float32 dQ buffer
+//     with atomic adds (order not reproducible), then a convert kernel.
+// KV tiles past a batch element's length store zeros without running the
+// pipeline; query tiles that see none of a key tile (causal) are skipped.
+//
+// dK/dV kernel: CTA = (batch, KV head, 128 keys); thread = key row = TMEM
+// lane.  It walks the G query heads of the group and their 64-row query
+// tiles.  Per step: S^T = K Q^T and dP^T = V dO^T (tcgen05, fp32 in TMEM),
+// the softmax warps turn them into P^T and dS^T (bf16, written back to TMEM
+// over the first half of their columns), then dV += P^T dO and
+// dK += dS^T Q take those as the A operand straight from TMEM.  S^T/dP^T are
+// double-buffered so the next step's MMAs run while the softmax works.
+// TMEM: dK [0,128) dV [128,256) stage s: S^T [256+128s, +64) dP^T [+64, +128).
+// The single-pass variant keeps one stage and adds dQ^T = K^T dS^T
+// (M = head_dim, N = 64 queries) in columns [384, 448), with dS^T staged in
+// shared memory; the softmax warps read it out (thread = head-dim column) and
+// reduce it into the float32 buffer.
+//
+// dQ kernel: CTA = (batch, head, 128 queries); thread = query row.  Per
+// 64-key step: S = Q K^T, dP = dO V^T, dS (bf16, into TMEM), dQ += dS K.
+// TMEM: dQ [0,128) stage s: S [128+128s, +64) dP [+64, +128).
+#include "attn_internal.h"
+
+namespace attn {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ int key_limit(int i, int Lq, int kvl, int causal) {
+  if (!causal) return kvl;
+  return min(kvl, i + 1 + kvl - Lq);
+}
+
+struct BwdKParams {
+  const float* lse2;   // [B, Hq, Lq_pad], log2 domain, +inf on empty/pad rows
+  const float* delta;  // [B, Hq, Lq_pad]
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dq_acc;       // single-pass variant
+  const int32_t* kv_lens;
+  int Lq, Lkv, Hq, Hkv, G, causal, Lq_pad, n_tiles;
+  float scale, scale_log2;
+  DeviceStatus* status;
+};
+
+// Store one row of D fp32 values from TMEM (columns col..col+D) as bf16, times `mul`.
+template <int D>
+__device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16* dst, float mul, bool do_store,
+                                               bool zero) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t r[32];
+    if (!zero) {
+      tmem_ld32(taddr + c * 32, r);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = 0u;
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+    if (do_store) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    }
+  }
+}
+
+// ============================================================================
+// dK / dV kernel
+// ============================================================================
+template <int D, bool ATOMIC>
+struct DkdvCfg {
+  static constexpr int kBN = 128;                    // keys per CTA
+  static constexpr int kBM = 64;                     // queries per step
+  static constexpr int kKVBytes = kBN * D * 2;       // K or V tile
+  static constexpr int kKBox = kBN * 128;            // one 64-column box of K/V
+  static constexpr int kQBytes = kBM * D * 2;        // Q_i or dO_i tile
+  static constexpr int kQBox = kBM * 128;            // one 64-column box of Q/dO
+  static constexpr int kStages = ATOMIC ? 3 : 4;     // shared-memory ring of (Q, dO, lse2, delta)
+  static constexpr int kTStages = ATOMIC ? 1 : 2;    // TMEM stages of (S^T, dP^T)
+  static constexpr int kOffV = kKVBytes;
+  static constexpr int kOffQ = 2 * kKVBytes;
+  static constexpr int kOffDS = kOffQ + kStages * 2 * kQBytes;
+  static constexpr int kOffStat = kOffDS + (ATOMIC ? kBN * kBM * 2 : 0);
+  static constexpr int kOffBars = kOffStat + kStages * 2 * kBM * 4;
+  static constexpr int kNumBars = 2 * kStages + 1 + 2 * kTStages + 3;
+  static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
+  static constexpr int kThreads = 192;
+  static constexpr uint32_t kColS = 256;   // first stage's S^T column
+  static constexpr uint32_t kColDQ = 384;  // dQ^T (single pass)
+};
+
+template <int D, bool ATOMIC>
+__global__ void __launch_bounds__(192, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdKParams p) {
+  using C = DkdvCfg<D, ATOMIC>;
+  constexpr int NS = C::kStages, TS = C::kTStages, BM = C::kBM;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::kOffV;
+  uint8_t* sQ = smem + C::kOffQ;  // stage s: Q at s * 2 * kQBytes, dO right after
+  uint8_t* sDS = smem + C::kOffDS;
+  float* sStat = reinterpret_cast<float*>(smem + C::kOffStat);  // stage s: lse2[64], delta[64]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + NS;
+  uint64_t* kv_full = bars + 2 * NS;
+  uint64_t* s_full = kv_full + 1;       // [TS]
+  uint64_t* p_full = s_full + TS;       // [TS]
+  uint64_t* acc_full = p_full + TS;
+  uint64_t* dq_full = acc_full + 1;
+  uint64_t* dq_free = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  const int j0 = blockIdx.x * C::kBN, hk = blockIdx.y, b = blockIdx.z;
+  int kvl = p.Lkv;
+  if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
+  const int q_first = p.causal ? max(0, j0 + p.Lq - kvl) : 0;
+  const int i_begin = q_first / BM;
+  const int n_qt = (p.Lq + BM - 1) / BM;
+  const int steps_per_head = (j0 < kvl && i_begin < n_qt) ? n_qt - i_begin : 0;
+  const int T = steps_per_head * p.G;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < TS; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 128);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_free, 128);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && T > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(kv_full, 2 * C::kKVBytes);
+      for (int h = 0; h < D / 64; ++h) {
+        tma_load_4d(sK + h * C::kKBox, &tm_k, kv_full, h * 64, j0, hk, b);
+        tma_load_4d(sV + h * C::kKBox, &tm_v, kv_full, h * 64, j0, hk, b);
+      }
+      for (int t = 0; t < T; ++t) {
+        const int s = t % NS, r = t / NS;
+        if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort_flag, p.status, 21)) break;
+        const int h = hk * p.G + t / steps_per_head;
+        const int q0 = (i_begin + t % steps_per_head) * BM;
+        mbar_arrive_expect_tx(&full[s], 2 * C::kQBytes + 2 * BM * 4);
+        uint8_t* q_dst = sQ + s * 2 * C::kQBytes;
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_4d(q_dst + c * C::kQBox, &tm_q, &full[s], c * 64, q0, h, b);
+          tma_load_4d(q_dst + C::kQBytes + c * C::kQBox, &tm_do, &full[s], c * 64, q0, h, b);
+        }
+        const size_t row = (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + q0;
+        bulk_load(sStat + s * 2 * BM, p.lse2 + row, BM * 4, &full[s]);
+        bulk_load(sStat + s * 2 * BM + BM, p.delta + row, BM * 4, &full[s]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && T > 0) {
+      constexpr uint32_t idesc_st = idesc_bf16_f32(128, BM, 0, 0);  // K x Q^T
+      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, 0, 1);  // P^T (TMEM) x dO (MN-major)
+      constexpr uint32_t idesc_dq = idesc_bf16_f32(128, BM, 1, 1);  // K^T (MN-major) x dS^T (MN-major)
+      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ);
+      const uint32_t ds_addr = smem_u32(sDS);
+      auto issue_scores = [&](int t) {
+        const int s = t % NS, ts = t % TS;
+        const uint32_t qa = q_addr + s * 2 * C::kQBytes, da = qa + C::kQBytes;
+        const uint32_t col = tbase + C::kColS + ts * 128;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t ko = (k >> 2) * C::kKBox + (k & 3) * 32;
+          const uint32_t qo = (k >> 2) * C::kQBox + (k & 3) * 32;
+          mma_ss(col, sdesc_sw128(k_addr + ko, 16, 1024), sdesc_sw128(qa + qo, 16, 1024), idesc_st, k > 0);
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t ko = (k >> 2) * C::kKBox + (k & 3) * 32;
+          const uint32_t qo = (k >> 2) * C::kQBox + (k & 3) * 32;
+          mma_ss(col + 64, sdesc_sw128(v_addr + ko, 16, 1024), sdesc_sw128(da + qo, 16, 1024), idesc_st, k > 0);
+        }
+        mma_commit(&s_full[ts]);
+      };
+      bool ok = mbar_wait(kv_full, 0, abort_flag, p.status, 22);
+      for (int t = 0; t < TS && t < T && ok; ++t) {
+        ok = mbar_wait(&full[t % NS], (t / NS) & 1, abort_flag, p.status, 23);
+        if (!ok) break;
+        tc_fence_after();
+        issue_scores(t);
+      }
+      for (int t = 0; t < T && ok; ++t) {
+        const int s = t % NS, ts = t % TS;
+        ok = mbar_wait(&p_full[ts], (t / TS) & 1, abort_flag, p.status, 24);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t qa = q_addr + s * 2 * C::kQBytes, da = qa + C::kQBytes;
+        const uint32_t col = tbase + C::kColS + ts * 128;
+#pragma unroll
+        for (int k = 0; k < BM / 16; ++k) {  // dV += P^T dO
+          mma_ts(tbase + 128, col + k * 8, sdesc_sw128(da + k * 2048, C::kQBox, 1024), idesc_acc,
+                 (t > 0 || k > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < BM / 16; ++k) {  // dK += dS^T Q
+          mma_ts(tbase + 0, col + 64 + k * 8, sdesc_sw128(qa + k * 2048, C::kQBox, 1024), idesc_acc,
+                 (t > 0 || k > 0) ? 1u : 0u);
+        }
+        if constexpr (ATOMIC) {
+          if (t > 0) {
+            ok = mbar_wait(dq_free, (t - 1) & 1, abort_flag, p.status, 25);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          // dQ^T = K^T dS^T : M = head dim (the second 64-row block repeats the
+          // first when D = 64), N = 64 queries, K = 128 keys.
+          constexpr uint32_t lbo_k = (D == 128) ? static_cast<uint32_t>(C::kKBox) : 0u;
+#pragma unroll
+          for (int k = 0; k < C::kBN / 16; ++k) {
+            mma_ss(tbase + C::kColDQ, sdesc_sw128(k_addr + k * 2048, lbo_k, 1024),
+                   sdesc_sw128(ds_addr + k * 2048, 16, 1024), idesc_dq, k > 0);
+          }
+          mma_commit(dq_full);
+        }
+        mma_commit(&empty[s]);
+        if (t + TS < T) {
+          const int tn = t + TS;
+          ok = mbar_wait(&full[tn % NS], (tn / NS) & 1, abort_flag, p.status, 26);
+          if (!ok) break;
+          tc_fence_after();
+          issue_scores(tn);
+        }
+      }
+      if (ok) mma_commit(acc_full);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax (thread = key row)
+    const int r = warp * 32 + lane;
+    const int j = j0 + r;
+    const uint32_t t_lane = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+    const bool key_ok = j < kvl;
+    const int q_min = p.causal ? j + p.Lq - kvl : -0x7fffffff;  // first query that sees key j
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int s = t % NS, ts = t % TS;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[ts], (t / TS) & 1, abort_flag, p.status, 27));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t col = t_lane + C::kColS + ts * 128;
+      const int q0 = (i_begin + t % steps_per_head) * BM;
+      const float* lse2 = sStat + s * 2 * BM;
+      const float* dlt = lse2 + BM;
+      uint32_t sr[64], dr[64];
+      {
+        uint32_t a[32];
+        tmem_ld32(col, a);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sr[i] = a[i];
+        tmem_ld32(col + 32, a);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sr[32 + i] = a[i];
+        tmem_ld32(col + 64, a);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) dr[i] = a[i];
+        tmem_ld32(col + 96, a);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) dr[32 + i] = a[i];
+      }
+      const bool all_valid = key_ok && q0 >= q_min;
+      uint32_t pk[32], dk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float pr[2], ds[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = 2 * i + e;
+          const bool valid = all_valid || (key_ok && q0 + c >= q_min);
+          const float pv = valid ? ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2[c])) : 0.f;
+          pr[e] = pv;
+          ds[e] = pv * (__uint_as_float(dr[c]) - dlt[c]);
+        }
+        pk[i] = pack_bf16x2(pr[0], pr[1]);
+        dk[i] = pack_bf16x2(ds[0], ds[1]);
+      }
+      tmem_st32(col, pk);
+      tmem_st32(col + 64, dk);
+      if constexpr (ATOMIC) {
+        // dS^T row r -> shared memory, 128B-swizzled (MN-major operand of dQ^T)
+        uint8_t* row = sDS + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) * 16)) =
+              make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+        fence_proxy_async_smem();
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full[ts]);
+      if constexpr (ATOMIC) {
+        ok = __all_sync(0xffffffffu, mbar_wait(dq_full, t & 1, abort_flag, p.status, 28));
+        if (!ok) break;
+        tc_fence_after();
+        if (r < D) {  // thread = head-dim column d = r; columns = the 64 queries
+          const int h = hk * p.G + t / steps_per_head;
+          uint32_t a[32];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            tmem_ld32(t_lane + C::kColDQ + half * 32, a);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int q = q0 + half * 32 + i;
+              if (q < p.Lq)
+                atomicAdd(p.dq_acc + ((static_cast<size_t>(b) * p.Lq + q) * p.Hq + h) * D + r, __uint_as_float(a[i]));
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(dq_free);
+      }
+    }
+    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 29));
+    if (ok) {
+      tc_fence_after();
+      const bool st = j < p.Lkv;
+      const size_t off = ((static_cast<size_t>(b) * p.Lkv + (st ? j : 0)) * p.Hkv + hk) * D;
+      store_row_bf16<D>(t_lane + 0, reinterpret_cast<__nv_bfloat16*>(p.dk) + off, p.scale, st, T == 0);
+      store_row_bf16<D>(t_lane + 128, reinterpret_cast<__nv_bfloat16*>(p.dv) + off, 1.0f, st, T == 0);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// ============================================================================
+// dQ kernel
+// ============================================================================
+template <int D>
+struct DqCfg {
+  static constexpr int kBM = 128;               // queries per CTA
+  static constexpr int kBN = 64;                // keys per step
+  static constexpr int kQBytes = kBM * D * 2;
+  static constexpr int kQBox = kBM * 128;
+  static constexpr int kKVBytes = kBN * D * 2;
+  static constexpr int kKBox = kBN * 128;
+  static constexpr int kStages = 4;
+  static constexpr int kOffDO = kQBytes;
+  static constexpr int kOffKV = 2 * kQBytes;  // stage s: K at s * 2 * kKVBytes, V right after
+  static constexpr int kOffBars = kOffKV + kStages * 2 * kKVBytes;
+  static constexpr int kNumBars = 2 * kStages + 1 + 4 + 1;
+  static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const BwdKParams p) {
+  using C = DqCfg<D>;
+  constexpr int NS = C::kStages, BN = C::kBN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* sQ = smem;
+  uint8_t* sDO = smem + C::kOffDO;
+  uint8_t* sKV = smem + C::kOffKV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + NS;
+  uint64_t* q_full = bars + 2 * NS;
+  uint64_t* s_full = q_full + 1;  // [2]
+  uint64_t* p_full = q_full + 3;  // [2]
+  uint64_t* acc_full = q_full + 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  const int qt = p.causal ? (p.n_tiles - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const int q0 = qt * C::kBM, h = blockIdx.y, b = blockIdx.z;
+  const int hk = h / p.G;
+  int kvl = p.Lkv;
+  if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
+  const int last = min(q0 + C::kBM - 1, p.Lq - 1);
+  const int lim_last = key_limit(last, p.Lq, kvl, p.causal);
+  const int T = lim_last > 0 ? (lim_last + BN - 1) / BN : 0;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 128);
+    }
+    mbar_init(acc_full, 1);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 4) {
+    if (lane == 0 && T > 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(q_full, 2 * C::kQBytes);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_4d(sQ + c * C::kQBox, &tm_q, q_full, c * 64, q0, h, b);
+        tma_load_4d(sDO + c * C::kQBox, &tm_do, q_full, c * 64, q0, h, b);
+      }
+      for (int t = 0; t < T; ++t) {
+        const int s = t % NS, r = t / NS;
+        if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort_flag, p.status, 31)) break;
+        mbar_arrive_expect_tx(&full[s], 2 * C::kKVBytes);
+        uint8_t* dst = sKV + s * 2 * C::kKVBytes;
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_4d(dst + c * C::kKBox, &tm_k, &full[s], c * 64, t * BN, hk, b);
+          tma_load_4d(dst + C::kKVBytes + c * C::kKBox, &tm_v, &full[s], c * 64, t * BN, hk, b);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    if (lane == 0 && T > 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, 0, 0);   // Q x K^T
+      constexpr uint32_t idesc_dq = idesc_bf16_f32(128, D, 0, 1);  // dS (TMEM) x K (MN-major)
+      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO), kv_addr = smem_u32(sKV);
+      auto issue_scores = [&](int t) {
+        const int s = t % NS, ts = t & 1;
+        const uint32_t ka = kv_addr + s * 2 * C::kKVBytes, va = ka + C::kKVBytes;
+        const uint32_t col = tbase + 128 + ts * 128;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t qo = (k >> 2) * C::kQBox + (k & 3) * 32;
+          const uint32_t ko = (k >> 2) * C::kKBox + (k & 3) * 32;
+          mma_ss(col, sdesc_sw128(q_addr + qo, 16, 1024), sdesc_sw128(ka + ko, 16, 1024), idesc_s, k > 0);
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t qo = (k >> 2) * C::kQBox + (k & 3) * 32;
+          const uint32_t ko = (k >> 2) * C::kKBox + (k & 3) * 32;
+          mma_ss(col + 64, sdesc_sw128(do_addr + qo, 16, 1024), sdesc_sw128(va + ko, 16, 1024), idesc_s, k > 0);
+        }
+        mma_commit(&s_full[ts]);
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.status, 32);
+      for (int t = 0; t < 2 && t < T && ok; ++t) {
+        ok = mbar_wait(&full[t % NS], (t / NS) & 1, abort_flag, p.status, 33);
+        if (!ok) break;
+        tc_fence_after();
+        issue_scores(t);
+      }
+      for (int t = 0; t < T && ok; ++t) {
+        const int s = t % NS, ts = t & 1;
+        ok = mbar_wait(&p_full[ts], (t >> 1) & 1, abort_flag, p.status, 34);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t ka = kv_addr + s * 2 * C::kKVBytes;
+        const uint32_t col = tbase + 128 + ts * 128;
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k) {  // dQ += dS K
+          mma_ts(tbase, col + k * 8, sdesc_sw128(ka + k * 2048, C::kKBox, 1024), idesc_dq,
+                 (t > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(&empty[s]);
+        if (t + 2 < T) {
+          const int tn = t + 2;
+          ok = mbar_wait(&full[tn % NS], (tn / NS) & 1, abort_flag, p.status, 35);
+          if (!ok) break;
+          tc_fence_after();
+          issue_scores(tn);
+        }
+      }
+      if (ok) mma_commit(acc_full);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax (thread = query row)
+    const int r = warp * 32 + lane;
+    const int i = q0 + r;
+    const uint32_t t_lane = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+    const size_t srow = (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + i;  // i < Lq_pad always
+    const float l2 = p.lse2[srow];
+    const float dl = p.delta[srow];
+    const int lim = i < p.Lq ? key_limit(i, p.Lq, kvl, p.causal) : 0;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int ts = t & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[ts], (t >> 1) & 1, abort_flag, p.status, 36));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t col = t_lane + 128 + ts * 128;
+      uint32_t sr[64], dr[64];
+      {
+        uint32_t a[32];
+        tmem_ld32(col, a);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sr[c] = a[c];
+        tmem_ld32(col + 32, a);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sr[32 + c] = a[c];
+        tmem_ld32(col + 64, a);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) dr[c] = a[c];
+        tmem_ld32(col + 96, a);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) dr[32 + c] = a[c];
+      }
+      const int kb = t * BN;
+      const bool all_valid = kb + BN <= lim;
+      uint32_t pk[32];
+#pragma unroll
+      for (int c2 = 0; c2 < 32; ++c2) {
+        float ds[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = 2 * c2 + e;
+          const bool valid = all_valid || kb + c < lim;
+          const float pv = valid ? ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -l2)) : 0.f;
+          ds[e] = pv * (__uint_as_float(dr[c]) - dl);
+        }
+        pk[c2] = pack_bf16x2(ds[0], ds[1]);
+      }
+      tmem_st32(col, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full[ts]);
+    }
+    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 37));
+    if (ok) {
+      tc_fence_after();
+      const bool st = i < p.Lq;
+      const size_t off = ((static_cast<size_t>(b) * p.Lq + (st ? i : 0)) * p.Hq + h) * D;
+      store_row_bf16<D>(t_lane, reinterpret_cast<__nv_bfloat16*>(p.dq) + off, p.scale, st, T == 0);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// dq = scale * dq_acc cast to bf16 (single-pass variant)
+__global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, long n4,
+                                  float scale) {
+  const long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const float4 a = reinterpret_cast<const float4*>(acc)[i];
+  uint2 o;
+  o.x = pack_bf16x2(a.x * scale, a.y * scale);
+  o.y = pack_bf16x2(a.z * scale, a.w * scale);
+  reinterpret_cast<uint2*>(dq)[i] = o;
+}
+
+template <int D>
+cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream) {
+  const Problem& pb = a.pb;
+  PreprocessArgs pa;
+  pa.o = a.o;
+  pa.dout = a.dout;
+  pa.lse = a.lse;
+  pa.delta = a.delta;
+  pa.lse2 = a.lse2;
+  pa.dq_acc = a.deterministic ? nullptr : a.dq_acc;
+  pa.B = pb.B;
+  pa.Lq = pb.Lq;
+  pa.Lq_pad = a.Lq_pad;
+  pa.Hq = pb.Hq;
+  pa.d = D;
+  pa.is_bf16 = 1;
+  cudaError_t e = launch_bwd_preprocess(pa, stream);
+  if (e != cudaSuccess) return e;
+
+  BwdKParams kp;
+  kp.lse2 = a.lse2;
+  kp.delta = a.delta;
+  kp.dq = a.dq;
+  kp.dk = a.dk;
+  kp.dv = a.dv;
+  kp.dq_acc = a.dq_acc;
+  kp.kv_lens = pb.kv_lens;
+  kp.Lq = pb.Lq;
+  kp.Lkv = pb.Lkv;
+  kp.Hq = pb.Hq;
+  kp.Hkv = pb.Hkv;
+  kp.G = pb.G;
+  kp.causal = pb.causal;
+  kp.Lq_pad = a.Lq_pad;
+  kp.scale = pb.scale;
+  kp.scale_log2 = pb.scale * kLog2e;
+  kp.status = st;
+
+  // dK/dV pass: K/V boxes of 128 rows, Q/dO boxes of 64 rows
+  {
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_bshd_tmap(&tq, a.q, true, pb.B, pb.Lq, pb.Hq, D, 64, 64) ||
+        !make_bshd_tmap(&tdo, a.dout, true, pb.B, pb.Lq, pb.Hq, D, 64, 64) ||
+        !make_bshd_tmap(&tk, a.k, true, pb.B, pb.Lkv, pb.Hkv, D, 64, 128) ||
+        !make_bshd_tmap(&tv, a.v, true, pb.B, pb.Lkv, pb.Hkv, D, 64, 128))
+      return cudaErrorInvalidValue;
+    dim3 grid((pb.Lkv + 127) / 128, pb.Hkv, pb.B);
+    kp.n_tiles = grid.x;
+    if (a.deterministic) {
+      using C = DkdvCfg<D, false>;
+      e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::kSmemBytes);
+      if (e != cudaSuccess) return e;
+      bwd_dkdv_kernel<D, false><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+    } else {
+      using C = DkdvCfg<D, true>;
+      e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::kSmemBytes);
+      if (e != cudaSuccess) return e;
+      bwd_dkdv_kernel<D, true><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (!a.deterministic) {
+    const long n4 = static_cast<long>(pb.B) * pb.Lq * pb.Hq * D / 4;
+    dq_convert_kernel<<<static_cast<int>((n4 + 255) / 256), 256, 0, stream>>>(
+        a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), n4, pb.scale);
+    return cudaGetLastError();
+  }
+  // dQ pass: Q/dO boxes of 128 rows, K/V boxes of 64 rows
+  {
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_bshd_tmap(&tq, a.q, true, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
+        !make_bshd_tmap(&tdo, a.dout, true, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
+        !make_bshd_tmap(&tk, a.k, true, pb.B, pb.Lkv, pb.Hkv, D, 64, 64) ||
+        !make_bshd_tmap(&tv, a.v, true, pb.B, pb.Lkv, pb.Hkv, D, 64, 64))
+      return cudaErrorInvalidValue;
+    using C = DqCfg<D>;
+    dim3 grid((pb.Lq + 127) / 128, pb.Hq, pb.B);
+    kp.n_tiles = grid.x;
+    e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    bwd_dq_kernel<D><<<grid, 192, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+    return cudaGetLastError();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_bf16(const BwdArgs& a, DeviceStatus* st, cudaStream_t s) {
+  return a.pb.d == 64 ? launch_bwd_bf16_d<64>(a, st, s) : launch_bwd_bf16_d<128>(a, st, s);
+}
+
+}  // namespace attn

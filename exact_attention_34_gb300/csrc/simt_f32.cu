@@ -497,8 +497,20 @@ cudaError_t launch_decode_f32(const DecodeArgs& a, DeviceStatus* st, cudaStream_
 cudaError_t launch_bwd_f32(const BwdArgs& a, DeviceStatus* st, cudaStream_t s) {
   (void)st;
   const Problem& pb = a.pb;
-  cudaError_t e = launch_bwd_preprocess(a.o, a.dout, a.delta, a.deterministic ? nullptr : a.dq_acc, pb.B, pb.Lq,
-                                        pb.Hq, pb.d, 0, s);
+  PreprocessArgs pa;
+  pa.o = a.o;
+  pa.dout = a.dout;
+  pa.lse = nullptr;
+  pa.delta = a.delta;  // unpadded [B, Hq, Lq] layout inside the (larger) workspace
+  pa.lse2 = nullptr;
+  pa.dq_acc = a.deterministic ? nullptr : a.dq_acc;
+  pa.B = pb.B;
+  pa.Lq = pb.Lq;
+  pa.Lq_pad = pb.Lq;
+  pa.Hq = pb.Hq;
+  pa.d = pb.d;
+  pa.is_bf16 = 0;
+  cudaError_t e = launch_bwd_preprocess(pa, s);
   if (e != cudaSuccess) return e;
   F32BwdParams p{};
   p.q = static_cast<const float*>(a.q);

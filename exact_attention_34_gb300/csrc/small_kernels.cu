@@ -28,23 +28,33 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&f)[8]) {
 }
 
 // delta[b, h, i] = sum_c dO[b, i, h, c] * O[b, i, h, c]  (float32 accumulate).
-// Each thread reduces 8 consecutive elements; D/8 threads share a row.  In the
-// atomic backward the same pass also zeroes the float32 dQ accumulator.
+// Rows are walked in the padded [B, Hq, Lq_pad] order of the outputs; D/8
+// threads share a row, each reducing 8 consecutive elements.  Optionally it
+// also writes lse2 = lse * log2(e) (+inf where lse = -inf, so that every
+// recomputed probability of such a row is 0), fills the pad rows
+// Lq <= i < Lq_pad with delta = 0 and lse2 = +inf, and zeroes the float32 dQ
+// accumulator of the atomic backward.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict__ o, const T* __restrict__ dout,
-                                                             float* __restrict__ delta, float* __restrict__ dq_acc,
-                                                             long n_rows, int Lq, int Hq) {
+                                                             const float* __restrict__ lse, float* __restrict__ delta,
+                                                             float* __restrict__ lse2, float* __restrict__ dq_acc,
+                                                             long n_rows_pad, int Lq, int Lq_pad, int Hq) {
   constexpr int kTPR = D / 8;  // threads per row
   const long tid = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long row = tid / kTPR;
+  const long prow = tid / kTPR;  // (b * Hq + h) * Lq_pad + i
   const int part = static_cast<int>(tid % kTPR);
+  const long bh = prow / Lq_pad;
+  const int i = static_cast<int>(prow % Lq_pad);
+  const long b = bh / Hq, h = bh % Hq;
+  const bool real = prow < n_rows_pad && i < Lq;
   float acc = 0.f;
-  if (row < n_rows) {
+  if (real) {
+    const long row = (b * Lq + i) * Hq + h;  // row of the [B, Lq, Hq, D] tensors
     float a[8], g[8];
     load8<T>(o + row * D + part * 8, a);
     load8<T>(dout + row * D + part * 8, g);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc = fmaf(a[i], g[i], acc);
+    for (int e = 0; e < 8; ++e) acc = fmaf(a[e], g[e], acc);
     if (dq_acc != nullptr) {
       float4* z = reinterpret_cast<float4*>(dq_acc + row * D + part * 8);
       z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -53,13 +63,12 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict
   }
 #pragma unroll
   for (int off = kTPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < n_rows && part == 0) {
-    // row = (b * Lq + i) * Hq + h
-    const long h = row % Hq;
-    const long bi = row / Hq;
-    const long i = bi % Lq;
-    const long b = bi / Lq;
-    delta[(b * Hq + h) * Lq + i] = acc;
+  if (prow < n_rows_pad && part == 0) {
+    delta[prow] = acc;  // 0 on pad rows
+    if (lse2 != nullptr) {
+      const float l = real ? lse[bh * Lq + i] : -INFINITY;
+      lse2[prow] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+    }
   }
 }
 
@@ -119,13 +128,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 }
 
 template <typename T, int D>
-cudaError_t run_preprocess(const void* o, const void* dout, float* delta, float* dq_acc, int B, int Lq, int Hq,
-                           cudaStream_t s) {
-  const long n_rows = static_cast<long>(B) * Lq * Hq;
+cudaError_t run_preprocess(const PreprocessArgs& a, cudaStream_t s) {
+  const long n_rows = static_cast<long>(a.B) * a.Hq * a.Lq_pad;
   const long threads = n_rows * (D / 8);
   const int blocks = static_cast<int>((threads + 255) / 256);
-  bwd_preprocess_kernel<T, D><<<blocks, 256, 0, s>>>(static_cast<const T*>(o), static_cast<const T*>(dout), delta,
-                                                     dq_acc, n_rows, Lq, Hq);
+  bwd_preprocess_kernel<T, D><<<blocks, 256, 0, s>>>(static_cast<const T*>(a.o), static_cast<const T*>(a.dout),
+                                                     a.lse, a.delta, a.lse2, a.dq_acc, n_rows, a.Lq, a.Lq_pad, a.Hq);
   return cudaGetLastError();
 }
 
@@ -140,14 +148,11 @@ cudaError_t run_combine(const float* o_part, const float* lse_part, void* o, flo
 
 }  // namespace
 
-cudaError_t launch_bwd_preprocess(const void* o, const void* dout, float* delta, float* dq_acc, int B, int Lq, int Hq,
-                                  int d, int is_bf16, cudaStream_t s) {
-  if (is_bf16) {
-    return d == 64 ? run_preprocess<__nv_bfloat16, 64>(o, dout, delta, dq_acc, B, Lq, Hq, s)
-                   : run_preprocess<__nv_bfloat16, 128>(o, dout, delta, dq_acc, B, Lq, Hq, s);
+cudaError_t launch_bwd_preprocess(const PreprocessArgs& a, cudaStream_t s) {
+  if (a.is_bf16) {
+    return a.d == 64 ? run_preprocess<__nv_bfloat16, 64>(a, s) : run_preprocess<__nv_bfloat16, 128>(a, s);
   }
-  return d == 64 ? run_preprocess<float, 64>(o, dout, delta, dq_acc, B, Lq, Hq, s)
-                 : run_preprocess<float, 128>(o, dout, delta, dq_acc, B, Lq, Hq, s);
+  return a.d == 64 ? run_preprocess<float, 64>(a, s) : run_preprocess<float, 128>(a, s);
 }
 
 cudaError_t launch_decode_combine(const float* o_part, const float* lse_part, void* o, float* lse, int B, int Lq,
