@@ -1,0 +1,509 @@
+#!/usr/bin/env python
+"""Benchmark: bf16 causal attention fwd+bwd at B4 H8 T8192 d128 on GB300.
+
+One step = one pass of the hot path over one batch of seeded synthetic input:
+attn_fwd (O, LSE) then attn_bwd (delta preprocess, dK/dV kernel, dQ kernel;
+the deterministic two-pass backward).  FLOPs follow the pages' convention:
+fwd = 4 * B * H * Lq * Lkv * d, exactly halved for causal, fwd+bwd = 3.5x.
+
+Prints ONE JSON line (rank 0).  Under torchrun (N > 1) every rank runs its own
+independent replica of the step on its own GPU (the units are independent; no
+collective on the data path) and the value is the total work of all ranks
+divided by the slowest rank's time ("weak" scaling).
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this
+project has) on the host cores, one bounded sample of the same workload per
+step; under torchrun only rank 0 runs it.
+
+Inputs (256 MiB of q/k/v/dO plus outputs) are larger than the 129 MB L2, so no
+L2 flush is done between steps.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "fwd+bwd TFLOP/s (bf16, B4 H8 T8192 d128 causal) and % of GB300 tensor peak"
+UNIT = "TFLOP/s"
+
+
+# ----------------------------------------------------------------------------
+# rank handling (host logic; tested with gloo on CPU)
+# ----------------------------------------------------------------------------
+
+def dist_env():
+    """(rank, local_rank, world_size) from the torchrun environment."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x over all ranks (x itself when world == 1)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """TFLOP/s of all ranks together: every rank does flops_per_step per step."""
+    return world * flops_per_step * steps / (max_ms * 1e-3) / 1e12
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+CLOCK_FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    """Samples nvidia-smi every 200 ms in the background; keeps the samples
+    taken between mark_start() and mark_stop()."""
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.t0 = self.t1 = None
+        self.proc = None
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(CLOCK_FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._reader, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+        return self
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.strip().split(",")]
+            if len(parts) == len(CLOCK_FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
+        time.sleep(0.25)
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples or self.t0 is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"], "samples": 0}
+        t1 = self.t1 if self.t1 is not None else time.time()
+        win = [p for (t, p) in self.samples if self.t0 - 0.2 <= t <= t1 + 0.2] or [p for (_, p) in self.samples]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = sorted(v for v in (num(p[1]) for p in win) if v is not None)
+        mx = [v for v in (num(p[2]) for p in win) if v is not None]
+        names = {5: "hw_slowdown", 6: "hw_thermal_slowdown", 7: "sw_thermal_slowdown", 8: "sw_power_cap"}
+        reasons = sorted({names[i] for p in win for i in names if p[i].lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(win),
+                "power_w_max": max((v for v in (num(p[3]) for p in win) if v is not None), default=None)}
+
+
+# ----------------------------------------------------------------------------
+# measured peaks and the committed ncu traffic summary
+# ----------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def source_digest(kernel_file: str) -> str:
+    with open(os.path.join(ROOT, "exact_attention_34_gb300", "csrc", kernel_file), "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()[:12]
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from profiles/ncu_traffic.json, or None
+    when absent or when the kernel source changed since the capture."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            d = json.load(f)[kernel]
+        if d["source_sha1"] != source_digest(d["source_file"]):
+            return None
+        return float(d["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError, TypeError):
+        return None
+
+
+# ----------------------------------------------------------------------------
+# the GPU arm
+# ----------------------------------------------------------------------------
+
+KERNEL_FILES = {"fwd": "fwd_sm103.cu", "bwd_dkdv": "bwd_sm103.cu", "bwd_dq": "bwd_sm103.cu",
+                "bwd_preprocess": "small_kernels.cu", "decode": "decode_sm103.cu", "combine": "small_kernels.cu"}
+
+
+def run_gpu(args):
+    import torch
+
+    import exact_attention_34_gb300 as ea
+    from exact_attention_34_gb300 import build as eb
+
+    rank, local_rank, world = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback)")
+    torch.cuda.set_device(local_rank)
+    dist_init(world, "nccl")
+    eb.build()
+    dev = torch.device("cuda", local_rank)
+
+    p = W.headline()
+    F_fwd = W.fwd_flops(p)
+    F_step = 3.5 * F_fwd
+    q_h, k_h, v_h, do_h = (t.pin_memory() for t in W.make_inputs(p, seed=0))
+    q, k, v, do = (t.to(dev) for t in (q_h, k_h, v_h, do_h))
+    o = torch.empty_like(q)
+    lse = torch.empty(p.B, p.Hq, p.Lq, device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(ea.attn_bwd_workspace_size(p.B, p.Lq, p.Hq, p.d, True, q.dtype), device=dev,
+                     dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ea.attn_fwd(q, k, v, o, lse, causal=True, stream=stream)
+        ea.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, ws, causal=True, deterministic=True, stream=stream)
+
+    # ---- device-resident timing: EXACTLY `steps` steps between events
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        clk.mark_start()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        clk.mark_stop()
+        barrier(world)
+    local_ms = ev0.elapsed_time(ev1)
+    max_ms = max_over_ranks(local_ms, world, dev)
+    value = whole_job_value(F_step, args.steps, world, max_ms)
+    ms_per_step = max_ms / args.steps
+
+    # ---- per-kernel durations (a separate pass with launch events enabled)
+    ea.attn_timing_enable(True)
+    for _ in range(args.kernel_steps):
+        step()
+    torch.cuda.synchronize()
+    ktimes = {}
+    for name in ("fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq"):
+        ms, n = ea.attn_timing_query(name)
+        ktimes[name] = {"avg_ms": ms / max(n, 1), "launches": n}
+    ea.attn_timing_enable(False)
+    # algorithmic work per launch: dK/dV carries 4 of the 5 backward GEMMs
+    # (S, dP, dV, dK), dQ carries dS K (its S and dP are recomputation)
+    peaks = measured_peaks()
+    algo = {"fwd": F_fwd, "bwd_dkdv": 2.0 * F_fwd, "bwd_dq": 0.5 * F_fwd}
+    dom = max(("fwd", "bwd_dkdv", "bwd_dq"), key=lambda n: ktimes[n]["avg_ms"])
+    achieved = algo[dom] / (ktimes[dom]["avg_ms"] * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(dom),
+                "peak_kind": f"bf16 dense, sustained, {peaks['source']}",
+                "per_kernel": {n: {"avg_ms": round(ktimes[n]["avg_ms"], 4), "launches": ktimes[n]["launches"],
+                                   **({"tflops": round(algo[n] / (ktimes[n]["avg_ms"] * 1e-3) / 1e12, 1)}
+                                      if n in algo and ktimes[n]["avg_ms"] > 0 else {})}
+                               for n in ktimes}}
+
+    # ---- end to end through the public API with host buffers
+    dq_h, dk_h, dv_h = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv))
+    q2, k2, v2, do2 = (torch.empty_like(t) for t in (q, k, v, do))
+
+    def e2e_step():
+        for dst, src in ((q2, q_h), (k2, k_h), (v2, v_h), (do2, do_h)):
+            dst.copy_(src, non_blocking=True)
+        ea.attn_fwd(q2, k2, v2, o, lse, causal=True, stream=stream)
+        ea.attn_bwd(q2, k2, v2, o, lse, do2, dq, dk, dv, ws, causal=True, deterministic=True, stream=stream)
+        for dst, src in ((dq_h, dq), (dk_h, dk), (dv_h, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_steps = max(3, args.steps // 10)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, do_h))
+    d2h = sum(t.numel() * t.element_size() for t in (dq_h, dk_h, dv_h))
+    e2e = {"value": round(whole_job_value(F_step, e2e_steps, world, e2e_ms), 2), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+
+    st, code, site = ea.attn_device_status()
+    if code != 0:
+        raise SystemExit(f"device status {code} at site {site}")
+
+    extra = {}
+    if rank == 0 and not args.no_extra:
+        extra = other_rows(args, dev, peaks)
+
+    result = None
+    if rank == 0:
+        clocks = clk.summary()
+        cpu = None if args.no_cpu_baseline else cpu_baseline_sample(args.cpu_budget_s)
+        result = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "bf16 causal attention fwd+bwd, B4 H8 T8192 d128 (deterministic two-pass bwd)",
+                       "global_batch": p.B * world, "seq_len": p.Lq, "heads": p.Hq, "head_dim": p.d,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (256 MiB q/k/v/dO), no flush",
+                       "flops_per_step": F_step},
+            "pct_of_peak": {"burst": round(value / world / peaks["bf16_tflops"], 4),
+                            "sustained": round(value / world / peaks["bf16_tflops_sustained"], 4),
+                            "source": peaks["source"]},
+            "roofline": roofline, "e2e": e2e, "gpu_launches": 4 * args.steps, "clocks": clocks,
+            "cpu_baseline": cpu, "rows": extra,
+        }
+    return result
+
+
+def other_rows(args, dev, peaks):
+    """Quick one-shot numbers for the other rows of the path (context, not the headline)."""
+    import torch
+
+    import exact_attention_34_gb300 as ea
+
+    out = {}
+
+    def timed(fn, n=10):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    g = torch.Generator(device=dev).manual_seed(0)
+    # KVLenMask + GQA + Lq != Lkv fwd+bwd (flops over valid keys)
+    p = W.kvlen_gqa()
+    q = torch.randn(p.B, p.Lq, p.Hq, p.d, device=dev, generator=g).to(torch.bfloat16)
+    k = torch.randn(p.B, p.Lkv, p.Hkv, p.d, device=dev, generator=g).to(torch.bfloat16)
+    v = torch.randn_like(k)
+    do = torch.randn_like(q)
+    kl = torch.tensor(p.kv_lens, dtype=torch.int32, device=dev)
+
+    def kv_step():
+        o, lse = ea.forward(q, k, v, kv_lens=kl)
+        ea.backward(q, k, v, o, lse, do, kv_lens=kl)
+
+    ms = timed(kv_step)
+    out["kvlen_gqa_fwd_bwd"] = {"ms": round(ms, 4), "tflops": round(3.5 * W.fwd_flops(p) / ms / 1e9, 1)}
+    del q, k, v, do
+    # split-KV decode (HBM-bound): bytes of valid K/V + q + partials + o
+    for Lq, causal in ((1, False), (16, True)):
+        p = W.decode(Lq, causal)
+        q = torch.randn(p.B, p.Lq, p.Hq, p.d, device=dev, generator=g).to(torch.bfloat16)
+        k = torch.randn(p.B, p.Lkv, p.Hkv, p.d, device=dev, generator=g).to(torch.bfloat16)
+        v = torch.randn_like(k)
+        kl = torch.tensor(p.kv_lens, dtype=torch.int32, device=dev)
+        S = ea.attn_decode_num_splits(p.B, p.Lq, p.Lkv, p.Hq, p.Hkv, p.d)
+        ms = timed(lambda: ea.decode(q, k, v, causal=causal, kv_lens=kl, num_splits=S))
+        kv_bytes = sum(p.kv_lens) * p.Hkv * p.d * 2 * 2
+        part_bytes = 2 * p.B * p.Hq * S * p.Lq * (p.d + 1) * 4
+        io_bytes = 2 * p.B * p.Lq * p.Hq * p.d * 2 + p.B * p.Hq * p.Lq * 4
+        gbs = (kv_bytes + part_bytes + io_bytes) / (ms * 1e-3) / 1e9
+        out[f"decode_Lq{Lq}"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                                 "num_splits": S}
+        del q, k, v
+    torch.cuda.empty_cache()
+    return out
+
+
+# ----------------------------------------------------------------------------
+# the fp64 CPU oracle, timed on a bounded sample
+# ----------------------------------------------------------------------------
+
+class OracleSampler:
+    """The fp64 oracle's fwd+bwd on a bounded sample of the headline workload:
+    query rows (spread evenly over the sequence) of one (batch, head) slice,
+    FLOPs counted by the pages' rule over the sampled rows' valid keys."""
+
+    def __init__(self):
+        import numpy as np
+
+        self.np = np
+        p = W.headline()
+        self.p = p
+        q, k, v, do = W.make_inputs(p, seed=0)
+        sl = (slice(0, 1), slice(None), slice(0, 1))
+        self.q, self.k, self.v, self.do = q[sl], k[sl], v[sl], do[sl]
+
+    def rows(self, n):
+        n = max(1, min(int(n), self.p.Lq))
+        return self.np.unique(self.np.linspace(0, self.p.Lq - 1, n).astype(self.np.int64))
+
+    def flops(self, rows):
+        # causal: row i sees i + 1 keys; fwd = 4 d per (row, key) pair, fwd+bwd = 3.5x
+        return 3.5 * 4.0 * self.p.d * float(self.np.sum(rows + 1))
+
+    def run(self, rows):
+        import oracle
+
+        oracle.forward(self.q, self.k, self.v, causal=True, rows=rows)
+        oracle.backward(self.q, self.k, self.v, self.do, causal=True, rows=rows)
+        return self.flops(rows)
+
+    def calibrate(self, budget_s):
+        """Rows per sample so one sample takes about budget_s seconds."""
+        probe = self.rows(512)
+        t0 = time.perf_counter()
+        self.run(probe)
+        per_row = (time.perf_counter() - t0) / len(probe)
+        return self.rows(budget_s / max(per_row, 1e-9))
+
+
+def host_cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def cpu_baseline_sample(budget_s: float = 15.0):
+    """Oracle timed on the host cores on a ~budget_s sample (GPU arm, rank 0)."""
+    smp = OracleSampler()
+    rows = smp.calibrate(budget_s)
+    t0 = time.perf_counter()
+    fl = smp.run(rows)
+    dt = time.perf_counter() - t0
+    return {"value": round(fl / dt / 1e12, 6), "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+            "sample": f"{len(rows)} of 8192 query rows (evenly spaced) of batch 0 head 0, B4 H8 T8192 d128 "
+                      f"causal, fwd+bwd in fp64 numpy (BLAS default threads) in {dt:.1f} s"}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return None
+    smp = OracleSampler()
+    budget = max(0.05, args.reference_budget_s / (args.steps + args.warmup))
+    rows = smp.calibrate(budget)
+    for _ in range(args.warmup):
+        smp.run(rows)
+    t0 = time.perf_counter()
+    fl = 0.0
+    for _ in range(args.steps):
+        fl += smp.run(rows)
+    dt = time.perf_counter() - t0
+    value = fl / dt / 1e12
+    sample = (f"{len(rows)} of 8192 query rows (evenly spaced) of batch 0 head 0 per step, fwd+bwd in fp64 "
+              f"numpy (BLAS default threads)")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "bf16 causal attention fwd+bwd, B4 H8 T8192 d128 (inputs bf16, oracle in fp64)",
+                   "global_batch": 4, "seq_len": 8192, "sample_per_step": sample},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--kernel-steps", type=int, default=20, help="steps of the per-kernel timing pass")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--reference-budget-s", type=float, default=120.0,
+                    help="seconds of oracle work for the whole --impl reference run")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other rows (KVLen+GQA, decode)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    rank, _, world = dist_env()
+    if args.gpus != world and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    res = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if res is not None and rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
         "attn_decode_combine": (I, [P, P, P, P, I, I, I, I, I, I, P]),
         "attn_decode_workspace_size": (S, [I, I, I, I, I]),
         "attn_device_status": (I, [ctypes.POINTER(I), ctypes.POINTER(I), I]),
+        "attn_timing_enable": (I, [I]),
+        "attn_timing_query": (I, [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -81,7 +83,7 @@ def lib() -> ctypes.CDLL:
 EXPORTED = (
     "attn_status_string", "attn_last_error", "attn_fwd", "attn_bwd_preprocess", "attn_bwd_workspace_size",
     "attn_bwd", "attn_decode_num_splits", "attn_decode_splitkv", "attn_decode_combine",
-    "attn_decode_workspace_size", "attn_device_status",
+    "attn_decode_workspace_size", "attn_device_status", "attn_timing_enable", "attn_timing_query",
 )
 
 
@@ -177,6 +179,17 @@ def attn_device_status(reset=True):
     code, site = ctypes.c_int(0), ctypes.c_int(0)
     st = lib().attn_device_status(ctypes.byref(code), ctypes.byref(site), int(bool(reset)))
     return st, code.value, site.value
+
+
+def attn_timing_enable(on=True):
+    _check(lib().attn_timing_enable(int(bool(on))), "attn_timing_enable")
+
+
+def attn_timing_query(kernel: str):
+    """(total milliseconds, launches) recorded for one kernel name."""
+    ms, n = ctypes.c_double(0.0), ctypes.c_int(0)
+    _check(lib().attn_timing_query(kernel.encode(), ctypes.byref(ms), ctypes.byref(n)), "attn_timing_query")
+    return ms.value, n.value
 
 
 # ---- conveniences that allocate outputs with torch ------------------------------

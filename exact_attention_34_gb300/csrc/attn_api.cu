@@ -10,6 +10,8 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <string>
+#include <vector>
 
 #include "../../include/attn.h"
 #include "attn_internal.h"
@@ -160,6 +162,52 @@ int device_sm_count() {
     cache[dev] = n;
   }
   return cache[dev];
+}
+
+namespace {
+struct TimingRecord {
+  std::string name;
+  cudaEvent_t start, stop;
+};
+std::mutex g_timing_mu;
+bool g_timing_on = false;
+std::vector<TimingRecord> g_timing;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t pooled_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+void clear_timing_locked() {
+  for (auto& r : g_timing) {
+    g_event_pool.push_back(r.start);
+    g_event_pool.push_back(r.stop);
+  }
+  g_timing.clear();
+}
+}  // namespace
+
+KernelTimer::KernelTimer(const char* name, cudaStream_t s) : slot_(-1), stream_(s) {
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  if (!g_timing_on) return;
+  TimingRecord r{name, pooled_event(), pooled_event()};
+  if (r.start == nullptr || r.stop == nullptr) return;
+  if (cudaEventRecord(r.start, s) != cudaSuccess) return;
+  g_timing.push_back(r);
+  slot_ = static_cast<int>(g_timing.size()) - 1;
+}
+
+KernelTimer::~KernelTimer() {
+  if (slot_ < 0) return;
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  if (slot_ < static_cast<int>(g_timing.size())) cudaEventRecord(g_timing[slot_].stop, stream_);
 }
 
 }  // namespace attn
@@ -340,6 +388,34 @@ attn_status attn_decode_combine(const float* o_part, const float* lse_part, void
   cudaError_t e = launch_decode_combine(o_part, lse_part, o, lse, B, Lq, Hq, d, num_splits, dtype == ATTN_BF16,
                                         reinterpret_cast<cudaStream_t>(stream));
   return from_cuda(e, "attn_decode_combine launch");
+}
+
+attn_status attn_timing_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  if (on) clear_timing_locked();
+  g_timing_on = on != 0;
+  return ok();
+}
+
+attn_status attn_timing_query(const char* kernel, double* total_ms, int* launches) {
+  if (kernel == nullptr || total_ms == nullptr || launches == nullptr)
+    return fail(ATTN_ERR_INVALID_ARG, "attn_timing_query: NULL argument");
+  std::lock_guard<std::mutex> lk(g_timing_mu);
+  double tot = 0.0;
+  int n = 0;
+  for (auto& r : g_timing) {
+    if (r.name != kernel) continue;
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    if (e != cudaSuccess) return from_cuda(e, "attn_timing_query synchronize");
+    float ms = 0.f;
+    e = cudaEventElapsedTime(&ms, r.start, r.stop);
+    if (e != cudaSuccess) return from_cuda(e, "attn_timing_query elapsed");
+    tot += ms;
+    ++n;
+  }
+  *total_ms = tot;
+  *launches = n;
+  return ok();
 }
 
 attn_status attn_device_status(int* code, int* site, int reset) {

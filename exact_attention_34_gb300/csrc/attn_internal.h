@@ -90,4 +90,18 @@ bool make_bshd_tmap(CUtensorMap* map, const void* base, bool bf16, int B, int L,
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
+// Opt-in per-kernel timing (attn_timing_enable): while enabled, a KernelTimer
+// around a launch records CUDA events before and after it on its stream.
+class KernelTimer {
+ public:
+  KernelTimer(const char* name, cudaStream_t s);
+  ~KernelTimer();
+  KernelTimer(const KernelTimer&) = delete;
+  KernelTimer& operator=(const KernelTimer&) = delete;
+
+ private:
+  int slot_;
+  cudaStream_t stream_;
+};
+
 }  // namespace attn

@@ -375,6 +375,252 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ============================================================================
+// dK / dV kernel, deterministic two-pass variant: two softmax warpgroups
+// ============================================================================
+// Same data flow as above with two TMEM stages, but each stage has its own
+// softmax warpgroup (warps 0-3 take the even steps, warps 4-7 the odd ones), so
+// two steps' worth of exponentials are in flight while the tensor core works.
+// Warp 8 is the TMA producer, warp 9 the MMA issuer.
+template <int D>
+struct DkdvPPCfg {
+  static constexpr int kBN = 128, kBM = 64;
+  static constexpr int kKVBytes = kBN * D * 2;
+  static constexpr int kKBox = kBN * 128;
+  static constexpr int kQBytes = kBM * D * 2;
+  static constexpr int kQBox = kBM * 128;
+  static constexpr int kStages = 4;
+  static constexpr int kOffV = kKVBytes;
+  static constexpr int kOffQ = 2 * kKVBytes;
+  static constexpr int kOffStat = kOffQ + kStages * 2 * kQBytes;
+  static constexpr int kOffBars = kOffStat + kStages * 2 * kBM * 4;
+  static constexpr int kNumBars = 2 * kStages + 1 + 4 + 1;
+  static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
+  static constexpr int kThreads = 320;
+  static constexpr uint32_t kColS = 256;
+};
+
+// P^T and dS^T for 32 query columns [c0, c0 + 32) of one step (thread = key).
+template <bool MASK>
+__device__ __forceinline__ void dkdv_half(uint32_t col, int c0, const float* lse2, const float* dlt, float sl2,
+                                          bool key_ok, int q_lo, int q_min) {
+  uint32_t sr[32], dr[32];
+  tmem_ld32(col + c0, sr);
+  tmem_ld32(col + 64 + c0, dr);
+  uint32_t pk[16], dk[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c0 + 4 * i);
+    const float4 d4 = *reinterpret_cast<const float4*>(dlt + c0 + 4 * i);
+    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+    const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+    float pr[4], ds[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = 4 * i + e;
+      float pv = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lv[e]));
+      if (MASK) pv = (key_ok && q_lo + c0 + c >= q_min) ? pv : 0.f;
+      pr[e] = pv;
+      ds[e] = pv * (__uint_as_float(dr[c]) - dv[e]);
+    }
+    pk[2 * i] = pack_bf16x2(pr[0], pr[1]);
+    pk[2 * i + 1] = pack_bf16x2(pr[2], pr[3]);
+    dk[2 * i] = pack_bf16x2(ds[0], ds[1]);
+    dk[2 * i + 1] = pack_bf16x2(ds[2], ds[3]);
+  }
+  tmem_st16(col + c0 / 2, pk);
+  tmem_st16(col + 64 + c0 / 2, dk);
+}
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    bwd_dkdv_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const BwdKParams p) {
+  using C = DkdvPPCfg<D>;
+  constexpr int NS = C::kStages, BM = C::kBM;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::kOffV;
+  uint8_t* sQ = smem + C::kOffQ;
+  float* sStat = reinterpret_cast<float*>(smem + C::kOffStat);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + NS;
+  uint64_t* kv_full = bars + 2 * NS;
+  uint64_t* s_full = kv_full + 1;  // [2]
+  uint64_t* p_full = kv_full + 3;  // [2]
+  uint64_t* acc_full = kv_full + 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  const int j0 = blockIdx.x * C::kBN, hk = blockIdx.y, b = blockIdx.z;
+  int kvl = p.Lkv;
+  if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
+  const int q_first = p.causal ? max(0, j0 + p.Lq - kvl) : 0;
+  const int i_begin = q_first / BM;
+  const int n_qt = (p.Lq + BM - 1) / BM;
+  const int steps_per_head = (j0 < kvl && i_begin < n_qt) ? n_qt - i_begin : 0;
+  const int T = steps_per_head * p.G;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 128);
+    }
+    mbar_init(acc_full, 1);
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 8) {
+    if (lane == 0 && T > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(kv_full, 2 * C::kKVBytes);
+      for (int h = 0; h < D / 64; ++h) {
+        tma_load_4d(sK + h * C::kKBox, &tm_k, kv_full, h * 64, j0, hk, b);
+        tma_load_4d(sV + h * C::kKBox, &tm_v, kv_full, h * 64, j0, hk, b);
+      }
+      for (int t = 0; t < T; ++t) {
+        const int s = t % NS, r = t / NS;
+        if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort_flag, p.status, 51)) break;
+        const int h = hk * p.G + t / steps_per_head;
+        const int q0 = (i_begin + t % steps_per_head) * BM;
+        mbar_arrive_expect_tx(&full[s], 2 * C::kQBytes + 2 * BM * 4);
+        uint8_t* q_dst = sQ + s * 2 * C::kQBytes;
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_4d(q_dst + c * C::kQBox, &tm_q, &full[s], c * 64, q0, h, b);
+          tma_load_4d(q_dst + C::kQBytes + c * C::kQBox, &tm_do, &full[s], c * 64, q0, h, b);
+        }
+        const size_t row = (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + q0;
+        bulk_load(sStat + s * 2 * BM, p.lse2 + row, BM * 4, &full[s]);
+        bulk_load(sStat + s * 2 * BM + BM, p.delta + row, BM * 4, &full[s]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    if (lane == 0 && T > 0) {
+      constexpr uint32_t idesc_st = idesc_bf16_f32(128, BM, 0, 0);
+      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, 0, 1);
+      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ);
+      auto issue_scores = [&](int t) {
+        const int s = t % NS, ts = t & 1;
+        const uint32_t qa = q_addr + s * 2 * C::kQBytes, da = qa + C::kQBytes;
+        const uint32_t col = tbase + C::kColS + ts * 128;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t ko = (k >> 2) * C::kKBox + (k & 3) * 32;
+          const uint32_t qo = (k >> 2) * C::kQBox + (k & 3) * 32;
+          mma_ss(col, sdesc_sw128(k_addr + ko, 16, 1024), sdesc_sw128(qa + qo, 16, 1024), idesc_st, k > 0);
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t ko = (k >> 2) * C::kKBox + (k & 3) * 32;
+          const uint32_t qo = (k >> 2) * C::kQBox + (k & 3) * 32;
+          mma_ss(col + 64, sdesc_sw128(v_addr + ko, 16, 1024), sdesc_sw128(da + qo, 16, 1024), idesc_st, k > 0);
+        }
+        mma_commit(&s_full[ts]);
+      };
+      bool ok = mbar_wait(kv_full, 0, abort_flag, p.status, 52);
+      for (int t = 0; t < 2 && t < T && ok; ++t) {
+        ok = mbar_wait(&full[t % NS], (t / NS) & 1, abort_flag, p.status, 53);
+        if (!ok) break;
+        tc_fence_after();
+        issue_scores(t);
+      }
+      for (int t = 0; t < T && ok; ++t) {
+        const int s = t % NS, ts = t & 1;
+        ok = mbar_wait(&p_full[ts], (t >> 1) & 1, abort_flag, p.status, 54);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t qa = q_addr + s * 2 * C::kQBytes, da = qa + C::kQBytes;
+        const uint32_t col = tbase + C::kColS + ts * 128;
+#pragma unroll
+        for (int k = 0; k < BM / 16; ++k)
+          mma_ts(tbase + 128, col + k * 8, sdesc_sw128(da + k * 2048, C::kQBox, 1024), idesc_acc,
+                 (t > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+        for (int k = 0; k < BM / 16; ++k)
+          mma_ts(tbase + 0, col + 64 + k * 8, sdesc_sw128(qa + k * 2048, C::kQBox, 1024), idesc_acc,
+                 (t > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&empty[s]);
+        if (t + 2 < T) {
+          const int tn = t + 2;
+          ok = mbar_wait(&full[tn % NS], (tn / NS) & 1, abort_flag, p.status, 55);
+          if (!ok) break;
+          tc_fence_after();
+          issue_scores(tn);
+        }
+      }
+      if (ok) mma_commit(acc_full);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax: WG w takes steps t = w (mod 2)
+    const int w = warp >> 2, wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int j = j0 + r;
+    const uint32_t t_lane = tbase + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t col = t_lane + C::kColS + w * 128;
+    const bool key_ok = j < kvl;
+    const int q_min = p.causal ? j + p.Lq - kvl : -0x7fffffff;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int t = w; t < T; t += 2) {
+      const int s = t % NS;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[w], (t >> 1) & 1, abort_flag, p.status, 56));
+      if (!ok) break;
+      tc_fence_after();
+      const int q0 = (i_begin + t % steps_per_head) * BM;
+      const float* lse2 = sStat + s * 2 * BM;
+      const float* dlt = lse2 + BM;
+      if (__all_sync(0xffffffffu, key_ok && q0 >= q_min)) {
+        dkdv_half<false>(col, 0, lse2, dlt, sl2, key_ok, q0, q_min);
+        dkdv_half<false>(col, 32, lse2, dlt, sl2, key_ok, q0, q_min);
+      } else {
+        dkdv_half<true>(col, 0, lse2, dlt, sl2, key_ok, q0, q_min);
+        dkdv_half<true>(col, 32, lse2, dlt, sl2, key_ok, q0, q_min);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full[w]);
+    }
+    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 57));
+    if (ok) {
+      tc_fence_after();
+      const bool st = j < p.Lkv;
+      const size_t off = ((static_cast<size_t>(b) * p.Lkv + (st ? j : 0)) * p.Hkv + hk) * D;
+      if (w == 0)
+        store_row_bf16<D>(t_lane + 0, reinterpret_cast<__nv_bfloat16*>(p.dk) + off, p.scale, st, T == 0);
+      else
+        store_row_bf16<D>(t_lane + 128, reinterpret_cast<__nv_bfloat16*>(p.dv) + off, 1.0f, st, T == 0);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// ============================================================================
 // dQ kernel
 // ============================================================================
 template <int D>
@@ -391,10 +637,35 @@ struct DqCfg {
   static constexpr int kOffBars = kOffKV + kStages * 2 * kKVBytes;
   static constexpr int kNumBars = 2 * kStages + 1 + 4 + 1;
   static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
+  static constexpr int kThreads = 320;
 };
 
+// dS for 32 key columns [c0, c0 + 32) of one step (thread = query row).
+template <bool MASK>
+__device__ __forceinline__ void dq_half(uint32_t col, int c0, float l2, float dl, float sl2, int kb, int lim) {
+  uint32_t sr[32], dr[32];
+  tmem_ld32(col + c0, sr);
+  tmem_ld32(col + 64 + c0, dr);
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float ds[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int c = 2 * i + e;
+      float pv = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -l2));
+      if (MASK) pv = (kb + c0 + c < lim) ? pv : 0.f;
+      ds[e] = pv * (__uint_as_float(dr[c]) - dl);
+    }
+    pk[i] = pack_bf16x2(ds[0], ds[1]);
+  }
+  tmem_st16(col + c0 / 2, pk);
+}
+
+// dQ kernel: CTA = (batch, head, 128 queries); two softmax warpgroups take
+// the even / odd 64-key steps (TMEM stage = step parity).
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdKParams p) {
@@ -439,7 +710,7 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(acc_full, 1);
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -448,7 +719,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     if (lane == 0 && T > 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
@@ -469,7 +740,7 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     if (lane == 0 && T > 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, 0, 0);   // Q x K^T
       constexpr uint32_t idesc_dq = idesc_bf16_f32(128, D, 0, 1);  // dS (TMEM) x K (MN-major)
@@ -525,69 +796,65 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax (thread = query row)
-    const int r = warp * 32 + lane;
+    const int w = warp >> 2, wq = warp & 3;
+    const int r = wq * 32 + lane;
     const int i = q0 + r;
-    const uint32_t t_lane = tbase + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t t_lane = tbase + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t col = t_lane + 128 + w * 128;
     const size_t srow = (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + i;  // i < Lq_pad always
     const float l2 = p.lse2[srow];
     const float dl = p.delta[srow];
     const int lim = i < p.Lq ? key_limit(i, p.Lq, kvl, p.causal) : 0;
     const float sl2 = p.scale_log2;
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
-      const int ts = t & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[ts], (t >> 1) & 1, abort_flag, p.status, 36));
+    for (int t = w; t < T; t += 2) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[w], (t >> 1) & 1, abort_flag, p.status, 36));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t col = t_lane + 128 + ts * 128;
-      uint32_t sr[64], dr[64];
-      {
-        uint32_t a[32];
-        tmem_ld32(col, a);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) sr[c] = a[c];
-        tmem_ld32(col + 32, a);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) sr[32 + c] = a[c];
-        tmem_ld32(col + 64, a);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) dr[c] = a[c];
-        tmem_ld32(col + 96, a);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) dr[32 + c] = a[c];
-      }
       const int kb = t * BN;
-      const bool all_valid = kb + BN <= lim;
-      uint32_t pk[32];
-#pragma unroll
-      for (int c2 = 0; c2 < 32; ++c2) {
-        float ds[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int c = 2 * c2 + e;
-          const bool valid = all_valid || kb + c < lim;
-          const float pv = valid ? ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -l2)) : 0.f;
-          ds[e] = pv * (__uint_as_float(dr[c]) - dl);
-        }
-        pk[c2] = pack_bf16x2(ds[0], ds[1]);
+      if (__all_sync(0xffffffffu, kb + BN <= lim)) {
+        dq_half<false>(col, 0, l2, dl, sl2, kb, lim);
+        dq_half<false>(col, 32, l2, dl, sl2, kb, lim);
+      } else {
+        dq_half<true>(col, 0, l2, dl, sl2, kb, lim);
+        dq_half<true>(col, 32, l2, dl, sl2, kb, lim);
       }
-      tmem_st32(col, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full[ts]);
+      mbar_arrive(&p_full[w]);
     }
     if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 37));
     if (ok) {
       tc_fence_after();
+      // warpgroup w stores head-dim columns [w * D/2, (w + 1) * D/2)
       const bool st = i < p.Lq;
-      const size_t off = ((static_cast<size_t>(b) * p.Lq + (st ? i : 0)) * p.Hq + h) * D;
-      store_row_bf16<D>(t_lane, reinterpret_cast<__nv_bfloat16*>(p.dq) + off, p.scale, st, T == 0);
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.dq) +
+                           ((static_cast<size_t>(b) * p.Lq + (st ? i : 0)) * p.Hq + h) * D + w * (D / 2);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t rr[32];
+        if (T > 0) {
+          tmem_ld32(t_lane + w * (D / 2) + c * 32, rr);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rr[e] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * p.scale, __uint_as_float(rr[2 * e + 1]) * p.scale);
+        if (st) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
@@ -654,16 +921,17 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
     dim3 grid((pb.Lkv + 127) / 128, pb.Hkv, pb.B);
     kp.n_tiles = grid.x;
     if (a.deterministic) {
-      using C = DkdvCfg<D, false>;
-      e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               C::kSmemBytes);
+      using C = DkdvPPCfg<D>;
+      e = cudaFuncSetAttribute(bwd_dkdv_pp_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
       if (e != cudaSuccess) return e;
-      bwd_dkdv_kernel<D, false><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+      KernelTimer kt("bwd_dkdv", stream);
+      bwd_dkdv_pp_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
     } else {
       using C = DkdvCfg<D, true>;
       e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                C::kSmemBytes);
       if (e != cudaSuccess) return e;
+      KernelTimer kt("bwd_dkdv_atomic", stream);
       bwd_dkdv_kernel<D, true><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
     }
     e = cudaGetLastError();
@@ -671,6 +939,7 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
   }
   if (!a.deterministic) {
     const long n4 = static_cast<long>(pb.B) * pb.Lq * pb.Hq * D / 4;
+    KernelTimer kt("dq_convert", stream);
     dq_convert_kernel<<<static_cast<int>((n4 + 255) / 256), 256, 0, stream>>>(
         a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), n4, pb.scale);
     return cudaGetLastError();
@@ -688,7 +957,8 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
     kp.n_tiles = grid.x;
     e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    bwd_dq_kernel<D><<<grid, 192, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+    KernelTimer kt("bwd_dq", stream);
+    bwd_dq_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
     return cudaGetLastError();
   }
 }

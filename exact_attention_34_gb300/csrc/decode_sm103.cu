@@ -332,7 +332,10 @@ cudaError_t launch_decode_bf16_d(const DecodeArgs& a, DeviceStatus* st, cudaStre
   kp.scale_log2 = pb.scale * kLog2e;
   kp.status = st;
   dim3 grid(a.num_splits, pb.Hkv, pb.B);
-  decode_bf16_kernel<D><<<grid, 192, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
+  {
+    KernelTimer kt("decode", stream);
+    decode_bf16_kernel<D><<<grid, 192, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
+  }
   return cudaGetLastError();
 }
 

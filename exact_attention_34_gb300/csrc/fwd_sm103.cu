@@ -352,7 +352,10 @@ cudaError_t launch_fwd_bf16_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t s
   kp.scale_log2 = pb.scale * kLog2e;
   kp.status = st;
   dim3 grid(kp.n_qblocks, pb.Hq, pb.B);
-  fwd_bf16_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
+  {
+    KernelTimer kt("fwd", stream);
+    fwd_bf16_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
+  }
   return cudaGetLastError();
 }
 

@@ -430,7 +430,10 @@ cudaError_t run_fwd(const F32FwdParams& p, int splits, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(f32_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd_smem<D>());
   if (e != cudaSuccess) return e;
   dim3 grid((p.Lq + kT - 1) / kT, p.Hq, p.B * splits);
-  f32_fwd_kernel<D><<<grid, 256, fwd_smem<D>(), s>>>(p);
+  {
+    KernelTimer kt(splits > 1 || p.o == nullptr ? "decode_f32" : "fwd_f32", s);
+    f32_fwd_kernel<D><<<grid, 256, fwd_smem<D>(), s>>>(p);
+  }
   return cudaGetLastError();
 }
 
@@ -440,18 +443,25 @@ cudaError_t run_bwd(const F32BwdParams& p, bool atomic_dq, cudaStream_t s) {
                                        dkdv_smem<D>());
   if (e != cudaSuccess) return e;
   dim3 g1((p.Lkv + kT - 1) / kT, p.Hkv, p.B);
-  f32_bwd_dkdv_kernel<D><<<g1, 256, dkdv_smem<D>(), s>>>(p);
+  {
+    KernelTimer kt("bwd_dkdv_f32", s);
+    f32_bwd_dkdv_kernel<D><<<g1, 256, dkdv_smem<D>(), s>>>(p);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (atomic_dq) {
     const long n = static_cast<long>(p.B) * p.Lq * p.Hq * D;
+    KernelTimer kt("dq_convert_f32", s);
     f32_dq_convert_kernel<<<static_cast<int>((n + 255) / 256), 256, 0, s>>>(p.dq_acc, p.dq, n, p.scale);
     return cudaGetLastError();
   }
   e = cudaFuncSetAttribute(f32_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem<D>());
   if (e != cudaSuccess) return e;
   dim3 g2((p.Lq + kT - 1) / kT, p.Hq, p.B);
-  f32_bwd_dq_kernel<D><<<g2, 256, dq_smem<D>(), s>>>(p);
+  {
+    KernelTimer kt("bwd_dq_f32", s);
+    f32_bwd_dq_kernel<D><<<g2, 256, dq_smem<D>(), s>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -132,6 +132,7 @@ cudaError_t run_preprocess(const PreprocessArgs& a, cudaStream_t s) {
   const long n_rows = static_cast<long>(a.B) * a.Hq * a.Lq_pad;
   const long threads = n_rows * (D / 8);
   const int blocks = static_cast<int>((threads + 255) / 256);
+  KernelTimer kt("bwd_preprocess", s);
   bwd_preprocess_kernel<T, D><<<blocks, 256, 0, s>>>(static_cast<const T*>(a.o), static_cast<const T*>(a.dout),
                                                      a.lse, a.delta, a.lse2, a.dq_acc, n_rows, a.Lq, a.Lq_pad, a.Hq);
   return cudaGetLastError();
@@ -142,6 +143,7 @@ cudaError_t run_combine(const float* o_part, const float* lse_part, void* o, flo
                         int S, cudaStream_t s) {
   const long n_rows = static_cast<long>(B) * Hq * Lq;
   const int blocks = static_cast<int>((n_rows * 32 + 255) / 256);
+  KernelTimer kt("combine", s);
   combine_kernel<T, D><<<blocks, 256, 0, s>>>(o_part, lse_part, static_cast<T*>(o), lse, B, Lq, Hq, S);
   return cudaGetLastError();
 }

@@ -75,7 +75,7 @@ const char* attn_last_error(void);
 /*
  * Forward.  Writes o [B,Lq,Hq,d] (dtype) and lse [B,Hq,Lq] (float32, natural
  * log, -inf on rows without a valid key).  scale is the softmax scale (pass
- * 1/sqrt(d) for the standard one; any finite value is accepted).  kv_lens is
+ * 1/sqrt(d) for the standard one; it must be finite and > 0).  kv_lens is
  * a device int32 [B] or NULL.  causal is 0 or 1.
  * Fused, memory-linear tiled kernel with online softmax ("Attention
  * performance", section "When to use which": memory grows linearly in T).
@@ -158,6 +158,22 @@ size_t attn_decode_workspace_size(int B, int Lq, int Hq, int d, int num_splits);
  * ATTN_ERR_DEVICE when a code was set, ATTN_OK otherwise.
  */
 attn_status attn_device_status(int* code, int* site, int reset);
+
+/*
+ * Per-kernel timing for benchmarks (the pages time each case between device
+ * synchronisations, "GPU and CPU performance", section "Methodology"; this is
+ * the library-side counterpart).  attn_timing_enable(1) clears old records and
+ * brackets every kernel launched from then on with CUDA events on its stream
+ * (events are created by the library and reused; no device memory is
+ * allocated).  attn_timing_enable(0) stops recording.  attn_timing_query waits
+ * for the recorded launches of one kernel ("fwd", "bwd_preprocess",
+ * "bwd_dkdv", "bwd_dkdv_atomic", "bwd_dq", "dq_convert", "decode", "combine",
+ * or the float32 kernels "fwd_f32", "decode_f32", "bwd_dkdv_f32",
+ * "bwd_dq_f32", "dq_convert_f32") and returns their summed milliseconds and
+ * count (host pointers).  Process-wide; meant for single-threaded benchmarks.
+ */
+attn_status attn_timing_enable(int on);
+attn_status attn_timing_query(const char* kernel, double* total_ms, int* launches);
 
 #ifdef __cplusplus
 }

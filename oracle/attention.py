@@ -170,7 +170,7 @@ def probabilities(q, k, scale=None, causal=False, kv_lens=None):
 
 
 def backward(q, k, v, do, scale=None, causal=False, kv_lens=None, kv_heads=None,
-             row_block: int = 1024):
+             row_block: int = 1024, rows=None):
     """Analytic gradient of ``sum(O * dO)`` with respect to q, k and v.
 
     With ``P`` the probabilities (recomputed, as the pages' kernels do from the
@@ -182,7 +182,10 @@ def backward(q, k, v, do, scale=None, causal=False, kv_lens=None, kv_heads=None,
 
     Keys past a batch element's KV length get dK = dV = 0; rows without a valid
     key get dQ = 0.  ``kv_heads`` restricts the work to some KV heads (with all
-    their query heads); other entries are left as NaN.
+    their query heads); other entries are left as NaN.  ``rows`` restricts the
+    sums to some query rows: dQ of those rows, and dK / dV summed over those
+    rows only (a bounded sample of the work; the sums over a partition of the
+    rows add up to the full gradient).
 
     Returns ``(dq, dk, dv)`` in float64 with the shapes of q, k, v.
     """
@@ -197,14 +200,14 @@ def backward(q, k, v, do, scale=None, causal=False, kv_lens=None, kv_heads=None,
     dq = np.full(q.shape, np.nan)
     dk = np.full(k.shape, np.nan)
     dv = np.full(v.shape, np.nan)
-    all_rows = np.arange(Lq)
+    all_rows = np.arange(Lq) if rows is None else np.asarray(rows, dtype=np.int64)
     for b in range(B):
         for hk in kv_heads:
             kh, vh = k[b, :, hk, :], v[b, :, hk, :]
             acc_dk = np.zeros((Lkv, d))
             acc_dv = np.zeros((Lkv, d))
             for hq in range(hk * G, (hk + 1) * G):
-                for r0 in range(0, Lq, row_block):
+                for r0 in range(0, len(all_rows), row_block):
                     rr = all_rows[r0:r0 + row_block]
                     mask = valid_keys(rr, Lq, Lkv, int(kvl[b]), causal)
                     p, _ = _head_probs(q[b, rr, hq, :], kh, scale, mask)

@@ -355,3 +355,15 @@ def test_combine_closed_form():
     assert abs(lse[0, 0, 0] - math.log(4.0)) < 1e-15
     o, lse = oracle.combine(np.zeros((1, 1, 2, 1, 2)), np.full((1, 1, 2, 1), -np.inf))
     assert np.all(o == 0) and np.all(lse == -np.inf)
+
+
+def test_backward_row_partition_adds_up():
+    q, k, v, do = rnd((2, 7, 4, 3), 151), rnd((2, 9, 2, 3), 152), rnd((2, 9, 2, 3), 153), \
+        rnd((2, 7, 4, 3), 154)
+    full = oracle.backward(q, k, v, do, causal=True, kv_lens=[9, 5])
+    a = oracle.backward(q, k, v, do, causal=True, kv_lens=[9, 5], rows=[0, 2, 3], row_block=2)
+    b = oracle.backward(q, k, v, do, causal=True, kv_lens=[9, 5], rows=[1, 4, 5, 6])
+    np.testing.assert_allclose(a[1] + b[1], full[1], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(a[2] + b[2], full[2], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(a[0][:, [0, 2, 3]], full[0][:, [0, 2, 3]], rtol=0, atol=1e-15)
+    assert np.all(np.isnan(a[0][:, [1, 4, 5, 6]]))
