@@ -375,37 +375,42 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ============================================================================
-// dK / dV kernel, deterministic two-pass variant: two softmax warpgroups
+// dK / dV kernel, deterministic two-pass variant
 // ============================================================================
-// Same data flow as above with two TMEM stages, but each stage has its own
-// softmax warpgroup (warps 0-3 take the even steps, warps 4-7 the odd ones), so
-// two steps' worth of exponentials are in flight while the tensor core works.
-// Warp 8 is the TMA producer, warp 9 the MMA issuer.
+// CTA = (batch, KV head, 128 keys); thread = key row = TMEM lane.  Each step
+// takes 128 queries so every tcgen05.mma is 128 x 128 (64-wide operands run
+// the tensor core at two thirds of its rate or less).  TMEM then holds one
+// stage: dK [0,128) dV [128,256) S^T [256,384) dP^T [384,512).  The step is
+// overlapped in two halves of 64 queries: both softmax warpgroups convert
+// half 0 (warpgroup w takes 32 of its columns), signal, and convert half 1
+// while the MMA warp already accumulates dV += P^T dO and dK += dS^T Q for
+// half 0.  Each warpgroup writes its bf16 P^T / dS^T over the first 16 of
+// the 32 fp32 columns it read, so no warpgroup overwrites columns another one
+// still reads.  Warp 8 is the TMA producer, warp 9 the MMA issuer.
 template <int D>
-struct DkdvPPCfg {
-  static constexpr int kBN = 128, kBM = 64;
+struct DkdvCfg2 {
+  static constexpr int kBN = 128, kBM = 128;
   static constexpr int kKVBytes = kBN * D * 2;
-  static constexpr int kKBox = kBN * 128;
+  static constexpr int kBox = 128 * 128;      // one 64-column box of a 128-row tile
   static constexpr int kQBytes = kBM * D * 2;
-  static constexpr int kQBox = kBM * 128;
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 2;
   static constexpr int kOffV = kKVBytes;
-  static constexpr int kOffQ = 2 * kKVBytes;
+  static constexpr int kOffQ = 2 * kKVBytes;  // stage s: Q at s * 2 * kQBytes, dO right after
   static constexpr int kOffStat = kOffQ + kStages * 2 * kQBytes;
   static constexpr int kOffBars = kOffStat + kStages * 2 * kBM * 4;
-  static constexpr int kNumBars = 2 * kStages + 1 + 4 + 1;
+  static constexpr int kNumBars = 2 * kStages + 1 + 1 + 2 + 1;
   static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
   static constexpr int kThreads = 320;
-  static constexpr uint32_t kColS = 256;
 };
 
-// P^T and dS^T for 32 query columns [c0, c0 + 32) of one step (thread = key).
+// P^T and dS^T for the 32 query columns [c0, c0 + 32) of the step (thread =
+// key).  S^T is at s_col, dP^T at s_col + 128; the packed bf16 results go to
+// the first 16 of the 32 columns that were read (query pair c -> column c).
 template <bool MASK>
-__device__ __forceinline__ void dkdv_half(uint32_t col, int c0, const float* lse2, const float* dlt, float sl2,
-                                          bool key_ok, int q_lo, int q_min) {
+__device__ __forceinline__ void dkdv_cols32(uint32_t s_col, int c0, const float* lse2, const float* dlt, float sl2,
+                                            bool key_ok, int q_lo, int q_min) {
   uint32_t sr[32], dr[32];
-  tmem_ld32(col + c0, sr);
-  tmem_ld32(col + 64 + c0, dr);
+  tmem_ld32_pair(s_col + c0, s_col + 128 + c0, sr, dr);
   uint32_t pk[16], dk[16];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -427,17 +432,18 @@ __device__ __forceinline__ void dkdv_half(uint32_t col, int c0, const float* lse
     dk[2 * i] = pack_bf16x2(ds[0], ds[1]);
     dk[2 * i + 1] = pack_bf16x2(ds[2], ds[3]);
   }
-  tmem_st16(col + c0 / 2, pk);
-  tmem_st16(col + 64 + c0 / 2, dk);
+  tmem_st16(s_col + c0, pk);
+  tmem_st16(s_col + 128 + c0, dk);
 }
 
 template <int D>
 __global__ void __launch_bounds__(320, 1)
-    bwd_dkdv_pp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                       const BwdKParams p) {
-  using C = DkdvPPCfg<D>;
+    bwd_dkdv_kernel2(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const BwdKParams p) {
+  using C = DkdvCfg2<D>;
   constexpr int NS = C::kStages, BM = C::kBM;
+  constexpr uint32_t kColS = 256;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sK = smem;
@@ -448,9 +454,9 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* full = bars;
   uint64_t* empty = bars + NS;
   uint64_t* kv_full = bars + 2 * NS;
-  uint64_t* s_full = kv_full + 1;  // [2]
-  uint64_t* p_full = kv_full + 3;  // [2]
-  uint64_t* acc_full = kv_full + 5;
+  uint64_t* s_full = kv_full + 1;
+  uint64_t* p_half = kv_full + 2;  // [2]
+  uint64_t* acc_full = kv_full + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -471,10 +477,9 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(kv_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 128);
-    }
+    mbar_init(s_full, 1);
+    mbar_init(&p_half[0], 256);
+    mbar_init(&p_half[1], 256);
     mbar_init(acc_full, 1);
     fence_barrier_init();
   }
@@ -493,19 +498,19 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(kv_full, 2 * C::kKVBytes);
       for (int h = 0; h < D / 64; ++h) {
-        tma_load_4d(sK + h * C::kKBox, &tm_k, kv_full, h * 64, j0, hk, b);
-        tma_load_4d(sV + h * C::kKBox, &tm_v, kv_full, h * 64, j0, hk, b);
+        tma_load_4d(sK + h * C::kBox, &tm_k, kv_full, h * 64, j0, hk, b);
+        tma_load_4d(sV + h * C::kBox, &tm_v, kv_full, h * 64, j0, hk, b);
       }
       for (int t = 0; t < T; ++t) {
         const int s = t % NS, r = t / NS;
-        if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort_flag, p.status, 51)) break;
+        if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort_flag, p.status, 61)) break;
         const int h = hk * p.G + t / steps_per_head;
         const int q0 = (i_begin + t % steps_per_head) * BM;
         mbar_arrive_expect_tx(&full[s], 2 * C::kQBytes + 2 * BM * 4);
         uint8_t* q_dst = sQ + s * 2 * C::kQBytes;
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(q_dst + c * C::kQBox, &tm_q, &full[s], c * 64, q0, h, b);
-          tma_load_4d(q_dst + C::kQBytes + c * C::kQBox, &tm_do, &full[s], c * 64, q0, h, b);
+          tma_load_4d(q_dst + c * C::kBox, &tm_q, &full[s], c * 64, q0, h, b);
+          tma_load_4d(q_dst + C::kQBytes + c * C::kBox, &tm_do, &full[s], c * 64, q0, h, b);
         }
         const size_t row = (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + q0;
         bulk_load(sStat + s * 2 * BM, p.lse2 + row, BM * 4, &full[s]);
@@ -515,92 +520,96 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp == 9) {
     if (lane == 0 && T > 0) {
-      constexpr uint32_t idesc_st = idesc_bf16_f32(128, BM, 0, 0);
-      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, 0, 1);
+      constexpr uint32_t idesc_st = idesc_bf16_f32(128, BM, 0, 0);  // K x Q^T, V x dO^T
+      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, 0, 1);  // (P^T|dS^T from TMEM) x (dO|Q MN-major)
       const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ);
+      const uint64_t dk_base = sdesc_sw128(k_addr, 16, 1024), dv_base = sdesc_sw128(v_addr, 16, 1024);
       auto issue_scores = [&](int t) {
-        const int s = t % NS, ts = t & 1;
-        const uint32_t qa = q_addr + s * 2 * C::kQBytes, da = qa + C::kQBytes;
-        const uint32_t col = tbase + C::kColS + ts * 128;
+        const int s = t % NS;
+        const uint32_t qa = q_addr + s * 2 * C::kQBytes;
+        const uint64_t dq_base = sdesc_sw128(qa, 16, 1024), ddo_base = sdesc_sw128(qa + C::kQBytes, 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t ko = (k >> 2) * C::kKBox + (k & 3) * 32;
-          const uint32_t qo = (k >> 2) * C::kQBox + (k & 3) * 32;
-          mma_ss(col, sdesc_sw128(k_addr + ko, 16, 1024), sdesc_sw128(qa + qo, 16, 1024), idesc_st, k > 0);
+          const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
+          mma_ss(tbase + kColS, dk_base + off, dq_base + off, idesc_st, k > 0);
         }
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t ko = (k >> 2) * C::kKBox + (k & 3) * 32;
-          const uint32_t qo = (k >> 2) * C::kQBox + (k & 3) * 32;
-          mma_ss(col + 64, sdesc_sw128(v_addr + ko, 16, 1024), sdesc_sw128(da + qo, 16, 1024), idesc_st, k > 0);
+          const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
+          mma_ss(tbase + kColS + 128, dv_base + off, ddo_base + off, idesc_st, k > 0);
         }
-        mma_commit(&s_full[ts]);
+        mma_commit(s_full);
       };
-      bool ok = mbar_wait(kv_full, 0, abort_flag, p.status, 52);
-      for (int t = 0; t < 2 && t < T && ok; ++t) {
-        ok = mbar_wait(&full[t % NS], (t / NS) & 1, abort_flag, p.status, 53);
-        if (!ok) break;
+      bool ok = mbar_wait(kv_full, 0, abort_flag, p.status, 62);
+      if (ok) ok = mbar_wait(&full[0], 0, abort_flag, p.status, 63);
+      if (ok) {
         tc_fence_after();
-        issue_scores(t);
+        issue_scores(0);
       }
       for (int t = 0; t < T && ok; ++t) {
-        const int s = t % NS, ts = t & 1;
-        ok = mbar_wait(&p_full[ts], (t >> 1) & 1, abort_flag, p.status, 54);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t qa = q_addr + s * 2 * C::kQBytes, da = qa + C::kQBytes;
-        const uint32_t col = tbase + C::kColS + ts * 128;
+        const int s = t % NS;
+        const uint32_t qa = q_addr + s * 2 * C::kQBytes;
+        const uint64_t bq = sdesc_sw128(qa, C::kBox, 1024), bdo = sdesc_sw128(qa + C::kQBytes, C::kBox, 1024);
 #pragma unroll
-        for (int k = 0; k < BM / 16; ++k)
-          mma_ts(tbase + 128, col + k * 8, sdesc_sw128(da + k * 2048, C::kQBox, 1024), idesc_acc,
-                 (t > 0 || k > 0) ? 1u : 0u);
-#pragma unroll
-        for (int k = 0; k < BM / 16; ++k)
-          mma_ts(tbase + 0, col + 64 + k * 8, sdesc_sw128(qa + k * 2048, C::kQBox, 1024), idesc_acc,
-                 (t > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&empty[s]);
-        if (t + 2 < T) {
-          const int tn = t + 2;
-          ok = mbar_wait(&full[tn % NS], (tn / NS) & 1, abort_flag, p.status, 55);
+        for (int h = 0; h < 2; ++h) {
+          ok = mbar_wait(&p_half[h], t & 1, abort_flag, p.status, 64 + h);
           if (!ok) break;
           tc_fence_after();
-          issue_scores(tn);
+          // query k-steps 4h .. 4h+3; warpgroup w packed queries [64h + 32w, +32) into
+          // columns [64h + 32w, +16) of S^T (P^T) and dP^T (dS^T)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t acol = kColS + 64 * h + 32 * (k >> 1) + 8 * (k & 1);
+            const uint32_t boff = ((64 * h + 16 * k) * 128) >> 4;
+            const uint32_t acc = (t > 0 || h > 0 || k > 0) ? 1u : 0u;
+            mma_ts(tbase + 128, tbase + acol, bdo + boff, idesc_acc, acc);        // dV += P^T dO
+            mma_ts(tbase + 0, tbase + acol + 128, bq + boff, idesc_acc, acc);     // dK += dS^T Q
+          }
+        }
+        if (!ok) break;
+        mma_commit(&empty[s]);
+        if (t + 1 < T) {
+          ok = mbar_wait(&full[(t + 1) % NS], ((t + 1) / NS) & 1, abort_flag, p.status, 66);
+          if (!ok) break;
+          tc_fence_after();
+          issue_scores(t + 1);
         }
       }
       if (ok) mma_commit(acc_full);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax: WG w takes steps t = w (mod 2)
+    // ------------------------------------------------------------ softmax (thread = key row)
     const int w = warp >> 2, wq = warp & 3;
     const int r = wq * 32 + lane;
     const int j = j0 + r;
     const uint32_t t_lane = tbase + (static_cast<uint32_t>(wq * 32) << 16);
-    const uint32_t col = t_lane + C::kColS + w * 128;
+    const uint32_t s_col = t_lane + kColS;
     const bool key_ok = j < kvl;
     const int q_min = p.causal ? j + p.Lq - kvl : -0x7fffffff;
     const float sl2 = p.scale_log2;
     bool ok = true;
-    for (int t = w; t < T; t += 2) {
+    for (int t = 0; t < T; ++t) {
       const int s = t % NS;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[w], (t >> 1) & 1, abort_flag, p.status, 56));
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full, t & 1, abort_flag, p.status, 67));
       if (!ok) break;
       tc_fence_after();
       const int q0 = (i_begin + t % steps_per_head) * BM;
       const float* lse2 = sStat + s * 2 * BM;
       const float* dlt = lse2 + BM;
-      if (__all_sync(0xffffffffu, key_ok && q0 >= q_min)) {
-        dkdv_half<false>(col, 0, lse2, dlt, sl2, key_ok, q0, q_min);
-        dkdv_half<false>(col, 32, lse2, dlt, sl2, key_ok, q0, q_min);
-      } else {
-        dkdv_half<true>(col, 0, lse2, dlt, sl2, key_ok, q0, q_min);
-        dkdv_half<true>(col, 32, lse2, dlt, sl2, key_ok, q0, q_min);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c0 = 64 * h + 32 * w;
+        if (__all_sync(0xffffffffu, key_ok && q0 + c0 >= q_min))
+          dkdv_cols32<false>(s_col, c0, lse2, dlt, sl2, key_ok, q0, q_min);
+        else
+          dkdv_cols32<true>(s_col, c0, lse2, dlt, sl2, key_ok, q0, q_min);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_half[h]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&p_full[w]);
     }
-    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 57));
+    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 68));
     if (ok) {
       tc_fence_after();
       const bool st = j < p.Lkv;
@@ -626,26 +635,25 @@ __global__ void __launch_bounds__(320, 1)
 template <int D>
 struct DqCfg {
   static constexpr int kBM = 128;               // queries per CTA
-  static constexpr int kBN = 64;                // keys per step
+  static constexpr int kBN = 128;               // keys per step
   static constexpr int kQBytes = kBM * D * 2;
-  static constexpr int kQBox = kBM * 128;
   static constexpr int kKVBytes = kBN * D * 2;
-  static constexpr int kKBox = kBN * 128;
-  static constexpr int kStages = 4;
+  static constexpr int kBox = 128 * 128;        // one 64-column box of a 128-row tile
+  static constexpr int kStages = 2;
   static constexpr int kOffDO = kQBytes;
   static constexpr int kOffKV = 2 * kQBytes;  // stage s: K at s * 2 * kKVBytes, V right after
   static constexpr int kOffBars = kOffKV + kStages * 2 * kKVBytes;
-  static constexpr int kNumBars = 2 * kStages + 1 + 4 + 1;
+  static constexpr int kNumBars = 2 * kStages + 1 + 1 + 2 + 1;
   static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
   static constexpr int kThreads = 320;
 };
 
-// dS for 32 key columns [c0, c0 + 32) of one step (thread = query row).
+// dS for the 32 key columns [c0, c0 + 32) of one step (thread = query row);
+// S at s_col, dP at s_col + 128; packed dS goes over the first 16 columns read.
 template <bool MASK>
-__device__ __forceinline__ void dq_half(uint32_t col, int c0, float l2, float dl, float sl2, int kb, int lim) {
+__device__ __forceinline__ void dq_cols32(uint32_t s_col, int c0, float l2, float dl, float sl2, int kb, int lim) {
   uint32_t sr[32], dr[32];
-  tmem_ld32(col + c0, sr);
-  tmem_ld32(col + 64 + c0, dr);
+  tmem_ld32_pair(s_col + c0, s_col + 128 + c0, sr, dr);
   uint32_t pk[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
@@ -659,11 +667,14 @@ __device__ __forceinline__ void dq_half(uint32_t col, int c0, float l2, float dl
     }
     pk[i] = pack_bf16x2(ds[0], ds[1]);
   }
-  tmem_st16(col + c0 / 2, pk);
+  tmem_st16(s_col + c0, pk);
 }
 
-// dQ kernel: CTA = (batch, head, 128 queries); two softmax warpgroups take
-// the even / odd 64-key steps (TMEM stage = step parity).
+// dQ kernel: CTA = (batch, head, 128 queries); thread = query row.  Each step
+// takes 128 keys (every MMA 128 x 128): S = Q K^T, dP = dO V^T, dS (bf16,
+// written back into S's columns), dQ += dS K.  TMEM: dQ [0,128) S [128,256)
+// dP [256,384).  The step runs in two 64-key halves so the dQ MMAs of half 0
+// overlap the softmax of half 1.
 template <int D>
 __global__ void __launch_bounds__(320, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -680,9 +691,9 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* full = bars;
   uint64_t* empty = bars + NS;
   uint64_t* q_full = bars + 2 * NS;
-  uint64_t* s_full = q_full + 1;  // [2]
-  uint64_t* p_full = q_full + 3;  // [2]
-  uint64_t* acc_full = q_full + 5;
+  uint64_t* s_full = q_full + 1;
+  uint64_t* p_half = q_full + 2;  // [2]
+  uint64_t* acc_full = q_full + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -703,10 +714,9 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 128);
-    }
+    mbar_init(s_full, 1);
+    mbar_init(&p_half[0], 256);
+    mbar_init(&p_half[1], 256);
     mbar_init(acc_full, 1);
     fence_barrier_init();
   }
@@ -725,8 +735,8 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_desc(&tm_v);
       mbar_arrive_expect_tx(q_full, 2 * C::kQBytes);
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_4d(sQ + c * C::kQBox, &tm_q, q_full, c * 64, q0, h, b);
-        tma_load_4d(sDO + c * C::kQBox, &tm_do, q_full, c * 64, q0, h, b);
+        tma_load_4d(sQ + c * C::kBox, &tm_q, q_full, c * 64, q0, h, b);
+        tma_load_4d(sDO + c * C::kBox, &tm_do, q_full, c * 64, q0, h, b);
       }
       for (int t = 0; t < T; ++t) {
         const int s = t % NS, r = t / NS;
@@ -734,61 +744,61 @@ __global__ void __launch_bounds__(320, 1)
         mbar_arrive_expect_tx(&full[s], 2 * C::kKVBytes);
         uint8_t* dst = sKV + s * 2 * C::kKVBytes;
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(dst + c * C::kKBox, &tm_k, &full[s], c * 64, t * BN, hk, b);
-          tma_load_4d(dst + C::kKVBytes + c * C::kKBox, &tm_v, &full[s], c * 64, t * BN, hk, b);
+          tma_load_4d(dst + c * C::kBox, &tm_k, &full[s], c * 64, t * BN, hk, b);
+          tma_load_4d(dst + C::kKVBytes + c * C::kBox, &tm_v, &full[s], c * 64, t * BN, hk, b);
         }
       }
     }
     __syncwarp();
   } else if (warp == 9) {
     if (lane == 0 && T > 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, 0, 0);   // Q x K^T
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, 0, 0);   // Q x K^T, dO x V^T
       constexpr uint32_t idesc_dq = idesc_bf16_f32(128, D, 0, 1);  // dS (TMEM) x K (MN-major)
       const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO), kv_addr = smem_u32(sKV);
+      const uint64_t dq_desc = sdesc_sw128(q_addr, 16, 1024), ddo_desc = sdesc_sw128(do_addr, 16, 1024);
       auto issue_scores = [&](int t) {
-        const int s = t % NS, ts = t & 1;
-        const uint32_t ka = kv_addr + s * 2 * C::kKVBytes, va = ka + C::kKVBytes;
-        const uint32_t col = tbase + 128 + ts * 128;
+        const uint32_t ka = kv_addr + (t % NS) * 2 * C::kKVBytes;
+        const uint64_t dk_desc = sdesc_sw128(ka, 16, 1024), dv_desc = sdesc_sw128(ka + C::kKVBytes, 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t qo = (k >> 2) * C::kQBox + (k & 3) * 32;
-          const uint32_t ko = (k >> 2) * C::kKBox + (k & 3) * 32;
-          mma_ss(col, sdesc_sw128(q_addr + qo, 16, 1024), sdesc_sw128(ka + ko, 16, 1024), idesc_s, k > 0);
+          const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
+          mma_ss(tbase + 128, dq_desc + off, dk_desc + off, idesc_s, k > 0);
         }
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t qo = (k >> 2) * C::kQBox + (k & 3) * 32;
-          const uint32_t ko = (k >> 2) * C::kKBox + (k & 3) * 32;
-          mma_ss(col + 64, sdesc_sw128(do_addr + qo, 16, 1024), sdesc_sw128(va + ko, 16, 1024), idesc_s, k > 0);
+          const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
+          mma_ss(tbase + 256, ddo_desc + off, dv_desc + off, idesc_s, k > 0);
         }
-        mma_commit(&s_full[ts]);
+        mma_commit(s_full);
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, p.status, 32);
-      for (int t = 0; t < 2 && t < T && ok; ++t) {
-        ok = mbar_wait(&full[t % NS], (t / NS) & 1, abort_flag, p.status, 33);
-        if (!ok) break;
+      if (ok) ok = mbar_wait(&full[0], 0, abort_flag, p.status, 33);
+      if (ok) {
         tc_fence_after();
-        issue_scores(t);
+        issue_scores(0);
       }
       for (int t = 0; t < T && ok; ++t) {
-        const int s = t % NS, ts = t & 1;
-        ok = mbar_wait(&p_full[ts], (t >> 1) & 1, abort_flag, p.status, 34);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t ka = kv_addr + s * 2 * C::kKVBytes;
-        const uint32_t col = tbase + 128 + ts * 128;
+        const int s = t % NS;
+        const uint64_t bk = sdesc_sw128(kv_addr + s * 2 * C::kKVBytes, C::kBox, 1024);
 #pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {  // dQ += dS K
-          mma_ts(tbase, col + k * 8, sdesc_sw128(ka + k * 2048, C::kKBox, 1024), idesc_dq,
-                 (t > 0 || k > 0) ? 1u : 0u);
-        }
-        mma_commit(&empty[s]);
-        if (t + 2 < T) {
-          const int tn = t + 2;
-          ok = mbar_wait(&full[tn % NS], (tn / NS) & 1, abort_flag, p.status, 35);
+        for (int hh = 0; hh < 2; ++hh) {
+          ok = mbar_wait(&p_half[hh], t & 1, abort_flag, p.status, 34 + hh);
           if (!ok) break;
           tc_fence_after();
-          issue_scores(tn);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // dQ += dS[:, keys 64hh + 16k ..] K[keys 64hh + 16k ..]
+            const uint32_t acol = 128 + 64 * hh + 32 * (k >> 1) + 8 * (k & 1);
+            const uint32_t boff = ((64 * hh + 16 * k) * 128) >> 4;
+            mma_ts(tbase, tbase + acol, bk + boff, idesc_dq, (t > 0 || hh > 0 || k > 0) ? 1u : 0u);
+          }
+        }
+        if (!ok) break;
+        mma_commit(&empty[s]);
+        if (t + 1 < T) {
+          ok = mbar_wait(&full[(t + 1) % NS], ((t + 1) / NS) & 1, abort_flag, p.status, 36);
+          if (!ok) break;
+          tc_fence_after();
+          issue_scores(t + 1);
         }
       }
       if (ok) mma_commit(acc_full);
@@ -800,30 +810,31 @@ __global__ void __launch_bounds__(320, 1)
     const int r = wq * 32 + lane;
     const int i = q0 + r;
     const uint32_t t_lane = tbase + (static_cast<uint32_t>(wq * 32) << 16);
-    const uint32_t col = t_lane + 128 + w * 128;
+    const uint32_t s_col = t_lane + 128;
     const size_t srow = (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + i;  // i < Lq_pad always
     const float l2 = p.lse2[srow];
     const float dl = p.delta[srow];
     const int lim = i < p.Lq ? key_limit(i, p.Lq, kvl, p.causal) : 0;
     const float sl2 = p.scale_log2;
     bool ok = true;
-    for (int t = w; t < T; t += 2) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[w], (t >> 1) & 1, abort_flag, p.status, 36));
+    for (int t = 0; t < T; ++t) {
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full, t & 1, abort_flag, p.status, 37));
       if (!ok) break;
       tc_fence_after();
       const int kb = t * BN;
-      if (__all_sync(0xffffffffu, kb + BN <= lim)) {
-        dq_half<false>(col, 0, l2, dl, sl2, kb, lim);
-        dq_half<false>(col, 32, l2, dl, sl2, kb, lim);
-      } else {
-        dq_half<true>(col, 0, l2, dl, sl2, kb, lim);
-        dq_half<true>(col, 32, l2, dl, sl2, kb, lim);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int c0 = 64 * hh + 32 * w;
+        if (__all_sync(0xffffffffu, kb + c0 + 32 <= lim))
+          dq_cols32<false>(s_col, c0, l2, dl, sl2, kb, lim);
+        else
+          dq_cols32<true>(s_col, c0, l2, dl, sl2, kb, lim);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_half[hh]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&p_full[w]);
     }
-    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 37));
+    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 38));
     if (ok) {
       tc_fence_after();
       // warpgroup w stores head-dim columns [w * D/2, (w + 1) * D/2)
@@ -910,10 +921,12 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
   kp.scale_log2 = pb.scale * kLog2e;
   kp.status = st;
 
-  // dK/dV pass: K/V boxes of 128 rows, Q/dO boxes of 64 rows
+  // dK/dV pass: K/V boxes of 128 rows, Q/dO boxes of 128 rows (two-pass) or 64 rows (single pass)
   {
-    CUtensorMap tq, tk, tv, tdo;
-    if (!make_bshd_tmap(&tq, a.q, true, pb.B, pb.Lq, pb.Hq, D, 64, 64) ||
+    CUtensorMap tq, tk, tv, tdo, tq128, tdo128;
+    if (!make_bshd_tmap(&tq128, a.q, true, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
+        !make_bshd_tmap(&tdo128, a.dout, true, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
+        !make_bshd_tmap(&tq, a.q, true, pb.B, pb.Lq, pb.Hq, D, 64, 64) ||
         !make_bshd_tmap(&tdo, a.dout, true, pb.B, pb.Lq, pb.Hq, D, 64, 64) ||
         !make_bshd_tmap(&tk, a.k, true, pb.B, pb.Lkv, pb.Hkv, D, 64, 128) ||
         !make_bshd_tmap(&tv, a.v, true, pb.B, pb.Lkv, pb.Hkv, D, 64, 128))
@@ -921,11 +934,11 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
     dim3 grid((pb.Lkv + 127) / 128, pb.Hkv, pb.B);
     kp.n_tiles = grid.x;
     if (a.deterministic) {
-      using C = DkdvPPCfg<D>;
-      e = cudaFuncSetAttribute(bwd_dkdv_pp_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+      using C = DkdvCfg2<D>;
+      e = cudaFuncSetAttribute(bwd_dkdv_kernel2<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
       if (e != cudaSuccess) return e;
       KernelTimer kt("bwd_dkdv", stream);
-      bwd_dkdv_pp_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+      bwd_dkdv_kernel2<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq128, tk, tv, tdo128, kp);
     } else {
       using C = DkdvCfg<D, true>;
       e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -944,13 +957,13 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
         a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), n4, pb.scale);
     return cudaGetLastError();
   }
-  // dQ pass: Q/dO boxes of 128 rows, K/V boxes of 64 rows
+  // dQ pass: Q/dO and K/V boxes of 128 rows
   {
     CUtensorMap tq, tk, tv, tdo;
     if (!make_bshd_tmap(&tq, a.q, true, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
         !make_bshd_tmap(&tdo, a.dout, true, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
-        !make_bshd_tmap(&tk, a.k, true, pb.B, pb.Lkv, pb.Hkv, D, 64, 64) ||
-        !make_bshd_tmap(&tv, a.v, true, pb.B, pb.Lkv, pb.Hkv, D, 64, 64))
+        !make_bshd_tmap(&tk, a.k, true, pb.B, pb.Lkv, pb.Hkv, D, 64, 128) ||
+        !make_bshd_tmap(&tv, a.v, true, pb.B, pb.Lkv, pb.Hkv, D, 64, 128))
       return cudaErrorInvalidValue;
     using C = DqCfg<D>;
     dim3 grid((pb.Lq + 127) / 128, pb.Hq, pb.B);

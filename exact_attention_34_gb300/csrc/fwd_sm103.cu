@@ -236,23 +236,27 @@ __global__ void __launch_bounds__(320, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], j & 1, abort_flag, p.status, 8));
       if (!ok) break;
       tc_fence_after();
+      uint32_t sraw[kBN];
+      tmem_ld128(s_addr, sraw);
       float s[kBN];
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(s_addr + c * 32, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
-      }
+      for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(sraw[i]);
       const int col0 = j * kBN;
       if (col0 + kBN > lim) {
 #pragma unroll
         for (int i = 0; i < kBN; ++i)
           if (col0 + i >= lim) s[i] = -INFINITY;
       }
-      float mx = s[0];
+      // row max as a tree (8 independent chains) instead of one 127-long chain
+      float mx8[8];
 #pragma unroll
-      for (int i = 1; i < kBN; ++i) mx = fmaxf(mx, s[i]);
+      for (int k = 0; k < 8; ++k) mx8[k] = s[k];
+#pragma unroll
+      for (int i = 8; i < kBN; i += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], s[i + k]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_tile = mx * sl2;  // scale > 0, so the max commutes with the scaling
       const bool grow = m_tile > m_used + kRescaleThreshold;
       const float m_new = grow ? m_tile : m_used;
@@ -270,6 +274,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       m_used = m_new;
       const float mb = (m_used == -INFINITY) ? 0.f : m_used;
+      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < kBN / 32; ++c) {
         uint32_t pk[16];
@@ -277,11 +282,12 @@ __global__ void __launch_bounds__(320, 1)
         for (int i = 0; i < 16; ++i) {
           const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, -mb));
           const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, -mb));
-          l_sum += p0 + p1;
+          ls4[i & 3] += p0 + p1;
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16(s_addr + c * 16, pk);
       }
+      l_sum += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full[x]);
