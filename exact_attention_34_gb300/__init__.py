@@ -71,6 +71,7 @@ def lib() -> ctypes.CDLL:
         "attn_device_status": (I, [ctypes.POINTER(I), ctypes.POINTER(I), I]),
         "attn_timing_enable": (I, [I]),
         "attn_timing_query": (I, [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I)]),
+        "attn_bwd_static_scratch": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, I, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -84,6 +85,7 @@ EXPORTED = (
     "attn_status_string", "attn_last_error", "attn_fwd", "attn_bwd_preprocess", "attn_bwd_workspace_size",
     "attn_bwd", "attn_decode_num_splits", "attn_decode_splitkv", "attn_decode_combine",
     "attn_decode_workspace_size", "attn_device_status", "attn_timing_enable", "attn_timing_query",
+    "attn_bwd_static_scratch",
 )
 
 
@@ -179,6 +181,19 @@ def attn_device_status(reset=True):
     code, site = ctypes.c_int(0), ctypes.c_int(0)
     st = lib().attn_device_status(ctypes.byref(code), ctypes.byref(site), int(bool(reset)))
     return st, code.value, site.value
+
+
+def attn_bwd_static_scratch(q, k, v, o, lse, dout, dq, dk, dv, scale=None, causal=False, kv_lens=None,
+                            stream=None):
+    """Deterministic backward with the library's own static scratch: no
+    workspace argument and no device allocation, for callers that cannot
+    allocate (graph capture, fixed memory pools, embeddings).  Calls on one
+    device must not overlap on the GPU."""
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    _check(lib().attn_bwd_static_scratch(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                                         _ptr(dk), _ptr(dv), B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d),
+                                         int(bool(causal)), _ptr(kv_lens), _dtype(q), _stream(stream)),
+           "attn_bwd_static_scratch")
 
 
 def attn_timing_enable(on=True):

@@ -438,3 +438,62 @@ attn_status attn_device_status(int* code, int* site, int reset) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward without any device allocation by the caller.
+//
+// Some callers cannot allocate device memory at the point where they need the
+// backward: code running while a CUDA graph is being captured (cudaMalloc is
+// not allowed inside most capture modes), hosts whose device memory is owned by
+// a fixed pool or another runtime's allocator, and plugin or interpreter
+// embeddings that hand the library only the tensors they already own.  For
+// them the deterministic backward's scratch (delta and lse*log2(e), one float
+// each per padded query row) lives in a file-scope device array instead of a
+// caller workspace.  Every GPU that loads this library holds the array until
+// the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB: B*Hq*roundup(Lq,128) <= 524288
+static __device__ __align__(256) unsigned char g_bwd_static_scratch[kStaticScratchBytes];
+
+void* g_static_scratch_ptr[kMaxDevices] = {};
+std::mutex g_static_scratch_mu;
+
+}  // namespace
+
+extern "C" attn_status attn_bwd_static_scratch(const void* q, const void* k, const void* v, const void* o,
+                                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                               int B, int Lq, int Lkv, int Hq, int Hkv, int d, float scale,
+                                               int causal, const int32_t* kv_lens, attn_dtype dtype,
+                                               attn_stream_t stream) {
+  const size_t need = attn_bwd_workspace_size(B, Lq, Hq, d, 1, dtype);
+  if (need == 0) return fail(ATTN_ERR_INVALID_ARG, "sizes must be positive (B=%d Lq=%d Hq=%d d=%d)", B, Lq, Hq, d);
+  if (need > kStaticScratchBytes)
+    return fail(ATTN_ERR_WORKSPACE,
+                "attn_bwd_static_scratch: this problem needs %zu bytes of scratch but the static scratch holds %zu "
+                "(B*Hq*roundup(Lq,128) must be <= 524288); use attn_bwd with a caller workspace",
+                need, kStaticScratchBytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e, "attn_bwd_static_scratch: cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTN_ERR_CUDA, "attn_bwd_static_scratch: device %d out of range", dev);
+  void* ptr = nullptr;
+  {
+    // First call on a device: look up the device address of the array (with
+    // that device current).  Make that first call before any stream capture.
+    std::lock_guard<std::mutex> lk(g_static_scratch_mu);
+    if (g_static_scratch_ptr[dev] == nullptr) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_bwd_static_scratch);
+      if (e != cudaSuccess) return from_cuda(e, "attn_bwd_static_scratch: cudaGetSymbolAddress");
+      g_static_scratch_ptr[dev] = p;
+    }
+    ptr = g_static_scratch_ptr[dev];
+  }
+  // The deterministic backward overwrites every scratch entry it reads (the
+  // preprocess writes delta and lse2 for all padded rows), so nothing has to be
+  // cleared between calls.
+  return attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Lq, Lkv, Hq, Hkv, d, scale, causal, kv_lens, dtype, 1, ptr,
+                  kStaticScratchBytes, stream);
+}

@@ -175,6 +175,31 @@ attn_status attn_device_status(int* code, int* site, int reset);
 attn_status attn_timing_enable(int on);
 attn_status attn_timing_query(const char* kernel, double* total_ms, int* launches);
 
+/*
+ * Deterministic backward that needs no workspace from the caller (the paper
+ * has no counterpart; this is a convenience of this library).  Same arguments
+ * and results as attn_bwd with deterministic = 1, minus the workspace.
+ *
+ * For callers that cannot allocate device memory where they run the backward:
+ * during CUDA graph capture, inside hosts whose device memory belongs to a fixed
+ * pool or another runtime, or in embeddings that only hand over existing
+ * tensors.  The scratch (two floats per padded query row) lives in a 4 MiB
+ * device array inside the library, held by every GPU that loads it until the
+ * process exits.  Limit: B * Hq * roundup(Lq, 128) <= 524288 (e.g. B4 H8
+ * Lq16384); larger problems return ATTN_ERR_WORKSPACE with a message.
+ *
+ * The first call on each device looks up the array's device address with that
+ * device current; make that first call before any stream capture.  Allocates
+ * nothing (no cudaMalloc/cudaFree, no library allocator).  All calls on a
+ * device share the one array: calls that overlap on the GPU (different
+ * streams, or host threads racing) corrupt each other's scratch -- serialise
+ * them.  No scratch content needs clearing between calls.
+ */
+attn_status attn_bwd_static_scratch(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                    const void* dout, void* dq, void* dk, void* dv, int B, int Lq, int Lkv, int Hq,
+                                    int Hkv, int d, float scale, int causal, const int32_t* kv_lens,
+                                    attn_dtype dtype, attn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
