@@ -523,20 +523,21 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t idesc_st = idesc_bf16_f32(128, BM, 0, 0);  // K x Q^T, V x dO^T
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, 0, 1);  // (P^T|dS^T from TMEM) x (dO|Q MN-major)
       const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ);
-      const uint64_t dk_base = sdesc_sw128(k_addr, 16, 1024), dv_base = sdesc_sw128(v_addr, 16, 1024);
+      const SDesc dk_base = sdesc_split(k_addr, 16, 1024), dv_base = sdesc_split(v_addr, 16, 1024);
+      const SDesc dq_base = sdesc_split(q_addr, 16, 1024), ddo_base = sdesc_split(q_addr + C::kQBytes, 16, 1024);
+      const SDesc bq_base = sdesc_split(q_addr, C::kBox, 1024), bdo_base = sdesc_split(q_addr + C::kQBytes, C::kBox, 1024);
+      constexpr uint32_t kStage16 = (2 * C::kQBytes) >> 4;
       auto issue_scores = [&](int t) {
-        const int s = t % NS;
-        const uint32_t qa = q_addr + s * 2 * C::kQBytes;
-        const uint64_t dq_base = sdesc_sw128(qa, 16, 1024), ddo_base = sdesc_sw128(qa + C::kQBytes, 16, 1024);
+        const uint32_t so = (t % NS) * kStage16;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
-          mma_ss(tbase + kColS, dk_base + off, dq_base + off, idesc_st, k > 0);
+          mma_ss_d(tbase + kColS, dk_base, off, dq_base, so + off, idesc_st, k > 0);
         }
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
-          mma_ss(tbase + kColS + 128, dv_base + off, ddo_base + off, idesc_st, k > 0);
+          mma_ss_d(tbase + kColS + 128, dv_base, off, ddo_base, so + off, idesc_st, k > 0);
         }
         mma_commit(s_full);
       };
@@ -548,8 +549,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       for (int t = 0; t < T && ok; ++t) {
         const int s = t % NS;
-        const uint32_t qa = q_addr + s * 2 * C::kQBytes;
-        const uint64_t bq = sdesc_sw128(qa, C::kBox, 1024), bdo = sdesc_sw128(qa + C::kQBytes, C::kBox, 1024);
+        const uint32_t so = s * kStage16;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           ok = mbar_wait(&p_half[h], t & 1, abort_flag, p.status, 64 + h);
@@ -562,8 +562,8 @@ __global__ void __launch_bounds__(320, 1)
             const uint32_t acol = kColS + 64 * h + 32 * (k >> 1) + 8 * (k & 1);
             const uint32_t boff = ((64 * h + 16 * k) * 128) >> 4;
             const uint32_t acc = (t > 0 || h > 0 || k > 0) ? 1u : 0u;
-            mma_ts(tbase + 128, tbase + acol, bdo + boff, idesc_acc, acc);        // dV += P^T dO
-            mma_ts(tbase + 0, tbase + acol + 128, bq + boff, idesc_acc, acc);     // dK += dS^T Q
+            mma_ts_d(tbase + 128, tbase + acol, bdo_base, so + boff, idesc_acc, acc);     // dV += P^T dO
+            mma_ts_d(tbase + 0, tbase + acol + 128, bq_base, so + boff, idesc_acc, acc);  // dK += dS^T Q
           }
         }
         if (!ok) break;
@@ -755,19 +755,21 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, 0, 0);   // Q x K^T, dO x V^T
       constexpr uint32_t idesc_dq = idesc_bf16_f32(128, D, 0, 1);  // dS (TMEM) x K (MN-major)
       const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO), kv_addr = smem_u32(sKV);
-      const uint64_t dq_desc = sdesc_sw128(q_addr, 16, 1024), ddo_desc = sdesc_sw128(do_addr, 16, 1024);
+      const SDesc dq_desc = sdesc_split(q_addr, 16, 1024), ddo_desc = sdesc_split(do_addr, 16, 1024);
+      const SDesc dk_desc = sdesc_split(kv_addr, 16, 1024), dv_desc = sdesc_split(kv_addr + C::kKVBytes, 16, 1024);
+      const SDesc bk_desc = sdesc_split(kv_addr, C::kBox, 1024);
+      constexpr uint32_t kStage16 = (2 * C::kKVBytes) >> 4;
       auto issue_scores = [&](int t) {
-        const uint32_t ka = kv_addr + (t % NS) * 2 * C::kKVBytes;
-        const uint64_t dk_desc = sdesc_sw128(ka, 16, 1024), dv_desc = sdesc_sw128(ka + C::kKVBytes, 16, 1024);
+        const uint32_t so = (t % NS) * kStage16;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
-          mma_ss(tbase + 128, dq_desc + off, dk_desc + off, idesc_s, k > 0);
+          mma_ss_d(tbase + 128, dq_desc, off, dk_desc, so + off, idesc_s, k > 0);
         }
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
-          mma_ss(tbase + 256, ddo_desc + off, dv_desc + off, idesc_s, k > 0);
+          mma_ss_d(tbase + 256, ddo_desc, off, dv_desc, so + off, idesc_s, k > 0);
         }
         mma_commit(s_full);
       };
@@ -779,7 +781,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       for (int t = 0; t < T && ok; ++t) {
         const int s = t % NS;
-        const uint64_t bk = sdesc_sw128(kv_addr + s * 2 * C::kKVBytes, C::kBox, 1024);
+        const uint32_t so = s * kStage16;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           ok = mbar_wait(&p_half[hh], t & 1, abort_flag, p.status, 34 + hh);
@@ -789,7 +791,7 @@ __global__ void __launch_bounds__(320, 1)
           for (int k = 0; k < 4; ++k) {  // dQ += dS[:, keys 64hh + 16k ..] K[keys 64hh + 16k ..]
             const uint32_t acol = 128 + 64 * hh + 32 * (k >> 1) + 8 * (k & 1);
             const uint32_t boff = ((64 * hh + 16 * k) * 128) >> 4;
-            mma_ts(tbase, tbase + acol, bk + boff, idesc_dq, (t > 0 || hh > 0 || k > 0) ? 1u : 0u);
+            mma_ts_d(tbase, tbase + acol, bk_desc, so + boff, idesc_dq, (t > 0 || hh > 0 || k > 0) ? 1u : 0u);
           }
         }
         if (!ok) break;

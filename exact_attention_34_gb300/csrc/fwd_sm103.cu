@@ -39,9 +39,10 @@ struct FwdCfg {
   static constexpr int kQTileBytes = kBM * D * 2;     // one query tile, bf16
   static constexpr int kSlotBytes = kBN * D * 2;      // one K or V tile
   static constexpr int kBoxBytes = 128 * 64 * 2;      // one TMA box (128 rows x 64 cols)
-  static constexpr int kSlots = (D == 128) ? 4 : 8;   // ring depth
+  static constexpr int kSlots = (D == 128) ? 2 : 4;   // ring depth in (K, V) stages
+  static constexpr int kStageBytes = 2 * kSlotBytes;  // K at 0, V at kSlotBytes
   static constexpr int kOffSlots = 2 * kQTileBytes;
-  static constexpr int kOffBars = kOffSlots + kSlots * kSlotBytes;
+  static constexpr int kOffBars = kOffSlots + kSlots * kStageBytes;
   static constexpr int kNumBars = 2 * kSlots + 7;
   static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;  // + alignment slack
   static constexpr int kThreads = 320;
@@ -137,17 +138,14 @@ __global__ void __launch_bounds__(320, 1)
           tma_load_4d(sQ + x * C::kQTileBytes + h * C::kBoxBytes, &tm_q, q_full, h * 64, row0, hq, b);
       }
       for (int j = 0; j < n; ++j) {
-        bool ok = true;
-        for (int t = 0; t < 2 && ok; ++t) {
-          const int ld = 2 * j + t, s = ld % C::kSlots, r = ld / C::kSlots;
-          if (r > 0) ok = mbar_wait(&empty[s], (r - 1) & 1, abort_flag, p.status, 1);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&full[s], C::kSlotBytes);
-          uint8_t* dst = sSlots + s * C::kSlotBytes;
-          for (int h = 0; h < D / 64; ++h)
-            tma_load_4d(dst + h * C::kBoxBytes, t == 0 ? &tm_k : &tm_v, &full[s], h * 64, j * kBN, hkv, b);
+        const int st = j % C::kSlots, r = j / C::kSlots;
+        if (r > 0 && !mbar_wait(&empty[st], (r - 1) & 1, abort_flag, p.status, 1)) break;
+        mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+        uint8_t* dst = sSlots + st * C::kStageBytes;
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_4d(dst + h * C::kBoxBytes, &tm_k, &full[st], h * 64, j * kBN, hkv, b);
+          tma_load_4d(dst + C::kSlotBytes + h * C::kBoxBytes, &tm_v, &full[st], h * 64, j * kBN, hkv, b);
         }
-        if (!ok) break;
       }
     }
     __syncwarp();
@@ -156,26 +154,25 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0 && n > 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);  // Q (K-major) x K^T (K-major)
       constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);    // P (TMEM) x V (MN-major)
-      const uint32_t q_addr = smem_u32(sQ);
-      const uint32_t slot_addr = smem_u32(sSlots);
+      const SDesc dq[2] = {sdesc_split(smem_u32(sQ), 16, 1024), sdesc_split(smem_u32(sQ) + C::kQTileBytes, 16, 1024)};
+      const SDesc dk0 = sdesc_split(smem_u32(sSlots), 16, 1024);
+      const SDesc dv0 = sdesc_split(smem_u32(sSlots) + C::kSlotBytes, C::kBoxBytes, 1024);
+      constexpr uint32_t kStage16 = C::kStageBytes >> 4;
       // S_x = Q_x K^T : 16-wide k-steps along d; each 64-column half of d is its own TMA box.
-      auto issue_s = [&](int x, int kslot) {
-        const uint32_t qa = q_addr + x * C::kQTileBytes;
-        const uint32_t ka = slot_addr + kslot * C::kSlotBytes;
+      auto issue_s = [&](int x, int st) {
+        const uint32_t so = st * kStage16;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * C::kBoxBytes + (k & 3) * 32;
-          mma_ss(tbase + x * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_s, k > 0);
+          const uint32_t off = ((k >> 2) * C::kBoxBytes + (k & 3) * 32) >> 4;
+          mma_ss_d(tbase + x * 128, dq[x], off, dk0, so + off, idesc_s, k > 0);
         }
       };
       // O_x (+)= P_x V : 16-key k-steps; P advances 8 TMEM columns, V 16 rows (2 KB).
-      auto issue_pv = [&](int x, int vslot, int acc) {
-        const uint32_t va = slot_addr + vslot * C::kSlotBytes;
+      auto issue_pv = [&](int x, int st, int acc) {
+        const uint32_t so = st * kStage16;
 #pragma unroll
-        for (int k = 0; k < kBN / 16; ++k) {
-          mma_ts(tbase + 256 + x * 128, tbase + x * 128 + k * 8, sdesc_sw128(va + k * 2048, C::kBoxBytes, 1024),
-                 idesc_o, (acc || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < kBN / 16; ++k)
+          mma_ts_d(tbase + 256 + x * 128, tbase + x * 128 + k * 8, dv0, so + k * 128, idesc_o, (acc || k > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, p.status, 2);
       if (ok) ok = mbar_wait(&full[0], 0, abort_flag, p.status, 3);
@@ -183,40 +180,33 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         if (n_a > 0) { issue_s(0, 0); mma_commit(&s_full[0]); }
         if (n_b > 0) { issue_s(1, 0); mma_commit(&s_full[1]); }
-        mma_commit(&empty[0]);
       }
       for (int j = 0; j < n && ok; ++j) {
-        const int vl = 2 * j + 1, vs = vl % C::kSlots;
-        const int kl = 2 * j + 2, ks = kl % C::kSlots;
+        const int st = j % C::kSlots;
+        const int stn = (j + 1) % C::kSlots;
         const bool has_next = j + 1 < n;
-        ok = mbar_wait(&full[vs], (vl / C::kSlots) & 1, abort_flag, p.status, 4);
-        if (!ok) break;
-        tc_fence_after();
         if (j < n_a) {
           ok = mbar_wait(&p_full[0], j & 1, abort_flag, p.status, 5);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(0, vs, j > 0);
+          issue_pv(0, st, j > 0);
           if (j == n_a - 1) mma_commit(&o_full[0]);
         }
         if (has_next) {
-          ok = mbar_wait(&full[ks], (kl / C::kSlots) & 1, abort_flag, p.status, 6);
+          ok = mbar_wait(&full[stn], ((j + 1) / C::kSlots) & 1, abort_flag, p.status, 6);
           if (!ok) break;
           tc_fence_after();
-          if (j + 1 < n_a) { issue_s(0, ks); mma_commit(&s_full[0]); }
+          if (j + 1 < n_a) { issue_s(0, stn); mma_commit(&s_full[0]); }
         }
         if (j < n_b) {
           ok = mbar_wait(&p_full[1], j & 1, abort_flag, p.status, 7);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(1, vs, j > 0);
+          issue_pv(1, st, j > 0);
           if (j == n_b - 1) mma_commit(&o_full[1]);
         }
-        mma_commit(&empty[vs]);
-        if (has_next) {
-          if (j + 1 < n_b) { issue_s(1, ks); mma_commit(&s_full[1]); }
-          mma_commit(&empty[ks]);
-        }
+        mma_commit(&empty[st]);
+        if (has_next && j + 1 < n_b) { issue_s(1, stn); mma_commit(&s_full[1]); }
       }
     }
     __syncwarp();

@@ -175,6 +175,44 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_maj
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Descriptor split into its two 32-bit halves.  The start address lives in
+// the low half (bits 0-13, address >> 4) and never carries into bit 14 for
+// shared-memory addresses, so stepping through a tile is one 32-bit add on
+// `lo` with a compile-time constant.
+struct SDesc {
+  uint32_t lo, hi;
+};
+
+__device__ __forceinline__ SDesc sdesc_split(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  const uint64_t d = sdesc_sw128(smem_addr, lbo_bytes, sbo_bytes);
+  return SDesc{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+
+// D[tmem] (+)= A[smem] * B[smem]; descriptors as halves, A/B offset (in 16-byte units)
+__device__ __forceinline__ void mma_ss_d(uint32_t d_tmem, SDesc a, uint32_t a_off16, SDesc b, uint32_t b_off16,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\t"
+      "mov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a.lo + a_off16), "r"(a.hi), "r"(b.lo + b_off16), "r"(b.hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]; B descriptor as halves plus offset (16-byte units)
+__device__ __forceinline__ void mma_ts_d(uint32_t d_tmem, uint32_t a_tmem, SDesc b, uint32_t b_off16, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b.lo + b_off16), "r"(b.hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] * B[smem]
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
