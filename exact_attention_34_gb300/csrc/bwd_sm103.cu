@@ -379,14 +379,17 @@ __global__ void __launch_bounds__(192, 1)
 // ============================================================================
 // CTA = (batch, KV head, 128 keys); thread = key row = TMEM lane.  Each step
 // takes 128 queries so every tcgen05.mma is 128 x 128 (64-wide operands run
-// the tensor core at two thirds of its rate or less).  TMEM then holds one
-// stage: dK [0,128) dV [128,256) S^T [256,384) dP^T [384,512).  The step is
-// overlapped in two halves of 64 queries: both softmax warpgroups convert
-// half 0 (warpgroup w takes 32 of its columns), signal, and convert half 1
-// while the MMA warp already accumulates dV += P^T dO and dK += dS^T Q for
-// half 0.  Each warpgroup writes its bf16 P^T / dS^T over the first 16 of
-// the 32 fp32 columns it read, so no warpgroup overwrites columns another one
-// still reads.  Warp 8 is the TMA producer, warp 9 the MMA issuer.
+// the tensor core at two thirds of its rate or less).  TMEM holds one stage:
+// dK [0,128) dV [128,256) S^T [256,384) dP^T [384,512).
+//
+// The two score GEMMs are separate, and so is the softmax work:
+//   tensor pipe:  S^T(t) | dP^T(t)           | dV += P^T dO | dK += dS^T Q | S^T(t+1) ...
+//   softmax:             | P^T = 2^(S^T - L)  | dS^T = P^T (dP^T - delta)   |
+// The P half needs only S^T and runs while dP^T is computed; the dS half runs
+// while dV accumulates.  Warpgroup w owns queries [64w, 64w + 64) of the step
+// and keeps its 64 probabilities in fp32 registers between the halves; the
+// packed bf16 P^T / dS^T go over the first 32 of its 64 S^T / dP^T columns.
+// Warps 0-7 softmax, warp 8 TMA producer, warp 9 MMA issuer.
 template <int D>
 struct DkdvCfg2 {
   static constexpr int kBN = 128, kBM = 128;
@@ -398,42 +401,91 @@ struct DkdvCfg2 {
   static constexpr int kOffQ = 2 * kKVBytes;  // stage s: Q at s * 2 * kQBytes, dO right after
   static constexpr int kOffStat = kOffQ + kStages * 2 * kQBytes;
   static constexpr int kOffBars = kOffStat + kStages * 2 * kBM * 4;
-  static constexpr int kNumBars = 2 * kStages + 1 + 1 + 2 + 1;
+  static constexpr int kNumBars = 2 * kStages + 1 + 2 + 2 + 1;
   static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
   static constexpr int kThreads = 320;
 };
 
-// P^T and dS^T for the 32 query columns [c0, c0 + 32) of the step (thread =
-// key).  S^T is at s_col, dP^T at s_col + 128; the packed bf16 results go to
-// the first 16 of the 32 columns that were read (query pair c -> column c).
-template <bool MASK>
-__device__ __forceinline__ void dkdv_cols32(uint32_t s_col, int c0, const float* lse2, const float* dlt, float sl2,
-                                            bool key_ok, int q_lo, int q_min) {
-  uint32_t sr[32], dr[32];
-  tmem_ld32_pair(s_col + c0, s_col + 128 + c0, sr, dr);
-  uint32_t pk[16], dk[16];
+// Store columns [c0, c0 + NC) of one fp32 TMEM row as bf16 (times mul).
+template <int NC>
+__device__ __forceinline__ void store_cols_bf16(uint32_t taddr, __nv_bfloat16* dst, float mul, bool do_store,
+                                                bool zero) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int c = 0; c < NC / 16; ++c) {
+    uint32_t r[16];
+    if (!zero) {
+      tmem_ld16(taddr + c * 16, r);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) r[i] = 0u;
+    }
+    uint32_t pk[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+    if (do_store) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 16);
+      d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+    }
+  }
+}
+
+// TMEM column (relative to the step's S^T / S block) of the packed A operand
+// for query (or key) k-step k of half h, when NWG warpgroups each convert
+// 64 / NWG columns of a half.
+template <int NWG>
+__device__ __forceinline__ constexpr uint32_t packed_col(int h, int k) {
+  constexpr int kC = 64 / NWG;
+  return 64 * h + kC * ((16 * k) / kC) + ((16 * k) % kC) / 2;
+}
+
+// P^T for the warpgroup's 64 queries [c0, c0 + 64): probabilities kept in
+// `pr` (fp32) and written packed over columns [c0, c0 + 32) of S^T.
+template <bool MASK>
+__device__ __forceinline__ void dkdv_probs(uint32_t s_col, int c0, const float* lse2, float sl2, bool key_ok,
+                                           int q_lo, int q_min, float (&pr)[64]) {
+  uint32_t sa[32], sb[32];
+  tmem_ld32_pair(s_col + c0, s_col + c0 + 32, sa, sb);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
     const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c0 + 4 * i);
-    const float4 d4 = *reinterpret_cast<const float4*>(dlt + c0 + 4 * i);
     const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-    const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-    float pr[4], ds[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int c = 4 * i + e;
-      float pv = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lv[e]));
+      const uint32_t raw = c < 32 ? sa[c] : sb[c - 32];
+      float pv = ex2_approx(fmaf(__uint_as_float(raw), sl2, -lv[e]));
       if (MASK) pv = (key_ok && q_lo + c0 + c >= q_min) ? pv : 0.f;
-      pr[e] = pv;
-      ds[e] = pv * (__uint_as_float(dr[c]) - dv[e]);
+      pr[c] = pv;
     }
-    pk[2 * i] = pack_bf16x2(pr[0], pr[1]);
-    pk[2 * i + 1] = pack_bf16x2(pr[2], pr[3]);
+  }
+  uint32_t pk[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
+  tmem_st32(s_col + c0, pk);
+}
+
+// dS^T = P^T (dP^T - delta) for the same 64 queries, written packed over
+// columns [c0, c0 + 32) of dP^T.
+__device__ __forceinline__ void dkdv_dscores(uint32_t dp_col, int c0, const float* dlt, const float (&pr)[64]) {
+  uint32_t da[32], db[32];
+  tmem_ld32_pair(dp_col + c0, dp_col + c0 + 32, da, db);
+  uint32_t dk[32];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float4 d4 = *reinterpret_cast<const float4*>(dlt + c0 + 4 * i);
+    const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+    float ds[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = 4 * i + e;
+      const uint32_t raw = c < 32 ? da[c] : db[c - 32];
+      ds[e] = pr[c] * (__uint_as_float(raw) - dv[e]);
+    }
     dk[2 * i] = pack_bf16x2(ds[0], ds[1]);
     dk[2 * i + 1] = pack_bf16x2(ds[2], ds[3]);
   }
-  tmem_st16(s_col + c0, pk);
-  tmem_st16(s_col + 128 + c0, dk);
+  tmem_st32(dp_col + c0, dk);
 }
 
 template <int D>
@@ -443,7 +495,7 @@ __global__ void __launch_bounds__(320, 1)
                      const BwdKParams p) {
   using C = DkdvCfg2<D>;
   constexpr int NS = C::kStages, BM = C::kBM;
-  constexpr uint32_t kColS = 256;
+  constexpr uint32_t kColS = 256, kColDP = 384;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sK = smem;
@@ -454,9 +506,11 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* full = bars;
   uint64_t* empty = bars + NS;
   uint64_t* kv_full = bars + 2 * NS;
-  uint64_t* s_full = kv_full + 1;
-  uint64_t* p_half = kv_full + 2;  // [2]
-  uint64_t* acc_full = kv_full + 4;
+  uint64_t* s_ready = kv_full + 1;   // S^T(t) computed
+  uint64_t* dp_ready = kv_full + 2;  // dP^T(t) computed
+  uint64_t* p_ready = kv_full + 3;   // P^T(t) written (256 arrivals)
+  uint64_t* ds_ready = kv_full + 4;  // dS^T(t) written (256 arrivals)
+  uint64_t* acc_full = kv_full + 5;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -477,9 +531,10 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(kv_full, 1);
-    mbar_init(s_full, 1);
-    mbar_init(&p_half[0], 256);
-    mbar_init(&p_half[1], 256);
+    mbar_init(s_ready, 1);
+    mbar_init(dp_ready, 1);
+    mbar_init(p_ready, 256);
+    mbar_init(ds_ready, 256);
     mbar_init(acc_full, 1);
     fence_barrier_init();
   }
@@ -534,12 +589,13 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
           mma_ss_d(tbase + kColS, dk_base, off, dq_base, so + off, idesc_st, k > 0);
         }
+        mma_commit(s_ready);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
-          mma_ss_d(tbase + kColS + 128, dv_base, off, ddo_base, so + off, idesc_st, k > 0);
+          mma_ss_d(tbase + kColDP, dv_base, off, ddo_base, so + off, idesc_st, k > 0);
         }
-        mma_commit(s_full);
+        mma_commit(dp_ready);
       };
       bool ok = mbar_wait(kv_full, 0, abort_flag, p.status, 62);
       if (ok) ok = mbar_wait(&full[0], 0, abort_flag, p.status, 63);
@@ -548,26 +604,27 @@ __global__ void __launch_bounds__(320, 1)
         issue_scores(0);
       }
       for (int t = 0; t < T && ok; ++t) {
-        const int s = t % NS;
-        const uint32_t so = s * kStage16;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          ok = mbar_wait(&p_half[h], t & 1, abort_flag, p.status, 64 + h);
-          if (!ok) break;
-          tc_fence_after();
-          // query k-steps 4h .. 4h+3; warpgroup w packed queries [64h + 32w, +32) into
-          // columns [64h + 32w, +16) of S^T (P^T) and dP^T (dS^T)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t acol = kColS + 64 * h + 32 * (k >> 1) + 8 * (k & 1);
-            const uint32_t boff = ((64 * h + 16 * k) * 128) >> 4;
-            const uint32_t acc = (t > 0 || h > 0 || k > 0) ? 1u : 0u;
-            mma_ts_d(tbase + 128, tbase + acol, bdo_base, so + boff, idesc_acc, acc);     // dV += P^T dO
-            mma_ts_d(tbase + 0, tbase + acol + 128, bq_base, so + boff, idesc_acc, acc);  // dK += dS^T Q
-          }
-        }
+        const uint32_t so = (t % NS) * kStage16;
+        // query k-step k (16 queries) of warpgroup w = k / 4 sits packed at 64 w + 8 (k - 4 w)
+        ok = mbar_wait(p_ready, t & 1, abort_flag, p.status, 64);
         if (!ok) break;
-        mma_commit(&empty[s]);
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // dV += P^T dO
+          const uint32_t acol = 64 * (k >> 2) + 8 * (k & 3);
+          mma_ts_d(tbase + 128, tbase + kColS + acol, bdo_base, so + ((16 * k * 128) >> 4), idesc_acc,
+                   (t > 0 || k > 0) ? 1u : 0u);
+        }
+        ok = mbar_wait(ds_ready, t & 1, abort_flag, p.status, 65);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // dK += dS^T Q
+          const uint32_t acol = 64 * (k >> 2) + 8 * (k & 3);
+          mma_ts_d(tbase + 0, tbase + kColDP + acol, bq_base, so + ((16 * k * 128) >> 4), idesc_acc,
+                   (t > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(&empty[t % NS]);
         if (t + 1 < T) {
           ok = mbar_wait(&full[(t + 1) % NS], ((t + 1) / NS) & 1, abort_flag, p.status, 66);
           if (!ok) break;
@@ -584,30 +641,34 @@ __global__ void __launch_bounds__(320, 1)
     const int r = wq * 32 + lane;
     const int j = j0 + r;
     const uint32_t t_lane = tbase + (static_cast<uint32_t>(wq * 32) << 16);
-    const uint32_t s_col = t_lane + kColS;
     const bool key_ok = j < kvl;
     const int q_min = p.causal ? j + p.Lq - kvl : -0x7fffffff;
     const float sl2 = p.scale_log2;
+    const int c0 = 64 * w;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int s = t % NS;
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full, t & 1, abort_flag, p.status, 67));
+      ok = __all_sync(0xffffffffu, mbar_wait(s_ready, t & 1, abort_flag, p.status, 67));
       if (!ok) break;
       tc_fence_after();
       const int q0 = (i_begin + t % steps_per_head) * BM;
       const float* lse2 = sStat + s * 2 * BM;
       const float* dlt = lse2 + BM;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c0 = 64 * h + 32 * w;
-        if (__all_sync(0xffffffffu, key_ok && q0 + c0 >= q_min))
-          dkdv_cols32<false>(s_col, c0, lse2, dlt, sl2, key_ok, q0, q_min);
-        else
-          dkdv_cols32<true>(s_col, c0, lse2, dlt, sl2, key_ok, q0, q_min);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&p_half[h]);
-      }
+      float pr[64];
+      if (__all_sync(0xffffffffu, key_ok && q0 + c0 >= q_min))
+        dkdv_probs<false>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, q_min, pr);
+      else
+        dkdv_probs<true>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, q_min, pr);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_ready);
+      ok = __all_sync(0xffffffffu, mbar_wait(dp_ready, t & 1, abort_flag, p.status, 69));
+      if (!ok) break;
+      tc_fence_after();
+      dkdv_dscores(t_lane + kColDP, c0, dlt, pr);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(ds_ready);
     }
     if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 68));
     if (ok) {
@@ -634,29 +695,38 @@ __global__ void __launch_bounds__(320, 1)
 // ============================================================================
 template <int D>
 struct DqCfg {
+  static constexpr int kNWG = 4;                // softmax warpgroups
+  static constexpr int kCols = 64 / kNWG;       // key columns per warpgroup per half-step
+  static constexpr int kProducerWarp = 4 * kNWG, kMmaWarp = 4 * kNWG + 1;
   static constexpr int kBM = 128;               // queries per CTA
   static constexpr int kBN = 128;               // keys per step
   static constexpr int kQBytes = kBM * D * 2;
   static constexpr int kKVBytes = kBN * D * 2;
   static constexpr int kBox = 128 * 128;        // one 64-column box of a 128-row tile
-  static constexpr int kStages = 2;
+  static constexpr int kKSlots = 3, kVSlots = 2;
   static constexpr int kOffDO = kQBytes;
-  static constexpr int kOffKV = 2 * kQBytes;  // stage s: K at s * 2 * kKVBytes, V right after
-  static constexpr int kOffBars = kOffKV + kStages * 2 * kKVBytes;
-  static constexpr int kNumBars = 2 * kStages + 1 + 1 + 2 + 1;
+  static constexpr int kOffK = 2 * kQBytes;
+  static constexpr int kOffV = kOffK + kKSlots * kKVBytes;
+  static constexpr int kOffBars = kOffV + kVSlots * kKVBytes;
+  static constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 1 + 1 + 2 + 1;
   static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 32 * (4 * kNWG + 2);
 };
 
-// dS for the 32 key columns [c0, c0 + 32) of one step (thread = query row);
-// S at s_col, dP at s_col + 128; packed dS goes over the first 16 columns read.
-template <bool MASK>
-__device__ __forceinline__ void dq_cols32(uint32_t s_col, int c0, float l2, float dl, float sl2, int kb, int lim) {
-  uint32_t sr[32], dr[32];
-  tmem_ld32_pair(s_col + c0, s_col + 128 + c0, sr, dr);
-  uint32_t pk[16];
+// dS for the N key columns [c0, c0 + N) of one step (thread = query row);
+// S at s_col, dP at dp_col; packed dS goes over the first N/2 S columns read.
+template <int N, bool MASK>
+__device__ __forceinline__ void dq_cols(uint32_t s_col, uint32_t dp_col, int c0, float l2, float dl, float sl2, int kb,
+                                        int lim) {
+  uint32_t sr[N], dr[N];
+  if constexpr (N == 32) {
+    tmem_ld32_pair(s_col + c0, dp_col + c0, sr, dr);
+  } else {
+    tmem_ld16_pair(s_col + c0, dp_col + c0, sr, dr);
+  }
+  uint32_t pk[N / 2];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
+  for (int i = 0; i < N / 2; ++i) {
     float ds[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
@@ -667,30 +737,39 @@ __device__ __forceinline__ void dq_cols32(uint32_t s_col, int c0, float l2, floa
     }
     pk[i] = pack_bf16x2(ds[0], ds[1]);
   }
-  tmem_st16(s_col + c0, pk);
+  if constexpr (N == 32)
+    tmem_st16(s_col + c0, pk);
+  else
+    tmem_st8(s_col + c0, pk);
 }
 
 // dQ kernel: CTA = (batch, head, 128 queries); thread = query row.  Each step
 // takes 128 keys (every MMA 128 x 128): S = Q K^T, dP = dO V^T, dS (bf16,
-// written back into S's columns), dQ += dS K.  TMEM: dQ [0,128) S [128,256)
-// dP [256,384).  The step runs in two 64-key halves so the dQ MMAs of half 0
-// overlap the softmax of half 1.
+// written back into S's columns), dQ += dS K.  TMEM: dQ [0,128), S in two
+// buffers [128,256) and [384,512) (step parity), dP [256,384).  S of step
+// t+2 is computed while the softmax warps convert step t+1, and each step runs
+// in two 64-key halves so the dQ MMAs of half 0 overlap the conversion of
+// half 1.  K tiles use a 3-slot ring (a K tile is read by S and later by dQ),
+// V tiles a 2-slot ring.
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                   const BwdKParams p) {
   using C = DqCfg<D>;
-  constexpr int NS = C::kStages, BN = C::kBN;
+  constexpr int NK = C::kKSlots, NV = C::kVSlots, BN = C::kBN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sQ = smem;
   uint8_t* sDO = smem + C::kOffDO;
-  uint8_t* sKV = smem + C::kOffKV;
+  uint8_t* sK = smem + C::kOffK;
+  uint8_t* sV = smem + C::kOffV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + NS;
-  uint64_t* q_full = bars + 2 * NS;
+  uint64_t* full_k = bars;
+  uint64_t* empty_k = bars + NK;
+  uint64_t* full_v = bars + 2 * NK;
+  uint64_t* empty_v = full_v + NV;
+  uint64_t* q_full = empty_v + NV;
   uint64_t* s_full = q_full + 1;
   uint64_t* p_half = q_full + 2;  // [2]
   uint64_t* acc_full = q_full + 4;
@@ -709,18 +788,22 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(&full_k[s], 1);
+      mbar_init(&empty_k[s], 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(&full_v[s], 1);
+      mbar_init(&empty_v[s], 1);
     }
     mbar_init(q_full, 1);
     mbar_init(s_full, 1);
-    mbar_init(&p_half[0], 256);
-    mbar_init(&p_half[1], 256);
+    mbar_init(&p_half[0], 128 * C::kNWG);
+    mbar_init(&p_half[1], 128 * C::kNWG);
     mbar_init(acc_full, 1);
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == C::kMmaWarp) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -729,7 +812,7 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == C::kProducerWarp) {
     if (lane == 0 && T > 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
@@ -738,50 +821,65 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_4d(sQ + c * C::kBox, &tm_q, q_full, c * 64, q0, h, b);
         tma_load_4d(sDO + c * C::kBox, &tm_do, q_full, c * 64, q0, h, b);
       }
-      for (int t = 0; t < T; ++t) {
-        const int s = t % NS, r = t / NS;
-        if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort_flag, p.status, 31)) break;
-        mbar_arrive_expect_tx(&full[s], 2 * C::kKVBytes);
-        uint8_t* dst = sKV + s * 2 * C::kKVBytes;
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(dst + c * C::kBox, &tm_k, &full[s], c * 64, t * BN, hk, b);
-          tma_load_4d(dst + C::kKVBytes + c * C::kBox, &tm_v, &full[s], c * 64, t * BN, hk, b);
-        }
+      bool ok = true;
+      for (int t = 0; t < T && ok; ++t) {
+        const int sk = t % NK, rk = t / NK, sv = t % NV, rv = t / NV;
+        if (rk > 0 && !(ok = mbar_wait(&empty_k[sk], (rk - 1) & 1, abort_flag, p.status, 31))) break;
+        mbar_arrive_expect_tx(&full_k[sk], C::kKVBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(sK + sk * C::kKVBytes + c * C::kBox, &tm_k, &full_k[sk], c * 64, t * BN, hk, b);
+        if (rv > 0 && !(ok = mbar_wait(&empty_v[sv], (rv - 1) & 1, abort_flag, p.status, 30))) break;
+        mbar_arrive_expect_tx(&full_v[sv], C::kKVBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(sV + sv * C::kKVBytes + c * C::kBox, &tm_v, &full_v[sv], c * 64, t * BN, hk, b);
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == C::kMmaWarp) {
     if (lane == 0 && T > 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, 0, 0);   // Q x K^T, dO x V^T
       constexpr uint32_t idesc_dq = idesc_bf16_f32(128, D, 0, 1);  // dS (TMEM) x K (MN-major)
-      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO), kv_addr = smem_u32(sKV);
+      const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
       const SDesc dq_desc = sdesc_split(q_addr, 16, 1024), ddo_desc = sdesc_split(do_addr, 16, 1024);
-      const SDesc dk_desc = sdesc_split(kv_addr, 16, 1024), dv_desc = sdesc_split(kv_addr + C::kKVBytes, 16, 1024);
-      const SDesc bk_desc = sdesc_split(kv_addr, C::kBox, 1024);
-      constexpr uint32_t kStage16 = (2 * C::kKVBytes) >> 4;
-      auto issue_scores = [&](int t) {
-        const uint32_t so = (t % NS) * kStage16;
+      const SDesc dk_desc = sdesc_split(smem_u32(sK), 16, 1024), dv_desc = sdesc_split(smem_u32(sV), 16, 1024);
+      const SDesc bk_desc = sdesc_split(smem_u32(sK), C::kBox, 1024);
+      constexpr uint32_t kSlot16 = C::kKVBytes >> 4;
+      auto s_buf = [](int t) -> uint32_t { return (t & 1) ? 384u : 128u; };
+      auto issue_s = [&](int t) {  // S(t) = Q K_t^T into its buffer
+        const uint32_t ko = (t % NK) * kSlot16;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
-          mma_ss_d(tbase + 128, dq_desc, off, dk_desc, so + off, idesc_s, k > 0);
+          mma_ss_d(tbase + s_buf(t), dq_desc, off, dk_desc, ko + off, idesc_s, k > 0);
         }
+      };
+      auto issue_dp = [&](int t) {  // dP(t) = dO V_t^T
+        const uint32_t vo = (t % NV) * kSlot16;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
-          mma_ss_d(tbase + 256, ddo_desc, off, dv_desc, so + off, idesc_s, k > 0);
+          mma_ss_d(tbase + 256, ddo_desc, off, dv_desc, vo + off, idesc_s, k > 0);
         }
-        mma_commit(s_full);
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, p.status, 32);
-      if (ok) ok = mbar_wait(&full[0], 0, abort_flag, p.status, 33);
+      if (ok) ok = mbar_wait(&full_k[0], 0, abort_flag, p.status, 33);
+      if (ok) ok = mbar_wait(&full_v[0], 0, abort_flag, p.status, 39);
       if (ok) {
         tc_fence_after();
-        issue_scores(0);
+        issue_s(0);
+        issue_dp(0);
+        mma_commit(s_full);
+        mma_commit(&empty_v[0]);
+        if (T > 1) {
+          ok = mbar_wait(&full_k[1 % NK], 0, abort_flag, p.status, 33);
+          if (ok) {
+            tc_fence_after();
+            issue_s(1);
+          }
+        }
       }
       for (int t = 0; t < T && ok; ++t) {
-        const int s = t % NS;
-        const uint32_t so = s * kStage16;
+        const uint32_t ko = (t % NK) * kSlot16;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           ok = mbar_wait(&p_half[hh], t & 1, abort_flag, p.status, 34 + hh);
@@ -789,18 +887,26 @@ __global__ void __launch_bounds__(320, 1)
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 4; ++k) {  // dQ += dS[:, keys 64hh + 16k ..] K[keys 64hh + 16k ..]
-            const uint32_t acol = 128 + 64 * hh + 32 * (k >> 1) + 8 * (k & 1);
+            const uint32_t acol = s_buf(t) + packed_col<C::kNWG>(hh, k);
             const uint32_t boff = ((64 * hh + 16 * k) * 128) >> 4;
-            mma_ts_d(tbase, tbase + acol, bk_desc, so + boff, idesc_dq, (t > 0 || hh > 0 || k > 0) ? 1u : 0u);
+            mma_ts_d(tbase, tbase + acol, bk_desc, ko + boff, idesc_dq, (t > 0 || hh > 0 || k > 0) ? 1u : 0u);
           }
         }
         if (!ok) break;
-        mma_commit(&empty[s]);
-        if (t + 1 < T) {
-          ok = mbar_wait(&full[(t + 1) % NS], ((t + 1) / NS) & 1, abort_flag, p.status, 36);
+        mma_commit(&empty_k[t % NK]);
+        if (t + 1 < T) {  // dP(t+1): the softmax has read all of dP(t)
+          ok = mbar_wait(&full_v[(t + 1) % NV], ((t + 1) / NV) & 1, abort_flag, p.status, 36);
           if (!ok) break;
           tc_fence_after();
-          issue_scores(t + 1);
+          issue_dp(t + 1);
+          mma_commit(s_full);
+          mma_commit(&empty_v[(t + 1) % NV]);
+        }
+        if (t + 2 < T) {  // S(t+2) into the buffer dQ(t) has just consumed
+          ok = mbar_wait(&full_k[(t + 2) % NK], ((t + 2) / NK) & 1, abort_flag, p.status, 38);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(t + 2);
         }
       }
       if (ok) mma_commit(acc_full);
@@ -812,7 +918,6 @@ __global__ void __launch_bounds__(320, 1)
     const int r = wq * 32 + lane;
     const int i = q0 + r;
     const uint32_t t_lane = tbase + (static_cast<uint32_t>(wq * 32) << 16);
-    const uint32_t s_col = t_lane + 128;
     const size_t srow = (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + i;  // i < Lq_pad always
     const float l2 = p.lse2[srow];
     const float dl = p.delta[srow];
@@ -824,13 +929,15 @@ __global__ void __launch_bounds__(320, 1)
       if (!ok) break;
       tc_fence_after();
       const int kb = t * BN;
+      const uint32_t s_col = t_lane + ((t & 1) ? 384u : 128u);
+      const uint32_t dp_col = t_lane + 256;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int c0 = 64 * hh + 32 * w;
-        if (__all_sync(0xffffffffu, kb + c0 + 32 <= lim))
-          dq_cols32<false>(s_col, c0, l2, dl, sl2, kb, lim);
+        const int c0 = 64 * hh + C::kCols * w;
+        if (__all_sync(0xffffffffu, kb + c0 + C::kCols <= lim))
+          dq_cols<C::kCols, false>(s_col, dp_col, c0, l2, dl, sl2, kb, lim);
         else
-          dq_cols32<true>(s_col, c0, l2, dl, sl2, kb, lim);
+          dq_cols<C::kCols, true>(s_col, dp_col, c0, l2, dl, sl2, kb, lim);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&p_half[hh]);
@@ -839,35 +946,18 @@ __global__ void __launch_bounds__(320, 1)
     if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 38));
     if (ok) {
       tc_fence_after();
-      // warpgroup w stores head-dim columns [w * D/2, (w + 1) * D/2)
+      // warpgroup w stores head-dim columns [w * D / NWG, (w + 1) * D / NWG)
+      constexpr int kPer = D / C::kNWG;
       const bool st = i < p.Lq;
       __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.dq) +
-                           ((static_cast<size_t>(b) * p.Lq + (st ? i : 0)) * p.Hq + h) * D + w * (D / 2);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t rr[32];
-        if (T > 0) {
-          tmem_ld32(t_lane + w * (D / 2) + c * 32, rr);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) rr[e] = 0u;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * p.scale, __uint_as_float(rr[2 * e + 1]) * p.scale);
-        if (st) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-        }
-      }
+                           ((static_cast<size_t>(b) * p.Lq + (st ? i : 0)) * p.Hq + h) * D + w * kPer;
+      store_cols_bf16<kPer>(t_lane + w * kPer, dst, p.scale, st, T == 0);
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
