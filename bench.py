@@ -395,8 +395,8 @@ def other_rows(args, dev, peaks):
 
 class OracleSampler:
     """The fp64 oracle's fwd+bwd on a bounded sample of the headline workload:
-    query rows (spread evenly over the sequence) of one (batch, head) slice,
-    FLOPs counted by the pages' rule over the sampled rows' valid keys."""
+    query rows (spread evenly over the sequence) of one or more (batch, head)
+    slices, FLOPs counted by the pages' rule over the sampled rows' valid keys."""
 
     def __init__(self):
         import numpy as np
@@ -404,9 +404,7 @@ class OracleSampler:
         self.np = np
         p = W.headline()
         self.p = p
-        q, k, v, do = W.make_inputs(p, seed=0)
-        sl = (slice(0, 1), slice(None), slice(0, 1))
-        self.q, self.k, self.v, self.do = q[sl], k[sl], v[sl], do[sl]
+        self.q, self.k, self.v, self.do = W.make_inputs(p, seed=0)
 
     def rows(self, n):
         n = max(1, min(int(n), self.p.Lq))
@@ -416,20 +414,35 @@ class OracleSampler:
         # causal: row i sees i + 1 keys; fwd = 4 d per (row, key) pair, fwd+bwd = 3.5x
         return 3.5 * 4.0 * self.p.d * float(self.np.sum(rows + 1))
 
-    def run(self, rows):
+    def run(self, sample):
+        """sample = (n_heads, rows): the same rows of the first n_heads (batch, head) slices."""
         import oracle
 
-        oracle.forward(self.q, self.k, self.v, causal=True, rows=rows)
-        oracle.backward(self.q, self.k, self.v, self.do, causal=True, rows=rows)
-        return self.flops(rows)
+        n_heads, rows = sample
+        fl = 0.0
+        for i in range(n_heads):
+            b, h = i % self.p.B, (i // self.p.B) % self.p.Hq
+            sl = (slice(b, b + 1), slice(None), slice(h, h + 1))
+            oracle.forward(self.q[sl], self.k[sl], self.v[sl], causal=True, rows=rows)
+            oracle.backward(self.q[sl], self.k[sl], self.v[sl], self.do[sl], causal=True, rows=rows)
+            fl += self.flops(rows)
+        return fl
 
     def calibrate(self, budget_s):
-        """Rows per sample so one sample takes about budget_s seconds."""
-        probe = self.rows(512)
+        """A sample taking about budget_s seconds: as many rows of one slice as fit, then whole slices."""
+        probe = (1, self.rows(512))
         t0 = time.perf_counter()
         self.run(probe)
-        per_row = (time.perf_counter() - t0) / len(probe)
-        return self.rows(budget_s / max(per_row, 1e-9))
+        per_row = (time.perf_counter() - t0) / len(probe[1])
+        n_rows = budget_s / max(per_row, 1e-9)
+        if n_rows <= self.p.Lq:
+            return (1, self.rows(n_rows))
+        return (int(min(self.p.B * self.p.Hq, max(1, round(n_rows / self.p.Lq)))), self.rows(self.p.Lq))
+
+    @staticmethod
+    def describe(sample):
+        n_heads, rows = sample
+        return f"{len(rows)} of 8192 query rows (evenly spaced) of {n_heads} of 32 (batch, head) slices"
 
 
 def host_cores():
@@ -439,13 +452,13 @@ def host_cores():
 def cpu_baseline_sample(budget_s: float = 15.0):
     """Oracle timed on the host cores on a ~budget_s sample (GPU arm, rank 0)."""
     smp = OracleSampler()
-    rows = smp.calibrate(budget_s)
+    sample = smp.calibrate(budget_s)
     t0 = time.perf_counter()
-    fl = smp.run(rows)
+    fl = smp.run(sample)
     dt = time.perf_counter() - t0
     return {"value": round(fl / dt / 1e12, 6), "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-            "sample": f"{len(rows)} of 8192 query rows (evenly spaced) of batch 0 head 0, B4 H8 T8192 d128 "
-                      f"causal, fwd+bwd in fp64 numpy (BLAS default threads) in {dt:.1f} s"}
+            "sample": f"{smp.describe(sample)}, B4 H8 T8192 d128 causal, fwd+bwd in fp64 numpy "
+                      f"(BLAS default threads) in {dt:.1f} s"}
 
 
 def run_reference(args):
@@ -454,17 +467,16 @@ def run_reference(args):
         return None
     smp = OracleSampler()
     budget = max(0.05, args.reference_budget_s / (args.steps + args.warmup))
-    rows = smp.calibrate(budget)
+    smp_rows = smp.calibrate(budget)
     for _ in range(args.warmup):
-        smp.run(rows)
+        smp.run(smp_rows)
     t0 = time.perf_counter()
     fl = 0.0
     for _ in range(args.steps):
-        fl += smp.run(rows)
+        fl += smp.run(smp_rows)
     dt = time.perf_counter() - t0
     value = fl / dt / 1e12
-    sample = (f"{len(rows)} of 8192 query rows (evenly spaced) of batch 0 head 0 per step, fwd+bwd in fp64 "
-              f"numpy (BLAS default threads)")
+    sample = f"{smp.describe(smp_rows)} per step, fwd+bwd in fp64 numpy (BLAS default threads)"
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 2),

@@ -77,3 +77,5 @@ def test_oracle_sampler_counts_causal_pairs():
     rows = s.rows(3)
     assert list(rows) == [0, 4095, 8191]
     assert s.flops(rows) == 3.5 * 4 * 128 * (1 + 4096 + 8192)
+    assert s.run((2, rows)) == 2 * s.flops(rows)
+    assert "2 of 32" in s.describe((2, rows))
