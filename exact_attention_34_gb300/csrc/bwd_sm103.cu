@@ -695,7 +695,7 @@ __global__ void __launch_bounds__(320, 1)
 // ============================================================================
 template <int D>
 struct DqCfg {
-  static constexpr int kNWG = 4;                // softmax warpgroups
+  static constexpr int kNWG = 2;                // softmax warpgroups
   static constexpr int kCols = 64 / kNWG;       // key columns per warpgroup per half-step
   static constexpr int kProducerWarp = 4 * kNWG, kMmaWarp = 4 * kNWG + 1;
   static constexpr int kBM = 128;               // queries per CTA
@@ -708,49 +708,58 @@ struct DqCfg {
   static constexpr int kOffK = 2 * kQBytes;
   static constexpr int kOffV = kOffK + kKSlots * kKVBytes;
   static constexpr int kOffBars = kOffV + kVSlots * kKVBytes;
-  static constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 1 + 1 + 2 + 1;
+  static constexpr int kNumBars = 2 * kKSlots + 2 * kVSlots + 1 + 3 + 2 + 1;
   static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
   static constexpr int kThreads = 32 * (4 * kNWG + 2);
 };
 
-// dS for the N key columns [c0, c0 + N) of one step (thread = query row);
-// S at s_col, dP at dp_col; packed dS goes over the first N/2 S columns read.
+// Probabilities of the N key columns [c0, c0 + N) of one step (thread =
+// query row), from S at s_col; kept in registers until dP is ready.
 template <int N, bool MASK>
-__device__ __forceinline__ void dq_cols(uint32_t s_col, uint32_t dp_col, int c0, float l2, float dl, float sl2, int kb,
-                                        int lim) {
-  uint32_t sr[N], dr[N];
-  if constexpr (N == 32) {
-    tmem_ld32_pair(s_col + c0, dp_col + c0, sr, dr);
-  } else {
-    tmem_ld16_pair(s_col + c0, dp_col + c0, sr, dr);
+__device__ __forceinline__ void dq_probs(uint32_t s_col, int c0, float l2, float sl2, int kb, int lim, float* pr) {
+  uint32_t sr[N];
+  if constexpr (N == 32)
+    tmem_ld32(s_col + c0, *reinterpret_cast<uint32_t(*)[32]>(sr));
+  else
+    tmem_ld16(s_col + c0, *reinterpret_cast<uint32_t(*)[16]>(sr));
+#pragma unroll
+  for (int c = 0; c < N; ++c) {
+    float pv = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -l2));
+    if (MASK) pv = (kb + c0 + c < lim) ? pv : 0.f;
+    pr[c] = pv;
   }
+}
+
+// dS = P (dP - delta) for the same N columns, packed over the first N/2 of
+// the S columns they came from.
+template <int N>
+__device__ __forceinline__ void dq_dscores(uint32_t s_col, uint32_t dp_col, int c0, float dl, const float* pr) {
+  uint32_t dr[N];
+  if constexpr (N == 32)
+    tmem_ld32(dp_col + c0, *reinterpret_cast<uint32_t(*)[32]>(dr));
+  else
+    tmem_ld16(dp_col + c0, *reinterpret_cast<uint32_t(*)[16]>(dr));
   uint32_t pk[N / 2];
 #pragma unroll
-  for (int i = 0; i < N / 2; ++i) {
-    float ds[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int c = 2 * i + e;
-      float pv = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -l2));
-      if (MASK) pv = (kb + c0 + c < lim) ? pv : 0.f;
-      ds[e] = pv * (__uint_as_float(dr[c]) - dl);
-    }
-    pk[i] = pack_bf16x2(ds[0], ds[1]);
-  }
+  for (int i = 0; i < N / 2; ++i)
+    pk[i] = pack_bf16x2(pr[2 * i] * (__uint_as_float(dr[2 * i]) - dl),
+                        pr[2 * i + 1] * (__uint_as_float(dr[2 * i + 1]) - dl));
   if constexpr (N == 32)
-    tmem_st16(s_col + c0, pk);
+    tmem_st16(s_col + c0, *reinterpret_cast<uint32_t(*)[16]>(pk));
   else
-    tmem_st8(s_col + c0, pk);
+    tmem_st8(s_col + c0, *reinterpret_cast<uint32_t(*)[8]>(pk));
 }
 
 // dQ kernel: CTA = (batch, head, 128 queries); thread = query row.  Each step
 // takes 128 keys (every MMA 128 x 128): S = Q K^T, dP = dO V^T, dS (bf16,
 // written back into S's columns), dQ += dS K.  TMEM: dQ [0,128), S in two
-// buffers [128,256) and [384,512) (step parity), dP [256,384).  S of step
-// t+2 is computed while the softmax warps convert step t+1, and each step runs
-// in two 64-key halves so the dQ MMAs of half 0 overlap the conversion of
-// half 1.  K tiles use a 3-slot ring (a K tile is read by S and later by dQ),
-// V tiles a 2-slot ring.
+// buffers [128,256) and [384,512) (step parity), dP [256,384).  S runs two
+// steps ahead, so the softmax warps compute the probabilities of step t+1
+// (which need only S) while dQ of step t and dP of step t+1 are on the tensor
+// core, and only the cheap dS = P (dP - delta) waits for dP.  dS is released in
+// two 64-key halves so the dQ MMAs of half 0 overlap the second half.  K tiles
+// use a 3-slot ring (a K tile is read by S and later by dQ), V tiles a 2-slot
+// ring.
 template <int D>
 __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -770,9 +779,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   uint64_t* full_v = bars + 2 * NK;
   uint64_t* empty_v = full_v + NV;
   uint64_t* q_full = empty_v + NV;
-  uint64_t* s_full = q_full + 1;
-  uint64_t* p_half = q_full + 2;  // [2]
-  uint64_t* acc_full = q_full + 4;
+  uint64_t* s_ready = q_full + 1;   // [2] S(t) computed, one barrier per S buffer (t & 1)
+  uint64_t* dp_ready = q_full + 3;  // dP(t) computed
+  uint64_t* p_half = q_full + 4;    // [2] dS(t) halves written
+  uint64_t* acc_full = q_full + 6;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -797,7 +807,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       mbar_init(&empty_v[s], 1);
     }
     mbar_init(q_full, 1);
-    mbar_init(s_full, 1);
+    mbar_init(&s_ready[0], 1);
+    mbar_init(&s_ready[1], 1);
+    mbar_init(dp_ready, 1);
     mbar_init(&p_half[0], 128 * C::kNWG);
     mbar_init(&p_half[1], 128 * C::kNWG);
     mbar_init(acc_full, 1);
@@ -852,6 +864,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
           mma_ss_d(tbase + s_buf(t), dq_desc, off, dk_desc, ko + off, idesc_s, k > 0);
         }
+        mma_commit(&s_ready[t & 1]);
       };
       auto issue_dp = [&](int t) {  // dP(t) = dO V_t^T
         const uint32_t vo = (t % NV) * kSlot16;
@@ -860,6 +873,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
           mma_ss_d(tbase + 256, ddo_desc, off, dv_desc, vo + off, idesc_s, k > 0);
         }
+        mma_commit(dp_ready);
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, p.status, 32);
       if (ok) ok = mbar_wait(&full_k[0], 0, abort_flag, p.status, 33);
@@ -868,7 +882,6 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         tc_fence_after();
         issue_s(0);
         issue_dp(0);
-        mma_commit(s_full);
         mma_commit(&empty_v[0]);
         if (T > 1) {
           ok = mbar_wait(&full_k[1 % NK], 0, abort_flag, p.status, 33);
@@ -899,7 +912,6 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           issue_dp(t + 1);
-          mma_commit(s_full);
           mma_commit(&empty_v[(t + 1) % NV]);
         }
         if (t + 2 < T) {  // S(t+2) into the buffer dQ(t) has just consumed
@@ -925,19 +937,27 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full, t & 1, abort_flag, p.status, 37));
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_ready[t & 1], (t >> 1) & 1, abort_flag, p.status, 37));
       if (!ok) break;
       tc_fence_after();
       const int kb = t * BN;
       const uint32_t s_col = t_lane + ((t & 1) ? 384u : 128u);
       const uint32_t dp_col = t_lane + 256;
+      float pr[2 * C::kCols];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int c0 = 64 * hh + C::kCols * w;
         if (__all_sync(0xffffffffu, kb + c0 + C::kCols <= lim))
-          dq_cols<C::kCols, false>(s_col, dp_col, c0, l2, dl, sl2, kb, lim);
+          dq_probs<C::kCols, false>(s_col, c0, l2, sl2, kb, lim, pr + hh * C::kCols);
         else
-          dq_cols<C::kCols, true>(s_col, dp_col, c0, l2, dl, sl2, kb, lim);
+          dq_probs<C::kCols, true>(s_col, c0, l2, sl2, kb, lim, pr + hh * C::kCols);
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(dp_ready, t & 1, abort_flag, p.status, 39));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        dq_dscores<C::kCols>(s_col, dp_col, 64 * hh + C::kCols * w, dl, pr + hh * C::kCols);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&p_half[hh]);
