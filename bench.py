@@ -490,6 +490,47 @@ def run_reference(args):
     }
 
 
+def run_sweep(args):
+    """The pages' attention grid ("Attention performance", section "Time"): B4 H8,
+    d in {64, 128}, T in {128 ... 8192} plus the ragged 600 / 1500 / 3000, causal
+    and not, bf16; fwd and fwd+bwd TFLOP/s (deterministic backward).  One JSON
+    line per case.  Also fp32 at d=128 for T <= 2048."""
+    import torch
+
+    import exact_attention_34_gb300 as ea
+    from exact_attention_34_gb300 import build as eb
+
+    eb.build()
+    dev = torch.device("cuda", 0)
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    cases = [(T, d, c, "bf16") for d in (64, 128) for T in W.GRID_T + W.RAGGED_T for c in (False, True)]
+    cases += [(T, 128, c, "fp32") for T in (128, 512, 1024, 2048) for c in (False, True)]
+    for T, d, c, dt in cases:
+        p = W.grid(T, d, c, dt)
+        g = torch.Generator(device=dev).manual_seed(0)
+        q, k, v, do = (torch.randn(p.B, T, p.Hq, d, device=dev, generator=g).to(W.DTYPES[dt]) for _ in range(4))
+        o, lse = ea.forward(q, k, v, causal=c)
+        n = max(3, min(200, int(2e12 / max(W.fwd_flops(p), 1.0))))
+        ms_f = timed(lambda: ea.forward(q, k, v, causal=c), n)
+        ms_b = timed(lambda: (ea.forward(q, k, v, causal=c), ea.backward(q, k, v, o, lse, do, causal=c)), n)
+        F = W.fwd_flops(p)
+        print(json.dumps({"T": T, "d": d, "causal": c, "dtype": dt, "fwd_ms": round(ms_f, 4),
+                          "fwd_tflops": round(F / ms_f / 1e9, 1), "fwd_bwd_ms": round(ms_b, 4),
+                          "fwd_bwd_tflops": round(3.5 * F / ms_b / 1e9, 1)}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -502,9 +543,13 @@ def main(argv=None):
                     help="seconds of oracle work for the whole --impl reference run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the other rows (KVLen+GQA, decode)")
+    ap.add_argument("--sweep", action="store_true", help="print the attention grid (one JSON line per case) and exit")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
+    if args.sweep:
+        run_sweep(args)
+        return
     rank, _, world = dist_env()
     if args.gpus != world and world > 1:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)

@@ -90,6 +90,20 @@ bool make_bshd_tmap(CUtensorMap* map, const void* base, bool bf16, int B, int L,
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
+// Opt kernel K into `bytes` of dynamic shared memory, once per device (the
+// attribute call is slow compared with a launch of a small problem).  Setting
+// it twice from racing threads is harmless.
+template <auto K>
+cudaError_t ensure_dynamic_smem(int bytes) {
+  static int done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  if (dev >= 0 && dev < 64 && done[dev] == bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = bytes;
+  return e;
+}
+
 // Opt-in per-kernel timing (attn_timing_enable): while enabled, a KernelTimer
 // around a launch records CUDA events before and after it on its stream.
 class KernelTimer {

@@ -1047,14 +1047,13 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
     kp.n_tiles = grid.x;
     if (a.deterministic) {
       using C = DkdvCfg2<D>;
-      e = cudaFuncSetAttribute(bwd_dkdv_kernel2<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+      e = ensure_dynamic_smem<bwd_dkdv_kernel2<D>>(C::kSmemBytes);
       if (e != cudaSuccess) return e;
       KernelTimer kt("bwd_dkdv", stream);
       bwd_dkdv_kernel2<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq128, tk, tv, tdo128, kp);
     } else {
       using C = DkdvCfg<D, true>;
-      e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               C::kSmemBytes);
+      e = ensure_dynamic_smem<bwd_dkdv_kernel<D, true>>(C::kSmemBytes);
       if (e != cudaSuccess) return e;
       KernelTimer kt("bwd_dkdv_atomic", stream);
       bwd_dkdv_kernel<D, true><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
@@ -1080,7 +1079,7 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
     using C = DqCfg<D>;
     dim3 grid((pb.Lq + 127) / 128, pb.Hq, pb.B);
     kp.n_tiles = grid.x;
-    e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    e = ensure_dynamic_smem<bwd_dq_kernel<D>>(C::kSmemBytes);
     if (e != cudaSuccess) return e;
     KernelTimer kt("bwd_dq", stream);
     bwd_dq_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);

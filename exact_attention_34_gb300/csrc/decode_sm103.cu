@@ -314,8 +314,7 @@ cudaError_t launch_decode_bf16_d(const DecodeArgs& a, DeviceStatus* st, cudaStre
   if (!make_q_group_tmap(&tq, a.q, pb.B, pb.Lq, pb.Hq, D, pb.G)) return cudaErrorInvalidValue;
   if (!make_bshd_tmap(&tk, a.k, true, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
   if (!make_bshd_tmap(&tv, a.v, true, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
-  cudaError_t e =
-      cudaFuncSetAttribute(decode_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  cudaError_t e = ensure_dynamic_smem<decode_bf16_kernel<D>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   DecKParams kp;
   kp.o_part = a.o_part;

@@ -331,8 +331,7 @@ cudaError_t launch_fwd_bf16_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t s
   if (!make_bshd_tmap(&tq, a.q, true, pb.B, pb.Lq, pb.Hq, D, 64, kBM)) return cudaErrorInvalidValue;
   if (!make_bshd_tmap(&tk, a.k, true, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
   if (!make_bshd_tmap(&tv, a.v, true, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes);
+  cudaError_t e = ensure_dynamic_smem<fwd_bf16_kernel<D>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   FwdKParams kp;
   kp.o = a.o;

@@ -427,7 +427,7 @@ constexpr int dq_smem() {
 
 template <int D>
 cudaError_t run_fwd(const F32FwdParams& p, int splits, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(f32_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd_smem<D>());
+  cudaError_t e = ensure_dynamic_smem<f32_fwd_kernel<D>>(fwd_smem<D>());
   if (e != cudaSuccess) return e;
   dim3 grid((p.Lq + kT - 1) / kT, p.Hq, p.B * splits);
   {
@@ -439,8 +439,7 @@ cudaError_t run_fwd(const F32FwdParams& p, int splits, cudaStream_t s) {
 
 template <int D>
 cudaError_t run_bwd(const F32BwdParams& p, bool atomic_dq, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(f32_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       dkdv_smem<D>());
+  cudaError_t e = ensure_dynamic_smem<f32_bwd_dkdv_kernel<D>>(dkdv_smem<D>());
   if (e != cudaSuccess) return e;
   dim3 g1((p.Lkv + kT - 1) / kT, p.Hkv, p.B);
   {
@@ -455,7 +454,7 @@ cudaError_t run_bwd(const F32BwdParams& p, bool atomic_dq, cudaStream_t s) {
     f32_dq_convert_kernel<<<static_cast<int>((n + 255) / 256), 256, 0, s>>>(p.dq_acc, p.dq, n, p.scale);
     return cudaGetLastError();
   }
-  e = cudaFuncSetAttribute(f32_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem<D>());
+  e = ensure_dynamic_smem<f32_bwd_dq_kernel<D>>(dq_smem<D>());
   if (e != cudaSuccess) return e;
   dim3 g2((p.Lq + kT - 1) / kT, p.Hq, p.B);
   {
