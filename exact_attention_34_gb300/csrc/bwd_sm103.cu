@@ -131,7 +131,9 @@ __global__ void __launch_bounds__(192, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
-  const int j0 = blockIdx.x * C::kBN, hk = blockIdx.y, b = blockIdx.z;
+  // grid (Hkv, B, key tiles): the key tile is the slowest launch dimension, so
+  // with causal masking the tiles that see the most queries start first.
+  const int j0 = blockIdx.z * C::kBN, hk = blockIdx.x, b = blockIdx.y;
   int kvl = p.Lkv;
   if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
   const int q_first = p.causal ? max(0, j0 + p.Lq - kvl) : 0;
@@ -515,7 +517,9 @@ __global__ void __launch_bounds__(320, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
-  const int j0 = blockIdx.x * C::kBN, hk = blockIdx.y, b = blockIdx.z;
+  // grid (Hkv, B, key tiles): the key tile is the slowest launch dimension, so
+  // with causal masking the tiles that see the most queries start first.
+  const int j0 = blockIdx.z * C::kBN, hk = blockIdx.x, b = blockIdx.y;
   int kvl = p.Lkv;
   if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
   const int q_first = p.causal ? max(0, j0 + p.Lq - kvl) : 0;
@@ -787,8 +791,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
-  const int qt = p.causal ? (p.n_tiles - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
-  const int q0 = qt * C::kBM, h = blockIdx.y, b = blockIdx.z;
+  // grid (Hq, B, query tiles), longest causal tiles first
+  const int qt = p.causal ? (p.n_tiles - 1 - static_cast<int>(blockIdx.z)) : static_cast<int>(blockIdx.z);
+  const int q0 = qt * C::kBM, h = blockIdx.x, b = blockIdx.y;
   const int hk = h / p.G;
   int kvl = p.Lkv;
   if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
@@ -1043,8 +1048,8 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
         !make_bshd_tmap(&tk, a.k, true, pb.B, pb.Lkv, pb.Hkv, D, 64, 128) ||
         !make_bshd_tmap(&tv, a.v, true, pb.B, pb.Lkv, pb.Hkv, D, 64, 128))
       return cudaErrorInvalidValue;
-    dim3 grid((pb.Lkv + 127) / 128, pb.Hkv, pb.B);
-    kp.n_tiles = grid.x;
+    dim3 grid(pb.Hkv, pb.B, (pb.Lkv + 127) / 128);
+    kp.n_tiles = grid.z;
     if (a.deterministic) {
       using C = DkdvCfg2<D>;
       e = ensure_dynamic_smem<bwd_dkdv_kernel2<D>>(C::kSmemBytes);
@@ -1077,8 +1082,8 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
         !make_bshd_tmap(&tv, a.v, true, pb.B, pb.Lkv, pb.Hkv, D, 64, 128))
       return cudaErrorInvalidValue;
     using C = DqCfg<D>;
-    dim3 grid((pb.Lq + 127) / 128, pb.Hq, pb.B);
-    kp.n_tiles = grid.x;
+    dim3 grid(pb.Hq, pb.B, (pb.Lq + 127) / 128);
+    kp.n_tiles = grid.z;
     e = ensure_dynamic_smem<bwd_dq_kernel<D>>(C::kSmemBytes);
     if (e != cudaSuccess) return e;
     KernelTimer kt("bwd_dq", stream);

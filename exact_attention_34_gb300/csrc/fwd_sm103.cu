@@ -83,8 +83,10 @@ __global__ void __launch_bounds__(320, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
-  const int qb = p.causal ? (p.n_qblocks - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
-  const int hq = blockIdx.y, b = blockIdx.z;
+  // grid (Hq, B, query blocks): the block index is the slowest launch dimension,
+  // so with causal masking the longest blocks of every head start first.
+  const int qb = p.causal ? (p.n_qblocks - 1 - static_cast<int>(blockIdx.z)) : static_cast<int>(blockIdx.z);
+  const int hq = blockIdx.x, b = blockIdx.y;
   const int hkv = hq / p.G;
   int kvl = p.Lkv;
   if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
@@ -346,7 +348,7 @@ cudaError_t launch_fwd_bf16_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t s
   kp.n_qblocks = (pb.Lq + 2 * kBM - 1) / (2 * kBM);
   kp.scale_log2 = pb.scale * kLog2e;
   kp.status = st;
-  dim3 grid(kp.n_qblocks, pb.Hq, pb.B);
+  dim3 grid(pb.Hq, pb.B, kp.n_qblocks);
   {
     KernelTimer kt("fwd", stream);
     fwd_bf16_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
