@@ -80,36 +80,40 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16* ds
 }
 
 // ============================================================================
-// dK / dV kernel
+// dK / dV kernel with atomic dQ (single-pass backward)
 // ============================================================================
-template <int D, bool ATOMIC>
-struct DkdvCfg {
+// 64-query steps with one TMEM stage: dK [0,128) dV [128,256) S^T [256,320)
+// dP^T [320,384) dQ^T [384,448).  The softmax warps write dS^T to TMEM (A of
+// dK += dS^T Q) and to swizzled shared memory (B of dQ^T = K^T dS^T), then read
+// dQ^T out (thread = head-dim column) and reduce it into the float32 buffer.
+template <int D>
+struct DkdvAtomicCfg {
   static constexpr int kBN = 128;                    // keys per CTA
   static constexpr int kBM = 64;                     // queries per step
   static constexpr int kKVBytes = kBN * D * 2;       // K or V tile
   static constexpr int kKBox = kBN * 128;            // one 64-column box of K/V
   static constexpr int kQBytes = kBM * D * 2;        // Q_i or dO_i tile
   static constexpr int kQBox = kBM * 128;            // one 64-column box of Q/dO
-  static constexpr int kStages = ATOMIC ? 3 : 4;     // shared-memory ring of (Q, dO, lse2, delta)
-  static constexpr int kTStages = ATOMIC ? 1 : 2;    // TMEM stages of (S^T, dP^T)
+  static constexpr int kStages = 3;                  // shared-memory ring of (Q, dO, lse2, delta)
+  static constexpr int kTStages = 1;                 // TMEM stages of (S^T, dP^T)
   static constexpr int kOffV = kKVBytes;
   static constexpr int kOffQ = 2 * kKVBytes;
   static constexpr int kOffDS = kOffQ + kStages * 2 * kQBytes;
-  static constexpr int kOffStat = kOffDS + (ATOMIC ? kBN * kBM * 2 : 0);
+  static constexpr int kOffStat = kOffDS + kBN * kBM * 2;
   static constexpr int kOffBars = kOffStat + kStages * 2 * kBM * 4;
   static constexpr int kNumBars = 2 * kStages + 1 + 2 * kTStages + 3;
   static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
   static constexpr int kThreads = 192;
   static constexpr uint32_t kColS = 256;   // first stage's S^T column
-  static constexpr uint32_t kColDQ = 384;  // dQ^T (single pass)
+  static constexpr uint32_t kColDQ = 384;  // dQ^T
 };
 
-template <int D, bool ATOMIC>
+template <int D>
 __global__ void __launch_bounds__(192, 1)
-    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    bwd_dkdv_atomic_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const BwdKParams p) {
-  using C = DkdvCfg<D, ATOMIC>;
+  using C = DkdvAtomicCfg<D>;
   constexpr int NS = C::kStages, TS = C::kTStages, BM = C::kBM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -244,7 +248,7 @@ __global__ void __launch_bounds__(192, 1)
           mma_ts(tbase + 0, col + 64 + k * 8, sdesc_sw128(qa + k * 2048, C::kQBox, 1024), idesc_acc,
                  (t > 0 || k > 0) ? 1u : 0u);
         }
-        if constexpr (ATOMIC) {
+        {
           if (t > 0) {
             ok = mbar_wait(dq_free, (t - 1) & 1, abort_flag, p.status, 25);
             if (!ok) break;
@@ -324,7 +328,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       tmem_st32(col, pk);
       tmem_st32(col + 64, dk);
-      if constexpr (ATOMIC) {
+      {
         // dS^T row r -> shared memory, 128B-swizzled (MN-major operand of dQ^T)
         uint8_t* row = sDS + r * 128;
 #pragma unroll
@@ -336,7 +340,7 @@ __global__ void __launch_bounds__(192, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full[ts]);
-      if constexpr (ATOMIC) {
+      {
         ok = __all_sync(0xffffffffu, mbar_wait(dq_full, t & 1, abort_flag, p.status, 28));
         if (!ok) break;
         tc_fence_after();
@@ -1057,11 +1061,11 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
       KernelTimer kt("bwd_dkdv", stream);
       bwd_dkdv_kernel2<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq128, tk, tv, tdo128, kp);
     } else {
-      using C = DkdvCfg<D, true>;
-      e = ensure_dynamic_smem<bwd_dkdv_kernel<D, true>>(C::kSmemBytes);
+      using C = DkdvAtomicCfg<D>;
+      e = ensure_dynamic_smem<bwd_dkdv_atomic_kernel<D>>(C::kSmemBytes);
       if (e != cudaSuccess) return e;
       KernelTimer kt("bwd_dkdv_atomic", stream);
-      bwd_dkdv_kernel<D, true><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+      bwd_dkdv_atomic_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
