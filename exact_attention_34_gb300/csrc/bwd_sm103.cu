@@ -80,307 +80,6 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16* ds
 }
 
 // ============================================================================
-// dK / dV kernel with atomic dQ (single-pass backward)
-// ============================================================================
-// 64-query steps with one TMEM stage: dK [0,128) dV [128,256) S^T [256,320)
-// dP^T [320,384) dQ^T [384,448).  The softmax warps write dS^T to TMEM (A of
-// dK += dS^T Q) and to swizzled shared memory (B of dQ^T = K^T dS^T), then read
-// dQ^T out (thread = head-dim column) and reduce it into the float32 buffer.
-template <int D>
-struct DkdvAtomicCfg {
-  static constexpr int kBN = 128;                    // keys per CTA
-  static constexpr int kBM = 64;                     // queries per step
-  static constexpr int kKVBytes = kBN * D * 2;       // K or V tile
-  static constexpr int kKBox = kBN * 128;            // one 64-column box of K/V
-  static constexpr int kQBytes = kBM * D * 2;        // Q_i or dO_i tile
-  static constexpr int kQBox = kBM * 128;            // one 64-column box of Q/dO
-  static constexpr int kStages = 3;                  // shared-memory ring of (Q, dO, lse2, delta)
-  static constexpr int kTStages = 1;                 // TMEM stages of (S^T, dP^T)
-  static constexpr int kOffV = kKVBytes;
-  static constexpr int kOffQ = 2 * kKVBytes;
-  static constexpr int kOffDS = kOffQ + kStages * 2 * kQBytes;
-  static constexpr int kOffStat = kOffDS + kBN * kBM * 2;
-  static constexpr int kOffBars = kOffStat + kStages * 2 * kBM * 4;
-  static constexpr int kNumBars = 2 * kStages + 1 + 2 * kTStages + 3;
-  static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
-  static constexpr int kThreads = 192;
-  static constexpr uint32_t kColS = 256;   // first stage's S^T column
-  static constexpr uint32_t kColDQ = 384;  // dQ^T
-};
-
-template <int D>
-__global__ void __launch_bounds__(192, 1)
-    bwd_dkdv_atomic_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const BwdKParams p) {
-  using C = DkdvAtomicCfg<D>;
-  constexpr int NS = C::kStages, TS = C::kTStages, BM = C::kBM;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint8_t* sK = smem;
-  uint8_t* sV = smem + C::kOffV;
-  uint8_t* sQ = smem + C::kOffQ;  // stage s: Q at s * 2 * kQBytes, dO right after
-  uint8_t* sDS = smem + C::kOffDS;
-  float* sStat = reinterpret_cast<float*>(smem + C::kOffStat);  // stage s: lse2[64], delta[64]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + NS;
-  uint64_t* kv_full = bars + 2 * NS;
-  uint64_t* s_full = kv_full + 1;       // [TS]
-  uint64_t* p_full = s_full + TS;       // [TS]
-  uint64_t* acc_full = p_full + TS;
-  uint64_t* dq_full = acc_full + 1;
-  uint64_t* dq_free = acc_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = warp_id(), lane = lane_id();
-  // grid (Hkv, B, key tiles): the key tile is the slowest launch dimension, so
-  // with causal masking the tiles that see the most queries start first.
-  const int j0 = blockIdx.z * C::kBN, hk = blockIdx.x, b = blockIdx.y;
-  int kvl = p.Lkv;
-  if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
-  const int q_first = p.causal ? max(0, j0 + p.Lq - kvl) : 0;
-  const int i_begin = q_first / BM;
-  const int n_qt = (p.Lq + BM - 1) / BM;
-  const int steps_per_head = (j0 < kvl && i_begin < n_qt) ? n_qt - i_begin : 0;
-  const int T = steps_per_head * p.G;
-
-  if (threadIdx.x == 0) {
-    *abort_flag = 0;
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    mbar_init(kv_full, 1);
-    for (int s = 0; s < TS; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 128);
-    }
-    mbar_init(acc_full, 1);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_free, 128);
-    fence_barrier_init();
-  }
-  if (warp == 5) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tbase = *tmem_slot;
-
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0 && T > 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(kv_full, 2 * C::kKVBytes);
-      for (int h = 0; h < D / 64; ++h) {
-        tma_load_4d(sK + h * C::kKBox, &tm_k, kv_full, h * 64, j0, hk, b);
-        tma_load_4d(sV + h * C::kKBox, &tm_v, kv_full, h * 64, j0, hk, b);
-      }
-      for (int t = 0; t < T; ++t) {
-        const int s = t % NS, r = t / NS;
-        if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort_flag, p.status, 21)) break;
-        const int h = hk * p.G + t / steps_per_head;
-        const int q0 = (i_begin + t % steps_per_head) * BM;
-        mbar_arrive_expect_tx(&full[s], 2 * C::kQBytes + 2 * BM * 4);
-        uint8_t* q_dst = sQ + s * 2 * C::kQBytes;
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(q_dst + c * C::kQBox, &tm_q, &full[s], c * 64, q0, h, b);
-          tma_load_4d(q_dst + C::kQBytes + c * C::kQBox, &tm_do, &full[s], c * 64, q0, h, b);
-        }
-        const size_t row = (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + q0;
-        bulk_load(sStat + s * 2 * BM, p.lse2 + row, BM * 4, &full[s]);
-        bulk_load(sStat + s * 2 * BM + BM, p.delta + row, BM * 4, &full[s]);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && T > 0) {
-      constexpr uint32_t idesc_st = idesc_bf16_f32(128, BM, 0, 0);  // K x Q^T
-      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, 0, 1);  // P^T (TMEM) x dO (MN-major)
-      constexpr uint32_t idesc_dq = idesc_bf16_f32(128, BM, 1, 1);  // K^T (MN-major) x dS^T (MN-major)
-      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ);
-      const uint32_t ds_addr = smem_u32(sDS);
-      auto issue_scores = [&](int t) {
-        const int s = t % NS, ts = t % TS;
-        const uint32_t qa = q_addr + s * 2 * C::kQBytes, da = qa + C::kQBytes;
-        const uint32_t col = tbase + C::kColS + ts * 128;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t ko = (k >> 2) * C::kKBox + (k & 3) * 32;
-          const uint32_t qo = (k >> 2) * C::kQBox + (k & 3) * 32;
-          mma_ss(col, sdesc_sw128(k_addr + ko, 16, 1024), sdesc_sw128(qa + qo, 16, 1024), idesc_st, k > 0);
-        }
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t ko = (k >> 2) * C::kKBox + (k & 3) * 32;
-          const uint32_t qo = (k >> 2) * C::kQBox + (k & 3) * 32;
-          mma_ss(col + 64, sdesc_sw128(v_addr + ko, 16, 1024), sdesc_sw128(da + qo, 16, 1024), idesc_st, k > 0);
-        }
-        mma_commit(&s_full[ts]);
-      };
-      bool ok = mbar_wait(kv_full, 0, abort_flag, p.status, 22);
-      for (int t = 0; t < TS && t < T && ok; ++t) {
-        ok = mbar_wait(&full[t % NS], (t / NS) & 1, abort_flag, p.status, 23);
-        if (!ok) break;
-        tc_fence_after();
-        issue_scores(t);
-      }
-      for (int t = 0; t < T && ok; ++t) {
-        const int s = t % NS, ts = t % TS;
-        ok = mbar_wait(&p_full[ts], (t / TS) & 1, abort_flag, p.status, 24);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t qa = q_addr + s * 2 * C::kQBytes, da = qa + C::kQBytes;
-        const uint32_t col = tbase + C::kColS + ts * 128;
-#pragma unroll
-        for (int k = 0; k < BM / 16; ++k) {  // dV += P^T dO
-          mma_ts(tbase + 128, col + k * 8, sdesc_sw128(da + k * 2048, C::kQBox, 1024), idesc_acc,
-                 (t > 0 || k > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int k = 0; k < BM / 16; ++k) {  // dK += dS^T Q
-          mma_ts(tbase + 0, col + 64 + k * 8, sdesc_sw128(qa + k * 2048, C::kQBox, 1024), idesc_acc,
-                 (t > 0 || k > 0) ? 1u : 0u);
-        }
-        {
-          if (t > 0) {
-            ok = mbar_wait(dq_free, (t - 1) & 1, abort_flag, p.status, 25);
-            if (!ok) break;
-            tc_fence_after();
-          }
-          // dQ^T = K^T dS^T : M = head dim (the second 64-row block repeats the
-          // first when D = 64), N = 64 queries, K = 128 keys.
-          constexpr uint32_t lbo_k = (D == 128) ? static_cast<uint32_t>(C::kKBox) : 0u;
-#pragma unroll
-          for (int k = 0; k < C::kBN / 16; ++k) {
-            mma_ss(tbase + C::kColDQ, sdesc_sw128(k_addr + k * 2048, lbo_k, 1024),
-                   sdesc_sw128(ds_addr + k * 2048, 16, 1024), idesc_dq, k > 0);
-          }
-          mma_commit(dq_full);
-        }
-        mma_commit(&empty[s]);
-        if (t + TS < T) {
-          const int tn = t + TS;
-          ok = mbar_wait(&full[tn % NS], (tn / NS) & 1, abort_flag, p.status, 26);
-          if (!ok) break;
-          tc_fence_after();
-          issue_scores(tn);
-        }
-      }
-      if (ok) mma_commit(acc_full);
-    }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------------------ softmax (thread = key row)
-    const int r = warp * 32 + lane;
-    const int j = j0 + r;
-    const uint32_t t_lane = tbase + (static_cast<uint32_t>(warp * 32) << 16);
-    const bool key_ok = j < kvl;
-    const int q_min = p.causal ? j + p.Lq - kvl : -0x7fffffff;  // first query that sees key j
-    const float sl2 = p.scale_log2;
-    bool ok = true;
-    for (int t = 0; t < T; ++t) {
-      const int s = t % NS, ts = t % TS;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[ts], (t / TS) & 1, abort_flag, p.status, 27));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t col = t_lane + C::kColS + ts * 128;
-      const int q0 = (i_begin + t % steps_per_head) * BM;
-      const float* lse2 = sStat + s * 2 * BM;
-      const float* dlt = lse2 + BM;
-      uint32_t sr[64], dr[64];
-      {
-        uint32_t a[32];
-        tmem_ld32(col, a);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sr[i] = a[i];
-        tmem_ld32(col + 32, a);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sr[32 + i] = a[i];
-        tmem_ld32(col + 64, a);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) dr[i] = a[i];
-        tmem_ld32(col + 96, a);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) dr[32 + i] = a[i];
-      }
-      const bool all_valid = key_ok && q0 >= q_min;
-      uint32_t pk[32], dk[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float pr[2], ds[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int c = 2 * i + e;
-          const bool valid = all_valid || (key_ok && q0 + c >= q_min);
-          const float pv = valid ? ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2[c])) : 0.f;
-          pr[e] = pv;
-          ds[e] = pv * (__uint_as_float(dr[c]) - dlt[c]);
-        }
-        pk[i] = pack_bf16x2(pr[0], pr[1]);
-        dk[i] = pack_bf16x2(ds[0], ds[1]);
-      }
-      tmem_st32(col, pk);
-      tmem_st32(col + 64, dk);
-      {
-        // dS^T row r -> shared memory, 128B-swizzled (MN-major operand of dQ^T)
-        uint8_t* row = sDS + r * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) * 16)) =
-              make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
-        fence_proxy_async_smem();
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&p_full[ts]);
-      {
-        ok = __all_sync(0xffffffffu, mbar_wait(dq_full, t & 1, abort_flag, p.status, 28));
-        if (!ok) break;
-        tc_fence_after();
-        if (r < D) {  // thread = head-dim column d = r; columns = the 64 queries
-          const int h = hk * p.G + t / steps_per_head;
-          uint32_t a[32];
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            tmem_ld32(t_lane + C::kColDQ + half * 32, a);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int q = q0 + half * 32 + i;
-              if (q < p.Lq)
-                atomicAdd(p.dq_acc + ((static_cast<size_t>(b) * p.Lq + q) * p.Hq + h) * D + r, __uint_as_float(a[i]));
-            }
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(dq_free);
-      }
-    }
-    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 29));
-    if (ok) {
-      tc_fence_after();
-      const bool st = j < p.Lkv;
-      const size_t off = ((static_cast<size_t>(b) * p.Lkv + (st ? j : 0)) * p.Hkv + hk) * D;
-      store_row_bf16<D>(t_lane + 0, reinterpret_cast<__nv_bfloat16*>(p.dk) + off, p.scale, st, T == 0);
-      store_row_bf16<D>(t_lane + 128, reinterpret_cast<__nv_bfloat16*>(p.dv) + off, 1.0f, st, T == 0);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 5) {
-    tc_fence_after();
-    tmem_dealloc(tbase, 512);
-  }
-}
-
-// ============================================================================
 // dK / dV kernel, deterministic two-pass variant
 // ============================================================================
 // CTA = (batch, KV head, 128 keys); thread = key row = TMEM lane.  Each step
@@ -679,6 +378,302 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive(ds_ready);
     }
     if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 68));
+    if (ok) {
+      tc_fence_after();
+      const bool st = j < p.Lkv;
+      const size_t off = ((static_cast<size_t>(b) * p.Lkv + (st ? j : 0)) * p.Hkv + hk) * D;
+      if (w == 0)
+        store_row_bf16<D>(t_lane + 0, reinterpret_cast<__nv_bfloat16*>(p.dk) + off, p.scale, st, T == 0);
+      else
+        store_row_bf16<D>(t_lane + 128, reinterpret_cast<__nv_bfloat16*>(p.dv) + off, 1.0f, st, T == 0);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+// ============================================================================
+// dK / dV kernel with atomic dQ (single-pass backward)
+// ============================================================================
+// CTA = (batch, KV head, 128 keys); thread = key row = TMEM lane; 128-query
+// steps, every MMA 128 x 128 x 16.  Five GEMMs per step instead of the
+// two-pass backward's seven:
+//   tensor pipe:  S^T | dP^T | dV += P^T dO | dK += dS^T Q | dQ^T = K^T dS^T | S^T(t+1) | dP^T(t+1) ...
+//   softmax:          | P^T  | dS^T        |               | dQ^T -> fp32 buffer (atomic adds)
+// TMEM: dK [0,128) dV [128,256) S^T [256,384) dP^T [384,512); dQ^T reuses the
+// dP^T columns once the softmax has read them, and dP^T(t+1) waits until the
+// softmax has reduced dQ^T(t) out.  P^T goes back to TMEM (A of dV); dS^T goes
+// to 128B-swizzled shared memory, where it is the K-major A of dK and the
+// MN-major B of dQ^T.  For head_dim 64 the M = 128 rows of dQ^T repeat the 64
+// head-dim rows (the second A block points at the first) and only the first
+// 64 lanes are read out.  The summation order of dQ over key tiles is not
+// fixed, so this variant is not bitwise reproducible.
+template <int D>
+struct DkdvAtomicCfg {
+  static constexpr int kBN = 128, kBM = 128;
+  static constexpr int kKVBytes = kBN * D * 2;
+  static constexpr int kBox = 128 * 128;      // one 64-column box of a 128-row tile
+  static constexpr int kQBytes = kBM * D * 2;
+  static constexpr int kStages = 2;
+  static constexpr int kOffV = kKVBytes;
+  static constexpr int kOffQ = 2 * kKVBytes;  // stage s: Q at s * 2 * kQBytes, dO right after
+  static constexpr int kOffDS = kOffQ + kStages * 2 * kQBytes;
+  static constexpr int kOffStat = kOffDS + kBN * kBM * 2;
+  static constexpr int kOffBars = kOffStat + kStages * 2 * kBM * 4;
+  static constexpr int kNumBars = 2 * kStages + 1 + 7;
+  // No alignment slack: the dynamic shared window starts right after the
+  // 1 KB the system reserves per block, which is 1024-aligned (checked at run
+  // time; a misaligned base makes the kernel report and do nothing).
+  static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16;
+  static constexpr int kThreads = 320;
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    bwd_dkdv_atomic_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                           const BwdKParams p) {
+  using C = DkdvAtomicCfg<D>;
+  constexpr int NS = C::kStages, BM = C::kBM;
+  constexpr uint32_t kColS = 256, kColDP = 384;
+  extern __shared__ uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {  // never expected: see kSmemBytes
+    if (threadIdx.x == 0) report_status(p.status, 2, 99);
+    return;
+  }
+  uint8_t* smem = smem_raw;
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::kOffV;
+  uint8_t* sQ = smem + C::kOffQ;
+  uint8_t* sDS = smem + C::kOffDS;
+  float* sStat = reinterpret_cast<float*>(smem + C::kOffStat);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + NS;
+  uint64_t* kv_full = bars + 2 * NS;
+  uint64_t* s_ready = kv_full + 1;   // S^T(t) computed
+  uint64_t* dp_ready = kv_full + 2;  // dP^T(t) computed
+  uint64_t* p_ready = kv_full + 3;   // P^T(t) in TMEM (256 arrivals)
+  uint64_t* ds_ready = kv_full + 4;  // dS^T(t) in shared memory (256 arrivals)
+  uint64_t* dq_ready = kv_full + 5;  // dQ^T(t) computed
+  uint64_t* dq_free = kv_full + 6;   // dQ^T(t) reduced out (256 arrivals)
+  uint64_t* acc_full = kv_full + 7;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  const int j0 = blockIdx.z * C::kBN, hk = blockIdx.x, b = blockIdx.y;
+  int kvl = p.Lkv;
+  if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
+  const int q_first = p.causal ? max(0, j0 + p.Lq - kvl) : 0;
+  const int i_begin = q_first / BM;
+  const int n_qt = (p.Lq + BM - 1) / BM;
+  const int steps_per_head = (j0 < kvl && i_begin < n_qt) ? n_qt - i_begin : 0;
+  const int T = steps_per_head * p.G;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(kv_full, 1);
+    mbar_init(s_ready, 1);
+    mbar_init(dp_ready, 1);
+    mbar_init(p_ready, 256);
+    mbar_init(ds_ready, 256);
+    mbar_init(dq_ready, 1);
+    mbar_init(dq_free, 256);
+    mbar_init(acc_full, 1);
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 8) {
+    if (lane == 0 && T > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(kv_full, 2 * C::kKVBytes);
+      for (int h = 0; h < D / 64; ++h) {
+        tma_load_4d(sK + h * C::kBox, &tm_k, kv_full, h * 64, j0, hk, b);
+        tma_load_4d(sV + h * C::kBox, &tm_v, kv_full, h * 64, j0, hk, b);
+      }
+      for (int t = 0; t < T; ++t) {
+        const int s = t % NS, r = t / NS;
+        if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort_flag, p.status, 71)) break;
+        const int h = hk * p.G + t / steps_per_head;
+        const int q0 = (i_begin + t % steps_per_head) * BM;
+        mbar_arrive_expect_tx(&full[s], 2 * C::kQBytes + 2 * BM * 4);
+        uint8_t* q_dst = sQ + s * 2 * C::kQBytes;
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_4d(q_dst + c * C::kBox, &tm_q, &full[s], c * 64, q0, h, b);
+          tma_load_4d(q_dst + C::kQBytes + c * C::kBox, &tm_do, &full[s], c * 64, q0, h, b);
+        }
+        const size_t row = (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + q0;
+        bulk_load(sStat + s * 2 * BM, p.lse2 + row, BM * 4, &full[s]);
+        bulk_load(sStat + s * 2 * BM + BM, p.delta + row, BM * 4, &full[s]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    if (lane == 0 && T > 0) {
+      constexpr uint32_t idesc_st = idesc_bf16_f32(128, BM, 0, 0);   // K x Q^T, V x dO^T
+      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, 0, 1);   // A (K-major or TMEM) x (dO|Q MN-major)
+      constexpr uint32_t idesc_dq = idesc_bf16_f32(128, BM, 1, 1);   // K^T (MN-major) x dS^T (MN-major)
+      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ), ds_addr = smem_u32(sDS);
+      const SDesc dk_base = sdesc_split(k_addr, 16, 1024), dv_base = sdesc_split(v_addr, 16, 1024);
+      const SDesc dq_base = sdesc_split(q_addr, 16, 1024), ddo_base = sdesc_split(q_addr + C::kQBytes, 16, 1024);
+      const SDesc bq_base = sdesc_split(q_addr, C::kBox, 1024), bdo_base = sdesc_split(q_addr + C::kQBytes, C::kBox, 1024);
+      const SDesc ads = sdesc_split(ds_addr, 16, 1024);              // dS^T as K-major A (keys x queries)
+      const SDesc bds = sdesc_split(ds_addr, C::kBox, 1024);         // dS^T as MN-major B (keys x queries)
+      const SDesc akt = sdesc_split(k_addr, D == 128 ? C::kBox : 0, 1024);  // K^T as MN-major A (d x keys)
+      constexpr uint32_t kStage16 = (2 * C::kQBytes) >> 4;
+      auto issue_s = [&](int t) {
+        const uint32_t so = (t % NS) * kStage16;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
+          mma_ss_d(tbase + kColS, dk_base, off, dq_base, so + off, idesc_st, k > 0);
+        }
+        mma_commit(s_ready);
+      };
+      auto issue_dp = [&](int t) {
+        const uint32_t so = (t % NS) * kStage16;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
+          mma_ss_d(tbase + kColDP, dv_base, off, ddo_base, so + off, idesc_st, k > 0);
+        }
+        mma_commit(dp_ready);
+      };
+      bool ok = mbar_wait(kv_full, 0, abort_flag, p.status, 72);
+      if (ok) ok = mbar_wait(&full[0], 0, abort_flag, p.status, 73);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int t = 0; t < T && ok; ++t) {
+        const uint32_t so = (t % NS) * kStage16;
+        ok = mbar_wait(p_ready, t & 1, abort_flag, p.status, 74);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // dV += P^T dO ; query k-step k of warpgroup k/4 is packed at 64(k/4) + 8(k%4)
+          const uint32_t acol = 64 * (k >> 2) + 8 * (k & 3);
+          mma_ts_d(tbase + 128, tbase + kColS + acol, bdo_base, so + ((16 * k * 128) >> 4), idesc_acc,
+                   (t > 0 || k > 0) ? 1u : 0u);
+        }
+        ok = mbar_wait(ds_ready, t & 1, abort_flag, p.status, 75);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // dK += dS^T Q (dS^T from shared memory)
+          const uint32_t aoff = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
+          mma_ss_d(tbase + 0, ads, aoff, bq_base, so + ((16 * k * 128) >> 4), idesc_acc, (t > 0 || k > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // dQ^T = K^T dS^T (dQ^T(t-1) was read out before dP^T(t) was issued)
+          const uint32_t off = (16 * k * 128) >> 4;
+          mma_ss_d(tbase + kColDP, akt, off, bds, off, idesc_dq, k > 0);
+        }
+        mma_commit(dq_ready);
+        mma_commit(&empty[t % NS]);
+        if (t + 1 < T) {
+          ok = mbar_wait(&full[(t + 1) % NS], ((t + 1) / NS) & 1, abort_flag, p.status, 77);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(t + 1);
+          ok = mbar_wait(dq_free, t & 1, abort_flag, p.status, 78);
+          if (!ok) break;
+          tc_fence_after();
+          issue_dp(t + 1);
+        }
+      }
+      if (ok) mma_commit(acc_full);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax (thread = key row)
+    const int w = warp >> 2, wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const int j = j0 + r;
+    const uint32_t t_lane = tbase + (static_cast<uint32_t>(wq * 32) << 16);
+    const bool key_ok = j < kvl;
+    const int q_min = p.causal ? j + p.Lq - kvl : -0x7fffffff;
+    const float sl2 = p.scale_log2;
+    const int c0 = 64 * w;
+    uint8_t* ds_row = sDS + w * C::kBox + r * 128;
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int s = t % NS;
+      ok = __all_sync(0xffffffffu, mbar_wait(s_ready, t & 1, abort_flag, p.status, 79));
+      if (!ok) break;
+      tc_fence_after();
+      const int h = hk * p.G + t / steps_per_head;
+      const int q0 = (i_begin + t % steps_per_head) * BM;
+      const float* lse2 = sStat + s * 2 * BM;
+      const float* dlt = lse2 + BM;
+      float pr[64];
+      if (__all_sync(0xffffffffu, key_ok && q0 + c0 >= q_min))
+        dkdv_probs<false>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, q_min, pr);
+      else
+        dkdv_probs<true>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, q_min, pr);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_ready);
+      ok = __all_sync(0xffffffffu, mbar_wait(dp_ready, t & 1, abort_flag, p.status, 80));
+      if (!ok) break;
+      tc_fence_after();
+      {  // dS^T = P^T (dP^T - delta) -> 128B-swizzled shared memory (this row, this warpgroup's 64 queries)
+        uint32_t da[32], db[32];
+        tmem_ld32_pair(t_lane + kColDP + c0, t_lane + kColDP + c0 + 32, da, db);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 8 * ch + 2 * e;
+            const float4 d4 = *reinterpret_cast<const float4*>(dlt + c0 + (c & ~3));
+            const float dv0 = (c & 3) ? d4.z : d4.x, dv1 = (c & 3) ? d4.w : d4.y;
+            const uint32_t r0 = c < 32 ? da[c] : db[c - 32], r1 = c + 1 < 32 ? da[c + 1] : db[c + 1 - 32];
+            pk[e] = pack_bf16x2(pr[c] * (__uint_as_float(r0) - dv0), pr[c + 1] * (__uint_as_float(r1) - dv1));
+          }
+          *reinterpret_cast<uint4*>(ds_row + ((ch ^ (r & 7)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(ds_ready);
+      ok = __all_sync(0xffffffffu, mbar_wait(dq_ready, t & 1, abort_flag, p.status, 81));
+      if (!ok) break;
+      tc_fence_after();
+      if (r < D) {  // thread = head-dim column d = r; warpgroup w reduces queries [64w, 64w + 64)
+        uint32_t qa[32], qb[32];
+        tmem_ld32_pair(t_lane + kColDP + c0, t_lane + kColDP + c0 + 32, qa, qb);
+        float* dst = p.dq_acc + ((static_cast<size_t>(b) * p.Lq + q0 + c0) * p.Hq + h) * D + r;
+        const size_t qstride = static_cast<size_t>(p.Hq) * D;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          if (q0 + c0 + c < p.Lq) atomicAdd(dst + c * qstride, __uint_as_float(c < 32 ? qa[c] : qb[c - 32]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(dq_free);
+    }
+    if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 82));
     if (ok) {
       tc_fence_after();
       const bool st = j < p.Lkv;
@@ -1065,7 +1060,7 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
       e = ensure_dynamic_smem<bwd_dkdv_atomic_kernel<D>>(C::kSmemBytes);
       if (e != cudaSuccess) return e;
       KernelTimer kt("bwd_dkdv_atomic", stream);
-      bwd_dkdv_atomic_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+      bwd_dkdv_atomic_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq128, tk, tv, tdo128, kp);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

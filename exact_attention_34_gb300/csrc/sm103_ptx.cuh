@@ -30,12 +30,16 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-__device__ __forceinline__ void report_timeout(DeviceStatus* st, int site) {
-  if (st != nullptr && atomicCAS(&st->code, 0, 1) == 0) {
+// Device status codes: 1 = a pipeline wait ran out of time, 2 = the dynamic
+// shared-memory window was not 1024-byte aligned (the kernel did nothing).
+__device__ __forceinline__ void report_status(DeviceStatus* st, int code, int site) {
+  if (st != nullptr && atomicCAS(&st->code, 0, code) == 0) {
     st->site = site;
     st->block = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
   }
 }
+
+__device__ __forceinline__ void report_timeout(DeviceStatus* st, int site) { report_status(st, 1, site); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -152,8 +152,9 @@ size_t attn_decode_workspace_size(int B, int Lq, int Hq, int d, int num_splits);
 
 /*
  * Device-side status of the current device: kernels never trap; a pipeline
- * wait that runs out of time (2 s) records a code and a site here and the
- * kernel ends early.  Synchronises the device.  Writes code/site (host
+ * wait that runs out of time (2 s) records code 1 and a site here and the
+ * kernel ends early; a kernel that finds its shared-memory window misaligned
+ * records code 2 and does nothing.  Synchronises the device.  Writes code/site (host
  * pointers, nullable) and clears the status when reset != 0.  Returns
  * ATTN_ERR_DEVICE when a code was set, ATTN_OK otherwise.
  */

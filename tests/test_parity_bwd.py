@@ -62,10 +62,16 @@ def test_atomic_variant(dtype):
     run_bwd(W.Problem(2, 600, 600, 4, 2, 128, dtype, True, None, "bwd_atomic"), deterministic=False)
 
 
+@pytest.mark.parametrize("T,d,causal", CASES)
+def test_atomic_small_grid(T, d, causal):
+    run_bwd(W.Problem(2, T, T, 2, 2, d, "bf16", causal, None, f"atomic_T{T}_d{d}_c{int(causal)}"), False)
+
+
+@pytest.mark.parametrize("deterministic", [True, False])
 @pytest.mark.parametrize("Lq,Lkv,causal", [(300, 1000, True), (1000, 300, True), (257, 700, False)])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-def test_lq_ne_lkv(Lq, Lkv, causal, dtype):
-    run_bwd(W.Problem(2, Lq, Lkv, 4, 2, 128, dtype, causal, None, "bwd_lq_ne_lkv"))
+def test_lq_ne_lkv(Lq, Lkv, causal, dtype, deterministic):
+    run_bwd(W.Problem(2, Lq, Lkv, 4, 2, 128, dtype, causal, None, "bwd_lq_ne_lkv"), deterministic)
 
 
 @pytest.mark.parametrize("deterministic", [True, False])
@@ -105,10 +111,11 @@ def test_preprocess(dtype, d):
     assert rel_err(to_np(delta), ref) <= 1e-5
 
 
-def test_headline_full_size_one_head():
+@pytest.mark.parametrize("deterministic", [True, False])
+def test_headline_full_size_one_head(deterministic):
     """bf16 causal B4 H8 T8192 d128, full-size run; the oracle checks batch 1, head 6."""
     p = W.headline()
-    (q, k, v, do), _, (dq, dk, dv) = gpu_fwd_bwd(p, True)
+    (q, k, v, do), _, (dq, dk, dv) = gpu_fwd_bwd(p, deterministic)
     b, h = 1, 6
     sl = lambda t: t[b:b + 1, :, h:h + 1]  # noqa: E731
     ref = oracle.backward(sl(q), sl(k), sl(v), sl(do), causal=True)
