@@ -118,4 +118,37 @@ class KernelTimer {
   cudaStream_t stream_;
 };
 
+// Launch order of the tiled kernels: a 1-D grid over (batch, head) pairs x
+// tiles.  Pairs go in groups of `group`, so that the tensors a pair's CTAs
+// share (K/V for query tiles, Q/dO for key tiles) stay in L2 while the group
+// runs; inside a group the tile rank is the slower index (rank 0 = most work
+// under causal masking starts first) and the pair the faster one.
+struct TileCoord {
+  int pair, rank;
+};
+
+__device__ __forceinline__ TileCoord grouped_tile(int linear, int n_pairs, int n_tiles, int group) {
+  const int per_group = group * n_tiles;
+  const int g = linear / per_group;
+  const int first = g * group;
+  const int in_group = min(group, n_pairs - first);
+  const int l = linear - g * per_group;
+  return {first + l % in_group, l / in_group};
+}
+
+#ifndef ATTN_L2_GROUP_BYTES
+#define ATTN_L2_GROUP_BYTES (32l << 20)
+#endif
+
+// Pairs per group: as many as keep `group` x bytes_per_pair within the L2
+// budget above, a multiple of `align` (the G query heads of one KV head share
+// its K/V), at least `align`, at most n_pairs.
+inline int l2_pair_group(long bytes_per_pair, int n_pairs, int align) {
+  long g = bytes_per_pair > 0 ? ATTN_L2_GROUP_BYTES / bytes_per_pair : n_pairs;
+  g = (g / align) * align;
+  if (g < align) g = align;
+  if (g > n_pairs) g = n_pairs;
+  return static_cast<int>(g);
+}
+
 }  // namespace attn

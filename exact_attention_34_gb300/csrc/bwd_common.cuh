@@ -1,0 +1,89 @@
+// Pieces shared by the backward kernels (two-pass dK/dV, dQ, single pass):
+// kernel parameters, the TMEM -> bf16 row store and the probability half of
+// the dK/dV softmax.
+#pragma once
+#include "attn_internal.h"
+
+namespace attn {
+namespace bwd {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ int key_limit(int i, int Lq, int kvl, int causal) {
+  if (!causal) return kvl;
+  return min(kvl, i + 1 + kvl - Lq);
+}
+
+struct BwdKParams {
+  const float* lse2;   // [B, Hq, Lq_pad], log2 domain, +inf on empty/pad rows
+  const float* delta;  // [B, Hq, Lq_pad]
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dq_acc;       // single-pass variant
+  const int32_t* kv_lens;
+  int Lq, Lkv, Hq, Hkv, G, causal, Lq_pad, n_tiles, n_pairs, pair_group;
+  float scale, scale_log2;
+  DeviceStatus* status;
+};
+
+// Store one row of D fp32 values from TMEM (columns col..col+D) as bf16, times `mul`.
+template <int D>
+__device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16* dst, float mul, bool do_store,
+                                               bool zero) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t r[32];
+    if (!zero) {
+      tmem_ld32(taddr + c * 32, r);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) r[i] = 0u;
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+    if (do_store) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    }
+  }
+}
+
+// P^T for the warpgroup's 64 queries [c0, c0 + 64): probabilities kept in
+// `pr` (fp32) and written packed over columns [c0, c0 + 32) of S^T.
+template <bool MASK>
+__device__ __forceinline__ void dkdv_probs(uint32_t s_col, int c0, const float* lse2, float sl2, bool key_ok,
+                                           int q_lo, int q_min, float (&pr)[64]) {
+  uint32_t sa[32], sb[32];
+  tmem_ld32_pair(s_col + c0, s_col + c0 + 32, sa, sb);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c0 + 4 * i);
+    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = 4 * i + e;
+      const uint32_t raw = c < 32 ? sa[c] : sb[c - 32];
+      float pv = ex2_approx(fmaf(__uint_as_float(raw), sl2, -lv[e]));
+      if (MASK) pv = (key_ok && q_lo + c0 + c >= q_min) ? pv : 0.f;
+      pr[c] = pv;
+    }
+  }
+  uint32_t pk[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
+  tmem_st32(s_col + c0, pk);
+}
+
+// Single-pass backward after the preprocess: the dK/dV kernel with atomic dQ
+// (grid = KV heads x batch x key tiles) and the dQ convert over n_dq values.
+// All four tensor maps use boxes of 64 columns x 128 rows.
+template <int D>
+cudaError_t launch_single_pass(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, long n_dq,
+                               cudaStream_t stream);
+
+}  // namespace bwd
+}  // namespace attn

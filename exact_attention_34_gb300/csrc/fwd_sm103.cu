@@ -52,7 +52,7 @@ struct FwdKParams {
   void* o;
   float* lse;
   const int32_t* kv_lens;
-  int Lq, Lkv, Hq, Hkv, G, causal, n_qblocks;
+  int Lq, Lkv, Hq, Hkv, G, causal, n_qblocks, n_pairs, pair_group;
   float scale_log2;
   DeviceStatus* status;
 };
@@ -83,10 +83,11 @@ __global__ void __launch_bounds__(320, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
-  // grid (Hq, B, query blocks): the block index is the slowest launch dimension,
-  // so with causal masking the longest blocks of every head start first.
-  const int qb = p.causal ? (p.n_qblocks - 1 - static_cast<int>(blockIdx.z)) : static_cast<int>(blockIdx.z);
-  const int hq = blockIdx.x, b = blockIdx.y;
+  // 1-D grid over (b, hq) pairs x query blocks in L2 groups; the longest
+  // causal blocks of a group start first.
+  const TileCoord tc = grouped_tile(blockIdx.x, p.n_pairs, p.n_qblocks, p.pair_group);
+  const int qb = p.causal ? p.n_qblocks - 1 - tc.rank : tc.rank;
+  const int hq = tc.pair % p.Hq, b = tc.pair / p.Hq;
   const int hkv = hq / p.G;
   int kvl = p.Lkv;
   if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
@@ -346,9 +347,11 @@ cudaError_t launch_fwd_bf16_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t s
   kp.G = pb.G;
   kp.causal = pb.causal;
   kp.n_qblocks = (pb.Lq + 2 * kBM - 1) / (2 * kBM);
+  kp.n_pairs = pb.B * pb.Hq;
+  kp.pair_group = l2_pair_group(2l * pb.Lkv * D * 2, kp.n_pairs, pb.G);
   kp.scale_log2 = pb.scale * kLog2e;
   kp.status = st;
-  dim3 grid(pb.Hq, pb.B, kp.n_qblocks);
+  dim3 grid(kp.n_pairs * kp.n_qblocks);
   {
     KernelTimer kt("fwd", stream);
     fwd_bf16_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
