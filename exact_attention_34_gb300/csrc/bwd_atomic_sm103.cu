@@ -16,16 +16,27 @@ namespace {
 // CTA = (batch, KV head, 128 keys); thread = key row = TMEM lane; 128-query
 // steps, every MMA 128 x 128 x 16.  Five GEMMs per step instead of the
 // two-pass backward's seven:
-//   tensor pipe:  S^T | dP^T | dV += P^T dO | dK += dS^T Q | dQ^T = K^T dS^T | S^T(t+1) | dP^T(t+1) ...
-//   softmax:          | P^T  | dS^T        |               | dQ^T -> fp32 buffer (atomic adds)
+//   tensor pipe:  S^T | dP^T | dV += P^T dO | dQ^T = K^T dS^T | dK += dS^T Q | S^T(t+1) | dP^T(t+1) ...
+//   softmax:          | P^T  | dS^T        |
+//   reduction:                              | dQ^T -> registers -> fp32 atomic adds (overlaps the next step)
 // TMEM: dK [0,128) dV [128,256) S^T [256,384) dP^T [384,512); dQ^T reuses the
-// dP^T columns once the softmax has read them, and dP^T(t+1) waits until the
-// softmax has reduced dQ^T(t) out.  P^T goes back to TMEM (A of dV); dS^T goes
-// to 128B-swizzled shared memory, where it is the K-major A of dK and the
-// MN-major B of dQ^T.  For head_dim 64 the M = 128 rows of dQ^T repeat the 64
-// head-dim rows (the second A block points at the first) and only the first
-// 64 lanes are read out.  The summation order of dQ over key tiles is not
-// fixed, so this variant is not bitwise reproducible.
+// dP^T columns once the softmax has read them.  P^T goes back to TMEM (A of
+// dV); dS^T goes to 128B-swizzled shared memory, where it is the K-major A of
+// dK and the MN-major B of dQ^T.  For head_dim 64 the M = 128 rows of dQ^T
+// repeat the 64 head-dim rows (the second A block points at the first) and
+// only the first 64 lanes are read out.
+//
+// The adds into the fp32 dQ buffer (64 KB per step and CTA) run at the L2's
+// reduction rate, well below the SM's, so four reduction warps own them: each
+// thread copies its head-dim row of dQ^T (128 queries) out of TMEM, releases
+// the columns for dP^T(t+1) at once, and then issues its 128 adds while the
+// next step's GEMMs and softmax run.  The summation order of dQ over key tiles
+// is not fixed, so this variant is not bitwise reproducible.
+//
+// Warps 0-7 softmax (warpgroup w owns queries [64w, 64w + 64) of the step),
+// 8-11 reduction (warp 8 + i reads TMEM lanes [32i, 32i + 32)), 12 TMA
+// producer, 13 MMA issuer, 14-15 idle; the control warpgroup gives its
+// registers to the other three.
 template <int D>
 struct DkdvAtomicCfg {
   static constexpr int kBN = 128, kBM = 128;
@@ -43,11 +54,15 @@ struct DkdvAtomicCfg {
   // 1 KB the system reserves per block, which is 1024-aligned (checked at run
   // time; a misaligned base makes the kernel report and do nothing).
   static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 512;
+  // Registers per thread after the split (launch: 512 x 128).  Each SM
+  // sub-partition holds one warp of each warpgroup: 3 x kRegsWork + kRegsCtl
+  // must equal 4 x 128.
+  static constexpr int kRegsWork = 144, kRegsCtl = 80;
 };
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(512, 1)
     bwd_dkdv_atomic_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                            const BwdKParams p) {
@@ -74,7 +89,7 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* p_ready = kv_full + 3;   // P^T(t) in TMEM (256 arrivals)
   uint64_t* ds_ready = kv_full + 4;  // dS^T(t) in shared memory (256 arrivals)
   uint64_t* dq_ready = kv_full + 5;  // dQ^T(t) computed
-  uint64_t* dq_free = kv_full + 6;   // dQ^T(t) reduced out (256 arrivals)
+  uint64_t* dq_free = kv_full + 6;   // dQ^T(t) copied out of TMEM (128 arrivals)
   uint64_t* acc_full = kv_full + 7;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -102,11 +117,11 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(p_ready, 256);
     mbar_init(ds_ready, 256);
     mbar_init(dq_ready, 1);
-    mbar_init(dq_free, 256);
+    mbar_init(dq_free, 128);
     mbar_init(acc_full, 1);
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -114,9 +129,12 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  static_assert(3 * C::kRegsWork + C::kRegsCtl == 4 * 128, "register split must match the launch allocation");
 
-  if (warp == 8) {
-    if (lane == 0 && T > 0) {
+  if (warp >= 12) {
+    setmaxnreg_dec<C::kRegsCtl>();
+    if (warp == 12 && lane == 0 && T > 0) {
+      // ---------------------------------------------------------------- TMA producer
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
       mbar_arrive_expect_tx(kv_full, 2 * C::kKVBytes);
@@ -139,10 +157,8 @@ __global__ void __launch_bounds__(320, 1)
         bulk_load(sStat + s * 2 * BM, p.lse2 + row, BM * 4, &full[s]);
         bulk_load(sStat + s * 2 * BM + BM, p.delta + row, BM * 4, &full[s]);
       }
-    }
-    __syncwarp();
-  } else if (warp == 9) {
-    if (lane == 0 && T > 0) {
+    } else if (warp == 13 && lane == 0 && T > 0) {
+      // ---------------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc_st = idesc_bf16_f32(128, BM, 0, 0);   // K x Q^T, V x dO^T
       constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, 0, 1);   // A (K-major or TMEM) x (dO|Q MN-major)
       constexpr uint32_t idesc_dq = idesc_bf16_f32(128, BM, 1, 1);   // K^T (MN-major) x dS^T (MN-major)
@@ -194,16 +210,16 @@ __global__ void __launch_bounds__(320, 1)
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {  // dK += dS^T Q (dS^T from shared memory)
-          const uint32_t aoff = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
-          mma_ss_d(tbase + 0, ads, aoff, bq_base, so + ((16 * k * 128) >> 4), idesc_acc, (t > 0 || k > 0) ? 1u : 0u);
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {  // dQ^T = K^T dS^T (dQ^T(t-1) was read out before dP^T(t) was issued)
+        for (int k = 0; k < 8; ++k) {  // dQ^T = K^T dS^T into the dP^T columns (the softmax has read dP^T(t))
           const uint32_t off = (16 * k * 128) >> 4;
           mma_ss_d(tbase + kColDP, akt, off, bds, off, idesc_dq, k > 0);
         }
         mma_commit(dq_ready);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // dK += dS^T Q (dS^T from shared memory)
+          const uint32_t aoff = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
+          mma_ss_d(tbase + 0, ads, aoff, bq_base, so + ((16 * k * 128) >> 4), idesc_acc, (t > 0 || k > 0) ? 1u : 0u);
+        }
         mma_commit(&empty[t % NS]);
         if (t + 1 < T) {
           ok = mbar_wait(&full[(t + 1) % NS], ((t + 1) / NS) & 1, abort_flag, p.status, 77);
@@ -219,8 +235,44 @@ __global__ void __launch_bounds__(320, 1)
       if (ok) mma_commit(acc_full);
     }
     __syncwarp();
+  } else if (warp >= 8) {
+    // ------------------------------------------------ reduction (thread = head-dim row of dQ^T)
+    setmaxnreg_inc<C::kRegsWork>();
+    const int quarter = warp - 8;
+    const int dr = quarter * 32 + lane;
+    const uint32_t t_lane = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
+    const bool active = quarter * 32 < D;  // head_dim 64: lanes [64, 128) hold a copy
+    const size_t qstride = static_cast<size_t>(p.Hq) * D;
+    for (int t = 0; t < T; ++t) {
+      if (!__all_sync(0xffffffffu, mbar_wait(dq_ready, t & 1, abort_flag, p.status, 83))) break;
+      tc_fence_after();
+      uint32_t v[128];
+      if (active) {
+        tmem_ld32_pair(t_lane + kColDP, t_lane + kColDP + 32, *reinterpret_cast<uint32_t(*)[32]>(v),
+                       *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+        tmem_ld32_pair(t_lane + kColDP + 64, t_lane + kColDP + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 64),
+                       *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+      }
+      tc_fence_before();
+      mbar_arrive(dq_free);
+      if (active) {
+        const int h = hk * p.G + t / steps_per_head;
+        const int q0 = (i_begin + t % steps_per_head) * BM;
+        float* dst = p.dq_acc + ((static_cast<size_t>(b) * p.Lq + q0) * p.Hq + h) * D + dr;
+        if (q0 + BM <= p.Lq) {
+#pragma unroll
+          for (int c = 0; c < BM; ++c) atomicAdd(dst + c * qstride, __uint_as_float(v[c]));
+        } else {
+          const int n = p.Lq - q0;
+#pragma unroll
+          for (int c = 0; c < BM; ++c)
+            if (c < n) atomicAdd(dst + c * qstride, __uint_as_float(v[c]));
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ softmax (thread = key row)
+    setmaxnreg_inc<C::kRegsWork>();
     const int w = warp >> 2, wq = warp & 3;
     const int r = wq * 32 + lane;
     const int j = j0 + r;
@@ -236,7 +288,6 @@ __global__ void __launch_bounds__(320, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(s_ready, t & 1, abort_flag, p.status, 79));
       if (!ok) break;
       tc_fence_after();
-      const int h = hk * p.G + t / steps_per_head;
       const int q0 = (i_begin + t % steps_per_head) * BM;
       const float* lse2 = sStat + s * 2 * BM;
       const float* dlt = lse2 + BM;
@@ -251,19 +302,22 @@ __global__ void __launch_bounds__(320, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(dp_ready, t & 1, abort_flag, p.status, 80));
       if (!ok) break;
       tc_fence_after();
-      {  // dS^T = P^T (dP^T - delta) -> 128B-swizzled shared memory (this row, this warpgroup's 64 queries)
-        uint32_t da[32], db[32];
-        tmem_ld32_pair(t_lane + kColDP + c0, t_lane + kColDP + c0 + 32, da, db);
+      // dS^T = P^T (dP^T - delta) -> 128B-swizzled shared memory (this row, this
+      // warpgroup's 64 queries), 32 columns of dP^T at a time
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t da[32];
+        tmem_ld32(t_lane + kColDP + c0 + 32 * hh, da);
+#pragma unroll
+        for (int ch = 4 * hh; ch < 4 * hh + 4; ++ch) {
           uint32_t pk[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int c = 8 * ch + 2 * e;
             const float4 d4 = *reinterpret_cast<const float4*>(dlt + c0 + (c & ~3));
             const float dv0 = (c & 3) ? d4.z : d4.x, dv1 = (c & 3) ? d4.w : d4.y;
-            const uint32_t r0 = c < 32 ? da[c] : db[c - 32], r1 = c + 1 < 32 ? da[c + 1] : db[c + 1 - 32];
-            pk[e] = pack_bf16x2(pr[c] * (__uint_as_float(r0) - dv0), pr[c + 1] * (__uint_as_float(r1) - dv1));
+            pk[e] = pack_bf16x2(pr[c] * (__uint_as_float(da[c - 32 * hh]) - dv0),
+                                pr[c + 1] * (__uint_as_float(da[c + 1 - 32 * hh]) - dv1));
           }
           *reinterpret_cast<uint4*>(ds_row + ((ch ^ (r & 7)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
@@ -271,21 +325,6 @@ __global__ void __launch_bounds__(320, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(ds_ready);
-      ok = __all_sync(0xffffffffu, mbar_wait(dq_ready, t & 1, abort_flag, p.status, 81));
-      if (!ok) break;
-      tc_fence_after();
-      if (r < D) {  // thread = head-dim column d = r; warpgroup w reduces queries [64w, 64w + 64)
-        uint32_t qa[32], qb[32];
-        tmem_ld32_pair(t_lane + kColDP + c0, t_lane + kColDP + c0 + 32, qa, qb);
-        float* dst = p.dq_acc + ((static_cast<size_t>(b) * p.Lq + q0 + c0) * p.Hq + h) * D + r;
-        const size_t qstride = static_cast<size_t>(p.Hq) * D;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          if (q0 + c0 + c < p.Lq) atomicAdd(dst + c * qstride, __uint_as_float(c < 32 ? qa[c] : qb[c - 32]));
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(dq_free);
     }
     if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 82));
     if (ok) {
@@ -301,7 +340,7 @@ __global__ void __launch_bounds__(320, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }

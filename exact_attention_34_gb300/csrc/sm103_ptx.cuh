@@ -41,6 +41,18 @@ __device__ __forceinline__ void report_status(DeviceStatus* st, int code, int si
 
 __device__ __forceinline__ void report_timeout(DeviceStatus* st, int site) { report_status(st, 1, site); }
 
+// Per-warpgroup register reallocation.  All warps of a warpgroup execute the
+// same call; an increase waits until enough registers have been released
+// from the block's launch allocation, so the shares must sum to it.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
