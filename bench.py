@@ -232,22 +232,26 @@ def run_gpu(args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one event per step boundary: the first-to-last span is the timed region,
+    # consecutive pairs give the per-step spread
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     with ClockSampler(local_rank) as clk:
         barrier(world)
         torch.cuda.synchronize()
         clk.mark_start()
-        ev0.record(stream)
-        for _ in range(args.steps):
+        evs[0].record(stream)
+        for i in range(args.steps):
             step()
-        ev1.record(stream)
+            evs[i + 1].record(stream)
         torch.cuda.synchronize()
         clk.mark_stop()
         barrier(world)
-    local_ms = ev0.elapsed_time(ev1)
+    local_ms = evs[0].elapsed_time(evs[-1])
     max_ms = max_over_ranks(local_ms, world, dev)
     value = whole_job_value(F_step, args.steps, world, max_ms)
     ms_per_step = max_ms / args.steps
+    per_step = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps))
+    quart = [round(per_step[min(len(per_step) - 1, int(f * len(per_step)))], 4) for f in (0.25, 0.5, 0.75)]
 
     # ---- per-kernel durations (a separate pass with launch events enabled)
     ea.attn_timing_enable(True)
@@ -317,7 +321,8 @@ def run_gpu(args):
         cpu = None if args.no_cpu_baseline else cpu_baseline_sample(args.cpu_budget_s)
         result = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "ms_per_step_q1_median_q3": quart, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "bf16 causal attention fwd+bwd, B4 H8 T8192 d128 (deterministic two-pass bwd)",
                        "global_batch": p.B * world, "seq_len": p.Lq, "heads": p.Hq, "head_dim": p.d,
@@ -354,6 +359,26 @@ def other_rows(args, dev, peaks):
         return a.elapsed_time(b) / n
 
     g = torch.Generator(device=dev).manual_seed(0)
+    # the headline workload with the single-pass backward (atomic dQ)
+    p = W.headline()
+    q = torch.randn(p.B, p.Lq, p.Hq, p.d, device=dev, generator=g).to(torch.bfloat16)
+    k, v, do = torch.randn_like(q), torch.randn_like(q), torch.randn_like(q)
+
+    def sp_step():
+        o, lse = ea.forward(q, k, v, causal=True)
+        ea.backward(q, k, v, o, lse, do, causal=True, deterministic=False)
+
+    ms = timed(sp_step)
+    ea.attn_timing_enable(True)
+    for _ in range(5):
+        sp_step()
+    torch.cuda.synchronize()
+    kt = {n: round(ea.attn_timing_query(n)[0] / 5, 4)
+          for n in ("fwd", "bwd_preprocess", "bwd_dkdv_atomic", "dq_convert")}
+    ea.attn_timing_enable(False)
+    out["single_pass_fwd_bwd"] = {"ms": round(ms, 4), "tflops": round(3.5 * W.fwd_flops(p) / ms / 1e9, 1),
+                                  "kernel_ms": kt, "note": "same workload, atomic-dQ backward (not bitwise reproducible)"}
+    del q, k, v, do
     # KVLenMask + GQA + Lq != Lkv fwd+bwd (flops over valid keys)
     p = W.kvlen_gqa()
     q = torch.randn(p.B, p.Lq, p.Hq, p.d, device=dev, generator=g).to(torch.bfloat16)
@@ -494,7 +519,8 @@ def run_sweep(args):
     """The pages' attention grid ("Attention performance", section "Time"): B4 H8,
     d in {64, 128}, T in {128 ... 8192} plus the ragged 600 / 1500 / 3000, causal
     and not, bf16; fwd and fwd+bwd TFLOP/s (deterministic backward).  One JSON
-    line per case.  Also fp32 at d=128 for T <= 2048."""
+    line per case, median of 5 repeats with the quartiles.  Also fp32 at d=128
+    for T <= 2048."""
     import torch
 
     import exact_attention_34_gb300 as ea
@@ -503,17 +529,22 @@ def run_sweep(args):
     eb.build()
     dev = torch.device("cuda", 0)
 
-    def timed(fn, n):
+    def timed(fn, n, repeats=5):
+        """(q1, median, q3) in ms of `repeats` runs of n back-to-back calls each."""
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(n):
-            fn()
-        b.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / n
+        runs = []
+        for _ in range(repeats):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(n):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            runs.append(a.elapsed_time(b) / n)
+        runs.sort()
+        return runs[len(runs) // 4], runs[len(runs) // 2], runs[(3 * len(runs)) // 4]
 
     cases = [(T, d, c, "bf16") for d in (64, 128) for T in W.GRID_T + W.RAGGED_T for c in (False, True)]
     cases += [(T, 128, c, "fp32") for T in (128, 512, 1024, 2048) for c in (False, True)]
@@ -523,12 +554,14 @@ def run_sweep(args):
         q, k, v, do = (torch.randn(p.B, T, p.Hq, d, device=dev, generator=g).to(W.DTYPES[dt]) for _ in range(4))
         o, lse = ea.forward(q, k, v, causal=c)
         n = max(3, min(200, int(2e12 / max(W.fwd_flops(p), 1.0))))
-        ms_f = timed(lambda: ea.forward(q, k, v, causal=c), n)
-        ms_b = timed(lambda: (ea.forward(q, k, v, causal=c), ea.backward(q, k, v, o, lse, do, causal=c)), n)
+        qf = timed(lambda: ea.forward(q, k, v, causal=c), n)
+        qb = timed(lambda: (ea.forward(q, k, v, causal=c), ea.backward(q, k, v, o, lse, do, causal=c)), n)
         F = W.fwd_flops(p)
-        print(json.dumps({"T": T, "d": d, "causal": c, "dtype": dt, "fwd_ms": round(ms_f, 4),
-                          "fwd_tflops": round(F / ms_f / 1e9, 1), "fwd_bwd_ms": round(ms_b, 4),
-                          "fwd_bwd_tflops": round(3.5 * F / ms_b / 1e9, 1)}), flush=True)
+        print(json.dumps({"T": T, "d": d, "causal": c, "dtype": dt, "fwd_ms": round(qf[1], 4),
+                          "fwd_ms_q1_q3": [round(qf[0], 4), round(qf[2], 4)],
+                          "fwd_tflops": round(F / qf[1] / 1e9, 1), "fwd_bwd_ms": round(qb[1], 4),
+                          "fwd_bwd_ms_q1_q3": [round(qb[0], 4), round(qb[2], 4)],
+                          "fwd_bwd_tflops": round(3.5 * F / qb[1] / 1e9, 1)}), flush=True)
 
 
 def main(argv=None):
