@@ -564,6 +564,131 @@ def run_sweep(args):
                           "fwd_bwd_tflops": round(3.5 * F / qb[1] / 1e9, 1)}), flush=True)
 
 
+def _timed_q(fn, n, repeats=5):
+    """(q1, median, q3) ms of `repeats` runs of n back-to-back calls (after 3 warm-up calls)."""
+    import torch
+
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    runs = []
+    for _ in range(repeats):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        runs.append(a.elapsed_time(b) / n)
+    runs.sort()
+    return runs[len(runs) // 4], runs[len(runs) // 2], runs[(3 * len(runs)) // 4]
+
+
+def _call_peak_bytes(fn):
+    """Device bytes one call allocates at its peak beyond what was live before it."""
+    import torch
+
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    out = fn()
+    torch.cuda.synchronize()
+    peak = torch.cuda.max_memory_allocated() - base
+    del out
+    torch.cuda.empty_cache()
+    return peak
+
+
+def run_gqa_suite(args):
+    """The pages' GQA workload ("Attention performance", section "Grouped-query
+    attention and decoding"): 32 query heads, head_dim 128, batch 1,
+    Lq = Lkv = T, bf16, non-causal; 8 KV heads (native GQA: the kernels read KV
+    head h // G) against 32 (plain multi-head).  Per case: fwd and fwd+bwd
+    TFLOP/s (median of five repeats) and the device peak of one fwd+bwd call
+    beyond its inputs; for GQA also the same call on K/V repeated to 32 heads
+    (the repeat, the 32-head gradients and their sum over the group)."""
+    import torch
+
+    import exact_attention_34_gb300 as ea
+    from exact_attention_34_gb300 import build as eb
+
+    eb.build()
+    dev = torch.device("cuda", 0)
+    Hq, d = 32, 128
+    for T in (1024, 2048, 4096, 8192, 16384):
+        for Hkv in (8, 32):
+            g = torch.Generator(device=dev).manual_seed(0)
+            q = torch.randn(1, T, Hq, d, device=dev, generator=g).to(torch.bfloat16)
+            k = torch.randn(1, T, Hkv, d, device=dev, generator=g).to(torch.bfloat16)
+            v = torch.randn_like(k)
+            do = torch.randn_like(q)
+            o, lse = ea.forward(q, k, v)
+            F = 4.0 * Hq * T * T * d
+            n = max(3, min(100, int(5e11 / F)))
+            qf = _timed_q(lambda: ea.forward(q, k, v), n)
+            qb = _timed_q(lambda: (ea.forward(q, k, v), ea.backward(q, k, v, o, lse, do)), n)
+
+            def native():
+                o2, l2 = ea.forward(q, k, v)
+                return ea.backward(q, k, v, o2, l2, do)
+
+            line = {"suite": "gqa", "T": T, "Hq": Hq, "Hkv": Hkv, "d": d, "B": 1, "causal": False, "dtype": "bf16",
+                    "fwd_ms": round(qf[1], 4), "fwd_tflops": round(F / qf[1] / 1e9, 1),
+                    "fwd_bwd_ms": round(qb[1], 4), "fwd_bwd_ms_q1_q3": [round(qb[0], 4), round(qb[2], 4)],
+                    "fwd_bwd_tflops": round(3.5 * F / qb[1] / 1e9, 1),
+                    "peak_mb_fwd_bwd": round(_call_peak_bytes(native) / 2**20, 1)}
+            if Hkv < Hq:
+                G = Hq // Hkv
+
+                def repeated():
+                    kr, vr = k.repeat_interleave(G, dim=2), v.repeat_interleave(G, dim=2)
+                    o2, l2 = ea.forward(q, kr, vr)
+                    dq, dkr, dvr = ea.backward(q, kr, vr, o2, l2, do)
+                    return dq, dkr.view(1, T, Hkv, G, d).sum(3), dvr.view(1, T, Hkv, G, d).sum(3)
+
+                line["peak_mb_fwd_bwd_repeated_kv"] = round(_call_peak_bytes(repeated) / 2**20, 1)
+            print(json.dumps(line), flush=True)
+            del q, k, v, do, o, lse
+            torch.cuda.empty_cache()
+
+
+def run_memory_suite(args):
+    """The pages' memory measurements ("Attention performance", section
+    "Memory"): bf16, head_dim 64, 8 heads, non-causal.  (1) The device peak of
+    one fwd+bwd call beyond its inputs at batch 4 for T = 1024 ... 65536 (the
+    pages' search stops at 65,536; every T up to there runs).  (2) The bytes
+    kept for the backward at batch 2: the output and the log-sum-exp (no T x T
+    buffer), as allocated by the forward."""
+    import torch
+
+    import exact_attention_34_gb300 as ea
+    from exact_attention_34_gb300 import build as eb
+
+    eb.build()
+    dev = torch.device("cuda", 0)
+    H, d = 8, 64
+    for T in (1024, 2048, 4096, 8192, 16384, 32768, 65536):
+        g = torch.Generator(device=dev).manual_seed(0)
+        q, k, v, do = (torch.randn(4, T, H, d, device=dev, generator=g).to(torch.bfloat16) for _ in range(4))
+
+        def call():
+            o, lse = ea.forward(q, k, v)
+            return ea.backward(q, k, v, o, lse, do)
+
+        peak = _call_peak_bytes(call)
+        inputs = 4 * q.numel() * q.element_size()
+        q2 = q[:2].contiguous()
+        k2, v2 = k[:2].contiguous(), v[:2].contiguous()
+        res = _call_peak_bytes(lambda: ea.forward(q2, k2, v2))
+        print(json.dumps({"suite": "memory", "T": T, "H": H, "d": d, "dtype": "bf16", "causal": False,
+                          "peak_mb_fwd_bwd_B4": round(peak / 2**20, 2), "inputs_mb_B4": round(inputs / 2**20, 2),
+                          "residual_mb_B2": round(res / 2**20, 2),
+                          "ran": True}), flush=True)
+        del q, k, v, do, q2, k2, v2
+        torch.cuda.empty_cache()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -577,11 +702,15 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the other rows (KVLen+GQA, decode)")
     ap.add_argument("--sweep", action="store_true", help="print the attention grid (one JSON line per case) and exit")
+    ap.add_argument("--suite", choices=("gqa", "memory"), help="print the GQA or the memory suite and exit")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
     if args.sweep:
         run_sweep(args)
+        return
+    if args.suite:
+        (run_gqa_suite if args.suite == "gqa" else run_memory_suite)(args)
         return
     rank, _, world = dist_env()
     if args.gpus != world and world > 1:
