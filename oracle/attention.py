@@ -19,8 +19,9 @@ against the pages:
 * per-batch KV lengths (KVLenMask): keys at or past a batch element's length
   are invalid, rows without a valid key return zeros, dK/dV of padded keys are
   zero -- probjax "H100 (Hopper)", section "Mosaic GPU";
-* equal-length causal masking -- "Attention performance", section "Short
-  sequences and the default dispatch" (position-only masks);
+* equal-length causal masking and local-window masks -- "Attention
+  performance", section "Short sequences and the default dispatch"
+  (position-only masks: causal, length or window);
 * GQA: query head h reads KV head h // G, K/V are never repeated -- same page,
   section "Grouped-query attention and decoding";
 * split-KV decoding combines per-split partial results by their log-sum-exp --
@@ -34,6 +35,11 @@ Readings where the pages are silent (each listed in the design notes):
   this is the usual ``j <= i``;
 * the log-sum-exp is the natural logarithm, ``lse[b, h, i]``, and ``-inf`` on a
   row with no valid key (whose output is 0);
+* a local window ``(left, right)`` is taken around the same bottom-right
+  aligned diagonal: key j is valid for row i iff
+  ``i + kvl[b] - Lq - left <= j <= i + kvl[b] - Lq + right`` (and ``j < kvl[b]``);
+  a negative or missing bound is unbounded, so ``(-1, 0)`` is causal and
+  ``(-1, -1)`` is no mask; combined with ``causal=True`` both conditions hold;
 * KV lengths outside [0, Lkv] are clamped into it;
 * the default scale is 1/sqrt(head_dim).
 
@@ -78,17 +84,26 @@ def effective_kv_lens(B: int, Lkv: int, kv_lens) -> np.ndarray:
     return np.clip(kl, 0, Lkv)
 
 
-def valid_keys(rows: np.ndarray, Lq: int, Lkv: int, kvl_b: int, causal: bool) -> np.ndarray:
+def valid_keys(rows: np.ndarray, Lq: int, Lkv: int, kvl_b: int, causal: bool, window=None) -> np.ndarray:
     """Boolean matrix ``[len(rows), Lkv]``: is key j valid for query row i.
 
     KVLenMask: ``j < kvl_b``.  Causal (bottom-right reading for Lq != Lkv):
-    ``j <= i + kvl_b - Lq``.
+    ``j <= i + kvl_b - Lq``.  Local window ``(left, right)`` around the same
+    diagonal: ``j >= i + kvl_b - Lq - left`` when left >= 0 and
+    ``j <= i + kvl_b - Lq + right`` when right >= 0.
     """
     j = np.arange(Lkv)[None, :]
+    i = np.asarray(rows, dtype=np.int64)[:, None]
+    diag = i + kvl_b - Lq
     ok = j < kvl_b
     if causal:
-        i = np.asarray(rows, dtype=np.int64)[:, None]
-        ok = ok & (j <= i + kvl_b - Lq)
+        ok = ok & (j <= diag)
+    if window is not None:
+        left, right = window
+        if left is not None and left >= 0:
+            ok = ok & (j >= diag - left)
+        if right is not None and right >= 0:
+            ok = ok & (j <= diag + right)
     return np.broadcast_to(ok, (len(rows), Lkv)).copy()
 
 
@@ -122,7 +137,7 @@ def _head_probs(qh, kh, scale, mask):
     return p, lse
 
 
-def forward(q, k, v, scale=None, causal=False, kv_lens=None, rows=None, heads=None,
+def forward(q, k, v, scale=None, causal=False, kv_lens=None, rows=None, heads=None, window=None,
             row_block: int = 1024):
     """Exact attention forward: ``O = softmax(scale * Q K^T) V`` and ``LSE``.
 
@@ -145,14 +160,14 @@ def forward(q, k, v, scale=None, causal=False, kv_lens=None, rows=None, heads=No
             hk = hq // G
             for r0 in range(0, len(rows), row_block):
                 rr = rows[r0:r0 + row_block]
-                mask = valid_keys(rr, Lq, Lkv, int(kvl[b]), causal)
+                mask = valid_keys(rr, Lq, Lkv, int(kvl[b]), causal, window)
                 p, l_ = _head_probs(q[b, rr, hq, :], k[b, :, hk, :], scale, mask)
                 o[b, r0:r0 + len(rr), hq, :] = p @ v[b, :, hk, :]
                 lse[b, hq, r0:r0 + len(rr)] = l_
     return o, lse
 
 
-def probabilities(q, k, scale=None, causal=False, kv_lens=None):
+def probabilities(q, k, scale=None, causal=False, kv_lens=None, window=None):
     """The full probability tensor ``P [B, Hq, Lq, Lkv]`` (tiny inputs only)."""
     q, k = _f64(q), _f64(k)
     B, Lq, Hq, d = q.shape
@@ -164,12 +179,12 @@ def probabilities(q, k, scale=None, causal=False, kv_lens=None):
     rows = np.arange(Lq)
     for b in range(B):
         for hq in range(Hq):
-            mask = valid_keys(rows, Lq, Lkv, int(kvl[b]), causal)
+            mask = valid_keys(rows, Lq, Lkv, int(kvl[b]), causal, window)
             out[b, hq], _ = _head_probs(q[b, :, hq, :], k[b, :, hq // G, :], scale, mask)
     return out
 
 
-def backward(q, k, v, do, scale=None, causal=False, kv_lens=None, kv_heads=None,
+def backward(q, k, v, do, scale=None, causal=False, kv_lens=None, kv_heads=None, window=None,
              row_block: int = 1024, rows=None):
     """Analytic gradient of ``sum(O * dO)`` with respect to q, k and v.
 
@@ -209,7 +224,7 @@ def backward(q, k, v, do, scale=None, causal=False, kv_lens=None, kv_heads=None,
             for hq in range(hk * G, (hk + 1) * G):
                 for r0 in range(0, len(all_rows), row_block):
                     rr = all_rows[r0:r0 + row_block]
-                    mask = valid_keys(rr, Lq, Lkv, int(kvl[b]), causal)
+                    mask = valid_keys(rr, Lq, Lkv, int(kvl[b]), causal, window)
                     p, _ = _head_probs(q[b, rr, hq, :], kh, scale, mask)
                     doh = do[b, rr, hq, :]
                     acc_dv += p.T @ doh

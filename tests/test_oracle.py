@@ -367,3 +367,139 @@ def test_backward_row_partition_adds_up():
     np.testing.assert_allclose(a[2] + b[2], full[2], rtol=0, atol=1e-14)
     np.testing.assert_allclose(a[0][:, [0, 2, 3]], full[0][:, [0, 2, 3]], rtol=0, atol=1e-15)
     assert np.all(np.isnan(a[0][:, [1, 4, 5, 6]]))
+
+
+# --------------------------------------------------------------------------
+# local-window masks ("Attention performance", section "Short sequences and
+# the default dispatch": position-only masks include window masks)
+# --------------------------------------------------------------------------
+
+def brute_force_window(q, k, v, scale, kv_lens, left, right):
+    """Pure-Python loops with the window written per (i, j): key j is kept for
+    row i iff it lies within `left` keys before and `right` keys after the
+    row's diagonal position i + kvl - Lq (negative = unbounded)."""
+    B, Lq, Hq, d = q.shape
+    Lkv, Hkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    o = np.zeros((B, Lq, Hq, d))
+    lse = np.full((B, Hq, Lq), -math.inf)
+    for b in range(B):
+        kvl = Lkv if kv_lens is None else max(0, min(Lkv, int(kv_lens[b])))
+        for h in range(Hq):
+            for i in range(Lq):
+                centre = i + kvl - Lq
+                keys = []
+                for j in range(kvl):
+                    before = centre - j  # > 0: j lies before the diagonal
+                    if left >= 0 and before > left:
+                        continue
+                    if right >= 0 and -before > right:
+                        continue
+                    keys.append(j)
+                if not keys:
+                    continue
+                sc = {j: scale * sum(float(q[b, i, h, c]) * float(k[b, j, h // G, c]) for c in range(d))
+                      for j in keys}
+                mx = max(sc.values())
+                z = sum(math.exp(sc[j] - mx) for j in keys)
+                for j in keys:
+                    w = math.exp(sc[j] - mx) / z
+                    for c in range(d):
+                        o[b, i, h, c] += w * float(v[b, j, h // G, c])
+                lse[b, h, i] = mx + math.log(z)
+    return o, lse
+
+
+WINDOW_CASES = [
+    # B, Lq, Lkv, Hq, Hkv, d, kv_lens, (left, right)
+    (1, 6, 6, 2, 2, 3, None, (2, 0)),        # causal sliding window
+    (1, 6, 6, 2, 1, 3, None, (1, 2)),        # two-sided
+    (2, 4, 7, 2, 2, 2, None, (-1, 1)),       # right-bounded only, Lq < Lkv
+    (2, 7, 4, 2, 1, 3, None, (0, -1)),       # left-bounded only, Lq > Lkv
+    (3, 5, 6, 2, 2, 2, [6, 2, 0], (1, 1)),   # with KV lengths, one empty batch
+    (1, 5, 5, 2, 2, 3, None, (0, 0)),        # one key per row
+]
+
+
+@pytest.mark.parametrize("case", WINDOW_CASES)
+def test_window_forward_matches_brute_force(case):
+    B, Lq, Lkv, Hq, Hkv, d, kl, win = case
+    q, k, v = rnd((B, Lq, Hq, d), 41), rnd((B, Lkv, Hkv, d), 42), rnd((B, Lkv, Hkv, d), 43)
+    o, lse = oracle.forward(q, k, v, scale=0.6, kv_lens=kl, window=win)
+    ob, lb = brute_force_window(q, k, v, 0.6, kl, *win)
+    np.testing.assert_allclose(o, ob, rtol=1e-12, atol=1e-12)
+    fin = np.isfinite(lb)
+    assert np.array_equal(np.isfinite(lse), fin)
+    np.testing.assert_allclose(lse[fin], lb[fin], rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("case", WINDOW_CASES[:5])
+def test_window_backward_matches_finite_differences(case):
+    B, Lq, Lkv, Hq, Hkv, d, kl, win = case
+    q, k, v, do = rnd((B, Lq, Hq, d), 51), rnd((B, Lkv, Hkv, d), 52), rnd((B, Lkv, Hkv, d), 53), \
+        rnd((B, Lq, Hq, d), 54)
+    dq, dk, dv = oracle.backward(q, k, v, do, scale=0.6, kv_lens=kl, window=win)
+
+    def loss():
+        o, _ = oracle.forward(q, k, v, scale=0.6, kv_lens=kl, window=win)
+        return float(np.sum(o * do))
+
+    h = 1e-6
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = x[idx]
+            x[idx] = old + h
+            fp = loss()
+            x[idx] = old - h
+            fm = loss()
+            x[idx] = old
+            num[idx] = (fp - fm) / (2 * h)
+        assert np.max(np.abs(num - g)) / max(1.0, np.max(np.abs(num))) < 1e-6
+
+
+@pytest.mark.parametrize("Lq,Lkv,left,right", [(9, 9, 3, 0), (9, 9, 2, 3), (6, 11, 4, 1), (11, 6, -1, 5)])
+def test_window_against_torch_band_mask(Lq, Lkv, left, right):
+    """torch float64 SDPA with a band mask built by tril/triu (a library
+    construction independent of the oracle's index arithmetic)."""
+    B, H, d, scale = 2, 2, 5, 0.45
+    q, k, v, do = rnd((B, Lq, H, d), 61), rnd((B, Lkv, H, d), 62), rnd((B, Lkv, H, d), 63), rnd((B, Lq, H, d), 64)
+    ones = torch.ones(Lq, Lkv, dtype=torch.bool)
+    off = Lkv - Lq
+    band = torch.tril(ones, diagonal=off + right) if right >= 0 else ones
+    if left >= 0:
+        band = band & torch.triu(ones, diagonal=off - left)
+    assert band.any(dim=1).all()  # torch's SDPA returns NaN on empty rows; keep every row non-empty here
+    o_t, dq_t, dk_t, dv_t = _torch_ref(q, k, v, do, scale, band)
+    o, _ = oracle.forward(q, k, v, scale=scale, window=(left, right))
+    dq, dk, dv = oracle.backward(q, k, v, do, scale=scale, window=(left, right))
+    for a, b in ((o, o_t), (dq, dq_t), (dk, dk_t), (dv, dv_t)):
+        np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-12)
+
+
+def test_window_special_cases_reduce_to_causal_and_unmasked():
+    B, Lq, Lkv, H, d = 2, 7, 9, 2, 3
+    q, k, v, do = rnd((B, Lq, H, d), 71), rnd((B, Lkv, H, d), 72), rnd((B, Lkv, H, d), 73), rnd((B, Lq, H, d), 74)
+    kl = [9, 5]
+    for win, causal in (((-1, 0), True), ((-1, -1), False), ((None, None), False)):
+        a = oracle.forward(q, k, v, kv_lens=kl, window=win)
+        b = oracle.forward(q, k, v, kv_lens=kl, causal=causal)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+        ga = oracle.backward(q, k, v, do, kv_lens=kl, window=win)
+        gb = oracle.backward(q, k, v, do, kv_lens=kl, causal=causal)
+        for x, y in zip(ga, gb):
+            assert np.array_equal(x, y)
+
+
+def test_window_zero_width_gives_the_diagonal_value():
+    """window (0, 0) with Lq == Lkv: row i sees only key i, so O[i] = V[i]
+    exactly and dQ = dK = 0 exactly (a single valid key)."""
+    B, L, H, d = 2, 6, 2, 4
+    q, k, v, do = rnd((B, L, H, d), 81), rnd((B, L, H, d), 82), rnd((B, L, H, d), 83), rnd((B, L, H, d), 84)
+    o, lse = oracle.forward(q, k, v, window=(0, 0))
+    np.testing.assert_array_equal(o, v)
+    dq, dk, dv = oracle.backward(q, k, v, do, window=(0, 0))
+    assert np.all(dq == 0) and np.all(dk == 0)
+    np.testing.assert_allclose(dv, do, rtol=0, atol=1e-15)
