@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
         "attn_timing_enable": (I, [I]),
         "attn_timing_query": (I, [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I)]),
         "attn_bwd_static_scratch": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, I, P]),
+        "attn_fwd_window": (I, [P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, I, P]),
+        "attn_bwd_window": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, I, I, P, S, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -85,7 +87,7 @@ EXPORTED = (
     "attn_status_string", "attn_last_error", "attn_fwd", "attn_bwd_preprocess", "attn_bwd_workspace_size",
     "attn_bwd", "attn_decode_num_splits", "attn_decode_splitkv", "attn_decode_combine",
     "attn_decode_workspace_size", "attn_device_status", "attn_timing_enable", "attn_timing_query",
-    "attn_bwd_static_scratch",
+    "attn_bwd_static_scratch", "attn_fwd_window", "attn_bwd_window",
 )
 
 
@@ -133,6 +135,20 @@ def attn_fwd(q, k, v, o, lse, scale=None, causal=False, kv_lens=None, stream=Non
            "attn_fwd")
 
 
+def _window(window):
+    """(left, right) with None or a negative value meaning unbounded."""
+    left, right = window
+    return (-1 if left is None else int(left)), (-1 if right is None else int(right))
+
+
+def attn_fwd_window(q, k, v, o, lse, window, scale=None, kv_lens=None, stream=None):
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    wl, wr = _window(window)
+    _check(lib().attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Lq, Lkv, Hq, Hkv, d,
+                                 _scale(scale, d), wl, wr, _ptr(kv_lens), _dtype(q), _stream(stream)),
+           "attn_fwd_window")
+
+
 def attn_bwd_preprocess(o, dout, delta, stream=None):
     B, Lq, Hq, d = o.shape
     _check(lib().attn_bwd_preprocess(_ptr(o), _ptr(dout), _ptr(delta), B, Lq, Hq, d, _dtype(o), _stream(stream)),
@@ -151,6 +167,17 @@ def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, scale=None, causal=Fa
                           B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d), int(bool(causal)), _ptr(kv_lens), _dtype(q),
                           int(bool(deterministic)), _ptr(workspace), ws_bytes, _stream(stream)),
            "attn_bwd")
+
+
+def attn_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, workspace, window, scale=None, kv_lens=None,
+                    deterministic=True, stream=None):
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    wl, wr = _window(window)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().attn_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                 _ptr(dv), B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d), wl, wr, _ptr(kv_lens),
+                                 _dtype(q), int(bool(deterministic)), _ptr(workspace), ws_bytes, _stream(stream)),
+           "attn_bwd_window")
 
 
 def attn_decode_num_splits(B, Lq, Lkv, Hq, Hkv, d) -> int:
@@ -209,22 +236,34 @@ def attn_timing_query(kernel: str):
 
 # ---- conveniences that allocate outputs with torch ------------------------------
 
-def forward(q, k, v, scale=None, causal=False, kv_lens=None, stream=None):
-    """(o, lse) for q [B,Lq,Hq,d], k/v [B,Lkv,Hkv,d] on the GPU."""
+def forward(q, k, v, scale=None, causal=False, kv_lens=None, stream=None, window=None):
+    """(o, lse) for q [B,Lq,Hq,d], k/v [B,Lkv,Hkv,d] on the GPU.  window =
+    (left, right) selects the local-window mask (causal must then be False)."""
     B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
     o = torch.empty_like(q)
     lse = torch.empty(B, Hq, Lq, device=q.device, dtype=torch.float32)
-    attn_fwd(q, k, v, o, lse, scale, causal, kv_lens, stream)
+    if window is not None:
+        if causal:
+            raise ValueError("pass either causal or window (causal is window (-1, 0))")
+        attn_fwd_window(q, k, v, o, lse, window, scale, kv_lens, stream)
+    else:
+        attn_fwd(q, k, v, o, lse, scale, causal, kv_lens, stream)
     return o, lse
 
 
-def backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_lens=None, deterministic=True, stream=None):
-    """(dq, dk, dv) given the forward's o and lse."""
+def backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_lens=None, deterministic=True, stream=None,
+             window=None):
+    """(dq, dk, dv) given the forward's o and lse (same mask arguments as forward)."""
     B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
     nbytes = attn_bwd_workspace_size(B, Lq, Hq, d, deterministic, q.dtype)
     ws = torch.empty(max(nbytes, 256), device=q.device, dtype=torch.uint8)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, ws, scale, causal, kv_lens, deterministic, stream)
+    if window is not None:
+        if causal:
+            raise ValueError("pass either causal or window (causal is window (-1, 0))")
+        attn_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, ws, window, scale, kv_lens, deterministic, stream)
+    else:
+        attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, ws, scale, causal, kv_lens, deterministic, stream)
     return dq, dk, dv
 
 

@@ -119,8 +119,23 @@ Problem make_problem(int B, int Lq, int Lkv, int Hq, int Hkv, int d, float scale
   p.d = d;
   p.G = Hq / Hkv;
   p.causal = causal;
+  p.wl = kWinInf;
+  p.wr = causal ? 0 : kWinInf;
   p.scale = scale;
   p.kv_lens = kl;
+  return p;
+}
+
+// A local window: a negative bound, or one at least as long as the keys (left)
+// or the queries (right), is unbounded, so finite bounds stay below 2^30 and
+// the span arithmetic cannot overflow.
+Problem make_window_problem(int B, int Lq, int Lkv, int Hq, int Hkv, int d, float scale, int window_left,
+                            int window_right, const int32_t* kl) {
+  Problem p = make_problem(B, Lq, Lkv, Hq, Hkv, d, scale, 0, kl);
+  p.wl = (window_left < 0 || window_left >= Lkv) ? kWinInf : window_left;
+  p.wr = (window_right < 0 || window_right >= Lq) ? kWinInf : window_right;
+  // later rows see more keys only when the left side is open and the right bounded
+  p.causal = (p.wl >= kWinInf && p.wr < kWinInf) ? 1 : 0;
   return p;
 }
 
@@ -230,17 +245,14 @@ const char* attn_status_string(attn_status s) {
 
 const char* attn_last_error(void) { return t_last_error; }
 
-attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Lq, int Lkv,
-                     int Hq, int Hkv, int d, float scale, int causal, const int32_t* kv_lens, attn_dtype dtype,
-                     attn_stream_t stream) {
-  attn_status s = check_problem(B, Lq, Lkv, Hq, Hkv, d, scale, causal, dtype);
+static attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, const Problem& pb,
+                     attn_dtype dtype, attn_stream_t stream) {
+  attn_status s = need_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}});
   if (s != ATTN_OK) return s;
-  s = need_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}});
-  if (s != ATTN_OK) return s;
-  if (kv_lens != nullptr && (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
+  if (pb.kv_lens != nullptr && (reinterpret_cast<uintptr_t>(pb.kv_lens) & 3u))
     return fail(ATTN_ERR_INVALID_ARG, "kv_lens is not 4-byte aligned");
   FwdArgs a;
-  a.pb = make_problem(B, Lq, Lkv, Hq, Hkv, d, scale, causal, kv_lens);
+  a.pb = pb;
   a.q = q;
   a.k = k;
   a.v = v;
@@ -250,6 +262,24 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = dtype == ATTN_BF16 ? launch_fwd_bf16(a, st, cs) : launch_fwd_f32(a, st, cs);
   return from_cuda(e, "attn_fwd launch");
+}
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Lq, int Lkv,
+                     int Hq, int Hkv, int d, float scale, int causal, const int32_t* kv_lens, attn_dtype dtype,
+                     attn_stream_t stream) {
+  attn_status s = check_problem(B, Lq, Lkv, Hq, Hkv, d, scale, causal, dtype);
+  if (s != ATTN_OK) return s;
+  return fwd_impl(q, k, v, o, lse, make_problem(B, Lq, Lkv, Hq, Hkv, d, scale, causal, kv_lens), dtype, stream);
+}
+
+attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Lq, int Lkv,
+                            int Hq, int Hkv, int d, float scale, int window_left, int window_right,
+                            const int32_t* kv_lens, attn_dtype dtype, attn_stream_t stream) {
+  attn_status s = check_problem(B, Lq, Lkv, Hq, Hkv, d, scale, 0, dtype);
+  if (s != ATTN_OK) return s;
+  return fwd_impl(q, k, v, o, lse,
+                  make_window_problem(B, Lq, Lkv, Hq, Hkv, d, scale, window_left, window_right, kv_lens), dtype,
+                  stream);
 }
 
 attn_status attn_bwd_preprocess(const void* o, const void* dout, float* delta, int B, int Lq, int Hq, int d,
@@ -283,16 +313,14 @@ size_t attn_bwd_workspace_size(int B, int Lq, int Hq, int d, int deterministic, 
   return bytes;
 }
 
-attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
-                     void* dq, void* dk, void* dv, int B, int Lq, int Lkv, int Hq, int Hkv, int d, float scale,
-                     int causal, const int32_t* kv_lens, attn_dtype dtype, int deterministic, void* workspace,
-                     size_t workspace_bytes, attn_stream_t stream) {
-  attn_status s = check_problem(B, Lq, Lkv, Hq, Hkv, d, scale, causal, dtype);
+static attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, const Problem& pb, attn_dtype dtype, int deterministic,
+                     void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  const int B = pb.B, Lq = pb.Lq, Hq = pb.Hq, d = pb.d;
+  attn_status s = need_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}, {dout, "dout"}, {dq, "dq"},
+                             {dk, "dk"}, {dv, "dv"}});
   if (s != ATTN_OK) return s;
-  s = need_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}, {dout, "dout"}, {dq, "dq"}, {dk, "dk"},
-                 {dv, "dv"}});
-  if (s != ATTN_OK) return s;
-  if (kv_lens != nullptr && (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
+  if (pb.kv_lens != nullptr && (reinterpret_cast<uintptr_t>(pb.kv_lens) & 3u))
     return fail(ATTN_ERR_INVALID_ARG, "kv_lens is not 4-byte aligned");
   if (deterministic != 0 && deterministic != 1) return fail(ATTN_ERR_INVALID_ARG, "deterministic must be 0 or 1");
   const size_t need = attn_bwd_workspace_size(B, Lq, Hq, d, deterministic, dtype);
@@ -302,7 +330,7 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   if (reinterpret_cast<uintptr_t>(workspace) & 255u)
     return fail(ATTN_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
   BwdArgs a;
-  a.pb = make_problem(B, Lq, Lkv, Hq, Hkv, d, scale, causal, kv_lens);
+  a.pb = pb;
   a.q = q;
   a.k = k;
   a.v = v;
@@ -322,6 +350,28 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = dtype == ATTN_BF16 ? launch_bwd_bf16(a, st, cs) : launch_bwd_f32(a, st, cs);
   return from_cuda(e, "attn_bwd launch");
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                     void* dq, void* dk, void* dv, int B, int Lq, int Lkv, int Hq, int Hkv, int d, float scale,
+                     int causal, const int32_t* kv_lens, attn_dtype dtype, int deterministic, void* workspace,
+                     size_t workspace_bytes, attn_stream_t stream) {
+  attn_status s = check_problem(B, Lq, Lkv, Hq, Hkv, d, scale, causal, dtype);
+  if (s != ATTN_OK) return s;
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, make_problem(B, Lq, Lkv, Hq, Hkv, d, scale, causal, kv_lens),
+                  dtype, deterministic, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, int B, int Lq, int Lkv, int Hq, int Hkv,
+                            int d, float scale, int window_left, int window_right, const int32_t* kv_lens,
+                            attn_dtype dtype, int deterministic, void* workspace, size_t workspace_bytes,
+                            attn_stream_t stream) {
+  attn_status s = check_problem(B, Lq, Lkv, Hq, Hkv, d, scale, 0, dtype);
+  if (s != ATTN_OK) return s;
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv,
+                  make_window_problem(B, Lq, Lkv, Hq, Hkv, d, scale, window_left, window_right, kv_lens), dtype,
+                  deterministic, workspace, workspace_bytes, stream);
 }
 
 int attn_decode_num_splits(int B, int Lq, int Lkv, int Hq, int Hkv, int d) {

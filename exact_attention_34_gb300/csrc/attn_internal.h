@@ -12,9 +12,40 @@ namespace attn {
 
 // Problem description shared by every kernel family.  All pointers are device
 // pointers; sizes are validated by the ABI layer before a launch.
+// Position masks.  Key j is valid for query row i of a batch element with kvl
+// valid keys iff lo <= j < hi, where with the row's diagonal position
+// diag = i + kvl - Lq:  lo = max(0, diag - wl),  hi = min(kvl, diag + wr + 1).
+// kWinInf marks an unbounded side: no mask is (kWinInf, kWinInf), causal is
+// (kWinInf, 0), a local window (left, right) bounds both sides.
+constexpr int kWinInf = 1 << 30;
+
+struct Span {
+  int lo, hi;  // [lo, hi); empty when hi <= lo
+};
+
+// Valid keys of query row i.
+__host__ __device__ __forceinline__ Span key_span(int i, int Lq, int kvl, int wl, int wr) {
+  const int diag = i + kvl - Lq;
+  Span s;
+  s.lo = wl >= kWinInf ? 0 : max(0, diag - wl);
+  s.hi = wr >= kWinInf ? kvl : min(kvl, diag + wr + 1);
+  return s;
+}
+
+// Query rows that see key j (j < kvl): i >= j - (kvl - Lq) - wr and
+// i <= j - (kvl - Lq) + wl.
+__host__ __device__ __forceinline__ Span query_span(int j, int Lq, int kvl, int wl, int wr) {
+  const int off = kvl - Lq;
+  Span s;
+  s.lo = wr >= kWinInf ? 0 : max(0, j - off - wr);
+  s.hi = wl >= kWinInf ? Lq : min(Lq, j - off + wl + 1);
+  return s;
+}
+
 struct Problem {
   int B, Lq, Lkv, Hq, Hkv, d, G;
-  int causal;
+  int causal;              // launch-order hint: later query rows see more keys
+  int wl, wr;              // position mask (see key_span)
   float scale;             // softmax scale (> 0)
   const int32_t* kv_lens;  // [B] or nullptr
 };

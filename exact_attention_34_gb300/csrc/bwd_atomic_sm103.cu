@@ -99,10 +99,17 @@ __global__ void __launch_bounds__(512, 1)
   const int j0 = tc.rank * C::kBN, hk = tc.pair % p.Hkv, b = tc.pair / p.Hkv;
   int kvl = p.Lkv;
   if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
-  const int q_first = p.causal ? max(0, j0 + p.Lq - kvl) : 0;
-  const int i_begin = q_first / BM;
-  const int n_qt = (p.Lq + BM - 1) / BM;
-  const int steps_per_head = (j0 < kvl && i_begin < n_qt) ? n_qt - i_begin : 0;
+  // query tiles that see some key of this tile: from the first row that sees
+  // key j0 to the last row that sees the tile's last valid key
+  int i_begin = 0, steps_per_head = 0;
+  if (j0 < kvl) {
+    const int q_lo = query_span(j0, p.Lq, kvl, p.wl, p.wr).lo;
+    const int q_hi = query_span(min(j0 + C::kBN, kvl) - 1, p.Lq, kvl, p.wl, p.wr).hi;
+    if (q_hi > q_lo) {
+      i_begin = q_lo / BM;
+      steps_per_head = (q_hi + BM - 1) / BM - i_begin;
+    }
+  }
   const int T = steps_per_head * p.G;
 
   if (threadIdx.x == 0) {
@@ -278,7 +285,7 @@ __global__ void __launch_bounds__(512, 1)
     const int j = j0 + r;
     const uint32_t t_lane = tbase + (static_cast<uint32_t>(wq * 32) << 16);
     const bool key_ok = j < kvl;
-    const int q_min = p.causal ? j + p.Lq - kvl : -0x7fffffff;
+    const Span qs = key_ok ? query_span(j, p.Lq, kvl, p.wl, p.wr) : Span{0, 0};
     const float sl2 = p.scale_log2;
     const int c0 = 64 * w;
     uint8_t* ds_row = sDS + w * C::kBox + r * 128;
@@ -292,10 +299,10 @@ __global__ void __launch_bounds__(512, 1)
       const float* lse2 = sStat + s * 2 * BM;
       const float* dlt = lse2 + BM;
       float pr[64];
-      if (__all_sync(0xffffffffu, key_ok && q0 + c0 >= q_min))
-        dkdv_probs<false>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, q_min, pr);
+      if (__all_sync(0xffffffffu, key_ok && q0 + c0 >= qs.lo && q0 + c0 + 64 <= qs.hi))
+        dkdv_probs<false>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
       else
-        dkdv_probs<true>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, q_min, pr);
+        dkdv_probs<true>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_ready);

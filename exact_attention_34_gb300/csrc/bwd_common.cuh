@@ -9,11 +9,6 @@ namespace bwd {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ int key_limit(int i, int Lq, int kvl, int causal) {
-  if (!causal) return kvl;
-  return min(kvl, i + 1 + kvl - Lq);
-}
-
 struct BwdKParams {
   const float* lse2;   // [B, Hq, Lq_pad], log2 domain, +inf on empty/pad rows
   const float* delta;  // [B, Hq, Lq_pad]
@@ -22,7 +17,7 @@ struct BwdKParams {
   void* dv;
   float* dq_acc;       // single-pass variant
   const int32_t* kv_lens;
-  int Lq, Lkv, Hq, Hkv, G, causal, Lq_pad, n_tiles, n_pairs, pair_group;
+  int Lq, Lkv, Hq, Hkv, G, causal, wl, wr, Lq_pad, n_tiles, n_pairs, pair_group;
   float scale, scale_log2;
   DeviceStatus* status;
 };
@@ -52,10 +47,12 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16* ds
 }
 
 // P^T for the warpgroup's 64 queries [c0, c0 + 64): probabilities kept in
-// `pr` (fp32) and written packed over columns [c0, c0 + 32) of S^T.
+// `pr` (fp32) and written packed over columns [c0, c0 + 32) of S^T.  With
+// MASK, query q_lo + c0 + c keeps its probability only if the key is valid and
+// the query lies in [q_min, q_max) (the rows that see this key).
 template <bool MASK>
 __device__ __forceinline__ void dkdv_probs(uint32_t s_col, int c0, const float* lse2, float sl2, bool key_ok,
-                                           int q_lo, int q_min, float (&pr)[64]) {
+                                           int q_lo, int q_min, int q_max, float (&pr)[64]) {
   uint32_t sa[32], sb[32];
   tmem_ld32_pair(s_col + c0, s_col + c0 + 32, sa, sb);
 #pragma unroll
@@ -67,7 +64,7 @@ __device__ __forceinline__ void dkdv_probs(uint32_t s_col, int c0, const float* 
       const int c = 4 * i + e;
       const uint32_t raw = c < 32 ? sa[c] : sb[c - 32];
       float pv = ex2_approx(fmaf(__uint_as_float(raw), sl2, -lv[e]));
-      if (MASK) pv = (key_ok && q_lo + c0 + c >= q_min) ? pv : 0.f;
+      if (MASK) pv = (key_ok && q_lo + c0 + c >= q_min && q_lo + c0 + c < q_max) ? pv : 0.f;
       pr[c] = pv;
     }
   }

@@ -151,10 +151,17 @@ __global__ void __launch_bounds__(320, 1)
   const int j0 = tc.rank * C::kBN, hk = tc.pair % p.Hkv, b = tc.pair / p.Hkv;
   int kvl = p.Lkv;
   if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
-  const int q_first = p.causal ? max(0, j0 + p.Lq - kvl) : 0;
-  const int i_begin = q_first / BM;
-  const int n_qt = (p.Lq + BM - 1) / BM;
-  const int steps_per_head = (j0 < kvl && i_begin < n_qt) ? n_qt - i_begin : 0;
+  // query tiles that see some key of this tile: from the first row that sees
+  // key j0 to the last row that sees the tile's last valid key
+  int i_begin = 0, steps_per_head = 0;
+  if (j0 < kvl) {
+    const int q_lo = query_span(j0, p.Lq, kvl, p.wl, p.wr).lo;
+    const int q_hi = query_span(min(j0 + C::kBN, kvl) - 1, p.Lq, kvl, p.wl, p.wr).hi;
+    if (q_hi > q_lo) {
+      i_begin = q_lo / BM;
+      steps_per_head = (q_hi + BM - 1) / BM - i_begin;
+    }
+  }
   const int T = steps_per_head * p.G;
 
   if (threadIdx.x == 0) {
@@ -275,7 +282,7 @@ __global__ void __launch_bounds__(320, 1)
     const int j = j0 + r;
     const uint32_t t_lane = tbase + (static_cast<uint32_t>(wq * 32) << 16);
     const bool key_ok = j < kvl;
-    const int q_min = p.causal ? j + p.Lq - kvl : -0x7fffffff;
+    const Span qs = key_ok ? query_span(j, p.Lq, kvl, p.wl, p.wr) : Span{0, 0};
     const float sl2 = p.scale_log2;
     const int c0 = 64 * w;
     bool ok = true;
@@ -288,10 +295,10 @@ __global__ void __launch_bounds__(320, 1)
       const float* lse2 = sStat + s * 2 * BM;
       const float* dlt = lse2 + BM;
       float pr[64];
-      if (__all_sync(0xffffffffu, key_ok && q0 + c0 >= q_min))
-        dkdv_probs<false>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, q_min, pr);
+      if (__all_sync(0xffffffffu, key_ok && q0 + c0 >= qs.lo && q0 + c0 + 64 <= qs.hi))
+        dkdv_probs<false>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
       else
-        dkdv_probs<true>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, q_min, pr);
+        dkdv_probs<true>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_ready);
@@ -349,7 +356,7 @@ struct DqCfg {
 // Probabilities of the N key columns [c0, c0 + N) of one step (thread =
 // query row), from S at s_col; kept in registers until dP is ready.
 template <int N, bool MASK>
-__device__ __forceinline__ void dq_probs(uint32_t s_col, int c0, float l2, float sl2, int kb, int lim, float* pr) {
+__device__ __forceinline__ void dq_probs(uint32_t s_col, int c0, float l2, float sl2, int kb, Span ks, float* pr) {
   uint32_t sr[N];
   if constexpr (N == 32)
     tmem_ld32(s_col + c0, *reinterpret_cast<uint32_t(*)[32]>(sr));
@@ -358,7 +365,7 @@ __device__ __forceinline__ void dq_probs(uint32_t s_col, int c0, float l2, float
 #pragma unroll
   for (int c = 0; c < N; ++c) {
     float pv = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -l2));
-    if (MASK) pv = (kb + c0 + c < lim) ? pv : 0.f;
+    if (MASK) pv = (kb + c0 + c >= ks.lo && kb + c0 + c < ks.hi) ? pv : 0.f;
     pr[c] = pv;
   }
 }
@@ -427,9 +434,13 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   const int hk = h / p.G;
   int kvl = p.Lkv;
   if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
+  // key tiles [t0, t0 + T): from the first key of row q0 to the last key of
+  // the tile's last row (both ends grow with the row index)
   const int last = min(q0 + C::kBM - 1, p.Lq - 1);
-  const int lim_last = key_limit(last, p.Lq, kvl, p.causal);
-  const int T = lim_last > 0 ? (lim_last + BN - 1) / BN : 0;
+  const int k_lo = key_span(q0, p.Lq, kvl, p.wl, p.wr).lo;
+  const int k_hi = key_span(last, p.Lq, kvl, p.wl, p.wr).hi;
+  const int t0 = k_lo / BN;
+  const int T = k_hi > k_lo ? (k_hi + BN - 1) / BN - t0 : 0;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -474,11 +485,11 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         if (rk > 0 && !(ok = mbar_wait(&empty_k[sk], (rk - 1) & 1, abort_flag, p.status, 31))) break;
         mbar_arrive_expect_tx(&full_k[sk], C::kKVBytes);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sK + sk * C::kKVBytes + c * C::kBox, &tm_k, &full_k[sk], c * 64, t * BN, hk, b);
+          tma_load_4d(sK + sk * C::kKVBytes + c * C::kBox, &tm_k, &full_k[sk], c * 64, (t0 + t) * BN, hk, b);
         if (rv > 0 && !(ok = mbar_wait(&empty_v[sv], (rv - 1) & 1, abort_flag, p.status, 30))) break;
         mbar_arrive_expect_tx(&full_v[sv], C::kKVBytes);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_4d(sV + sv * C::kKVBytes + c * C::kBox, &tm_v, &full_v[sv], c * 64, t * BN, hk, b);
+          tma_load_4d(sV + sv * C::kKVBytes + c * C::kBox, &tm_v, &full_v[sv], c * 64, (t0 + t) * BN, hk, b);
       }
     }
     __syncwarp();
@@ -568,24 +579,25 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     const size_t srow = (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + i;  // i < Lq_pad always
     const float l2 = p.lse2[srow];
     const float dl = p.delta[srow];
-    const int lim = i < p.Lq ? key_limit(i, p.Lq, kvl, p.causal) : 0;
+    Span ks = key_span(i, p.Lq, kvl, p.wl, p.wr);
+    if (i >= p.Lq) ks.lo = ks.hi = 0;
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       ok = __all_sync(0xffffffffu, mbar_wait(&s_ready[t & 1], (t >> 1) & 1, abort_flag, p.status, 37));
       if (!ok) break;
       tc_fence_after();
-      const int kb = t * BN;
+      const int kb = (t0 + t) * BN;
       const uint32_t s_col = t_lane + ((t & 1) ? 384u : 128u);
       const uint32_t dp_col = t_lane + 256;
       float pr[2 * C::kCols];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int c0 = 64 * hh + C::kCols * w;
-        if (__all_sync(0xffffffffu, kb + c0 + C::kCols <= lim))
-          dq_probs<C::kCols, false>(s_col, c0, l2, sl2, kb, lim, pr + hh * C::kCols);
+        if (__all_sync(0xffffffffu, kb + c0 >= ks.lo && kb + c0 + C::kCols <= ks.hi))
+          dq_probs<C::kCols, false>(s_col, c0, l2, sl2, kb, ks, pr + hh * C::kCols);
         else
-          dq_probs<C::kCols, true>(s_col, c0, l2, sl2, kb, lim, pr + hh * C::kCols);
+          dq_probs<C::kCols, true>(s_col, c0, l2, sl2, kb, ks, pr + hh * C::kCols);
       }
       ok = __all_sync(0xffffffffu, mbar_wait(dp_ready, t & 1, abort_flag, p.status, 39));
       if (!ok) break;
@@ -651,6 +663,8 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
   kp.Hkv = pb.Hkv;
   kp.G = pb.G;
   kp.causal = pb.causal;
+  kp.wl = pb.wl;
+  kp.wr = pb.wr;
   kp.Lq_pad = a.Lq_pad;
   kp.scale = pb.scale;
   kp.scale_log2 = pb.scale * kLog2e;

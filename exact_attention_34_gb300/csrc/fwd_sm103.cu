@@ -52,16 +52,10 @@ struct FwdKParams {
   void* o;
   float* lse;
   const int32_t* kv_lens;
-  int Lq, Lkv, Hq, Hkv, G, causal, n_qblocks, n_pairs, pair_group;
+  int Lq, Lkv, Hq, Hkv, G, causal, wl, wr, n_qblocks, n_pairs, pair_group;
   float scale_log2;
   DeviceStatus* status;
 };
-
-// Number of key columns row i may attend to: keys [0, limit) are valid.
-__device__ __forceinline__ int key_limit(int i, int Lq, int kvl, int causal) {
-  if (!causal) return kvl;
-  return min(kvl, i + 1 + kvl - Lq);
-}
 
 template <int D>
 __global__ void __launch_bounds__(320, 1)
@@ -92,16 +86,27 @@ __global__ void __launch_bounds__(320, 1)
   int kvl = p.Lkv;
   if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
 
-  // KV tiles each query tile needs (the limit grows with the row index).
-  auto tiles_for = [&](int x) {
+  // KV tiles [first, first + count) query tile x needs: both ends of a row's
+  // valid keys grow with the row index.  The two tiles share one K/V stream
+  // over the union of their ranges, [jlo, jlo + n) (consecutive rows: no gap).
+  auto tile_range = [&](int x, int& first, int& count) {
     const int row0 = qb * 2 * kBM + x * kBM;
-    if (row0 >= p.Lq) return 0;
+    first = 0;
+    count = 0;
+    if (row0 >= p.Lq) return;
     const int last = min(row0 + kBM - 1, p.Lq - 1);
-    const int lim = key_limit(last, p.Lq, kvl, p.causal);
-    return lim > 0 ? (lim + kBN - 1) / kBN : 0;
+    const int lo = key_span(row0, p.Lq, kvl, p.wl, p.wr).lo;
+    const int hi = key_span(last, p.Lq, kvl, p.wl, p.wr).hi;
+    if (hi <= lo) return;
+    first = lo / kBN;
+    count = (hi + kBN - 1) / kBN - first;
   };
-  const int n_a = tiles_for(0), n_b = tiles_for(1);
-  const int n = max(n_a, n_b);
+  int jlo_a, n_a, jlo_b, n_b;
+  tile_range(0, jlo_a, n_a);
+  tile_range(1, jlo_b, n_b);
+  const int jlo = n_a > 0 ? jlo_a : jlo_b;
+  const int n = n_b > 0 ? jlo_b + n_b - jlo : n_a;
+  const int lo_a = jlo_a - jlo, lo_b = jlo_b - jlo;  // tile starts within the stream
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -140,14 +145,15 @@ __global__ void __launch_bounds__(320, 1)
         for (int h = 0; h < D / 64; ++h)
           tma_load_4d(sQ + x * C::kQTileBytes + h * C::kBoxBytes, &tm_q, q_full, h * 64, row0, hq, b);
       }
-      for (int j = 0; j < n; ++j) {
-        const int st = j % C::kSlots, r = j / C::kSlots;
+      for (int u = 0; u < n; ++u) {
+        const int st = u % C::kSlots, r = u / C::kSlots;
         if (r > 0 && !mbar_wait(&empty[st], (r - 1) & 1, abort_flag, p.status, 1)) break;
         mbar_arrive_expect_tx(&full[st], C::kStageBytes);
         uint8_t* dst = sSlots + st * C::kStageBytes;
+        const int key0 = (jlo + u) * kBN;
         for (int h = 0; h < D / 64; ++h) {
-          tma_load_4d(dst + h * C::kBoxBytes, &tm_k, &full[st], h * 64, j * kBN, hkv, b);
-          tma_load_4d(dst + C::kSlotBytes + h * C::kBoxBytes, &tm_v, &full[st], h * 64, j * kBN, hkv, b);
+          tma_load_4d(dst + h * C::kBoxBytes, &tm_k, &full[st], h * 64, key0, hkv, b);
+          tma_load_4d(dst + C::kSlotBytes + h * C::kBoxBytes, &tm_v, &full[st], h * 64, key0, hkv, b);
         }
       }
     }
@@ -177,39 +183,45 @@ __global__ void __launch_bounds__(320, 1)
         for (int k = 0; k < kBN / 16; ++k)
           mma_ts_d(tbase + 256 + x * 128, tbase + x * 128 + k * 8, dv0, so + k * 128, idesc_o, (acc || k > 0) ? 1u : 0u);
       };
+      // stream step u serves tile x when lo_x <= u < lo_x + n_x; the tile's own
+      // step index u - lo_x drives its barrier parities
+      auto in_a = [&](int u) { return u >= lo_a && u < lo_a + n_a; };
+      auto in_b = [&](int u) { return u >= lo_b && u < lo_b + n_b; };
       bool ok = mbar_wait(q_full, 0, abort_flag, p.status, 2);
       if (ok) ok = mbar_wait(&full[0], 0, abort_flag, p.status, 3);
       if (ok) {
         tc_fence_after();
-        if (n_a > 0) { issue_s(0, 0); mma_commit(&s_full[0]); }
-        if (n_b > 0) { issue_s(1, 0); mma_commit(&s_full[1]); }
+        if (in_a(0)) { issue_s(0, 0); mma_commit(&s_full[0]); }
+        if (in_b(0)) { issue_s(1, 0); mma_commit(&s_full[1]); }
       }
-      for (int j = 0; j < n && ok; ++j) {
-        const int st = j % C::kSlots;
-        const int stn = (j + 1) % C::kSlots;
-        const bool has_next = j + 1 < n;
-        if (j < n_a) {
-          ok = mbar_wait(&p_full[0], j & 1, abort_flag, p.status, 5);
+      for (int u = 0; u < n && ok; ++u) {
+        const int st = u % C::kSlots;
+        const int stn = (u + 1) % C::kSlots;
+        const bool has_next = u + 1 < n;
+        if (in_a(u)) {
+          const int ja = u - lo_a;
+          ok = mbar_wait(&p_full[0], ja & 1, abort_flag, p.status, 5);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(0, st, j > 0);
-          if (j == n_a - 1) mma_commit(&o_full[0]);
+          issue_pv(0, st, ja > 0);
+          if (ja == n_a - 1) mma_commit(&o_full[0]);
         }
         if (has_next) {
-          ok = mbar_wait(&full[stn], ((j + 1) / C::kSlots) & 1, abort_flag, p.status, 6);
+          ok = mbar_wait(&full[stn], ((u + 1) / C::kSlots) & 1, abort_flag, p.status, 6);
           if (!ok) break;
           tc_fence_after();
-          if (j + 1 < n_a) { issue_s(0, stn); mma_commit(&s_full[0]); }
+          if (in_a(u + 1)) { issue_s(0, stn); mma_commit(&s_full[0]); }
         }
-        if (j < n_b) {
-          ok = mbar_wait(&p_full[1], j & 1, abort_flag, p.status, 7);
+        if (in_b(u)) {
+          const int jb = u - lo_b;
+          ok = mbar_wait(&p_full[1], jb & 1, abort_flag, p.status, 7);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(1, st, j > 0);
-          if (j == n_b - 1) mma_commit(&o_full[1]);
+          issue_pv(1, st, jb > 0);
+          if (jb == n_b - 1) mma_commit(&o_full[1]);
         }
         mma_commit(&empty[st]);
-        if (has_next && j + 1 < n_b) { issue_s(1, stn); mma_commit(&s_full[1]); }
+        if (has_next && in_b(u + 1)) { issue_s(1, stn); mma_commit(&s_full[1]); }
       }
     }
     __syncwarp();
@@ -221,7 +233,9 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t t_lane = tbase + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t s_addr = t_lane + x * 128;
     const uint32_t o_addr = t_lane + 256 + x * 128;
-    const int lim = row < p.Lq ? key_limit(row, p.Lq, kvl, p.causal) : 0;
+    Span span = key_span(row, p.Lq, kvl, p.wl, p.wr);
+    if (row >= p.Lq) span.lo = span.hi = 0;
+    const int jbase = x == 0 ? jlo_a : jlo_b;
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY, l_sum = 0.f;
     bool ok = true;
@@ -234,11 +248,11 @@ __global__ void __launch_bounds__(320, 1)
       float s[kBN];
 #pragma unroll
       for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(sraw[i]);
-      const int col0 = j * kBN;
-      if (col0 + kBN > lim) {
+      const int col0 = (jbase + j) * kBN;
+      if (col0 < span.lo || col0 + kBN > span.hi) {
 #pragma unroll
         for (int i = 0; i < kBN; ++i)
-          if (col0 + i >= lim) s[i] = -INFINITY;
+          if (col0 + i < span.lo || col0 + i >= span.hi) s[i] = -INFINITY;
       }
       // row max as a tree (8 independent chains) instead of one 127-long chain
       float mx8[8];
@@ -346,6 +360,8 @@ cudaError_t launch_fwd_bf16_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t s
   kp.Hkv = pb.Hkv;
   kp.G = pb.G;
   kp.causal = pb.causal;
+  kp.wl = pb.wl;
+  kp.wr = pb.wr;
   kp.n_qblocks = (pb.Lq + 2 * kBM - 1) / (2 * kBM);
   kp.n_pairs = pb.B * pb.Hq;
   kp.pair_group = l2_pair_group(2l * pb.Lkv * D * 2, kp.n_pairs, pb.G);

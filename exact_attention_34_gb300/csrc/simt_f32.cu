@@ -24,11 +24,6 @@ constexpr int kPad = 1;   // shared-memory row padding (floats)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-__device__ __forceinline__ int key_limit(int i, int Lq, int kvl, int causal) {
-  if (!causal) return kvl;
-  return min(kvl, i + 1 + kvl - Lq);
-}
-
 __device__ __forceinline__ int seq_len_of(const int32_t* kv_lens, int b, int Lkv) {
   return kv_lens == nullptr ? Lkv : min(max(kv_lens[b], 0), Lkv);
 }
@@ -127,7 +122,7 @@ struct F32FwdParams {
   float* o_part;     // partial mode: [B, Hq, S, Lq, D]
   float* lse_part;   // partial mode: [B, Hq, S, Lq]
   const int32_t* kv_lens;
-  int B, Lq, Lkv, Hq, Hkv, G, causal, num_splits, chunk;
+  int B, Lq, Lkv, Hq, Hkv, G, causal, wl, wr, num_splits, chunk;
   float scale_log2;
 };
 
@@ -148,21 +143,26 @@ __global__ void __launch_bounds__(256) f32_fwd_kernel(const F32FwdParams p) {
   const int k_lo = split * p.chunk;
   const int k_hi = min(kvl, k_lo + p.chunk);
   const int last_row = min(q0 + kT - 1, p.Lq - 1);
-  const int hi_all = min(k_hi, key_limit(last_row, p.Lq, kvl, p.causal));
+  const int hi_all = min(k_hi, key_span(last_row, p.Lq, kvl, p.wl, p.wr).hi);
+  // first key tile (a multiple of kT past k_lo) holding a key of row q0
+  const int lo_first = max(k_lo, key_span(q0, p.Lq, kvl, p.wl, p.wr).lo);
+  const int j_start = k_lo + ((lo_first - k_lo) / kT) * kT;
 
   load_tile<D>(Qs, p.q, b, q0, h, p.Lq, p.Hq);
   float m[4], l[4], acc[4][D / 16];
-  int lim[4];
+  int klo[4], khi[4];
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
     m[a] = -INFINITY;
     l[a] = 0.f;
     const int i = q0 + 4 * ty + a;
-    lim[a] = i < p.Lq ? min(k_hi, key_limit(i, p.Lq, kvl, p.causal)) : 0;
+    const Span ks = key_span(i, p.Lq, kvl, p.wl, p.wr);
+    klo[a] = i < p.Lq ? ks.lo : 0;
+    khi[a] = i < p.Lq ? min(k_hi, ks.hi) : 0;
 #pragma unroll
     for (int e = 0; e < D / 16; ++e) acc[a][e] = 0.f;
   }
-  for (int j0 = k_lo; j0 < hi_all; j0 += kT) {
+  for (int j0 = j_start; j0 < hi_all; j0 += kT) {
     __syncthreads();
     load_tile<D>(Ks, p.k, b, j0, hk, p.Lkv, p.Hkv);
     load_tile<D>(Vs, p.v, b, j0, hk, p.Lkv, p.Hkv);
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(256) f32_fwd_kernel(const F32FwdParams p) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int j = j0 + tx + 16 * c;
-        s[a][c] = (j < lim[a]) ? s[a][c] * p.scale_log2 : -INFINITY;
+        s[a][c] = (j >= klo[a] && j < khi[a]) ? s[a][c] * p.scale_log2 : -INFINITY;
         mx = fmaxf(mx, s[a][c]);
       }
       mx = row_reduce_max(mx);
@@ -230,7 +230,7 @@ struct F32BwdParams {
   float* dv;
   float* dq_acc;  // atomic variant: [B, Lq, Hq, D] (unscaled)
   const int32_t* kv_lens;
-  int B, Lq, Lkv, Hq, Hkv, G, causal;
+  int B, Lq, Lkv, Hq, Hkv, G, causal, wl, wr;
   float scale, scale_log2;
 };
 
@@ -238,7 +238,8 @@ struct F32BwdParams {
 // element [a][c] is key 4*ty + a (of the key tile) and query tx + 16*c.
 template <int D>
 __device__ __forceinline__ void kt_probs(const float* Ks, const float* Vs, const float* Qs, const float* dOs,
-                                         const float* lse2_s, const float* delta_s, const int* lim_s, int j0, int ty,
+                                         const float* lse2_s, const float* delta_s, const int* klo_s,
+                                         const int* khi_s, int j0, int ty,
                                          int tx, float scale_log2, float (&P)[4][4], float (&dS)[4][4]) {
   float s[4][4], dp[4][4];
   tile_dot<D>(Ks, Qs, ty, tx, s);
@@ -247,12 +248,12 @@ __device__ __forceinline__ void kt_probs(const float* Ks, const float* Vs, const
   for (int c = 0; c < 4; ++c) {
     const int qi = tx + 16 * c;
     const float l2 = lse2_s[qi];
-    const int lim = lim_s[qi];
+    const int klo = klo_s[qi], khi = khi_s[qi];
     const float dl = delta_s[qi];
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
       const int j = j0 + 4 * ty + a;
-      const float pv = (j < lim) ? ex2_approx(fmaf(s[a][c], scale_log2, -l2)) : 0.f;
+      const float pv = (j >= klo && j < khi) ? ex2_approx(fmaf(s[a][c], scale_log2, -l2)) : 0.f;
       P[a][c] = pv;
       dS[a][c] = pv * (dp[a][c] - dl);
     }
@@ -273,7 +274,8 @@ __global__ void __launch_bounds__(256) f32_bwd_dkdv_kernel(const F32BwdParams p)
   float* dSt = Pt + kT * (kT + kPad);
   float* lse2_s = dSt + kT * (kT + kPad);
   float* delta_s = lse2_s + kT;
-  int* lim_s = reinterpret_cast<int*>(delta_s + kT);
+  int* klo_s = reinterpret_cast<int*>(delta_s + kT);
+  int* khi_s = klo_s + kT;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int j0 = blockIdx.x * kT, hk = blockIdx.y, b = blockIdx.z;
   const int kvl = seq_len_of(p.kv_lens, b, p.Lkv);
@@ -285,10 +287,12 @@ __global__ void __launch_bounds__(256) f32_bwd_dkdv_kernel(const F32BwdParams p)
   if (j0 < kvl) {
     load_tile<D>(Ks, p.k, b, j0, hk, p.Lkv, p.Hkv);
     load_tile<D>(Vs, p.v, b, j0, hk, p.Lkv, p.Hkv);
-    const int q_first = p.causal ? max(0, j0 + p.Lq - kvl) : 0;
+    // rows that see some key of this tile: [q_first, q_end)
+    const int q_first = query_span(j0, p.Lq, kvl, p.wl, p.wr).lo;
+    const int q_end = query_span(min(j0 + kT, kvl) - 1, p.Lq, kvl, p.wl, p.wr).hi;
     for (int g = 0; g < p.G; ++g) {
       const int h = hk * p.G + g;
-      for (int q0 = (q_first / kT) * kT; q0 < p.Lq; q0 += kT) {
+      for (int q0 = (q_first / kT) * kT; q0 < q_end; q0 += kT) {
         __syncthreads();
         load_tile<D>(Qs, p.q, b, q0, h, p.Lq, p.Hq);
         load_tile<D>(dOs, p.dout, b, q0, h, p.Lq, p.Hq);
@@ -298,11 +302,14 @@ __global__ void __launch_bounds__(256) f32_bwd_dkdv_kernel(const F32BwdParams p)
           const float ls = in ? p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Lq + i] : -INFINITY;
           lse2_s[threadIdx.x] = ls * kLog2e;
           delta_s[threadIdx.x] = in ? p.delta[(static_cast<size_t>(b) * p.Hq + h) * p.Lq + i] : 0.f;
-          lim_s[threadIdx.x] = (in && ls != -INFINITY) ? key_limit(i, p.Lq, kvl, p.causal) : 0;
+          const Span ks = key_span(i, p.Lq, kvl, p.wl, p.wr);
+          const bool any = in && ls != -INFINITY;
+          klo_s[threadIdx.x] = any ? ks.lo : 0;
+          khi_s[threadIdx.x] = any ? ks.hi : 0;
         }
         __syncthreads();
         float P[4][4], dS[4][4];
-        kt_probs<D>(Ks, Vs, Qs, dOs, lse2_s, delta_s, lim_s, j0, ty, tx, p.scale_log2, P, dS);
+        kt_probs<D>(Ks, Vs, Qs, dOs, lse2_s, delta_s, klo_s, khi_s, j0, ty, tx, p.scale_log2, P, dS);
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -362,7 +369,7 @@ __global__ void __launch_bounds__(256) f32_bwd_dq_kernel(const F32BwdParams p) {
   load_tile<D>(Qs, p.q, b, q0, h, p.Lq, p.Hq);
   load_tile<D>(dOs, p.dout, b, q0, h, p.Lq, p.Hq);
   float l2[4], dl[4];
-  int lim[4];
+  int klo[4], khi[4];
   float acc[4][D / 16];
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
@@ -371,13 +378,17 @@ __global__ void __launch_bounds__(256) f32_bwd_dq_kernel(const F32BwdParams p) {
     const float ls = in ? p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Lq + i] : -INFINITY;
     l2[a] = ls * kLog2e;
     dl[a] = in ? p.delta[(static_cast<size_t>(b) * p.Hq + h) * p.Lq + i] : 0.f;
-    lim[a] = (in && ls != -INFINITY) ? key_limit(i, p.Lq, kvl, p.causal) : 0;
+    const Span ks = key_span(i, p.Lq, kvl, p.wl, p.wr);
+    const bool any = in && ls != -INFINITY;
+    klo[a] = any ? ks.lo : 0;
+    khi[a] = any ? ks.hi : 0;
 #pragma unroll
     for (int e = 0; e < D / 16; ++e) acc[a][e] = 0.f;
   }
   const int last_row = min(q0 + kT - 1, p.Lq - 1);
-  const int hi_all = key_limit(last_row, p.Lq, kvl, p.causal);
-  for (int j0 = 0; j0 < hi_all; j0 += kT) {
+  const int hi_all = key_span(last_row, p.Lq, kvl, p.wl, p.wr).hi;
+  const int lo_all = key_span(min(q0, p.Lq - 1), p.Lq, kvl, p.wl, p.wr).lo;
+  for (int j0 = (lo_all / kT) * kT; j0 < hi_all; j0 += kT) {
     __syncthreads();
     load_tile<D>(Ks, p.k, b, j0, hk, p.Lkv, p.Hkv);
     load_tile<D>(Vs, p.v, b, j0, hk, p.Lkv, p.Hkv);
@@ -390,7 +401,7 @@ __global__ void __launch_bounds__(256) f32_bwd_dq_kernel(const F32BwdParams p) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int j = j0 + tx + 16 * c;
-        const float pv = (j < lim[a]) ? ex2_approx(fmaf(s[a][c], p.scale_log2, -l2[a])) : 0.f;
+        const float pv = (j >= klo[a] && j < khi[a]) ? ex2_approx(fmaf(s[a][c], p.scale_log2, -l2[a])) : 0.f;
         dSs[(4 * ty + a) * (kT + kPad) + tx + 16 * c] = pv * (dp[a][c] - dl[a]);
       }
     __syncthreads();
@@ -418,7 +429,7 @@ constexpr int fwd_smem() {
 }
 template <int D>
 constexpr int dkdv_smem() {
-  return (4 * kT * (D + kPad) + 2 * kT * (kT + kPad) + 3 * kT) * 4;
+  return (4 * kT * (D + kPad) + 2 * kT * (kT + kPad) + 4 * kT) * 4;  // + lse2, delta, span lo, span hi
 }
 template <int D>
 constexpr int dq_smem() {
@@ -477,6 +488,8 @@ F32FwdParams fwd_params(const Problem& pb, const void* q, const void* k, const v
   p.Hkv = pb.Hkv;
   p.G = pb.G;
   p.causal = pb.causal;
+  p.wl = pb.wl;
+  p.wr = pb.wr;
   p.scale_log2 = pb.scale * kLog2e;
   return p;
 }
@@ -540,6 +553,8 @@ cudaError_t launch_bwd_f32(const BwdArgs& a, DeviceStatus* st, cudaStream_t s) {
   p.Hkv = pb.Hkv;
   p.G = pb.G;
   p.causal = pb.causal;
+  p.wl = pb.wl;
+  p.wr = pb.wr;
   p.scale = pb.scale;
   p.scale_log2 = pb.scale * kLog2e;
   return pb.d == 64 ? run_bwd<64>(p, !a.deterministic, s) : run_bwd<128>(p, !a.deterministic, s);

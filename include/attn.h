@@ -115,6 +115,29 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * Local-window (sliding) attention, forward and backward ("Attention
+ * performance", section "Short sequences and the default dispatch": window
+ * masks are among the position-only masks the fused kernel computes).  Same
+ * arguments, outputs, workspace and errors as attn_fwd / attn_bwd, with the
+ * causal flag replaced by a window around each row's diagonal: key j is valid
+ * for query row i of batch b iff j < kvl[b] and
+ *     i + kvl[b] - Lq - window_left  <=  j  <=  i + kvl[b] - Lq + window_right
+ * (kvl[b] = Lkv without kv_lens; the diagonal is aligned to the bottom right,
+ * as for causal).  A negative bound is unbounded on that side, so (-1, 0) is
+ * causal and (-1, -1) is no mask.  Key tiles outside every row's window are
+ * neither loaded nor computed; rows whose window holds no valid key get o = 0,
+ * lse = -inf and dq = 0.
+ */
+attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Lq, int Lkv,
+                            int Hq, int Hkv, int d, float scale, int window_left, int window_right,
+                            const int32_t* kv_lens, attn_dtype dtype, attn_stream_t stream);
+attn_status attn_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                            const void* dout, void* dq, void* dk, void* dv, int B, int Lq, int Lkv, int Hq, int Hkv,
+                            int d, float scale, int window_left, int window_right, const int32_t* kv_lens,
+                            attn_dtype dtype, int deterministic, void* workspace, size_t workspace_bytes,
+                            attn_stream_t stream);
+
+/*
  * Split-KV decode for few queries over a long KV cache ("Attention
  * performance", section "Grouped-query attention and decoding"): the keys are
  * split across programs, the G query heads of a KV head (times the Lq rows)
