@@ -379,6 +379,23 @@ def other_rows(args, dev, peaks):
     out["single_pass_fwd_bwd"] = {"ms": round(ms, 4), "tflops": round(3.5 * W.fwd_flops(p) / ms / 1e9, 1),
                                   "kernel_ms": kt, "note": "same workload, atomic-dQ backward (not bitwise reproducible)"}
     del q, k, v, do
+    # local-window mask on the headline shapes: a 1024-key causal sliding
+    # window (flops over the valid (row, key) pairs)
+    p = W.headline()
+    win = (1024, 0)
+    q = torch.randn(p.B, p.Lq, p.Hq, p.d, device=dev, generator=g).to(torch.bfloat16)
+    k, v, do = torch.randn_like(q), torch.randn_like(q), torch.randn_like(q)
+
+    def win_step():
+        o, lse = ea.forward(q, k, v, window=win)
+        ea.backward(q, k, v, o, lse, do, window=win)
+
+    ms = timed(win_step)
+    pairs = sum(min(i + 1, win[0] + 1) for i in range(p.Lq))
+    f_win = 4.0 * p.B * p.Hq * p.d * pairs
+    out["window_fwd_bwd"] = {"ms": round(ms, 4), "tflops": round(3.5 * f_win / ms / 1e9, 1),
+                             "window": list(win), "note": "B4 H8 T8192 d128 bf16, keys within 1024 before the row"}
+    del q, k, v, do
     # KVLenMask + GQA + Lq != Lkv fwd+bwd (flops over valid keys)
     p = W.kvlen_gqa()
     q = torch.randn(p.B, p.Lq, p.Hq, p.d, device=dev, generator=g).to(torch.bfloat16)

@@ -61,7 +61,7 @@ struct DkdvAtomicCfg {
   static constexpr int kRegsWork = 144, kRegsCtl = 80;
 };
 
-template <int D>
+template <int D, bool kLeftBound>
 __global__ void __launch_bounds__(512, 1)
     bwd_dkdv_atomic_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -299,10 +299,12 @@ __global__ void __launch_bounds__(512, 1)
       const float* lse2 = sStat + s * 2 * BM;
       const float* dlt = lse2 + BM;
       float pr[64];
-      if (__all_sync(0xffffffffu, key_ok && q0 + c0 >= qs.lo && q0 + c0 + 64 <= qs.hi))
-        dkdv_probs<false>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
+      // without a left window bound every row after the first that sees the
+      // key sees it too, so only the lower end needs checking
+      if (__all_sync(0xffffffffu, key_ok && q0 + c0 >= qs.lo && (!kLeftBound || q0 + c0 + 64 <= qs.hi)))
+        dkdv_probs<false, kLeftBound>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
       else
-        dkdv_probs<true>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
+        dkdv_probs<true, kLeftBound>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_ready);
@@ -372,11 +374,16 @@ cudaError_t launch_single_pass(const CUtensorMap& tq, const CUtensorMap& tk, con
                                const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, long n_dq,
                                cudaStream_t stream) {
   using C = DkdvAtomicCfg<D>;
-  cudaError_t e = ensure_dynamic_smem<bwd_dkdv_atomic_kernel<D>>(C::kSmemBytes);
+  const bool left = kp.wl < kWinInf;
+  cudaError_t e = left ? ensure_dynamic_smem<bwd_dkdv_atomic_kernel<D, true>>(C::kSmemBytes)
+                       : ensure_dynamic_smem<bwd_dkdv_atomic_kernel<D, false>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   {
     KernelTimer kt("bwd_dkdv_atomic", stream);
-    bwd_dkdv_atomic_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+    if (left)
+      bwd_dkdv_atomic_kernel<D, true><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+    else
+      bwd_dkdv_atomic_kernel<D, false><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -50,7 +50,7 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16* ds
 // `pr` (fp32) and written packed over columns [c0, c0 + 32) of S^T.  With
 // MASK, query q_lo + c0 + c keeps its probability only if the key is valid and
 // the query lies in [q_min, q_max) (the rows that see this key).
-template <bool MASK>
+template <bool MASK, bool kUpper = true>
 __device__ __forceinline__ void dkdv_probs(uint32_t s_col, int c0, const float* lse2, float sl2, bool key_ok,
                                            int q_lo, int q_min, int q_max, float (&pr)[64]) {
   uint32_t sa[32], sb[32];
@@ -64,7 +64,7 @@ __device__ __forceinline__ void dkdv_probs(uint32_t s_col, int c0, const float* 
       const int c = 4 * i + e;
       const uint32_t raw = c < 32 ? sa[c] : sb[c - 32];
       float pv = ex2_approx(fmaf(__uint_as_float(raw), sl2, -lv[e]));
-      if (MASK) pv = (key_ok && q_lo + c0 + c >= q_min && q_lo + c0 + c < q_max) ? pv : 0.f;
+      if (MASK) pv = (key_ok && q_lo + c0 + c >= q_min && (!kUpper || q_lo + c0 + c < q_max)) ? pv : 0.f;
       pr[c] = pv;
     }
   }

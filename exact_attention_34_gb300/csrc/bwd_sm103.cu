@@ -118,7 +118,7 @@ __device__ __forceinline__ void dkdv_dscores(uint32_t dp_col, int c0, const floa
   tmem_st32(dp_col + c0, dk);
 }
 
-template <int D>
+template <int D, bool kLeftBound>
 __global__ void __launch_bounds__(320, 1)
     bwd_dkdv_kernel2(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -295,10 +295,12 @@ __global__ void __launch_bounds__(320, 1)
       const float* lse2 = sStat + s * 2 * BM;
       const float* dlt = lse2 + BM;
       float pr[64];
-      if (__all_sync(0xffffffffu, key_ok && q0 + c0 >= qs.lo && q0 + c0 + 64 <= qs.hi))
-        dkdv_probs<false>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
+      // without a left window bound every row after the first that sees the
+      // key sees it too, so only the lower end needs checking
+      if (__all_sync(0xffffffffu, key_ok && q0 + c0 >= qs.lo && (!kLeftBound || q0 + c0 + 64 <= qs.hi)))
+        dkdv_probs<false, kLeftBound>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
       else
-        dkdv_probs<true>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
+        dkdv_probs<true, kLeftBound>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_ready);
@@ -355,7 +357,7 @@ struct DqCfg {
 
 // Probabilities of the N key columns [c0, c0 + N) of one step (thread =
 // query row), from S at s_col; kept in registers until dP is ready.
-template <int N, bool MASK>
+template <int N, bool MASK, bool kLower = true>
 __device__ __forceinline__ void dq_probs(uint32_t s_col, int c0, float l2, float sl2, int kb, Span ks, float* pr) {
   uint32_t sr[N];
   if constexpr (N == 32)
@@ -365,7 +367,7 @@ __device__ __forceinline__ void dq_probs(uint32_t s_col, int c0, float l2, float
 #pragma unroll
   for (int c = 0; c < N; ++c) {
     float pv = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -l2));
-    if (MASK) pv = (kb + c0 + c >= ks.lo && kb + c0 + c < ks.hi) ? pv : 0.f;
+    if (MASK) pv = ((!kLower || kb + c0 + c >= ks.lo) && kb + c0 + c < ks.hi) ? pv : 0.f;
     pr[c] = pv;
   }
 }
@@ -400,7 +402,7 @@ __device__ __forceinline__ void dq_dscores(uint32_t s_col, uint32_t dp_col, int 
 // two 64-key halves so the dQ MMAs of half 0 overlap the second half.  K tiles
 // use a 3-slot ring (a K tile is read by S and later by dQ), V tiles a 2-slot
 // ring.
-template <int D>
+template <int D, bool kLeftBound>
 __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -439,7 +441,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   const int last = min(q0 + C::kBM - 1, p.Lq - 1);
   const int k_lo = key_span(q0, p.Lq, kvl, p.wl, p.wr).lo;
   const int k_hi = key_span(last, p.Lq, kvl, p.wl, p.wr).hi;
-  const int t0 = k_lo / BN;
+  const int t0 = kLeftBound ? k_lo / BN : 0;
   const int T = k_hi > k_lo ? (k_hi + BN - 1) / BN - t0 : 0;
 
   if (threadIdx.x == 0) {
@@ -580,6 +582,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     const float l2 = p.lse2[srow];
     const float dl = p.delta[srow];
     Span ks = key_span(i, p.Lq, kvl, p.wl, p.wr);
+    if (!kLeftBound) ks.lo = 0;
     if (i >= p.Lq) ks.lo = ks.hi = 0;
     const float sl2 = p.scale_log2;
     bool ok = true;
@@ -594,10 +597,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int c0 = 64 * hh + C::kCols * w;
-        if (__all_sync(0xffffffffu, kb + c0 >= ks.lo && kb + c0 + C::kCols <= ks.hi))
-          dq_probs<C::kCols, false>(s_col, c0, l2, sl2, kb, ks, pr + hh * C::kCols);
+        if (__all_sync(0xffffffffu, (!kLeftBound || kb + c0 >= ks.lo) && kb + c0 + C::kCols <= ks.hi))
+          dq_probs<C::kCols, false, kLeftBound>(s_col, c0, l2, sl2, kb, ks, pr + hh * C::kCols);
         else
-          dq_probs<C::kCols, true>(s_col, c0, l2, sl2, kb, ks, pr + hh * C::kCols);
+          dq_probs<C::kCols, true, kLeftBound>(s_col, c0, l2, sl2, kb, ks, pr + hh * C::kCols);
       }
       ok = __all_sync(0xffffffffu, mbar_wait(dp_ready, t & 1, abort_flag, p.status, 39));
       if (!ok) break;
@@ -686,11 +689,16 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
       return launch_single_pass<D>(tq128, tk, tv, tdo128, kp, grid, static_cast<long>(pb.B) * pb.Lq * pb.Hq * D,
                                    stream);
     using C = DkdvCfg2<D>;
-    e = ensure_dynamic_smem<bwd_dkdv_kernel2<D>>(C::kSmemBytes);
+    const bool left = pb.wl < kWinInf;
+    e = left ? ensure_dynamic_smem<bwd_dkdv_kernel2<D, true>>(C::kSmemBytes)
+             : ensure_dynamic_smem<bwd_dkdv_kernel2<D, false>>(C::kSmemBytes);
     if (e != cudaSuccess) return e;
     {
       KernelTimer kt("bwd_dkdv", stream);
-      bwd_dkdv_kernel2<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq128, tk, tv, tdo128, kp);
+      if (left)
+        bwd_dkdv_kernel2<D, true><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq128, tk, tv, tdo128, kp);
+      else
+        bwd_dkdv_kernel2<D, false><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq128, tk, tv, tdo128, kp);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -708,10 +716,15 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
     kp.n_pairs = pb.B * pb.Hq;
     kp.pair_group = l2_pair_group(2l * pb.Lkv * D * 2, kp.n_pairs, pb.G);
     dim3 grid(kp.n_pairs * kp.n_tiles);
-    e = ensure_dynamic_smem<bwd_dq_kernel<D>>(C::kSmemBytes);
+    const bool left = pb.wl < kWinInf;
+    e = left ? ensure_dynamic_smem<bwd_dq_kernel<D, true>>(C::kSmemBytes)
+             : ensure_dynamic_smem<bwd_dq_kernel<D, false>>(C::kSmemBytes);
     if (e != cudaSuccess) return e;
     KernelTimer kt("bwd_dq", stream);
-    bwd_dq_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+    if (left)
+      bwd_dq_kernel<D, true><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+    else
+      bwd_dq_kernel<D, false><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
     return cudaGetLastError();
   }
 }

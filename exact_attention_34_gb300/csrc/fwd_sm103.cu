@@ -57,7 +57,7 @@ struct FwdKParams {
   DeviceStatus* status;
 };
 
-template <int D>
+template <int D, bool kLeftBound>
 __global__ void __launch_bounds__(320, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdKParams p) {
@@ -104,9 +104,10 @@ __global__ void __launch_bounds__(320, 1)
   int jlo_a, n_a, jlo_b, n_b;
   tile_range(0, jlo_a, n_a);
   tile_range(1, jlo_b, n_b);
-  const int jlo = n_a > 0 ? jlo_a : jlo_b;
-  const int n = n_b > 0 ? jlo_b + n_b - jlo : n_a;
-  const int lo_a = jlo_a - jlo, lo_b = jlo_b - jlo;  // tile starts within the stream
+  // without a left bound every range starts at key tile 0 (compile-time)
+  const int jlo = kLeftBound ? (n_a > 0 ? jlo_a : jlo_b) : 0;
+  const int n = kLeftBound ? (n_b > 0 ? jlo_b + n_b - jlo : n_a) : max(n_a, n_b);
+  const int lo_a = kLeftBound ? jlo_a - jlo : 0, lo_b = kLeftBound ? jlo_b - jlo : 0;  // tile starts in the stream
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -233,9 +234,12 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t t_lane = tbase + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t s_addr = t_lane + x * 128;
     const uint32_t o_addr = t_lane + 256 + x * 128;
+    // a row's valid keys [span.lo, span.hi); without a left window bound the
+    // lower end is 0 (kept out of the registers of the causal/unmasked build)
     Span span = key_span(row, p.Lq, kvl, p.wl, p.wr);
+    if (!kLeftBound) span.lo = 0;
     if (row >= p.Lq) span.lo = span.hi = 0;
-    const int jbase = x == 0 ? jlo_a : jlo_b;
+    const int jbase = kLeftBound ? (x == 0 ? jlo_a : jlo_b) : 0;
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY, l_sum = 0.f;
     bool ok = true;
@@ -249,10 +253,10 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
       for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(sraw[i]);
       const int col0 = (jbase + j) * kBN;
-      if (col0 < span.lo || col0 + kBN > span.hi) {
+      if ((kLeftBound && col0 < span.lo) || col0 + kBN > span.hi) {
 #pragma unroll
         for (int i = 0; i < kBN; ++i)
-          if (col0 + i < span.lo || col0 + i >= span.hi) s[i] = -INFINITY;
+          if ((kLeftBound && col0 + i < span.lo) || col0 + i >= span.hi) s[i] = -INFINITY;
       }
       // row max as a tree (8 independent chains) instead of one 127-long chain
       float mx8[8];
@@ -348,7 +352,8 @@ cudaError_t launch_fwd_bf16_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t s
   if (!make_bshd_tmap(&tq, a.q, true, pb.B, pb.Lq, pb.Hq, D, 64, kBM)) return cudaErrorInvalidValue;
   if (!make_bshd_tmap(&tk, a.k, true, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
   if (!make_bshd_tmap(&tv, a.v, true, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
-  cudaError_t e = ensure_dynamic_smem<fwd_bf16_kernel<D>>(C::kSmemBytes);
+  cudaError_t e = pb.wl < kWinInf ? ensure_dynamic_smem<fwd_bf16_kernel<D, true>>(C::kSmemBytes)
+                                  : ensure_dynamic_smem<fwd_bf16_kernel<D, false>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   FwdKParams kp;
   kp.o = a.o;
@@ -370,7 +375,10 @@ cudaError_t launch_fwd_bf16_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t s
   dim3 grid(kp.n_pairs * kp.n_qblocks);
   {
     KernelTimer kt("fwd", stream);
-    fwd_bf16_kernel<D><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
+    if (pb.wl < kWinInf)
+      fwd_bf16_kernel<D, true><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
+    else
+      fwd_bf16_kernel<D, false><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
   }
   return cudaGetLastError();
 }
