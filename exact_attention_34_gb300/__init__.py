@@ -31,8 +31,9 @@ ATTN_ERR_DEVICE = 5
 
 ATTN_BF16 = 0
 ATTN_FP32 = 1
+ATTN_FP16 = 2
 
-_DT = {torch.bfloat16: ATTN_BF16, torch.float32: ATTN_FP32}
+_DT = {torch.bfloat16: ATTN_BF16, torch.float32: ATTN_FP32, torch.float16: ATTN_FP16}
 
 
 class AttnError(RuntimeError):

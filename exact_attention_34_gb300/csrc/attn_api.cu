@@ -91,7 +91,8 @@ attn_status check_problem(int B, int Lq, int Lkv, int Hq, int Hkv, int d, float 
   if (Hq % Hkv != 0) return fail(ATTN_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
   if (!(std::isfinite(scale) && scale > 0.f)) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and > 0");
   if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
-  if (dtype != ATTN_BF16 && dtype != ATTN_FP32) return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+  if (dtype != ATTN_BF16 && dtype != ATTN_FP32 && dtype != ATTN_FP16)
+    return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
   if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head_dim %d not supported (64 or 128)", d);
   // 32-bit index headroom for per-row offsets (elements of one tensor)
   const double big = static_cast<double>(B) * Lq * Hq * d;
@@ -118,6 +119,7 @@ Problem make_problem(int B, int Lq, int Lkv, int Hq, int Hkv, int d, float scale
   p.Hkv = Hkv;
   p.d = d;
   p.G = Hq / Hkv;
+  p.f16 = 0;
   p.causal = causal;
   p.wl = kWinInf;
   p.wr = causal ? 0 : kWinInf;
@@ -150,18 +152,21 @@ size_t bwd_rowstat_bytes(int B, int Lq, int Hq) {
 
 }  // namespace
 
-bool make_bshd_tmap(CUtensorMap* map, const void* base, bool bf16, int B, int L, int H, int d, int box_inner,
+bool make_bshd_tmap(CUtensorMap* map, const void* base, int elem, int B, int L, int H, int d, int box_inner,
                     int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
-  const cuuint64_t es = bf16 ? 2 : 4;
+  const cuuint64_t es = elem == kElemF32 ? 4 : 2;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(B)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(H) * d * es, static_cast<cuuint64_t>(d) * es,
                            static_cast<cuuint64_t>(L) * H * d * es};
   cuuint32_t box[4] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows), 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+  const CUtensorMapDataType ty = elem == kElemF32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : elem == kElemF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = enc(map, ty, 4,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -260,7 +265,8 @@ static attn_status fwd_impl(const void* q, const void* k, const void* v, void* o
   a.lse = lse;
   DeviceStatus* st = status_ptr();
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = dtype == ATTN_BF16 ? launch_fwd_bf16(a, st, cs) : launch_fwd_f32(a, st, cs);
+  a.pb.f16 = dtype == ATTN_FP16;
+  cudaError_t e = dtype == ATTN_FP32 ? launch_fwd_f32(a, st, cs) : launch_fwd_16(a, st, cs);
   return from_cuda(e, "attn_fwd launch");
 }
 
@@ -300,7 +306,7 @@ attn_status attn_bwd_preprocess(const void* o, const void* dout, float* delta, i
   pa.Lq_pad = Lq;
   pa.Hq = Hq;
   pa.d = d;
-  pa.is_bf16 = dtype == ATTN_BF16;
+  pa.elem = dtype == ATTN_FP32 ? kElemF32 : dtype == ATTN_FP16 ? kElemF16 : kElemBF16;
   cudaError_t e = launch_bwd_preprocess(pa, reinterpret_cast<cudaStream_t>(stream));
   return from_cuda(e, "attn_bwd_preprocess launch");
 }
@@ -348,7 +354,8 @@ static attn_status bwd_impl(const void* q, const void* k, const void* v, const v
   a.deterministic = deterministic;
   DeviceStatus* st = status_ptr();
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = dtype == ATTN_BF16 ? launch_bwd_bf16(a, st, cs) : launch_bwd_f32(a, st, cs);
+  a.pb.f16 = dtype == ATTN_FP16;
+  cudaError_t e = dtype == ATTN_FP32 ? launch_bwd_f32(a, st, cs) : launch_bwd_16(a, st, cs);
   return from_cuda(e, "attn_bwd launch");
 }
 
@@ -424,7 +431,8 @@ attn_status attn_decode_splitkv(const void* q, const void* k_cache, const void* 
   a.chunk = 128 * ((per + 127) / 128);
   DeviceStatus* st = status_ptr();
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = dtype == ATTN_BF16 ? launch_decode_bf16(a, st, cs) : launch_decode_f32(a, st, cs);
+  a.pb.f16 = dtype == ATTN_FP16;
+  cudaError_t e = dtype == ATTN_FP32 ? launch_decode_f32(a, st, cs) : launch_decode_16(a, st, cs);
   return from_cuda(e, "attn_decode_splitkv launch");
 }
 
@@ -435,7 +443,8 @@ attn_status attn_decode_combine(const float* o_part, const float* lse_part, void
   s = need_ptrs({{o_part, "o_part"}, {lse_part, "lse_part"}, {o, "o"}, {lse, "lse"}});
   if (s != ATTN_OK) return s;
   if (num_splits <= 0) return fail(ATTN_ERR_INVALID_ARG, "num_splits must be > 0");
-  cudaError_t e = launch_decode_combine(o_part, lse_part, o, lse, B, Lq, Hq, d, num_splits, dtype == ATTN_BF16,
+  cudaError_t e = launch_decode_combine(o_part, lse_part, o, lse, B, Lq, Hq, d, num_splits,
+                                        dtype == ATTN_FP32 ? kElemF32 : dtype == ATTN_FP16 ? kElemF16 : kElemBF16,
                                         reinterpret_cast<cudaStream_t>(stream));
   return from_cuda(e, "attn_decode_combine launch");
 }

@@ -42,8 +42,12 @@ __host__ __device__ __forceinline__ Span query_span(int j, int Lq, int kvl, int 
   return s;
 }
 
+// Element formats of the tensors a call reads and writes.
+enum Elem : int { kElemF32 = 0, kElemBF16 = 1, kElemF16 = 2 };
+
 struct Problem {
   int B, Lq, Lkv, Hq, Hkv, d, G;
+  int f16;                 // 16-bit kernels: 1 = fp16 tensors, 0 = bf16
   int causal;              // launch-order hint: later query rows see more keys
   int wl, wr;              // position mask (see key_span)
   float scale;             // softmax scale (> 0)
@@ -59,7 +63,7 @@ struct FwdArgs {
   void* o;
   float* lse;
 };
-cudaError_t launch_fwd_bf16(const FwdArgs& a, DeviceStatus* st, cudaStream_t s);
+cudaError_t launch_fwd_16(const FwdArgs& a, DeviceStatus* st, cudaStream_t s);  // bf16 or fp16
 cudaError_t launch_fwd_f32(const FwdArgs& a, DeviceStatus* st, cudaStream_t s);
 
 // ---- backward --------------------------------------------------------------
@@ -90,10 +94,11 @@ struct PreprocessArgs {
   float* delta;
   float* lse2;       // nullable
   float* dq_acc;     // nullable
-  int B, Lq, Lq_pad, Hq, d, is_bf16;
+  int B, Lq, Lq_pad, Hq, d;
+  int elem;  // Elem of o and dout
 };
 cudaError_t launch_bwd_preprocess(const PreprocessArgs& a, cudaStream_t s);
-cudaError_t launch_bwd_bf16(const BwdArgs& a, DeviceStatus* st, cudaStream_t s);
+cudaError_t launch_bwd_16(const BwdArgs& a, DeviceStatus* st, cudaStream_t s);
 cudaError_t launch_bwd_f32(const BwdArgs& a, DeviceStatus* st, cudaStream_t s);
 
 // ---- split-KV decode ---------------------------------------------------------
@@ -107,15 +112,15 @@ struct DecodeArgs {
   int num_splits;
   int chunk;  // keys per split, a multiple of 128
 };
-cudaError_t launch_decode_bf16(const DecodeArgs& a, DeviceStatus* st, cudaStream_t s);
+cudaError_t launch_decode_16(const DecodeArgs& a, DeviceStatus* st, cudaStream_t s);
 cudaError_t launch_decode_f32(const DecodeArgs& a, DeviceStatus* st, cudaStream_t s);
 cudaError_t launch_decode_combine(const float* o_part, const float* lse_part, void* o, float* lse, int B, int Lq,
-                                  int Hq, int d, int num_splits, int is_bf16, cudaStream_t s);
+                                  int Hq, int d, int num_splits, int elem, cudaStream_t s);
 
 // ---- host helpers (attn_api.cu) ---------------------------------------------
 // Tiled TMA descriptor over a [B, L, H, d] tensor: dims (d, L, H, B), box
 // (box_inner, box_rows, 1, 1), 128-byte swizzle, zero fill out of bounds.
-bool make_bshd_tmap(CUtensorMap* map, const void* base, bool bf16, int B, int L, int H, int d, int box_inner,
+bool make_bshd_tmap(CUtensorMap* map, const void* base, int elem, int B, int L, int H, int d, int box_inner,
                     int box_rows);
 
 // Number of SMs of the current device (cached per device).

@@ -1,4 +1,4 @@
-// Single-pass backward, bf16, head_dim 64/128: dK and dV as in the two-pass
+// Single-pass backward, bf16 or fp16, head_dim 64/128: dK and dV as in the two-pass
 // variant, while dQ is summed over key tiles with float32 atomic adds into a
 // buffer that a convert kernel scales and casts to bf16 (probjax "Attention
 // performance", section "When to use which", backward pass: dQ = scale * dS K).
@@ -61,7 +61,7 @@ struct DkdvAtomicCfg {
   static constexpr int kRegsWork = 144, kRegsCtl = 80;
 };
 
-template <int D, bool kLeftBound>
+template <int D, bool kLeftBound, bool kF16>
 __global__ void __launch_bounds__(512, 1)
     bwd_dkdv_atomic_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -166,9 +166,9 @@ __global__ void __launch_bounds__(512, 1)
       }
     } else if (warp == 13 && lane == 0 && T > 0) {
       // ---------------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc_st = idesc_bf16_f32(128, BM, 0, 0);   // K x Q^T, V x dO^T
-      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, 0, 1);   // A (K-major or TMEM) x (dO|Q MN-major)
-      constexpr uint32_t idesc_dq = idesc_bf16_f32(128, BM, 1, 1);   // K^T (MN-major) x dS^T (MN-major)
+      constexpr uint32_t idesc_st = idesc_16_f32<kF16>(128, BM, 0, 0);   // K x Q^T, V x dO^T
+      constexpr uint32_t idesc_acc = idesc_16_f32<kF16>(128, D, 0, 1);   // A (K-major or TMEM) x (dO|Q MN-major)
+      constexpr uint32_t idesc_dq = idesc_16_f32<kF16>(128, BM, 1, 1);   // K^T (MN-major) x dS^T (MN-major)
       const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ), ds_addr = smem_u32(sDS);
       const SDesc dk_base = sdesc_split(k_addr, 16, 1024), dv_base = sdesc_split(v_addr, 16, 1024);
       const SDesc dq_base = sdesc_split(q_addr, 16, 1024), ddo_base = sdesc_split(q_addr + C::kQBytes, 16, 1024);
@@ -302,9 +302,9 @@ __global__ void __launch_bounds__(512, 1)
       // without a left window bound every row after the first that sees the
       // key sees it too, so only the lower end needs checking
       if (__all_sync(0xffffffffu, key_ok && q0 + c0 >= qs.lo && (!kLeftBound || q0 + c0 + 64 <= qs.hi)))
-        dkdv_probs<false, kLeftBound>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
+        dkdv_probs<false, kLeftBound, kF16>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
       else
-        dkdv_probs<true, kLeftBound>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
+        dkdv_probs<true, kLeftBound, kF16>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_ready);
@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(512, 1)
             const int c = 8 * ch + 2 * e;
             const float4 d4 = *reinterpret_cast<const float4*>(dlt + c0 + (c & ~3));
             const float dv0 = (c & 3) ? d4.z : d4.x, dv1 = (c & 3) ? d4.w : d4.y;
-            pk[e] = pack_bf16x2(pr[c] * (__uint_as_float(da[c - 32 * hh]) - dv0),
+            pk[e] = pack2<kF16>(pr[c] * (__uint_as_float(da[c - 32 * hh]) - dv0),
                                 pr[c + 1] * (__uint_as_float(da[c + 1 - 32 * hh]) - dv1));
           }
           *reinterpret_cast<uint4*>(ds_row + ((ch ^ (r & 7)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -341,9 +341,9 @@ __global__ void __launch_bounds__(512, 1)
       const bool st = j < p.Lkv;
       const size_t off = ((static_cast<size_t>(b) * p.Lkv + (st ? j : 0)) * p.Hkv + hk) * D;
       if (w == 0)
-        store_row_bf16<D>(t_lane + 0, reinterpret_cast<__nv_bfloat16*>(p.dk) + off, p.scale, st, T == 0);
+        store_row16<D, kF16>(t_lane + 0, reinterpret_cast<uint16_t*>(p.dk) + off, p.scale, st, T == 0);
       else
-        store_row_bf16<D>(t_lane + 128, reinterpret_cast<__nv_bfloat16*>(p.dv) + off, 1.0f, st, T == 0);
+        store_row16<D, kF16>(t_lane + 128, reinterpret_cast<uint16_t*>(p.dv) + off, 1.0f, st, T == 0);
     }
   }
 
@@ -356,48 +356,60 @@ __global__ void __launch_bounds__(512, 1)
 }
 
 // dq = scale * dq_acc cast to bf16 (single-pass variant)
-__global__ void dq_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq, long n4,
+template <bool kF16>
+__global__ void dq_convert_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq, long n4,
                                   float scale) {
   const long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n4) return;
   const float4 a = reinterpret_cast<const float4*>(acc)[i];
   uint2 o;
-  o.x = pack_bf16x2(a.x * scale, a.y * scale);
-  o.y = pack_bf16x2(a.z * scale, a.w * scale);
+  o.x = pack2<kF16>(a.x * scale, a.y * scale);
+  o.y = pack2<kF16>(a.z * scale, a.w * scale);
   reinterpret_cast<uint2*>(dq)[i] = o;
+}
+
+}  // namespace
+
+namespace {
+
+template <int D, bool kLeftBound, bool kF16>
+cudaError_t launch_single_pass_inst(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                    const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, long n_dq,
+                                    cudaStream_t stream) {
+  using C = DkdvAtomicCfg<D>;
+  cudaError_t e = ensure_dynamic_smem<bwd_dkdv_atomic_kernel<D, kLeftBound, kF16>>(C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  {
+    KernelTimer kt("bwd_dkdv_atomic", stream);
+    bwd_dkdv_atomic_kernel<D, kLeftBound, kF16><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long n4 = n_dq / 4;
+  KernelTimer kt("dq_convert", stream);
+  dq_convert_kernel<kF16><<<static_cast<int>((n4 + 255) / 256), 256, 0, stream>>>(
+      kp.dq_acc, static_cast<uint16_t*>(kp.dq), n4, kp.scale);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 template <int D>
 cudaError_t launch_single_pass(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, long n_dq,
+                               const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, long n_dq, bool f16,
                                cudaStream_t stream) {
-  using C = DkdvAtomicCfg<D>;
   const bool left = kp.wl < kWinInf;
-  cudaError_t e = left ? ensure_dynamic_smem<bwd_dkdv_atomic_kernel<D, true>>(C::kSmemBytes)
-                       : ensure_dynamic_smem<bwd_dkdv_atomic_kernel<D, false>>(C::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  {
-    KernelTimer kt("bwd_dkdv_atomic", stream);
-    if (left)
-      bwd_dkdv_atomic_kernel<D, true><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
-    else
-      bwd_dkdv_atomic_kernel<D, false><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
-  }
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const long n4 = n_dq / 4;
-  KernelTimer kt("dq_convert", stream);
-  dq_convert_kernel<<<static_cast<int>((n4 + 255) / 256), 256, 0, stream>>>(
-      kp.dq_acc, static_cast<__nv_bfloat16*>(kp.dq), n4, kp.scale);
-  return cudaGetLastError();
+  if (f16)
+    return left ? launch_single_pass_inst<D, true, true>(tq, tk, tv, tdo, kp, grid, n_dq, stream)
+                : launch_single_pass_inst<D, false, true>(tq, tk, tv, tdo, kp, grid, n_dq, stream);
+  return left ? launch_single_pass_inst<D, true, false>(tq, tk, tv, tdo, kp, grid, n_dq, stream)
+              : launch_single_pass_inst<D, false, false>(tq, tk, tv, tdo, kp, grid, n_dq, stream);
 }
 
 template cudaError_t launch_single_pass<64>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                            const CUtensorMap&, const BwdKParams&, dim3, long, cudaStream_t);
+                                            const CUtensorMap&, const BwdKParams&, dim3, long, bool, cudaStream_t);
 template cudaError_t launch_single_pass<128>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                             const CUtensorMap&, const BwdKParams&, dim3, long, cudaStream_t);
+                                             const CUtensorMap&, const BwdKParams&, dim3, long, bool, cudaStream_t);
 
 }  // namespace bwd
 }  // namespace attn

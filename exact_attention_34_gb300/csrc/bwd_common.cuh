@@ -22,9 +22,10 @@ struct BwdKParams {
   DeviceStatus* status;
 };
 
-// Store one row of D fp32 values from TMEM (columns col..col+D) as bf16, times `mul`.
-template <int D>
-__device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16* dst, float mul, bool do_store,
+// Store one row of D fp32 values from TMEM (columns col..col+D) in the 16-bit
+// format (fp16 when kF16, else bf16), times `mul`.
+template <int D, bool kF16>
+__device__ __forceinline__ void store_row16(uint32_t taddr, uint16_t* dst, float mul, bool do_store,
                                                bool zero) {
 #pragma unroll
   for (int c = 0; c < D / 32; ++c) {
@@ -37,7 +38,7 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16* ds
     }
     uint32_t pk[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+    for (int i = 0; i < 16; ++i) pk[i] = pack2<kF16>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
     if (do_store) {
       uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
@@ -50,7 +51,7 @@ __device__ __forceinline__ void store_row_bf16(uint32_t taddr, __nv_bfloat16* ds
 // `pr` (fp32) and written packed over columns [c0, c0 + 32) of S^T.  With
 // MASK, query q_lo + c0 + c keeps its probability only if the key is valid and
 // the query lies in [q_min, q_max) (the rows that see this key).
-template <bool MASK, bool kUpper = true>
+template <bool MASK, bool kUpper, bool kF16>
 __device__ __forceinline__ void dkdv_probs(uint32_t s_col, int c0, const float* lse2, float sl2, bool key_ok,
                                            int q_lo, int q_min, int q_max, float (&pr)[64]) {
   uint32_t sa[32], sb[32];
@@ -70,7 +71,7 @@ __device__ __forceinline__ void dkdv_probs(uint32_t s_col, int c0, const float* 
   }
   uint32_t pk[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2(pr[2 * i], pr[2 * i + 1]);
+  for (int i = 0; i < 32; ++i) pk[i] = pack2<kF16>(pr[2 * i], pr[2 * i + 1]);
   tmem_st32(s_col + c0, pk);
 }
 
@@ -79,7 +80,7 @@ __device__ __forceinline__ void dkdv_probs(uint32_t s_col, int c0, const float* 
 // All four tensor maps use boxes of 64 columns x 128 rows.
 template <int D>
 cudaError_t launch_single_pass(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, long n_dq,
+                               const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, long n_dq, bool f16,
                                cudaStream_t stream);
 
 }  // namespace bwd

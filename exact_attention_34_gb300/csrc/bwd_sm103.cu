@@ -1,4 +1,4 @@
-// Backward attention, bf16, head_dim 64/128, on the sm_103a tensor cores.
+// Backward attention, bf16 or fp16, head_dim 64/128, on the sm_103a tensor cores.
 //
 // Method (probjax "Attention performance", section "When to use which",
 // backward pass): the probabilities are recomputed from the forward's
@@ -63,8 +63,8 @@ struct DkdvCfg2 {
 };
 
 // Store columns [c0, c0 + NC) of one fp32 TMEM row as bf16 (times mul).
-template <int NC>
-__device__ __forceinline__ void store_cols_bf16(uint32_t taddr, __nv_bfloat16* dst, float mul, bool do_store,
+template <int NC, bool kF16>
+__device__ __forceinline__ void store_cols16(uint32_t taddr, uint16_t* dst, float mul, bool do_store,
                                                 bool zero) {
 #pragma unroll
   for (int c = 0; c < NC / 16; ++c) {
@@ -77,7 +77,7 @@ __device__ __forceinline__ void store_cols_bf16(uint32_t taddr, __nv_bfloat16* d
     }
     uint32_t pk[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+    for (int i = 0; i < 8; ++i) pk[i] = pack2<kF16>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
     if (do_store) {
       uint4* d4 = reinterpret_cast<uint4*>(dst + c * 16);
       d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -97,6 +97,7 @@ __device__ __forceinline__ constexpr uint32_t packed_col(int h, int k) {
 
 // dS^T = P^T (dP^T - delta) for the same 64 queries, written packed over
 // columns [c0, c0 + 32) of dP^T.
+template <bool kF16>
 __device__ __forceinline__ void dkdv_dscores(uint32_t dp_col, int c0, const float* dlt, const float (&pr)[64]) {
   uint32_t da[32], db[32];
   tmem_ld32_pair(dp_col + c0, dp_col + c0 + 32, da, db);
@@ -112,13 +113,13 @@ __device__ __forceinline__ void dkdv_dscores(uint32_t dp_col, int c0, const floa
       const uint32_t raw = c < 32 ? da[c] : db[c - 32];
       ds[e] = pr[c] * (__uint_as_float(raw) - dv[e]);
     }
-    dk[2 * i] = pack_bf16x2(ds[0], ds[1]);
-    dk[2 * i + 1] = pack_bf16x2(ds[2], ds[3]);
+    dk[2 * i] = pack2<kF16>(ds[0], ds[1]);
+    dk[2 * i + 1] = pack2<kF16>(ds[2], ds[3]);
   }
   tmem_st32(dp_col + c0, dk);
 }
 
-template <int D, bool kLeftBound>
+template <int D, bool kLeftBound, bool kF16>
 __global__ void __launch_bounds__(320, 1)
     bwd_dkdv_kernel2(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -215,8 +216,8 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp == 9) {
     if (lane == 0 && T > 0) {
-      constexpr uint32_t idesc_st = idesc_bf16_f32(128, BM, 0, 0);  // K x Q^T, V x dO^T
-      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, D, 0, 1);  // (P^T|dS^T from TMEM) x (dO|Q MN-major)
+      constexpr uint32_t idesc_st = idesc_16_f32<kF16>(128, BM, 0, 0);  // K x Q^T, V x dO^T
+      constexpr uint32_t idesc_acc = idesc_16_f32<kF16>(128, D, 0, 1);  // (P^T|dS^T from TMEM) x (dO|Q MN-major)
       const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ);
       const SDesc dk_base = sdesc_split(k_addr, 16, 1024), dv_base = sdesc_split(v_addr, 16, 1024);
       const SDesc dq_base = sdesc_split(q_addr, 16, 1024), ddo_base = sdesc_split(q_addr + C::kQBytes, 16, 1024);
@@ -298,16 +299,16 @@ __global__ void __launch_bounds__(320, 1)
       // without a left window bound every row after the first that sees the
       // key sees it too, so only the lower end needs checking
       if (__all_sync(0xffffffffu, key_ok && q0 + c0 >= qs.lo && (!kLeftBound || q0 + c0 + 64 <= qs.hi)))
-        dkdv_probs<false, kLeftBound>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
+        dkdv_probs<false, kLeftBound, kF16>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
       else
-        dkdv_probs<true, kLeftBound>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
+        dkdv_probs<true, kLeftBound, kF16>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_ready);
       ok = __all_sync(0xffffffffu, mbar_wait(dp_ready, t & 1, abort_flag, p.status, 69));
       if (!ok) break;
       tc_fence_after();
-      dkdv_dscores(t_lane + kColDP, c0, dlt, pr);
+      dkdv_dscores<kF16>(t_lane + kColDP, c0, dlt, pr);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(ds_ready);
@@ -318,9 +319,9 @@ __global__ void __launch_bounds__(320, 1)
       const bool st = j < p.Lkv;
       const size_t off = ((static_cast<size_t>(b) * p.Lkv + (st ? j : 0)) * p.Hkv + hk) * D;
       if (w == 0)
-        store_row_bf16<D>(t_lane + 0, reinterpret_cast<__nv_bfloat16*>(p.dk) + off, p.scale, st, T == 0);
+        store_row16<D, kF16>(t_lane + 0, reinterpret_cast<uint16_t*>(p.dk) + off, p.scale, st, T == 0);
       else
-        store_row_bf16<D>(t_lane + 128, reinterpret_cast<__nv_bfloat16*>(p.dv) + off, 1.0f, st, T == 0);
+        store_row16<D, kF16>(t_lane + 128, reinterpret_cast<uint16_t*>(p.dv) + off, 1.0f, st, T == 0);
     }
   }
 
@@ -374,7 +375,7 @@ __device__ __forceinline__ void dq_probs(uint32_t s_col, int c0, float l2, float
 
 // dS = P (dP - delta) for the same N columns, packed over the first N/2 of
 // the S columns they came from.
-template <int N>
+template <int N, bool kF16>
 __device__ __forceinline__ void dq_dscores(uint32_t s_col, uint32_t dp_col, int c0, float dl, const float* pr) {
   uint32_t dr[N];
   if constexpr (N == 32)
@@ -384,7 +385,7 @@ __device__ __forceinline__ void dq_dscores(uint32_t s_col, uint32_t dp_col, int 
   uint32_t pk[N / 2];
 #pragma unroll
   for (int i = 0; i < N / 2; ++i)
-    pk[i] = pack_bf16x2(pr[2 * i] * (__uint_as_float(dr[2 * i]) - dl),
+    pk[i] = pack2<kF16>(pr[2 * i] * (__uint_as_float(dr[2 * i]) - dl),
                         pr[2 * i + 1] * (__uint_as_float(dr[2 * i + 1]) - dl));
   if constexpr (N == 32)
     tmem_st16(s_col + c0, *reinterpret_cast<uint32_t(*)[16]>(pk));
@@ -402,7 +403,7 @@ __device__ __forceinline__ void dq_dscores(uint32_t s_col, uint32_t dp_col, int 
 // two 64-key halves so the dQ MMAs of half 0 overlap the second half.  K tiles
 // use a 3-slot ring (a K tile is read by S and later by dQ), V tiles a 2-slot
 // ring.
-template <int D, bool kLeftBound>
+template <int D, bool kLeftBound, bool kF16>
 __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -497,8 +498,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     __syncwarp();
   } else if (warp == C::kMmaWarp) {
     if (lane == 0 && T > 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, BN, 0, 0);   // Q x K^T, dO x V^T
-      constexpr uint32_t idesc_dq = idesc_bf16_f32(128, D, 0, 1);  // dS (TMEM) x K (MN-major)
+      constexpr uint32_t idesc_s = idesc_16_f32<kF16>(128, BN, 0, 0);   // Q x K^T, dO x V^T
+      constexpr uint32_t idesc_dq = idesc_16_f32<kF16>(128, D, 0, 1);  // dS (TMEM) x K (MN-major)
       const uint32_t q_addr = smem_u32(sQ), do_addr = smem_u32(sDO);
       const SDesc dq_desc = sdesc_split(q_addr, 16, 1024), ddo_desc = sdesc_split(do_addr, 16, 1024);
       const SDesc dk_desc = sdesc_split(smem_u32(sK), 16, 1024), dv_desc = sdesc_split(smem_u32(sV), 16, 1024);
@@ -607,7 +608,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       tc_fence_after();
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        dq_dscores<C::kCols>(s_col, dp_col, 64 * hh + C::kCols * w, dl, pr + hh * C::kCols);
+        dq_dscores<C::kCols, kF16>(s_col, dp_col, 64 * hh + C::kCols * w, dl, pr + hh * C::kCols);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&p_half[hh]);
@@ -619,9 +620,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       // warpgroup w stores head-dim columns [w * D / NWG, (w + 1) * D / NWG)
       constexpr int kPer = D / C::kNWG;
       const bool st = i < p.Lq;
-      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.dq) +
+      uint16_t* dst = reinterpret_cast<uint16_t*>(p.dq) +
                            ((static_cast<size_t>(b) * p.Lq + (st ? i : 0)) * p.Hq + h) * D + w * kPer;
-      store_cols_bf16<kPer>(t_lane + w * kPer, dst, p.scale, st, T == 0);
+      store_cols16<kPer, kF16>(t_lane + w * kPer, dst, p.scale, st, T == 0);
     }
   }
 
@@ -633,9 +634,32 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   }
 }
 
+template <int D, bool kLeftBound, bool kF16>
+cudaError_t launch_dkdv_inst(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, cudaStream_t stream) {
+  using C = DkdvCfg2<D>;
+  cudaError_t e = ensure_dynamic_smem<bwd_dkdv_kernel2<D, kLeftBound, kF16>>(C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  KernelTimer kt("bwd_dkdv", stream);
+  bwd_dkdv_kernel2<D, kLeftBound, kF16><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+  return cudaGetLastError();
+}
+
+template <int D, bool kLeftBound, bool kF16>
+cudaError_t launch_dq_inst(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, cudaStream_t stream) {
+  using C = DqCfg<D>;
+  cudaError_t e = ensure_dynamic_smem<bwd_dq_kernel<D, kLeftBound, kF16>>(C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  KernelTimer kt("bwd_dq", stream);
+  bwd_dq_kernel<D, kLeftBound, kF16><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+  return cudaGetLastError();
+}
+
 template <int D>
-cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream) {
+cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream) {
   const Problem& pb = a.pb;
+  const int elem = pb.f16 ? kElemF16 : kElemBF16;
   PreprocessArgs pa;
   pa.o = a.o;
   pa.dout = a.dout;
@@ -648,7 +672,7 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
   pa.Lq_pad = a.Lq_pad;
   pa.Hq = pb.Hq;
   pa.d = D;
-  pa.is_bf16 = 1;
+  pa.elem = elem;
   cudaError_t e = launch_bwd_preprocess(pa, stream);
   if (e != cudaSuccess) return e;
 
@@ -676,10 +700,10 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
   // dK/dV pass (both variants): Q/dO and K/V boxes of 128 rows
   {
     CUtensorMap tk, tv, tq128, tdo128;
-    if (!make_bshd_tmap(&tq128, a.q, true, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
-        !make_bshd_tmap(&tdo128, a.dout, true, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
-        !make_bshd_tmap(&tk, a.k, true, pb.B, pb.Lkv, pb.Hkv, D, 64, 128) ||
-        !make_bshd_tmap(&tv, a.v, true, pb.B, pb.Lkv, pb.Hkv, D, 64, 128))
+    if (!make_bshd_tmap(&tq128, a.q, elem, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
+        !make_bshd_tmap(&tdo128, a.dout, elem, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
+        !make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, D, 64, 128) ||
+        !make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, D, 64, 128))
       return cudaErrorInvalidValue;
     kp.n_tiles = (pb.Lkv + 127) / 128;
     kp.n_pairs = pb.B * pb.Hkv;
@@ -687,52 +711,38 @@ cudaError_t launch_bwd_bf16_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t s
     dim3 grid(kp.n_pairs * kp.n_tiles);
     if (!a.deterministic)
       return launch_single_pass<D>(tq128, tk, tv, tdo128, kp, grid, static_cast<long>(pb.B) * pb.Lq * pb.Hq * D,
-                                   stream);
-    using C = DkdvCfg2<D>;
+                                   pb.f16 != 0, stream);
     const bool left = pb.wl < kWinInf;
-    e = left ? ensure_dynamic_smem<bwd_dkdv_kernel2<D, true>>(C::kSmemBytes)
-             : ensure_dynamic_smem<bwd_dkdv_kernel2<D, false>>(C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    {
-      KernelTimer kt("bwd_dkdv", stream);
-      if (left)
-        bwd_dkdv_kernel2<D, true><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq128, tk, tv, tdo128, kp);
-      else
-        bwd_dkdv_kernel2<D, false><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq128, tk, tv, tdo128, kp);
-    }
-    e = cudaGetLastError();
+    e = pb.f16 ? (left ? launch_dkdv_inst<D, true, true>(tq128, tk, tv, tdo128, kp, grid, stream)
+                       : launch_dkdv_inst<D, false, true>(tq128, tk, tv, tdo128, kp, grid, stream))
+               : (left ? launch_dkdv_inst<D, true, false>(tq128, tk, tv, tdo128, kp, grid, stream)
+                       : launch_dkdv_inst<D, false, false>(tq128, tk, tv, tdo128, kp, grid, stream));
     if (e != cudaSuccess) return e;
   }
   // dQ pass: Q/dO and K/V boxes of 128 rows
   {
     CUtensorMap tq, tk, tv, tdo;
-    if (!make_bshd_tmap(&tq, a.q, true, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
-        !make_bshd_tmap(&tdo, a.dout, true, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
-        !make_bshd_tmap(&tk, a.k, true, pb.B, pb.Lkv, pb.Hkv, D, 64, 128) ||
-        !make_bshd_tmap(&tv, a.v, true, pb.B, pb.Lkv, pb.Hkv, D, 64, 128))
+    if (!make_bshd_tmap(&tq, a.q, elem, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
+        !make_bshd_tmap(&tdo, a.dout, elem, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
+        !make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, D, 64, 128) ||
+        !make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, D, 64, 128))
       return cudaErrorInvalidValue;
-    using C = DqCfg<D>;
     kp.n_tiles = (pb.Lq + 127) / 128;
     kp.n_pairs = pb.B * pb.Hq;
     kp.pair_group = l2_pair_group(2l * pb.Lkv * D * 2, kp.n_pairs, pb.G);
     dim3 grid(kp.n_pairs * kp.n_tiles);
     const bool left = pb.wl < kWinInf;
-    e = left ? ensure_dynamic_smem<bwd_dq_kernel<D, true>>(C::kSmemBytes)
-             : ensure_dynamic_smem<bwd_dq_kernel<D, false>>(C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    KernelTimer kt("bwd_dq", stream);
-    if (left)
-      bwd_dq_kernel<D, true><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
-    else
-      bwd_dq_kernel<D, false><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
-    return cudaGetLastError();
+    return pb.f16 ? (left ? launch_dq_inst<D, true, true>(tq, tk, tv, tdo, kp, grid, stream)
+                          : launch_dq_inst<D, false, true>(tq, tk, tv, tdo, kp, grid, stream))
+                  : (left ? launch_dq_inst<D, true, false>(tq, tk, tv, tdo, kp, grid, stream)
+                          : launch_dq_inst<D, false, false>(tq, tk, tv, tdo, kp, grid, stream));
   }
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_bf16(const BwdArgs& a, DeviceStatus* st, cudaStream_t s) {
-  return a.pb.d == 64 ? launch_bwd_bf16_d<64>(a, st, s) : launch_bwd_bf16_d<128>(a, st, s);
+cudaError_t launch_bwd_16(const BwdArgs& a, DeviceStatus* st, cudaStream_t s) {
+  return a.pb.d == 64 ? launch_bwd_d<64>(a, st, s) : launch_bwd_d<128>(a, st, s);
 }
 
 }  // namespace attn

@@ -1,4 +1,4 @@
-// Split-KV decode forward, bf16, head_dim 64/128, on the sm_103a tensor cores.
+// Split-KV decode forward, bf16 or fp16, head_dim 64/128, on the sm_103a tensor cores.
 //
 // Method (probjax "Attention performance", section "Grouped-query attention
 // and decoding"): for few queries over a long KV cache the keys are split
@@ -45,9 +45,9 @@ struct DecKParams {
   DeviceStatus* status;
 };
 
-template <int D>
+template <int D, bool kF16>
 __global__ void __launch_bounds__(192, 1)
-    decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const DecKParams p) {
   using C = DecCfg<D>;
   constexpr int NS = C::kSlots;
@@ -128,8 +128,8 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else if (warp == 5) {
     if (lane == 0 && n > 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kBN, 0, 0);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
+      constexpr uint32_t idesc_s = idesc_16_f32<kF16>(128, kBN, 0, 0);
+      constexpr uint32_t idesc_o = idesc_16_f32<kF16>(128, D, 0, 1);
       const uint32_t q_addr = smem_u32(sQ), slot_addr = smem_u32(sSlots);
       auto issue_s = [&](int j) {
         const uint32_t ka = slot_addr + ((2 * j) % NS) * C::kSlotBytes;
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(192, 1)
           const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * e], sl2, -mb));
           const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * e + 1], sl2, -mb));
           l_sum += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
+          pk[e] = pack2<kF16>(p0, p1);
         }
         tmem_st16(s_addr + c * 16, pk);
       }
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(192, 1)
 
 // TMA map over q viewed as (d, Hq, Lq, B) with box (64, G, Lq, 1): one load
 // packs the G heads of a KV head times the Lq queries as rows i * G + g.
-bool make_q_group_tmap(CUtensorMap* map, const void* q, int B, int Lq, int Hq, int d, int G) {
+bool make_q_group_tmap(CUtensorMap* map, const void* q, int B, int Lq, int Hq, int d, int G, bool f16) {
   typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -301,21 +301,31 @@ bool make_q_group_tmap(CUtensorMap* map, const void* q, int B, int Lq, int Hq, i
                            static_cast<cuuint64_t>(Lq) * Hq * d * 2};
   cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(Lq), 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims, strides, box, es,
+  return fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims,
+            strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
-cudaError_t launch_decode_bf16_d(const DecodeArgs& a, DeviceStatus* st, cudaStream_t stream) {
+template <int D, bool kF16>
+cudaError_t launch_decode_inst(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const DecKParams& kp, dim3 grid, cudaStream_t stream) {
   using C = DecCfg<D>;
-  const Problem& pb = a.pb;
-  CUtensorMap tq, tk, tv;
-  if (!make_q_group_tmap(&tq, a.q, pb.B, pb.Lq, pb.Hq, D, pb.G)) return cudaErrorInvalidValue;
-  if (!make_bshd_tmap(&tk, a.k, true, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
-  if (!make_bshd_tmap(&tv, a.v, true, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
-  cudaError_t e = ensure_dynamic_smem<decode_bf16_kernel<D>>(C::kSmemBytes);
+  cudaError_t e = ensure_dynamic_smem<decode_tc_kernel<D, kF16>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
+  KernelTimer kt("decode", stream);
+  decode_tc_kernel<D, kF16><<<grid, 192, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_decode_d(const DecodeArgs& a, DeviceStatus* st, cudaStream_t stream) {
+  const Problem& pb = a.pb;
+  const int elem = pb.f16 ? kElemF16 : kElemBF16;
+  CUtensorMap tq, tk, tv;
+  if (!make_q_group_tmap(&tq, a.q, pb.B, pb.Lq, pb.Hq, D, pb.G, pb.f16 != 0)) return cudaErrorInvalidValue;
+  if (!make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
+  if (!make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
   DecKParams kp;
   kp.o_part = a.o_part;
   kp.lse_part = a.lse_part;
@@ -330,18 +340,15 @@ cudaError_t launch_decode_bf16_d(const DecodeArgs& a, DeviceStatus* st, cudaStre
   kp.chunk = a.chunk;
   kp.scale_log2 = pb.scale * kLog2e;
   kp.status = st;
-  dim3 grid(a.num_splits, pb.Hkv, pb.B);
-  {
-    KernelTimer kt("decode", stream);
-    decode_bf16_kernel<D><<<grid, 192, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
-  }
-  return cudaGetLastError();
+  const dim3 grid(a.num_splits, pb.Hkv, pb.B);
+  return pb.f16 ? launch_decode_inst<D, true>(tq, tk, tv, kp, grid, stream)
+                : launch_decode_inst<D, false>(tq, tk, tv, kp, grid, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_decode_bf16(const DecodeArgs& a, DeviceStatus* st, cudaStream_t s) {
-  return a.pb.d == 64 ? launch_decode_bf16_d<64>(a, st, s) : launch_decode_bf16_d<128>(a, st, s);
+cudaError_t launch_decode_16(const DecodeArgs& a, DeviceStatus* st, cudaStream_t s) {
+  return a.pb.d == 64 ? launch_decode_d<64>(a, st, s) : launch_decode_d<128>(a, st, s);
 }
 
 }  // namespace attn

@@ -1,4 +1,4 @@
-// Forward attention, bf16, head_dim 64/128, on the sm_103a tensor cores.
+// Forward attention, bf16 or fp16, head_dim 64/128, on the sm_103a tensor cores.
 //
 // Method (probjax "Attention performance", sections "When to use which" and
 // "Memory"): exact softmax attention computed tile by tile with an online
@@ -57,9 +57,9 @@ struct FwdKParams {
   DeviceStatus* status;
 };
 
-template <int D, bool kLeftBound>
+template <int D, bool kLeftBound, bool kF16>
 __global__ void __launch_bounds__(320, 1)
-    fwd_bf16_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdKParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -162,8 +162,8 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n > 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);  // Q (K-major) x K^T (K-major)
-      constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);    // P (TMEM) x V (MN-major)
+      constexpr uint32_t idesc_s = idesc_16_f32<kF16>(kBM, kBN, 0, 0);  // Q (K-major) x K^T (K-major)
+      constexpr uint32_t idesc_o = idesc_16_f32<kF16>(kBM, D, 0, 1);    // P (TMEM) x V (MN-major)
       const SDesc dq[2] = {sdesc_split(smem_u32(sQ), 16, 1024), sdesc_split(smem_u32(sQ) + C::kQTileBytes, 16, 1024)};
       const SDesc dk0 = sdesc_split(smem_u32(sSlots), 16, 1024);
       const SDesc dv0 = sdesc_split(smem_u32(sSlots) + C::kSlotBytes, C::kBoxBytes, 1024);
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(320, 1)
           const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, -mb));
           const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, -mb));
           ls4[i & 3] += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
+          pk[i] = pack2<kF16>(p0, p1);
         }
         tmem_st16(s_addr + c * 16, pk);
       }
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(320, 1)
     if (ok) {
       tc_fence_after();
       const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
+      uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
                             ((static_cast<size_t>(b) * p.Lq + row) * p.Hq + hq) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
+          pk[i] = pack2<kF16>(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
         if (row < p.Lq) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
@@ -344,17 +344,25 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D>
-cudaError_t launch_fwd_bf16_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t stream) {
+template <int D, bool kLeftBound, bool kF16>
+cudaError_t launch_fwd_inst(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdKParams& kp, dim3 grid, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  const Problem& pb = a.pb;
-  CUtensorMap tq, tk, tv;
-  if (!make_bshd_tmap(&tq, a.q, true, pb.B, pb.Lq, pb.Hq, D, 64, kBM)) return cudaErrorInvalidValue;
-  if (!make_bshd_tmap(&tk, a.k, true, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
-  if (!make_bshd_tmap(&tv, a.v, true, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
-  cudaError_t e = pb.wl < kWinInf ? ensure_dynamic_smem<fwd_bf16_kernel<D, true>>(C::kSmemBytes)
-                                  : ensure_dynamic_smem<fwd_bf16_kernel<D, false>>(C::kSmemBytes);
+  cudaError_t e = ensure_dynamic_smem<fwd_tc_kernel<D, kLeftBound, kF16>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
+  KernelTimer kt("fwd", stream);
+  fwd_tc_kernel<D, kLeftBound, kF16><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t stream) {
+  const Problem& pb = a.pb;
+  const int elem = pb.f16 ? kElemF16 : kElemBF16;
+  CUtensorMap tq, tk, tv;
+  if (!make_bshd_tmap(&tq, a.q, elem, pb.B, pb.Lq, pb.Hq, D, 64, kBM)) return cudaErrorInvalidValue;
+  if (!make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
+  if (!make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
   FwdKParams kp;
   kp.o = a.o;
   kp.lse = a.lse;
@@ -372,22 +380,20 @@ cudaError_t launch_fwd_bf16_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t s
   kp.pair_group = l2_pair_group(2l * pb.Lkv * D * 2, kp.n_pairs, pb.G);
   kp.scale_log2 = pb.scale * kLog2e;
   kp.status = st;
-  dim3 grid(kp.n_pairs * kp.n_qblocks);
-  {
-    KernelTimer kt("fwd", stream);
-    if (pb.wl < kWinInf)
-      fwd_bf16_kernel<D, true><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
-    else
-      fwd_bf16_kernel<D, false><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
-  }
-  return cudaGetLastError();
+  const dim3 grid(kp.n_pairs * kp.n_qblocks);
+  const bool left = pb.wl < kWinInf;
+  if (pb.f16)
+    return left ? launch_fwd_inst<D, true, true>(tq, tk, tv, kp, grid, stream)
+                : launch_fwd_inst<D, false, true>(tq, tk, tv, kp, grid, stream);
+  return left ? launch_fwd_inst<D, true, false>(tq, tk, tv, kp, grid, stream)
+              : launch_fwd_inst<D, false, false>(tq, tk, tv, kp, grid, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_fwd_bf16(const FwdArgs& a, DeviceStatus* st, cudaStream_t s) {
-  if (a.pb.d == 64) return launch_fwd_bf16_d<64>(a, st, s);
-  return launch_fwd_bf16_d<128>(a, st, s);
+cudaError_t launch_fwd_16(const FwdArgs& a, DeviceStatus* st, cudaStream_t s) {
+  if (a.pb.d == 64) return launch_fwd_d<64>(a, st, s);
+  return launch_fwd_d<128>(a, st, s);
 }
 
 }  // namespace attn

@@ -531,7 +531,7 @@ cudaError_t launch_bwd_f32(const BwdArgs& a, DeviceStatus* st, cudaStream_t s) {
   pa.Lq_pad = pb.Lq;
   pa.Hq = pb.Hq;
   pa.d = pb.d;
-  pa.is_bf16 = 0;
+  pa.elem = kElemF32;
   cudaError_t e = launch_bwd_preprocess(pa, s);
   if (e != cudaSuccess) return e;
   F32BwdParams p{};

@@ -6,6 +6,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace attn {
@@ -191,6 +192,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn_maj
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The same for fp16 operands (A and B format 0) when kF16, bf16 otherwise.
+// Both operands of one kind::f16 MMA always share the format.
+template <bool kF16>
+__host__ __device__ constexpr uint32_t idesc_16_f32(int M, int N, int a_mn_major, int b_mn_major) {
+  return kF16 ? (idesc_bf16_f32(M, N, a_mn_major, b_mn_major) & ~((7u << 7) | (7u << 10)))
+              : idesc_bf16_f32(M, N, a_mn_major, b_mn_major);
+}
+
 // Descriptor split into its two 32-bit halves.  The start address lives in
 // the low half (bits 0-13, address >> 4) and never carries into bit 14 for
 // shared-memory addresses, so stepping through a tile is one 32-bit add on
@@ -372,6 +381,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// two fp32 -> packed 16-bit pair of the kernel's format (fp16 when kF16)
+template <bool kF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (kF16) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+  } else {
+    return pack_bf16x2(lo, hi);
+  }
 }
 
 }  // namespace attn

@@ -1,5 +1,8 @@
 // HBM-bound helper kernels: the backward preprocess (delta = rowsum(dO * O))
 // and the log-sum-exp combine of split-KV partials.
+#include <cstring>
+#include <type_traits>
+
 #include "attn_internal.h"
 
 namespace attn {
@@ -16,6 +19,20 @@ __device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, flo
   for (int i = 0; i < 4; ++i) {
     f[2 * i] = __uint_as_float(w[i] << 16);
     f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+template <>
+__device__ __forceinline__ void load8<__half>(const __half* p, float (&f)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 h;
+    memcpy(&h, &w[i], sizeof(h));
+    const float2 v = __half22float2(h);
+    f[2 * i] = v.x;
+    f[2 * i + 1] = v.y;
   }
 }
 
@@ -119,8 +136,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   T* dst = o + ((static_cast<long>(b) * Lq + i) * Hq + h) * D + lane * kPer;
 #pragma unroll
   for (int e = 0; e < kPer; ++e) {
-    if constexpr (sizeof(T) == 2)
+    if constexpr (std::is_same<T, __nv_bfloat16>::value)
       dst[e] = __float2bfloat16_rn(acc[e]);
+    else if constexpr (std::is_same<T, __half>::value)
+      dst[e] = __float2half_rn(acc[e]);
     else
       dst[e] = acc[e];
   }
@@ -151,17 +170,21 @@ cudaError_t run_combine(const float* o_part, const float* lse_part, void* o, flo
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const PreprocessArgs& a, cudaStream_t s) {
-  if (a.is_bf16) {
+  if (a.elem == kElemBF16)
     return a.d == 64 ? run_preprocess<__nv_bfloat16, 64>(a, s) : run_preprocess<__nv_bfloat16, 128>(a, s);
-  }
+  if (a.elem == kElemF16) return a.d == 64 ? run_preprocess<__half, 64>(a, s) : run_preprocess<__half, 128>(a, s);
   return a.d == 64 ? run_preprocess<float, 64>(a, s) : run_preprocess<float, 128>(a, s);
 }
 
 cudaError_t launch_decode_combine(const float* o_part, const float* lse_part, void* o, float* lse, int B, int Lq,
-                                  int Hq, int d, int num_splits, int is_bf16, cudaStream_t s) {
-  if (is_bf16) {
+                                  int Hq, int d, int num_splits, int elem, cudaStream_t s) {
+  if (elem == kElemBF16) {
     return d == 64 ? run_combine<__nv_bfloat16, 64>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s)
                    : run_combine<__nv_bfloat16, 128>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s);
+  }
+  if (elem == kElemF16) {
+    return d == 64 ? run_combine<__half, 64>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s)
+                   : run_combine<__half, 128>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s);
   }
   return d == 64 ? run_combine<float, 64>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s)
                  : run_combine<float, 128>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s);

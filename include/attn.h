@@ -64,7 +64,10 @@ typedef enum {
   ATTN_ERR_DEVICE = 5       /* a kernel reported a device-side fault (see attn_device_status) */
 } attn_status;
 
-typedef enum { ATTN_BF16 = 0, ATTN_FP32 = 1 } attn_dtype;
+/* Element type of q, k, v, o, dout, dq, dk, dv (lse, delta and the decode
+ * partials are always float32).  bf16 and fp16 run on the tensor cores with
+ * fp32 accumulation; fp32 runs in true fp32. */
+typedef enum { ATTN_BF16 = 0, ATTN_FP32 = 1, ATTN_FP16 = 2 } attn_dtype;
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* attn_status_string(attn_status s);

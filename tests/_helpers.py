@@ -36,4 +36,6 @@ def cuda(*ts):
     return tuple(t.cuda() for t in ts)
 
 
-TOL = {"bf16": 1e-2, "fp32": 1e-4}
+# bf16 and fp32 targets as stated for the method; fp16 takes the bf16 target's
+# multiple of the unit roundoff (1e-2 = 2.56 * 2^-8) at fp16's 2^-11, rounded up
+TOL = {"bf16": 1e-2, "fp32": 1e-4, "fp16": 2e-3}

@@ -19,7 +19,7 @@ from dataclasses import dataclass, field
 
 import torch
 
-DTYPES = {"bf16": torch.bfloat16, "fp32": torch.float32}
+DTYPES = {"bf16": torch.bfloat16, "fp32": torch.float32, "fp16": torch.float16}
 
 
 @dataclass(frozen=True)
