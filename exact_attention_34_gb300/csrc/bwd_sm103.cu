@@ -52,13 +52,20 @@ struct DkdvCfg2 {
   static constexpr int kKVBytes = kBN * D * 2;
   static constexpr int kBox = 128 * 128;      // one 64-column box of a 128-row tile
   static constexpr int kQBytes = kBM * D * 2;
-  static constexpr int kStages = 2;
+  // Q (with its lse2 rows) in a ring of 3: S^T(t+1) is issued right after
+  // dV(t), before dK(t) has released Q(t).  dO (with its delta rows) in a ring
+  // of 2: dP^T(t+1) comes after dK(t).  Both release a slot after dK.
+  static constexpr int kQSlots = 3, kDOSlots = 2;
   static constexpr int kOffV = kKVBytes;
-  static constexpr int kOffQ = 2 * kKVBytes;  // stage s: Q at s * 2 * kQBytes, dO right after
-  static constexpr int kOffStat = kOffQ + kStages * 2 * kQBytes;
-  static constexpr int kOffBars = kOffStat + kStages * 2 * kBM * 4;
-  static constexpr int kNumBars = 2 * kStages + 1 + 2 + 2 + 1;
-  static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16 + 1024;
+  static constexpr int kOffQ = 2 * kKVBytes;
+  static constexpr int kOffDO = kOffQ + kQSlots * kQBytes;
+  static constexpr int kOffLse = kOffDO + kDOSlots * kQBytes;
+  static constexpr int kOffDelta = kOffLse + kQSlots * kBM * 4;
+  static constexpr int kOffBars = kOffDelta + kDOSlots * kBM * 4;
+  static constexpr int kNumBars = 2 * kQSlots + 2 * kDOSlots + 6;
+  // No alignment slack: the dynamic shared window starts 1024-aligned (checked
+  // at run time; a misaligned base makes the kernel report and do nothing).
+  static constexpr int kSmemBytes = kOffBars + kNumBars * 8 + 16;
   static constexpr int kThreads = 320;
 };
 
@@ -125,18 +132,26 @@ __global__ void __launch_bounds__(320, 1)
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const BwdKParams p) {
   using C = DkdvCfg2<D>;
-  constexpr int NS = C::kStages, BM = C::kBM;
+  constexpr int NQ = C::kQSlots, NO = C::kDOSlots, BM = C::kBM;
   constexpr uint32_t kColS = 256, kColDP = 384;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  if (smem_u32(smem_raw) & 1023u) {  // never expected: see kSmemBytes
+    if (threadIdx.x == 0) report_status(p.status, 2, 60);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* sK = smem;
   uint8_t* sV = smem + C::kOffV;
   uint8_t* sQ = smem + C::kOffQ;
-  float* sStat = reinterpret_cast<float*>(smem + C::kOffStat);
+  uint8_t* sDO = smem + C::kOffDO;
+  float* sLse = reinterpret_cast<float*>(smem + C::kOffLse);
+  float* sDelta = reinterpret_cast<float*>(smem + C::kOffDelta);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + NS;
-  uint64_t* kv_full = bars + 2 * NS;
+  uint64_t* full_q = bars;
+  uint64_t* empty_q = bars + NQ;
+  uint64_t* full_do = bars + 2 * NQ;
+  uint64_t* empty_do = bars + 2 * NQ + NO;
+  uint64_t* kv_full = bars + 2 * NQ + 2 * NO;
   uint64_t* s_ready = kv_full + 1;   // S^T(t) computed
   uint64_t* dp_ready = kv_full + 2;  // dP^T(t) computed
   uint64_t* p_ready = kv_full + 3;   // P^T(t) written (256 arrivals)
@@ -167,9 +182,13 @@ __global__ void __launch_bounds__(320, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < NQ; ++s) {
+      mbar_init(&full_q[s], 1);
+      mbar_init(&empty_q[s], 1);
+    }
+    for (int s = 0; s < NO; ++s) {
+      mbar_init(&full_do[s], 1);
+      mbar_init(&empty_do[s], 1);
     }
     mbar_init(kv_full, 1);
     mbar_init(s_ready, 1);
@@ -198,19 +217,21 @@ __global__ void __launch_bounds__(320, 1)
         tma_load_4d(sV + h * C::kBox, &tm_v, kv_full, h * 64, j0, hk, b);
       }
       for (int t = 0; t < T; ++t) {
-        const int s = t % NS, r = t / NS;
-        if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort_flag, p.status, 61)) break;
         const int h = hk * p.G + t / steps_per_head;
         const int q0 = (i_begin + t % steps_per_head) * BM;
-        mbar_arrive_expect_tx(&full[s], 2 * C::kQBytes + 2 * BM * 4);
-        uint8_t* q_dst = sQ + s * 2 * C::kQBytes;
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_4d(q_dst + c * C::kBox, &tm_q, &full[s], c * 64, q0, h, b);
-          tma_load_4d(q_dst + C::kQBytes + c * C::kBox, &tm_do, &full[s], c * 64, q0, h, b);
-        }
         const size_t row = (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + q0;
-        bulk_load(sStat + s * 2 * BM, p.lse2 + row, BM * 4, &full[s]);
-        bulk_load(sStat + s * 2 * BM + BM, p.delta + row, BM * 4, &full[s]);
+        const int sq = t % NQ, rq = t / NQ;
+        if (rq > 0 && !mbar_wait(&empty_q[sq], (rq - 1) & 1, abort_flag, p.status, 61)) break;
+        mbar_arrive_expect_tx(&full_q[sq], C::kQBytes + BM * 4);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(sQ + sq * C::kQBytes + c * C::kBox, &tm_q, &full_q[sq], c * 64, q0, h, b);
+        bulk_load(sLse + sq * BM, p.lse2 + row, BM * 4, &full_q[sq]);
+        const int so = t % NO, ro = t / NO;
+        if (ro > 0 && !mbar_wait(&empty_do[so], (ro - 1) & 1, abort_flag, p.status, 59)) break;
+        mbar_arrive_expect_tx(&full_do[so], C::kQBytes + BM * 4);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_4d(sDO + so * C::kQBytes + c * C::kBox, &tm_do, &full_do[so], c * 64, q0, h, b);
+        bulk_load(sDelta + so * BM, p.delta + row, BM * 4, &full_do[so]);
       }
     }
     __syncwarp();
@@ -218,34 +239,46 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0 && T > 0) {
       constexpr uint32_t idesc_st = idesc_16_f32<kF16>(128, BM, 0, 0);  // K x Q^T, V x dO^T
       constexpr uint32_t idesc_acc = idesc_16_f32<kF16>(128, D, 0, 1);  // (P^T|dS^T from TMEM) x (dO|Q MN-major)
-      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ);
+      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), q_addr = smem_u32(sQ), o_addr = smem_u32(sDO);
       const SDesc dk_base = sdesc_split(k_addr, 16, 1024), dv_base = sdesc_split(v_addr, 16, 1024);
-      const SDesc dq_base = sdesc_split(q_addr, 16, 1024), ddo_base = sdesc_split(q_addr + C::kQBytes, 16, 1024);
-      const SDesc bq_base = sdesc_split(q_addr, C::kBox, 1024), bdo_base = sdesc_split(q_addr + C::kQBytes, C::kBox, 1024);
-      constexpr uint32_t kStage16 = (2 * C::kQBytes) >> 4;
-      auto issue_scores = [&](int t) {
-        const uint32_t so = (t % NS) * kStage16;
+      const SDesc dq_base = sdesc_split(q_addr, 16, 1024), ddo_base = sdesc_split(o_addr, 16, 1024);
+      const SDesc bq_base = sdesc_split(q_addr, C::kBox, 1024), bdo_base = sdesc_split(o_addr, C::kBox, 1024);
+      constexpr uint32_t kSlot16 = C::kQBytes >> 4;
+      auto issue_s = [&](int t) {  // S^T(t) = K Q(t)^T
+        const uint32_t qo = (t % NQ) * kSlot16;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
-          mma_ss_d(tbase + kColS, dk_base, off, dq_base, so + off, idesc_st, k > 0);
+          mma_ss_d(tbase + kColS, dk_base, off, dq_base, qo + off, idesc_st, k > 0);
         }
         mma_commit(s_ready);
+      };
+      auto issue_dp = [&](int t) {  // dP^T(t) = V dO(t)^T
+        const uint32_t oo = (t % NO) * kSlot16;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = ((k >> 2) * C::kBox + (k & 3) * 32) >> 4;
-          mma_ss_d(tbase + kColDP, dv_base, off, ddo_base, so + off, idesc_st, k > 0);
+          mma_ss_d(tbase + kColDP, dv_base, off, ddo_base, oo + off, idesc_st, k > 0);
         }
         mma_commit(dp_ready);
       };
+      // Order per step: dV(t), S^T(t+1), dK(t), dP^T(t+1).  S^T(t+1) overwrites
+      // P^T(t) right after dV(t) has read it (one thread issues all MMAs; the
+      // tensor pipe runs them in order), so the probabilities of step t+1 run
+      // while dK(t) and dP^T(t+1) are on the tensor core.
       bool ok = mbar_wait(kv_full, 0, abort_flag, p.status, 62);
-      if (ok) ok = mbar_wait(&full[0], 0, abort_flag, p.status, 63);
+      if (ok) ok = mbar_wait(&full_q[0], 0, abort_flag, p.status, 63);
       if (ok) {
         tc_fence_after();
-        issue_scores(0);
+        issue_s(0);
+        ok = mbar_wait(&full_do[0], 0, abort_flag, p.status, 58);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_dp(0);
       }
       for (int t = 0; t < T && ok; ++t) {
-        const uint32_t so = (t % NS) * kStage16;
+        const uint32_t qo = (t % NQ) * kSlot16, oo = (t % NO) * kSlot16;
         // query k-step k (16 queries) of warpgroup w = k / 4 sits packed at 64 w + 8 (k - 4 w)
         ok = mbar_wait(p_ready, t & 1, abort_flag, p.status, 64);
         if (!ok) break;
@@ -253,8 +286,14 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int k = 0; k < 8; ++k) {  // dV += P^T dO
           const uint32_t acol = 64 * (k >> 2) + 8 * (k & 3);
-          mma_ts_d(tbase + 128, tbase + kColS + acol, bdo_base, so + ((16 * k * 128) >> 4), idesc_acc,
+          mma_ts_d(tbase + 128, tbase + kColS + acol, bdo_base, oo + ((16 * k * 128) >> 4), idesc_acc,
                    (t > 0 || k > 0) ? 1u : 0u);
+        }
+        if (t + 1 < T) {
+          ok = mbar_wait(&full_q[(t + 1) % NQ], ((t + 1) / NQ) & 1, abort_flag, p.status, 66);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(t + 1);
         }
         ok = mbar_wait(ds_ready, t & 1, abort_flag, p.status, 65);
         if (!ok) break;
@@ -262,15 +301,16 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int k = 0; k < 8; ++k) {  // dK += dS^T Q
           const uint32_t acol = 64 * (k >> 2) + 8 * (k & 3);
-          mma_ts_d(tbase + 0, tbase + kColDP + acol, bq_base, so + ((16 * k * 128) >> 4), idesc_acc,
+          mma_ts_d(tbase + 0, tbase + kColDP + acol, bq_base, qo + ((16 * k * 128) >> 4), idesc_acc,
                    (t > 0 || k > 0) ? 1u : 0u);
         }
-        mma_commit(&empty[t % NS]);
+        mma_commit(&empty_q[t % NQ]);
+        mma_commit(&empty_do[t % NO]);
         if (t + 1 < T) {
-          ok = mbar_wait(&full[(t + 1) % NS], ((t + 1) / NS) & 1, abort_flag, p.status, 66);
+          ok = mbar_wait(&full_do[(t + 1) % NO], ((t + 1) / NO) & 1, abort_flag, p.status, 57);
           if (!ok) break;
           tc_fence_after();
-          issue_scores(t + 1);
+          issue_dp(t + 1);
         }
       }
       if (ok) mma_commit(acc_full);
@@ -288,13 +328,12 @@ __global__ void __launch_bounds__(320, 1)
     const int c0 = 64 * w;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
-      const int s = t % NS;
       ok = __all_sync(0xffffffffu, mbar_wait(s_ready, t & 1, abort_flag, p.status, 67));
       if (!ok) break;
       tc_fence_after();
       const int q0 = (i_begin + t % steps_per_head) * BM;
-      const float* lse2 = sStat + s * 2 * BM;
-      const float* dlt = lse2 + BM;
+      const float* lse2 = sLse + (t % NQ) * BM;
+      const float* dlt = sDelta + (t % NO) * BM;
       float pr[64];
       // without a left window bound every row after the first that sees the
       // key sees it too, so only the lower end needs checking
