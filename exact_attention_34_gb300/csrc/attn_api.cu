@@ -93,7 +93,8 @@ attn_status check_problem(int B, int Lq, int Lkv, int Hq, int Hkv, int d, float 
   if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
   if (dtype != ATTN_BF16 && dtype != ATTN_FP32 && dtype != ATTN_FP16)
     return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
-  if (d != 64 && d != 128) return fail(ATTN_ERR_UNSUPPORTED, "head_dim %d not supported (64 or 128)", d);
+  if (d != 32 && d != 64 && d != 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "head_dim %d not supported (32, 64 or 128)", d);
   // 32-bit index headroom for per-row offsets (elements of one tensor)
   const double big = static_cast<double>(B) * Lq * Hq * d;
   const double bigk = static_cast<double>(B) * Lkv * Hkv * d;

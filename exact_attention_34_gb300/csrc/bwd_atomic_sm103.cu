@@ -248,8 +248,8 @@ __global__ void __launch_bounds__(512, 1)
     const int quarter = warp - 8;
     const int dr = quarter * 32 + lane;
     const uint32_t t_lane = tbase + (static_cast<uint32_t>(quarter * 32) << 16);
-    const bool active = quarter * 32 < D;  // head_dim 64: lanes [64, 128) hold a copy
-    const size_t qstride = static_cast<size_t>(p.Hq) * D;
+    const bool active = quarter * 32 < p.dh;  // lanes past the stored head_dim hold copies or padding
+    const size_t qstride = static_cast<size_t>(p.Hq) * p.dh;
     for (int t = 0; t < T; ++t) {
       if (!__all_sync(0xffffffffu, mbar_wait(dq_ready, t & 1, abort_flag, p.status, 83))) break;
       tc_fence_after();
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(512, 1)
       if (active) {
         const int h = hk * p.G + t / steps_per_head;
         const int q0 = (i_begin + t % steps_per_head) * BM;
-        float* dst = p.dq_acc + ((static_cast<size_t>(b) * p.Lq + q0) * p.Hq + h) * D + dr;
+        float* dst = p.dq_acc + ((static_cast<size_t>(b) * p.Lq + q0) * p.Hq + h) * p.dh + dr;
         if (q0 + BM <= p.Lq) {
 #pragma unroll
           for (int c = 0; c < BM; ++c) atomicAdd(dst + c * qstride, __uint_as_float(v[c]));
@@ -339,11 +339,11 @@ __global__ void __launch_bounds__(512, 1)
     if (ok) {
       tc_fence_after();
       const bool st = j < p.Lkv;
-      const size_t off = ((static_cast<size_t>(b) * p.Lkv + (st ? j : 0)) * p.Hkv + hk) * D;
+      const size_t off = ((static_cast<size_t>(b) * p.Lkv + (st ? j : 0)) * p.Hkv + hk) * p.dh;
       if (w == 0)
-        store_row16<D, kF16>(t_lane + 0, reinterpret_cast<uint16_t*>(p.dk) + off, p.scale, st, T == 0);
+        store_row16<D, kF16>(t_lane + 0, reinterpret_cast<uint16_t*>(p.dk) + off, p.scale, st, T == 0, p.dh);
       else
-        store_row16<D, kF16>(t_lane + 128, reinterpret_cast<uint16_t*>(p.dv) + off, 1.0f, st, T == 0);
+        store_row16<D, kF16>(t_lane + 128, reinterpret_cast<uint16_t*>(p.dv) + off, 1.0f, st, T == 0, p.dh);
     }
   }
 

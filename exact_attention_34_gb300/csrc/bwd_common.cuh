@@ -18,17 +18,19 @@ struct BwdKParams {
   float* dq_acc;       // single-pass variant
   const int32_t* kv_lens;
   int Lq, Lkv, Hq, Hkv, G, causal, wl, wr, Lq_pad, n_tiles, n_pairs, pair_group;
+  int dh;  // stored head_dim (32 runs as D = 64 with zero-filled columns)
   float scale, scale_log2;
   DeviceStatus* status;
 };
 
-// Store one row of D fp32 values from TMEM (columns col..col+D) in the 16-bit
-// format (fp16 when kF16, else bf16), times `mul`.
+// Store the first ncols (a multiple of 32, <= D) of one row of fp32 values
+// from TMEM in the 16-bit format (fp16 when kF16, else bf16), times `mul`.
 template <int D, bool kF16>
-__device__ __forceinline__ void store_row16(uint32_t taddr, uint16_t* dst, float mul, bool do_store,
-                                               bool zero) {
+__device__ __forceinline__ void store_row16(uint32_t taddr, uint16_t* dst, float mul, bool do_store, bool zero,
+                                            int ncols) {
 #pragma unroll
   for (int c = 0; c < D / 32; ++c) {
+    if (c * 32 >= ncols) break;
     uint32_t r[32];
     if (!zero) {
       tmem_ld32(taddr + c * 32, r);

@@ -356,11 +356,11 @@ __global__ void __launch_bounds__(320, 1)
     if (ok) {
       tc_fence_after();
       const bool st = j < p.Lkv;
-      const size_t off = ((static_cast<size_t>(b) * p.Lkv + (st ? j : 0)) * p.Hkv + hk) * D;
+      const size_t off = ((static_cast<size_t>(b) * p.Lkv + (st ? j : 0)) * p.Hkv + hk) * p.dh;
       if (w == 0)
-        store_row16<D, kF16>(t_lane + 0, reinterpret_cast<uint16_t*>(p.dk) + off, p.scale, st, T == 0);
+        store_row16<D, kF16>(t_lane + 0, reinterpret_cast<uint16_t*>(p.dk) + off, p.scale, st, T == 0, p.dh);
       else
-        store_row16<D, kF16>(t_lane + 128, reinterpret_cast<uint16_t*>(p.dv) + off, 1.0f, st, T == 0);
+        store_row16<D, kF16>(t_lane + 128, reinterpret_cast<uint16_t*>(p.dv) + off, 1.0f, st, T == 0, p.dh);
     }
   }
 
@@ -660,8 +660,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       constexpr int kPer = D / C::kNWG;
       const bool st = i < p.Lq;
       uint16_t* dst = reinterpret_cast<uint16_t*>(p.dq) +
-                           ((static_cast<size_t>(b) * p.Lq + (st ? i : 0)) * p.Hq + h) * D + w * kPer;
-      store_cols16<kPer, kF16>(t_lane + w * kPer, dst, p.scale, st, T == 0);
+                      ((static_cast<size_t>(b) * p.Lq + (st ? i : 0)) * p.Hq + h) * p.dh + w * kPer;
+      if (w * kPer < p.dh) store_cols16<kPer, kF16>(t_lane + w * kPer, dst, p.scale, st, T == 0);
     }
   }
 
@@ -710,7 +710,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
   pa.Lq = pb.Lq;
   pa.Lq_pad = a.Lq_pad;
   pa.Hq = pb.Hq;
-  pa.d = D;
+  pa.d = pb.d;  // stored head_dim: the preprocess reads O and dO rows of this width
   pa.elem = elem;
   cudaError_t e = launch_bwd_preprocess(pa, stream);
   if (e != cudaSuccess) return e;
@@ -732,6 +732,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
   kp.wl = pb.wl;
   kp.wr = pb.wr;
   kp.Lq_pad = a.Lq_pad;
+  kp.dh = pb.d;
   kp.scale = pb.scale;
   kp.scale_log2 = pb.scale * kLog2e;
   kp.status = st;
@@ -739,17 +740,17 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
   // dK/dV pass (both variants): Q/dO and K/V boxes of 128 rows
   {
     CUtensorMap tk, tv, tq128, tdo128;
-    if (!make_bshd_tmap(&tq128, a.q, elem, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
-        !make_bshd_tmap(&tdo128, a.dout, elem, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
-        !make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, D, 64, 128) ||
-        !make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, D, 64, 128))
+    if (!make_bshd_tmap(&tq128, a.q, elem, pb.B, pb.Lq, pb.Hq, pb.d, 64, 128) ||
+        !make_bshd_tmap(&tdo128, a.dout, elem, pb.B, pb.Lq, pb.Hq, pb.d, 64, 128) ||
+        !make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, 128) ||
+        !make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, 128))
       return cudaErrorInvalidValue;
     kp.n_tiles = (pb.Lkv + 127) / 128;
     kp.n_pairs = pb.B * pb.Hkv;
     kp.pair_group = l2_pair_group(2l * pb.G * pb.Lq * D * 2, kp.n_pairs, 1);
     dim3 grid(kp.n_pairs * kp.n_tiles);
     if (!a.deterministic)
-      return launch_single_pass<D>(tq128, tk, tv, tdo128, kp, grid, static_cast<long>(pb.B) * pb.Lq * pb.Hq * D,
+      return launch_single_pass<D>(tq128, tk, tv, tdo128, kp, grid, static_cast<long>(pb.B) * pb.Lq * pb.Hq * pb.d,
                                    pb.f16 != 0, stream);
     const bool left = pb.wl < kWinInf;
     e = pb.f16 ? (left ? launch_dkdv_inst<D, true, true>(tq128, tk, tv, tdo128, kp, grid, stream)
@@ -761,10 +762,10 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
   // dQ pass: Q/dO and K/V boxes of 128 rows
   {
     CUtensorMap tq, tk, tv, tdo;
-    if (!make_bshd_tmap(&tq, a.q, elem, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
-        !make_bshd_tmap(&tdo, a.dout, elem, pb.B, pb.Lq, pb.Hq, D, 64, 128) ||
-        !make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, D, 64, 128) ||
-        !make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, D, 64, 128))
+    if (!make_bshd_tmap(&tq, a.q, elem, pb.B, pb.Lq, pb.Hq, pb.d, 64, 128) ||
+        !make_bshd_tmap(&tdo, a.dout, elem, pb.B, pb.Lq, pb.Hq, pb.d, 64, 128) ||
+        !make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, 128) ||
+        !make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, 128))
       return cudaErrorInvalidValue;
     kp.n_tiles = (pb.Lq + 127) / 128;
     kp.n_pairs = pb.B * pb.Hq;
@@ -781,7 +782,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
 }  // namespace
 
 cudaError_t launch_bwd_16(const BwdArgs& a, DeviceStatus* st, cudaStream_t s) {
-  return a.pb.d == 64 ? launch_bwd_d<64>(a, st, s) : launch_bwd_d<128>(a, st, s);
+  return a.pb.d <= 64 ? launch_bwd_d<64>(a, st, s) : launch_bwd_d<128>(a, st, s);  // head_dim 32 runs as 64
 }
 
 }  // namespace attn

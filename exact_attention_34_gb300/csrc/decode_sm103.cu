@@ -41,6 +41,7 @@ struct DecKParams {
   float* lse_part;
   const int32_t* kv_lens;
   int Lq, Lkv, Hq, Hkv, G, causal, num_splits, chunk;
+  int dh;  // stored head_dim (32 runs as D = 64 with zero-filled columns)
   float scale_log2;
   DeviceStatus* status;
 };
@@ -252,6 +253,7 @@ __global__ void __launch_bounds__(192, 1)
       const size_t prow = ((static_cast<size_t>(b) * p.Hq + hq) * p.num_splits + split) * p.Lq + i;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
+        if (c * 32 >= p.dh) break;
         uint32_t rr[32];
         if (n > 0) {
           tmem_ld32(t_lane + 256 + c * 32, rr);
@@ -260,7 +262,7 @@ __global__ void __launch_bounds__(192, 1)
           for (int e = 0; e < 32; ++e) rr[e] = 0u;
         }
         if (real) {
-          float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D + c * 32);
+          float4* dst = reinterpret_cast<float4*>(p.o_part + prow * p.dh + c * 32);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             dst[e] = make_float4(__uint_as_float(rr[4 * e]) * inv_l, __uint_as_float(rr[4 * e + 1]) * inv_l,
@@ -323,9 +325,9 @@ cudaError_t launch_decode_d(const DecodeArgs& a, DeviceStatus* st, cudaStream_t 
   const Problem& pb = a.pb;
   const int elem = pb.f16 ? kElemF16 : kElemBF16;
   CUtensorMap tq, tk, tv;
-  if (!make_q_group_tmap(&tq, a.q, pb.B, pb.Lq, pb.Hq, D, pb.G, pb.f16 != 0)) return cudaErrorInvalidValue;
-  if (!make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
-  if (!make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
+  if (!make_q_group_tmap(&tq, a.q, pb.B, pb.Lq, pb.Hq, pb.d, pb.G, pb.f16 != 0)) return cudaErrorInvalidValue;
+  if (!make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, kBN)) return cudaErrorInvalidValue;
+  if (!make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, kBN)) return cudaErrorInvalidValue;
   DecKParams kp;
   kp.o_part = a.o_part;
   kp.lse_part = a.lse_part;
@@ -336,6 +338,7 @@ cudaError_t launch_decode_d(const DecodeArgs& a, DeviceStatus* st, cudaStream_t 
   kp.Hkv = pb.Hkv;
   kp.G = pb.G;
   kp.causal = pb.causal;
+  kp.dh = pb.d;
   kp.num_splits = a.num_splits;
   kp.chunk = a.chunk;
   kp.scale_log2 = pb.scale * kLog2e;
@@ -348,7 +351,7 @@ cudaError_t launch_decode_d(const DecodeArgs& a, DeviceStatus* st, cudaStream_t 
 }  // namespace
 
 cudaError_t launch_decode_16(const DecodeArgs& a, DeviceStatus* st, cudaStream_t s) {
-  return a.pb.d == 64 ? launch_decode_d<64>(a, st, s) : launch_decode_d<128>(a, st, s);
+  return a.pb.d <= 64 ? launch_decode_d<64>(a, st, s) : launch_decode_d<128>(a, st, s);  // head_dim 32 runs as 64
 }
 
 }  // namespace attn

@@ -53,6 +53,7 @@ struct FwdKParams {
   float* lse;
   const int32_t* kv_lens;
   int Lq, Lkv, Hq, Hkv, G, causal, wl, wr, n_qblocks, n_pairs, pair_group;
+  int dh;  // stored head_dim (32 runs as D = 64 with zero-filled columns)
   float scale_log2;
   DeviceStatus* status;
 };
@@ -309,9 +310,10 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
       uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
-                            ((static_cast<size_t>(b) * p.Lq + row) * p.Hq + hq) * D;
+                            ((static_cast<size_t>(b) * p.Lq + row) * p.Hq + hq) * p.dh;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
+        if (c * 32 >= p.dh) break;
         uint32_t r[32];
         if (n_x > 0) {
           tmem_ld32(o_addr + c * 32, r);
@@ -360,9 +362,9 @@ cudaError_t launch_fwd_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t stream
   const Problem& pb = a.pb;
   const int elem = pb.f16 ? kElemF16 : kElemBF16;
   CUtensorMap tq, tk, tv;
-  if (!make_bshd_tmap(&tq, a.q, elem, pb.B, pb.Lq, pb.Hq, D, 64, kBM)) return cudaErrorInvalidValue;
-  if (!make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
-  if (!make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, D, 64, kBN)) return cudaErrorInvalidValue;
+  if (!make_bshd_tmap(&tq, a.q, elem, pb.B, pb.Lq, pb.Hq, pb.d, 64, kBM)) return cudaErrorInvalidValue;
+  if (!make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, kBN)) return cudaErrorInvalidValue;
+  if (!make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, kBN)) return cudaErrorInvalidValue;
   FwdKParams kp;
   kp.o = a.o;
   kp.lse = a.lse;
@@ -375,6 +377,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t stream
   kp.causal = pb.causal;
   kp.wl = pb.wl;
   kp.wr = pb.wr;
+  kp.dh = pb.d;
   kp.n_qblocks = (pb.Lq + 2 * kBM - 1) / (2 * kBM);
   kp.n_pairs = pb.B * pb.Hq;
   kp.pair_group = l2_pair_group(2l * pb.Lkv * D * 2, kp.n_pairs, pb.G);
@@ -392,7 +395,9 @@ cudaError_t launch_fwd_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t stream
 }  // namespace
 
 cudaError_t launch_fwd_16(const FwdArgs& a, DeviceStatus* st, cudaStream_t s) {
-  if (a.pb.d == 64) return launch_fwd_d<64>(a, st, s);
+  // head_dim 32 runs through the 64-column kernel: TMA zero-fills columns
+  // 32..63 of Q, K and V, so S and the first 32 columns of O are exact
+  if (a.pb.d <= 64) return launch_fwd_d<64>(a, st, s);
   return launch_fwd_d<128>(a, st, s);
 }
 

@@ -503,7 +503,7 @@ cudaError_t launch_fwd_f32(const FwdArgs& a, DeviceStatus* st, cudaStream_t s) {
   p.lse = a.lse;
   p.num_splits = 1;
   p.chunk = a.pb.Lkv;
-  return a.pb.d == 64 ? run_fwd<64>(p, 1, s) : run_fwd<128>(p, 1, s);
+  return a.pb.d == 32 ? run_fwd<32>(p, 1, s) : a.pb.d == 64 ? run_fwd<64>(p, 1, s) : run_fwd<128>(p, 1, s);
 }
 
 cudaError_t launch_decode_f32(const DecodeArgs& a, DeviceStatus* st, cudaStream_t s) {
@@ -513,7 +513,9 @@ cudaError_t launch_decode_f32(const DecodeArgs& a, DeviceStatus* st, cudaStream_
   p.lse_part = a.lse_part;
   p.num_splits = a.num_splits;
   p.chunk = a.chunk;
-  return a.pb.d == 64 ? run_fwd<64>(p, a.num_splits, s) : run_fwd<128>(p, a.num_splits, s);
+  return a.pb.d == 32   ? run_fwd<32>(p, a.num_splits, s)
+         : a.pb.d == 64 ? run_fwd<64>(p, a.num_splits, s)
+                        : run_fwd<128>(p, a.num_splits, s);
 }
 
 cudaError_t launch_bwd_f32(const BwdArgs& a, DeviceStatus* st, cudaStream_t s) {
@@ -557,7 +559,9 @@ cudaError_t launch_bwd_f32(const BwdArgs& a, DeviceStatus* st, cudaStream_t s) {
   p.wr = pb.wr;
   p.scale = pb.scale;
   p.scale_log2 = pb.scale * kLog2e;
-  return pb.d == 64 ? run_bwd<64>(p, !a.deterministic, s) : run_bwd<128>(p, !a.deterministic, s);
+  return pb.d == 32   ? run_bwd<32>(p, !a.deterministic, s)
+         : pb.d == 64 ? run_bwd<64>(p, !a.deterministic, s)
+                      : run_bwd<128>(p, !a.deterministic, s);
 }
 
 }  // namespace attn

@@ -125,11 +125,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       if (ls == -INFINITY) continue;
       const float w = expf(ls - m) * inv;
       const float* src = o_part + ((bh * S + s) * Lq + i) * D + lane * kPer;
+      if constexpr (kPer % 2 == 0) {
 #pragma unroll
-      for (int e = 0; e < kPer; e += 2) {
-        const float2 v = *reinterpret_cast<const float2*>(src + e);
-        acc[e] = fmaf(w, v.x, acc[e]);
-        acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
+        for (int e = 0; e < kPer; e += 2) {
+          const float2 v = *reinterpret_cast<const float2*>(src + e);
+          acc[e] = fmaf(w, v.x, acc[e]);
+          acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) acc[e] = fmaf(w, src[e], acc[e]);
       }
     }
   }
@@ -171,23 +176,29 @@ cudaError_t run_combine(const float* o_part, const float* lse_part, void* o, flo
 
 cudaError_t launch_bwd_preprocess(const PreprocessArgs& a, cudaStream_t s) {
   if (a.elem == kElemBF16)
-    return a.d == 64 ? run_preprocess<__nv_bfloat16, 64>(a, s) : run_preprocess<__nv_bfloat16, 128>(a, s);
-  if (a.elem == kElemF16) return a.d == 64 ? run_preprocess<__half, 64>(a, s) : run_preprocess<__half, 128>(a, s);
-  return a.d == 64 ? run_preprocess<float, 64>(a, s) : run_preprocess<float, 128>(a, s);
+    return a.d == 32   ? run_preprocess<__nv_bfloat16, 32>(a, s)
+           : a.d == 64 ? run_preprocess<__nv_bfloat16, 64>(a, s)
+                       : run_preprocess<__nv_bfloat16, 128>(a, s);
+  if (a.elem == kElemF16)
+    return a.d == 32   ? run_preprocess<__half, 32>(a, s)
+           : a.d == 64 ? run_preprocess<__half, 64>(a, s)
+                       : run_preprocess<__half, 128>(a, s);
+  return a.d == 32 ? run_preprocess<float, 32>(a, s)
+         : a.d == 64 ? run_preprocess<float, 64>(a, s)
+                     : run_preprocess<float, 128>(a, s);
 }
 
 cudaError_t launch_decode_combine(const float* o_part, const float* lse_part, void* o, float* lse, int B, int Lq,
                                   int Hq, int d, int num_splits, int elem, cudaStream_t s) {
-  if (elem == kElemBF16) {
-    return d == 64 ? run_combine<__nv_bfloat16, 64>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s)
-                   : run_combine<__nv_bfloat16, 128>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s);
-  }
-  if (elem == kElemF16) {
-    return d == 64 ? run_combine<__half, 64>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s)
-                   : run_combine<__half, 128>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s);
-  }
-  return d == 64 ? run_combine<float, 64>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s)
-                 : run_combine<float, 128>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s);
+  auto run = [&](auto tag) -> cudaError_t {
+    using T = decltype(tag);
+    if (d == 32) return run_combine<T, 32>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s);
+    if (d == 64) return run_combine<T, 64>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s);
+    return run_combine<T, 128>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s);
+  };
+  if (elem == kElemBF16) return run(__nv_bfloat16{});
+  if (elem == kElemF16) return run(__half{});
+  return run(float{});
 }
 
 }  // namespace attn

@@ -36,9 +36,11 @@
  *     argument returns an error code and launches nothing.  Values that live
  *     on the device (kv_lens) cannot be checked there and are clamped into
  *     [0, Lkv] by the kernels.
- *   - dtype ATTN_BF16: q/k/v/o/dout/dq/dk/dv are bf16; ATTN_FP32: all float32.
- *     lse, delta, partials and workspaces are always float32.
- *   - head_dim d must be 64 or 128.
+ *   - dtype ATTN_BF16 / ATTN_FP16: q/k/v/o/dout/dq/dk/dv are bf16 / fp16;
+ *     ATTN_FP32: all float32.  lse, delta, partials and workspaces are always
+ *     float32.
+ *   - head_dim d must be 32, 64 or 128 (32 runs through the 64-wide kernels
+ *     with zero-filled columns, as the pages' kernels pad it).
  *   - Calls are thread-safe: no mutable global state is shared between calls
  *     (tensor-map descriptors are built per call and passed by value).
  */
