@@ -536,8 +536,8 @@ def run_sweep(args):
     """The pages' attention grid ("Attention performance", section "Time"): B4 H8,
     d in {64, 128}, T in {128 ... 8192} plus the ragged 600 / 1500 / 3000, causal
     and not, bf16; fwd and fwd+bwd TFLOP/s (deterministic backward).  One JSON
-    line per case, median of 5 repeats with the quartiles.  Also fp32 at d=128
-    for T <= 2048."""
+    line per case, median of 5 repeats with the quartiles.  Also head_dim 32
+    (bf16) and fp32 at d=128 for T <= 2048."""
     import torch
 
     import exact_attention_34_gb300 as ea
@@ -564,6 +564,7 @@ def run_sweep(args):
         return runs[len(runs) // 4], runs[len(runs) // 2], runs[(3 * len(runs)) // 4]
 
     cases = [(T, d, c, "bf16") for d in (64, 128) for T in W.GRID_T + W.RAGGED_T for c in (False, True)]
+    cases += [(T, 32, c, "bf16") for T in W.GRID_T for c in (False, True)]  # head_dim 32 (runs as 64)
     cases += [(T, 128, c, "fp32") for T in (128, 512, 1024, 2048) for c in (False, True)]
     for T, d, c, dt in cases:
         p = W.grid(T, d, c, dt)
