@@ -278,34 +278,92 @@ def run_gpu(args):
                                       if n in algo and ktimes[n]["avg_ms"] > 0 else {})}
                                for n in ktimes}}
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers.  Every step
+    # copies its inputs host -> device and its gradients device -> host; the
+    # uploads of step t+1 and the downloads of step t-1 run on two copy streams
+    # (one per direction) while step t computes, with two sets of device buffers.
     dq_h, dk_h, dv_h = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv))
-    q2, k2, v2, do2 = (torch.empty_like(t) for t in (q, k, v, do))
+    host_in, host_out = (q_h, k_h, v_h, do_h), (dq_h, dk_h, dv_h)
+    dev_in = [[torch.empty_like(t) for t in (q, k, v, do)] for _ in range(2)]
+    dev_out = [[torch.empty_like(t) for t in (dq, dk, dv)] for _ in range(2)]
+    dev_ol = [(torch.empty_like(o), torch.empty_like(lse)) for _ in range(2)]
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    h2d_done, comp_done, d2h_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
 
-    def e2e_step():
-        for dst, src in ((q2, q_h), (k2, k_h), (v2, v_h), (do2, do_h)):
-            dst.copy_(src, non_blocking=True)
-        ea.attn_fwd(q2, k2, v2, o, lse, causal=True, stream=stream)
-        ea.attn_bwd(q2, k2, v2, o, lse, do2, dq, dk, dv, ws, causal=True, deterministic=True, stream=stream)
-        for dst, src in ((dq_h, dq), (dk_h, dk), (dv_h, dv)):
-            dst.copy_(src, non_blocking=True)
+    def h2d(t):
+        bi = t % 2
+        with torch.cuda.stream(up):
+            if t >= 2:
+                up.wait_event(comp_done[bi])  # step t-2 has finished reading these inputs
+            for dst, src in zip(dev_in[bi], host_in):
+                dst.copy_(src, non_blocking=True)
+            h2d_done[bi].record(up)
+
+    def compute(t):
+        bi = t % 2
+        stream.wait_event(h2d_done[bi])
+        if t >= 2:
+            stream.wait_event(d2h_done[bi])  # step t-2's gradients have left these buffers
+        q2, k2, v2, do2 = dev_in[bi]
+        o2, lse2 = dev_ol[bi]
+        g = dev_out[bi]
+        ea.attn_fwd(q2, k2, v2, o2, lse2, causal=True, stream=stream)
+        ea.attn_bwd(q2, k2, v2, o2, lse2, do2, g[0], g[1], g[2], ws, causal=True, deterministic=True, stream=stream)
+        comp_done[bi].record(stream)
+
+    def d2h(t):
+        bi = t % 2
+        with torch.cuda.stream(down):
+            down.wait_event(comp_done[bi])
+            for dst, src in zip(host_out, dev_out[bi]):
+                dst.copy_(src, non_blocking=True)
+            d2h_done[bi].record(down)
+
+    def run_pipelined(n):
+        h2d(0)
+        for t in range(n):
+            if t + 1 < n:
+                h2d(t + 1)
+            compute(t)
+            d2h(t)
 
     e2e_steps = max(3, args.steps // 10)
-    for _ in range(2):
-        e2e_step()
+    run_pipelined(2)
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(up)
+    run_pipelined(e2e_steps)
+    e1.record(down)  # after the last gradients reached the host
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, do_h))
-    d2h = sum(t.numel() * t.element_size() for t in (dq_h, dk_h, dv_h))
+
+    # the same steps with every copy serialised on the compute stream (context)
+    def serial_step():
+        q2, k2, v2, do2 = dev_in[0]
+        for dst, src in zip(dev_in[0], host_in):
+            dst.copy_(src, non_blocking=True)
+        ea.attn_fwd(q2, k2, v2, o, lse, causal=True, stream=stream)
+        ea.attn_bwd(q2, k2, v2, o, lse, do2, dq, dk, dv, ws, causal=True, deterministic=True, stream=stream)
+        for dst, src in zip(host_out, (dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    serial_step()
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(e2e_steps):
+        serial_step()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    serial_ms = max_over_ranks(s0.elapsed_time(s1), world, dev)
+    h2d_b = sum(t.numel() * t.element_size() for t in host_in)
+    d2h_b = sum(t.numel() * t.element_size() for t in host_out)
     e2e = {"value": round(whole_job_value(F_step, e2e_steps, world, e2e_ms), 2), "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+           "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b, "steps": e2e_steps,
+           "overlap": "H2D of step t+1 and D2H of step t-1 on two copy streams during step t",
+           "serial_value": round(whole_job_value(F_step, e2e_steps, world, serial_ms), 2)}
 
     st, code, site = ea.attn_device_status()
     if code != 0:
