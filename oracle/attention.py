@@ -35,6 +35,9 @@ Readings where the pages are silent (each listed in the design notes):
   this is the usual ``j <= i``;
 * the log-sum-exp is the natural logarithm, ``lse[b, h, i]``, and ``-inf`` on a
   row with no valid key (whose output is 0);
+* segment (document) masks compare per-token ids: key j is valid for row i
+  of batch b only if ``q_segment[b, i] == kv_segment[b, j]`` (on top of the
+  position masks);
 * a local window ``(left, right)`` is taken around the same bottom-right
   aligned diagonal: key j is valid for row i iff
   ``i + kvl[b] - Lq - left <= j <= i + kvl[b] - Lq + right`` (and ``j < kvl[b]``);
@@ -84,7 +87,8 @@ def effective_kv_lens(B: int, Lkv: int, kv_lens) -> np.ndarray:
     return np.clip(kl, 0, Lkv)
 
 
-def valid_keys(rows: np.ndarray, Lq: int, Lkv: int, kvl_b: int, causal: bool, window=None) -> np.ndarray:
+def valid_keys(rows: np.ndarray, Lq: int, Lkv: int, kvl_b: int, causal: bool, window=None, q_seg_b=None,
+               kv_seg_b=None) -> np.ndarray:
     """Boolean matrix ``[len(rows), Lkv]``: is key j valid for query row i.
 
     KVLenMask: ``j < kvl_b``.  Causal (bottom-right reading for Lq != Lkv):
@@ -104,7 +108,20 @@ def valid_keys(rows: np.ndarray, Lq: int, Lkv: int, kvl_b: int, causal: bool, wi
             ok = ok & (j >= diag - left)
         if right is not None and right >= 0:
             ok = ok & (j <= diag + right)
+    if q_seg_b is not None:
+        qs = np.asarray(q_seg_b)[np.asarray(rows, dtype=np.int64)][:, None]
+        ok = ok & (qs == np.asarray(kv_seg_b)[None, :])
     return np.broadcast_to(ok, (len(rows), Lkv)).copy()
+
+
+def _segments_of(segments, b):
+    """(q_segment[b], kv_segment[b]) as int64 arrays, or (None, None)."""
+    if segments is None:
+        return None, None
+    qs, ks = segments
+    qs = np.asarray(qs if not hasattr(qs, "numpy") else qs.cpu().numpy()).astype(np.int64)
+    ks = np.asarray(ks if not hasattr(ks, "numpy") else ks.cpu().numpy()).astype(np.int64)
+    return qs[b], ks[b]
 
 
 def _check_shapes(q, k, v):
@@ -137,7 +154,7 @@ def _head_probs(qh, kh, scale, mask):
     return p, lse
 
 
-def forward(q, k, v, scale=None, causal=False, kv_lens=None, rows=None, heads=None, window=None,
+def forward(q, k, v, scale=None, causal=False, kv_lens=None, rows=None, heads=None, window=None, segments=None,
             row_block: int = 1024):
     """Exact attention forward: ``O = softmax(scale * Q K^T) V`` and ``LSE``.
 
@@ -160,14 +177,14 @@ def forward(q, k, v, scale=None, causal=False, kv_lens=None, rows=None, heads=No
             hk = hq // G
             for r0 in range(0, len(rows), row_block):
                 rr = rows[r0:r0 + row_block]
-                mask = valid_keys(rr, Lq, Lkv, int(kvl[b]), causal, window)
+                mask = valid_keys(rr, Lq, Lkv, int(kvl[b]), causal, window, *_segments_of(segments, b))
                 p, l_ = _head_probs(q[b, rr, hq, :], k[b, :, hk, :], scale, mask)
                 o[b, r0:r0 + len(rr), hq, :] = p @ v[b, :, hk, :]
                 lse[b, hq, r0:r0 + len(rr)] = l_
     return o, lse
 
 
-def probabilities(q, k, scale=None, causal=False, kv_lens=None, window=None):
+def probabilities(q, k, scale=None, causal=False, kv_lens=None, window=None, segments=None):
     """The full probability tensor ``P [B, Hq, Lq, Lkv]`` (tiny inputs only)."""
     q, k = _f64(q), _f64(k)
     B, Lq, Hq, d = q.shape
@@ -179,12 +196,12 @@ def probabilities(q, k, scale=None, causal=False, kv_lens=None, window=None):
     rows = np.arange(Lq)
     for b in range(B):
         for hq in range(Hq):
-            mask = valid_keys(rows, Lq, Lkv, int(kvl[b]), causal, window)
+            mask = valid_keys(rows, Lq, Lkv, int(kvl[b]), causal, window, *_segments_of(segments, b))
             out[b, hq], _ = _head_probs(q[b, :, hq, :], k[b, :, hq // G, :], scale, mask)
     return out
 
 
-def backward(q, k, v, do, scale=None, causal=False, kv_lens=None, kv_heads=None, window=None,
+def backward(q, k, v, do, scale=None, causal=False, kv_lens=None, kv_heads=None, window=None, segments=None,
              row_block: int = 1024, rows=None):
     """Analytic gradient of ``sum(O * dO)`` with respect to q, k and v.
 
@@ -224,7 +241,7 @@ def backward(q, k, v, do, scale=None, causal=False, kv_lens=None, kv_heads=None,
             for hq in range(hk * G, (hk + 1) * G):
                 for r0 in range(0, len(all_rows), row_block):
                     rr = all_rows[r0:r0 + row_block]
-                    mask = valid_keys(rr, Lq, Lkv, int(kvl[b]), causal, window)
+                    mask = valid_keys(rr, Lq, Lkv, int(kvl[b]), causal, window, *_segments_of(segments, b))
                     p, _ = _head_probs(q[b, rr, hq, :], kh, scale, mask)
                     doh = do[b, rr, hq, :]
                     acc_dv += p.T @ doh

@@ -503,3 +503,102 @@ def test_window_zero_width_gives_the_diagonal_value():
     dq, dk, dv = oracle.backward(q, k, v, do, window=(0, 0))
     assert np.all(dq == 0) and np.all(dk == 0)
     np.testing.assert_allclose(dv, do, rtol=0, atol=1e-15)
+
+
+# --------------------------------------------------------------------------
+# segment (document) masks: ids per token, a key is kept only for rows with
+# the same id ("Attention performance", section "H100 (Hopper)" / "Mosaic
+# GPU" list segments among the masks; flex-attention style document masks)
+# --------------------------------------------------------------------------
+
+def brute_force_segments(q, k, v, scale, qseg, kseg, causal):
+    B, Lq, Hq, d = q.shape
+    Lkv, Hkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    o = np.zeros((B, Lq, Hq, d))
+    for b in range(B):
+        for h in range(Hq):
+            for i in range(Lq):
+                keys = [j for j in range(Lkv) if qseg[b][i] == kseg[b][j] and (not causal or j <= i + Lkv - Lq)]
+                if not keys:
+                    continue
+                sc = [scale * sum(float(q[b, i, h, c]) * float(k[b, j, h // G, c]) for c in range(d)) for j in keys]
+                mx = max(sc)
+                w = [math.exp(x - mx) for x in sc]
+                z = sum(w)
+                for wj, j in zip(w, keys):
+                    for c in range(d):
+                        o[b, i, h, c] += wj / z * float(v[b, j, h // G, c])
+    return o
+
+
+SEG_CASES = [
+    # B, Lq, Lkv, H, d, causal, q segment ids, kv segment ids
+    (1, 6, 6, 2, 3, False, [[0, 0, 1, 1, 1, 2]], [[0, 0, 1, 1, 1, 2]]),
+    (1, 6, 6, 2, 3, True, [[0, 0, 1, 1, 1, 2]], [[0, 0, 1, 1, 1, 2]]),
+    (2, 4, 7, 2, 2, False, [[3, 1, 1, 9], [0, 0, 0, 0]], [[1, 3, 3, 1, 7, 7, 1], [0, 1, 0, 1, 0, 1, 0]]),
+]
+
+
+@pytest.mark.parametrize("case", SEG_CASES)
+def test_segments_forward_matches_brute_force(case):
+    B, Lq, Lkv, H, d, causal, qs, ks = case
+    q, k, v = rnd((B, Lq, H, d), 91), rnd((B, Lkv, H, d), 92), rnd((B, Lkv, H, d), 93)
+    o, _ = oracle.forward(q, k, v, scale=0.8, causal=causal, segments=(qs, ks))
+    np.testing.assert_allclose(o, brute_force_segments(q, k, v, 0.8, qs, ks, causal), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("case", SEG_CASES)
+def test_segments_backward_matches_finite_differences(case):
+    B, Lq, Lkv, H, d, causal, qs, ks = case
+    q, k, v, do = rnd((B, Lq, H, d), 94), rnd((B, Lkv, H, d), 95), rnd((B, Lkv, H, d), 96), rnd((B, Lq, H, d), 97)
+    dq, dk, dv = oracle.backward(q, k, v, do, scale=0.8, causal=causal, segments=(qs, ks))
+
+    def loss():
+        o, _ = oracle.forward(q, k, v, scale=0.8, causal=causal, segments=(qs, ks))
+        return float(np.sum(o * do))
+
+    h = 1e-6
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = x[idx]
+            x[idx] = old + h
+            fp = loss()
+            x[idx] = old - h
+            fm = loss()
+            x[idx] = old
+            num[idx] = (fp - fm) / (2 * h)
+        assert np.max(np.abs(num - g)) / max(1.0, np.max(np.abs(num))) < 1e-6
+
+
+def test_segments_against_torch_boolean_mask():
+    """torch float64 SDPA with the mask built by comparing the id tensors."""
+    B, Lq, Lkv, H, d, scale = 2, 9, 9, 2, 4, 0.5
+    rng = np.random.default_rng(3)
+    qs = np.sort(rng.integers(0, 3, size=(B, Lq)), axis=1)
+    ks = qs.copy()
+    q, k, v, do = rnd((B, Lq, H, d), 101), rnd((B, Lkv, H, d), 102), rnd((B, Lkv, H, d), 103), rnd((B, Lq, H, d), 104)
+    mask = torch.tensor(qs)[:, None, :, None] == torch.tensor(ks)[:, None, None, :]
+    o_t, dq_t, dk_t, dv_t = _torch_ref(q, k, v, do, scale, mask)
+    o, _ = oracle.forward(q, k, v, scale=scale, segments=(qs, ks))
+    dq, dk, dv = oracle.backward(q, k, v, do, scale=scale, segments=(qs, ks))
+    for a, b in ((o, o_t), (dq, dq_t), (dk, dk_t), (dv, dv_t)):
+        np.testing.assert_allclose(a, b, rtol=1e-11, atol=1e-12)
+
+
+def test_segments_special_cases():
+    """one shared id is no mask; per-token unique ids with Lq == Lkv leave each
+    row its own key (O = V exactly, dQ = dK = 0)."""
+    B, L, H, d = 2, 7, 2, 3
+    q, k, v, do = rnd((B, L, H, d), 111), rnd((B, L, H, d), 112), rnd((B, L, H, d), 113), rnd((B, L, H, d), 114)
+    same = np.zeros((B, L), dtype=np.int64)
+    a, b_ = oracle.forward(q, k, v, segments=(same, same)), oracle.forward(q, k, v)
+    assert np.array_equal(a[0], b_[0]) and np.array_equal(a[1], b_[1])
+    uniq = np.tile(np.arange(L), (B, 1))
+    o, _ = oracle.forward(q, k, v, segments=(uniq, uniq))
+    np.testing.assert_array_equal(o, v)
+    dq, dk, dv = oracle.backward(q, k, v, do, segments=(uniq, uniq))
+    assert np.all(dq == 0) and np.all(dk == 0)
