@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
         "attn_bwd_static_scratch": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, I, P]),
         "attn_fwd_window": (I, [P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, I, P]),
         "attn_bwd_window": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, I, I, P, S, P]),
+        "attn_fwd_segments": (I, [P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, P, P, I, P]),
+        "attn_bwd_segments": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, P, P, I, I, P, S, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -88,7 +90,7 @@ EXPORTED = (
     "attn_status_string", "attn_last_error", "attn_fwd", "attn_bwd_preprocess", "attn_bwd_workspace_size",
     "attn_bwd", "attn_decode_num_splits", "attn_decode_splitkv", "attn_decode_combine",
     "attn_decode_workspace_size", "attn_device_status", "attn_timing_enable", "attn_timing_query",
-    "attn_bwd_static_scratch", "attn_fwd_window", "attn_bwd_window",
+    "attn_bwd_static_scratch", "attn_fwd_window", "attn_bwd_window", "attn_fwd_segments", "attn_bwd_segments",
 )
 
 
@@ -150,6 +152,16 @@ def attn_fwd_window(q, k, v, o, lse, window, scale=None, kv_lens=None, stream=No
            "attn_fwd_window")
 
 
+def attn_fwd_segments(q, k, v, o, lse, q_segment, kv_segment, window=(-1, -1), scale=None, kv_lens=None,
+                      stream=None):
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    wl, wr = _window(window)
+    _check(lib().attn_fwd_segments(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Lq, Lkv, Hq, Hkv, d,
+                                   _scale(scale, d), wl, wr, _ptr(q_segment), _ptr(kv_segment), _ptr(kv_lens),
+                                   _dtype(q), _stream(stream)),
+           "attn_fwd_segments")
+
+
 def attn_bwd_preprocess(o, dout, delta, stream=None):
     B, Lq, Hq, d = o.shape
     _check(lib().attn_bwd_preprocess(_ptr(o), _ptr(dout), _ptr(delta), B, Lq, Hq, d, _dtype(o), _stream(stream)),
@@ -179,6 +191,18 @@ def attn_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, workspace, window, scale=
                                  _ptr(dv), B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d), wl, wr, _ptr(kv_lens),
                                  _dtype(q), int(bool(deterministic)), _ptr(workspace), ws_bytes, _stream(stream)),
            "attn_bwd_window")
+
+
+def attn_bwd_segments(q, k, v, o, lse, dout, dq, dk, dv, workspace, q_segment, kv_segment, window=(-1, -1),
+                      scale=None, kv_lens=None, deterministic=True, stream=None):
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    wl, wr = _window(window)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().attn_bwd_segments(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                   _ptr(dv), B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d), wl, wr, _ptr(q_segment),
+                                   _ptr(kv_segment), _ptr(kv_lens), _dtype(q), int(bool(deterministic)),
+                                   _ptr(workspace), ws_bytes, _stream(stream)),
+           "attn_bwd_segments")
 
 
 def attn_decode_num_splits(B, Lq, Lkv, Hq, Hkv, d) -> int:
@@ -237,13 +261,23 @@ def attn_timing_query(kernel: str):
 
 # ---- conveniences that allocate outputs with torch ------------------------------
 
-def forward(q, k, v, scale=None, causal=False, kv_lens=None, stream=None, window=None):
+def _mask_window(causal, window):
+    if window is not None and causal:
+        raise ValueError("pass either causal or window (causal is window (-1, 0))")
+    return window if window is not None else ((-1, 0) if causal else (-1, -1))
+
+
+def forward(q, k, v, scale=None, causal=False, kv_lens=None, stream=None, window=None, segments=None):
     """(o, lse) for q [B,Lq,Hq,d], k/v [B,Lkv,Hkv,d] on the GPU.  window =
-    (left, right) selects the local-window mask (causal must then be False)."""
+    (left, right) selects the local-window mask (causal must then be False);
+    segments = (q_segment [B,Lq], kv_segment [B,Lkv]) int32 adds a segment mask."""
     B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
     o = torch.empty_like(q)
     lse = torch.empty(B, Hq, Lq, device=q.device, dtype=torch.float32)
-    if window is not None:
+    if segments is not None:
+        attn_fwd_segments(q, k, v, o, lse, segments[0], segments[1], _mask_window(causal, window), scale, kv_lens,
+                          stream)
+    elif window is not None:
         if causal:
             raise ValueError("pass either causal or window (causal is window (-1, 0))")
         attn_fwd_window(q, k, v, o, lse, window, scale, kv_lens, stream)
@@ -253,13 +287,16 @@ def forward(q, k, v, scale=None, causal=False, kv_lens=None, stream=None, window
 
 
 def backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_lens=None, deterministic=True, stream=None,
-             window=None):
+             window=None, segments=None):
     """(dq, dk, dv) given the forward's o and lse (same mask arguments as forward)."""
     B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
     nbytes = attn_bwd_workspace_size(B, Lq, Hq, d, deterministic, q.dtype)
     ws = torch.empty(max(nbytes, 256), device=q.device, dtype=torch.uint8)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    if window is not None:
+    if segments is not None:
+        attn_bwd_segments(q, k, v, o, lse, dout, dq, dk, dv, ws, segments[0], segments[1],
+                          _mask_window(causal, window), scale, kv_lens, deterministic, stream)
+    elif window is not None:
         if causal:
             raise ValueError("pass either causal or window (causal is window (-1, 0))")
         attn_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, ws, window, scale, kv_lens, deterministic, stream)

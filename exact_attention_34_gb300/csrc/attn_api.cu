@@ -126,6 +126,8 @@ Problem make_problem(int B, int Lq, int Lkv, int Hq, int Hkv, int d, float scale
   p.wr = causal ? 0 : kWinInf;
   p.scale = scale;
   p.kv_lens = kl;
+  p.q_seg = nullptr;
+  p.kv_seg = nullptr;
   return p;
 }
 
@@ -289,6 +291,20 @@ attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o
                   stream);
 }
 
+attn_status attn_fwd_segments(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Lq,
+                              int Lkv, int Hq, int Hkv, int d, float scale, int window_left, int window_right,
+                              const int32_t* q_segment, const int32_t* kv_segment, const int32_t* kv_lens,
+                              attn_dtype dtype, attn_stream_t stream) {
+  attn_status s = check_problem(B, Lq, Lkv, Hq, Hkv, d, scale, 0, dtype);
+  if (s != ATTN_OK) return s;
+  s = need_ptrs({{q_segment, "q_segment"}, {kv_segment, "kv_segment"}});
+  if (s != ATTN_OK) return s;
+  Problem pb = make_window_problem(B, Lq, Lkv, Hq, Hkv, d, scale, window_left, window_right, kv_lens);
+  pb.q_seg = q_segment;
+  pb.kv_seg = kv_segment;
+  return fwd_impl(q, k, v, o, lse, pb, dtype, stream);
+}
+
 attn_status attn_bwd_preprocess(const void* o, const void* dout, float* delta, int B, int Lq, int Hq, int d,
                                 attn_dtype dtype, attn_stream_t stream) {
   attn_status s = check_problem(B, Lq, Lq, Hq, Hq, d, 1.0f, 0, dtype);
@@ -380,6 +396,22 @@ attn_status attn_bwd_window(const void* q, const void* k, const void* v, const v
   return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv,
                   make_window_problem(B, Lq, Lkv, Hq, Hkv, d, scale, window_left, window_right, kv_lens), dtype,
                   deterministic, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_bwd_segments(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                              const void* dout, void* dq, void* dk, void* dv, int B, int Lq, int Lkv, int Hq,
+                              int Hkv, int d, float scale, int window_left, int window_right,
+                              const int32_t* q_segment, const int32_t* kv_segment, const int32_t* kv_lens,
+                              attn_dtype dtype, int deterministic, void* workspace, size_t workspace_bytes,
+                              attn_stream_t stream) {
+  attn_status s = check_problem(B, Lq, Lkv, Hq, Hkv, d, scale, 0, dtype);
+  if (s != ATTN_OK) return s;
+  s = need_ptrs({{q_segment, "q_segment"}, {kv_segment, "kv_segment"}});
+  if (s != ATTN_OK) return s;
+  Problem pb = make_window_problem(B, Lq, Lkv, Hq, Hkv, d, scale, window_left, window_right, kv_lens);
+  pb.q_seg = q_segment;
+  pb.kv_seg = kv_segment;
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, pb, dtype, deterministic, workspace, workspace_bytes, stream);
 }
 
 int attn_decode_num_splits(int B, int Lq, int Lkv, int Hq, int Hkv, int d) {

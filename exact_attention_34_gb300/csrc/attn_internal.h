@@ -52,7 +52,23 @@ struct Problem {
   int wl, wr;              // position mask (see key_span)
   float scale;             // softmax scale (> 0)
   const int32_t* kv_lens;  // [B] or nullptr
+  const int32_t* q_seg;    // [B, Lq] segment ids or nullptr (then kv_seg is nullptr too)
+  const int32_t* kv_seg;   // [B, Lkv]
 };
+
+// Segment ids of 4 consecutive positions col.. of one sequence (ids past n,
+// the sequence's valid length, are never read and come back as 0: those
+// positions are masked by their span).  vec: the sequence's ids start
+// 16-byte aligned, so a full group is one vector load.
+__device__ __forceinline__ int4 load_ids4(const int32_t* __restrict__ ids, int col, int n, bool vec) {
+  if (vec && col + 3 < n) return __ldg(reinterpret_cast<const int4*>(ids + col));
+  int4 r;
+  r.x = col < n ? __ldg(ids + col) : 0;
+  r.y = col + 1 < n ? __ldg(ids + col + 1) : 0;
+  r.z = col + 2 < n ? __ldg(ids + col + 2) : 0;
+  r.w = col + 3 < n ? __ldg(ids + col + 3) : 0;
+  return r;
+}
 
 // ---- forward ---------------------------------------------------------------
 struct FwdArgs {

@@ -61,7 +61,7 @@ struct DkdvAtomicCfg {
   static constexpr int kRegsWork = 144, kRegsCtl = 80;
 };
 
-template <int D, bool kLeftBound, bool kF16>
+template <int D, bool kLeftBound, bool kF16, bool kSeg>
 __global__ void __launch_bounds__(512, 1)
     bwd_dkdv_atomic_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -286,25 +286,35 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t t_lane = tbase + (static_cast<uint32_t>(wq * 32) << 16);
     const bool key_ok = j < kvl;
     const Span qs = key_ok ? query_span(j, p.Lq, kvl, p.wl, p.wr) : Span{0, 0};
+    // segment masks: the key's id, and the queries' ids of this sequence
+    const int my_seg = (kSeg && j < p.Lkv) ? __ldg(p.kv_seg + static_cast<size_t>(b) * p.Lkv + j) : 0;
+    const int32_t* qid = kSeg ? p.q_seg + static_cast<size_t>(b) * p.Lq : nullptr;
+    const bool qid_vec = kSeg && ((static_cast<size_t>(b) * p.Lq) & 3) == 0;
     const float sl2 = p.scale_log2;
     const int c0 = 64 * w;
     uint8_t* ds_row = sDS + w * C::kBox + r * 128;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int s = t % NS;
+      const int q0 = (i_begin + t % steps_per_head) * BM;
+      uint32_t sg0 = 0u, sg1 = 0u;  // segment bits of this warpgroup's 64 queries (before S is ready)
+      if (kSeg) {
+        sg0 = segment_bits32(qid, q0 + c0, p.Lq, qid_vec, my_seg);
+        sg1 = segment_bits32(qid, q0 + c0 + 32, p.Lq, qid_vec, my_seg);
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(s_ready, t & 1, abort_flag, p.status, 79));
       if (!ok) break;
       tc_fence_after();
-      const int q0 = (i_begin + t % steps_per_head) * BM;
       const float* lse2 = sStat + s * 2 * BM;
       const float* dlt = lse2 + BM;
       float pr[64];
       // without a left window bound every row after the first that sees the
       // key sees it too, so only the lower end needs checking
-      if (__all_sync(0xffffffffu, key_ok && q0 + c0 >= qs.lo && (!kLeftBound || q0 + c0 + 64 <= qs.hi)))
+      if (!kSeg && __all_sync(0xffffffffu, key_ok && q0 + c0 >= qs.lo && (!kLeftBound || q0 + c0 + 64 <= qs.hi)))
         dkdv_probs<false, kLeftBound, kF16>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
       else
-        dkdv_probs<true, kLeftBound, kF16>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
+        dkdv_probs<true, kLeftBound, kF16, kSeg>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr, sg0,
+                                                 sg1);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_ready);
@@ -372,16 +382,17 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, uint16_t* __res
 
 namespace {
 
-template <int D, bool kLeftBound, bool kF16>
+template <int D, bool kLeftBound, bool kF16, bool kSeg>
 cudaError_t launch_single_pass_inst(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                     const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, long n_dq,
                                     cudaStream_t stream) {
   using C = DkdvAtomicCfg<D>;
-  cudaError_t e = ensure_dynamic_smem<bwd_dkdv_atomic_kernel<D, kLeftBound, kF16>>(C::kSmemBytes);
+  cudaError_t e = ensure_dynamic_smem<bwd_dkdv_atomic_kernel<D, kLeftBound, kF16, kSeg>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   {
     KernelTimer kt("bwd_dkdv_atomic", stream);
-    bwd_dkdv_atomic_kernel<D, kLeftBound, kF16><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+    bwd_dkdv_atomic_kernel<D, kLeftBound, kF16, kSeg>
+        <<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -399,11 +410,14 @@ cudaError_t launch_single_pass(const CUtensorMap& tq, const CUtensorMap& tk, con
                                const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, long n_dq, bool f16,
                                cudaStream_t stream) {
   const bool left = kp.wl < kWinInf;
+  if (kp.q_seg != nullptr)  // segment masks run the general (two-sided span) build
+    return f16 ? launch_single_pass_inst<D, true, true, true>(tq, tk, tv, tdo, kp, grid, n_dq, stream)
+               : launch_single_pass_inst<D, true, false, true>(tq, tk, tv, tdo, kp, grid, n_dq, stream);
   if (f16)
-    return left ? launch_single_pass_inst<D, true, true>(tq, tk, tv, tdo, kp, grid, n_dq, stream)
-                : launch_single_pass_inst<D, false, true>(tq, tk, tv, tdo, kp, grid, n_dq, stream);
-  return left ? launch_single_pass_inst<D, true, false>(tq, tk, tv, tdo, kp, grid, n_dq, stream)
-              : launch_single_pass_inst<D, false, false>(tq, tk, tv, tdo, kp, grid, n_dq, stream);
+    return left ? launch_single_pass_inst<D, true, true, false>(tq, tk, tv, tdo, kp, grid, n_dq, stream)
+                : launch_single_pass_inst<D, false, true, false>(tq, tk, tv, tdo, kp, grid, n_dq, stream);
+  return left ? launch_single_pass_inst<D, true, false, false>(tq, tk, tv, tdo, kp, grid, n_dq, stream)
+              : launch_single_pass_inst<D, false, false, false>(tq, tk, tv, tdo, kp, grid, n_dq, stream);
 }
 
 template cudaError_t launch_single_pass<64>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,

@@ -19,6 +19,8 @@ struct BwdKParams {
   const int32_t* kv_lens;
   int Lq, Lkv, Hq, Hkv, G, causal, wl, wr, Lq_pad, n_tiles, n_pairs, pair_group;
   int dh;  // stored head_dim (32 runs as D = 64 with zero-filled columns)
+  const int32_t* q_seg;   // [B, Lq] segment ids (kSeg builds)
+  const int32_t* kv_seg;  // [B, Lkv]
   float scale, scale_log2;
   DeviceStatus* status;
 };
@@ -53,9 +55,10 @@ __device__ __forceinline__ void store_row16(uint32_t taddr, uint16_t* dst, float
 // `pr` (fp32) and written packed over columns [c0, c0 + 32) of S^T.  With
 // MASK, query q_lo + c0 + c keeps its probability only if the key is valid and
 // the query lies in [q_min, q_max) (the rows that see this key).
-template <bool MASK, bool kUpper, bool kF16>
+template <bool MASK, bool kUpper, bool kF16, bool kSeg = false>
 __device__ __forceinline__ void dkdv_probs(uint32_t s_col, int c0, const float* lse2, float sl2, bool key_ok,
-                                           int q_lo, int q_min, int q_max, float (&pr)[64]) {
+                                           int q_lo, int q_min, int q_max, float (&pr)[64],
+                                           uint32_t seg_lo = 0u, uint32_t seg_hi = 0u) {
   uint32_t sa[32], sb[32];
   tmem_ld32_pair(s_col + c0, s_col + c0 + 32, sa, sb);
 #pragma unroll
@@ -68,6 +71,7 @@ __device__ __forceinline__ void dkdv_probs(uint32_t s_col, int c0, const float* 
       const uint32_t raw = c < 32 ? sa[c] : sb[c - 32];
       float pv = ex2_approx(fmaf(__uint_as_float(raw), sl2, -lv[e]));
       if (MASK) pv = (key_ok && q_lo + c0 + c >= q_min && (!kUpper || q_lo + c0 + c < q_max)) ? pv : 0.f;
+      if (kSeg) pv = (((c < 32 ? seg_lo >> c : seg_hi >> (c - 32)) & 1u) != 0u) ? pv : 0.f;
       pr[c] = pv;
     }
   }
@@ -75,6 +79,21 @@ __device__ __forceinline__ void dkdv_probs(uint32_t s_col, int c0, const float* 
 #pragma unroll
   for (int i = 0; i < 32; ++i) pk[i] = pack2<kF16>(pr[2 * i], pr[2 * i + 1]);
   tmem_st32(s_col + c0, pk);
+}
+
+// Bit c (c < 32) of the result: id[col + c] == mine, for the ids of one
+// sequence with n valid positions (positions past n never match).
+__device__ __forceinline__ uint32_t segment_bits32(const int32_t* ids, int col, int n, bool vec, int mine) {
+  uint32_t bits = 0u;
+#pragma unroll 2
+  for (int i = 0; i < 32; i += 4) {
+    const int4 id = load_ids4(ids, col + i, n, vec);
+    bits |= (static_cast<uint32_t>(id.x == mine && col + i < n) | (static_cast<uint32_t>(id.y == mine && col + i + 1 < n) << 1) |
+             (static_cast<uint32_t>(id.z == mine && col + i + 2 < n) << 2) |
+             (static_cast<uint32_t>(id.w == mine && col + i + 3 < n) << 3))
+            << i;
+  }
+  return bits;
 }
 
 // Single-pass backward after the preprocess: the dK/dV kernel with atomic dQ

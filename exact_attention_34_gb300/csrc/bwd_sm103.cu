@@ -126,7 +126,7 @@ __device__ __forceinline__ void dkdv_dscores(uint32_t dp_col, int c0, const floa
   tmem_st32(dp_col + c0, dk);
 }
 
-template <int D, bool kLeftBound, bool kF16>
+template <int D, bool kLeftBound, bool kF16, bool kSeg>
 __global__ void __launch_bounds__(320, 1)
     bwd_dkdv_kernel2(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -324,23 +324,33 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t t_lane = tbase + (static_cast<uint32_t>(wq * 32) << 16);
     const bool key_ok = j < kvl;
     const Span qs = key_ok ? query_span(j, p.Lq, kvl, p.wl, p.wr) : Span{0, 0};
+    // segment masks: the key's id, and the queries' ids of this sequence
+    const int my_seg = (kSeg && j < p.Lkv) ? __ldg(p.kv_seg + static_cast<size_t>(b) * p.Lkv + j) : 0;
+    const int32_t* qid = kSeg ? p.q_seg + static_cast<size_t>(b) * p.Lq : nullptr;
+    const bool qid_vec = kSeg && ((static_cast<size_t>(b) * p.Lq) & 3) == 0;
     const float sl2 = p.scale_log2;
     const int c0 = 64 * w;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
+      const int q0 = (i_begin + t % steps_per_head) * BM;
+      uint32_t sg0 = 0u, sg1 = 0u;  // segment bits of this warpgroup's 64 queries (before S is ready)
+      if (kSeg) {
+        sg0 = segment_bits32(qid, q0 + c0, p.Lq, qid_vec, my_seg);
+        sg1 = segment_bits32(qid, q0 + c0 + 32, p.Lq, qid_vec, my_seg);
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(s_ready, t & 1, abort_flag, p.status, 67));
       if (!ok) break;
       tc_fence_after();
-      const int q0 = (i_begin + t % steps_per_head) * BM;
       const float* lse2 = sLse + (t % NQ) * BM;
       const float* dlt = sDelta + (t % NO) * BM;
       float pr[64];
       // without a left window bound every row after the first that sees the
       // key sees it too, so only the lower end needs checking
-      if (__all_sync(0xffffffffu, key_ok && q0 + c0 >= qs.lo && (!kLeftBound || q0 + c0 + 64 <= qs.hi)))
+      if (!kSeg && __all_sync(0xffffffffu, key_ok && q0 + c0 >= qs.lo && (!kLeftBound || q0 + c0 + 64 <= qs.hi)))
         dkdv_probs<false, kLeftBound, kF16>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
       else
-        dkdv_probs<true, kLeftBound, kF16>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
+        dkdv_probs<true, kLeftBound, kF16, kSeg>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr, sg0,
+                                                 sg1);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_ready);
@@ -397,8 +407,9 @@ struct DqCfg {
 
 // Probabilities of the N key columns [c0, c0 + N) of one step (thread =
 // query row), from S at s_col; kept in registers until dP is ready.
-template <int N, bool MASK, bool kLower = true>
-__device__ __forceinline__ void dq_probs(uint32_t s_col, int c0, float l2, float sl2, int kb, Span ks, float* pr) {
+template <int N, bool MASK, bool kLower = true, bool kSeg = false>
+__device__ __forceinline__ void dq_probs(uint32_t s_col, int c0, float l2, float sl2, int kb, Span ks, float* pr,
+                                         uint32_t seg = 0u) {
   uint32_t sr[N];
   if constexpr (N == 32)
     tmem_ld32(s_col + c0, *reinterpret_cast<uint32_t(*)[32]>(sr));
@@ -408,6 +419,7 @@ __device__ __forceinline__ void dq_probs(uint32_t s_col, int c0, float l2, float
   for (int c = 0; c < N; ++c) {
     float pv = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -l2));
     if (MASK) pv = ((!kLower || kb + c0 + c >= ks.lo) && kb + c0 + c < ks.hi) ? pv : 0.f;
+    if (kSeg) pv = ((seg >> c) & 1u) ? pv : 0.f;
     pr[c] = pv;
   }
 }
@@ -442,7 +454,7 @@ __device__ __forceinline__ void dq_dscores(uint32_t s_col, uint32_t dp_col, int 
 // two 64-key halves so the dQ MMAs of half 0 overlap the second half.  K tiles
 // use a 3-slot ring (a K tile is read by S and later by dQ), V tiles a 2-slot
 // ring.
-template <int D, bool kLeftBound, bool kF16>
+template <int D, bool kLeftBound, bool kF16, bool kSeg>
 __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -625,22 +637,31 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     if (!kLeftBound) ks.lo = 0;
     if (i >= p.Lq) ks.lo = ks.hi = 0;
     const float sl2 = p.scale_log2;
+    // segment masks: the row's id, and the keys' ids of this sequence
+    const int my_seg = (kSeg && i < p.Lq) ? __ldg(p.q_seg + static_cast<size_t>(b) * p.Lq + i) : 0;
+    const int32_t* kid = kSeg ? p.kv_seg + static_cast<size_t>(b) * p.Lkv : nullptr;
+    const bool kid_vec = kSeg && ((static_cast<size_t>(b) * p.Lkv) & 3) == 0;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
+      const int kb = (t0 + t) * BN;
+      uint32_t sg[2] = {0u, 0u};  // segment bits of this thread's two key column groups
+      if (kSeg) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) sg[hh] = segment_bits32(kid, kb + 64 * hh + C::kCols * w, kvl, kid_vec, my_seg);
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(&s_ready[t & 1], (t >> 1) & 1, abort_flag, p.status, 37));
       if (!ok) break;
       tc_fence_after();
-      const int kb = (t0 + t) * BN;
       const uint32_t s_col = t_lane + ((t & 1) ? 384u : 128u);
       const uint32_t dp_col = t_lane + 256;
       float pr[2 * C::kCols];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int c0 = 64 * hh + C::kCols * w;
-        if (__all_sync(0xffffffffu, (!kLeftBound || kb + c0 >= ks.lo) && kb + c0 + C::kCols <= ks.hi))
+        if (!kSeg && __all_sync(0xffffffffu, (!kLeftBound || kb + c0 >= ks.lo) && kb + c0 + C::kCols <= ks.hi))
           dq_probs<C::kCols, false, kLeftBound>(s_col, c0, l2, sl2, kb, ks, pr + hh * C::kCols);
         else
-          dq_probs<C::kCols, true, kLeftBound>(s_col, c0, l2, sl2, kb, ks, pr + hh * C::kCols);
+          dq_probs<C::kCols, true, kLeftBound, kSeg>(s_col, c0, l2, sl2, kb, ks, pr + hh * C::kCols, sg[hh]);
       }
       ok = __all_sync(0xffffffffu, mbar_wait(dp_ready, t & 1, abort_flag, p.status, 39));
       if (!ok) break;
@@ -673,27 +694,49 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   }
 }
 
-template <int D, bool kLeftBound, bool kF16>
+template <int D, bool kLeftBound, bool kF16, bool kSeg>
 cudaError_t launch_dkdv_inst(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, cudaStream_t stream) {
   using C = DkdvCfg2<D>;
-  cudaError_t e = ensure_dynamic_smem<bwd_dkdv_kernel2<D, kLeftBound, kF16>>(C::kSmemBytes);
+  cudaError_t e = ensure_dynamic_smem<bwd_dkdv_kernel2<D, kLeftBound, kF16, kSeg>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   KernelTimer kt("bwd_dkdv", stream);
-  bwd_dkdv_kernel2<D, kLeftBound, kF16><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+  bwd_dkdv_kernel2<D, kLeftBound, kF16, kSeg><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
   return cudaGetLastError();
 }
 
-template <int D, bool kLeftBound, bool kF16>
+template <int D, bool kLeftBound, bool kF16, bool kSeg>
 cudaError_t launch_dq_inst(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, cudaStream_t stream) {
   using C = DqCfg<D>;
-  cudaError_t e = ensure_dynamic_smem<bwd_dq_kernel<D, kLeftBound, kF16>>(C::kSmemBytes);
+  cudaError_t e = ensure_dynamic_smem<bwd_dq_kernel<D, kLeftBound, kF16, kSeg>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   KernelTimer kt("bwd_dq", stream);
-  bwd_dq_kernel<D, kLeftBound, kF16><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+  bwd_dq_kernel<D, kLeftBound, kF16, kSeg><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
   return cudaGetLastError();
 }
+
+// The kernel build for a problem: format x (no left bound | two-sided span |
+// two-sided span + segment ids).
+template <template <int, bool, bool, bool> class L, int D, typename... A>
+cudaError_t dispatch_build(const Problem& pb, A&&... args) {
+  const bool left = pb.wl < kWinInf;
+  if (pb.q_seg != nullptr)
+    return pb.f16 ? L<D, true, true, true>::run(args...) : L<D, true, false, true>::run(args...);
+  if (pb.f16) return left ? L<D, true, true, false>::run(args...) : L<D, false, true, false>::run(args...);
+  return left ? L<D, true, false, false>::run(args...) : L<D, false, false, false>::run(args...);
+}
+
+template <int D, bool kL, bool kF, bool kS>
+struct DkdvLaunch {
+  template <typename... A>
+  static cudaError_t run(A&&... args) { return launch_dkdv_inst<D, kL, kF, kS>(args...); }
+};
+template <int D, bool kL, bool kF, bool kS>
+struct DqLaunch {
+  template <typename... A>
+  static cudaError_t run(A&&... args) { return launch_dq_inst<D, kL, kF, kS>(args...); }
+};
 
 template <int D>
 cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream) {
@@ -733,6 +776,8 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
   kp.wr = pb.wr;
   kp.Lq_pad = a.Lq_pad;
   kp.dh = pb.d;
+  kp.q_seg = pb.q_seg;
+  kp.kv_seg = pb.kv_seg;
   kp.scale = pb.scale;
   kp.scale_log2 = pb.scale * kLog2e;
   kp.status = st;
@@ -752,11 +797,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
     if (!a.deterministic)
       return launch_single_pass<D>(tq128, tk, tv, tdo128, kp, grid, static_cast<long>(pb.B) * pb.Lq * pb.Hq * pb.d,
                                    pb.f16 != 0, stream);
-    const bool left = pb.wl < kWinInf;
-    e = pb.f16 ? (left ? launch_dkdv_inst<D, true, true>(tq128, tk, tv, tdo128, kp, grid, stream)
-                       : launch_dkdv_inst<D, false, true>(tq128, tk, tv, tdo128, kp, grid, stream))
-               : (left ? launch_dkdv_inst<D, true, false>(tq128, tk, tv, tdo128, kp, grid, stream)
-                       : launch_dkdv_inst<D, false, false>(tq128, tk, tv, tdo128, kp, grid, stream));
+    e = dispatch_build<DkdvLaunch, D>(pb, tq128, tk, tv, tdo128, kp, grid, stream);
     if (e != cudaSuccess) return e;
   }
   // dQ pass: Q/dO and K/V boxes of 128 rows
@@ -771,11 +812,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
     kp.n_pairs = pb.B * pb.Hq;
     kp.pair_group = l2_pair_group(2l * pb.Lkv * D * 2, kp.n_pairs, pb.G);
     dim3 grid(kp.n_pairs * kp.n_tiles);
-    const bool left = pb.wl < kWinInf;
-    return pb.f16 ? (left ? launch_dq_inst<D, true, true>(tq, tk, tv, tdo, kp, grid, stream)
-                          : launch_dq_inst<D, false, true>(tq, tk, tv, tdo, kp, grid, stream))
-                  : (left ? launch_dq_inst<D, true, false>(tq, tk, tv, tdo, kp, grid, stream)
-                          : launch_dq_inst<D, false, false>(tq, tk, tv, tdo, kp, grid, stream));
+    return dispatch_build<DqLaunch, D>(pb, tq, tk, tv, tdo, kp, grid, stream);
   }
 }
 

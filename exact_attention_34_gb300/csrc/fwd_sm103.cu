@@ -54,11 +54,13 @@ struct FwdKParams {
   const int32_t* kv_lens;
   int Lq, Lkv, Hq, Hkv, G, causal, wl, wr, n_qblocks, n_pairs, pair_group;
   int dh;  // stored head_dim (32 runs as D = 64 with zero-filled columns)
+  const int32_t* q_seg;   // [B, Lq] segment ids (kSeg builds)
+  const int32_t* kv_seg;  // [B, Lkv]
   float scale_log2;
   DeviceStatus* status;
 };
 
-template <int D, bool kLeftBound, bool kF16>
+template <int D, bool kLeftBound, bool kF16, bool kSeg>
 __global__ void __launch_bounds__(320, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdKParams p) {
@@ -240,11 +242,33 @@ __global__ void __launch_bounds__(320, 1)
     Span span = key_span(row, p.Lq, kvl, p.wl, p.wr);
     if (!kLeftBound) span.lo = 0;
     if (row >= p.Lq) span.lo = span.hi = 0;
+    // segment masks: a key counts only if its id equals the row's
+    const int my_seg = (kSeg && row < p.Lq) ? __ldg(p.q_seg + static_cast<size_t>(b) * p.Lq + row) : 0;
+    const int32_t* kid = kSeg ? p.kv_seg + static_cast<size_t>(b) * p.Lkv : nullptr;
+    const bool kid_vec = kSeg && ((static_cast<size_t>(b) * p.Lkv) & 3) == 0;
     const int jbase = kLeftBound ? (x == 0 ? jlo_a : jlo_b) : 0;
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY, l_sum = 0.f;
     bool ok = true;
     for (int j = 0; j < n_x; ++j) {
+      const int col0 = (jbase + j) * kBN;
+      // segment masks: bit i says key col0 + i has the row's id (loaded while
+      // the tensor core computes S, so the ids are not live next to S)
+      uint32_t segbits[kBN / 32];
+      if (kSeg) {
+#pragma unroll
+        for (int w4 = 0; w4 < kBN / 32; ++w4) {
+          uint32_t bits = 0u;
+#pragma unroll 2
+          for (int i = 0; i < 32; i += 4) {
+            const int4 id = load_ids4(kid, col0 + 32 * w4 + i, kvl, kid_vec);
+            bits |= (static_cast<uint32_t>(id.x == my_seg) | (static_cast<uint32_t>(id.y == my_seg) << 1) |
+                     (static_cast<uint32_t>(id.z == my_seg) << 2) | (static_cast<uint32_t>(id.w == my_seg) << 3))
+                    << i;
+          }
+          segbits[w4] = bits;
+        }
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], j & 1, abort_flag, p.status, 8));
       if (!ok) break;
       tc_fence_after();
@@ -253,11 +277,15 @@ __global__ void __launch_bounds__(320, 1)
       float s[kBN];
 #pragma unroll
       for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(sraw[i]);
-      const int col0 = (jbase + j) * kBN;
       if ((kLeftBound && col0 < span.lo) || col0 + kBN > span.hi) {
 #pragma unroll
         for (int i = 0; i < kBN; ++i)
           if ((kLeftBound && col0 + i < span.lo) || col0 + i >= span.hi) s[i] = -INFINITY;
+      }
+      if (kSeg) {
+#pragma unroll
+        for (int i = 0; i < kBN; ++i)
+          if (!((segbits[i / 32] >> (i % 32)) & 1u)) s[i] = -INFINITY;
       }
       // row max as a tree (8 independent chains) instead of one 127-long chain
       float mx8[8];
@@ -346,14 +374,14 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D, bool kLeftBound, bool kF16>
+template <int D, bool kLeftBound, bool kF16, bool kSeg = false>
 cudaError_t launch_fwd_inst(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdKParams& kp, dim3 grid, cudaStream_t stream) {
   using C = FwdCfg<D>;
-  cudaError_t e = ensure_dynamic_smem<fwd_tc_kernel<D, kLeftBound, kF16>>(C::kSmemBytes);
+  cudaError_t e = ensure_dynamic_smem<fwd_tc_kernel<D, kLeftBound, kF16, kSeg>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   KernelTimer kt("fwd", stream);
-  fwd_tc_kernel<D, kLeftBound, kF16><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
+  fwd_tc_kernel<D, kLeftBound, kF16, kSeg><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
   return cudaGetLastError();
 }
 
@@ -378,6 +406,8 @@ cudaError_t launch_fwd_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t stream
   kp.wl = pb.wl;
   kp.wr = pb.wr;
   kp.dh = pb.d;
+  kp.q_seg = pb.q_seg;
+  kp.kv_seg = pb.kv_seg;
   kp.n_qblocks = (pb.Lq + 2 * kBM - 1) / (2 * kBM);
   kp.n_pairs = pb.B * pb.Hq;
   kp.pair_group = l2_pair_group(2l * pb.Lkv * D * 2, kp.n_pairs, pb.G);
@@ -385,6 +415,9 @@ cudaError_t launch_fwd_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t stream
   kp.status = st;
   const dim3 grid(kp.n_pairs * kp.n_qblocks);
   const bool left = pb.wl < kWinInf;
+  if (pb.q_seg != nullptr)  // segment masks run the general (two-sided span) build
+    return pb.f16 ? launch_fwd_inst<D, true, true, true>(tq, tk, tv, kp, grid, stream)
+                  : launch_fwd_inst<D, true, false, true>(tq, tk, tv, kp, grid, stream);
   if (pb.f16)
     return left ? launch_fwd_inst<D, true, true>(tq, tk, tv, kp, grid, stream)
                 : launch_fwd_inst<D, false, true>(tq, tk, tv, kp, grid, stream);

@@ -123,6 +123,8 @@ struct F32FwdParams {
   float* lse_part;   // partial mode: [B, Hq, S, Lq]
   const int32_t* kv_lens;
   int B, Lq, Lkv, Hq, Hkv, G, causal, wl, wr, num_splits, chunk;
+  const int32_t* q_seg;   // [B, Lq] segment ids or nullptr
+  const int32_t* kv_seg;  // [B, Lkv]
   float scale_log2;
 };
 
@@ -150,7 +152,8 @@ __global__ void __launch_bounds__(256) f32_fwd_kernel(const F32FwdParams p) {
 
   load_tile<D>(Qs, p.q, b, q0, h, p.Lq, p.Hq);
   float m[4], l[4], acc[4][D / 16];
-  int klo[4], khi[4];
+  int klo[4], khi[4], qseg[4];
+  const bool seg = p.q_seg != nullptr;
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
     m[a] = -INFINITY;
@@ -159,6 +162,7 @@ __global__ void __launch_bounds__(256) f32_fwd_kernel(const F32FwdParams p) {
     const Span ks = key_span(i, p.Lq, kvl, p.wl, p.wr);
     klo[a] = i < p.Lq ? ks.lo : 0;
     khi[a] = i < p.Lq ? min(k_hi, ks.hi) : 0;
+    qseg[a] = (seg && i < p.Lq) ? p.q_seg[static_cast<size_t>(b) * p.Lq + i] : 0;
 #pragma unroll
     for (int e = 0; e < D / 16; ++e) acc[a][e] = 0.f;
   }
@@ -169,13 +173,20 @@ __global__ void __launch_bounds__(256) f32_fwd_kernel(const F32FwdParams p) {
     __syncthreads();
     float s[4][4];
     tile_dot<D>(Qs, Ks, ty, tx, s);
+    int kseg[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int j = j0 + tx + 16 * c;
+      kseg[c] = (seg && j < kvl) ? p.kv_seg[static_cast<size_t>(b) * p.Lkv + j] : 0;
+    }
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int j = j0 + tx + 16 * c;
-        s[a][c] = (j >= klo[a] && j < khi[a]) ? s[a][c] * p.scale_log2 : -INFINITY;
+        const bool ok = j >= klo[a] && j < khi[a] && (!seg || kseg[c] == qseg[a]);
+        s[a][c] = ok ? s[a][c] * p.scale_log2 : -INFINITY;
         mx = fmaxf(mx, s[a][c]);
       }
       mx = row_reduce_max(mx);
@@ -231,6 +242,8 @@ struct F32BwdParams {
   float* dq_acc;  // atomic variant: [B, Lq, Hq, D] (unscaled)
   const int32_t* kv_lens;
   int B, Lq, Lkv, Hq, Hkv, G, causal, wl, wr;
+  const int32_t* q_seg;   // [B, Lq] segment ids or nullptr
+  const int32_t* kv_seg;  // [B, Lkv]
   float scale, scale_log2;
 };
 
@@ -239,7 +252,8 @@ struct F32BwdParams {
 template <int D>
 __device__ __forceinline__ void kt_probs(const float* Ks, const float* Vs, const float* Qs, const float* dOs,
                                          const float* lse2_s, const float* delta_s, const int* klo_s,
-                                         const int* khi_s, int j0, int ty,
+                                         const int* khi_s, const int* qseg_s, const int (&kseg)[4], bool seg,
+                                         int j0, int ty,
                                          int tx, float scale_log2, float (&P)[4][4], float (&dS)[4][4]) {
   float s[4][4], dp[4][4];
   tile_dot<D>(Ks, Qs, ty, tx, s);
@@ -253,7 +267,8 @@ __device__ __forceinline__ void kt_probs(const float* Ks, const float* Vs, const
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
       const int j = j0 + 4 * ty + a;
-      const float pv = (j >= klo && j < khi) ? ex2_approx(fmaf(s[a][c], scale_log2, -l2)) : 0.f;
+      const bool ok = j >= klo && j < khi && (!seg || qseg_s[qi] == kseg[a]);
+      const float pv = ok ? ex2_approx(fmaf(s[a][c], scale_log2, -l2)) : 0.f;
       P[a][c] = pv;
       dS[a][c] = pv * (dp[a][c] - dl);
     }
@@ -276,9 +291,17 @@ __global__ void __launch_bounds__(256) f32_bwd_dkdv_kernel(const F32BwdParams p)
   float* delta_s = lse2_s + kT;
   int* klo_s = reinterpret_cast<int*>(delta_s + kT);
   int* khi_s = klo_s + kT;
+  int* qseg_s = khi_s + kT;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int j0 = blockIdx.x * kT, hk = blockIdx.y, b = blockIdx.z;
   const int kvl = seq_len_of(p.kv_lens, b, p.Lkv);
+  const bool seg = p.q_seg != nullptr;
+  int kseg[4];  // segment ids of this thread's 4 keys
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int j = j0 + 4 * ty + a;
+    kseg[a] = (seg && j < p.Lkv) ? p.kv_seg[static_cast<size_t>(b) * p.Lkv + j] : 0;
+  }
   float dk[4][D / 16], dv[4][D / 16];
 #pragma unroll
   for (int a = 0; a < 4; ++a)
@@ -306,10 +329,12 @@ __global__ void __launch_bounds__(256) f32_bwd_dkdv_kernel(const F32BwdParams p)
           const bool any = in && ls != -INFINITY;
           klo_s[threadIdx.x] = any ? ks.lo : 0;
           khi_s[threadIdx.x] = any ? ks.hi : 0;
+          qseg_s[threadIdx.x] = (seg && in) ? p.q_seg[static_cast<size_t>(b) * p.Lq + i] : 0;
         }
         __syncthreads();
         float P[4][4], dS[4][4];
-        kt_probs<D>(Ks, Vs, Qs, dOs, lse2_s, delta_s, klo_s, khi_s, j0, ty, tx, p.scale_log2, P, dS);
+        kt_probs<D>(Ks, Vs, Qs, dOs, lse2_s, delta_s, klo_s, khi_s, qseg_s, kseg, seg, j0, ty, tx, p.scale_log2, P,
+                    dS);
 #pragma unroll
         for (int a = 0; a < 4; ++a)
 #pragma unroll
@@ -369,7 +394,8 @@ __global__ void __launch_bounds__(256) f32_bwd_dq_kernel(const F32BwdParams p) {
   load_tile<D>(Qs, p.q, b, q0, h, p.Lq, p.Hq);
   load_tile<D>(dOs, p.dout, b, q0, h, p.Lq, p.Hq);
   float l2[4], dl[4];
-  int klo[4], khi[4];
+  int klo[4], khi[4], qseg[4];
+  const bool seg = p.q_seg != nullptr;
   float acc[4][D / 16];
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
@@ -382,6 +408,7 @@ __global__ void __launch_bounds__(256) f32_bwd_dq_kernel(const F32BwdParams p) {
     const bool any = in && ls != -INFINITY;
     klo[a] = any ? ks.lo : 0;
     khi[a] = any ? ks.hi : 0;
+    qseg[a] = (seg && in) ? p.q_seg[static_cast<size_t>(b) * p.Lq + i] : 0;
 #pragma unroll
     for (int e = 0; e < D / 16; ++e) acc[a][e] = 0.f;
   }
@@ -396,12 +423,19 @@ __global__ void __launch_bounds__(256) f32_bwd_dq_kernel(const F32BwdParams p) {
     float s[4][4], dp[4][4];
     tile_dot<D>(Qs, Ks, ty, tx, s);
     tile_dot<D>(dOs, Vs, ty, tx, dp);
+    int kseg[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int j = j0 + tx + 16 * c;
+      kseg[c] = (seg && j < kvl) ? p.kv_seg[static_cast<size_t>(b) * p.Lkv + j] : 0;
+    }
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int j = j0 + tx + 16 * c;
-        const float pv = (j >= klo[a] && j < khi[a]) ? ex2_approx(fmaf(s[a][c], p.scale_log2, -l2[a])) : 0.f;
+        const bool ok = j >= klo[a] && j < khi[a] && (!seg || kseg[c] == qseg[a]);
+        const float pv = ok ? ex2_approx(fmaf(s[a][c], p.scale_log2, -l2[a])) : 0.f;
         dSs[(4 * ty + a) * (kT + kPad) + tx + 16 * c] = pv * (dp[a][c] - dl[a]);
       }
     __syncthreads();
@@ -429,7 +463,7 @@ constexpr int fwd_smem() {
 }
 template <int D>
 constexpr int dkdv_smem() {
-  return (4 * kT * (D + kPad) + 2 * kT * (kT + kPad) + 4 * kT) * 4;  // + lse2, delta, span lo, span hi
+  return (4 * kT * (D + kPad) + 2 * kT * (kT + kPad) + 5 * kT) * 4;  // + lse2, delta, span lo/hi, segment ids
 }
 template <int D>
 constexpr int dq_smem() {
@@ -490,6 +524,8 @@ F32FwdParams fwd_params(const Problem& pb, const void* q, const void* k, const v
   p.causal = pb.causal;
   p.wl = pb.wl;
   p.wr = pb.wr;
+  p.q_seg = pb.q_seg;
+  p.kv_seg = pb.kv_seg;
   p.scale_log2 = pb.scale * kLog2e;
   return p;
 }
@@ -557,6 +593,8 @@ cudaError_t launch_bwd_f32(const BwdArgs& a, DeviceStatus* st, cudaStream_t s) {
   p.causal = pb.causal;
   p.wl = pb.wl;
   p.wr = pb.wr;
+  p.q_seg = pb.q_seg;
+  p.kv_seg = pb.kv_seg;
   p.scale = pb.scale;
   p.scale_log2 = pb.scale * kLog2e;
   return pb.d == 32   ? run_bwd<32>(p, !a.deterministic, s)

@@ -143,6 +143,28 @@ attn_status attn_bwd_window(const void* q, const void* k, const void* v, const v
                             attn_stream_t stream);
 
 /*
+ * Segment (document) masks on top of the window masks above ("H100 (Hopper)",
+ * section "Mosaic GPU", lists segments beside KV lengths, causal and local
+ * windows): key j is valid for query row i of batch b only if, in addition,
+ * q_segment[b][i] == kv_segment[b][j].  q_segment is a device int32 [B, Lq],
+ * kv_segment a device int32 [B, Lkv], both 16-byte aligned and required; ids
+ * are arbitrary int32 values and need not be sorted.  Key tiles are skipped by
+ * the position masks only; within them the ids are compared per element.
+ * Rows with no valid key get o = 0, lse = -inf and dq = 0.  Otherwise as
+ * attn_fwd_window / attn_bwd_window.
+ */
+attn_status attn_fwd_segments(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Lq,
+                              int Lkv, int Hq, int Hkv, int d, float scale, int window_left, int window_right,
+                              const int32_t* q_segment, const int32_t* kv_segment, const int32_t* kv_lens,
+                              attn_dtype dtype, attn_stream_t stream);
+attn_status attn_bwd_segments(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                              const void* dout, void* dq, void* dk, void* dv, int B, int Lq, int Lkv, int Hq,
+                              int Hkv, int d, float scale, int window_left, int window_right,
+                              const int32_t* q_segment, const int32_t* kv_segment, const int32_t* kv_lens,
+                              attn_dtype dtype, int deterministic, void* workspace, size_t workspace_bytes,
+                              attn_stream_t stream);
+
+/*
  * Split-KV decode for few queries over a long KV cache ("Attention
  * performance", section "Grouped-query attention and decoding"): the keys are
  * split across programs, the G query heads of a KV head (times the Lq rows)
