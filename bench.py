@@ -454,6 +454,24 @@ def other_rows(args, dev, peaks):
     out["window_fwd_bwd"] = {"ms": round(ms, 4), "tflops": round(3.5 * f_win / ms / 1e9, 1),
                              "window": list(win), "note": "B4 H8 T8192 d128 bf16, keys within 1024 before the row"}
     del q, k, v, do
+    # segment (document) mask on the headline shapes: packed documents of
+    # 1024 tokens each, causal within a document (flops over the valid pairs)
+    p = W.headline()
+    seg = (torch.arange(p.Lq, device=dev, dtype=torch.int32) // 1024).expand(p.B, p.Lq).contiguous()
+    q = torch.randn(p.B, p.Lq, p.Hq, p.d, device=dev, generator=g).to(torch.bfloat16)
+    k, v, do = torch.randn_like(q), torch.randn_like(q), torch.randn_like(q)
+
+    def seg_step():
+        o, lse = ea.forward(q, k, v, causal=True, segments=(seg, seg))
+        ea.backward(q, k, v, o, lse, do, causal=True, segments=(seg, seg))
+
+    ms = timed(seg_step)
+    pairs = p.Lq // 1024 * (1024 * 1025 // 2)
+    f_seg = 4.0 * p.B * p.Hq * p.d * pairs
+    out["segments_fwd_bwd"] = {"ms": round(ms, 4), "tflops": round(3.5 * f_seg / ms / 1e9, 1),
+                               "note": "B4 H8 T8192 d128 bf16, causal within packed 1024-token documents; key tiles "
+                                       "are skipped by the causal mask only (arbitrary ids), the rest masked per element"}
+    del q, k, v, do
     # KVLenMask + GQA + Lq != Lkv fwd+bwd (flops over valid keys)
     p = W.kvlen_gqa()
     q = torch.randn(p.B, p.Lq, p.Hq, p.d, device=dev, generator=g).to(torch.bfloat16)
