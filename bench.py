@@ -398,6 +398,7 @@ def run_gpu(args):
 
 def other_rows(args, dev, peaks):
     """Quick one-shot numbers for the other rows of the path (context, not the headline)."""
+    import numpy as np
     import torch
 
     import exact_attention_34_gb300 as ea
@@ -454,23 +455,43 @@ def other_rows(args, dev, peaks):
     out["window_fwd_bwd"] = {"ms": round(ms, 4), "tflops": round(3.5 * f_win / ms / 1e9, 1),
                              "window": list(win), "note": "B4 H8 T8192 d128 bf16, keys within 1024 before the row"}
     del q, k, v, do
-    # segment (document) mask on the headline shapes: packed documents of
-    # 1024 tokens each, causal within a document (flops over the valid pairs)
+    # segment (document) masks on the headline shapes, causal within each
+    # document (flops over the valid pairs): packed documents of 1024 tokens,
+    # and documents of seeded random lengths 1..2047 (boundaries off the tile
+    # grid).  A step computes the ids' block summary once, then fwd + bwd.
     p = W.headline()
-    seg = (torch.arange(p.Lq, device=dev, dtype=torch.int32) // 1024).expand(p.B, p.Lq).contiguous()
     q = torch.randn(p.B, p.Lq, p.Hq, p.d, device=dev, generator=g).to(torch.bfloat16)
     k, v, do = torch.randn_like(q), torch.randn_like(q), torch.randn_like(q)
+    rng = np.random.default_rng(11)
+    ragged = []
+    for _ in range(p.B):
+        lens, tot = [], 0
+        while tot < p.Lq:
+            n = min(int(rng.integers(1, 2048)), p.Lq - tot)
+            lens.append(n)
+            tot += n
+        ragged.append(lens)
+    layouts = {
+        "segments_fwd_bwd": [[1024] * (p.Lq // 1024)] * p.B,
+        "segments_ragged_fwd_bwd": ragged,
+    }
+    for name, lens in layouts.items():
+        seg = torch.tensor(np.stack([np.repeat(np.arange(len(ls), dtype=np.int32), ls) for ls in lens]),
+                           device=dev)
 
-    def seg_step():
-        o, lse = ea.forward(q, k, v, causal=True, segments=(seg, seg))
-        ea.backward(q, k, v, o, lse, do, causal=True, segments=(seg, seg))
+        def seg_step():
+            segs = (seg, seg, ea.segment_info(seg, seg))
+            o, lse = ea.forward(q, k, v, causal=True, segments=segs)
+            ea.backward(q, k, v, o, lse, do, causal=True, segments=segs)
 
-    ms = timed(seg_step)
-    pairs = p.Lq // 1024 * (1024 * 1025 // 2)
-    f_seg = 4.0 * p.B * p.Hq * p.d * pairs
-    out["segments_fwd_bwd"] = {"ms": round(ms, 4), "tflops": round(3.5 * f_seg / ms / 1e9, 1),
-                               "note": "B4 H8 T8192 d128 bf16, causal within packed 1024-token documents; key tiles "
-                                       "are skipped by the causal mask only (arbitrary ids), the rest masked per element"}
+        ms = timed(seg_step)
+        pairs = sum(n * (n + 1) // 2 for ls in lens for n in ls)  # over all batch elements
+        f_seg = 4.0 * p.Hq * p.d * pairs
+        kind = "packed 1024-token documents" if name == "segments_fwd_bwd" else \
+            f"{sum(len(ls) for ls in lens)} documents of seeded random lengths 1..2047"
+        out[name] = {"ms": round(ms, 4), "tflops": round(3.5 * f_seg / ms / 1e9, 1),
+                     "note": f"B4 H8 T8192 d128 bf16, causal within {kind}; the block summary drops tiles "
+                             "across documents and runs single-document tiles unmasked"}
     del q, k, v, do
     # KVLenMask + GQA + Lq != Lkv fwd+bwd (flops over valid keys)
     p = W.kvlen_gqa()

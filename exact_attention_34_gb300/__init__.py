@@ -75,8 +75,10 @@ def lib() -> ctypes.CDLL:
         "attn_bwd_static_scratch": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P, I, P]),
         "attn_fwd_window": (I, [P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, I, P]),
         "attn_bwd_window": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, I, I, P, S, P]),
-        "attn_fwd_segments": (I, [P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, P, P, I, P]),
-        "attn_bwd_segments": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, P, P, I, I, P, S, P]),
+        "attn_fwd_segments": (I, [P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, P, P, P, I, P]),
+        "attn_bwd_segments": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, P, P, P, I, I, P, S, P]),
+        "attn_segment_info_size": (S, [I, I, I]),
+        "attn_segment_info": (I, [P, P, I, I, I, P, S, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -91,6 +93,7 @@ EXPORTED = (
     "attn_bwd", "attn_decode_num_splits", "attn_decode_splitkv", "attn_decode_combine",
     "attn_decode_workspace_size", "attn_device_status", "attn_timing_enable", "attn_timing_query",
     "attn_bwd_static_scratch", "attn_fwd_window", "attn_bwd_window", "attn_fwd_segments", "attn_bwd_segments",
+    "attn_segment_info_size", "attn_segment_info",
 )
 
 
@@ -152,13 +155,35 @@ def attn_fwd_window(q, k, v, o, lse, window, scale=None, kv_lens=None, stream=No
            "attn_fwd_window")
 
 
+def attn_segment_info_size(B, Lq, Lkv) -> int:
+    return int(lib().attn_segment_info_size(B, Lq, Lkv))
+
+
+def attn_segment_info(q_segment, kv_segment, info, stream=None):
+    B, Lq = q_segment.shape
+    Lkv = kv_segment.shape[1]
+    _check(lib().attn_segment_info(_ptr(q_segment), _ptr(kv_segment), B, Lq, Lkv, _ptr(info),
+                                   info.numel() * info.element_size(), _stream(stream)),
+           "attn_segment_info")
+
+
+def segment_info(q_segment, kv_segment, stream=None):
+    """Block summary of the segment ids (a uint8 device tensor) for the
+    segment entry points; recompute it whenever the ids change."""
+    B, Lq = q_segment.shape
+    info = torch.empty(attn_segment_info_size(B, Lq, kv_segment.shape[1]), device=q_segment.device,
+                       dtype=torch.uint8)
+    attn_segment_info(q_segment, kv_segment, info, stream)
+    return info
+
+
 def attn_fwd_segments(q, k, v, o, lse, q_segment, kv_segment, window=(-1, -1), scale=None, kv_lens=None,
-                      stream=None):
+                      stream=None, segment_info=None):
     B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
     wl, wr = _window(window)
     _check(lib().attn_fwd_segments(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Lq, Lkv, Hq, Hkv, d,
-                                   _scale(scale, d), wl, wr, _ptr(q_segment), _ptr(kv_segment), _ptr(kv_lens),
-                                   _dtype(q), _stream(stream)),
+                                   _scale(scale, d), wl, wr, _ptr(q_segment), _ptr(kv_segment), _ptr(segment_info),
+                                   _ptr(kv_lens), _dtype(q), _stream(stream)),
            "attn_fwd_segments")
 
 
@@ -194,13 +219,14 @@ def attn_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, workspace, window, scale=
 
 
 def attn_bwd_segments(q, k, v, o, lse, dout, dq, dk, dv, workspace, q_segment, kv_segment, window=(-1, -1),
-                      scale=None, kv_lens=None, deterministic=True, stream=None):
+                      scale=None, kv_lens=None, deterministic=True, stream=None, segment_info=None):
     B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
     wl, wr = _window(window)
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(lib().attn_bwd_segments(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
                                    _ptr(dv), B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d), wl, wr, _ptr(q_segment),
-                                   _ptr(kv_segment), _ptr(kv_lens), _dtype(q), int(bool(deterministic)),
+                                   _ptr(kv_segment), _ptr(segment_info), _ptr(kv_lens), _dtype(q),
+                                   int(bool(deterministic)),
                                    _ptr(workspace), ws_bytes, _stream(stream)),
            "attn_bwd_segments")
 
@@ -267,16 +293,24 @@ def _mask_window(causal, window):
     return window if window is not None else ((-1, 0) if causal else (-1, -1))
 
 
+def _segment_info_of(segments, stream):
+    if len(segments) > 2:
+        return segments[2]
+    return segment_info(segments[0], segments[1], stream)
+
+
 def forward(q, k, v, scale=None, causal=False, kv_lens=None, stream=None, window=None, segments=None):
     """(o, lse) for q [B,Lq,Hq,d], k/v [B,Lkv,Hkv,d] on the GPU.  window =
     (left, right) selects the local-window mask (causal must then be False);
-    segments = (q_segment [B,Lq], kv_segment [B,Lkv]) int32 adds a segment mask."""
+    segments = (q_segment [B,Lq], kv_segment [B,Lkv]) int32 adds a segment mask;
+    a third element, the segment_info() of those ids, saves recomputing it
+    (None there: no tile skipping, ids compared on every tile)."""
     B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
     o = torch.empty_like(q)
     lse = torch.empty(B, Hq, Lq, device=q.device, dtype=torch.float32)
     if segments is not None:
         attn_fwd_segments(q, k, v, o, lse, segments[0], segments[1], _mask_window(causal, window), scale, kv_lens,
-                          stream)
+                          stream, _segment_info_of(segments, stream))
     elif window is not None:
         if causal:
             raise ValueError("pass either causal or window (causal is window (-1, 0))")
@@ -295,7 +329,8 @@ def backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_lens=None, dete
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if segments is not None:
         attn_bwd_segments(q, k, v, o, lse, dout, dq, dk, dv, ws, segments[0], segments[1],
-                          _mask_window(causal, window), scale, kv_lens, deterministic, stream)
+                          _mask_window(causal, window), scale, kv_lens, deterministic, stream,
+                          _segment_info_of(segments, stream))
     elif window is not None:
         if causal:
             raise ValueError("pass either causal or window (causal is window (-1, 0))")

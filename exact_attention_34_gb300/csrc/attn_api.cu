@@ -128,7 +128,29 @@ Problem make_problem(int B, int Lq, int Lkv, int Hq, int Hkv, int d, float scale
   p.kv_lens = kl;
   p.q_seg = nullptr;
   p.kv_seg = nullptr;
+  p.seg_qblk = nullptr;
+  p.seg_kblk = nullptr;
   return p;
+}
+
+size_t seg_info_bytes(int B, int Lq, int Lkv) {
+  const size_t nq = (static_cast<size_t>(Lq) + kSegBlock - 1) / kSegBlock;
+  const size_t nk = (static_cast<size_t>(Lkv) + kSegBlock - 1) / kSegBlock;
+  return static_cast<size_t>(B) * (nq + nk) * sizeof(int4);
+}
+
+// Segment ids (required) and their block summary (optional) on a problem.
+attn_status set_segments(Problem& pb, const int32_t* q_segment, const int32_t* kv_segment, const void* info) {
+  attn_status s = need_ptrs({{q_segment, "q_segment"}, {kv_segment, "kv_segment"}});
+  if (s != ATTN_OK) return s;
+  pb.q_seg = q_segment;
+  pb.kv_seg = kv_segment;
+  if (info != nullptr) {
+    if (!aligned16(info)) return fail(ATTN_ERR_INVALID_ARG, "segment_info is not 16-byte aligned");
+    pb.seg_qblk = static_cast<const int4*>(info);
+    pb.seg_kblk = pb.seg_qblk + static_cast<size_t>(pb.B) * ((pb.Lq + kSegBlock - 1) / kSegBlock);
+  }
+  return ATTN_OK;
 }
 
 // A local window: a negative bound, or one at least as long as the keys (left)
@@ -293,16 +315,33 @@ attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o
 
 attn_status attn_fwd_segments(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Lq,
                               int Lkv, int Hq, int Hkv, int d, float scale, int window_left, int window_right,
-                              const int32_t* q_segment, const int32_t* kv_segment, const int32_t* kv_lens,
-                              attn_dtype dtype, attn_stream_t stream) {
+                              const int32_t* q_segment, const int32_t* kv_segment, const void* segment_info,
+                              const int32_t* kv_lens, attn_dtype dtype, attn_stream_t stream) {
   attn_status s = check_problem(B, Lq, Lkv, Hq, Hkv, d, scale, 0, dtype);
   if (s != ATTN_OK) return s;
-  s = need_ptrs({{q_segment, "q_segment"}, {kv_segment, "kv_segment"}});
-  if (s != ATTN_OK) return s;
   Problem pb = make_window_problem(B, Lq, Lkv, Hq, Hkv, d, scale, window_left, window_right, kv_lens);
-  pb.q_seg = q_segment;
-  pb.kv_seg = kv_segment;
+  s = set_segments(pb, q_segment, kv_segment, segment_info);
+  if (s != ATTN_OK) return s;
   return fwd_impl(q, k, v, o, lse, pb, dtype, stream);
+}
+
+size_t attn_segment_info_size(int B, int Lq, int Lkv) {
+  if (B <= 0 || Lq <= 0 || Lkv <= 0) return 0;
+  return seg_info_bytes(B, Lq, Lkv);
+}
+
+attn_status attn_segment_info(const int32_t* q_segment, const int32_t* kv_segment, int B, int Lq, int Lkv,
+                              void* info, size_t info_bytes, attn_stream_t stream) {
+  if (B <= 0 || Lq <= 0 || Lkv <= 0)
+    return fail(ATTN_ERR_INVALID_ARG, "sizes must be positive (B=%d Lq=%d Lkv=%d)", B, Lq, Lkv);
+  if (Lq > (1 << 30) || Lkv > (1 << 30)) return fail(ATTN_ERR_INVALID_ARG, "sequence too long");
+  attn_status s = need_ptrs({{q_segment, "q_segment"}, {kv_segment, "kv_segment"}, {info, "segment_info"}});
+  if (s != ATTN_OK) return s;
+  const size_t need = seg_info_bytes(B, Lq, Lkv);
+  if (info_bytes < need) return fail(ATTN_ERR_WORKSPACE, "segment_info of %zu bytes needed, %zu given", need, info_bytes);
+  cudaError_t e = launch_segment_info(q_segment, kv_segment, B, Lq, Lkv, static_cast<int4*>(info),
+                                      reinterpret_cast<cudaStream_t>(stream));
+  return from_cuda(e, "attn_segment_info launch");
 }
 
 attn_status attn_bwd_preprocess(const void* o, const void* dout, float* delta, int B, int Lq, int Hq, int d,
@@ -401,16 +440,14 @@ attn_status attn_bwd_window(const void* q, const void* k, const void* v, const v
 attn_status attn_bwd_segments(const void* q, const void* k, const void* v, const void* o, const float* lse,
                               const void* dout, void* dq, void* dk, void* dv, int B, int Lq, int Lkv, int Hq,
                               int Hkv, int d, float scale, int window_left, int window_right,
-                              const int32_t* q_segment, const int32_t* kv_segment, const int32_t* kv_lens,
-                              attn_dtype dtype, int deterministic, void* workspace, size_t workspace_bytes,
-                              attn_stream_t stream) {
+                              const int32_t* q_segment, const int32_t* kv_segment, const void* segment_info,
+                              const int32_t* kv_lens, attn_dtype dtype, int deterministic, void* workspace,
+                              size_t workspace_bytes, attn_stream_t stream) {
   attn_status s = check_problem(B, Lq, Lkv, Hq, Hkv, d, scale, 0, dtype);
   if (s != ATTN_OK) return s;
-  s = need_ptrs({{q_segment, "q_segment"}, {kv_segment, "kv_segment"}});
-  if (s != ATTN_OK) return s;
   Problem pb = make_window_problem(B, Lq, Lkv, Hq, Hkv, d, scale, window_left, window_right, kv_lens);
-  pb.q_seg = q_segment;
-  pb.kv_seg = kv_segment;
+  s = set_segments(pb, q_segment, kv_segment, segment_info);
+  if (s != ATTN_OK) return s;
   return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, pb, dtype, deterministic, workspace, workspace_bytes, stream);
 }
 

@@ -54,7 +54,27 @@ struct Problem {
   const int32_t* kv_lens;  // [B] or nullptr
   const int32_t* q_seg;    // [B, Lq] segment ids or nullptr (then kv_seg is nullptr too)
   const int32_t* kv_seg;   // [B, Lkv]
+  const int4* seg_qblk;    // [B, ceil(Lq/128)] SegBlock records or nullptr (no tile skipping)
+  const int4* seg_kblk;    // [B, ceil(Lkv/128)]
 };
+
+// Segment summary of one 128-position block of a sequence, as an int4:
+//   x, y  the smallest and largest segment id in the block;
+//   z, w  the positions [z, w) of the other side (keys for a query block,
+//         queries for a key block) that may share an id with the block: the
+//         span from the first to the last other-side block whose id range
+//         meets [x, y] (empty when z == w).
+// Every pair (query, key) with equal ids lies inside both blocks' spans, so a
+// kernel may drop the tiles outside them; a query block and a key block that
+// both hold the single id u (x == y == u) match on every pair, so the id
+// compare can be skipped for that tile.
+constexpr int kSegBlock = 128;
+__device__ __forceinline__ int4 seg_block(const int4* tab, int b, int nblk, int blk) {
+  return __ldg(tab + static_cast<size_t>(b) * nblk + blk);
+}
+__device__ __forceinline__ bool seg_same_single_id(int4 a, int4 c) {
+  return a.x == a.y && c.x == c.y && a.x == c.x;
+}
 
 // Segment ids of 4 consecutive positions col.. of one sequence (ids past n,
 // the sequence's valid length, are never read and come back as 0: those
@@ -116,6 +136,12 @@ struct PreprocessArgs {
 cudaError_t launch_bwd_preprocess(const PreprocessArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_16(const BwdArgs& a, DeviceStatus* st, cudaStream_t s);
 cudaError_t launch_bwd_f32(const BwdArgs& a, DeviceStatus* st, cudaStream_t s);
+
+// ---- segment summary ----------------------------------------------------------
+// Writes the SegBlock records of q_seg ([B, Lq]) and kv_seg ([B, Lkv]) into
+// info: B * ceil(Lq/128) query records, then B * ceil(Lkv/128) key records.
+cudaError_t launch_segment_info(const int32_t* q_seg, const int32_t* kv_seg, int B, int Lq, int Lkv, int4* info,
+                                cudaStream_t s);
 
 // ---- split-KV decode ---------------------------------------------------------
 struct DecodeArgs {

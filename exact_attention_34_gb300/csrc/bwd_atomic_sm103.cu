@@ -103,8 +103,13 @@ __global__ void __launch_bounds__(512, 1)
   // key j0 to the last row that sees the tile's last valid key
   int i_begin = 0, steps_per_head = 0;
   if (j0 < kvl) {
-    const int q_lo = query_span(j0, p.Lq, kvl, p.wl, p.wr).lo;
-    const int q_hi = query_span(min(j0 + C::kBN, kvl) - 1, p.Lq, kvl, p.wl, p.wr).hi;
+    int q_lo = query_span(j0, p.Lq, kvl, p.wl, p.wr).lo;
+    int q_hi = query_span(min(j0 + C::kBN, kvl) - 1, p.Lq, kvl, p.wl, p.wr).hi;
+    if (kSeg && p.seg_kblk != nullptr) {  // queries whose blocks may share an id with this key block
+      const int4 r = seg_block(p.seg_kblk, b, p.nkb, j0 / kSegBlock);
+      q_lo = max(q_lo, r.z);
+      q_hi = min(q_hi, r.w);
+    }
     if (q_hi > q_lo) {
       i_begin = q_lo / BM;
       steps_per_head = (q_hi + BM - 1) / BM - i_begin;
@@ -290,6 +295,9 @@ __global__ void __launch_bounds__(512, 1)
     const int my_seg = (kSeg && j < p.Lkv) ? __ldg(p.kv_seg + static_cast<size_t>(b) * p.Lkv + j) : 0;
     const int32_t* qid = kSeg ? p.q_seg + static_cast<size_t>(b) * p.Lq : nullptr;
     const bool qid_vec = kSeg && ((static_cast<size_t>(b) * p.Lq) & 3) == 0;
+    // this key block's summary; (0, -1) never counts as a single id
+    const int4 krec = (kSeg && p.seg_kblk != nullptr) ? seg_block(p.seg_kblk, b, p.nkb, j0 / kSegBlock)
+                                                      : make_int4(0, -1, 0, 0);
     const float sl2 = p.scale_log2;
     const int c0 = 64 * w;
     uint8_t* ds_row = sDS + w * C::kBox + r * 128;
@@ -297,8 +305,11 @@ __global__ void __launch_bounds__(512, 1)
     for (int t = 0; t < T; ++t) {
       const int s = t % NS;
       const int q0 = (i_begin + t % steps_per_head) * BM;
-      uint32_t sg0 = 0u, sg1 = 0u;  // segment bits of this warpgroup's 64 queries (before S is ready)
-      if (kSeg) {
+      uint32_t sg0 = ~0u, sg1 = ~0u;  // segment bits of this warpgroup's 64 queries (before S is ready)
+      // query and key block hold one and the same id: every pair matches
+      const bool seg_all =
+          kSeg && p.seg_qblk != nullptr && seg_same_single_id(seg_block(p.seg_qblk, b, p.nqb, q0 / kSegBlock), krec);
+      if (kSeg && !seg_all) {
         sg0 = segment_bits32(qid, q0 + c0, p.Lq, qid_vec, my_seg);
         sg1 = segment_bits32(qid, q0 + c0 + 32, p.Lq, qid_vec, my_seg);
       }
@@ -310,7 +321,8 @@ __global__ void __launch_bounds__(512, 1)
       float pr[64];
       // without a left window bound every row after the first that sees the
       // key sees it too, so only the lower end needs checking
-      if (!kSeg && __all_sync(0xffffffffu, key_ok && q0 + c0 >= qs.lo && (!kLeftBound || q0 + c0 + 64 <= qs.hi)))
+      if ((!kSeg || seg_all) &&
+          __all_sync(0xffffffffu, key_ok && q0 + c0 >= qs.lo && (!kLeftBound || q0 + c0 + 64 <= qs.hi)))
         dkdv_probs<false, kLeftBound, kF16>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
       else
         dkdv_probs<true, kLeftBound, kF16, kSeg>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr, sg0,

@@ -21,6 +21,9 @@ struct BwdKParams {
   int dh;  // stored head_dim (32 runs as D = 64 with zero-filled columns)
   const int32_t* q_seg;   // [B, Lq] segment ids (kSeg builds)
   const int32_t* kv_seg;  // [B, Lkv]
+  const int4* seg_qblk;   // segment block summary (kSeg builds; nullptr: none)
+  const int4* seg_kblk;
+  int nqb, nkb;           // 128-position blocks per sequence: ceil(Lq/128), ceil(Lkv/128)
   float scale, scale_log2;
   DeviceStatus* status;
 };

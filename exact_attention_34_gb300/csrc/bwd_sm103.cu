@@ -171,8 +171,13 @@ __global__ void __launch_bounds__(320, 1)
   // key j0 to the last row that sees the tile's last valid key
   int i_begin = 0, steps_per_head = 0;
   if (j0 < kvl) {
-    const int q_lo = query_span(j0, p.Lq, kvl, p.wl, p.wr).lo;
-    const int q_hi = query_span(min(j0 + C::kBN, kvl) - 1, p.Lq, kvl, p.wl, p.wr).hi;
+    int q_lo = query_span(j0, p.Lq, kvl, p.wl, p.wr).lo;
+    int q_hi = query_span(min(j0 + C::kBN, kvl) - 1, p.Lq, kvl, p.wl, p.wr).hi;
+    if (kSeg && p.seg_kblk != nullptr) {  // queries whose blocks may share an id with this key block
+      const int4 r = seg_block(p.seg_kblk, b, p.nkb, j0 / kSegBlock);
+      q_lo = max(q_lo, r.z);
+      q_hi = min(q_hi, r.w);
+    }
     if (q_hi > q_lo) {
       i_begin = q_lo / BM;
       steps_per_head = (q_hi + BM - 1) / BM - i_begin;
@@ -328,13 +333,19 @@ __global__ void __launch_bounds__(320, 1)
     const int my_seg = (kSeg && j < p.Lkv) ? __ldg(p.kv_seg + static_cast<size_t>(b) * p.Lkv + j) : 0;
     const int32_t* qid = kSeg ? p.q_seg + static_cast<size_t>(b) * p.Lq : nullptr;
     const bool qid_vec = kSeg && ((static_cast<size_t>(b) * p.Lq) & 3) == 0;
+    // this key block's summary; (0, -1) never counts as a single id
+    const int4 krec = (kSeg && p.seg_kblk != nullptr) ? seg_block(p.seg_kblk, b, p.nkb, j0 / kSegBlock)
+                                                      : make_int4(0, -1, 0, 0);
     const float sl2 = p.scale_log2;
     const int c0 = 64 * w;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int q0 = (i_begin + t % steps_per_head) * BM;
-      uint32_t sg0 = 0u, sg1 = 0u;  // segment bits of this warpgroup's 64 queries (before S is ready)
-      if (kSeg) {
+      uint32_t sg0 = ~0u, sg1 = ~0u;  // segment bits of this warpgroup's 64 queries (before S is ready)
+      // query and key block hold one and the same id: every pair matches
+      const bool seg_all =
+          kSeg && p.seg_qblk != nullptr && seg_same_single_id(seg_block(p.seg_qblk, b, p.nqb, q0 / kSegBlock), krec);
+      if (kSeg && !seg_all) {
         sg0 = segment_bits32(qid, q0 + c0, p.Lq, qid_vec, my_seg);
         sg1 = segment_bits32(qid, q0 + c0 + 32, p.Lq, qid_vec, my_seg);
       }
@@ -346,7 +357,8 @@ __global__ void __launch_bounds__(320, 1)
       float pr[64];
       // without a left window bound every row after the first that sees the
       // key sees it too, so only the lower end needs checking
-      if (!kSeg && __all_sync(0xffffffffu, key_ok && q0 + c0 >= qs.lo && (!kLeftBound || q0 + c0 + 64 <= qs.hi)))
+      if ((!kSeg || seg_all) &&
+          __all_sync(0xffffffffu, key_ok && q0 + c0 >= qs.lo && (!kLeftBound || q0 + c0 + 64 <= qs.hi)))
         dkdv_probs<false, kLeftBound, kF16>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr);
       else
         dkdv_probs<true, kLeftBound, kF16, kSeg>(t_lane + kColS, c0, lse2, sl2, key_ok, q0, qs.lo, qs.hi, pr, sg0,
@@ -491,8 +503,15 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   // key tiles [t0, t0 + T): from the first key of row q0 to the last key of
   // the tile's last row (both ends grow with the row index)
   const int last = min(q0 + C::kBM - 1, p.Lq - 1);
-  const int k_lo = key_span(q0, p.Lq, kvl, p.wl, p.wr).lo;
-  const int k_hi = key_span(last, p.Lq, kvl, p.wl, p.wr).hi;
+  int k_lo = key_span(q0, p.Lq, kvl, p.wl, p.wr).lo;
+  int k_hi = key_span(last, p.Lq, kvl, p.wl, p.wr).hi;
+  // segment ids: this query block's summary; keys outside its span never match
+  const int4 qrec = (kSeg && p.seg_qblk != nullptr) ? seg_block(p.seg_qblk, b, p.nqb, q0 / kSegBlock)
+                                                    : make_int4(0, -1, 0, 0);
+  if (kSeg && p.seg_qblk != nullptr) {
+    k_lo = max(k_lo, qrec.z);
+    k_hi = min(k_hi, qrec.w);
+  }
   const int t0 = kLeftBound ? k_lo / BN : 0;
   const int T = k_hi > k_lo ? (k_hi + BN - 1) / BN - t0 : 0;
 
@@ -644,8 +663,11 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int kb = (t0 + t) * BN;
-      uint32_t sg[2] = {0u, 0u};  // segment bits of this thread's two key column groups
-      if (kSeg) {
+      uint32_t sg[2] = {~0u, ~0u};  // segment bits of this thread's two key column groups
+      // query and key block hold one and the same id: every pair matches
+      const bool seg_all =
+          kSeg && p.seg_kblk != nullptr && seg_same_single_id(qrec, seg_block(p.seg_kblk, b, p.nkb, t0 + t));
+      if (kSeg && !seg_all) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) sg[hh] = segment_bits32(kid, kb + 64 * hh + C::kCols * w, kvl, kid_vec, my_seg);
       }
@@ -658,7 +680,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int c0 = 64 * hh + C::kCols * w;
-        if (!kSeg && __all_sync(0xffffffffu, (!kLeftBound || kb + c0 >= ks.lo) && kb + c0 + C::kCols <= ks.hi))
+        if ((!kSeg || seg_all) &&
+            __all_sync(0xffffffffu, (!kLeftBound || kb + c0 >= ks.lo) && kb + c0 + C::kCols <= ks.hi))
           dq_probs<C::kCols, false, kLeftBound>(s_col, c0, l2, sl2, kb, ks, pr + hh * C::kCols);
         else
           dq_probs<C::kCols, true, kLeftBound, kSeg>(s_col, c0, l2, sl2, kb, ks, pr + hh * C::kCols, sg[hh]);
@@ -778,6 +801,10 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
   kp.dh = pb.d;
   kp.q_seg = pb.q_seg;
   kp.kv_seg = pb.kv_seg;
+  kp.seg_qblk = pb.seg_qblk;
+  kp.seg_kblk = pb.seg_kblk;
+  kp.nqb = (pb.Lq + kSegBlock - 1) / kSegBlock;
+  kp.nkb = (pb.Lkv + kSegBlock - 1) / kSegBlock;
   kp.scale = pb.scale;
   kp.scale_log2 = pb.scale * kLog2e;
   kp.status = st;

@@ -56,6 +56,9 @@ struct FwdKParams {
   int dh;  // stored head_dim (32 runs as D = 64 with zero-filled columns)
   const int32_t* q_seg;   // [B, Lq] segment ids (kSeg builds)
   const int32_t* kv_seg;  // [B, Lkv]
+  const int4* seg_qblk;   // segment block summary (kSeg builds; nullptr: none)
+  const int4* seg_kblk;
+  int nqb, nkb;           // 128-position blocks per sequence: ceil(Lq/128), ceil(Lkv/128)
   float scale_log2;
   DeviceStatus* status;
 };
@@ -98,8 +101,13 @@ __global__ void __launch_bounds__(320, 1)
     count = 0;
     if (row0 >= p.Lq) return;
     const int last = min(row0 + kBM - 1, p.Lq - 1);
-    const int lo = key_span(row0, p.Lq, kvl, p.wl, p.wr).lo;
-    const int hi = key_span(last, p.Lq, kvl, p.wl, p.wr).hi;
+    int lo = key_span(row0, p.Lq, kvl, p.wl, p.wr).lo;
+    int hi = key_span(last, p.Lq, kvl, p.wl, p.wr).hi;
+    if (kSeg && p.seg_qblk != nullptr) {  // keys whose blocks may share an id with this block
+      const int4 r = seg_block(p.seg_qblk, b, p.nqb, row0 / kSegBlock);
+      lo = max(lo, r.z);
+      hi = min(hi, r.w);
+    }
     if (hi <= lo) return;
     first = lo / kBN;
     count = (hi + kBN - 1) / kBN - first;
@@ -107,9 +115,15 @@ __global__ void __launch_bounds__(320, 1)
   int jlo_a, n_a, jlo_b, n_b;
   tile_range(0, jlo_a, n_a);
   tile_range(1, jlo_b, n_b);
-  // without a left bound every range starts at key tile 0 (compile-time)
-  const int jlo = kLeftBound ? (n_a > 0 ? jlo_a : jlo_b) : 0;
-  const int n = kLeftBound ? (n_b > 0 ? jlo_b + n_b - jlo : n_a) : max(n_a, n_b);
+  // without a left bound every range starts at key tile 0 (compile-time);
+  // otherwise the stream is the hull of the two ranges (with segment ids the
+  // ranges need not grow with the row index, and tiles between two disjoint
+  // ranges are streamed and released unused)
+  int jlo = 0, n = max(n_a, n_b);
+  if (kLeftBound) {
+    jlo = n_a == 0 ? jlo_b : n_b == 0 ? jlo_a : min(jlo_a, jlo_b);
+    n = n_a == 0 ? n_b : n_b == 0 ? n_a : max(jlo_a + n_a, jlo_b + n_b) - jlo;
+  }
   const int lo_a = kLeftBound ? jlo_a - jlo : 0, lo_b = kLeftBound ? jlo_b - jlo : 0;  // tile starts in the stream
 
   if (threadIdx.x == 0) {
@@ -246,6 +260,11 @@ __global__ void __launch_bounds__(320, 1)
     const int my_seg = (kSeg && row < p.Lq) ? __ldg(p.q_seg + static_cast<size_t>(b) * p.Lq + row) : 0;
     const int32_t* kid = kSeg ? p.kv_seg + static_cast<size_t>(b) * p.Lkv : nullptr;
     const bool kid_vec = kSeg && ((static_cast<size_t>(b) * p.Lkv) & 3) == 0;
+    // this query block's summary; (0, -1) never counts as a single id
+    const int row0x = qb * 2 * kBM + x * kBM;
+    const int4 qrec = (kSeg && p.seg_qblk != nullptr && row0x < p.Lq)
+                          ? seg_block(p.seg_qblk, b, p.nqb, row0x / kSegBlock)
+                          : make_int4(0, -1, 0, 0);
     const int jbase = kLeftBound ? (x == 0 ? jlo_a : jlo_b) : 0;
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY, l_sum = 0.f;
@@ -255,7 +274,10 @@ __global__ void __launch_bounds__(320, 1)
       // segment masks: bit i says key col0 + i has the row's id (loaded while
       // the tensor core computes S, so the ids are not live next to S)
       uint32_t segbits[kBN / 32];
-      if (kSeg) {
+      // query and key block hold one and the same id: every pair matches
+      const bool seg_all =
+          kSeg && p.seg_kblk != nullptr && seg_same_single_id(qrec, seg_block(p.seg_kblk, b, p.nkb, jbase + j));
+      if (kSeg && !seg_all) {
 #pragma unroll
         for (int w4 = 0; w4 < kBN / 32; ++w4) {
           uint32_t bits = 0u;
@@ -282,7 +304,7 @@ __global__ void __launch_bounds__(320, 1)
         for (int i = 0; i < kBN; ++i)
           if ((kLeftBound && col0 + i < span.lo) || col0 + i >= span.hi) s[i] = -INFINITY;
       }
-      if (kSeg) {
+      if (kSeg && !seg_all) {
 #pragma unroll
         for (int i = 0; i < kBN; ++i)
           if (!((segbits[i / 32] >> (i % 32)) & 1u)) s[i] = -INFINITY;
@@ -408,6 +430,10 @@ cudaError_t launch_fwd_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t stream
   kp.dh = pb.d;
   kp.q_seg = pb.q_seg;
   kp.kv_seg = pb.kv_seg;
+  kp.seg_qblk = pb.seg_qblk;
+  kp.seg_kblk = pb.seg_kblk;
+  kp.nqb = (pb.Lq + kSegBlock - 1) / kSegBlock;
+  kp.nkb = (pb.Lkv + kSegBlock - 1) / kSegBlock;
   kp.n_qblocks = (pb.Lq + 2 * kBM - 1) / (2 * kBM);
   kp.n_pairs = pb.B * pb.Hq;
   kp.pair_group = l2_pair_group(2l * pb.Lkv * D * 2, kp.n_pairs, pb.G);

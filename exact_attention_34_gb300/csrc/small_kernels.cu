@@ -1,5 +1,7 @@
-// HBM-bound helper kernels: the backward preprocess (delta = rowsum(dO * O))
-// and the log-sum-exp combine of split-KV partials.
+// HBM-bound helper kernels: the backward preprocess (delta = rowsum(dO * O)),
+// the log-sum-exp combine of split-KV partials and the per-block summary of
+// segment ids that lets the tensor-core kernels skip tiles.
+#include <climits>
 #include <cstring>
 #include <type_traits>
 
@@ -172,7 +174,92 @@ cudaError_t run_combine(const float* o_part, const float* lse_part, void* o, flo
   return cudaGetLastError();
 }
 
+// ---- segment summary -----------------------------------------------------------
+// Pass 1: one warp per 128-position block (query blocks of every batch
+// element first, then key blocks) writes the block's smallest and largest id.
+__global__ void __launch_bounds__(256) seg_minmax_kernel(const int32_t* __restrict__ q_seg,
+                                                         const int32_t* __restrict__ kv_seg, int B, int Lq, int Lkv,
+                                                         int nq, int nk, int4* __restrict__ info) {
+  const long rec = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const long nqr = static_cast<long>(B) * nq;
+  if (rec >= nqr + static_cast<long>(B) * nk) return;
+  const bool is_q = rec < nqr;
+  const long r = is_q ? rec : rec - nqr;
+  const int nblk = is_q ? nq : nk, L = is_q ? Lq : Lkv;
+  const int b = static_cast<int>(r / nblk), blk = static_cast<int>(r % nblk);
+  const int32_t* ids = (is_q ? q_seg : kv_seg) + static_cast<size_t>(b) * L;
+  int mn = INT_MAX, mx = INT_MIN;
+#pragma unroll
+  for (int i = 0; i < kSegBlock / 32; ++i) {
+    const int pos = blk * kSegBlock + i * 32 + lane;
+    if (pos < L) {
+      const int id = __ldg(ids + pos);
+      mn = min(mn, id);
+      mx = max(mx, id);
+    }
+  }
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) info[rec] = make_int4(mn, mx, 0, 0);
+}
+
+// Pass 2: one thread per block record finds the first and last block of the
+// other side (same batch element) whose id range meets its own; the other
+// side's ranges are staged through shared memory 256 at a time.
+__global__ void __launch_bounds__(256) seg_span_kernel(int B, int Lq, int Lkv, int nq, int nk, int4* __restrict__ info) {
+  __shared__ int2 other[256];
+  const int side = blockIdx.z;  // 0: query blocks look at key blocks, 1: the reverse
+  const int n_mine = side == 0 ? nq : nk, n_other = side == 0 ? nk : nq;
+  const int L_other = side == 0 ? Lkv : Lq;
+  const int idx = blockIdx.x * 256 + threadIdx.x;
+  for (int b = blockIdx.y; b < B; b += gridDim.y) {
+    int4* mine =
+        info + (side == 0 ? static_cast<size_t>(b) * nq : static_cast<size_t>(B) * nq + static_cast<size_t>(b) * nk);
+    const int4* theirs =
+        info + (side == 0 ? static_cast<size_t>(B) * nq + static_cast<size_t>(b) * nk : static_cast<size_t>(b) * nq);
+    int4 me = make_int4(0, -1, 0, 0);
+    if (idx < n_mine) me = mine[idx];
+    int first = INT_MAX, last = -1;
+    for (int c0 = 0; c0 < n_other; c0 += 256) {
+      __syncthreads();
+      if (c0 + static_cast<int>(threadIdx.x) < n_other) {
+        const int4 o = theirs[c0 + threadIdx.x];
+        other[threadIdx.x] = make_int2(o.x, o.y);
+      }
+      __syncthreads();
+      const int cn = min(256, n_other - c0);
+      for (int c = 0; c < cn; ++c) {
+        const int2 o = other[c];
+        if (o.x <= me.y && o.y >= me.x) {
+          first = min(first, c0 + c);
+          last = c0 + c;
+        }
+      }
+    }
+    // the other side's records are read for their id range only, which this
+    // pass never changes, so writing z and w concurrently is harmless
+    if (idx < n_mine) {
+      me.z = last >= 0 ? first * kSegBlock : 0;
+      me.w = last >= 0 ? min(L_other, (last + 1) * kSegBlock) : 0;
+      mine[idx] = me;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_segment_info(const int32_t* q_seg, const int32_t* kv_seg, int B, int Lq, int Lkv, int4* info,
+                                cudaStream_t s) {
+  const int nq = (Lq + kSegBlock - 1) / kSegBlock, nk = (Lkv + kSegBlock - 1) / kSegBlock;
+  const long recs = static_cast<long>(B) * (nq + nk);
+  seg_minmax_kernel<<<static_cast<unsigned>((recs + 7) / 8), 256, 0, s>>>(q_seg, kv_seg, B, Lq, Lkv, nq, nk, info);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const dim3 grid((max(nq, nk) + 255) / 256, min(B, 65535), 2);
+  seg_span_kernel<<<grid, 256, 0, s>>>(B, Lq, Lkv, nq, nk, info);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_bwd_preprocess(const PreprocessArgs& a, cudaStream_t s) {
   if (a.elem == kElemBF16)

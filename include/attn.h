@@ -148,21 +148,45 @@ attn_status attn_bwd_window(const void* q, const void* k, const void* v, const v
  * windows): key j is valid for query row i of batch b only if, in addition,
  * q_segment[b][i] == kv_segment[b][j].  q_segment is a device int32 [B, Lq],
  * kv_segment a device int32 [B, Lkv], both 16-byte aligned and required; ids
- * are arbitrary int32 values and need not be sorted.  Key tiles are skipped by
- * the position masks only; within them the ids are compared per element.
- * Rows with no valid key get o = 0, lse = -inf and dq = 0.  Otherwise as
- * attn_fwd_window / attn_bwd_window.
+ * are arbitrary int32 values and need not be sorted.  Rows with no valid key
+ * get o = 0, lse = -inf and dq = 0.  Otherwise as attn_fwd_window /
+ * attn_bwd_window.
+ *
+ * segment_info (optional, device, 16-byte aligned) is the block summary that
+ * attn_segment_info writes for the same q_segment, kv_segment, B, Lq and Lkv.
+ * With it the 16-bit kernels drop the tiles whose query and key blocks share no
+ * id and skip the per-element id compare on tiles where both blocks hold one
+ * and the same id (packed documents run at the speed of their own causal
+ * blocks).  The library does not check that it matches the ids: after the ids
+ * change, recompute it.  NULL: every tile inside the position masks is
+ * computed and its ids compared per element (same results, slower).
  */
 attn_status attn_fwd_segments(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Lq,
                               int Lkv, int Hq, int Hkv, int d, float scale, int window_left, int window_right,
-                              const int32_t* q_segment, const int32_t* kv_segment, const int32_t* kv_lens,
-                              attn_dtype dtype, attn_stream_t stream);
+                              const int32_t* q_segment, const int32_t* kv_segment, const void* segment_info,
+                              const int32_t* kv_lens, attn_dtype dtype, attn_stream_t stream);
 attn_status attn_bwd_segments(const void* q, const void* k, const void* v, const void* o, const float* lse,
                               const void* dout, void* dq, void* dk, void* dv, int B, int Lq, int Lkv, int Hq,
                               int Hkv, int d, float scale, int window_left, int window_right,
-                              const int32_t* q_segment, const int32_t* kv_segment, const int32_t* kv_lens,
-                              attn_dtype dtype, int deterministic, void* workspace, size_t workspace_bytes,
-                              attn_stream_t stream);
+                              const int32_t* q_segment, const int32_t* kv_segment, const void* segment_info,
+                              const int32_t* kv_lens, attn_dtype dtype, int deterministic, void* workspace,
+                              size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * Block summary of segment ids for attn_fwd_segments / attn_bwd_segments.
+ * For every 128-position block of q_segment ([B, Lq]) and of kv_segment
+ * ([B, Lkv]) it records the smallest and largest id and the range of the other
+ * side's positions whose blocks' id ranges meet it: B*ceil(Lq/128) query
+ * records then B*ceil(Lkv/128) key records of four int32 each, which is
+ * attn_segment_info_size(B, Lq, Lkv) bytes (0 for non-positive sizes).  info
+ * is caller-owned device memory, 16-byte aligned; it is written by two small
+ * kernels on `stream`.  Positions past a batch element's KV length still enter
+ * the summary (they only widen it).  Returns ATTN_ERR_WORKSPACE when
+ * info_bytes is too small.
+ */
+size_t attn_segment_info_size(int B, int Lq, int Lkv);
+attn_status attn_segment_info(const int32_t* q_segment, const int32_t* kv_segment, int B, int Lq, int Lkv,
+                              void* info, size_t info_bytes, attn_stream_t stream);
 
 /*
  * Split-KV decode for few queries over a long KV cache ("Attention

@@ -91,3 +91,29 @@ def test_decode_rules(L):
 def test_preprocess_rejects_bad_arguments(L):
     assert L.attn_bwd_preprocess(FAKE, FAKE, None, 1, 128, 2, 64, 0, None) == 1
     assert L.attn_bwd_preprocess(FAKE, FAKE, FAKE, 1, 128, 2, 80, 0, None) == 2
+
+
+def test_segment_info_rules(L):
+    # one int4 record per 128-position block of each side, per batch element
+    assert L.attn_segment_info_size(2, 300, 129) == 2 * (3 + 2) * 16
+    assert L.attn_segment_info_size(1, 1, 1) == 32
+    assert L.attn_segment_info_size(0, 128, 128) == 0
+    need = L.attn_segment_info_size(2, 300, 129)
+    assert L.attn_segment_info(FAKE, FAKE, 2, 300, 129, FAKE, need - 1, None) == 3  # too small
+    assert L.attn_segment_info(FAKE, FAKE, 2, 300, 129, None, need, None) == 1
+    assert L.attn_segment_info(FAKE, FAKE, 2, 300, 129, FAKE + 4, need, None) == 1
+    assert L.attn_segment_info(None, FAKE, 2, 300, 129, FAKE, need, None) == 1
+    assert L.attn_segment_info(FAKE, FAKE, 0, 300, 129, FAKE, need, None) == 1
+
+
+def test_segment_entry_points_reject_bad_arguments(L):
+    base = [FAKE] * 5 + [1, 128, 128, 2, 2, 64, 0.125, -1, 0]
+    # q_segment, kv_segment, segment_info, kv_lens, dtype, stream
+    assert L.attn_fwd_segments(*base, None, FAKE, None, None, 0, None) == 1
+    assert L.attn_fwd_segments(*base, FAKE, FAKE + 4, None, None, 0, None) == 1
+    assert L.attn_fwd_segments(*base, FAKE, FAKE, FAKE + 8, None, 0, None) == 1  # misaligned info
+    assert L.attn_fwd_segments(*([FAKE] * 5 + [1, 128, 128, 2, 2, 80, 0.125, -1, 0]), FAKE, FAKE, None, None, 0,
+                               None) == 2
+    bbase = [FAKE] * 9 + [1, 128, 128, 2, 2, 64, 0.125, -1, 0]
+    assert L.attn_bwd_segments(*bbase, FAKE, None, None, None, 0, 1, FAKE, 1 << 20, None) == 1
+    assert L.attn_bwd_segments(*bbase, FAKE, FAKE, FAKE + 8, None, 0, 1, FAKE, 1 << 20, None) == 1

@@ -1,6 +1,8 @@
 """Segment (document) masks on the GPU against the fp64 oracle: packed
 documents (sorted ids) and arbitrary unsorted ids, with causal and window
-masks, KV lengths, GQA, Lq != Lkv, all dtypes and both backward variants."""
+masks, KV lengths, GQA, Lq != Lkv, all dtypes and both backward variants;
+with the block summary (tile skipping, single-id tiles unmasked) and without
+it; and the block summary itself against a brute-force count."""
 
 import numpy as np
 import pytest
@@ -26,12 +28,14 @@ def doc_ids(B, L, seed, mean_len):
     return out
 
 
-def check(p, qs, ks, window=None, deterministic=True, seed=0):
+def check(p, qs, ks, window=None, deterministic=True, seed=0, use_info=True):
     import exact_attention_34_gb300 as ea
 
     q, k, v, do = W.make_inputs(p, seed)
     qd, kd, vd, dod = cuda(q, k, v, do)
     segs = (torch.tensor(qs).cuda(), torch.tensor(ks).cuda())
+    if not use_info:
+        segs = segs + (None,)
     kl = None if p.kv_lens is None else torch.tensor(p.kv_lens, dtype=torch.int32).cuda()
     o, lse = ea.forward(qd, kd, vd, causal=p.causal, kv_lens=kl, window=window, segments=segs)
     grads = ea.backward(qd, kd, vd, o, lse, dod, causal=p.causal, kv_lens=kl, window=window, segments=segs,
@@ -53,13 +57,92 @@ def check(p, qs, ks, window=None, deterministic=True, seed=0):
     return o, lse
 
 
+@pytest.mark.parametrize("use_info", [True, False])
 @pytest.mark.parametrize("deterministic", [True, False])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 @pytest.mark.parametrize("causal", [False, True])
-def test_packed_documents(causal, dtype, deterministic):
+def test_packed_documents(causal, dtype, deterministic, use_info):
     p = W.Problem(2, 700, 700, 4, 2, 128, dtype, causal, None, "docs")
     ids = doc_ids(2, 700, 1, 150)
+    check(p, ids, ids, deterministic=deterministic, use_info=use_info)
+
+
+@pytest.mark.parametrize("deterministic", [True, False])
+@pytest.mark.parametrize("d", [64, 128])
+def test_block_aligned_documents(d, deterministic):
+    """Documents of 256 and 384 tokens: every tile inside a document holds one
+    id on both sides (the unmasked path), tiles across documents are dropped."""
+    p = W.Problem(2, 1664, 1664, 4, 2, d, "bf16", True, None, "aligned_docs")
+    lens = [256, 384, 256, 384, 384]
+    ids = np.repeat(np.arange(len(lens), dtype=np.int32), lens)[None].repeat(2, 0)
     check(p, ids, ids, deterministic=deterministic)
+
+
+def block_shuffled_ids(B, L, seed, nblk_ids):
+    """Ids constant over 128-blocks in a shuffled order, with some blocks split
+    in two at a ragged offset: query tiles of one CTA see disjoint key ranges."""
+    rng = np.random.default_rng(seed)
+    nb = (L + 127) // 128
+    out = np.zeros((B, L), dtype=np.int32)
+    for b in range(B):
+        ids = rng.permutation(nblk_ids)[:nb] if nb <= nblk_ids else rng.integers(0, nblk_ids, nb)
+        for i in range(nb):
+            out[b, 128 * i:128 * (i + 1)] = ids[i]
+            if rng.random() < 0.3:
+                cut = 128 * i + int(rng.integers(1, 127))
+                out[b, cut:128 * (i + 1)] = rng.integers(0, nblk_ids)
+    return out
+
+
+@pytest.mark.parametrize("use_info", [True, False])
+@pytest.mark.parametrize("deterministic", [True, False])
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_shuffled_ids(causal, deterministic, use_info):
+    p = W.Problem(2, 1100, 900, 4, 2, 128, "bf16", causal, None, "shuffled")
+    qs = block_shuffled_ids(2, 1100, 3, 12)
+    ks = block_shuffled_ids(2, 900, 4, 12)
+    check(p, qs, ks, deterministic=deterministic, use_info=use_info)
+
+
+def summary_brute_force(qs, ks):
+    """Expected block summary: per 128-block (min id, max id, other-side span)."""
+    def blocks(ids):
+        return [ids[i:i + 128] for i in range(0, len(ids), 128)]
+
+    B, Lq = qs.shape
+    Lkv = ks.shape[1]
+    qrec, krec = [], []
+    for b in range(B):
+        qb, kb = blocks(qs[b]), blocks(ks[b])
+        qmm = [(int(x.min()), int(x.max())) for x in qb]
+        kmm = [(int(x.min()), int(x.max())) for x in kb]
+        for mine, other, L_other, out in ((qmm, kmm, Lkv, qrec), (kmm, qmm, Lq, krec)):
+            for lo, hi in mine:
+                hit = [c for c, (olo, ohi) in enumerate(other) if olo <= hi and ohi >= lo]
+                span = (128 * hit[0], min(L_other, 128 * (hit[-1] + 1))) if hit else (0, 0)
+                out.append((lo, hi) + span)
+    return np.array(qrec + krec, dtype=np.int32)
+
+
+@pytest.mark.parametrize("B,Lq,Lkv,kind", [(3, 700, 300, "random"), (2, 1100, 900, "shuffled"),
+                                           (1, 5000, 5000, "docs"), (2, 1, 129, "random"),
+                                           (1, 40000, 300, "shuffled")])
+def test_segment_info_matches_brute_force(B, Lq, Lkv, kind):
+    import exact_attention_34_gb300 as ea
+
+    rng = np.random.default_rng(B * 7 + Lq)
+    if kind == "random":
+        qs = rng.integers(-5, 5, size=(B, Lq)).astype(np.int32)
+        ks = rng.integers(-5, 5, size=(B, Lkv)).astype(np.int32)
+    elif kind == "shuffled":
+        qs, ks = block_shuffled_ids(B, Lq, 1, 400), block_shuffled_ids(B, Lkv, 2, 400)
+    else:
+        qs = doc_ids(B, Lq, 5, 300)
+        ks = qs.copy()
+    info = ea.segment_info(torch.tensor(qs).cuda(), torch.tensor(ks).cuda())
+    torch.cuda.synchronize()
+    got = info.cpu().view(torch.int32).numpy().reshape(-1, 4)
+    np.testing.assert_array_equal(got, summary_brute_force(qs, ks))
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
