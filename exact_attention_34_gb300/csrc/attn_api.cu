@@ -93,8 +93,10 @@ attn_status check_problem(int B, int Lq, int Lkv, int Hq, int Hkv, int d, float 
   if (causal != 0 && causal != 1) return fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
   if (dtype != ATTN_BF16 && dtype != ATTN_FP32 && dtype != ATTN_FP16)
     return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
-  if (d != 32 && d != 64 && d != 128)
-    return fail(ATTN_ERR_UNSUPPORTED, "head_dim %d not supported (32, 64 or 128)", d);
+  if (d != 32 && d != 64 && d != 128 && d != 256)
+    return fail(ATTN_ERR_UNSUPPORTED, "head_dim %d not supported (32, 64, 128 or 256)", d);
+  if (d == 256 && dtype == ATTN_FP32)
+    return fail(ATTN_ERR_UNSUPPORTED, "head_dim 256 runs on the 16-bit tensor-core path only (bf16 or fp16)");
   // 32-bit index headroom for per-row offsets (elements of one tensor)
   const double big = static_cast<double>(B) * Lq * Hq * d;
   const double bigk = static_cast<double>(B) * Lkv * Hkv * d;
@@ -385,6 +387,7 @@ static attn_status bwd_impl(const void* q, const void* k, const void* v, const v
   if (pb.kv_lens != nullptr && (reinterpret_cast<uintptr_t>(pb.kv_lens) & 3u))
     return fail(ATTN_ERR_INVALID_ARG, "kv_lens is not 4-byte aligned");
   if (deterministic != 0 && deterministic != 1) return fail(ATTN_ERR_INVALID_ARG, "deterministic must be 0 or 1");
+  if (d == 256) return fail(ATTN_ERR_UNSUPPORTED, "head_dim 256: the backward is not built yet");
   const size_t need = attn_bwd_workspace_size(B, Lq, Hq, d, deterministic, dtype);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
@@ -483,6 +486,7 @@ attn_status attn_decode_splitkv(const void* q, const void* k_cache, const void* 
   if (s != ATTN_OK) return s;
   if (kv_lens != nullptr && (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
     return fail(ATTN_ERR_INVALID_ARG, "kv_lens is not 4-byte aligned");
+  if (d == 256) return fail(ATTN_ERR_UNSUPPORTED, "head_dim 256: the split-KV decode is not built yet");
   if (num_splits < 0) return fail(ATTN_ERR_INVALID_ARG, "num_splits must be >= 0");
   if (num_splits == 0) num_splits = attn_decode_num_splits(B, Lq, Lkv, Hq, Hkv, d);
   const int G = Hq / Hkv;

@@ -101,6 +101,7 @@ struct FwdArgs {
 };
 cudaError_t launch_fwd_16(const FwdArgs& a, DeviceStatus* st, cudaStream_t s);  // bf16 or fp16
 cudaError_t launch_fwd_f32(const FwdArgs& a, DeviceStatus* st, cudaStream_t s);
+cudaError_t launch_fwd_d256(const FwdArgs& a, DeviceStatus* st, cudaStream_t s);  // 16-bit, d = 256
 
 // ---- backward --------------------------------------------------------------
 struct BwdArgs {

@@ -457,6 +457,7 @@ cudaError_t launch_fwd_16(const FwdArgs& a, DeviceStatus* st, cudaStream_t s) {
   // head_dim 32 runs through the 64-column kernel: TMA zero-fills columns
   // 32..63 of Q, K and V, so S and the first 32 columns of O are exact
   if (a.pb.d <= 64) return launch_fwd_d<64>(a, st, s);
+  if (a.pb.d == 256) return launch_fwd_d256(a, st, s);
   return launch_fwd_d<128>(a, st, s);
 }
 

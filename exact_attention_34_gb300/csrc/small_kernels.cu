@@ -262,17 +262,16 @@ cudaError_t launch_segment_info(const int32_t* q_seg, const int32_t* kv_seg, int
 }
 
 cudaError_t launch_bwd_preprocess(const PreprocessArgs& a, cudaStream_t s) {
-  if (a.elem == kElemBF16)
-    return a.d == 32   ? run_preprocess<__nv_bfloat16, 32>(a, s)
-           : a.d == 64 ? run_preprocess<__nv_bfloat16, 64>(a, s)
-                       : run_preprocess<__nv_bfloat16, 128>(a, s);
-  if (a.elem == kElemF16)
-    return a.d == 32   ? run_preprocess<__half, 32>(a, s)
-           : a.d == 64 ? run_preprocess<__half, 64>(a, s)
-                       : run_preprocess<__half, 128>(a, s);
-  return a.d == 32 ? run_preprocess<float, 32>(a, s)
-         : a.d == 64 ? run_preprocess<float, 64>(a, s)
-                     : run_preprocess<float, 128>(a, s);
+  auto run = [&](auto tag) -> cudaError_t {
+    using T = decltype(tag);
+    if (a.d == 32) return run_preprocess<T, 32>(a, s);
+    if (a.d == 64) return run_preprocess<T, 64>(a, s);
+    if (a.d == 256) return run_preprocess<T, 256>(a, s);
+    return run_preprocess<T, 128>(a, s);
+  };
+  if (a.elem == kElemBF16) return run(__nv_bfloat16{});
+  if (a.elem == kElemF16) return run(__half{});
+  return run(float{});
 }
 
 cudaError_t launch_decode_combine(const float* o_part, const float* lse_part, void* o, float* lse, int B, int Lq,
@@ -281,6 +280,7 @@ cudaError_t launch_decode_combine(const float* o_part, const float* lse_part, vo
     using T = decltype(tag);
     if (d == 32) return run_combine<T, 32>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s);
     if (d == 64) return run_combine<T, 64>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s);
+    if (d == 256) return run_combine<T, 256>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s);
     return run_combine<T, 128>(o_part, lse_part, o, lse, B, Lq, Hq, num_splits, s);
   };
   if (elem == kElemBF16) return run(__nv_bfloat16{});

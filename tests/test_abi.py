@@ -51,7 +51,7 @@ def fwd(L, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, Lq=128, Lkv=128, Hq=2,
 
 @pytest.mark.parametrize("kw,code", [
     (dict(B=0), 1), (dict(Lq=-1), 1), (dict(Lkv=0), 1), (dict(Hq=3, Hkv=2), 1), (dict(d=96), 2),
-    (dict(d=48), 2), (dict(d=256), 2), (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(scale=-1.0), 1),
+    (dict(d=48), 2), (dict(d=256, dt=1), 2), (dict(d=512), 2), (dict(scale=0.0), 1), (dict(scale=float("nan")), 1), (dict(scale=-1.0), 1),
     (dict(causal=2), 1), (dict(dt=7), 1), (dict(q=None), 1), (dict(lse=None), 1), (dict(k=FAKE + 8), 1),
     (dict(kv=FAKE + 2), 1),
 ])
