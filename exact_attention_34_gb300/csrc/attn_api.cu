@@ -387,7 +387,6 @@ static attn_status bwd_impl(const void* q, const void* k, const void* v, const v
   if (pb.kv_lens != nullptr && (reinterpret_cast<uintptr_t>(pb.kv_lens) & 3u))
     return fail(ATTN_ERR_INVALID_ARG, "kv_lens is not 4-byte aligned");
   if (deterministic != 0 && deterministic != 1) return fail(ATTN_ERR_INVALID_ARG, "deterministic must be 0 or 1");
-  if (d == 256) return fail(ATTN_ERR_UNSUPPORTED, "head_dim 256: the backward is not built yet");
   const size_t need = attn_bwd_workspace_size(B, Lq, Hq, d, deterministic, dtype);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,

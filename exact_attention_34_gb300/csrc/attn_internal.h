@@ -137,6 +137,7 @@ struct PreprocessArgs {
 cudaError_t launch_bwd_preprocess(const PreprocessArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_16(const BwdArgs& a, DeviceStatus* st, cudaStream_t s);
 cudaError_t launch_bwd_f32(const BwdArgs& a, DeviceStatus* st, cudaStream_t s);
+cudaError_t launch_bwd_d256(const BwdArgs& a, DeviceStatus* st, cudaStream_t s);  // 16-bit, d = 256
 
 // ---- segment summary ----------------------------------------------------------
 // Writes the SegBlock records of q_seg ([B, Lq]) and kv_seg ([B, Lkv]) into

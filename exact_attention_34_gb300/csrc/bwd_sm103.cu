@@ -846,6 +846,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
 }  // namespace
 
 cudaError_t launch_bwd_16(const BwdArgs& a, DeviceStatus* st, cudaStream_t s) {
+  if (a.pb.d == 256) return launch_bwd_d256(a, st, s);
   return a.pb.d <= 64 ? launch_bwd_d<64>(a, st, s) : launch_bwd_d<128>(a, st, s);  // head_dim 32 runs as 64
 }
 

@@ -88,3 +88,69 @@ def test_d256_forward_full_size_sampled():
     o_ref, lse_ref = oracle.forward(sl(q), sl(k), sl(v), causal=True)
     assert rel_err(to_np(sl(o)), o_ref) <= TOL["bf16"]
     lse_check(to_np(lse[b:b + 1, h:h + 1]), lse_ref, TOL["bf16"])
+
+
+def check_bwd(p, window=None, segments=None, deterministic=True, seed=0):
+    import exact_attention_34_gb300 as ea
+
+    q, k, v, do = W.make_inputs(p, seed)
+    qd, kd, vd, dod = cuda(q, k, v, do)
+    kl = kvt(p.kv_lens)
+    segs = None if segments is None else (torch.tensor(segments[0]).cuda(), torch.tensor(segments[1]).cuda())
+    o, lse = ea.forward(qd, kd, vd, causal=p.causal, kv_lens=kl, window=window, segments=segs)
+    grads = ea.backward(qd, kd, vd, o, lse, dod, causal=p.causal, kv_lens=kl, window=window, segments=segs,
+                        deterministic=deterministic)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status()[1] == 0
+    ref = oracle.backward(q, k, v, do, causal=p.causal, kv_lens=p.kv_lens, window=window, segments=segments)
+    gmax = max(float(np.max(np.abs(r))) for r in ref) or 1.0
+    for name, g, r in zip(("dQ", "dK", "dV"), grads, ref):
+        g = to_np(g)
+        assert np.all(np.isfinite(g)), name
+        scale = max(float(np.max(np.abs(r))), 0.1 * gmax)  # single-key rows: exact zeros, bound the noise
+        err = float(np.max(np.abs(g - r))) / scale
+        assert err <= TOL[p.dtype], f"{name} rel err {err:.3e}"
+    return grads
+
+
+@pytest.mark.parametrize("deterministic", [True, False])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("case", CASES)
+def test_d256_backward(case, dtype, deterministic):
+    B, Lq, Lkv, Hq, Hkv, causal, kl, win = case
+    check_bwd(W.Problem(B, Lq, Lkv, Hq, Hkv, 256, dtype, causal, kl, "d256bwd"), window=win,
+              deterministic=deterministic)
+
+
+@pytest.mark.parametrize("use_causal", [False, True])
+def test_d256_backward_segments(use_causal):
+    p = W.Problem(2, 700, 700, 4, 2, 256, "bf16", use_causal, None, "d256segbwd")
+    ids = segments_of(2, 700, 5)
+    check_bwd(p, segments=(ids, ids))
+
+
+def test_d256_backward_is_bitwise_reproducible():
+    p = W.Problem(2, 700, 700, 4, 2, 256, "bf16", True, None, "d256rep")
+    g1 = check_bwd(p)
+    g2 = check_bwd(p)
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)
+
+
+def test_d256_backward_full_size_sampled():
+    """bf16 causal B2 Hq8 Hkv2 T4096 d256; the oracle checks one KV group of batch 1."""
+    import exact_attention_34_gb300 as ea
+
+    p = W.Problem(2, 4096, 4096, 8, 2, 256, "bf16", True, None, "d256bwdbig")
+    q, k, v, do = W.make_inputs(p)
+    qd, kd, vd, dod = cuda(q, k, v, do)
+    o, lse = ea.forward(qd, kd, vd, causal=True)
+    dq, dk, dv = ea.backward(qd, kd, vd, o, lse, dod, causal=True)
+    torch.cuda.synchronize()
+    b, hk, G = 1, 1, 4
+    sq = lambda t: t[b:b + 1, :, hk * G:(hk + 1) * G]  # noqa: E731
+    sk = lambda t: t[b:b + 1, :, hk:hk + 1]  # noqa: E731
+    ref = oracle.backward(sq(q), sk(k), sk(v), sq(do), causal=True)
+    for name, g, r in zip(("dQ", "dK", "dV"), (sq(dq), sk(dk), sk(dv)), ref):
+        e = rel_err(to_np(g), r)
+        assert e <= TOL["bf16"], f"{name} rel err {e:.3e}"
