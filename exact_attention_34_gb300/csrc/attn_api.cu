@@ -485,7 +485,6 @@ attn_status attn_decode_splitkv(const void* q, const void* k_cache, const void* 
   if (s != ATTN_OK) return s;
   if (kv_lens != nullptr && (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
     return fail(ATTN_ERR_INVALID_ARG, "kv_lens is not 4-byte aligned");
-  if (d == 256) return fail(ATTN_ERR_UNSUPPORTED, "head_dim 256: the split-KV decode is not built yet");
   if (num_splits < 0) return fail(ATTN_ERR_INVALID_ARG, "num_splits must be >= 0");
   if (num_splits == 0) num_splits = attn_decode_num_splits(B, Lq, Lkv, Hq, Hkv, d);
   const int G = Hq / Hkv;

@@ -1,4 +1,4 @@
-// Split-KV decode forward, bf16 or fp16, head_dim 64/128, on the sm_103a tensor cores.
+// Split-KV decode forward, bf16 or fp16, head_dim 64/128/256, on the sm_103a tensor cores.
 //
 // Method (probjax "Attention performance", section "Grouped-query attention
 // and decoding"): for few queries over a long KV cache the keys are split
@@ -12,24 +12,26 @@
 // The KV stream is the whole cost (HBM-bound), so K/V tiles flow through a
 // deep TMA ring; S is double-buffered in TMEM (S0 [0,128) S1 [128,256),
 // O [256,256+d)) so the softmax of tile j+1 runs while PV of tile j is on the
-// tensor core.  Warps: 0-3 softmax (only the warps holding real rows work),
+// tensor core.  Key tiles are 128 keys wide, 64 at d = 256 (a 128 x 256 K or V
+// tile would be 64 KB and leave room for only two ring slots).  Warps: 0-3 softmax (only the warps holding real rows work),
 // 4 TMA producer, 5 MMA issuer.
 #include "attn_internal.h"
 
 namespace attn {
 namespace {
 
-constexpr int kBN = 128;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct DecCfg {
+  static constexpr int kBN = (D == 256) ? 64 : 128;  // keys per tile
   static constexpr int kQBytes = 128 * D * 2;
-  static constexpr int kBox = 128 * 128;  // 128 rows x 64 cols bf16
+  static constexpr int kBox = 128 * 128;      // query tile box: 128 rows x 64 cols, 16-bit
+  static constexpr int kKVBox = kBN * 128;    // K/V tile box: kBN rows x 64 cols
   static constexpr int kSlotBytes = kBN * D * 2;
-  static constexpr int kSlots = (D == 128) ? 5 : 10;
+  static constexpr int kSlots = (D == 256) ? 5 : (D == 128) ? 5 : 10;
   static constexpr int kOffSlots = kQBytes;
   static constexpr int kOffBars = kOffSlots + kSlots * kSlotBytes;
   static constexpr int kNumBars = 2 * kSlots + 1 + 2 + 2 + 2;
@@ -52,6 +54,7 @@ __global__ void __launch_bounds__(192, 1)
                        const __grid_constant__ CUtensorMap tm_v, const DecKParams p) {
   using C = DecCfg<D>;
   constexpr int NS = C::kSlots;
+  constexpr int kBN = C::kBN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* sQ = smem;
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(192, 1)
           mbar_arrive_expect_tx(&full[s], C::kSlotBytes);
           uint8_t* dst = sSlots + s * C::kSlotBytes;
           for (int c = 0; c < D / 64; ++c)
-            tma_load_4d(dst + c * C::kBox, t == 0 ? &tm_k : &tm_v, &full[s], c * 64, (t0 + j) * kBN, hkv, b);
+            tma_load_4d(dst + c * C::kKVBox, t == 0 ? &tm_k : &tm_v, &full[s], c * 64, (t0 + j) * kBN, hkv, b);
         }
         if (!ok) break;
       }
@@ -136,8 +139,9 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t ka = slot_addr + ((2 * j) % NS) * C::kSlotBytes;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * C::kBox + (k & 3) * 32;
-          mma_ss(tbase + (j & 1) * 128, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+          const uint32_t qoff = (k >> 2) * C::kBox + (k & 3) * 32;
+          const uint32_t koff = (k >> 2) * C::kKVBox + (k & 3) * 32;
+          mma_ss(tbase + (j & 1) * 128, sdesc_sw128(q_addr + qoff, 16, 1024), sdesc_sw128(ka + koff, 16, 1024),
                  idesc_s, k > 0);
         }
         mma_commit(&s_full[j & 1]);
@@ -160,7 +164,7 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t va = slot_addr + vs * C::kSlotBytes;
 #pragma unroll
         for (int k = 0; k < kBN / 16; ++k)
-          mma_ts(tbase + 256, tbase + (j & 1) * 128 + k * 8, sdesc_sw128(va + k * 2048, C::kBox, 1024), idesc_o,
+          mma_ts(tbase + 256, tbase + (j & 1) * 128 + k * 8, sdesc_sw128(va + k * 2048, C::kKVBox, 1024), idesc_o,
                  (j > 0 || k > 0) ? 1u : 0u);
         mma_commit(o_done);
         mma_commit(&empty[vs]);
@@ -326,6 +330,7 @@ cudaError_t launch_decode_d(const DecodeArgs& a, DeviceStatus* st, cudaStream_t 
   const int elem = pb.f16 ? kElemF16 : kElemBF16;
   CUtensorMap tq, tk, tv;
   if (!make_q_group_tmap(&tq, a.q, pb.B, pb.Lq, pb.Hq, pb.d, pb.G, pb.f16 != 0)) return cudaErrorInvalidValue;
+  constexpr int kBN = DecCfg<D>::kBN;
   if (!make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, kBN)) return cudaErrorInvalidValue;
   if (!make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, kBN)) return cudaErrorInvalidValue;
   DecKParams kp;
@@ -351,6 +356,7 @@ cudaError_t launch_decode_d(const DecodeArgs& a, DeviceStatus* st, cudaStream_t 
 }  // namespace
 
 cudaError_t launch_decode_16(const DecodeArgs& a, DeviceStatus* st, cudaStream_t s) {
+  if (a.pb.d == 256) return launch_decode_d<256>(a, st, s);
   return a.pb.d <= 64 ? launch_decode_d<64>(a, st, s) : launch_decode_d<128>(a, st, s);  // head_dim 32 runs as 64
 }
 

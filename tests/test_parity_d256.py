@@ -154,3 +154,18 @@ def test_d256_backward_full_size_sampled():
     for name, g, r in zip(("dQ", "dK", "dV"), (sq(dq), sk(dk), sk(dv)), ref):
         e = rel_err(to_np(g), r)
         assert e <= TOL["bf16"], f"{name} rel err {e:.3e}"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("Lq,causal", [(1, False), (16, True)])
+def test_d256_decode(Lq, causal, dtype):
+    import exact_attention_34_gb300 as ea
+
+    p = W.Problem(2, Lq, 3000, 8, 2, 256, dtype, causal, (3000, 900), "dec256")
+    q, k, v, _ = W.make_inputs(p)
+    o, lse = ea.decode(*cuda(q, k, v), causal=causal, kv_lens=kvt(p.kv_lens), num_splits=4)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status()[1] == 0
+    o_ref, lse_ref = oracle.forward(q, k, v, causal=causal, kv_lens=p.kv_lens)
+    assert rel_err(to_np(o), o_ref) <= TOL[dtype]
+    lse_check(to_np(lse), lse_ref, TOL[dtype])
