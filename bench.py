@@ -493,6 +493,19 @@ def other_rows(args, dev, peaks):
                      "note": f"B4 H8 T8192 d128 bf16, causal within {kind}; the block summary drops tiles "
                              "across documents and runs single-document tiles unmasked"}
     del q, k, v, do
+    # head_dim 256 (its own kernels): the headline shapes at d = 256
+    q = torch.randn(p.B, p.Lq, p.Hq, 256, device=dev, generator=g).to(torch.bfloat16)
+    k, v, do = torch.randn_like(q), torch.randn_like(q), torch.randn_like(q)
+
+    def d256_step():
+        o, lse = ea.forward(q, k, v, causal=True)
+        ea.backward(q, k, v, o, lse, do, causal=True)
+
+    ms = timed(d256_step)
+    f256 = 4.0 * p.B * p.Hq * p.Lq * p.Lq * 256 / 2
+    out["d256_fwd_bwd"] = {"ms": round(ms, 4), "tflops": round(3.5 * f256 / ms / 1e9, 1),
+                           "note": "B4 H8 T8192 d256 bf16 causal, deterministic backward (dV, dK, dQ kernels)"}
+    del q, k, v, do
     # KVLenMask + GQA + Lq != Lkv fwd+bwd (flops over valid keys)
     p = W.kvlen_gqa()
     q = torch.randn(p.B, p.Lq, p.Hq, p.d, device=dev, generator=g).to(torch.bfloat16)

@@ -39,8 +39,11 @@
  *   - dtype ATTN_BF16 / ATTN_FP16: q/k/v/o/dout/dq/dk/dv are bf16 / fp16;
  *     ATTN_FP32: all float32.  lse, delta, partials and workspaces are always
  *     float32.
- *   - head_dim d must be 32, 64 or 128 (32 runs through the 64-wide kernels
- *     with zero-filled columns, as the pages' kernels pad it).
+ *   - head_dim d must be 32, 64, 128 or 256 (32 runs through the 64-wide
+ *     kernels with zero-filled columns, as the pages' kernels pad it; 256 has
+ *     its own 16-bit kernels and is ATTN_ERR_UNSUPPORTED with ATTN_FP32).
+ *     At d = 256 the backward is deterministic for either value of
+ *     `deterministic`.
  *   - Calls are thread-safe: no mutable global state is shared between calls
  *     (tensor-map descriptors are built per call and passed by value).
  */
