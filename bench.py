@@ -647,7 +647,10 @@ def run_sweep(args):
     d in {64, 128}, T in {128 ... 8192} plus the ragged 600 / 1500 / 3000, causal
     and not, bf16; fwd and fwd+bwd TFLOP/s (deterministic backward).  One JSON
     line per case, median of 5 repeats with the quartiles.  Also head_dim 32
-    (bf16) and fp32 at d=128 for T <= 2048."""
+    (bf16) and fp32 at d=128 for T <= 2048.  Each case is timed twice: as eager
+    calls (host work of every call included: the Python binding, tensor-map
+    encoding and launches) and as replays of a CUDA graph that captured the
+    same calls (device time; what a compiled training step sees)."""
     import torch
 
     import exact_attention_34_gb300 as ea
@@ -673,6 +676,19 @@ def run_sweep(args):
         runs.sort()
         return runs[len(runs) // 4], runs[len(runs) // 2], runs[(3 * len(runs)) // 4]
 
+    def graph_timed(fn, n):
+        """timed() of replays of a CUDA graph holding one fn() call."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+        return timed(graph.replay, n)
+
     cases = [(T, d, c, "bf16") for d in (64, 128) for T in W.GRID_T + W.RAGGED_T for c in (False, True)]
     cases += [(T, 32, c, "bf16") for T in W.GRID_T for c in (False, True)]  # head_dim 32 (runs as 64)
     cases += [(T, 128, c, "fp32") for T in (128, 512, 1024, 2048) for c in (False, True)]
@@ -680,16 +696,27 @@ def run_sweep(args):
         p = W.grid(T, d, c, dt)
         g = torch.Generator(device=dev).manual_seed(0)
         q, k, v, do = (torch.randn(p.B, T, p.Hq, d, device=dev, generator=g).to(W.DTYPES[dt]) for _ in range(4))
-        o, lse = ea.forward(q, k, v, causal=c)
         n = max(3, min(200, int(2e12 / max(W.fwd_flops(p), 1.0))))
-        qf = timed(lambda: ea.forward(q, k, v, causal=c), n)
-        qb = timed(lambda: (ea.forward(q, k, v, causal=c), ea.backward(q, k, v, o, lse, do, causal=c)), n)
+        def fwd_call():
+            return ea.forward(q, k, v, causal=c)
+
+        def fwd_bwd_call():
+            o2, lse2 = ea.forward(q, k, v, causal=c)
+            return ea.backward(q, k, v, o2, lse2, do, causal=c)
+
+        qf = timed(fwd_call, n)
+        qb = timed(fwd_bwd_call, n)
+        gf = graph_timed(fwd_call, n)
+        gb = graph_timed(fwd_bwd_call, n)
         F = W.fwd_flops(p)
         print(json.dumps({"T": T, "d": d, "causal": c, "dtype": dt, "fwd_ms": round(qf[1], 4),
                           "fwd_ms_q1_q3": [round(qf[0], 4), round(qf[2], 4)],
                           "fwd_tflops": round(F / qf[1] / 1e9, 1), "fwd_bwd_ms": round(qb[1], 4),
                           "fwd_bwd_ms_q1_q3": [round(qb[0], 4), round(qb[2], 4)],
-                          "fwd_bwd_tflops": round(3.5 * F / qb[1] / 1e9, 1)}), flush=True)
+                          "fwd_bwd_tflops": round(3.5 * F / qb[1] / 1e9, 1),
+                          "graph_fwd_ms": round(gf[1], 4), "graph_fwd_tflops": round(F / gf[1] / 1e9, 1),
+                          "graph_fwd_bwd_ms": round(gb[1], 4),
+                          "graph_fwd_bwd_tflops": round(3.5 * F / gb[1] / 1e9, 1)}), flush=True)
 
 
 def _timed_q(fn, n, repeats=5):
