@@ -13,7 +13,9 @@
 // Tiles are 64 x 64; 256 threads form a 16 x 16 grid.  Thread (ty, tx) owns
 // tile rows 4*ty .. 4*ty+3 and the tile columns tx, tx+16, tx+32, tx+48 (and
 // head-dim columns tx + 16*e), so shared-memory rows padded by one float are
-// read without bank conflicts.
+// read without bank conflicts.  The forward at head_dim >= 64 instead pads
+// rows by four floats, reads them with 16-byte loads, owns head-dim columns
+// 4*tx + 64*g + e, and double-buffers its K/V tiles with asynchronous copies.
 #include "attn_internal.h"
 
 namespace attn {
@@ -101,6 +103,101 @@ __device__ __forceinline__ void tile_ptv(const float* __restrict__ P, const floa
   }
 }
 
+// ---- forward tiles: rows padded by 4 floats so 16-byte shared loads are
+// aligned and conflict-free (row stride 16 bytes past a multiple of 128) ----
+constexpr int kPadV = 4;
+
+// Like load_tile, into rows of D + kPadV floats (16-byte stores).
+template <int D>
+__device__ __forceinline__ void load_tile_v(float* __restrict__ dst, const float* __restrict__ src, int b, int l0,
+                                            int h, int L, int H) {
+  constexpr int kW = D / 4;
+  for (int idx = threadIdx.x; idx < kT * kW; idx += blockDim.x) {
+    const int r = idx / kW, c4 = idx % kW;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (l0 + r < L) v = *reinterpret_cast<const float4*>(src + ((static_cast<size_t>(b) * L + l0 + r) * H + h) * D + c4 * 4);
+    *reinterpret_cast<float4*>(dst + r * (D + kPadV) + c4 * 4) = v;
+  }
+}
+
+// Like load_tile_v, but with asynchronous 16-byte copies (rows past L are
+// zero-filled by a zero source size); the caller commits and waits.
+template <int D>
+__device__ __forceinline__ void load_tile_async(float* __restrict__ dst, const float* __restrict__ src, int b, int l0,
+                                                int h, int L, int H) {
+  constexpr int kW = D / 4;
+  for (int idx = threadIdx.x; idx < kT * kW; idx += blockDim.x) {
+    const int r = idx / kW, c4 = idx % kW;
+    const bool in = l0 + r < L;
+    const float* g = src + ((static_cast<size_t>(b) * L + (in ? l0 + r : 0)) * H + h) * D + c4 * 4;
+    const uint32_t d = smem_u32(dst + r * (D + kPadV) + c4 * 4);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(g), "r"(in ? 16 : 0) : "memory");
+  }
+}
+
+__device__ __forceinline__ void async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// acc[a][c] = sum_k A[4*ty + a][k] * Bm[tx + 16*c][k], four k at a time
+// (A reads are broadcast across tx, B reads hit 16 distinct rows).
+template <int D>
+__device__ __forceinline__ void tile_dot_v(const float* __restrict__ A, const float* __restrict__ Bm, int ty, int tx,
+                                           float (&acc)[4][4]) {
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[a][c] = 0.f;
+#pragma unroll 2
+  for (int k = 0; k < D; k += 4) {
+    float4 av[4], bv[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) av[a] = *reinterpret_cast<const float4*>(A + (4 * ty + a) * (D + kPadV) + k);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) bv[c] = *reinterpret_cast<const float4*>(Bm + (tx + 16 * c) * (D + kPadV) + k);
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        acc[a][c] = fmaf(av[a].x, bv[c].x, acc[a][c]);
+        acc[a][c] = fmaf(av[a].y, bv[c].y, acc[a][c]);
+        acc[a][c] = fmaf(av[a].z, bv[c].z, acc[a][c]);
+        acc[a][c] = fmaf(av[a].w, bv[c].w, acc[a][c]);
+      }
+  }
+}
+
+// out[a][4*g + e] += sum_j P[4*ty + a][j] * M[j][4*tx + 64*g + e] for
+// g < D/64, e < 4: each thread owns two (D = 128) or one (D = 64) groups of
+// four adjacent output columns, read from M with 16-byte loads.  P rows are
+// padded to kT + kPadV floats, M rows to D + kPadV.
+template <int D>
+__device__ __forceinline__ void tile_pv_v(const float* __restrict__ P, const float* __restrict__ M, int ty, int tx,
+                                          float (&out)[4][D / 16]) {
+  constexpr int kGroups = D / 64;  // groups of 4 contiguous columns per thread
+#pragma unroll 2
+  for (int j = 0; j < kT; j += 4) {
+    float4 pv[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) pv[a] = *reinterpret_cast<const float4*>(P + (4 * ty + a) * (kT + kPadV) + j);
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+      for (int g = 0; g < kGroups; ++g) {
+        const float4 m = *reinterpret_cast<const float4*>(M + (j + jj) * (D + kPadV) + 4 * tx + 64 * g);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const float pa = jj == 0 ? pv[a].x : jj == 1 ? pv[a].y : jj == 2 ? pv[a].z : pv[a].w;
+          out[a][4 * g + 0] = fmaf(pa, m.x, out[a][4 * g + 0]);
+          out[a][4 * g + 1] = fmaf(pa, m.y, out[a][4 * g + 1]);
+          out[a][4 * g + 2] = fmaf(pa, m.z, out[a][4 * g + 2]);
+          out[a][4 * g + 3] = fmaf(pa, m.w, out[a][4 * g + 3]);
+        }
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ float row_reduce_max(float v) {
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
@@ -132,11 +229,18 @@ struct F32FwdParams {
 // ordinary forward; otherwise split s covers keys [s*chunk, (s+1)*chunk).
 template <int D>
 __global__ void __launch_bounds__(256) f32_fwd_kernel(const F32FwdParams p) {
+  // head_dim >= 64 reads its tiles with 16-byte loads (rows padded by
+  // kPadV); head_dim 32 keeps scalar loads (rows padded by kPad)
+  constexpr bool kVec = D >= 64;
+  constexpr int kP = kVec ? kPadV : kPad;
+  // K and V tiles are double-buffered (head_dim >= 64): tile j+1 is copied
+  // asynchronously while tile j is computed
+  constexpr int kBufs = kVec ? 2 : 1;
   extern __shared__ float sm[];
   float* Qs = sm;
-  float* Ks = Qs + kT * (D + kPad);
-  float* Vs = Ks + kT * (D + kPad);
-  float* Ps = Vs + kT * (D + kPad);
+  float* Kb = Qs + kT * (D + kP);
+  float* Vb = Kb + kBufs * kT * (D + kP);
+  float* Ps = Vb + kBufs * kT * (D + kP);
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int q0 = blockIdx.x * kT, h = blockIdx.y;
   const int b = blockIdx.z % p.B, split = blockIdx.z / p.B;
@@ -150,7 +254,8 @@ __global__ void __launch_bounds__(256) f32_fwd_kernel(const F32FwdParams p) {
   const int lo_first = max(k_lo, key_span(q0, p.Lq, kvl, p.wl, p.wr).lo);
   const int j_start = k_lo + ((lo_first - k_lo) / kT) * kT;
 
-  load_tile<D>(Qs, p.q, b, q0, h, p.Lq, p.Hq);
+  if (kVec) load_tile_v<D>(Qs, p.q, b, q0, h, p.Lq, p.Hq);
+  else load_tile<D>(Qs, p.q, b, q0, h, p.Lq, p.Hq);
   float m[4], l[4], acc[4][D / 16];
   int klo[4], khi[4], qseg[4];
   const bool seg = p.q_seg != nullptr;
@@ -166,13 +271,35 @@ __global__ void __launch_bounds__(256) f32_fwd_kernel(const F32FwdParams p) {
 #pragma unroll
     for (int e = 0; e < D / 16; ++e) acc[a][e] = 0.f;
   }
-  for (int j0 = j_start; j0 < hi_all; j0 += kT) {
-    __syncthreads();
-    load_tile<D>(Ks, p.k, b, j0, hk, p.Lkv, p.Hkv);
-    load_tile<D>(Vs, p.v, b, j0, hk, p.Lkv, p.Hkv);
-    __syncthreads();
+  auto issue_kv = [&](int j, int buf) {
+    load_tile_async<D>(Kb + buf * kT * (D + kP), p.k, b, j, hk, p.Lkv, p.Hkv);
+    load_tile_async<D>(Vb + buf * kT * (D + kP), p.v, b, j, hk, p.Lkv, p.Hkv);
+    async_commit();
+  };
+  if (kVec && j_start < hi_all) issue_kv(j_start, 0);
+  for (int j0 = j_start, it = 0; j0 < hi_all; j0 += kT, ++it) {
+    const int buf = kVec ? (it & 1) : 0;
+    float* Ks = Kb + buf * kT * (D + kP);
+    float* Vs = Vb + buf * kT * (D + kP);
+    if (kVec) {
+      // buffer buf ^ 1 was last read in the previous iteration, which every
+      // thread has left (barrier at its end)
+      if (j0 + kT < hi_all) {
+        issue_kv(j0 + kT, buf ^ 1);
+        async_wait<1>();
+      } else {
+        async_wait<0>();
+      }
+      __syncthreads();
+    } else {
+      __syncthreads();
+      load_tile<D>(Ks, p.k, b, j0, hk, p.Lkv, p.Hkv);
+      load_tile<D>(Vs, p.v, b, j0, hk, p.Lkv, p.Hkv);
+      __syncthreads();
+    }
     float s[4][4];
-    tile_dot<D>(Qs, Ks, ty, tx, s);
+    if (kVec) tile_dot_v<D>(Qs, Ks, ty, tx, s);
+    else tile_dot<D>(Qs, Ks, ty, tx, s);
     int kseg[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -199,14 +326,16 @@ __global__ void __launch_bounds__(256) f32_fwd_kernel(const F32FwdParams p) {
       for (int c = 0; c < 4; ++c) {
         const float pv = ex2_approx(s[a][c] - mb);
         ls += pv;
-        Ps[(4 * ty + a) * (kT + kPad) + tx + 16 * c] = pv;
+        Ps[(4 * ty + a) * (kT + kP) + tx + 16 * c] = pv;
       }
       l[a] = l[a] * alpha + row_reduce_sum(ls);
 #pragma unroll
       for (int e = 0; e < D / 16; ++e) acc[a][e] *= alpha;
     }
     __syncthreads();
-    tile_pv<D>(Ps, Vs, ty, tx, acc);
+    if (kVec) tile_pv_v<D>(Ps, Vs, ty, tx, acc);
+    else tile_pv<D>(Ps, Vs, ty, tx, acc);
+    if (kVec) __syncthreads();  // Ps, Ks and Vs are rewritten next iteration
   }
   const bool partial = p.o == nullptr;
 #pragma unroll
@@ -224,8 +353,15 @@ __global__ void __launch_bounds__(256) f32_fwd_kernel(const F32FwdParams p) {
       orow = p.o_part + r * D;
       if (tx == 0) p.lse_part[r] = lse_v;
     }
+    if (kVec) {  // columns 4*tx + 64*g + e
 #pragma unroll
-    for (int e = 0; e < D / 16; ++e) orow[tx + 16 * e] = acc[a][e] * inv;
+      for (int g = 0; g < D / 64; ++g)
+        *reinterpret_cast<float4*>(orow + 4 * tx + 64 * g) =
+            make_float4(acc[a][4 * g] * inv, acc[a][4 * g + 1] * inv, acc[a][4 * g + 2] * inv, acc[a][4 * g + 3] * inv);
+    } else {  // columns tx + 16*e
+#pragma unroll
+      for (int e = 0; e < D / 16; ++e) orow[tx + 16 * e] = acc[a][e] * inv;
+    }
   }
 }
 
@@ -459,7 +595,9 @@ __global__ void f32_dq_convert_kernel(const float* __restrict__ acc, float* __re
 
 template <int D>
 constexpr int fwd_smem() {
-  return (3 * kT * (D + kPad) + kT * (kT + kPad)) * 4;
+  constexpr int kP = D >= 64 ? kPadV : kPad;
+  constexpr int kBufs = D >= 64 ? 2 : 1;
+  return ((1 + 2 * kBufs) * kT * (D + kP) + kT * (kT + kP)) * 4;
 }
 template <int D>
 constexpr int dkdv_smem() {
