@@ -115,10 +115,12 @@ __device__ __forceinline__ void dkdv_dscores(uint32_t dp_col, int c0, const floa
     const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
     float ds[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < 4; e += 2) {  // P^T (dP^T - delta), two columns per paired instruction
       const int c = 4 * i + e;
-      const uint32_t raw = c < 32 ? da[c] : db[c - 32];
-      ds[e] = pr[c] * (__uint_as_float(raw) - dv[e]);
+      const uint32_t r0 = c < 32 ? da[c] : db[c - 32], r1 = c + 1 < 32 ? da[c + 1] : db[c + 1 - 32];
+      f2_unpack(f2_mul(f2_pack(pr[c], pr[c + 1]),
+                       f2_sub(f2_pack(__uint_as_float(r0), __uint_as_float(r1)), f2_pack(dv[e], dv[e + 1]))),
+                ds[e], ds[e + 1]);
     }
     dk[2 * i] = pack2<kF16>(ds[0], ds[1]);
     dk[2 * i + 1] = pack2<kF16>(ds[2], ds[3]);
@@ -427,12 +429,19 @@ __device__ __forceinline__ void dq_probs(uint32_t s_col, int c0, float l2, float
     tmem_ld32(s_col + c0, *reinterpret_cast<uint32_t(*)[32]>(sr));
   else
     tmem_ld16(s_col + c0, *reinterpret_cast<uint32_t(*)[16]>(sr));
+  // 2^(s sl2 - l2), two columns per paired fp32 FMA
+  const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(-l2, -l2);
 #pragma unroll
-  for (int c = 0; c < N; ++c) {
-    float pv = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -l2));
-    if (MASK) pv = ((!kLower || kb + c0 + c >= ks.lo) && kb + c0 + c < ks.hi) ? pv : 0.f;
-    if (kSeg) pv = ((seg >> c) & 1u) ? pv : 0.f;
-    pr[c] = pv;
+  for (int c = 0; c < N; c += 2) {
+    float t0, t1;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2x2, nl2), t0, t1);
+    float pv[2] = {ex2_approx(t0), ex2_approx(t1)};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      if (MASK) pv[e] = ((!kLower || kb + c0 + c + e >= ks.lo) && kb + c0 + c + e < ks.hi) ? pv[e] : 0.f;
+      if (kSeg) pv[e] = ((seg >> (c + e)) & 1u) ? pv[e] : 0.f;
+      pr[c + e] = pv[e];
+    }
   }
 }
 
@@ -446,10 +455,15 @@ __device__ __forceinline__ void dq_dscores(uint32_t s_col, uint32_t dp_col, int 
   else
     tmem_ld16(dp_col + c0, *reinterpret_cast<uint32_t(*)[16]>(dr));
   uint32_t pk[N / 2];
+  const uint64_t dl2 = f2_pack(dl, dl);
 #pragma unroll
-  for (int i = 0; i < N / 2; ++i)
-    pk[i] = pack2<kF16>(pr[2 * i] * (__uint_as_float(dr[2 * i]) - dl),
-                        pr[2 * i + 1] * (__uint_as_float(dr[2 * i + 1]) - dl));
+  for (int i = 0; i < N / 2; ++i) {  // P (dP - delta), two columns per paired instruction
+    float d0, d1;
+    f2_unpack(f2_mul(f2_pack(pr[2 * i], pr[2 * i + 1]),
+                     f2_sub(f2_pack(__uint_as_float(dr[2 * i]), __uint_as_float(dr[2 * i + 1])), dl2)),
+              d0, d1);
+    pk[i] = pack2<kF16>(d0, d1);
+  }
   if constexpr (N == 32)
     tmem_st16(s_col + c0, *reinterpret_cast<uint32_t(*)[16]>(pk));
   else
