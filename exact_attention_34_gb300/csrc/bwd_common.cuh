@@ -64,15 +64,23 @@ __device__ __forceinline__ void dkdv_probs(uint32_t s_col, int c0, const float* 
                                            uint32_t seg_lo = 0u, uint32_t seg_hi = 0u) {
   uint32_t sa[32], sb[32];
   tmem_ld32_pair(s_col + c0, s_col + c0 + 32, sa, sb);
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c0 + 4 * i);
-    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+    float t[4];  // s sl2 - lse2, two columns per paired FMA
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(i < 8 ? sa[4 * i] : sb[4 * i - 32]),
+                             __uint_as_float(i < 8 ? sa[4 * i + 1] : sb[4 * i + 1 - 32])),
+                     sl2x2, f2_pack(-l4.x, -l4.y)),
+              t[0], t[1]);
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(i < 8 ? sa[4 * i + 2] : sb[4 * i + 2 - 32]),
+                             __uint_as_float(i < 8 ? sa[4 * i + 3] : sb[4 * i + 3 - 32])),
+                     sl2x2, f2_pack(-l4.z, -l4.w)),
+              t[2], t[3]);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int c = 4 * i + e;
-      const uint32_t raw = c < 32 ? sa[c] : sb[c - 32];
-      float pv = ex2_approx(fmaf(__uint_as_float(raw), sl2, -lv[e]));
+      float pv = ex2_approx(t[e]);
       if (MASK) pv = (key_ok && q_lo + c0 + c >= q_min && (!kUpper || q_lo + c0 + c < q_max)) ? pv : 0.f;
       if (kSeg) pv = (((c < 32 ? seg_lo >> c : seg_hi >> (c - 32)) & 1u) != 0u) ? pv : 0.f;
       pr[c] = pv;
