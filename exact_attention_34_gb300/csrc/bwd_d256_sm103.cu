@@ -280,13 +280,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sa[32], da[32];
       tmem_ld32_pair(s_col, dp_col, sa, da);
       float ds[32];
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(-l2, -l2), dl2 = f2_pack(dl, dl);
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int key = col0 + c;
-        float pv = ex2_approx(fmaf(__uint_as_float(sa[c]), sl2, -l2));
-        if (edge && (key < ks.lo || key >= ks.hi)) pv = 0.f;
-        if (kSeg && !((sg >> c) & 1u)) pv = 0.f;
-        ds[c] = pv * (__uint_as_float(da[c]) - dl);
+      for (int c = 0; c < 32; c += 2) {  // two columns per paired fp32 instruction
+        float t[2], pv[2];
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sa[c]), __uint_as_float(sa[c + 1])), sl2x2, nl2), t[0], t[1]);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int key = col0 + c + e;
+          pv[e] = ex2_approx(t[e]);
+          if (edge && (key < ks.lo || key >= ks.hi)) pv[e] = 0.f;
+          if (kSeg && !((sg >> (c + e)) & 1u)) pv[e] = 0.f;
+        }
+        f2_unpack(f2_mul(f2_pack(pv[0], pv[1]),
+                         f2_sub(f2_pack(__uint_as_float(da[c]), __uint_as_float(da[c + 1])), dl2)),
+                  ds[c], ds[c + 1]);
       }
       store_operand32<kF16>(s_col, ds);
       tmem_st_wait();
@@ -561,16 +569,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float4 l4 = kDK ? *reinterpret_cast<const float4*>(lse2 + 4 * c4) : lg[c4];
         float4 d4 = make_float4(0.f, 0.f, 0.f, 0.f);
         if (kDK) d4 = *reinterpret_cast<const float4*>(dlt + 4 * c4);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        const float nlv[4] = {-l4.x, -l4.y, -l4.z, -l4.w};
         const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 4; e += 2) {  // two columns per paired fp32 instruction
           const int c = 4 * c4 + e;
-          const int q = q0 + c;
-          float pv = ex2_approx(fmaf(__uint_as_float(sa[c]), sl2, -lv[e]));
-          if (edge && (!key_ok || q < qs.lo || q >= qs.hi)) pv = 0.f;
-          if (kSeg && !((sg >> c) & 1u)) pv = 0.f;
-          val[c] = kDK ? pv * (__uint_as_float(da[c]) - dv4[e]) : pv;
+          float t[2], pv[2];
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sa[c]), __uint_as_float(sa[c + 1])), f2_pack(sl2, sl2),
+                           f2_pack(nlv[e], nlv[e + 1])),
+                    t[0], t[1]);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int q = q0 + c + u;
+            pv[u] = ex2_approx(t[u]);
+            if (edge && (!key_ok || q < qs.lo || q >= qs.hi)) pv[u] = 0.f;
+            if (kSeg && !((sg >> (c + u)) & 1u)) pv[u] = 0.f;
+          }
+          if (kDK) {
+            f2_unpack(f2_mul(f2_pack(pv[0], pv[1]), f2_sub(f2_pack(__uint_as_float(da[c]), __uint_as_float(da[c + 1])),
+                                                            f2_pack(dv4[e], dv4[e + 1]))),
+                      val[c], val[c + 1]);
+          } else {
+            val[c] = pv[0];
+            val[c + 1] = pv[1];
+          }
         }
       }
       store_operand32<kF16>(s_col, val);

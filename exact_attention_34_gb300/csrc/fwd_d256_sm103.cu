@@ -270,15 +270,15 @@ __global__ void __launch_bounds__(Cfg256::kThreads, 1)
         for (int i = 0; i < kBN; ++i)
           if (!((segbits[i / 32] >> (i % 32)) & 1u)) s[i] = -INFINITY;
       }
+      // row max: 8 chains of three-input max, then a short tree
       float mx8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx8[k] = s[k];
 #pragma unroll
-      for (int i = 8; i < kBN; i += 8)
+      for (int i = 8; i < kBN; i += 16)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], s[i + k]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int k = 0; k < 8; ++k) mx8[k] = max3f(mx8[k], s[i + k], s[i + 8 + k]);
+      const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
       const float m_tile = mx * sl2;
       const bool grow = m_tile > m_used + kRescaleThreshold;
       const float m_new = grow ? m_tile : m_used;
@@ -302,20 +302,26 @@ __global__ void __launch_bounds__(Cfg256::kThreads, 1)
       }
       m_used = m_new;
       const float mb = (m_used == -INFINITY) ? 0.f : m_used;
-      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+      // P = 2^(s sl2 - mb), two columns per paired fp32 instruction
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), nmb2 = f2_pack(-mb, -mb);
+      uint64_t ls2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < kBN / 32; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(fmaf(s[c * 32 + 2 * i], sl2, -mb));
-          const float p1 = ex2_approx(fmaf(s[c * 32 + 2 * i + 1], sl2, -mb));
-          ls4[i & 3] += p0 + p1;
+          float t0, t1;
+          f2_unpack(f2_fma(f2_pack(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sl2x2, nmb2), t0, t1);
+          const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+          ls2[i & 1] = f2_add(ls2[i & 1], f2_pack(p0, p1));
           pk[i] = pack2<kF16>(p0, p1);
         }
         tmem_st16(s_addr + c * 16, pk);
       }
-      l_sum += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+      float la, lb, lc, ld;
+      f2_unpack(ls2[0], la, lb);
+      f2_unpack(ls2[1], lc, ld);
+      l_sum += (la + lb) + (lc + ld);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&p_full[buf]);
