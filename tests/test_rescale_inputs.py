@@ -7,12 +7,12 @@ workload inputs give almost none.  No GPU."""
 import numpy as np
 
 import workloads as W
-from tests.test_parity_rescale import ramped_inputs
+from tests.test_parity_rescale import WINDOW_GROWTH, ramped_inputs
 
 THRESHOLD = 8.0  # log2 units, as in the forward kernel
 
 
-def rescale_events(q, k, scale, causal):
+def rescale_events(q, k, scale, causal, window=None):
     q = q.double().numpy()
     k = k.double().numpy()
     B, Lq, Hq, d = q.shape
@@ -25,6 +25,9 @@ def rescale_events(q, k, scale, causal):
             s = q[b, :, h] @ k[b, :, h // G].T * scale * np.log2(np.e)
             if causal:
                 s = np.where(np.arange(Lkv)[None, :] <= np.arange(Lq)[:, None] + Lkv - Lq, s, -np.inf)
+            if window is not None:
+                i, j = np.arange(Lq)[:, None] + Lkv - Lq, np.arange(Lkv)[None, :]
+                s = np.where((j >= i - window[0]) & (j <= i + window[1]), s, -np.inf)
             m_used = np.full(Lq, -np.inf)
             for j0 in range(0, Lkv, 128):
                 m_tile = s[:, j0:j0 + 128].max(axis=1)
@@ -44,3 +47,10 @@ def test_plain_inputs_rarely_rescale():
     p = W.Problem(2, 700, 700, 4, 2, 128, "bf16", False, None, "plain")
     q, k, _, _ = W.make_inputs(p, 0)
     assert rescale_events(q, k, 1.0 / np.sqrt(128), False) <= 5
+
+
+def test_window_inputs_rescale():
+    p = W.Problem(2, 700, 700, 4, 2, 128, "bf16", False, None, "rampwin")
+    q, k, _, _ = ramped_inputs(p, 3, WINDOW_GROWTH)
+    for window in ((200, 0), (100, 50)):
+        assert rescale_events(q, k, 2.0 / np.sqrt(128), False, window) >= 300
