@@ -28,6 +28,7 @@ ATTN_ERR_UNSUPPORTED = 2
 ATTN_ERR_WORKSPACE = 3
 ATTN_ERR_CUDA = 4
 ATTN_ERR_DEVICE = 5
+ATTN_ERR_DEVICE = 5
 
 ATTN_BF16 = 0
 ATTN_FP32 = 1
@@ -79,6 +80,7 @@ def lib() -> ctypes.CDLL:
         "attn_bwd_segments": (I, [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, P, P, P, I, I, P, S, P]),
         "attn_segment_info_size": (S, [I, I, I]),
         "attn_segment_info": (I, [P, P, I, I, I, P, S, P]),
+        "attn_selftest_wait_timeout": (I, [I, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -93,7 +95,7 @@ EXPORTED = (
     "attn_bwd", "attn_decode_num_splits", "attn_decode_splitkv", "attn_decode_combine",
     "attn_decode_workspace_size", "attn_device_status", "attn_timing_enable", "attn_timing_query",
     "attn_bwd_static_scratch", "attn_fwd_window", "attn_bwd_window", "attn_fwd_segments", "attn_bwd_segments",
-    "attn_segment_info_size", "attn_segment_info",
+    "attn_segment_info_size", "attn_segment_info", "attn_selftest_wait_timeout",
 )
 
 
@@ -259,6 +261,12 @@ def attn_device_status(reset=True):
     code, site = ctypes.c_int(0), ctypes.c_int(0)
     st = lib().attn_device_status(ctypes.byref(code), ctypes.byref(site), int(bool(reset)))
     return st, code.value, site.value
+
+
+def attn_selftest_wait_timeout(site, stream=None):
+    """Run the kernels' bounded-wait failure path once (about 2 s); the
+    outcome is read with attn_device_status()."""
+    _check(lib().attn_selftest_wait_timeout(int(site), _stream(stream)), "attn_selftest_wait_timeout")
 
 
 def attn_bwd_static_scratch(q, k, v, o, lse, dout, dq, dk, dv, scale=None, causal=False, kv_lens=None,

@@ -261,7 +261,51 @@ KernelTimer::~KernelTimer() {
 
 using namespace attn;
 
+namespace attn {
+namespace {
+
+// The failure path every pipeline kernel relies on, run on purpose: two warps
+// wait for an mbarrier phase that nothing completes.  The first wait to pass
+// the time limit records (code 1, site) in the status word and raises the
+// abort flag, the other warp's wait then returns at once, and the CTA frees
+// the TMEM it holds before it exits, as the real kernels do.
+__global__ void __launch_bounds__(64) wait_timeout_selftest_kernel(DeviceStatus* st, int site) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  __shared__ uint32_t tmem_slot;
+  const int warp = static_cast<int>(warp_id());
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);  // one arrival completes the phase; none comes
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&tmem_slot, 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  (void)__all_sync(0xffffffffu, mbar_wait(&bar, 0, &abort_flag, st, site));
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem_slot, 32);
+  }
+}
+
+}  // namespace
+}  // namespace attn
+
 extern "C" {
+
+attn_status attn_selftest_wait_timeout(int site, attn_stream_t stream) {
+  DeviceStatus* st = status_ptr();
+  if (st == nullptr) return fail(ATTN_ERR_CUDA, "cannot resolve the device status word");
+  attn::wait_timeout_selftest_kernel<<<1, 64, 0, reinterpret_cast<cudaStream_t>(stream)>>>(st, site);
+  return from_cuda(cudaGetLastError(), "attn_selftest_wait_timeout launch");
+}
 
 const char* attn_status_string(attn_status s) {
   switch (s) {

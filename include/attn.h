@@ -238,6 +238,16 @@ size_t attn_decode_workspace_size(int B, int Lq, int Hq, int d, int num_splits);
 attn_status attn_device_status(int* code, int* site, int reset);
 
 /*
+ * Diagnostic: runs the bounded-wait failure path of the kernels on purpose.
+ * One CTA waits for an mbarrier phase that nothing completes; after the wait
+ * limit (2 s of the GPU's global timer) it records code 1 at `site` in the
+ * device status word, stops its other waiting warp, frees its TMEM and exits.
+ * The device stays usable.  Asynchronous on `stream`; read the outcome with
+ * attn_device_status.  Returns ATTN_ERR_CUDA if the launch fails.
+ */
+attn_status attn_selftest_wait_timeout(int site, attn_stream_t stream);
+
+/*
  * Per-kernel timing for benchmarks (the pages time each case between device
  * synchronisations, "GPU and CPU performance", section "Methodology"; this is
  * the library-side counterpart).  attn_timing_enable(1) clears old records and
