@@ -3,6 +3,7 @@
 // launch; nothing here allocates device memory or synchronises (except
 // attn_device_status, which is documented to).
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <initializer_list>
@@ -200,15 +201,15 @@ bool make_bshd_tmap(CUtensorMap* map, const void* base, int elem, int B, int L, 
 }
 
 int device_sm_count() {
-  static int cache[kMaxDevices] = {};
+  static std::atomic<int> cache[kMaxDevices] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
-  if (cache[dev] == 0) {
-    int n = 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return n;
 }
 
 namespace {

@@ -2,6 +2,8 @@
 // translation units.  Not installed; the public ABI is include/attn.h.
 #pragma once
 
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -175,12 +177,14 @@ int device_sm_count();
 // it twice from racing threads is harmless.
 template <auto K>
 cudaError_t ensure_dynamic_smem(int bytes) {
-  static int done[64] = {};
+  // per device: the size already set (callers on several host threads may
+  // both set it once; the attribute call is idempotent)
+  static std::atomic<int> done[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
-  if (dev >= 0 && dev < 64 && done[dev] == bytes) return cudaSuccess;
+  if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_relaxed) == bytes) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = bytes;
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(bytes, std::memory_order_relaxed);
   return e;
 }
 

@@ -291,16 +291,17 @@ bool make_q_group_tmap(CUtensorMap* map, const void* q, int B, int Lq, int Hq, i
   typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-  static EncodeFn fn = nullptr;
-  if (fn == nullptr) {
+  // looked up once (a function-local static is initialised thread-safely)
+  static const EncodeFn fn = []() -> EncodeFn {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult qr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qr) !=
             cudaSuccess ||
         qr != cudaDriverEntryPointSuccess)
-      return false;
-    fn = reinterpret_cast<EncodeFn>(ptr);
-  }
+      return nullptr;
+    return reinterpret_cast<EncodeFn>(ptr);
+  }();
+  if (fn == nullptr) return false;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(Lq),
                         static_cast<cuuint64_t>(B)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(Hq) * d * 2,
