@@ -109,7 +109,17 @@ def _check(status: int, where: str) -> None:
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device address of a tensor the library reads or writes.  The library
+    indexes dense row-major memory on the GPU, so anything else is refused
+    here rather than read with the wrong strides."""
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError(f"expected a contiguous tensor (shape {tuple(t.shape)}, strides {t.stride()}); "
+                         "call .contiguous() first")
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device}")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream):
@@ -124,9 +134,20 @@ def _dtype(t) -> int:
     return _DT[t.dtype]
 
 
-def _dims(q, k):
+def _dims(q, k, v=None):
+    """(B, Lq, Lkv, Hq, Hkv, d) of q [B, Lq, Hq, d] and k (and v) [B, Lkv, Hkv, d]."""
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q and k must be [batch, seq, heads, head_dim]")
     B, Lq, Hq, d = q.shape
     Lkv, Hkv = k.shape[1], k.shape[2]
+    if k.shape[0] != B or k.shape[3] != d:
+        raise ValueError(f"k {tuple(k.shape)} does not match q {tuple(q.shape)} in batch or head_dim")
+    if v is not None and v.shape != k.shape:
+        raise ValueError(f"v {tuple(v.shape)} must have k's shape {tuple(k.shape)}")
+    if k.dtype != q.dtype or (v is not None and v.dtype != q.dtype):
+        raise TypeError("q, k and v must share one dtype")
+    if Hkv == 0 or Hq % Hkv != 0:
+        raise ValueError(f"query heads {Hq} must be a multiple of KV heads {Hkv}")
     return B, Lq, Lkv, Hq, Hkv, d
 
 
@@ -137,7 +158,7 @@ def _scale(scale, d):
 # ---- entry points with the C names -------------------------------------------
 
 def attn_fwd(q, k, v, o, lse, scale=None, causal=False, kv_lens=None, stream=None):
-    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     _check(lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Lq, Lkv, Hq, Hkv, d,
                           _scale(scale, d), int(bool(causal)), _ptr(kv_lens), _dtype(q), _stream(stream)),
            "attn_fwd")
@@ -150,7 +171,7 @@ def _window(window):
 
 
 def attn_fwd_window(q, k, v, o, lse, window, scale=None, kv_lens=None, stream=None):
-    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     wl, wr = _window(window)
     _check(lib().attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Lq, Lkv, Hq, Hkv, d,
                                  _scale(scale, d), wl, wr, _ptr(kv_lens), _dtype(q), _stream(stream)),
@@ -181,7 +202,7 @@ def segment_info(q_segment, kv_segment, stream=None):
 
 def attn_fwd_segments(q, k, v, o, lse, q_segment, kv_segment, window=(-1, -1), scale=None, kv_lens=None,
                       stream=None, segment_info=None):
-    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     wl, wr = _window(window)
     _check(lib().attn_fwd_segments(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Lq, Lkv, Hq, Hkv, d,
                                    _scale(scale, d), wl, wr, _ptr(q_segment), _ptr(kv_segment), _ptr(segment_info),
@@ -201,7 +222,7 @@ def attn_bwd_workspace_size(B, Lq, Hq, d, deterministic=True, dtype=torch.bfloat
 
 def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, scale=None, causal=False, kv_lens=None,
              deterministic=True, stream=None):
-    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                           B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d), int(bool(causal)), _ptr(kv_lens), _dtype(q),
@@ -211,7 +232,7 @@ def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, scale=None, causal=Fa
 
 def attn_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, workspace, window, scale=None, kv_lens=None,
                     deterministic=True, stream=None):
-    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     wl, wr = _window(window)
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(lib().attn_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
@@ -222,7 +243,7 @@ def attn_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, workspace, window, scale=
 
 def attn_bwd_segments(q, k, v, o, lse, dout, dq, dk, dv, workspace, q_segment, kv_segment, window=(-1, -1),
                       scale=None, kv_lens=None, deterministic=True, stream=None, segment_info=None):
-    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     wl, wr = _window(window)
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(lib().attn_bwd_segments(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
@@ -239,7 +260,7 @@ def attn_decode_num_splits(B, Lq, Lkv, Hq, Hkv, d) -> int:
 
 def attn_decode_splitkv(q, k_cache, v_cache, o_part, lse_part, num_splits, scale=None, causal=False,
                         kv_lens=None, stream=None):
-    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k_cache)
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k_cache, v_cache)
     _check(lib().attn_decode_splitkv(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o_part), _ptr(lse_part), B, Lq,
                                      Lkv, Hq, Hkv, d, _scale(scale, d), int(bool(causal)), _ptr(kv_lens),
                                      int(num_splits), _dtype(q), _stream(stream)),
@@ -275,7 +296,7 @@ def attn_bwd_static_scratch(q, k, v, o, lse, dout, dq, dk, dv, scale=None, causa
     workspace argument and no device allocation, for callers that cannot
     allocate (graph capture, fixed memory pools, embeddings).  Calls on one
     device must not overlap on the GPU."""
-    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     _check(lib().attn_bwd_static_scratch(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                                          _ptr(dk), _ptr(dv), B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d),
                                          int(bool(causal)), _ptr(kv_lens), _dtype(q), _stream(stream)),
@@ -313,7 +334,7 @@ def forward(q, k, v, scale=None, causal=False, kv_lens=None, stream=None, window
     segments = (q_segment [B,Lq], kv_segment [B,Lkv]) int32 adds a segment mask;
     a third element, the segment_info() of those ids, saves recomputing it
     (None there: no tile skipping, ids compared on every tile)."""
-    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     o = torch.empty_like(q)
     lse = torch.empty(B, Hq, Lq, device=q.device, dtype=torch.float32)
     if segments is not None:
@@ -331,7 +352,7 @@ def forward(q, k, v, scale=None, causal=False, kv_lens=None, stream=None, window
 def backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_lens=None, deterministic=True, stream=None,
              window=None, segments=None):
     """(dq, dk, dv) given the forward's o and lse (same mask arguments as forward)."""
-    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k)
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     nbytes = attn_bwd_workspace_size(B, Lq, Hq, d, deterministic, q.dtype)
     ws = torch.empty(max(nbytes, 256), device=q.device, dtype=torch.uint8)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -351,7 +372,7 @@ def backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_lens=None, dete
 def decode(q, k_cache, v_cache, scale=None, causal=False, kv_lens=None, num_splits=0, stream=None,
            return_partials=False):
     """Split-KV decode + log-sum-exp combine: (o, lse) [and the partials]."""
-    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k_cache)
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k_cache, v_cache)
     S = num_splits if num_splits > 0 else attn_decode_num_splits(B, Lq, Lkv, Hq, Hkv, d)
     o_part = torch.empty(B, Hq, S, Lq, d, device=q.device, dtype=torch.float32)
     lse_part = torch.empty(B, Hq, S, Lq, device=q.device, dtype=torch.float32)
