@@ -81,6 +81,9 @@ def lib() -> ctypes.CDLL:
         "attn_segment_info_size": (S, [I, I, I]),
         "attn_segment_info": (I, [P, P, I, I, I, P, S, P]),
         "attn_selftest_wait_timeout": (I, [I, P]),
+        "attn_fwd_num_splits": (I, [I, I, I, I, I, I, I]),
+        "attn_fwd_split_workspace_size": (S, [I, I, I, I, I]),
+        "attn_fwd_split": (I, [P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, I, P, S, I, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -95,7 +98,8 @@ EXPORTED = (
     "attn_bwd", "attn_decode_num_splits", "attn_decode_splitkv", "attn_decode_combine",
     "attn_decode_workspace_size", "attn_device_status", "attn_timing_enable", "attn_timing_query",
     "attn_bwd_static_scratch", "attn_fwd_window", "attn_bwd_window", "attn_fwd_segments", "attn_bwd_segments",
-    "attn_segment_info_size", "attn_segment_info", "attn_selftest_wait_timeout",
+    "attn_segment_info_size", "attn_segment_info", "attn_selftest_wait_timeout", "attn_fwd_num_splits",
+    "attn_fwd_split_workspace_size", "attn_fwd_split",
 )
 
 
@@ -176,6 +180,24 @@ def attn_fwd_window(q, k, v, o, lse, window, scale=None, kv_lens=None, stream=No
     _check(lib().attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Lq, Lkv, Hq, Hkv, d,
                                  _scale(scale, d), wl, wr, _ptr(kv_lens), _dtype(q), _stream(stream)),
            "attn_fwd_window")
+
+
+def attn_fwd_num_splits(B, Lq, Lkv, Hq, d, has_kv_lens, dtype) -> int:
+    return int(lib().attn_fwd_num_splits(B, Lq, Lkv, Hq, d, int(bool(has_kv_lens)), _DT[dtype]))
+
+
+def attn_fwd_split_workspace_size(B, Lq, Hq, d, num_splits) -> int:
+    return int(lib().attn_fwd_split_workspace_size(B, Lq, Hq, d, num_splits))
+
+
+def attn_fwd_split(q, k, v, o, lse, workspace, num_splits, window=(-1, -1), scale=None, kv_lens=None, stream=None):
+    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
+    wl, wr = _window(window)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().attn_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Lq, Lkv, Hq, Hkv, d,
+                                _scale(scale, d), wl, wr, _ptr(kv_lens), int(num_splits), _ptr(workspace), nbytes,
+                                _dtype(q), _stream(stream)),
+           "attn_fwd_split")
 
 
 def attn_segment_info_size(B, Lq, Lkv) -> int:
@@ -328,15 +350,27 @@ def _segment_info_of(segments, stream):
     return segment_info(segments[0], segments[1], stream)
 
 
-def forward(q, k, v, scale=None, causal=False, kv_lens=None, stream=None, window=None, segments=None):
+def forward(q, k, v, scale=None, causal=False, kv_lens=None, stream=None, window=None, segments=None,
+            num_splits=1):
     """(o, lse) for q [B,Lq,Hq,d], k/v [B,Lkv,Hkv,d] on the GPU.  window =
     (left, right) selects the local-window mask (causal must then be False);
     segments = (q_segment [B,Lq], kv_segment [B,Lkv]) int32 adds a segment mask;
     a third element, the segment_info() of those ids, saves recomputing it
-    (None there: no tile skipping, ids compared on every tile)."""
+    (None there: no tile skipping, ids compared on every tile).  num_splits
+    other than 1 splits each query tile pair's key range over up to that many
+    programs (0: the library's choice), through a float32 workspace and a
+    log-sum-exp combine (not with segments)."""
     B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     o = torch.empty_like(q)
     lse = torch.empty(B, Hq, Lq, device=q.device, dtype=torch.float32)
+    if num_splits != 1:
+        if segments is not None:
+            raise ValueError("num_splits applies to the causal, window and KV-length masks, not to segments")
+        S = num_splits if num_splits > 0 else attn_fwd_num_splits(B, Lq, Lkv, Hq, d, kv_lens is not None, q.dtype)
+        nbytes = attn_fwd_split_workspace_size(B, Lq, Hq, d, S)
+        ws = torch.empty(nbytes, device=q.device, dtype=torch.uint8) if nbytes > 0 else None
+        attn_fwd_split(q, k, v, o, lse, ws, S, _mask_window(causal, window), scale, kv_lens, stream)
+        return o, lse
     if segments is not None:
         attn_fwd_segments(q, k, v, o, lse, segments[0], segments[1], _mask_window(causal, window), scale, kv_lens,
                           stream, _segment_info_of(segments, stream))

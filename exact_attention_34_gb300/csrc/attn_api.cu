@@ -4,6 +4,7 @@
 // attn_device_status, which is documented to).
 #include <algorithm>
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <initializer_list>
@@ -322,8 +323,20 @@ const char* attn_status_string(attn_status s) {
 
 const char* attn_last_error(void) { return t_last_error; }
 
+// Split key ranges of the forward: pieces per query-tile pair, the KV tiles a
+// piece holds before a stream is cut further, the partial buffers and the
+// per-pair ticket counters.
+struct FwdSplit {
+  int n_split;
+  int chunk;
+  float* o_part;
+  float* lse_part;
+  int* counters;
+  size_t counter_bytes;
+};
+
 static attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, const Problem& pb,
-                     attn_dtype dtype, attn_stream_t stream) {
+                     attn_dtype dtype, attn_stream_t stream, const FwdSplit* split = nullptr) {
   attn_status s = need_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}});
   if (s != ATTN_OK) return s;
   if (pb.kv_lens != nullptr && (reinterpret_cast<uintptr_t>(pb.kv_lens) & 3u))
@@ -337,6 +350,15 @@ static attn_status fwd_impl(const void* q, const void* k, const void* v, void* o
   a.lse = lse;
   DeviceStatus* st = status_ptr();
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (split != nullptr) {
+    a.n_split = split->n_split;
+    a.split_chunk = split->chunk;
+    a.o_part = split->o_part;
+    a.lse_part = split->lse_part;
+    a.counters = split->counters;
+    cudaError_t e = cudaMemsetAsync(split->counters, 0, split->counter_bytes, cs);
+    if (e != cudaSuccess) return from_cuda(e, "attn_fwd_split counters");
+  }
   a.pb.f16 = dtype == ATTN_FP16;
   cudaError_t e = dtype == ATTN_FP32 ? launch_fwd_f32(a, st, cs) : launch_fwd_16(a, st, cs);
   return from_cuda(e, "attn_fwd launch");
@@ -370,6 +392,78 @@ attn_status attn_fwd_segments(const void* q, const void* k, const void* v, void*
   s = set_segments(pb, q_segment, kv_segment, segment_info);
   if (s != ATTN_OK) return s;
   return fwd_impl(q, k, v, o, lse, pb, dtype, stream);
+}
+
+int attn_fwd_num_splits(int B, int Lq, int Lkv, int Hq, int d, int has_kv_lens, attn_dtype dtype) {
+  if (B <= 0 || Lq <= 0 || Lkv <= 0 || Hq <= 0 || d <= 0 || d > 128 || dtype == ATTN_FP32) return 1;
+  // The pairs of 128-row query tiles that may be busy: with KV lengths on the
+  // device every key may sit in one batch element, so only its pairs count.
+  // From one full wave of them on, cutting does not shorten the run.
+  const long tiles = (Lkv + 127) / 128;
+  const long busy = static_cast<long>(Hq) * ((Lq + 255) / 256) * (has_kv_lens ? 1 : B);
+  const long sms = device_sm_count();
+  if (busy >= sms) return 1;
+  // Cutting each busy pair into s pieces takes ceil(s * busy / sms) rounds of
+  // 1/s of a pair; each piece also costs its float32 partial (written, then
+  // read by the combine) and a program start, charged at 5 % of a pair.  Each
+  // piece keeps at least 8 KV tiles, and at most Lkv / 4096 pieces keep the
+  // partials small next to the tensor work when every batch element is full.
+  const long cap = std::min({8L, tiles / 8, static_cast<long>(Lkv) / 4096});
+  int best = 1;
+  double best_cost = 1.05;
+  for (long s = 2; s <= cap; ++s) {
+    const double cost = static_cast<double>((s * busy + sms - 1) / sms) / s + 0.05 * s;
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = static_cast<int>(s);
+    }
+  }
+  return best;
+}
+
+// o_part [B, Hq, S, Lq, d] fp32, lse_part [B, Hq, S, Lq] fp32, then one int
+// ticket counter per pair of 128-row query tiles; each region 256-byte aligned
+static size_t fwd_split_counter_bytes(int B, int Lq, int Hq) {
+  return static_cast<size_t>(B) * Hq * ((Lq + 255) / 256) * sizeof(int);
+}
+
+size_t attn_fwd_split_workspace_size(int B, int Lq, int Hq, int d, int num_splits) {
+  if (B <= 0 || Lq <= 0 || Hq <= 0 || d <= 0 || d > 128 || num_splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(B) * Hq * num_splits * Lq;
+  return align256(rows * d * sizeof(float)) + align256(rows * sizeof(float)) +
+         align256(fwd_split_counter_bytes(B, Lq, Hq));
+}
+
+attn_status attn_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Lq, int Lkv,
+                           int Hq, int Hkv, int d, float scale, int window_left, int window_right,
+                           const int32_t* kv_lens, int num_splits, void* workspace, size_t workspace_bytes,
+                           attn_dtype dtype, attn_stream_t stream) {
+  attn_status s = check_problem(B, Lq, Lkv, Hq, Hkv, d, scale, 0, dtype);
+  if (s != ATTN_OK) return s;
+  if (num_splits < 0) return fail(ATTN_ERR_INVALID_ARG, "num_splits must be >= 0");
+  if (num_splits > 1024) return fail(ATTN_ERR_INVALID_ARG, "num_splits must be <= 1024");
+  if (num_splits == 0) num_splits = attn_fwd_num_splits(B, Lq, Lkv, Hq, d, kv_lens != nullptr, dtype);
+  const Problem pb = make_window_problem(B, Lq, Lkv, Hq, Hkv, d, scale, window_left, window_right, kv_lens);
+  if (num_splits == 1 || d > 128 || dtype == ATTN_FP32) return fwd_impl(q, k, v, o, lse, pb, dtype, stream);
+  if (static_cast<long>(B) * Hq * ((Lq + 255) / 256) * num_splits > INT_MAX)
+    return fail(ATTN_ERR_UNSUPPORTED, "grid of %ld programs too large", static_cast<long>(B) * Hq * ((Lq + 255) / 256) * num_splits);
+  const size_t need = attn_fwd_split_workspace_size(B, Lq, Hq, d, num_splits);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                workspace == nullptr ? static_cast<size_t>(0) : workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(ATTN_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  const size_t rows = static_cast<size_t>(B) * Hq * num_splits * Lq;
+  FwdSplit sp;
+  sp.n_split = num_splits;
+  const int tiles = (Lkv + 127) / 128;
+  sp.chunk = (tiles + num_splits - 1) / num_splits;
+  sp.o_part = static_cast<float*>(workspace);
+  sp.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * d * sizeof(float)));
+  sp.counters = reinterpret_cast<int*>(static_cast<char*>(workspace) + align256(rows * d * sizeof(float)) +
+                                       align256(rows * sizeof(float)));
+  sp.counter_bytes = fwd_split_counter_bytes(B, Lq, Hq);
+  return fwd_impl(q, k, v, o, lse, pb, dtype, stream, &sp);
 }
 
 size_t attn_segment_info_size(int B, int Lq, int Lkv) {

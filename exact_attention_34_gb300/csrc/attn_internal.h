@@ -100,6 +100,14 @@ struct FwdArgs {
   const void* v;
   void* o;
   float* lse;
+  // split key ranges (16-bit, head_dim <= 128): pieces write fp32 partials
+  // and the last piece of each pair merges them into o and lse; n_split = 1
+  // writes them directly
+  int n_split = 1;
+  int split_chunk = 0;      // KV tiles per piece before a stream is cut further
+  float* o_part = nullptr;  // [B, Hq, n_split, Lq, d]
+  float* lse_part = nullptr;  // [B, Hq, n_split, Lq]
+  int* counters = nullptr;    // one ticket counter per query-tile pair, zeroed before the launch
 };
 cudaError_t launch_fwd_16(const FwdArgs& a, DeviceStatus* st, cudaStream_t s);  // bf16 or fp16
 cudaError_t launch_fwd_f32(const FwdArgs& a, DeviceStatus* st, cudaStream_t s);

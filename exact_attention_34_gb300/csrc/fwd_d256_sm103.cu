@@ -273,9 +273,9 @@ __global__ void __launch_bounds__(Cfg256::kThreads, 1)
       // row max: 8 chains of three-input max, then a short tree
       float mx8[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = s[k];
+      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(s[k], s[8 + k]);  // columns 0..15
 #pragma unroll
-      for (int i = 8; i < kBN; i += 16)
+      for (int i = 16; i < kBN; i += 16)  // then 16 more a step: the last reads column kBN - 1
 #pragma unroll
         for (int k = 0; k < 8; ++k) mx8[k] = max3f(mx8[k], s[i + k], s[i + 8 + k]);
       const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));

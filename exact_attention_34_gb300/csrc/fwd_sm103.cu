@@ -23,6 +23,18 @@
 // columns (tcgen05.mma ops of one thread execute in issue order).  O is
 // rescaled lazily: only when a row's running maximum grows by more than
 // 2^8 (kRescaleThreshold), done by the softmax warps in TMEM.
+//
+// Split key ranges (left-bounded builds, n_split > 1): every tile pair gets
+// n_split programs and program sp takes piece sp of the pair's key stream,
+// cut into pieces = min(n_split, ceil(n / split_chunk)) near-equal parts;
+// programs past the last piece exit at once.  A pair left whole writes o and
+// lse as usual.  A piece of a cut pair writes O / l of its keys in fp32 and
+// its own log-sum-exp to the partial buffers ([B, Hq, n_split, Lq, dh] and
+// [B, Hq, n_split, Lq]), then takes a ticket from the pair's counter; the
+// piece that draws the last ticket merges all pieces by their log-sum-exps
+// (from L2, no wait on anyone) and writes o and lse, and resets the counter.
+// So a KV-length mask that puts most keys in a few batch elements still
+// spreads them over every SM.
 #include "attn_internal.h"
 
 namespace attn {
@@ -61,6 +73,11 @@ struct FwdKParams {
   int nqb, nkb;           // 128-position blocks per sequence: ceil(Lq/128), ceil(Lkv/128)
   float scale_log2;
   DeviceStatus* status;
+  int n_split;            // 1, or copies of the tile-pair grid (split key ranges)
+  int split_chunk;        // KV tiles a piece may hold before the stream is cut further
+  float* o_part;          // [B, Hq, n_split, Lq, dh] fp32 (n_split > 1)
+  float* lse_part;        // [B, Hq, n_split, Lq]
+  int* counters;          // [n_pairs * n_qblocks] tickets, zero on entry and on exit
 };
 
 template <int D, bool kLeftBound, bool kF16, bool kSeg>
@@ -81,11 +98,16 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* o_full = q_full + 5;  // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_piece = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
   const int warp = warp_id(), lane = lane_id();
   // 1-D grid over (b, hq) pairs x query blocks in L2 groups; the longest
   // causal blocks of a group start first.
-  const TileCoord tc = grouped_tile(blockIdx.x, p.n_pairs, p.n_qblocks, p.pair_group);
+  // split key ranges: the pieces of one pair are neighbours in the grid, so
+  // the longest pairs' pieces all start in the first wave
+  const int sp = kLeftBound ? static_cast<int>(blockIdx.x) % p.n_split : 0;  // key-range piece
+  const int item = kLeftBound ? static_cast<int>(blockIdx.x) / p.n_split : static_cast<int>(blockIdx.x);
+  const TileCoord tc = grouped_tile(item, p.n_pairs, p.n_qblocks, p.pair_group);
   const int qb = p.causal ? p.n_qblocks - 1 - tc.rank : tc.rank;
   const int hq = tc.pair % p.Hq, b = tc.pair / p.Hq;
   const int hkv = hq / p.G;
@@ -124,6 +146,24 @@ __global__ void __launch_bounds__(320, 1)
     jlo = n_a == 0 ? jlo_b : n_b == 0 ? jlo_a : min(jlo_a, jlo_b);
     n = n_a == 0 ? n_b : n_b == 0 ? n_a : max(jlo_a + n_a, jlo_b + n_b) - jlo;
   }
+  int pieces = 1;
+  if (kLeftBound && p.n_split > 1) {
+    pieces = n == 0 ? 1 : min(p.n_split, (n + p.split_chunk - 1) / p.split_chunk);
+    if (sp >= pieces) return;  // nothing of this pair's stream left
+    // piece sp is the stream's tiles [c0, c1); each tile keeps its part of it
+    const int c0 = jlo + static_cast<int>(static_cast<long>(sp) * n / pieces);
+    const int c1 = jlo + static_cast<int>(static_cast<long>(sp + 1) * n / pieces);
+    auto clip = [&](int& first, int& count) {
+      const int a = max(first, c0), e = min(first + count, c1);
+      first = e > a ? a : c0;
+      count = e > a ? e - a : 0;
+    };
+    clip(jlo_a, n_a);
+    clip(jlo_b, n_b);
+    jlo = c0;
+    n = (n_a == 0 && n_b == 0) ? 0 : c1 - c0;
+  }
+  const bool split = pieces > 1;  // this pair is cut: partials, then a ticket
   const int lo_a = kLeftBound ? jlo_a - jlo : 0, lo_b = kLeftBound ? jlo_b - jlo : 0;  // tile starts in the stream
 
   if (threadIdx.x == 0) {
@@ -312,9 +352,9 @@ __global__ void __launch_bounds__(320, 1)
       // row max: 8 independent chains of three-input max, then a short tree
       float mx8[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = s[k];
+      for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(s[k], s[8 + k]);  // columns 0..15
 #pragma unroll
-      for (int i = 8; i < kBN; i += 16)
+      for (int i = 16; i < kBN; i += 16)  // then 16 more a step: the last reads column kBN - 1
 #pragma unroll
         for (int k = 0; k < 8; ++k) mx8[k] = max3f(mx8[k], s[i + k], s[i + 8 + k]);
       const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
@@ -364,6 +404,8 @@ __global__ void __launch_bounds__(320, 1)
     if (ok) {
       tc_fence_after();
       const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
+      // a piece of a split stream writes fp32 partials, a whole stream the output
+      const size_t prow = ((static_cast<size_t>(b) * p.Hq + hq) * p.n_split + sp) * p.Lq + row;
       uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
                             ((static_cast<size_t>(b) * p.Lq + row) * p.Hq + hq) * p.dh;
 #pragma unroll
@@ -376,6 +418,16 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = 0u;
         }
+        if (split) {
+          if (row < p.Lq) {
+            float4* dst = reinterpret_cast<float4*>(p.o_part + prow * p.dh + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
+                                   __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
+          }
+          continue;
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -387,8 +439,69 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       if (row < p.Lq) {
-        p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Lq + row] =
-            l_sum > 0.f ? (m_used + lg2_approx(l_sum)) * kLn2 : -INFINITY;
+        const float lv = l_sum > 0.f ? (m_used + lg2_approx(l_sum)) * kLn2 : -INFINITY;
+        if (split)
+          p.lse_part[prow] = lv;
+        else
+          p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Lq + row] = lv;
+      }
+    }
+    if (split) {
+      // every softmax thread of the CTA reaches this point (a failed wait only
+      // skips work), so the 256-thread named barrier always completes
+      __threadfence();  // this row's partial is visible device-wide
+      named_barrier_sync(1, 2 * kBM);
+      if (threadIdx.x == 0) {
+        const int ticket = atomicAdd(p.counters + item, 1);
+        const int last = ticket == pieces - 1;
+        if (last) p.counters[item] = 0;  // ready for the next call
+        *last_piece = last;
+      }
+      named_barrier_sync(1, 2 * kBM);
+      if (*last_piece && row < p.Lq) {
+        __threadfence();
+        // merge the pieces of this row by their log-sum-exps (natural log)
+        const size_t row0p = (static_cast<size_t>(b) * p.Hq + hq) * p.n_split * p.Lq + row;
+        const size_t lstride = p.Lq;
+        float m = -INFINITY;
+        for (int t = 0; t < pieces; ++t) m = fmaxf(m, __ldcg(p.lse_part + row0p + t * lstride));
+        float tot = 0.f;
+        if (m != -INFINITY)
+          for (int t = 0; t < pieces; ++t) {
+            const float ls = __ldcg(p.lse_part + row0p + t * lstride);
+            if (ls != -INFINITY) tot += expf(ls - m);
+          }
+        const float inv = m == -INFINITY ? 0.f : 1.0f / tot;
+        uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
+                         ((static_cast<size_t>(b) * p.Lq + row) * p.Hq + hq) * p.dh;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          if (c * 32 >= p.dh) break;
+          float acc[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+          for (int t = 0; t < pieces && m != -INFINITY; ++t) {
+            const float ls = __ldcg(p.lse_part + row0p + t * lstride);
+            if (ls == -INFINITY) continue;
+            const float w = expf(ls - m) * inv;
+            const float4* src = reinterpret_cast<const float4*>(p.o_part + (row0p + t * lstride) * p.dh + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 v4 = __ldcg(src + i);
+              acc[4 * i] = fmaf(w, v4.x, acc[4 * i]);
+              acc[4 * i + 1] = fmaf(w, v4.y, acc[4 * i + 1]);
+              acc[4 * i + 2] = fmaf(w, v4.z, acc[4 * i + 2]);
+              acc[4 * i + 3] = fmaf(w, v4.w, acc[4 * i + 3]);
+            }
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack2<kF16>(acc[2 * i], acc[2 * i + 1]);
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+        p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Lq + row] = m == -INFINITY ? -INFINITY : m + logf(tot);
       }
     }
   }
@@ -444,8 +557,14 @@ cudaError_t launch_fwd_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t stream
   kp.pair_group = l2_pair_group(2l * pb.Lkv * D * 2, kp.n_pairs, pb.G);
   kp.scale_log2 = pb.scale * kLog2e;
   kp.status = st;
-  const dim3 grid(kp.n_pairs * kp.n_qblocks);
-  const bool left = pb.wl < kWinInf;
+  kp.n_split = a.n_split > 1 ? a.n_split : 1;
+  kp.split_chunk = a.split_chunk > 0 ? a.split_chunk : 1;
+  kp.o_part = a.o_part;
+  kp.lse_part = a.lse_part;
+  kp.counters = a.counters;
+  const dim3 grid(kp.n_pairs * kp.n_qblocks * kp.n_split);
+  // split key ranges run in the left-bounded builds (their streams start anywhere)
+  const bool left = pb.wl < kWinInf || kp.n_split > 1;
   if (pb.q_seg != nullptr)  // segment masks run the general (two-sided span) build
     return pb.f16 ? launch_fwd_inst<D, true, true, true>(tq, tk, tv, kp, grid, stream)
                   : launch_fwd_inst<D, true, false, true>(tq, tk, tv, kp, grid, stream);

@@ -1,6 +1,7 @@
 // HBM-bound helper kernels: the backward preprocess (delta = rowsum(dO * O)),
 // the log-sum-exp combine of split-KV partials and the per-block summary of
 // segment ids that lets the tensor-core kernels skip tiles.
+#include <algorithm>
 #include <climits>
 #include <cstring>
 #include <type_traits>
@@ -10,13 +11,28 @@
 namespace attn {
 namespace {
 
+// Eight consecutive elements: fetched as raw 16-byte words (one for 16-bit
+// types, two for float32) and widened to float32 only when used, so that a
+// thread can keep several rows' loads in flight in few registers.
 template <typename T>
-__device__ __forceinline__ void load8(const T* p, float (&f)[8]);
+struct Raw8 {
+  uint4 w[sizeof(T) / 2];
+};
+
+template <typename T>
+__device__ __forceinline__ Raw8<T> load_raw8(const T* p) {
+  Raw8<T> r;
+#pragma unroll
+  for (int k = 0; k < static_cast<int>(sizeof(T) / 2); ++k) r.w[k] = reinterpret_cast<const uint4*>(p)[k];
+  return r;
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack8(const Raw8<T>& r, float (&f)[8]);
 
 template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&f)[8]) {
-  const uint4 u = *reinterpret_cast<const uint4*>(p);
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+__device__ __forceinline__ void unpack8<__nv_bfloat16>(const Raw8<__nv_bfloat16>& r, float (&f)[8]) {
+  const uint32_t w[4] = {r.w[0].x, r.w[0].y, r.w[0].z, r.w[0].w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     f[2 * i] = __uint_as_float(w[i] << 16);
@@ -25,9 +41,8 @@ __device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, flo
 }
 
 template <>
-__device__ __forceinline__ void load8<__half>(const __half* p, float (&f)[8]) {
-  const uint4 u = *reinterpret_cast<const uint4*>(p);
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+__device__ __forceinline__ void unpack8<__half>(const Raw8<__half>& r, float (&f)[8]) {
+  const uint32_t w[4] = {r.w[0].x, r.w[0].y, r.w[0].z, r.w[0].w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     __half2 h;
@@ -39,128 +54,240 @@ __device__ __forceinline__ void load8<__half>(const __half* p, float (&f)[8]) {
 }
 
 template <>
-__device__ __forceinline__ void load8<float>(const float* p, float (&f)[8]) {
-  const float4 a = *reinterpret_cast<const float4*>(p);
-  const float4 b = *reinterpret_cast<const float4*>(p + 4);
-  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+__device__ __forceinline__ void unpack8<float>(const Raw8<float>& r, float (&f)[8]) {
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    f[4 * k] = __uint_as_float(r.w[k].x);
+    f[4 * k + 1] = __uint_as_float(r.w[k].y);
+    f[4 * k + 2] = __uint_as_float(r.w[k].z);
+    f[4 * k + 3] = __uint_as_float(r.w[k].w);
+  }
 }
 
 // delta[b, h, i] = sum_c dO[b, i, h, c] * O[b, i, h, c]  (float32 accumulate).
-// Rows are walked in the padded [B, Hq, Lq_pad] order of the outputs; D/8
-// threads share a row, each reducing 8 consecutive elements.  Optionally it
-// also writes lse2 = lse * log2(e) (+inf where lse = -inf, so that every
-// recomputed probability of such a row is 0), fills the pad rows
-// Lq <= i < Lq_pad with delta = 0 and lse2 = +inf, and zeroes the float32 dQ
-// accumulator of the atomic backward.
+// The grid is 2-D: y walks the (b, h) pairs, x blocks of kRowsPerBlock padded
+// rows 0 <= i < Lq_pad of a pair.  D/8 threads share a row, each reducing 8
+// consecutive elements, and a thread takes kRowsPerThread rows a block-row
+// apart with all their loads issued before the first add, so that enough
+// bytes are in flight to stream HBM.  Optionally it also writes
+// lse2 = lse * log2(e) (+inf where lse = -inf, so that every recomputed
+// probability of such a row is 0), fills the pad rows Lq <= i < Lq_pad with
+// delta = 0 and lse2 = +inf, and zeroes the float32 dQ accumulator of the
+// atomic backward.
+constexpr int kPreThreads = 256;
+constexpr int kRowsPerThread = 4;
+
 template <typename T, int D>
-__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict__ o, const T* __restrict__ dout,
-                                                             const float* __restrict__ lse, float* __restrict__ delta,
-                                                             float* __restrict__ lse2, float* __restrict__ dq_acc,
-                                                             long n_rows_pad, int Lq, int Lq_pad, int Hq) {
-  constexpr int kTPR = D / 8;  // threads per row
-  const long tid = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long prow = tid / kTPR;  // (b * Hq + h) * Lq_pad + i
-  const int part = static_cast<int>(tid % kTPR);
-  const long bh = prow / Lq_pad;
-  const int i = static_cast<int>(prow % Lq_pad);
-  const long b = bh / Hq, h = bh % Hq;
-  const bool real = prow < n_rows_pad && i < Lq;
-  float acc = 0.f;
-  if (real) {
-    const long row = (b * Lq + i) * Hq + h;  // row of the [B, Lq, Hq, D] tensors
-    float a[8], g[8];
-    load8<T>(o + row * D + part * 8, a);
-    load8<T>(dout + row * D + part * 8, g);
+__global__ void __launch_bounds__(kPreThreads) bwd_preprocess_kernel(
+    const T* __restrict__ o, const T* __restrict__ dout, const float* __restrict__ lse, float* __restrict__ delta,
+    float* __restrict__ lse2, float* __restrict__ dq_acc, long n_bh, int Lq, int Lq_pad, int Hq) {
+  constexpr int kTPR = D / 8;                              // threads per row (a power of two)
+  constexpr int kRowStep = kPreThreads / kTPR;             // rows one pass of the block covers
+  const int part = static_cast<int>(threadIdx.x) % kTPR;
+  const long i0 = static_cast<long>(blockIdx.x) * kRowStep * kRowsPerThread + threadIdx.x / kTPR;
+  for (long bh = blockIdx.y; bh < n_bh; bh += gridDim.y) {
+    long b;  // bh = b * Hq + h, uniform across the block
+    if (n_bh <= 0x7fffffffL)
+      b = static_cast<unsigned>(bh) / static_cast<unsigned>(Hq);
+    else
+      b = bh / Hq;
+    const long h = bh - b * Hq;
+    Raw8<T> ra[kRowsPerThread], rg[kRowsPerThread];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc = fmaf(a[e], g[e], acc);
-    if (dq_acc != nullptr) {
-      float4* z = reinterpret_cast<float4*>(dq_acc + row * D + part * 8);
-      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < kRowsPerThread; ++k) {
+      const long i = i0 + k * kRowStep;
+      if (i < Lq) {
+        const long row = (b * Lq + i) * Hq + h;  // row of the [B, Lq, Hq, D] tensors
+        ra[k] = load_raw8<T>(o + row * D + part * 8);
+        rg[k] = load_raw8<T>(dout + row * D + part * 8);
+      }
     }
-  }
 #pragma unroll
-  for (int off = kTPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (prow < n_rows_pad && part == 0) {
-    delta[prow] = acc;  // 0 on pad rows
-    if (lse2 != nullptr) {
-      const float l = real ? lse[bh * Lq + i] : -INFINITY;
-      lse2[prow] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+    for (int k = 0; k < kRowsPerThread; ++k) {
+      const long i = i0 + k * kRowStep;
+      const bool real = i < Lq;
+      float acc = 0.f;
+      if (real) {
+        float a[8], g[8];
+        unpack8<T>(ra[k], a);
+        unpack8<T>(rg[k], g);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc = fmaf(a[e], g[e], acc);
+        if (dq_acc != nullptr) {
+          float4* z = reinterpret_cast<float4*>(dq_acc + ((b * Lq + i) * Hq + h) * D + part * 8);
+          z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+          z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int off = kTPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (i < Lq_pad && part == 0) {
+        const long prow = bh * Lq_pad + i;
+        delta[prow] = acc;  // 0 on pad rows
+        if (lse2 != nullptr) {
+          const float l = real ? lse[bh * Lq + i] : -INFINITY;
+          lse2[prow] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+        }
+      }
     }
   }
 }
 
-// One warp per output row (b, h, i): lse = log sum_s exp(lse_s),
-// o = sum_s exp(lse_s - lse) o_s.  Empty splits (lse_s = -inf) weigh 0.
-template <typename T, int D>
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ o_part,
+// Log-sum-exp combine of split partials, for output rows (b, h, i):
+// lse = log sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s.  Empty splits
+// (lse_s = -inf) weigh 0 and their o_s is never read.  A warp takes kRows
+// consecutive rows, lane l the elements [l*kPer, (l+1)*kPer) of each; lane s
+// keeps split s's log-sum-exp (the first 32 in registers).  The partial rows
+// are fetched kU splits of every row at a time, all those loads in flight
+// before the adds.  The row index is split into (b, h, i) once per warp, in
+// 32-bit arithmetic where it fits: 64-bit divisions per row made the kernel
+// instruction-bound.  Many rows (a split forward) run four to a warp, few
+// rows with many splits (a decode) one to a warp.
+template <typename T, int D, int kRows>
+__global__ void __launch_bounds__(256, 2) combine_kernel(const float* __restrict__ o_part,
                                                       const float* __restrict__ lse_part, T* __restrict__ o,
                                                       float* __restrict__ lse, int B, int Lq, int Hq, int S) {
+  constexpr int kPer = D / 32;             // elements per lane
+  constexpr int kU = kPer >= 8 ? 1 : kPer >= 4 ? 2 : 4;  // splits per row fetched together
   const long warp = (static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long n_rows = static_cast<long>(B) * Hq * Lq;
-  if (warp >= n_rows) return;
-  // warp = (b * Hq + h) * Lq + i
-  const int i = static_cast<int>(warp % Lq);
-  const long bh = warp / Lq;
-  const int h = static_cast<int>(bh % Hq);
-  const int b = static_cast<int>(bh / Hq);
-  const float* lrow = lse_part + bh * S * Lq + i;  // stride Lq between splits
-  float m = -INFINITY;
-  for (int s = lane; s < S; s += 32) m = fmaxf(m, lrow[static_cast<long>(s) * Lq]);
+  if (warp * kRows >= n_rows) return;
+  long bh[kRows];
+  int ri[kRows];
+  bool live[kRows];
+  float l0[kRows], m[kRows], tot[kRows], inv[kRows];
+  {
+    const long row0 = warp * kRows;  // row = (b * Hq + h) * Lq + i
+    long bhc;
+    int ic;
+    if (n_rows <= 0x7fffffffL) {
+      const unsigned r0 = static_cast<unsigned>(row0);
+      bhc = r0 / static_cast<unsigned>(Lq);
+      ic = static_cast<int>(r0 - static_cast<unsigned>(bhc) * static_cast<unsigned>(Lq));
+    } else {
+      bhc = row0 / Lq;
+      ic = static_cast<int>(row0 - bhc * Lq);
+    }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  float tot = 0.f;
-  if (m != -INFINITY)
-    for (int s = lane; s < S; s += 32) tot += expf(lrow[static_cast<long>(s) * Lq] - m);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
-  constexpr int kPer = D / 32;  // elements per lane
-  float acc[kPer];
-#pragma unroll
-  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-  if (m != -INFINITY) {
-    const float inv = 1.0f / tot;
-    for (int s = 0; s < S; ++s) {
-      const float ls = lrow[static_cast<long>(s) * Lq];
-      if (ls == -INFINITY) continue;
-      const float w = expf(ls - m) * inv;
-      const float* src = o_part + ((bh * S + s) * Lq + i) * D + lane * kPer;
-      if constexpr (kPer % 2 == 0) {
-#pragma unroll
-        for (int e = 0; e < kPer; e += 2) {
-          const float2 v = *reinterpret_cast<const float2*>(src + e);
-          acc[e] = fmaf(w, v.x, acc[e]);
-          acc[e + 1] = fmaf(w, v.y, acc[e + 1]);
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < kPer; ++e) acc[e] = fmaf(w, src[e], acc[e]);
+    for (int r = 0; r < kRows; ++r) {
+      live[r] = row0 + r < n_rows;
+      ri[r] = ic;
+      bh[r] = bhc;
+      if (++ic == Lq) {
+        ic = 0;
+        ++bhc;
       }
+      l0[r] = (live[r] && lane < S) ? lse_part[(bh[r] * S + lane) * Lq + ri[r]] : -INFINITY;
     }
   }
-  T* dst = o + ((static_cast<long>(b) * Lq + i) * Hq + h) * D + lane * kPer;
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) {
-    if constexpr (std::is_same<T, __nv_bfloat16>::value)
-      dst[e] = __float2bfloat16_rn(acc[e]);
-    else if constexpr (std::is_same<T, __half>::value)
-      dst[e] = __float2half_rn(acc[e]);
-    else
-      dst[e] = acc[e];
+  for (int r = 0; r < kRows; ++r) {
+    m[r] = l0[r];
+    for (int s = 32 + lane; s < S && live[r]; s += 32) m[r] = fmaxf(m[r], lse_part[(bh[r] * S + s) * Lq + ri[r]]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m[r] = fmaxf(m[r], __shfl_xor_sync(0xffffffffu, m[r], off));
+    tot[r] = 0.f;
+    if (m[r] != -INFINITY) {
+      tot[r] = l0[r] == -INFINITY ? 0.f : expf(l0[r] - m[r]);
+      for (int s = 32 + lane; s < S; s += 32) {
+        const float ls = lse_part[(bh[r] * S + s) * Lq + ri[r]];
+        if (ls != -INFINITY) tot[r] += expf(ls - m[r]);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) tot[r] += __shfl_xor_sync(0xffffffffu, tot[r], off);
+    inv[r] = m[r] == -INFINITY ? 0.f : 1.0f / tot[r];
   }
-  if (lane == 0) lse[bh * Lq + i] = (m == -INFINITY) ? -INFINITY : m + logf(tot);
+  float acc[kRows][kPer];
+#pragma unroll
+  for (int r = 0; r < kRows; ++r)
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[r][e] = 0.f;
+  for (int s0 = 0; s0 < S; s0 += 32) {
+    float w_lane[kRows];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      float ls = l0[r];
+      if (s0 > 0) ls = (live[r] && s0 + lane < S) ? lse_part[(bh[r] * S + s0 + lane) * Lq + ri[r]] : -INFINITY;
+      w_lane[r] = (m[r] == -INFINITY || ls == -INFINITY) ? 0.f : expf(ls - m[r]) * inv[r];
+    }
+    const int cnt = min(32, S - s0);
+    for (int t0 = 0; t0 < cnt; t0 += kU) {
+      float w[kRows][kU], val[kRows][kU][kPer];
+#pragma unroll
+      for (int r = 0; r < kRows; ++r)
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          w[r][u] = t0 + u < cnt ? __shfl_sync(0xffffffffu, w_lane[r], t0 + u) : 0.f;
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) val[r][u][e] = 0.f;
+          if (w[r][u] != 0.f) {
+            const float* src = o_part + ((bh[r] * S + s0 + t0 + u) * Lq + ri[r]) * D + lane * kPer;
+            if constexpr (kPer % 4 == 0) {
+#pragma unroll
+              for (int e = 0; e < kPer; e += 4) {
+                const float4 x = *reinterpret_cast<const float4*>(src + e);
+                val[r][u][e] = x.x; val[r][u][e + 1] = x.y; val[r][u][e + 2] = x.z; val[r][u][e + 3] = x.w;
+              }
+            } else if constexpr (kPer % 2 == 0) {
+#pragma unroll
+              for (int e = 0; e < kPer; e += 2) {
+                const float2 x = *reinterpret_cast<const float2*>(src + e);
+                val[r][u][e] = x.x; val[r][u][e + 1] = x.y;
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < kPer; ++e) val[r][u][e] = src[e];
+            }
+          }
+        }
+#pragma unroll
+      for (int r = 0; r < kRows; ++r)
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          if (w[r][u] == 0.f) continue;
+#pragma unroll
+          for (int e = 0; e < kPer; ++e) acc[r][e] = fmaf(w[r][u], val[r][u][e], acc[r][e]);
+        }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    if (!live[r]) continue;
+    long b;  // bh = b * Hq + h
+    int h;
+    if (static_cast<long>(B) * Hq <= 0x7fffffffL) {
+      const unsigned bhu = static_cast<unsigned>(bh[r]);
+      b = bhu / static_cast<unsigned>(Hq);
+      h = static_cast<int>(bhu - static_cast<unsigned>(b) * static_cast<unsigned>(Hq));
+    } else {
+      b = bh[r] / Hq;
+      h = static_cast<int>(bh[r] - b * Hq);
+    }
+    T* dst = o + ((b * Lq + ri[r]) * Hq + h) * D + lane * kPer;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      if constexpr (std::is_same<T, __nv_bfloat16>::value)
+        dst[e] = __float2bfloat16_rn(acc[r][e]);
+      else if constexpr (std::is_same<T, __half>::value)
+        dst[e] = __float2half_rn(acc[r][e]);
+      else
+        dst[e] = acc[r][e];
+    }
+    if (lane == 0) lse[bh[r] * Lq + ri[r]] = (m[r] == -INFINITY) ? -INFINITY : m[r] + logf(tot[r]);
+  }
 }
 
 template <typename T, int D>
 cudaError_t run_preprocess(const PreprocessArgs& a, cudaStream_t s) {
-  const long n_rows = static_cast<long>(a.B) * a.Hq * a.Lq_pad;
-  const long threads = n_rows * (D / 8);
-  const int blocks = static_cast<int>((threads + 255) / 256);
+  const long n_bh = static_cast<long>(a.B) * a.Hq;
+  const long rows_per_block = static_cast<long>(kPreThreads / (D / 8)) * kRowsPerThread;
+  const dim3 grid(static_cast<unsigned>((a.Lq_pad + rows_per_block - 1) / rows_per_block),
+                  static_cast<unsigned>(std::min(n_bh, 65535L)));
   KernelTimer kt("bwd_preprocess", s);
-  bwd_preprocess_kernel<T, D><<<blocks, 256, 0, s>>>(static_cast<const T*>(a.o), static_cast<const T*>(a.dout),
-                                                     a.lse, a.delta, a.lse2, a.dq_acc, n_rows, a.Lq, a.Lq_pad, a.Hq);
+  bwd_preprocess_kernel<T, D><<<grid, kPreThreads, 0, s>>>(static_cast<const T*>(a.o), static_cast<const T*>(a.dout),
+                                                   a.lse, a.delta, a.lse2, a.dq_acc, n_bh, a.Lq, a.Lq_pad, a.Hq);
   return cudaGetLastError();
 }
 
@@ -168,9 +295,15 @@ template <typename T, int D>
 cudaError_t run_combine(const float* o_part, const float* lse_part, void* o, float* lse, int B, int Lq, int Hq,
                         int S, cudaStream_t s) {
   const long n_rows = static_cast<long>(B) * Hq * Lq;
-  const int blocks = static_cast<int>((n_rows * 32 + 255) / 256);
   KernelTimer kt("combine", s);
-  combine_kernel<T, D><<<blocks, 256, 0, s>>>(o_part, lse_part, static_cast<T*>(o), lse, B, Lq, Hq, S);
+  if (n_rows >= 16384) {  // four rows a warp
+    const long warps = (n_rows + 3) / 4;
+    const int blocks = static_cast<int>((warps * 32 + 255) / 256);
+    combine_kernel<T, D, 4><<<blocks, 256, 0, s>>>(o_part, lse_part, static_cast<T*>(o), lse, B, Lq, Hq, S);
+  } else {
+    const int blocks = static_cast<int>((n_rows * 32 + 255) / 256);
+    combine_kernel<T, D, 1><<<blocks, 256, 0, s>>>(o_part, lse_part, static_cast<T*>(o), lse, B, Lq, Hq, S);
+  }
   return cudaGetLastError();
 }
 

@@ -192,6 +192,47 @@ attn_status attn_segment_info(const int32_t* q_segment, const int32_t* kv_segmen
                               void* info, size_t info_bytes, attn_stream_t stream);
 
 /*
+ * Forward with each query tile's key range split across programs: the
+ * split-KV scheme of the decode ("Attention performance", section
+ * "Grouped-query attention and decoding") applied to the whole forward, for
+ * KV-length masks that put most keys in a few batch elements and for grids
+ * too small to fill the GPU.  Arguments, outputs, masks and errors as
+ * attn_fwd_window, plus:
+ *   num_splits  the most pieces one pair of 128-row query tiles cuts its key
+ *               range into; 0 picks attn_fwd_num_splits(...).  A pair whose
+ *               masks and KV length leave n KV tiles of 128 keys cuts them into
+ *               min(num_splits, ceil(n / C)) near-equal pieces,
+ *               C = ceil(ceil(Lkv / 128) / num_splits), so short ranges stay
+ *               whole and a batch element's pieces follow its own length.
+ *   workspace   device memory, 256-byte aligned, at least
+ *               attn_fwd_split_workspace_size(B, Lq, Hq, d, num_splits) bytes;
+ *               its contents on entry do not matter.  It receives each piece's
+ *               float32 output (normalised within the piece) and log-sum-exp,
+ *               and one ticket counter per pair (zeroed by the call with a
+ *               memset on `stream`).  The piece of a pair that finishes last
+ *               (by an atomic ticket; no program waits on another) merges the
+ *               pieces by their log-sum-exps, as attn_decode_combine does, and
+ *               writes o and lse; a pair left whole writes them directly.
+ * attn_fwd_num_splits is the library's choice: with kv_lens (has_kv_lens != 0)
+ * it assumes every key may sit in one batch element, so only that element's
+ * ceil(Lq/256)*Hq tile pairs are busy (all B elements' pairs otherwise); it
+ * cuts only while the busy pairs are fewer than the SMs, weighs the rounds
+ * of programs saved against a fixed cost per piece, and keeps each piece at 8
+ * KV tiles or more and the count at most 8 and at most Lkv / 4096.
+ * num_splits = 1, head_dim 256 and float32 run attn_fwd_window as is and use
+ * no workspace (workspace may then be NULL).  Results equal attn_fwd_window's
+ * up to rounding (pieces are normalised and combined in float32), and are the
+ * same on every run: the merge adds the pieces in a fixed order, whichever
+ * piece performs it.
+ */
+int attn_fwd_num_splits(int B, int Lq, int Lkv, int Hq, int d, int has_kv_lens, attn_dtype dtype);
+size_t attn_fwd_split_workspace_size(int B, int Lq, int Hq, int d, int num_splits);
+attn_status attn_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Lq, int Lkv,
+                           int Hq, int Hkv, int d, float scale, int window_left, int window_right,
+                           const int32_t* kv_lens, int num_splits, void* workspace, size_t workspace_bytes,
+                           attn_dtype dtype, attn_stream_t stream);
+
+/*
  * Split-KV decode for few queries over a long KV cache ("Attention
  * performance", section "Grouped-query attention and decoding"): the keys are
  * split across programs, the G query heads of a KV head (times the Lq rows)

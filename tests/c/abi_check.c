@@ -30,6 +30,10 @@ int main(void) {
          "small workspace");
   expect(attn_segment_info_size(2, 300, 129) == 2 * (3 + 2) * 16, "segment info size");
   expect(attn_decode_num_splits(8, 1, 131072, 32, 8, 128) >= 1, "decode splits");
+  expect(attn_fwd_num_splits(4, 2048, 16384, 8, 128, 1, ATTN_BF16) == 2, "forward splits");
+  expect(attn_fwd_split(fake, fake, fake, fake, (float*)fake, 2, 300, 4096, 4, 2, 64, 0.125f, -1, 0, NULL, 3, NULL,
+                        0, ATTN_BF16, NULL) == ATTN_ERR_WORKSPACE,
+         "split forward without workspace");
   printf("%s\n", fails ? "FAILED" : "OK");
   return fails ? 1 : 0;
 }

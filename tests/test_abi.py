@@ -117,3 +117,36 @@ def test_segment_entry_points_reject_bad_arguments(L):
     bbase = [FAKE] * 9 + [1, 128, 128, 2, 2, 64, 0.125, -1, 0]
     assert L.attn_bwd_segments(*bbase, FAKE, None, None, None, 0, 1, FAKE, 1 << 20, None) == 1
     assert L.attn_bwd_segments(*bbase, FAKE, FAKE, FAKE + 8, None, 0, 1, FAKE, 1 << 20, None) == 1
+
+
+def test_split_forward_rules(L):
+    # the library's choice: one batch element may hold every key when KV lengths
+    # are given (B=4 H8 Lq 2048 Lkv 16384: 64 busy pairs, two pieces fill one
+    # wave); a full grid is not split; one pair alone is cut in four (rounds of
+    # 1/s plus 5 % a piece); head_dim 256 and float32 are never split
+    assert L.attn_fwd_num_splits(4, 2048, 16384, 8, 128, 1, 0) == 2
+    assert L.attn_fwd_num_splits(4, 8192, 8192, 8, 128, 0, 0) == 1
+    assert L.attn_fwd_num_splits(1, 256, 65536, 1, 64, 0, 2) == 4
+    assert L.attn_fwd_num_splits(1, 256, 65536, 1, 256, 0, 0) == 1
+    assert L.attn_fwd_num_splits(1, 256, 65536, 1, 128, 0, 1) == 1
+    assert L.attn_fwd_num_splits(1, 256, 1000, 1, 128, 0, 0) == 1  # under 8 tiles a piece
+    assert L.attn_fwd_num_splits(0, 256, 65536, 1, 128, 0, 0) == 1
+    # partial outputs, log-sum-exps and one counter per query-tile pair, each
+    # 256-byte aligned; nothing for one piece or d = 256
+    rows = 2 * 4 * 3 * 300
+    pairs = 2 * 4 * 2
+    assert L.attn_fwd_split_workspace_size(2, 300, 4, 64, 3) == (-(-rows * 64 * 4 // 256) * 256 + -(-rows * 4 // 256) * 256
+                                                                 + -(-pairs * 4 // 256) * 256)
+    assert L.attn_fwd_split_workspace_size(2, 300, 4, 64, 1) == 0
+    assert L.attn_fwd_split_workspace_size(2, 300, 4, 256, 3) == 0
+    base = [FAKE] * 5 + [2, 300, 4096, 4, 2, 64, 0.125, -1, 0, None]
+    need = L.attn_fwd_split_workspace_size(2, 300, 4, 64, 3)
+    assert L.attn_fwd_split(*base, -1, FAKE, need, 0, None) == 1
+    assert L.attn_fwd_split(*base, 2000, FAKE, 1 << 40, 0, None) == 1
+    assert L.attn_fwd_split(*base, 3, None, need, 0, None) == 3
+    assert L.attn_fwd_split(*base, 3, FAKE, need - 1, 0, None) == 3
+    assert L.attn_fwd_split(*base, 3, FAKE + 16, need, 0, None) == 1  # workspace not 256-byte aligned
+    assert L.attn_fwd_split(*([FAKE] * 5 + [2, 300, 4096, 4, 2, 96, 0.125, -1, 0, None]), 3, FAKE, need, 0,
+                            None) == 2
+    assert L.attn_fwd_split(*([FAKE] * 4 + [None] + [2, 300, 4096, 4, 2, 64, 0.125, -1, 0, None]), 3, FAKE, need, 0,
+                            None) == 1
