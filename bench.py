@@ -514,12 +514,19 @@ def other_rows(args, dev, peaks):
     do = torch.randn_like(q)
     kl = torch.tensor(p.kv_lens, dtype=torch.int32, device=dev)
 
-    def kv_step():
-        o, lse = ea.forward(q, k, v, kv_lens=kl)
+    def kv_step(splits):
+        o, lse = ea.forward(q, k, v, kv_lens=kl, num_splits=splits)
         ea.backward(q, k, v, o, lse, do, kv_lens=kl)
 
-    ms = timed(kv_step)
-    out["kvlen_gqa_fwd_bwd"] = {"ms": round(ms, 4), "tflops": round(3.5 * W.fwd_flops(p) / ms / 1e9, 1)}
+    ms = timed(lambda: kv_step(0))
+    ms1 = timed(lambda: kv_step(1))
+    n_split = ea.attn_fwd_num_splits(p.B, p.Lq, p.Lkv, p.Hq, p.d, True, q.dtype)
+    out["kvlen_gqa_fwd_bwd"] = {
+        "ms": round(ms, 4), "tflops": round(3.5 * W.fwd_flops(p) / ms / 1e9, 1),
+        "forward_pieces": n_split, "unsplit_ms": round(ms1, 4),
+        "unsplit_tflops": round(3.5 * W.fwd_flops(p) / ms1 / 1e9, 1),
+        "note": "B4 Hq8 Hkv2 Lq2048 Lkv16384 d128 bf16, KV lengths (13350, 236, 1, 0); the forward cuts each "
+                "query-tile pair's key range into the library's number of pieces (num_splits=0)"}
     del q, k, v, do
     # split-KV decode (HBM-bound): bytes of valid K/V + q + partials + o
     for Lq, causal in ((1, False), (16, True)):

@@ -480,18 +480,29 @@ __global__ void __launch_bounds__(320, 1)
           float acc[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-          for (int t = 0; t < pieces && m != -INFINITY; ++t) {
-            const float ls = __ldcg(p.lse_part + row0p + t * lstride);
-            if (ls == -INFINITY) continue;
-            const float w = expf(ls - m) * inv;
-            const float4* src = reinterpret_cast<const float4*>(p.o_part + (row0p + t * lstride) * p.dh + c * 32);
+          // two pieces a step, their 16 loads in flight together
+          for (int t0 = 0; t0 < pieces && m != -INFINITY; t0 += 2) {
+            float w[2];
+            float4 v4[2][8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 v4 = __ldcg(src + i);
-              acc[4 * i] = fmaf(w, v4.x, acc[4 * i]);
-              acc[4 * i + 1] = fmaf(w, v4.y, acc[4 * i + 1]);
-              acc[4 * i + 2] = fmaf(w, v4.z, acc[4 * i + 2]);
-              acc[4 * i + 3] = fmaf(w, v4.w, acc[4 * i + 3]);
+            for (int u = 0; u < 2; ++u) {
+              const int t = t0 + u;
+              const float ls = t < pieces ? __ldcg(p.lse_part + row0p + t * lstride) : -INFINITY;
+              w[u] = ls == -INFINITY ? 0.f : expf(ls - m) * inv;
+              const float4* src = reinterpret_cast<const float4*>(p.o_part + (row0p + t * lstride) * p.dh + c * 32);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v4[u][i] = w[u] != 0.f ? __ldcg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              if (w[u] == 0.f) continue;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                acc[4 * i] = fmaf(w[u], v4[u][i].x, acc[4 * i]);
+                acc[4 * i + 1] = fmaf(w[u], v4[u][i].y, acc[4 * i + 1]);
+                acc[4 * i + 2] = fmaf(w[u], v4[u][i].z, acc[4 * i + 2]);
+                acc[4 * i + 3] = fmaf(w[u], v4[u][i].w, acc[4 * i + 3]);
+              }
             }
           }
           uint32_t pk[16];

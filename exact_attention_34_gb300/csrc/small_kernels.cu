@@ -1,7 +1,6 @@
 // HBM-bound helper kernels: the backward preprocess (delta = rowsum(dO * O)),
 // the log-sum-exp combine of split-KV partials and the per-block summary of
 // segment ids that lets the tensor-core kernels skip tiles.
-#include <algorithm>
 #include <climits>
 #include <cstring>
 #include <type_traits>
@@ -11,28 +10,13 @@
 namespace attn {
 namespace {
 
-// Eight consecutive elements: fetched as raw 16-byte words (one for 16-bit
-// types, two for float32) and widened to float32 only when used, so that a
-// thread can keep several rows' loads in flight in few registers.
 template <typename T>
-struct Raw8 {
-  uint4 w[sizeof(T) / 2];
-};
-
-template <typename T>
-__device__ __forceinline__ Raw8<T> load_raw8(const T* p) {
-  Raw8<T> r;
-#pragma unroll
-  for (int k = 0; k < static_cast<int>(sizeof(T) / 2); ++k) r.w[k] = reinterpret_cast<const uint4*>(p)[k];
-  return r;
-}
-
-template <typename T>
-__device__ __forceinline__ void unpack8(const Raw8<T>& r, float (&f)[8]);
+__device__ __forceinline__ void load8(const T* p, float (&f)[8]);
 
 template <>
-__device__ __forceinline__ void unpack8<__nv_bfloat16>(const Raw8<__nv_bfloat16>& r, float (&f)[8]) {
-  const uint32_t w[4] = {r.w[0].x, r.w[0].y, r.w[0].z, r.w[0].w};
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&f)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     f[2 * i] = __uint_as_float(w[i] << 16);
@@ -41,8 +25,9 @@ __device__ __forceinline__ void unpack8<__nv_bfloat16>(const Raw8<__nv_bfloat16>
 }
 
 template <>
-__device__ __forceinline__ void unpack8<__half>(const Raw8<__half>& r, float (&f)[8]) {
-  const uint32_t w[4] = {r.w[0].x, r.w[0].y, r.w[0].z, r.w[0].w};
+__device__ __forceinline__ void load8<__half>(const __half* p, float (&f)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     __half2 h;
@@ -54,81 +39,54 @@ __device__ __forceinline__ void unpack8<__half>(const Raw8<__half>& r, float (&f
 }
 
 template <>
-__device__ __forceinline__ void unpack8<float>(const Raw8<float>& r, float (&f)[8]) {
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    f[4 * k] = __uint_as_float(r.w[k].x);
-    f[4 * k + 1] = __uint_as_float(r.w[k].y);
-    f[4 * k + 2] = __uint_as_float(r.w[k].z);
-    f[4 * k + 3] = __uint_as_float(r.w[k].w);
-  }
+__device__ __forceinline__ void load8<float>(const float* p, float (&f)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
 // delta[b, h, i] = sum_c dO[b, i, h, c] * O[b, i, h, c]  (float32 accumulate).
-// The grid is 2-D: y walks the (b, h) pairs, x blocks of kRowsPerBlock padded
-// rows 0 <= i < Lq_pad of a pair.  D/8 threads share a row, each reducing 8
-// consecutive elements, and a thread takes kRowsPerThread rows a block-row
-// apart with all their loads issued before the first add, so that enough
-// bytes are in flight to stream HBM.  Optionally it also writes
-// lse2 = lse * log2(e) (+inf where lse = -inf, so that every recomputed
-// probability of such a row is 0), fills the pad rows Lq <= i < Lq_pad with
-// delta = 0 and lse2 = +inf, and zeroes the float32 dQ accumulator of the
-// atomic backward.
-constexpr int kPreThreads = 256;
-constexpr int kRowsPerThread = 4;
-
+// Rows are walked in the padded [B, Hq, Lq_pad] order of the outputs; D/8
+// threads share a row, each reducing 8 consecutive elements.  Optionally it
+// also writes lse2 = lse * log2(e) (+inf where lse = -inf, so that every
+// recomputed probability of such a row is 0), fills the pad rows
+// Lq <= i < Lq_pad with delta = 0 and lse2 = +inf, and zeroes the float32 dQ
+// accumulator of the atomic backward.
 template <typename T, int D>
-__global__ void __launch_bounds__(kPreThreads) bwd_preprocess_kernel(
-    const T* __restrict__ o, const T* __restrict__ dout, const float* __restrict__ lse, float* __restrict__ delta,
-    float* __restrict__ lse2, float* __restrict__ dq_acc, long n_bh, int Lq, int Lq_pad, int Hq) {
-  constexpr int kTPR = D / 8;                              // threads per row (a power of two)
-  constexpr int kRowStep = kPreThreads / kTPR;             // rows one pass of the block covers
-  const int part = static_cast<int>(threadIdx.x) % kTPR;
-  const long i0 = static_cast<long>(blockIdx.x) * kRowStep * kRowsPerThread + threadIdx.x / kTPR;
-  for (long bh = blockIdx.y; bh < n_bh; bh += gridDim.y) {
-    long b;  // bh = b * Hq + h, uniform across the block
-    if (n_bh <= 0x7fffffffL)
-      b = static_cast<unsigned>(bh) / static_cast<unsigned>(Hq);
-    else
-      b = bh / Hq;
-    const long h = bh - b * Hq;
-    Raw8<T> ra[kRowsPerThread], rg[kRowsPerThread];
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict__ o, const T* __restrict__ dout,
+                                                             const float* __restrict__ lse, float* __restrict__ delta,
+                                                             float* __restrict__ lse2, float* __restrict__ dq_acc,
+                                                             long n_rows_pad, int Lq, int Lq_pad, int Hq) {
+  constexpr int kTPR = D / 8;  // threads per row
+  const long tid = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long prow = tid / kTPR;  // (b * Hq + h) * Lq_pad + i
+  const int part = static_cast<int>(tid % kTPR);
+  const long bh = prow / Lq_pad;
+  const int i = static_cast<int>(prow % Lq_pad);
+  const long b = bh / Hq, h = bh % Hq;
+  const bool real = prow < n_rows_pad && i < Lq;
+  float acc = 0.f;
+  if (real) {
+    const long row = (b * Lq + i) * Hq + h;  // row of the [B, Lq, Hq, D] tensors
+    float a[8], g[8];
+    load8<T>(o + row * D + part * 8, a);
+    load8<T>(dout + row * D + part * 8, g);
 #pragma unroll
-    for (int k = 0; k < kRowsPerThread; ++k) {
-      const long i = i0 + k * kRowStep;
-      if (i < Lq) {
-        const long row = (b * Lq + i) * Hq + h;  // row of the [B, Lq, Hq, D] tensors
-        ra[k] = load_raw8<T>(o + row * D + part * 8);
-        rg[k] = load_raw8<T>(dout + row * D + part * 8);
-      }
+    for (int e = 0; e < 8; ++e) acc = fmaf(a[e], g[e], acc);
+    if (dq_acc != nullptr) {
+      float4* z = reinterpret_cast<float4*>(dq_acc + row * D + part * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+  }
 #pragma unroll
-    for (int k = 0; k < kRowsPerThread; ++k) {
-      const long i = i0 + k * kRowStep;
-      const bool real = i < Lq;
-      float acc = 0.f;
-      if (real) {
-        float a[8], g[8];
-        unpack8<T>(ra[k], a);
-        unpack8<T>(rg[k], g);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc = fmaf(a[e], g[e], acc);
-        if (dq_acc != nullptr) {
-          float4* z = reinterpret_cast<float4*>(dq_acc + ((b * Lq + i) * Hq + h) * D + part * 8);
-          z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-          z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-#pragma unroll
-      for (int off = kTPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (i < Lq_pad && part == 0) {
-        const long prow = bh * Lq_pad + i;
-        delta[prow] = acc;  // 0 on pad rows
-        if (lse2 != nullptr) {
-          const float l = real ? lse[bh * Lq + i] : -INFINITY;
-          lse2[prow] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
-        }
-      }
+  for (int off = kTPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (prow < n_rows_pad && part == 0) {
+    delta[prow] = acc;  // 0 on pad rows
+    if (lse2 != nullptr) {
+      const float l = real ? lse[bh * Lq + i] : -INFINITY;
+      lse2[prow] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
     }
   }
 }
@@ -281,13 +239,12 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const float* __restrict
 
 template <typename T, int D>
 cudaError_t run_preprocess(const PreprocessArgs& a, cudaStream_t s) {
-  const long n_bh = static_cast<long>(a.B) * a.Hq;
-  const long rows_per_block = static_cast<long>(kPreThreads / (D / 8)) * kRowsPerThread;
-  const dim3 grid(static_cast<unsigned>((a.Lq_pad + rows_per_block - 1) / rows_per_block),
-                  static_cast<unsigned>(std::min(n_bh, 65535L)));
+  const long n_rows = static_cast<long>(a.B) * a.Hq * a.Lq_pad;
+  const long threads = n_rows * (D / 8);
+  const int blocks = static_cast<int>((threads + 255) / 256);
   KernelTimer kt("bwd_preprocess", s);
-  bwd_preprocess_kernel<T, D><<<grid, kPreThreads, 0, s>>>(static_cast<const T*>(a.o), static_cast<const T*>(a.dout),
-                                                   a.lse, a.delta, a.lse2, a.dq_acc, n_bh, a.Lq, a.Lq_pad, a.Hq);
+  bwd_preprocess_kernel<T, D><<<blocks, 256, 0, s>>>(static_cast<const T*>(a.o), static_cast<const T*>(a.dout),
+                                                     a.lse, a.delta, a.lse2, a.dq_acc, n_rows, a.Lq, a.Lq_pad, a.Hq);
   return cudaGetLastError();
 }
 
