@@ -514,21 +514,32 @@ __global__ void __launch_bounds__(256) f32_bwd_dkdv_kernel(const F32BwdParams p)
   }
 }
 
-// dQ for one 64-row query tile: loops over the key tiles it sees.
+// dQ for one 64-row query tile: loops over the key tiles it sees.  At
+// head_dim >= 64 (as in the forward) tiles are read with 16-byte shared loads
+// (rows padded by kPadV) and the K/V tiles are double-buffered: tile j+1 is
+// copied asynchronously while tile j is computed.
 template <int D>
 __global__ void __launch_bounds__(256) f32_bwd_dq_kernel(const F32BwdParams p) {
+  constexpr bool kVec = D >= 64;
+  constexpr int kP = kVec ? kPadV : kPad;
+  constexpr int kBufs = kVec ? 2 : 1;
   extern __shared__ float sm[];
   float* Qs = sm;
-  float* dOs = Qs + kT * (D + kPad);
-  float* Ks = dOs + kT * (D + kPad);
-  float* Vs = Ks + kT * (D + kPad);
-  float* dSs = Vs + kT * (D + kPad);  // [query][key]
+  float* dOs = Qs + kT * (D + kP);
+  float* Kb = dOs + kT * (D + kP);
+  float* Vb = Kb + kBufs * kT * (D + kP);
+  float* dSs = Vb + kBufs * kT * (D + kP);  // [query][key]
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int q0 = blockIdx.x * kT, h = blockIdx.y, b = blockIdx.z;
   const int hk = h / p.G;
   const int kvl = seq_len_of(p.kv_lens, b, p.Lkv);
-  load_tile<D>(Qs, p.q, b, q0, h, p.Lq, p.Hq);
-  load_tile<D>(dOs, p.dout, b, q0, h, p.Lq, p.Hq);
+  if (kVec) {
+    load_tile_v<D>(Qs, p.q, b, q0, h, p.Lq, p.Hq);
+    load_tile_v<D>(dOs, p.dout, b, q0, h, p.Lq, p.Hq);
+  } else {
+    load_tile<D>(Qs, p.q, b, q0, h, p.Lq, p.Hq);
+    load_tile<D>(dOs, p.dout, b, q0, h, p.Lq, p.Hq);
+  }
   float l2[4], dl[4];
   int klo[4], khi[4], qseg[4];
   const bool seg = p.q_seg != nullptr;
@@ -551,14 +562,41 @@ __global__ void __launch_bounds__(256) f32_bwd_dq_kernel(const F32BwdParams p) {
   const int last_row = min(q0 + kT - 1, p.Lq - 1);
   const int hi_all = key_span(last_row, p.Lq, kvl, p.wl, p.wr).hi;
   const int lo_all = key_span(min(q0, p.Lq - 1), p.Lq, kvl, p.wl, p.wr).lo;
-  for (int j0 = (lo_all / kT) * kT; j0 < hi_all; j0 += kT) {
-    __syncthreads();
-    load_tile<D>(Ks, p.k, b, j0, hk, p.Lkv, p.Hkv);
-    load_tile<D>(Vs, p.v, b, j0, hk, p.Lkv, p.Hkv);
-    __syncthreads();
+  const int j_start = (lo_all / kT) * kT;
+  auto issue_kv = [&](int j, int buf) {
+    load_tile_async<D>(Kb + buf * kT * (D + kP), p.k, b, j, hk, p.Lkv, p.Hkv);
+    load_tile_async<D>(Vb + buf * kT * (D + kP), p.v, b, j, hk, p.Lkv, p.Hkv);
+    async_commit();
+  };
+  if (kVec && j_start < hi_all) issue_kv(j_start, 0);
+  for (int j0 = j_start, it = 0; j0 < hi_all; j0 += kT, ++it) {
+    const int buf = kVec ? (it & 1) : 0;
+    float* Ks = Kb + buf * kT * (D + kP);
+    float* Vs = Vb + buf * kT * (D + kP);
+    if (kVec) {
+      // buffer buf ^ 1 was last read in the previous iteration, which every
+      // thread has left (barrier at its end)
+      if (j0 + kT < hi_all) {
+        issue_kv(j0 + kT, buf ^ 1);
+        async_wait<1>();
+      } else {
+        async_wait<0>();
+      }
+      __syncthreads();
+    } else {
+      __syncthreads();
+      load_tile<D>(Ks, p.k, b, j0, hk, p.Lkv, p.Hkv);
+      load_tile<D>(Vs, p.v, b, j0, hk, p.Lkv, p.Hkv);
+      __syncthreads();
+    }
     float s[4][4], dp[4][4];
-    tile_dot<D>(Qs, Ks, ty, tx, s);
-    tile_dot<D>(dOs, Vs, ty, tx, dp);
+    if (kVec) {
+      tile_dot_v<D>(Qs, Ks, ty, tx, s);
+      tile_dot_v<D>(dOs, Vs, ty, tx, dp);
+    } else {
+      tile_dot<D>(Qs, Ks, ty, tx, s);
+      tile_dot<D>(dOs, Vs, ty, tx, dp);
+    }
     int kseg[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -572,18 +610,31 @@ __global__ void __launch_bounds__(256) f32_bwd_dq_kernel(const F32BwdParams p) {
         const int j = j0 + tx + 16 * c;
         const bool ok = j >= klo[a] && j < khi[a] && (!seg || kseg[c] == qseg[a]);
         const float pv = ok ? ex2_approx(fmaf(s[a][c], p.scale_log2, -l2[a])) : 0.f;
-        dSs[(4 * ty + a) * (kT + kPad) + tx + 16 * c] = pv * (dp[a][c] - dl[a]);
+        dSs[(4 * ty + a) * (kT + kP) + tx + 16 * c] = pv * (dp[a][c] - dl[a]);
       }
     __syncthreads();
-    tile_pv<D>(dSs, Ks, ty, tx, acc);
+    if (kVec) {
+      tile_pv_v<D>(dSs, Ks, ty, tx, acc);
+      __syncthreads();  // dSs, Ks and Vs are rewritten next iteration
+    } else {
+      tile_pv<D>(dSs, Ks, ty, tx, acc);
+    }
   }
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
     const int i = q0 + 4 * ty + a;
     if (i >= p.Lq) continue;
     float* dst = p.dq + ((static_cast<size_t>(b) * p.Lq + i) * p.Hq + h) * D;
+    if (kVec) {  // columns 4*tx + 64*g + e
 #pragma unroll
-    for (int e = 0; e < D / 16; ++e) dst[tx + 16 * e] = acc[a][e] * p.scale;
+      for (int g = 0; g < D / 64; ++g)
+        *reinterpret_cast<float4*>(dst + 4 * tx + 64 * g) =
+            make_float4(acc[a][4 * g] * p.scale, acc[a][4 * g + 1] * p.scale, acc[a][4 * g + 2] * p.scale,
+                        acc[a][4 * g + 3] * p.scale);
+    } else {  // columns tx + 16*e
+#pragma unroll
+      for (int e = 0; e < D / 16; ++e) dst[tx + 16 * e] = acc[a][e] * p.scale;
+    }
   }
 }
 
@@ -605,7 +656,9 @@ constexpr int dkdv_smem() {
 }
 template <int D>
 constexpr int dq_smem() {
-  return (4 * kT * (D + kPad) + kT * (kT + kPad)) * 4;
+  constexpr int kP = D >= 64 ? kPadV : kPad;
+  constexpr int kBufs = D >= 64 ? 2 : 1;
+  return ((2 + 2 * kBufs) * kT * (D + kP) + kT * (kT + kP)) * 4;
 }
 
 template <int D>
