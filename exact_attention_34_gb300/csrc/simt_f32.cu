@@ -385,15 +385,21 @@ struct F32BwdParams {
 
 // Recompute P and dS for one (query tile, key tile) pair in "key-major" form:
 // element [a][c] is key 4*ty + a (of the key tile) and query tx + 16*c.
-template <int D>
+// kVec: tiles with rows padded by kPadV, read with 16-byte loads.
+template <int D, bool kVec = false>
 __device__ __forceinline__ void kt_probs(const float* Ks, const float* Vs, const float* Qs, const float* dOs,
                                          const float* lse2_s, const float* delta_s, const int* klo_s,
                                          const int* khi_s, const int* qseg_s, const int (&kseg)[4], bool seg,
                                          int j0, int ty,
                                          int tx, float scale_log2, float (&P)[4][4], float (&dS)[4][4]) {
   float s[4][4], dp[4][4];
-  tile_dot<D>(Ks, Qs, ty, tx, s);
-  tile_dot<D>(Vs, dOs, ty, tx, dp);
+  if constexpr (kVec) {
+    tile_dot_v<D>(Ks, Qs, ty, tx, s);
+    tile_dot_v<D>(Vs, dOs, ty, tx, dp);
+  } else {
+    tile_dot<D>(Ks, Qs, ty, tx, s);
+    tile_dot<D>(Vs, dOs, ty, tx, dp);
+  }
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const int qi = tx + 16 * c;
@@ -510,6 +516,128 @@ __global__ void __launch_bounds__(256) f32_bwd_dkdv_kernel(const F32BwdParams p)
     for (int e = 0; e < D / 16; ++e) {
       p.dk[off + tx + 16 * e] = dk[a][e] * p.scale;
       p.dv[off + tx + 16 * e] = dv[a][e];
+    }
+  }
+}
+
+// Row data of query tile q0 of head h for the dK/dV pass, one query row per
+// thread threadIdx.x < kT: log2-domain LSE, delta, the row's key span (empty
+// for rows past Lq or without a valid key) and its segment id.
+__device__ __forceinline__ void dkdv_row_data(const F32BwdParams& p, int b, int h, int q0, int kvl, bool seg,
+                                              float* lse2_s, float* delta_s, int* klo_s, int* khi_s, int* qseg_s) {
+  if (threadIdx.x < kT) {
+    const int i = q0 + threadIdx.x;
+    const bool in = i < p.Lq;
+    const float ls = in ? p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Lq + i] : -INFINITY;
+    lse2_s[threadIdx.x] = ls * kLog2e;
+    delta_s[threadIdx.x] = in ? p.delta[(static_cast<size_t>(b) * p.Hq + h) * p.Lq + i] : 0.f;
+    const Span ks = key_span(i, p.Lq, kvl, p.wl, p.wr);
+    const bool any = in && ls != -INFINITY;
+    klo_s[threadIdx.x] = any ? ks.lo : 0;
+    khi_s[threadIdx.x] = any ? ks.hi : 0;
+    qseg_s[threadIdx.x] = (seg && in) ? p.q_seg[static_cast<size_t>(b) * p.Lq + i] : 0;
+  }
+}
+
+// dK/dV of the deterministic backward at head_dim >= 64: the steps of
+// f32_bwd_dkdv_kernel (G heads x the query tiles that see the key tile, in
+// that order) with tiles read by 16-byte shared loads (rows padded by kPadV)
+// and each step's Q, dO and row data double-buffered: step s+1's copies run
+// asynchronously while step s computes.  P and dS take turns in one shared
+// tile (dV += P^T dO first, then dK += dS^T Q).
+template <int D>
+__global__ void __launch_bounds__(256) f32_bwd_dkdv_v_kernel(const F32BwdParams p) {
+  constexpr int kRow = D + kPadV;
+  extern __shared__ float sm[];
+  float* Ks = sm;
+  float* Vs = Ks + kT * kRow;
+  float* Qb = Vs + kT * kRow;         // [2][kT][kRow]
+  float* dOb = Qb + 2 * kT * kRow;    // [2][kT][kRow]
+  float* PdS = dOb + 2 * kT * kRow;   // [key][query], rows of kT + kPadV
+  float* meta = PdS + kT * (kT + kPadV);  // [2] x {lse2, delta, klo, khi, qseg} x kT
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int j0 = blockIdx.x * kT, hk = blockIdx.y, b = blockIdx.z;
+  const int kvl = seq_len_of(p.kv_lens, b, p.Lkv);
+  const bool seg = p.q_seg != nullptr;
+  int kseg[4];  // segment ids of this thread's 4 keys
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int j = j0 + 4 * ty + a;
+    kseg[a] = (seg && j < p.Lkv) ? p.kv_seg[static_cast<size_t>(b) * p.Lkv + j] : 0;
+  }
+  float dk[4][D / 16], dv[4][D / 16];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int e = 0; e < D / 16; ++e) dk[a][e] = dv[a][e] = 0.f;
+  if (j0 < kvl) {
+    load_tile_v<D>(Ks, p.k, b, j0, hk, p.Lkv, p.Hkv);
+    load_tile_v<D>(Vs, p.v, b, j0, hk, p.Lkv, p.Hkv);
+    // rows that see some key of this tile: [q_first, q_end)
+    const int q_first = query_span(j0, p.Lq, kvl, p.wl, p.wr).lo;
+    const int q_end = query_span(min(j0 + kT, kvl) - 1, p.Lq, kvl, p.wl, p.wr).hi;
+    const int qt0 = (q_first / kT) * kT;
+    const int n_qt = q_end > qt0 ? (q_end - qt0 + kT - 1) / kT : 0;
+    const int n_steps = n_qt * p.G;
+    auto row_data = [&](int buf) { return meta + buf * 5 * kT; };
+    // copies of step `step` into buffer `buf`: Q and dO asynchronously, the
+    // row data directly (made visible by the barrier that precedes its use)
+    auto issue = [&](int step, int buf) {
+      const int h = hk * p.G + step / n_qt, q0 = qt0 + (step % n_qt) * kT;
+      load_tile_async<D>(Qb + buf * kT * kRow, p.q, b, q0, h, p.Lq, p.Hq);
+      load_tile_async<D>(dOb + buf * kT * kRow, p.dout, b, q0, h, p.Lq, p.Hq);
+      async_commit();
+      float* m = row_data(buf);
+      dkdv_row_data(p, b, h, q0, kvl, seg, m, m + kT, reinterpret_cast<int*>(m + 2 * kT),
+                    reinterpret_cast<int*>(m + 3 * kT), reinterpret_cast<int*>(m + 4 * kT));
+    };
+    if (n_steps > 0) issue(0, 0);
+    for (int step = 0; step < n_steps; ++step) {
+      const int buf = step & 1;
+      // buffer buf ^ 1 was last read in the previous step, which every thread
+      // has left (barrier at its end)
+      if (step + 1 < n_steps) {
+        issue(step + 1, buf ^ 1);
+        async_wait<1>();
+      } else {
+        async_wait<0>();
+      }
+      __syncthreads();
+      const float* Qs = Qb + buf * kT * kRow;
+      const float* dOs = dOb + buf * kT * kRow;
+      const float* m = row_data(buf);
+      float P[4][4], dS[4][4];
+      kt_probs<D, true>(Ks, Vs, Qs, dOs, m, m + kT, reinterpret_cast<const int*>(m + 2 * kT),
+                        reinterpret_cast<const int*>(m + 3 * kT), reinterpret_cast<const int*>(m + 4 * kT), kseg, seg,
+                        j0, ty, tx, p.scale_log2, P, dS);
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) PdS[(4 * ty + a) * (kT + kPadV) + tx + 16 * c] = P[a][c];
+      __syncthreads();
+      tile_pv_v<D>(PdS, dOs, ty, tx, dv);
+      __syncthreads();
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) PdS[(4 * ty + a) * (kT + kPadV) + tx + 16 * c] = dS[a][c];
+      __syncthreads();
+      tile_pv_v<D>(PdS, Qs, ty, tx, dk);
+      __syncthreads();  // PdS and this step's buffers are rewritten next step
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int j = j0 + 4 * ty + a;
+    if (j >= p.Lkv) continue;
+    const size_t off = ((static_cast<size_t>(b) * p.Lkv + j) * p.Hkv + hk) * D;
+#pragma unroll
+    for (int g = 0; g < D / 64; ++g) {  // columns 4*tx + 64*g + e
+      *reinterpret_cast<float4*>(p.dk + off + 4 * tx + 64 * g) =
+          make_float4(dk[a][4 * g] * p.scale, dk[a][4 * g + 1] * p.scale, dk[a][4 * g + 2] * p.scale,
+                      dk[a][4 * g + 3] * p.scale);
+      *reinterpret_cast<float4*>(p.dv + off + 4 * tx + 64 * g) =
+          make_float4(dv[a][4 * g], dv[a][4 * g + 1], dv[a][4 * g + 2], dv[a][4 * g + 3]);
     }
   }
 }
@@ -655,6 +783,10 @@ constexpr int dkdv_smem() {
   return (4 * kT * (D + kPad) + 2 * kT * (kT + kPad) + 5 * kT) * 4;  // + lse2, delta, span lo/hi, segment ids
 }
 template <int D>
+constexpr int dkdv_v_smem() {
+  return (6 * kT * (D + kPadV) + kT * (kT + kPadV) + 2 * 5 * kT) * 4;
+}
+template <int D>
 constexpr int dq_smem() {
   constexpr int kP = D >= 64 ? kPadV : kPad;
   constexpr int kBufs = D >= 64 ? 2 : 1;
@@ -675,10 +807,20 @@ cudaError_t run_fwd(const F32FwdParams& p, int splits, cudaStream_t s) {
 
 template <int D>
 cudaError_t run_bwd(const F32BwdParams& p, bool atomic_dq, cudaStream_t s) {
-  cudaError_t e = ensure_dynamic_smem<f32_bwd_dkdv_kernel<D>>(dkdv_smem<D>());
-  if (e != cudaSuccess) return e;
   dim3 g1((p.Lkv + kT - 1) / kT, p.Hkv, p.B);
-  {
+  cudaError_t e;
+  bool vec = false;
+  if constexpr (D >= 64) vec = !atomic_dq;
+  if (vec) {  // 16-byte loads, double-buffered query tiles
+    if constexpr (D >= 64) {
+      e = ensure_dynamic_smem<f32_bwd_dkdv_v_kernel<D>>(dkdv_v_smem<D>());
+      if (e != cudaSuccess) return e;
+      KernelTimer kt("bwd_dkdv_f32", s);
+      f32_bwd_dkdv_v_kernel<D><<<g1, 256, dkdv_v_smem<D>(), s>>>(p);
+    }
+  } else {
+    e = ensure_dynamic_smem<f32_bwd_dkdv_kernel<D>>(dkdv_smem<D>());
+    if (e != cudaSuccess) return e;
     KernelTimer kt("bwd_dkdv_f32", s);
     f32_bwd_dkdv_kernel<D><<<g1, 256, dkdv_smem<D>(), s>>>(p);
   }
