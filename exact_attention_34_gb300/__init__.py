@@ -140,15 +140,17 @@ def _dtype(t) -> int:
 
 def _dims(q, k, v=None):
     """(B, Lq, Lkv, Hq, Hkv, d) of q [B, Lq, Hq, d] and k (and v) [B, Lkv, Hkv, d]."""
-    if q.dim() != 4 or k.dim() != 4:
+    qs, ks = q.shape, k.shape
+    if len(qs) != 4 or len(ks) != 4:
         raise ValueError("q and k must be [batch, seq, heads, head_dim]")
-    B, Lq, Hq, d = q.shape
-    Lkv, Hkv = k.shape[1], k.shape[2]
-    if k.shape[0] != B or k.shape[3] != d:
-        raise ValueError(f"k {tuple(k.shape)} does not match q {tuple(q.shape)} in batch or head_dim")
-    if v is not None and v.shape != k.shape:
-        raise ValueError(f"v {tuple(v.shape)} must have k's shape {tuple(k.shape)}")
-    if k.dtype != q.dtype or (v is not None and v.dtype != q.dtype):
+    B, Lq, Hq, d = qs
+    kB, Lkv, Hkv, kd = ks
+    if kB != B or kd != d:
+        raise ValueError(f"k {tuple(ks)} does not match q {tuple(qs)} in batch or head_dim")
+    dt = q.dtype
+    if v is not None and (v.shape != ks or v.dtype != dt):
+        raise ValueError(f"v {tuple(v.shape)} {v.dtype} must have k's shape {tuple(ks)} and q's dtype")
+    if k.dtype != dt:
         raise TypeError("q, k and v must share one dtype")
     if Hkv == 0 or Hq % Hkv != 0:
         raise ValueError(f"query heads {Hq} must be a multiple of KV heads {Hkv}")
