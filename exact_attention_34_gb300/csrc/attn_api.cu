@@ -713,10 +713,10 @@ attn_status attn_device_status(int* code, int* site, int reset) {
 // Backward without any device allocation by the caller.
 //
 // Some callers cannot allocate device memory at the point where they need the
-// backward: code running while a CUDA graph is being captured (cudaMalloc is
-// not allowed inside most capture modes), hosts whose device memory is owned by
-// a fixed pool or another runtime's allocator, and plugin or interpreter
-// embeddings that hand the library only the tensors they already own.  For
+// backward: hosts whose device memory is owned by a fixed pool or another
+// runtime's allocator, latency-critical loops that must not take cudaMalloc's
+// implicit device synchronisation, and plugin or interpreter embeddings that
+// hand the library only the tensors they already own.  For
 // them the deterministic backward's scratch (delta and lse*log2(e), one float
 // each per padded query row) lives in a file-scope device array instead of a
 // caller workspace.  Every GPU that loads this library holds the array until

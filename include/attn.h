@@ -310,9 +310,9 @@ attn_status attn_timing_query(const char* kernel, double* total_ms, int* launche
  * and results as attn_bwd with deterministic = 1, minus the workspace.
  *
  * For callers that cannot allocate device memory where they run the backward:
- * during CUDA graph capture, inside hosts whose device memory belongs to a fixed
- * pool or another runtime, or in embeddings that only hand over existing
- * tensors.  The scratch (two floats per padded query row) lives in a 4 MiB
+ * hosts whose device memory belongs to a fixed pool or another runtime's
+ * allocator, latency-critical loops that must not take cudaMalloc's implicit
+ * device synchronisation, or embeddings that only hand over existing tensors.  The scratch (two floats per padded query row) lives in a 4 MiB
  * device array inside the library, held by every GPU that loads it until the
  * process exits.  Limit: B * Hq * roundup(Lq, 128) <= 524288 (e.g. B4 H8
  * Lq16384); larger problems return ATTN_ERR_WORKSPACE with a message.
