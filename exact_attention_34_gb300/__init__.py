@@ -148,9 +148,9 @@ def _dims(q, k, v=None):
     if kB != B or kd != d:
         raise ValueError(f"k {tuple(ks)} does not match q {tuple(qs)} in batch or head_dim")
     dt = q.dtype
-    if v is not None and (v.shape != ks or v.dtype != dt):
-        raise ValueError(f"v {tuple(v.shape)} {v.dtype} must have k's shape {tuple(ks)} and q's dtype")
-    if k.dtype != dt:
+    if v is not None and v.shape != ks:
+        raise ValueError(f"v {tuple(v.shape)} must have k's shape {tuple(ks)}")
+    if k.dtype != dt or (v is not None and v.dtype != dt):
         raise TypeError("q, k and v must share one dtype")
     if Hkv == 0 or Hq % Hkv != 0:
         raise ValueError(f"query heads {Hq} must be a multiple of KV heads {Hkv}")

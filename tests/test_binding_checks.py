@@ -27,6 +27,8 @@ def test_shape_and_dtype_mismatches_are_refused():
         ea._dims(q, k, torch.zeros(1, 100, 2, 64, dtype=q.dtype))
     with pytest.raises(TypeError, match="one dtype"):
         ea._dims(q, k.float(), v)
+    with pytest.raises(TypeError, match="one dtype"):
+        ea._dims(q, k, v.float())
     with pytest.raises(ValueError, match="multiple of KV heads"):
         ea._dims(torch.zeros(1, 128, 3, 64), torch.zeros(1, 128, 2, 64))
     with pytest.raises(ValueError, match="head_dim"):
