@@ -530,22 +530,66 @@ def other_rows(args, dev, peaks):
     del q, k, v, do
     # split-KV decode (HBM-bound): bytes of valid K/V + q + partials + o
     for Lq, causal in ((1, False), (16, True)):
-        p = W.decode(Lq, causal)
-        q = torch.randn(p.B, p.Lq, p.Hq, p.d, device=dev, generator=g).to(torch.bfloat16)
-        k = torch.randn(p.B, p.Lkv, p.Hkv, p.d, device=dev, generator=g).to(torch.bfloat16)
-        v = torch.randn_like(k)
-        kl = torch.tensor(p.kv_lens, dtype=torch.int32, device=dev)
-        S = ea.attn_decode_num_splits(p.B, p.Lq, p.Lkv, p.Hq, p.Hkv, p.d)
-        ms = timed(lambda: ea.decode(q, k, v, causal=causal, kv_lens=kl, num_splits=S))
-        kv_bytes = sum(p.kv_lens) * p.Hkv * p.d * 2 * 2
-        part_bytes = 2 * p.B * p.Hq * S * p.Lq * (p.d + 1) * 4
-        io_bytes = 2 * p.B * p.Lq * p.Hq * p.d * 2 + p.B * p.Hq * p.Lq * 4
-        gbs = (kv_bytes + part_bytes + io_bytes) / (ms * 1e-3) / 1e9
-        out[f"decode_Lq{Lq}"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
-                                 "num_splits": S}
-        del q, k, v
+        out[f"decode_Lq{Lq}"] = decode_row(dev, g, peaks, timed, Lq, causal)
     torch.cuda.empty_cache()
     return out
+
+
+def decode_row(dev, g, peaks, timed, Lq, causal, Lkv=131072):
+    """One split-KV decode row (B8 Hq32 Hkv8 d128 bf16, KV lengths uniform in
+    [4096, Lkv]): decode + combine time, and GB/s over the algorithmic bytes
+    (K and V of the valid keys, q, o, lse and the fp32 partials written and
+    read once)."""
+    import torch
+
+    import exact_attention_34_gb300 as ea
+
+    p = W.decode(Lq, causal, Lkv=Lkv)
+    q = torch.randn(p.B, p.Lq, p.Hq, p.d, device=dev, generator=g).to(torch.bfloat16)
+    k = torch.randn(p.B, p.Lkv, p.Hkv, p.d, device=dev, generator=g).to(torch.bfloat16)
+    v = torch.randn_like(k)
+    kl = torch.tensor(p.kv_lens, dtype=torch.int32, device=dev)
+    S = ea.attn_decode_num_splits(p.B, p.Lq, p.Lkv, p.Hq, p.Hkv, p.d)
+    ms = timed(lambda: ea.decode(q, k, v, causal=causal, kv_lens=kl, num_splits=S))
+    kv_bytes = sum(p.kv_lens) * p.Hkv * p.d * 2 * 2
+    part_bytes = 2 * p.B * p.Hq * S * p.Lq * (p.d + 1) * 4
+    io_bytes = 2 * p.B * p.Lq * p.Hq * p.d * 2 + p.B * p.Hq * p.Lq * 4
+    gbs = (kv_bytes + part_bytes + io_bytes) / (ms * 1e-3) / 1e9
+    del q, k, v
+    return {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+            "num_splits": S, "bytes": kv_bytes + part_bytes + io_bytes}
+
+
+def run_decode_suite(args):
+    """The split-KV decode rows alone ("Attention performance", section
+    "Grouped-query attention and decoding"): Lq = 1 and Lq = 16 with the causal
+    offset, B8 Hq32 Hkv8 d128 bf16, cache length --decode-lkv (lengths uniform
+    in [4096, that]).  One JSON line per row; a short cache keeps an ncu
+    capture to about a GB of device memory."""
+    import torch
+
+    from exact_attention_34_gb300 import build as eb
+
+    eb.build()
+    dev = torch.device("cuda", 0)
+    peaks = measured_peaks()
+
+    def timed(fn, n=max(3, args.steps)):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    for Lq, causal in ((1, False), (16, True)):
+        g = torch.Generator(device=dev).manual_seed(0)
+        row = decode_row(dev, g, peaks, timed, Lq, causal, Lkv=args.decode_lkv)
+        print(json.dumps({"suite": "decode", "Lq": Lq, "causal": causal, "Lkv": args.decode_lkv, **row}), flush=True)
 
 
 # ----------------------------------------------------------------------------
@@ -864,7 +908,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the other rows (KVLen+GQA, decode)")
     ap.add_argument("--sweep", action="store_true", help="print the attention grid (one JSON line per case) and exit")
-    ap.add_argument("--suite", choices=("gqa", "memory"), help="print the GQA or the memory suite and exit")
+    ap.add_argument("--suite", choices=("gqa", "memory", "decode"),
+                    help="print the GQA, the memory or the decode suite and exit")
+    ap.add_argument("--decode-lkv", type=int, default=131072, help="cache length of --suite decode")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
@@ -872,7 +918,7 @@ def main(argv=None):
         run_sweep(args)
         return
     if args.suite:
-        (run_gqa_suite if args.suite == "gqa" else run_memory_suite)(args)
+        {"gqa": run_gqa_suite, "memory": run_memory_suite, "decode": run_decode_suite}[args.suite](args)
         return
     rank, _, world = dist_env()
     if args.gpus != world and world > 1:
