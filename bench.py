@@ -693,6 +693,41 @@ def run_reference(args):
     }
 
 
+def sweep_key(T, d, causal, dtype):
+    """Identity of one case of the attention grid."""
+    return (int(T), int(d), bool(causal), str(dtype))
+
+
+def sweep_done_keys(path):
+    """Keys of the cases already recorded in an --append file: one JSON object
+    per line; a line cut short by a killed run (not valid JSON) is ignored, so
+    that case runs again."""
+    done = set()
+    if not path or not os.path.exists(path):
+        return done
+    with open(path) as f:
+        for line in f:
+            try:
+                r = json.loads(line)
+                done.add(sweep_key(r["T"], r["d"], r["causal"], r["dtype"]))
+            except (ValueError, KeyError, TypeError):
+                continue
+    return done
+
+
+def sweep_end_partial_line(path):
+    """Terminate a last line cut short by a killed run, so the next appended
+    line starts on a line of its own."""
+    if not path or not os.path.exists(path) or os.path.getsize(path) == 0:
+        return
+    with open(path, "rb") as f:
+        f.seek(-1, os.SEEK_END)
+        last = f.read(1)
+    if last != b"\n":
+        with open(path, "a") as f:
+            f.write("\n")
+
+
 def run_sweep(args):
     """The pages' attention grid ("Attention performance", section "Time"): B4 H8,
     d in {64, 128}, T in {128 ... 8192} plus the ragged 600 / 1500 / 3000, causal
@@ -701,7 +736,9 @@ def run_sweep(args):
     (bf16) and fp32 at d=128 for T <= 2048.  Each case is timed twice: as eager
     calls (host work of every call included: the Python binding, tensor-map
     encoding and launches) and as replays of a CUDA graph that captured the
-    same calls (device time; what a compiled training step sees)."""
+    same calls (device time; what a compiled training step sees).  With
+    --append FILE each finished case is also appended to FILE, and cases
+    already there are skipped, so a killed sweep resumes where it stopped."""
     import torch
 
     import exact_attention_34_gb300 as ea
@@ -743,6 +780,9 @@ def run_sweep(args):
     cases = [(T, d, c, "bf16") for d in (64, 128) for T in W.GRID_T + W.RAGGED_T for c in (False, True)]
     cases += [(T, 32, c, "bf16") for T in W.GRID_T for c in (False, True)]  # head_dim 32 (runs as 64)
     cases += [(T, 128, c, "fp32") for T in (128, 512, 1024, 2048) for c in (False, True)]
+    done = sweep_done_keys(args.append)
+    sweep_end_partial_line(args.append)
+    cases = [cs for cs in cases if sweep_key(*cs) not in done]
     for T, d, c, dt in cases:
         p = W.grid(T, d, c, dt)
         g = torch.Generator(device=dev).manual_seed(0)
@@ -760,14 +800,18 @@ def run_sweep(args):
         gf = graph_timed(fwd_call, n)
         gb = graph_timed(fwd_bwd_call, n)
         F = W.fwd_flops(p)
-        print(json.dumps({"T": T, "d": d, "causal": c, "dtype": dt, "fwd_ms": round(qf[1], 4),
+        line = json.dumps({"T": T, "d": d, "causal": c, "dtype": dt, "fwd_ms": round(qf[1], 4),
                           "fwd_ms_q1_q3": [round(qf[0], 4), round(qf[2], 4)],
                           "fwd_tflops": round(F / qf[1] / 1e9, 1), "fwd_bwd_ms": round(qb[1], 4),
                           "fwd_bwd_ms_q1_q3": [round(qb[0], 4), round(qb[2], 4)],
                           "fwd_bwd_tflops": round(3.5 * F / qb[1] / 1e9, 1),
                           "graph_fwd_ms": round(gf[1], 4), "graph_fwd_tflops": round(F / gf[1] / 1e9, 1),
                           "graph_fwd_bwd_ms": round(gb[1], 4),
-                          "graph_fwd_bwd_tflops": round(3.5 * F / gb[1] / 1e9, 1)}), flush=True)
+                          "graph_fwd_bwd_tflops": round(3.5 * F / gb[1] / 1e9, 1)})
+        print(line, flush=True)
+        if args.append:  # one line per finished case: a killed sweep resumes after it
+            with open(args.append, "a") as f:
+                f.write(line + "\n")
 
 
 def _timed_q(fn, n, repeats=5):
@@ -908,6 +952,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the other rows (KVLen+GQA, decode)")
     ap.add_argument("--sweep", action="store_true", help="print the attention grid (one JSON line per case) and exit")
+    ap.add_argument("--append", default=None,
+                    help="with --sweep: also append each case's line to this file and skip cases already in it")
     ap.add_argument("--suite", choices=("gqa", "memory", "decode"),
                     help="print the GQA, the memory or the decode suite and exit")
     ap.add_argument("--decode-lkv", type=int, default=131072, help="cache length of --suite decode")

@@ -79,3 +79,23 @@ def test_oracle_sampler_counts_causal_pairs():
     assert s.flops(rows) == 3.5 * 4 * 128 * (1 + 4096 + 8192)
     assert s.run((2, rows)) == 2 * s.flops(rows)
     assert "2 of 32" in s.describe((2, rows))
+
+
+def test_sweep_append_file_resumes_after_a_killed_run(tmp_path):
+    """Cases recorded in an --append file are skipped; a last line cut short
+    by a killed run does not count, so that case runs again."""
+    path = tmp_path / "sweep.jsonl"
+    assert bench.sweep_done_keys(str(path)) == set()
+    assert bench.sweep_done_keys(None) == set()
+    path.write_text('{"T": 128, "d": 64, "causal": false, "dtype": "bf16", "fwd_ms": 0.01}\n'
+                    '{"T": 8192, "d": 128, "causal": true, "dtype": "fp32", "fwd_ms": 9.0}\n'
+                    '{"T": 512, "d": 128, "causal": tr')
+    done = bench.sweep_done_keys(str(path))
+    assert done == {bench.sweep_key(128, 64, False, "bf16"), bench.sweep_key(8192, 128, True, "fp32")}
+    assert bench.sweep_key(512, 128, True, "bf16") not in done
+    bench.sweep_end_partial_line(str(path))
+    with open(path, "a") as f:
+        f.write('{"T": 512, "d": 128, "causal": true, "dtype": "bf16", "fwd_ms": 0.02}\n')
+    assert bench.sweep_key(512, 128, True, "bf16") in bench.sweep_done_keys(str(path))
+    bench.sweep_end_partial_line(str(path))  # a complete file is left as it is
+    assert path.read_text().count("\n") == 4
