@@ -28,7 +28,6 @@ ATTN_ERR_UNSUPPORTED = 2
 ATTN_ERR_WORKSPACE = 3
 ATTN_ERR_CUDA = 4
 ATTN_ERR_DEVICE = 5
-ATTN_ERR_DEVICE = 5
 
 ATTN_BF16 = 0
 ATTN_FP32 = 1
@@ -318,8 +317,12 @@ def attn_bwd_static_scratch(q, k, v, o, lse, dout, dq, dk, dv, scale=None, causa
                             stream=None):
     """Deterministic backward with the library's own static scratch: no
     workspace argument and no device allocation, for callers that cannot
-    allocate (graph capture, fixed memory pools, embeddings).  Calls on one
-    device must not overlap on the GPU."""
+    allocate device memory where they run the backward (fixed memory pools or
+    another runtime's allocator, loops that must not take cudaMalloc's
+    implicit synchronisation, embeddings that only pass existing tensors).
+    The first call on each device looks up the scratch's device address, so
+    make it before any stream capture.  Calls on one device must not overlap
+    on the GPU."""
     B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     _check(lib().attn_bwd_static_scratch(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                                          _ptr(dk), _ptr(dv), B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d),

@@ -737,8 +737,10 @@ extern "C" attn_status attn_bwd_static_scratch(const void* q, const void* k, con
                                                int B, int Lq, int Lkv, int Hq, int Hkv, int d, float scale,
                                                int causal, const int32_t* kv_lens, attn_dtype dtype,
                                                attn_stream_t stream) {
+  // sizes first: the scratch size below assumes them in range
+  attn_status s = check_problem(B, Lq, Lkv, Hq, Hkv, d, scale, causal, dtype);
+  if (s != ATTN_OK) return s;
   const size_t need = attn_bwd_workspace_size(B, Lq, Hq, d, 1, dtype);
-  if (need == 0) return fail(ATTN_ERR_INVALID_ARG, "sizes must be positive (B=%d Lq=%d Hq=%d d=%d)", B, Lq, Hq, d);
   if (need > kStaticScratchBytes)
     return fail(ATTN_ERR_WORKSPACE,
                 "attn_bwd_static_scratch: this problem needs %zu bytes of scratch but the static scratch holds %zu "

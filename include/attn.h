@@ -312,9 +312,10 @@ attn_status attn_timing_query(const char* kernel, double* total_ms, int* launche
  * For callers that cannot allocate device memory where they run the backward:
  * hosts whose device memory belongs to a fixed pool or another runtime's
  * allocator, latency-critical loops that must not take cudaMalloc's implicit
- * device synchronisation, or embeddings that only hand over existing tensors.  The scratch (two floats per padded query row) lives in a 4 MiB
- * device array inside the library, held by every GPU that loads it until the
- * process exits.  Limit: B * Hq * roundup(Lq, 128) <= 524288 (e.g. B4 H8
+ * device synchronisation, or embeddings that only hand over existing tensors.
+ * The scratch (two floats per padded query row) lives in a 4 MiB device array
+ * inside the library, held by every GPU that loads it until the process
+ * exits.  Limit: B * Hq * roundup(Lq, 128) <= 524288 (e.g. B4 H8
  * Lq16384); larger problems return ATTN_ERR_WORKSPACE with a message.
  *
  * The first call on each device looks up the array's device address with that

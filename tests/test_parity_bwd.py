@@ -139,3 +139,35 @@ def test_kvlen_gqa_full_size_one_group():
             assert rel_err(got[2], ref[2]) <= TOL["bf16"]
         else:
             check_grads(p, got, ref)
+
+
+def check_one_slice(p, inputs, grads, b, h):
+    q, k, v, do = inputs
+    sl = lambda t: t[b:b + 1, :, h:h + 1]  # noqa: E731
+    ref = oracle.backward(sl(q), sl(k), sl(v), sl(do), causal=p.causal)
+    check_grads(p, tuple(to_np(sl(g)) for g in grads), ref)
+
+
+# The attention grid's largest cells and the ragged lengths at their full size
+# (B4 H8), run through the same launch configuration the bench times (grouped
+# launch order over all 32 (batch, head) pairs, the head_dim 64 K/V ring); the
+# oracle checks two (batch, head) slices of each.
+FULL = [(8192, 64, False, "bf16"), (8192, 64, True, "bf16"), (3000, 64, True, "bf16"), (3000, 128, True, "bf16"),
+        (1500, 128, False, "bf16"), (2048, 128, True, "fp32")]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("T,d,causal,dtype", FULL)
+def test_grid_full_size_two_slices(T, d, causal, dtype):
+    p = W.grid(T, d, causal, dtype)
+    inputs, _, grads = gpu_fwd_bwd(p, True)
+    for b, h in ((0, 3), (3, 7)):
+        check_one_slice(p, inputs, grads, b, h)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("T,d", [(8192, 64), (3000, 128)])
+def test_grid_full_size_atomic(T, d):
+    p = W.grid(T, d, True)
+    inputs, _, grads = gpu_fwd_bwd(p, False)
+    check_one_slice(p, inputs, grads, 2, 5)

@@ -1,19 +1,22 @@
 """The allocation-free backward entry point (attn_bwd_static_scratch), called
-through the C ABI, against the regular attn_bwd with a caller workspace.
+through the C ABI, against the regular attn_bwd with a caller workspace and
+against the fp64 oracle.
 
 Callers that cannot allocate device memory where they run the backward
 (hosts whose device memory belongs to a fixed pool or another runtime,
 latency-critical loops that must not hit cudaMalloc's implicit device
 synchronisation, embeddings that only hand over existing tensors) use this
 entry point; its scratch is a static array inside the library shared by every
-call on a device.  This file is collected last so a
-run that stops at the first failure has already run every other test."""
+call on a device.  Both entry points run the same deterministic kernels, so
+their results must agree bit for bit.  This file is collected last so a run
+that stops at the first failure has already run every other test."""
 
 import ctypes
 
 import pytest
 import torch
 
+import oracle
 import workloads as W
 from tests._helpers import TOL, rel_err, to_np
 
@@ -40,7 +43,8 @@ def test_static_scratch_backward_matches_workspace_backward(dtype):
     import exact_attention_34_gb300 as ea
 
     p = W.Problem(2, 700, 900, 4, 2, 128, dtype, True, (900, 333), "no_alloc")
-    q, k, v, do = (t.cuda() for t in W.make_inputs(p, seed=7))
+    q_h, k_h, v_h, do_h = W.make_inputs(p, seed=7)
+    q, k, v, do = (t.cuda() for t in (q_h, k_h, v_h, do_h))
     kv = torch.tensor(p.kv_lens, dtype=torch.int32, device="cuda")
     o, lse = ea.forward(q, k, v, causal=True, kv_lens=kv)
     ref = ea.backward(q, k, v, o, lse, do, causal=True, kv_lens=kv, deterministic=True)
@@ -48,7 +52,11 @@ def test_static_scratch_backward_matches_workspace_backward(dtype):
         got = _static_bwd(ea, q, k, v, o, lse, do, True, kv)
         torch.cuda.synchronize()
         for a, b in zip(got, ref):
-            assert rel_err(to_np(a), to_np(b)) <= TOL[dtype]
+            assert torch.equal(a, b)
+    # and the result itself against the fp64 oracle
+    exact = oracle.backward(q_h, k_h, v_h, do_h, causal=True, kv_lens=p.kv_lens)
+    for a, b in zip(got, exact):
+        assert rel_err(to_np(a), b) <= TOL[dtype]
 
 
 def test_static_scratch_rejects_oversized_problem():
@@ -61,4 +69,3 @@ def test_static_scratch_rejects_oversized_problem():
     st = ea.lib().attn_bwd_static_scratch(*([fake] * 9), 8, 4096, 4096, 32, 8, 128, 0.1, 0, None, ea.ATTN_BF16, None)
     assert st == ea.ATTN_ERR_WORKSPACE
     assert "static scratch" in ea.lib().attn_last_error().decode()
-
