@@ -452,6 +452,24 @@ def other_rows(args, dev, peaks):
     ea.attn_timing_enable(False)
     out["single_pass_fwd_bwd"] = {"ms": round(ms, 4), "tflops": round(3.5 * W.fwd_flops(p) / ms / 1e9, 1),
                                   "kernel_ms": kt, "note": "same workload, atomic-dQ backward (not bitwise reproducible)"}
+
+    # the single pass with dQ added in key-tile order (bitwise reproducible)
+    def ordered_step():
+        o, lse = ea.forward(q, k, v, causal=True)
+        ea.backward(q, k, v, o, lse, do, causal=True, deterministic=2)
+
+    ms = timed(ordered_step)
+    ea.attn_timing_enable(True)
+    for _ in range(5):
+        ordered_step()
+    torch.cuda.synchronize()
+    kt = {n: round(ea.attn_timing_query(n)[0] / 5, 4)
+          for n in ("fwd", "bwd_preprocess", "bwd_dkdv_ordered", "dq_convert")}
+    ea.attn_timing_enable(False)
+    out["single_pass_deterministic"] = {
+        "ms": round(ms, 4), "tflops": round(3.5 * W.fwd_flops(p) / ms / 1e9, 1), "kernel_ms": kt,
+        "note": "same workload, single-pass backward with each query tile's dQ added in key-tile order "
+                "(bitwise reproducible; deterministic=2)"}
     del q, k, v, do
     # local-window mask on the headline shapes: a 1024-key causal sliding
     # window (flops over the valid (row, key) pairs)

@@ -239,8 +239,14 @@ def attn_bwd_preprocess(o, dout, delta, stream=None):
            "attn_bwd_preprocess")
 
 
+def _det(deterministic) -> int:
+    """The C ABI's backward variant: True/1 two-pass, False/0 single pass with
+    atomic dQ, 2 single pass with dQ added in key-tile order."""
+    return int(deterministic)
+
+
 def attn_bwd_workspace_size(B, Lq, Hq, d, deterministic=True, dtype=torch.bfloat16) -> int:
-    return int(lib().attn_bwd_workspace_size(B, Lq, Hq, d, int(bool(deterministic)), _DT[dtype]))
+    return int(lib().attn_bwd_workspace_size(B, Lq, Hq, d, _det(deterministic), _DT[dtype]))
 
 
 def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, scale=None, causal=False, kv_lens=None,
@@ -249,7 +255,7 @@ def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, scale=None, causal=Fa
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                           B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d), int(bool(causal)), _ptr(kv_lens), _dtype(q),
-                          int(bool(deterministic)), _ptr(workspace), ws_bytes, _stream(stream)),
+                          _det(deterministic), _ptr(workspace), ws_bytes, _stream(stream)),
            "attn_bwd")
 
 
@@ -260,7 +266,7 @@ def attn_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, workspace, window, scale=
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(lib().attn_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
                                  _ptr(dv), B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d), wl, wr, _ptr(kv_lens),
-                                 _dtype(q), int(bool(deterministic)), _ptr(workspace), ws_bytes, _stream(stream)),
+                                 _dtype(q), _det(deterministic), _ptr(workspace), ws_bytes, _stream(stream)),
            "attn_bwd_window")
 
 
@@ -272,7 +278,7 @@ def attn_bwd_segments(q, k, v, o, lse, dout, dq, dk, dv, workspace, q_segment, k
     _check(lib().attn_bwd_segments(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
                                    _ptr(dv), B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d), wl, wr, _ptr(q_segment),
                                    _ptr(kv_segment), _ptr(segment_info), _ptr(kv_lens), _dtype(q),
-                                   int(bool(deterministic)),
+                                   _det(deterministic),
                                    _ptr(workspace), ws_bytes, _stream(stream)),
            "attn_bwd_segments")
 
@@ -390,7 +396,9 @@ def forward(q, k, v, scale=None, causal=False, kv_lens=None, stream=None, window
 
 def backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_lens=None, deterministic=True, stream=None,
              window=None, segments=None):
-    """(dq, dk, dv) given the forward's o and lse (same mask arguments as forward)."""
+    """(dq, dk, dv) given the forward's o and lse (same mask arguments as
+    forward).  deterministic: True (two-pass), False (single pass, atomic dQ)
+    or 2 (single pass, dQ added in key-tile order; reproducible)."""
     B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     nbytes = attn_bwd_workspace_size(B, Lq, Hq, d, deterministic, q.dtype)
     ws = torch.empty(max(nbytes, 256), device=q.device, dtype=torch.uint8)

@@ -508,11 +508,18 @@ attn_status attn_bwd_preprocess(const void* o, const void* dout, float* delta, i
   return from_cuda(e, "attn_bwd_preprocess launch");
 }
 
+// ordered single pass: one turn counter per (batch, query head, 128-row query
+// tile), then the work-item ticket
+static size_t bwd_turn_bytes(int B, int Lq, int Hq) {
+  return (static_cast<size_t>(B) * Hq * ((Lq + 127) / 128) + 1) * sizeof(int);
+}
+
 size_t attn_bwd_workspace_size(int B, int Lq, int Hq, int d, int deterministic, attn_dtype dtype) {
   (void)dtype;
   if (B <= 0 || Lq <= 0 || Hq <= 0 || d <= 0) return 0;
   size_t bytes = 2 * bwd_rowstat_bytes(B, Lq, Hq);  // delta and lse2, padded rows
-  if (!deterministic) bytes += align256(static_cast<size_t>(B) * Lq * Hq * d * sizeof(float));
+  if (deterministic != 1) bytes += align256(static_cast<size_t>(B) * Lq * Hq * d * sizeof(float));
+  if (deterministic == 2) bytes += align256(bwd_turn_bytes(B, Lq, Hq));
   return bytes;
 }
 
@@ -525,7 +532,11 @@ static attn_status bwd_impl(const void* q, const void* k, const void* v, const v
   if (s != ATTN_OK) return s;
   if (pb.kv_lens != nullptr && (reinterpret_cast<uintptr_t>(pb.kv_lens) & 3u))
     return fail(ATTN_ERR_INVALID_ARG, "kv_lens is not 4-byte aligned");
-  if (deterministic != 0 && deterministic != 1) return fail(ATTN_ERR_INVALID_ARG, "deterministic must be 0 or 1");
+  if (deterministic < 0 || deterministic > 2) return fail(ATTN_ERR_INVALID_ARG, "deterministic must be 0, 1 or 2");
+  if (deterministic == 2 && (dtype == ATTN_FP32 || d > 128))
+    return fail(ATTN_ERR_UNSUPPORTED,
+                "the ordered single-pass backward (deterministic = 2) runs on the 16-bit tensor-core path at "
+                "head_dim <= 128; use deterministic = 1 (two-pass, also reproducible)");
   const size_t need = attn_bwd_workspace_size(B, Lq, Hq, d, deterministic, dtype);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
@@ -546,7 +557,16 @@ static attn_status bwd_impl(const void* q, const void* k, const void* v, const v
   const size_t rs = bwd_rowstat_bytes(B, Lq, Hq);
   a.delta = static_cast<float*>(workspace);
   a.lse2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + rs);
-  a.dq_acc = deterministic ? nullptr : reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * rs);
+  a.dq_acc = deterministic == 1 ? nullptr : reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * rs);
+  a.dq_turn = nullptr;
+  a.ticket = nullptr;
+  a.turn_bytes = 0;
+  if (deterministic == 2) {
+    const size_t acc = align256(static_cast<size_t>(B) * Lq * Hq * d * sizeof(float));
+    a.dq_turn = reinterpret_cast<int*>(static_cast<char*>(workspace) + 2 * rs + acc);
+    a.turn_bytes = bwd_turn_bytes(B, Lq, Hq);
+    a.ticket = a.dq_turn + static_cast<size_t>(B) * Hq * ((Lq + 127) / 128);
+  }
   a.Lq_pad = lq_padded(Lq);
   a.deterministic = deterministic;
   DeviceStatus* st = status_ptr();

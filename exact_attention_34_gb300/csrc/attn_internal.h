@@ -127,9 +127,12 @@ struct BwdArgs {
   void* dv;
   float* delta;   // workspace [B, Hq, Lq_pad]
   float* lse2;    // workspace [B, Hq, Lq_pad]: lse * log2(e), +inf on empty and pad rows
-  float* dq_acc;  // workspace [B, Lq, Hq, d] (atomic variant only)
+  float* dq_acc;  // workspace [B, Lq, Hq, d] (single-pass variants)
+  int* dq_turn;   // workspace: [B, Hq, ceil(Lq/128)] turn counters, then the ticket (ordered single pass)
+  size_t turn_bytes;
   int Lq_pad;     // Lq rounded up to a multiple of 128
-  int deterministic;
+  int deterministic;  // 0 single pass (atomic dQ), 1 two-pass, 2 single pass with ordered dQ adds
+  int* ticket;
 };
 
 // delta = rowsum(dO * O) in the padded [B, Hq, Lq_pad] layout; optional lse2,

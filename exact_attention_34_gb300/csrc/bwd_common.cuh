@@ -15,7 +15,10 @@ struct BwdKParams {
   void* dq;
   void* dk;
   void* dv;
-  float* dq_acc;       // single-pass variant
+  float* dq_acc;       // single-pass variants: [B, Lq, Hq, dh] fp32, zeroed before the launch
+  int* dq_turn;        // ordered single pass: [B, Hq, nq] turn counters, zeroed before the launch
+  int* ticket;         // ordered single pass: work-item ticket, zeroed before the launch
+  int nq;              // 128-row query tiles per sequence
   const int32_t* kv_lens;
   int Lq, Lkv, Hq, Hkv, G, causal, wl, wr, Lq_pad, n_tiles, n_pairs, pair_group;
   int dh;  // stored head_dim (32 runs as D = 64 with zero-filled columns)
@@ -107,13 +110,19 @@ __device__ __forceinline__ uint32_t segment_bits32(const int32_t* ids, int col, 
   return bits;
 }
 
-// Single-pass backward after the preprocess: the dK/dV kernel with atomic dQ
-// (grid = KV heads x batch x key tiles) and the dQ convert over n_dq values.
-// All four tensor maps use boxes of 64 columns x 128 rows.
+// Single-pass backward after the preprocess: the dK/dV kernel that also
+// sums dQ into kp.dq_acc (grid = KV heads x batch x key tiles), then the dQ
+// convert over n_dq values.  ordered: the sums of each query tile run in
+// key-tile order (bitwise reproducible); otherwise as the adds arrive.  All
+// four tensor maps use boxes of 64 columns x 128 rows.
 template <int D>
 cudaError_t launch_single_pass(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, long n_dq, bool f16,
-                               cudaStream_t stream);
+                               bool ordered, cudaStream_t stream);
+template <int D>
+cudaError_t launch_single_pass_ordered(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                       const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, long n_dq, bool f16,
+                                       cudaStream_t stream);
 
 }  // namespace bwd
 }  // namespace attn

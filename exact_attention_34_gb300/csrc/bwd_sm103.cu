@@ -785,7 +785,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
   pa.lse = a.lse;
   pa.delta = a.delta;
   pa.lse2 = a.lse2;
-  pa.dq_acc = a.deterministic ? nullptr : a.dq_acc;
+  pa.dq_acc = a.deterministic == 1 ? nullptr : a.dq_acc;  // the single-pass variants sum into it
   pa.B = pb.B;
   pa.Lq = pb.Lq;
   pa.Lq_pad = a.Lq_pad;
@@ -802,6 +802,9 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
   kp.dk = a.dk;
   kp.dv = a.dv;
   kp.dq_acc = a.dq_acc;
+  kp.dq_turn = a.dq_turn;
+  kp.ticket = a.ticket;
+  kp.nq = (pb.Lq + 127) / 128;
   kp.kv_lens = pb.kv_lens;
   kp.Lq = pb.Lq;
   kp.Lkv = pb.Lkv;
@@ -835,9 +838,14 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
     kp.n_pairs = pb.B * pb.Hkv;
     kp.pair_group = l2_pair_group(2l * pb.G * pb.Lq * D * 2, kp.n_pairs, 1);
     dim3 grid(kp.n_pairs * kp.n_tiles);
-    if (!a.deterministic)
+    if (a.deterministic != 1) {
+      if (a.deterministic == 2) {  // turn counters and the work-item ticket start at zero
+        e = cudaMemsetAsync(a.dq_turn, 0, a.turn_bytes, stream);
+        if (e != cudaSuccess) return e;
+      }
       return launch_single_pass<D>(tq128, tk, tv, tdo128, kp, grid, static_cast<long>(pb.B) * pb.Lq * pb.Hq * pb.d,
-                                   pb.f16 != 0, stream);
+                                   pb.f16 != 0, a.deterministic == 2, stream);
+    }
     e = dispatch_build<DkdvLaunch, D>(pb, tq128, tk, tv, tdo128, kp, grid, stream);
     if (e != cudaSuccess) return e;
   }

@@ -101,12 +101,20 @@ attn_status attn_bwd_preprocess(const void* o, const void* dout, float* delta, i
                                 attn_dtype dtype, attn_stream_t stream);
 
 /*
- * Bytes of device workspace attn_bwd needs.  deterministic = 1: the two-pass
- * backward (a dK/dV kernel per KV block, then a separate dQ kernel; bitwise
- * reproducible), workspace = delta.  deterministic = 0: the single-pass
- * backward with dQ accumulated by float32 atomic adds (order not
- * reproducible), workspace = delta + a float32 dQ buffer [B,Lq,Hq,d]
- * ("Attention performance", section "When to use which", backward pass).
+ * Bytes of device workspace attn_bwd needs ("Attention performance", section
+ * "When to use which", backward pass: one pass with atomic dQ, or the split
+ * into a dK/dV pass and a dQ pass).  `deterministic` picks the variant:
+ *   1: the two-pass backward (a dK/dV kernel per KV block, then a separate
+ *      dQ kernel; bitwise reproducible), workspace = delta and lse*log2(e)
+ *      per padded query row;
+ *   0: the single-pass backward with dQ accumulated by float32 atomic adds
+ *      (summation order not reproducible), workspace = the above + a float32
+ *      dQ buffer [B,Lq,Hq,d];
+ *   2: the single-pass backward with each query tile's dQ parts added in
+ *      key-tile order (a turn counter per query tile; bitwise reproducible),
+ *      workspace = the above + one int32 per (batch, query head, 128-row
+ *      query tile) + 4 bytes.  16-bit types at head_dim <= 128 only
+ *      (ATTN_ERR_UNSUPPORTED otherwise).
  */
 size_t attn_bwd_workspace_size(int B, int Lq, int Hq, int d, int deterministic, attn_dtype dtype);
 
@@ -296,7 +304,7 @@ attn_status attn_selftest_wait_timeout(int site, attn_stream_t stream);
  * (events are created by the library and reused; no device memory is
  * allocated).  attn_timing_enable(0) stops recording.  attn_timing_query waits
  * for the recorded launches of one kernel ("fwd", "bwd_preprocess",
- * "bwd_dkdv", "bwd_dkdv_atomic", "bwd_dq", "dq_convert", "decode", "combine",
+ * "bwd_dkdv", "bwd_dkdv_atomic", "bwd_dkdv_ordered", "bwd_dq", "dq_convert", "decode", "combine",
  * or the float32 kernels "fwd_f32", "decode_f32", "bwd_dkdv_f32",
  * "bwd_dq_f32", "dq_convert_f32") and returns their summed milliseconds and
  * count (host pointers).  Process-wide; meant for single-threaded benchmarks.

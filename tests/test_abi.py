@@ -76,6 +76,22 @@ def test_bwd_workspace_rules(L):
     assert L.attn_bwd(*bad_det, FAKE, atom, None) == 1
 
 
+def test_bwd_ordered_single_pass_rules(L):
+    """deterministic = 2: the dQ buffer plus one turn counter per (batch, head,
+    query tile) and a ticket; 16-bit types at head_dim <= 128 only."""
+    B, Lq, Hq, d = 2, 300, 4, 128
+    atom = L.attn_bwd_workspace_size(B, Lq, Hq, d, 0, 0)
+    ordered = L.attn_bwd_workspace_size(B, Lq, Hq, d, 2, 0)
+    assert ordered >= atom + (B * Hq * 3 + 1) * 4 and ordered % 256 == 0
+    args = [FAKE] * 9 + [B, Lq, Lq, Hq, Hq, d, 0.1, 0, None, 0, 2]
+    assert L.attn_bwd(*args, FAKE, atom, None) == 3          # the counters do not fit
+    f32 = [FAKE] * 9 + [B, Lq, Lq, Hq, Hq, d, 0.1, 0, None, 1, 2]
+    assert L.attn_bwd(*f32, FAKE, 1 << 30, None) == 2        # float32: unsupported
+    assert "deterministic = 1" in L.attn_last_error().decode()
+    d256 = [FAKE] * 9 + [B, Lq, Lq, Hq, Hq, 256, 0.1, 0, None, 0, 2]
+    assert L.attn_bwd(*d256, FAKE, 1 << 30, None) == 2       # head_dim 256: unsupported
+
+
 def test_decode_rules(L):
     s = L.attn_decode_num_splits(8, 1, 131072, 32, 8, 128)
     assert 1 <= s <= 1024

@@ -68,7 +68,7 @@ def test_forward_and_backward_stay_inside_their_buffers(p):
     lse.check("lse")
     assert torch.equal(o.t, o_ref) and torch.equal(lse.t, lse_ref)
 
-    variants = (True,) if p.d == 256 else (True, False)
+    variants = (True,) if p.d == 256 else (True, False) if p.dtype == "fp32" else (True, False, 2)
     for det in variants:
         dq, dk, dv = Guarded(q.shape, dt), Guarded(k.shape, dt), Guarded(v.shape, dt)
         ws = Guarded((ea.attn_bwd_workspace_size(p.B, p.Lq, p.Hq, p.d, det, dt),), torch.uint8)
