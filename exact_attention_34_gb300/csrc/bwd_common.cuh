@@ -19,6 +19,7 @@ struct BwdKParams {
   int* dq_turn;        // ordered single pass: [B, Hq, nq] turn counters, zeroed before the launch
   int* ticket;         // ordered single pass: work-item ticket, zeroed before the launch
   int nq;              // 128-row query tiles per sequence
+  int rev;             // ordered single pass: turns go from the last key tile down (causal-like masks)
   const int32_t* kv_lens;
   int Lq, Lkv, Hq, Hkv, G, causal, wl, wr, Lq_pad, n_tiles, n_pairs, pair_group;
   int dh;  // stored head_dim (32 runs as D = 64 with zero-filled columns)

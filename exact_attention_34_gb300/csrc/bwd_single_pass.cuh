@@ -42,11 +42,19 @@
 // 64 KB of adds are performed in L2) runs beside the next step's adds.
 //
 // Step order: the atomic build walks the G query heads, each over its query
-// tiles upwards.  The ordered build walks its query tiles downwards (last
-// first), the G heads of each tile in a row: neighbouring key tiles j - 1 and
-// j then visit every (head, query tile) at the same step index, so tile j
-// runs at most a fixed lag behind tile j - 1 instead of falling further behind
-// with every step.
+// tiles upwards.  The ordered build visits the G heads of one query tile in a
+// row, and its turn order follows the mask:
+//  * masks where later rows see more keys (causal): the turns of a query tile
+//    go from its last key tile down to key tile 0, key tiles are claimed from
+//    the last down, and each walks its query tiles upwards.  Key tile j then
+//    reaches a query tile one step after tile j + 1 did, and its first query
+//    tile (the diagonal) waits for nobody, so the tiles that start together
+//    hardly wait on one another (a tile lags its predecessor only by the part
+//    of a turn's latency that exceeds a step);
+//  * other masks: turns go from key tile 0 up, key tiles are claimed from the
+//    first up, and each walks its query tiles downwards, so neighbouring tiles
+//    visit every query tile at the same step index and tile j runs a fixed lag
+//    behind tile j - 1.
 //
 // Warps 0-7 softmax (warpgroup w owns queries [64w, 64w + 64) of the step),
 // 8-11 reduction (warp 8 + i reads TMEM lanes [32i, 32i + 32)), 12 TMA
@@ -117,8 +125,8 @@ struct StepCoord {
   int h, it;
 };
 template <bool kOrdered>
-__device__ __forceinline__ StepCoord step_coord(int t, int hk, int G, int i_begin, int steps_per_head) {
-  if (kOrdered) return {hk * G + t % G, i_begin + steps_per_head - 1 - t / G};
+__device__ __forceinline__ StepCoord step_coord(int t, int hk, int G, int i_begin, int steps_per_head, bool rev) {
+  if (kOrdered) return {hk * G + t % G, rev ? i_begin + t / G : i_begin + steps_per_head - 1 - t / G};
   return {hk * G + t / steps_per_head, i_begin + t % steps_per_head};
 }
 
@@ -218,8 +226,11 @@ __global__ void __launch_bounds__(512, 1)
   static_assert(3 * C::kRegsWork + C::kRegsCtl == 4 * 128, "register split must match the launch allocation");
 
   const int linear = kOrdered ? *item_slot : static_cast<int>(blockIdx.x);
+  const bool rev = kOrdered && p.rev != 0;
   const TileCoord tc = grouped_tile(linear, p.n_pairs, p.n_tiles, p.pair_group);
-  const int j0 = tc.rank * C::kBN, hk = tc.pair % p.Hkv, b = tc.pair / p.Hkv;
+  // claimed in rank order; with reversed turns the last key tile has rank 0
+  const int tile = rev ? p.n_tiles - 1 - tc.rank : tc.rank;
+  const int j0 = tile * C::kBN, hk = tc.pair % p.Hkv, b = tc.pair / p.Hkv;
   int kvl = p.Lkv;
   if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
   // The ordered build keeps each key tile's query range a position span (no
@@ -244,7 +255,7 @@ __global__ void __launch_bounds__(512, 1)
       for (int t = 0; t < T; ++t) {
         const int s = t % NS, r = t / NS;
         if (r > 0 && !mbar_wait(&empty[s], (r - 1) & 1, abort_flag, p.status, kSite + 1)) break;
-        const StepCoord sc = step_coord<kOrdered>(t, hk, p.G, i_begin, steps_per_head);
+        const StepCoord sc = step_coord<kOrdered>(t, hk, p.G, i_begin, steps_per_head, rev);
         const int q0 = sc.it * BM;
         mbar_arrive_expect_tx(&full[s], 2 * C::kQBytes + 2 * BM * 4);
         uint8_t* q_dst = sQ + s * 2 * C::kQBytes;
@@ -335,11 +346,13 @@ __global__ void __launch_bounds__(512, 1)
     } else if (kOrdered && warp >= 14) {
       // ---------------------------------------------------------------- turn keepers (even / odd steps)
       const int par = warp - 14;
-      // the previous key tile's query tiles: where it adds, this tile waits for it
+      // The tile before this one in turn order (key tile j - 1, or j + 1 when
+      // reversed) adds first wherever it adds; a turn counter holds the turn
+      // position (tc.rank) of the next tile to add.
       int pb = 0, ps = 0;
-      if (tc.rank > 0) key_tile_queries(p, b, j0 - C::kBN, kvl, false, pb, ps);
+      if (tc.rank > 0) key_tile_queries(p, b, rev ? j0 + C::kBN : j0 - C::kBN, kvl, false, pb, ps);
       for (int t = par; t < T; t += 2) {
-        const StepCoord sc = step_coord<kOrdered>(t, hk, p.G, i_begin, steps_per_head);
+        const StepCoord sc = step_coord<kOrdered>(t, hk, p.G, i_begin, steps_per_head, rev);
         int* turn = p.dq_turn + (static_cast<size_t>(b) * p.Hq + sc.h) * p.nq + sc.it;
         if (lane == 0 && sc.it >= pb && sc.it < pb + ps) (void)wait_turn(turn, tc.rank, abort_flag, p.status, kSite + 14);
         __syncwarp();
@@ -379,7 +392,7 @@ __global__ void __launch_bounds__(512, 1)
       }
       if (kOrdered) named_barrier_sync(kBarTurn + (t & 1), kBarThreads);
       if (ok && active) {
-        const StepCoord sc = step_coord<kOrdered>(t, hk, p.G, i_begin, steps_per_head);
+        const StepCoord sc = step_coord<kOrdered>(t, hk, p.G, i_begin, steps_per_head, rev);
         const int q0 = sc.it * BM;
         float* dst = p.dq_acc + ((static_cast<size_t>(b) * p.Lq + q0) * p.Hq + sc.h) * p.dh + dr;
         if (q0 + BM <= p.Lq) {
@@ -416,7 +429,7 @@ __global__ void __launch_bounds__(512, 1)
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int s = t % NS;
-      const int q0 = step_coord<kOrdered>(t, hk, p.G, i_begin, steps_per_head).it * BM;
+      const int q0 = step_coord<kOrdered>(t, hk, p.G, i_begin, steps_per_head, rev).it * BM;
       uint32_t sg0 = ~0u, sg1 = ~0u;  // segment bits of this warpgroup's 64 queries (before S is ready)
       // query and key block hold one and the same id: every pair matches
       const bool seg_all =

@@ -805,6 +805,7 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
   kp.dq_turn = a.dq_turn;
   kp.ticket = a.ticket;
   kp.nq = (pb.Lq + 127) / 128;
+  kp.rev = pb.causal;  // later rows see more keys: the light key tiles (the last ones) start the turns
   kp.kv_lens = pb.kv_lens;
   kp.Lq = pb.Lq;
   kp.Lkv = pb.Lkv;
