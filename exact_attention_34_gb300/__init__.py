@@ -122,13 +122,22 @@ def _ptr(t):
                          "call .contiguous() first")
     if not t.is_cuda:
         raise ValueError(f"expected a CUDA tensor, got one on {t.device}")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()  # a plain int: ctypes converts it for the void* argument
 
 
-def _stream(stream):
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+# torch's current stream as a raw handle, without building a Stream object
+# (a few microseconds per call, which short calls notice)
+_raw_current_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, like=None):
+    """The stream handle to pass: `stream`, else torch's current stream on the
+    device of tensor `like` (or the current device)."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_current_stream is not None:
+        return _raw_current_stream(like.get_device() if like is not None else torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def _dtype(t) -> int:
@@ -163,9 +172,13 @@ def _scale(scale, d):
 # ---- entry points with the C names -------------------------------------------
 
 def attn_fwd(q, k, v, o, lse, scale=None, causal=False, kv_lens=None, stream=None):
-    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
+    _attn_fwd(_dims(q, k, v), q, k, v, o, lse, scale, causal, kv_lens, stream)
+
+
+def _attn_fwd(dims, q, k, v, o, lse, scale, causal, kv_lens, stream):
+    B, Lq, Lkv, Hq, Hkv, d = dims
     _check(lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Lq, Lkv, Hq, Hkv, d,
-                          _scale(scale, d), int(bool(causal)), _ptr(kv_lens), _dtype(q), _stream(stream)),
+                          _scale(scale, d), int(bool(causal)), _ptr(kv_lens), _dtype(q), _stream(stream, q)),
            "attn_fwd")
 
 
@@ -179,7 +192,7 @@ def attn_fwd_window(q, k, v, o, lse, window, scale=None, kv_lens=None, stream=No
     B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     wl, wr = _window(window)
     _check(lib().attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Lq, Lkv, Hq, Hkv, d,
-                                 _scale(scale, d), wl, wr, _ptr(kv_lens), _dtype(q), _stream(stream)),
+                                 _scale(scale, d), wl, wr, _ptr(kv_lens), _dtype(q), _stream(stream, q)),
            "attn_fwd_window")
 
 
@@ -197,7 +210,7 @@ def attn_fwd_split(q, k, v, o, lse, workspace, num_splits, window=(-1, -1), scal
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().attn_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Lq, Lkv, Hq, Hkv, d,
                                 _scale(scale, d), wl, wr, _ptr(kv_lens), int(num_splits), _ptr(workspace), nbytes,
-                                _dtype(q), _stream(stream)),
+                                _dtype(q), _stream(stream, q)),
            "attn_fwd_split")
 
 
@@ -209,7 +222,7 @@ def attn_segment_info(q_segment, kv_segment, info, stream=None):
     B, Lq = q_segment.shape
     Lkv = kv_segment.shape[1]
     _check(lib().attn_segment_info(_ptr(q_segment), _ptr(kv_segment), B, Lq, Lkv, _ptr(info),
-                                   info.numel() * info.element_size(), _stream(stream)),
+                                   info.numel() * info.element_size(), _stream(stream, info)),
            "attn_segment_info")
 
 
@@ -229,13 +242,13 @@ def attn_fwd_segments(q, k, v, o, lse, q_segment, kv_segment, window=(-1, -1), s
     wl, wr = _window(window)
     _check(lib().attn_fwd_segments(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Lq, Lkv, Hq, Hkv, d,
                                    _scale(scale, d), wl, wr, _ptr(q_segment), _ptr(kv_segment), _ptr(segment_info),
-                                   _ptr(kv_lens), _dtype(q), _stream(stream)),
+                                   _ptr(kv_lens), _dtype(q), _stream(stream, q)),
            "attn_fwd_segments")
 
 
 def attn_bwd_preprocess(o, dout, delta, stream=None):
     B, Lq, Hq, d = o.shape
-    _check(lib().attn_bwd_preprocess(_ptr(o), _ptr(dout), _ptr(delta), B, Lq, Hq, d, _dtype(o), _stream(stream)),
+    _check(lib().attn_bwd_preprocess(_ptr(o), _ptr(dout), _ptr(delta), B, Lq, Hq, d, _dtype(o), _stream(stream, o)),
            "attn_bwd_preprocess")
 
 
@@ -245,17 +258,29 @@ def _det(deterministic) -> int:
     return int(deterministic)
 
 
+_ws_sizes = {}
+
+
 def attn_bwd_workspace_size(B, Lq, Hq, d, deterministic=True, dtype=torch.bfloat16) -> int:
-    return int(lib().attn_bwd_workspace_size(B, Lq, Hq, d, _det(deterministic), _DT[dtype]))
+    key = (B, Lq, Hq, d, _det(deterministic), dtype)
+    n = _ws_sizes.get(key)
+    if n is None:  # a pure function of its arguments: asked once per shape
+        n = _ws_sizes[key] = int(lib().attn_bwd_workspace_size(B, Lq, Hq, d, key[4], _DT[dtype]))
+    return n
 
 
 def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, scale=None, causal=False, kv_lens=None,
              deterministic=True, stream=None):
-    B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
+    _attn_bwd(_dims(q, k, v), q, k, v, o, lse, dout, dq, dk, dv, workspace, scale, causal, kv_lens, deterministic,
+              stream)
+
+
+def _attn_bwd(dims, q, k, v, o, lse, dout, dq, dk, dv, workspace, scale, causal, kv_lens, deterministic, stream):
+    B, Lq, Lkv, Hq, Hkv, d = dims
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                           B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d), int(bool(causal)), _ptr(kv_lens), _dtype(q),
-                          _det(deterministic), _ptr(workspace), ws_bytes, _stream(stream)),
+                          _det(deterministic), _ptr(workspace), ws_bytes, _stream(stream, q)),
            "attn_bwd")
 
 
@@ -266,7 +291,7 @@ def attn_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, workspace, window, scale=
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(lib().attn_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
                                  _ptr(dv), B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d), wl, wr, _ptr(kv_lens),
-                                 _dtype(q), _det(deterministic), _ptr(workspace), ws_bytes, _stream(stream)),
+                                 _dtype(q), _det(deterministic), _ptr(workspace), ws_bytes, _stream(stream, q)),
            "attn_bwd_window")
 
 
@@ -279,7 +304,7 @@ def attn_bwd_segments(q, k, v, o, lse, dout, dq, dk, dv, workspace, q_segment, k
                                    _ptr(dv), B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d), wl, wr, _ptr(q_segment),
                                    _ptr(kv_segment), _ptr(segment_info), _ptr(kv_lens), _dtype(q),
                                    _det(deterministic),
-                                   _ptr(workspace), ws_bytes, _stream(stream)),
+                                   _ptr(workspace), ws_bytes, _stream(stream, q)),
            "attn_bwd_segments")
 
 
@@ -292,14 +317,14 @@ def attn_decode_splitkv(q, k_cache, v_cache, o_part, lse_part, num_splits, scale
     B, Lq, Lkv, Hq, Hkv, d = _dims(q, k_cache, v_cache)
     _check(lib().attn_decode_splitkv(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o_part), _ptr(lse_part), B, Lq,
                                      Lkv, Hq, Hkv, d, _scale(scale, d), int(bool(causal)), _ptr(kv_lens),
-                                     int(num_splits), _dtype(q), _stream(stream)),
+                                     int(num_splits), _dtype(q), _stream(stream, q)),
            "attn_decode_splitkv")
 
 
 def attn_decode_combine(o_part, lse_part, o, lse, stream=None):
     B, Hq, S, Lq, d = o_part.shape
     _check(lib().attn_decode_combine(_ptr(o_part), _ptr(lse_part), _ptr(o), _ptr(lse), B, Lq, Hq, d, S, _dtype(o),
-                                     _stream(stream)),
+                                     _stream(stream, o)),
            "attn_decode_combine")
 
 
@@ -332,7 +357,7 @@ def attn_bwd_static_scratch(q, k, v, o, lse, dout, dq, dk, dv, scale=None, causa
     B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     _check(lib().attn_bwd_static_scratch(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                                          _ptr(dk), _ptr(dv), B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d),
-                                         int(bool(causal)), _ptr(kv_lens), _dtype(q), _stream(stream)),
+                                         int(bool(causal)), _ptr(kv_lens), _dtype(q), _stream(stream, q)),
            "attn_bwd_static_scratch")
 
 
@@ -390,7 +415,7 @@ def forward(q, k, v, scale=None, causal=False, kv_lens=None, stream=None, window
             raise ValueError("pass either causal or window (causal is window (-1, 0))")
         attn_fwd_window(q, k, v, o, lse, window, scale, kv_lens, stream)
     else:
-        attn_fwd(q, k, v, o, lse, scale, causal, kv_lens, stream)
+        _attn_fwd((B, Lq, Lkv, Hq, Hkv, d), q, k, v, o, lse, scale, causal, kv_lens, stream)
     return o, lse
 
 
@@ -412,7 +437,8 @@ def backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_lens=None, dete
             raise ValueError("pass either causal or window (causal is window (-1, 0))")
         attn_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, ws, window, scale, kv_lens, deterministic, stream)
     else:
-        attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, ws, scale, causal, kv_lens, deterministic, stream)
+        _attn_bwd((B, Lq, Lkv, Hq, Hkv, d), q, k, v, o, lse, dout, dq, dk, dv, ws, scale, causal, kv_lens,
+                  deterministic, stream)
     return dq, dk, dv
 
 

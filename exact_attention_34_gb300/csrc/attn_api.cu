@@ -48,20 +48,23 @@ attn_status from_cuda(cudaError_t e, const char* what) {
 }
 
 constexpr int kMaxDevices = 64;
-DeviceStatus* g_status_ptr[kMaxDevices] = {};
+std::atomic<DeviceStatus*> g_status_ptr[kMaxDevices] = {};
 std::mutex g_status_mu;
 
-// Device address of g_status for the current device (looked up once per device).
+// Device address of g_status for the current device (looked up once per
+// device; later calls read it without taking the lock).
 DeviceStatus* status_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceStatus* known = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (known != nullptr) return known;
   std::lock_guard<std::mutex> lk(g_status_mu);
-  if (g_status_ptr[dev] == nullptr) {
+  if (g_status_ptr[dev].load(std::memory_order_relaxed) == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
-    g_status_ptr[dev] = static_cast<DeviceStatus*>(p);
+    g_status_ptr[dev].store(static_cast<DeviceStatus*>(p), std::memory_order_release);
   }
-  return g_status_ptr[dev];
+  return g_status_ptr[dev].load(std::memory_order_relaxed);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -181,8 +184,57 @@ size_t bwd_rowstat_bytes(int B, int Lq, int Hq) {
 
 }  // namespace
 
+namespace {
+
+// Descriptors encoded recently on this thread.  An encode takes about a
+// microsecond of host time; a training loop or a benchmark calls the library
+// with the same tensors again and again, and a short call is host-bound.  The
+// descriptor is a pure function of the key, so a hit is exact; the cache is
+// per thread, so calls stay thread-safe.
+struct TmapKey {
+  const void* base;
+  int elem, B, L, H, d, box_inner, box_rows;
+  bool operator==(const TmapKey& o) const {
+    return base == o.base && elem == o.elem && B == o.B && L == o.L && H == o.H && d == o.d &&
+           box_inner == o.box_inner && box_rows == o.box_rows;
+  }
+};
+struct TmapEntry {
+  TmapKey key;
+  CUtensorMap map;
+  bool valid;
+};
+constexpr int kTmapCacheSize = 32;
+thread_local TmapEntry t_tmap_cache[kTmapCacheSize];
+thread_local int t_tmap_next = 0;
+
+bool encode_bshd_tmap(CUtensorMap* map, const void* base, int elem, int B, int L, int H, int d, int box_inner,
+                      int box_rows);
+
+}  // namespace
+
 bool make_bshd_tmap(CUtensorMap* map, const void* base, int elem, int B, int L, int H, int d, int box_inner,
                     int box_rows) {
+  const TmapKey key{base, elem, B, L, H, d, box_inner, box_rows};
+  for (int i = 0; i < kTmapCacheSize; ++i) {
+    if (t_tmap_cache[i].valid && t_tmap_cache[i].key == key) {
+      *map = t_tmap_cache[i].map;
+      return true;
+    }
+  }
+  if (!encode_bshd_tmap(map, base, elem, B, L, H, d, box_inner, box_rows)) return false;
+  TmapEntry& e = t_tmap_cache[t_tmap_next];
+  t_tmap_next = (t_tmap_next + 1) % kTmapCacheSize;
+  e.key = key;
+  e.map = *map;
+  e.valid = true;
+  return true;
+}
+
+namespace {
+
+bool encode_bshd_tmap(CUtensorMap* map, const void* base, int elem, int B, int L, int H, int d, int box_inner,
+                      int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t es = elem == kElemF32 ? 4 : 2;
@@ -200,6 +252,8 @@ bool make_bshd_tmap(CUtensorMap* map, const void* base, int elem, int B, int L, 
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+}  // namespace
 
 int device_sm_count() {
   static std::atomic<int> cache[kMaxDevices] = {};
@@ -220,6 +274,7 @@ struct TimingRecord {
 };
 std::mutex g_timing_mu;
 bool g_timing_on = false;
+std::atomic<bool> g_timing_flag{false};  // g_timing_on, readable without the lock
 std::vector<TimingRecord> g_timing;
 std::vector<cudaEvent_t> g_event_pool;
 
@@ -244,6 +299,7 @@ void clear_timing_locked() {
 }  // namespace
 
 KernelTimer::KernelTimer(const char* name, cudaStream_t s) : slot_(-1), stream_(s) {
+  if (!g_timing_flag.load(std::memory_order_relaxed)) return;  // timing off: no lock per launch
   std::lock_guard<std::mutex> lk(g_timing_mu);
   if (!g_timing_on) return;
   TimingRecord r{name, pooled_event(), pooled_event()};
@@ -684,6 +740,7 @@ attn_status attn_timing_enable(int on) {
   std::lock_guard<std::mutex> lk(g_timing_mu);
   if (on) clear_timing_locked();
   g_timing_on = on != 0;
+  g_timing_flag.store(g_timing_on, std::memory_order_relaxed);
   return ok();
 }
 

@@ -827,14 +827,15 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
   kp.scale_log2 = pb.scale * kLog2e;
   kp.status = st;
 
-  // dK/dV pass (both variants): Q/dO and K/V boxes of 128 rows
+  // both passes read Q/dO and K/V in boxes of 64 columns x 128 rows
+  CUtensorMap tk, tv, tq128, tdo128;
+  if (!make_bshd_tmap(&tq128, a.q, elem, pb.B, pb.Lq, pb.Hq, pb.d, 64, 128) ||
+      !make_bshd_tmap(&tdo128, a.dout, elem, pb.B, pb.Lq, pb.Hq, pb.d, 64, 128) ||
+      !make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, 128) ||
+      !make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, 128))
+    return cudaErrorInvalidValue;
+  // dK/dV pass (both variants)
   {
-    CUtensorMap tk, tv, tq128, tdo128;
-    if (!make_bshd_tmap(&tq128, a.q, elem, pb.B, pb.Lq, pb.Hq, pb.d, 64, 128) ||
-        !make_bshd_tmap(&tdo128, a.dout, elem, pb.B, pb.Lq, pb.Hq, pb.d, 64, 128) ||
-        !make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, 128) ||
-        !make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, 128))
-      return cudaErrorInvalidValue;
     kp.n_tiles = (pb.Lkv + 127) / 128;
     kp.n_pairs = pb.B * pb.Hkv;
     kp.pair_group = l2_pair_group(2l * pb.G * pb.Lq * D * 2, kp.n_pairs, 1);
@@ -850,19 +851,13 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
     e = dispatch_build<DkdvLaunch, D>(pb, tq128, tk, tv, tdo128, kp, grid, stream);
     if (e != cudaSuccess) return e;
   }
-  // dQ pass: Q/dO and K/V boxes of 128 rows
+  // dQ pass
   {
-    CUtensorMap tq, tk, tv, tdo;
-    if (!make_bshd_tmap(&tq, a.q, elem, pb.B, pb.Lq, pb.Hq, pb.d, 64, 128) ||
-        !make_bshd_tmap(&tdo, a.dout, elem, pb.B, pb.Lq, pb.Hq, pb.d, 64, 128) ||
-        !make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, 128) ||
-        !make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, 128))
-      return cudaErrorInvalidValue;
     kp.n_tiles = (pb.Lq + 127) / 128;
     kp.n_pairs = pb.B * pb.Hq;
     kp.pair_group = l2_pair_group(2l * pb.Lkv * D * 2, kp.n_pairs, pb.G);
     dim3 grid(kp.n_pairs * kp.n_tiles);
-    return dispatch_build<DqLaunch, D>(pb, tq, tk, tv, tdo, kp, grid, stream);
+    return dispatch_build<DqLaunch, D>(pb, tq128, tk, tv, tdo128, kp, grid, stream);
   }
 }
 
