@@ -416,7 +416,9 @@ static attn_status fwd_impl(const void* q, const void* k, const void* v, void* o
     if (e != cudaSuccess) return from_cuda(e, "attn_fwd_split counters");
   }
   a.pb.f16 = dtype == ATTN_FP16;
-  cudaError_t e = dtype == ATTN_FP32 ? launch_fwd_f32(a, st, cs) : launch_fwd_16(a, st, cs);
+  cudaError_t e = dtype != ATTN_FP32           ? launch_fwd_16(a, st, cs)
+                  : split_f32_applies(a.pb) ? launch_fwd_split_f32(a, st, cs)
+                                            : launch_fwd_f32(a, st, cs);
   return from_cuda(e, "attn_fwd launch");
 }
 

@@ -112,6 +112,10 @@ struct FwdArgs {
 cudaError_t launch_fwd_16(const FwdArgs& a, DeviceStatus* st, cudaStream_t s);  // bf16 or fp16
 cudaError_t launch_fwd_f32(const FwdArgs& a, DeviceStatus* st, cudaStream_t s);
 cudaError_t launch_fwd_d256(const FwdArgs& a, DeviceStatus* st, cudaStream_t s);  // 16-bit, d = 256
+// float32 on the bf16 tensor cores by splitting each operand into bf16 hi + lo
+// (head_dim 64 and 128, no segment ids); the CUDA-core kernels take the rest
+bool split_f32_applies(const Problem& pb);
+cudaError_t launch_fwd_split_f32(const FwdArgs& a, DeviceStatus* st, cudaStream_t s);
 
 // ---- backward --------------------------------------------------------------
 struct BwdArgs {

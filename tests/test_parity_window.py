@@ -76,11 +76,16 @@ def test_zero_width_window_is_one_key_per_row(dtype):
     o, lse = ea.forward(q, k, v, window=(0, 0))
     dq, dk, dv = ea.backward(q, k, v, o, lse, do, window=(0, 0))
     torch.cuda.synchronize()
-    # P = 2^(s - m) with s = m up to the rounding of one fused multiply-add, so
-    # O and dV equal V and dO to within an ulp of the output type
+    # The forward's P of the one key is exactly 1, so O = V to within an ulp
+    # of the output type.  The backward's P = 2^(s sl2 - lse2) recomputes s: in
+    # bf16 to within its rounding; in float32 the forward's scores come from
+    # split bf16 tensor-core products (about 2^-16 of relative error each)
+    # while the backward's may be summed differently, so dV = P dO is held to
+    # the float32 target (1e-4) rather than to an ulp
     rt = 2.0 ** -7 if dtype == "bf16" else 1e-6
     assert torch.allclose(o.float(), v.float(), rtol=rt, atol=0)
-    assert torch.allclose(dv.float(), do.float(), rtol=rt, atol=1e-30)
+    rt_bwd = 2.0 ** -7 if dtype == "bf16" else 1e-4
+    assert torch.allclose(dv.float(), do.float(), rtol=rt_bwd, atol=1e-30)
     assert dq.abs().max() <= 1e-2 * do.abs().max() and dk.abs().max() <= 1e-2 * do.abs().max()
 
 

@@ -51,6 +51,19 @@ def test_kv_length_one(d, dtype):
     assert float((lse.double() - ref).abs().max()) <= 1e-5 * max(1.0, float(ref.abs().max()))
 
 
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_kv_length_one_fp32(d):
+    """float32: head_dim 64/128 run on the tensor cores with split operands
+    (V in three exact bf16 parts, P = 1 exact), 32 on the CUDA cores."""
+    import exact_attention_34_gb300 as ea
+
+    q, k, v = _inputs(3, 300, 520, 8, 2, d, "fp32")
+    kl = torch.ones(3, dtype=torch.int32, device="cuda")
+    o, _ = ea.forward(q, k, v, kv_lens=kl)
+    torch.cuda.synchronize()
+    _expect_v0(o, v)
+
+
 @pytest.mark.parametrize("d", [64, 128, 256])
 def test_causal_first_row(d):
     """Equal lengths, causal: row 0 sees key 0 only."""
