@@ -630,7 +630,9 @@ static attn_status bwd_impl(const void* q, const void* k, const void* v, const v
   DeviceStatus* st = status_ptr();
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   a.pb.f16 = dtype == ATTN_FP16;
-  cudaError_t e = dtype == ATTN_FP32 ? launch_bwd_f32(a, st, cs) : launch_bwd_16(a, st, cs);
+  cudaError_t e = dtype != ATTN_FP32                                  ? launch_bwd_16(a, st, cs)
+                  : (deterministic == 1 && split_f32_applies(a.pb)) ? launch_bwd_split_f32(a, st, cs)
+                                                                     : launch_bwd_f32(a, st, cs);
   return from_cuda(e, "attn_bwd launch");
 }
 

@@ -155,6 +155,9 @@ cudaError_t launch_bwd_preprocess(const PreprocessArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_16(const BwdArgs& a, DeviceStatus* st, cudaStream_t s);
 cudaError_t launch_bwd_f32(const BwdArgs& a, DeviceStatus* st, cudaStream_t s);
 cudaError_t launch_bwd_d256(const BwdArgs& a, DeviceStatus* st, cudaStream_t s);  // 16-bit, d = 256
+// float32 deterministic backward on the bf16 tensor cores (split operands;
+// where split_f32_applies)
+cudaError_t launch_bwd_split_f32(const BwdArgs& a, DeviceStatus* st, cudaStream_t s);
 
 // ---- segment summary ----------------------------------------------------------
 // Writes the SegBlock records of q_seg ([B, Lq]) and kv_seg ([B, Lkv]) into

@@ -46,7 +46,10 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&f)[8]) {
   f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
-// delta[b, h, i] = sum_c dO[b, i, h, c] * O[b, i, h, c]  (float32 accumulate).
+// delta[b, h, i] = sum_c dO[b, i, h, c] * O[b, i, h, c]  (float32 accumulate
+// for 16-bit inputs; float64 for float32 inputs, whose backward subtracts
+// delta from dP values accurate to about 2^-24, so a float32 sum's rounding
+// would dominate dP - delta where a row's probability sits on one key).
 // Rows are walked in the padded [B, Hq, Lq_pad] order of the outputs; D/8
 // threads share a row, each reducing 8 consecutive elements.  Optionally it
 // also writes lse2 = lse * log2(e) (+inf where lse = -inf, so that every
@@ -66,14 +69,15 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict
   const int i = static_cast<int>(prow % Lq_pad);
   const long b = bh / Hq, h = bh % Hq;
   const bool real = prow < n_rows_pad && i < Lq;
-  float acc = 0.f;
+  using Acc = typename std::conditional<std::is_same<T, float>::value, double, float>::type;
+  Acc acc = 0;
   if (real) {
     const long row = (b * Lq + i) * Hq + h;  // row of the [B, Lq, Hq, D] tensors
     float a[8], g[8];
     load8<T>(o + row * D + part * 8, a);
     load8<T>(dout + row * D + part * 8, g);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc = fmaf(a[e], g[e], acc);
+    for (int e = 0; e < 8; ++e) acc = fma(static_cast<Acc>(a[e]), static_cast<Acc>(g[e]), acc);
     if (dq_acc != nullptr) {
       float4* z = reinterpret_cast<float4*>(dq_acc + row * D + part * 8);
       z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -83,7 +87,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict
 #pragma unroll
   for (int off = kTPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (prow < n_rows_pad && part == 0) {
-    delta[prow] = acc;  // 0 on pad rows
+    delta[prow] = static_cast<float>(acc);  // 0 on pad rows
     if (lse2 != nullptr) {
       const float l = real ? lse[bh * Lq + i] : -INFINITY;
       lse2[prow] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
