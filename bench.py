@@ -1023,6 +1023,38 @@ def run_memory_suite(args):
         torch.cuda.empty_cache()
 
 
+PROFILE_CASES = {
+    # name: (workload, dtype, backward variant)
+    "headline": ("B4 H8 T8192 d128 causal", "bf16", True),
+    "single_pass": ("B4 H8 T8192 d128 causal", "bf16", False),
+    "ordered": ("B4 H8 T8192 d128 causal", "bf16", 2),
+    "fp32": ("B4 H8 T2048 d128", "fp32", True),
+}
+
+
+def run_profile_suite(args):
+    """A fixed number of fwd+bwd steps of one case, for profilers: no timing,
+    no other rows.  `--case` picks the workload and backward variant (see
+    PROFILE_CASES); each step is one forward and one backward call."""
+    import torch
+
+    import exact_attention_34_gb300 as ea
+    from exact_attention_34_gb300 import build as eb
+
+    eb.build()
+    dev = torch.device("cuda", 0)
+    _, dt, det = PROFILE_CASES[args.case]
+    p = W.grid(2048, 128, False, "fp32") if dt == "fp32" else W.headline()
+    g = torch.Generator(device=dev).manual_seed(0)
+    q, k, v, do = (torch.randn(p.B, p.Lq, p.Hq, p.d, device=dev, generator=g).to(W.DTYPES[dt]) for _ in range(4))
+    for _ in range(args.iters):
+        o, lse = ea.forward(q, k, v, causal=p.causal)
+        ea.backward(q, k, v, o, lse, do, causal=p.causal, deterministic=det)
+    torch.cuda.synchronize()
+    st, code, site = ea.attn_device_status()
+    print(json.dumps({"suite": "profile", "case": args.case, "iters": args.iters, "device_status": code}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -1038,8 +1070,11 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true", help="print the attention grid (one JSON line per case) and exit")
     ap.add_argument("--append", default=None,
                     help="with --sweep: also append each case's line to this file and skip cases already in it")
-    ap.add_argument("--suite", choices=("gqa", "memory", "decode"),
-                    help="print the GQA, the memory or the decode suite and exit")
+    ap.add_argument("--suite", choices=("gqa", "memory", "decode", "profile"),
+                    help="print the GQA, the memory or the decode suite and exit; `profile` runs --iters steps of "
+                         "--case for a profiler")
+    ap.add_argument("--case", choices=tuple(PROFILE_CASES), default="headline", help="with --suite profile")
+    ap.add_argument("--iters", type=int, default=3, help="with --suite profile: fwd+bwd steps to run")
     ap.add_argument("--decode-lkv", type=int, default=131072, help="cache length of --suite decode")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
@@ -1048,7 +1083,8 @@ def main(argv=None):
         run_sweep(args)
         return
     if args.suite:
-        {"gqa": run_gqa_suite, "memory": run_memory_suite, "decode": run_decode_suite}[args.suite](args)
+        {"gqa": run_gqa_suite, "memory": run_memory_suite, "decode": run_decode_suite,
+         "profile": run_profile_suite}[args.suite](args)
         return
     rank, _, world = dist_env()
     if args.gpus != world and world > 1:

@@ -71,7 +71,13 @@ typedef enum {
 
 /* Element type of q, k, v, o, dout, dq, dk, dv (lse, delta and the decode
  * partials are always float32).  bf16 and fp16 run on the tensor cores with
- * fp32 accumulation; fp32 runs in true fp32. */
+ * fp32 accumulation.  fp32 at head_dim 64 and 128 (forward, and the two-pass
+ * backward) also runs on the tensor cores: every float32 operand is split
+ * into bf16 parts (two, or three exact ones where a difference cancels) and
+ * each product taken as the few bf16 MMAs that keep its error near float32
+ * rounding (within 1e-4 of the exact result); softmax and statistics stay in
+ * float32.  Head_dim 32, segment ids, the atomic backward and the decode run
+ * fp32 on the CUDA cores. */
 typedef enum { ATTN_BF16 = 0, ATTN_FP32 = 1, ATTN_FP16 = 2 } attn_dtype;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -304,9 +310,11 @@ attn_status attn_selftest_wait_timeout(int site, attn_stream_t stream);
  * (events are created by the library and reused; no device memory is
  * allocated).  attn_timing_enable(0) stops recording.  attn_timing_query waits
  * for the recorded launches of one kernel ("fwd", "bwd_preprocess",
- * "bwd_dkdv", "bwd_dkdv_atomic", "bwd_dkdv_ordered", "bwd_dq", "dq_convert", "decode", "combine",
- * or the float32 kernels "fwd_f32", "decode_f32", "bwd_dkdv_f32",
- * "bwd_dq_f32", "dq_convert_f32") and returns their summed milliseconds and
+ * "bwd_dkdv", "bwd_dkdv_atomic", "bwd_dkdv_ordered", "bwd_dq", "dq_convert",
+ * "decode", "combine", the float32 tensor-core kernels "fwd_split_f32",
+ * "bwd_dkdv_split_f32", "bwd_dq_split_f32", or the float32 CUDA-core kernels
+ * "fwd_f32", "decode_f32", "bwd_dkdv_f32", "bwd_dq_f32", "dq_convert_f32")
+ * and returns their summed milliseconds and
  * count (host pointers).  Process-wide; meant for single-threaded benchmarks.
  */
 attn_status attn_timing_enable(int on);
