@@ -47,15 +47,29 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&f)[8]) {
 }
 
 // delta[b, h, i] = sum_c dO[b, i, h, c] * O[b, i, h, c]  (float32 accumulate
-// for 16-bit inputs; float64 for float32 inputs, whose backward subtracts
-// delta from dP values accurate to about 2^-24, so a float32 sum's rounding
-// would dominate dP - delta where a row's probability sits on one key).
+// for 16-bit inputs; for float32 inputs a compensated float32 sum, whose
+// backward subtracts delta from dP values accurate to about 2^-24, so a plain
+// float32 sum's rounding would dominate dP - delta where a row's probability
+// sits on one key).  The compensated sum follows Ogita, Rump and Oishi's
+// Dot2: each product's rounding error is recovered exactly with an FMA and
+// each addition's with Knuth's TwoSum, and the errors are summed beside the
+// result, which is then as accurate as a sum in twice the working precision
+// (float64 arithmetic runs at a small fraction of the float32 rate here).
 // Rows are walked in the padded [B, Hq, Lq_pad] order of the outputs; D/8
 // threads share a row, each reducing 8 consecutive elements.  Optionally it
 // also writes lse2 = lse * log2(e) (+inf where lse = -inf, so that every
 // recomputed probability of such a row is 0), fills the pad rows
 // Lq <= i < Lq_pad with delta = 0 and lse2 = +inf, and zeroes the float32 dQ
 // accumulator of the atomic backward.
+// s += x with the rounding error of the addition added to err (Knuth's
+// TwoSum: exact for any ordering of the magnitudes).
+__device__ __forceinline__ void two_sum_add(float& s, float& err, float x) {
+  const float t = s + x;
+  const float z = t - s;
+  err += (s - (t - z)) + (x - z);
+  s = t;
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict__ o, const T* __restrict__ dout,
                                                              const float* __restrict__ lse, float* __restrict__ delta,
@@ -69,15 +83,24 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict
   const int i = static_cast<int>(prow % Lq_pad);
   const long b = bh / Hq, h = bh % Hq;
   const bool real = prow < n_rows_pad && i < Lq;
-  using Acc = typename std::conditional<std::is_same<T, float>::value, double, float>::type;
-  Acc acc = 0;
+  constexpr bool kComp = std::is_same<T, float>::value;
+  float acc = 0.f, err = 0.f;  // err: the compensation of the float32 path
   if (real) {
     const long row = (b * Lq + i) * Hq + h;  // row of the [B, Lq, Hq, D] tensors
     float a[8], g[8];
     load8<T>(o + row * D + part * 8, a);
     load8<T>(dout + row * D + part * 8, g);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc = fma(static_cast<Acc>(a[e]), static_cast<Acc>(g[e]), acc);
+    for (int e = 0; e < 8; ++e) {
+      if (kComp) {
+        const float pr = a[e] * g[e];
+        const float pe = fmaf(a[e], g[e], -pr);  // exact: a g = pr + pe
+        two_sum_add(acc, err, pr);
+        err += pe;
+      } else {
+        acc = fmaf(a[e], g[e], acc);
+      }
+    }
     if (dq_acc != nullptr) {
       float4* z = reinterpret_cast<float4*>(dq_acc + row * D + part * 8);
       z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -85,9 +108,18 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict
     }
   }
 #pragma unroll
-  for (int off = kTPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  for (int off = kTPR / 2; off > 0; off >>= 1) {
+    const float other = __shfl_xor_sync(0xffffffffu, acc, off);
+    const float other_err = __shfl_xor_sync(0xffffffffu, err, off);
+    if (kComp) {
+      two_sum_add(acc, err, other);
+      err += other_err;
+    } else {
+      acc += other;
+    }
+  }
   if (prow < n_rows_pad && part == 0) {
-    delta[prow] = static_cast<float>(acc);  // 0 on pad rows
+    delta[prow] = acc + err;  // 0 on pad rows
     if (lse2 != nullptr) {
       const float l = real ? lse[bh * Lq + i] : -INFINITY;
       lse2[prow] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
