@@ -165,8 +165,16 @@ def _dims(q, k, v=None):
     return B, Lq, Lkv, Hq, Hkv, d
 
 
+_default_scales = {}
+
+
 def _scale(scale, d):
-    return 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if scale is not None:
+        return float(scale)
+    s = _default_scales.get(d)
+    if s is None:
+        s = _default_scales[d] = 1.0 / math.sqrt(d)
+    return s
 
 
 # ---- entry points with the C names -------------------------------------------
@@ -177,9 +185,10 @@ def attn_fwd(q, k, v, o, lse, scale=None, causal=False, kv_lens=None, stream=Non
 
 def _attn_fwd(dims, q, k, v, o, lse, scale, causal, kv_lens, stream):
     B, Lq, Lkv, Hq, Hkv, d = dims
-    _check(lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Lq, Lkv, Hq, Hkv, d,
-                          _scale(scale, d), int(bool(causal)), _ptr(kv_lens), _dtype(q), _stream(stream, q)),
-           "attn_fwd")
+    st = (_lib or lib()).attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Lq, Lkv, Hq, Hkv, d,
+                                  _scale(scale, d), 1 if causal else 0, _ptr(kv_lens), _dtype(q), _stream(stream, q))
+    if st:
+        _check(st, "attn_fwd")
 
 
 def _window(window):
@@ -278,10 +287,12 @@ def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace, scale=None, causal=Fa
 def _attn_bwd(dims, q, k, v, o, lse, dout, dq, dk, dv, workspace, scale, causal, kv_lens, deterministic, stream):
     B, Lq, Lkv, Hq, Hkv, d = dims
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
-                          B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d), int(bool(causal)), _ptr(kv_lens), _dtype(q),
-                          _det(deterministic), _ptr(workspace), ws_bytes, _stream(stream, q)),
-           "attn_bwd")
+    st = (_lib or lib()).attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), B, Lq, Lkv, Hq, Hkv, d, _scale(scale, d), 1 if causal else 0,
+                                  _ptr(kv_lens), _dtype(q), _det(deterministic), _ptr(workspace), ws_bytes,
+                                  _stream(stream, q))
+    if st:
+        _check(st, "attn_bwd")
 
 
 def attn_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, workspace, window, scale=None, kv_lens=None,
@@ -398,7 +409,7 @@ def forward(q, k, v, scale=None, causal=False, kv_lens=None, stream=None, window
     log-sum-exp combine (not with segments)."""
     B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     o = torch.empty_like(q)
-    lse = torch.empty(B, Hq, Lq, device=q.device, dtype=torch.float32)
+    lse = q.new_empty((B, Hq, Lq), dtype=torch.float32)
     if num_splits != 1:
         if segments is not None:
             raise ValueError("num_splits applies to the causal, window and KV-length masks, not to segments")
@@ -426,7 +437,7 @@ def backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_lens=None, dete
     or 2 (single pass, dQ added in key-tile order; reproducible)."""
     B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     nbytes = attn_bwd_workspace_size(B, Lq, Hq, d, deterministic, q.dtype)
-    ws = torch.empty(max(nbytes, 256), device=q.device, dtype=torch.uint8)
+    ws = q.new_empty(max(nbytes, 256), dtype=torch.uint8)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if segments is not None:
         attn_bwd_segments(q, k, v, o, lse, dout, dq, dk, dv, ws, segments[0], segments[1],
@@ -451,7 +462,7 @@ def decode(q, k_cache, v_cache, scale=None, causal=False, kv_lens=None, num_spli
     lse_part = torch.empty(B, Hq, S, Lq, device=q.device, dtype=torch.float32)
     attn_decode_splitkv(q, k_cache, v_cache, o_part, lse_part, S, scale, causal, kv_lens, stream)
     o = torch.empty_like(q)
-    lse = torch.empty(B, Hq, Lq, device=q.device, dtype=torch.float32)
+    lse = q.new_empty((B, Hq, Lq), dtype=torch.float32)
     attn_decode_combine(o_part, lse_part, o, lse, stream)
     if return_partials:
         return o, lse, o_part, lse_part
