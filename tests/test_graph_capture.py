@@ -11,17 +11,20 @@ from tests._helpers import cuda
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("d", [64, 128, 256])
-def test_fwd_bwd_graph_replay_matches_eager(d):
+@pytest.mark.parametrize("d,dtype,det", [(64, "bf16", True), (128, "bf16", True), (256, "bf16", True),
+                                         (128, "bf16", 2), (128, "fp32", True), (64, "fp32", True)])
+def test_fwd_bwd_graph_replay_matches_eager(d, dtype, det):
+    """Also the ordered single pass (its counters are reset by a memset node)
+    and the float32 tensor-core path."""
     import exact_attention_34_gb300 as ea
 
-    p = W.Problem(2, 700, 900, 4, 2, d, "bf16", True, None, "graph")
+    p = W.Problem(2, 700, 900, 4, 2, d, dtype, True, None, "graph")
     q, k, v, do = cuda(*W.make_inputs(p))
     kl = torch.tensor([900, 333], dtype=torch.int32, device="cuda")
 
     def step():
         o, lse = ea.forward(q, k, v, causal=True, kv_lens=kl)
-        return (o, lse) + tuple(ea.backward(q, k, v, o, lse, do, causal=True, kv_lens=kl))
+        return (o, lse) + tuple(ea.backward(q, k, v, o, lse, do, causal=True, kv_lens=kl, deterministic=det))
 
     eager = step()
     side = torch.cuda.Stream()

@@ -142,3 +142,32 @@ def test_unsupported_combinations_are_refused():
         with pytest.raises(ea.AttnError) as e:
             ea.backward(q, k, v, o, lse, do, deterministic=ORDERED)
         assert e.value.status == ea.ATTN_ERR_UNSUPPORTED
+
+
+def draw(seed):
+    """A seeded configuration: format, head_dim, GQA group, lengths (tile
+    multiples, ragged, one), KV lengths (0, 1, partial, past Lkv), causal or a
+    window."""
+    rng = np.random.default_rng(7000 + seed)
+    dtype = ["bf16", "fp16"][rng.integers(2)]
+    d = int(rng.choice([32, 64, 128]))
+    Hkv = int(rng.choice([1, 2]))
+    G = int(rng.choice([1, 2, 4]))
+    B = int(rng.integers(1, 4))
+    lens = [1, 64, 127, 128, 129, 300, 511, 700, 1030]
+    Lq, Lkv = int(rng.choice(lens)), int(rng.choice(lens))
+    mask = rng.integers(3)
+    window = None
+    causal = mask == 1
+    if mask == 2:
+        window = (int(rng.choice([-1, 0, 5, 100, 400])), int(rng.choice([-1, 0, 3, 64])))
+    kv_lens = None
+    if rng.random() < 0.5:
+        kv_lens = tuple(int(rng.choice([0, 1, Lkv // 2, Lkv, Lkv + 7])) for _ in range(B))
+    return W.Problem(B, Lq, Lkv, Hkv * G, Hkv, d, dtype, causal, kv_lens, f"ordered_rand{seed}"), window
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_configuration(seed):
+    p, window = draw(seed)
+    check(p, window=window, seed=seed)
