@@ -69,6 +69,18 @@ DeviceStatus* status_ptr() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
+bool overlap_launch_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("EXACT_ATTN_NO_PDL");
+    return v == nullptr || v[0] == '\0' || v[0] == '0';
+  }();
+  return on;
+}
+
+namespace {
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);

@@ -3,6 +3,8 @@
 #pragma once
 
 #include <atomic>
+#include <cstdlib>
+#include <utility>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -204,6 +206,34 @@ cudaError_t ensure_dynamic_smem(int bytes) {
   cudaError_t e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(bytes, std::memory_order_relaxed);
   return e;
+}
+
+// Launch k so that it may overlap the kernel before it in the stream
+// (programmatic stream serialization): its CTAs start once every CTA of that
+// kernel has run griddepcontrol.launch_dependents (or exited).  k must run
+// griddepcontrol.wait before it reads anything that kernel may still be
+// writing, and at least one of its CTAs must run it before exiting, so that k
+// still completes after its predecessor and the stream's next operation
+// follows both.  The chain built on this: forward (waits first) ->
+// preprocess (waits first) -> dK/dV pass (waits after its prologue) -> dQ
+// pass (reads only what the preprocess wrote, which is complete once every
+// dK/dV CTA has triggered; its last CTA waits before exiting).  The
+// environment variable EXACT_ATTN_NO_PDL=1 turns the overlap off (plain
+// stream order).
+bool overlap_launch_enabled();
+template <typename... P, typename... A>
+cudaError_t launch_overlapping(void (*k)(P...), dim3 grid, int block, int smem, cudaStream_t s, A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = overlap_launch_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<A>(args)...);
 }
 
 // Opt-in per-kernel timing (attn_timing_enable): while enabled, a KernelTimer

@@ -213,6 +213,11 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // Launched to overlap the preprocess: delta and lse2 are complete from here
+  // on.  The dQ pass reads nothing this kernel writes, so its CTAs may then
+  // take the SMs that this grid's finished CTAs leave.
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 8) {
     if (lane == 0 && T > 0) {
@@ -556,6 +561,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  griddep_launch_dependents();  // the next kernel waits for this grid before it reads anything
 
   if (warp == C::kProducerWarp) {
     if (lane == 0 && T > 0) {
@@ -729,6 +735,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
+  // Launched to overlap the dK/dV pass (it reads nothing that pass writes).
+  // One CTA waits for that grid before it exits, so this grid completes after
+  // it and whatever follows in the stream sees dK and dV.
+  if (blockIdx.x == gridDim.x - 1) griddep_wait();
 }
 
 template <int D, bool kLeftBound, bool kF16, bool kSeg>
@@ -738,8 +748,8 @@ cudaError_t launch_dkdv_inst(const CUtensorMap& tq, const CUtensorMap& tk, const
   cudaError_t e = ensure_dynamic_smem<bwd_dkdv_kernel2<D, kLeftBound, kF16, kSeg>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   KernelTimer kt("bwd_dkdv", stream);
-  bwd_dkdv_kernel2<D, kLeftBound, kF16, kSeg><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
-  return cudaGetLastError();
+  return launch_overlapping(bwd_dkdv_kernel2<D, kLeftBound, kF16, kSeg>, grid, C::kThreads, C::kSmemBytes, stream, tq,
+                            tk, tv, tdo, kp);
 }
 
 template <int D, bool kLeftBound, bool kF16, bool kSeg>
@@ -749,8 +759,8 @@ cudaError_t launch_dq_inst(const CUtensorMap& tq, const CUtensorMap& tk, const C
   cudaError_t e = ensure_dynamic_smem<bwd_dq_kernel<D, kLeftBound, kF16, kSeg>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   KernelTimer kt("bwd_dq", stream);
-  bwd_dq_kernel<D, kLeftBound, kF16, kSeg><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
-  return cudaGetLastError();
+  return launch_overlapping(bwd_dq_kernel<D, kLeftBound, kF16, kSeg>, grid, C::kThreads, C::kSmemBytes, stream, tq, tk,
+                            tv, tdo, kp);
 }
 
 // The kernel build for a problem: format x (no left bound | two-sided span |

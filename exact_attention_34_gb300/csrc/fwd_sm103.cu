@@ -111,6 +111,9 @@ __global__ void __launch_bounds__(320, 1)
   const int qb = p.causal ? p.n_qblocks - 1 - tc.rank : tc.rank;
   const int hq = tc.pair % p.Hq, b = tc.pair / p.Hq;
   const int hkv = hq / p.G;
+  // launched to overlap the tail of the kernel before it: nothing in global
+  // memory is read before that grid has completed
+  griddep_wait();
   int kvl = p.Lkv;
   if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
 
@@ -188,6 +191,7 @@ __global__ void __launch_bounds__(320, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  griddep_launch_dependents();  // the next kernel waits for this grid before it reads anything
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
@@ -532,8 +536,8 @@ cudaError_t launch_fwd_inst(const CUtensorMap& tq, const CUtensorMap& tk, const 
   cudaError_t e = ensure_dynamic_smem<fwd_tc_kernel<D, kLeftBound, kF16, kSeg>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   KernelTimer kt("fwd", stream);
-  fwd_tc_kernel<D, kLeftBound, kF16, kSeg><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
-  return cudaGetLastError();
+  return launch_overlapping(fwd_tc_kernel<D, kLeftBound, kF16, kSeg>, grid, C::kThreads, C::kSmemBytes, stream, tq, tk,
+                            tv, kp);
 }
 
 template <int D>

@@ -78,6 +78,17 @@ __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Programmatic dependent launch (PTX ISA, griddepcontrol).  launch_dependents:
+// the grid that follows in the stream, if launched with programmatic stream
+// serialization, may start its CTAs once every CTA of this grid has issued it
+// (or exited).  wait: block until the grids this one was allowed to overlap
+// have completed and their writes are visible; returns at once when there are
+// none.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }

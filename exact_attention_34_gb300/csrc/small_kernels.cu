@@ -76,6 +76,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict
                                                              float* __restrict__ lse2, float* __restrict__ dq_acc,
                                                              long n_rows_pad, int Lq, int Lq_pad, int Hq) {
   constexpr int kTPR = D / 8;  // threads per row
+  griddep_wait();  // launched to overlap the forward's tail: O is complete from here on
+  griddep_launch_dependents();
   const long tid = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long prow = tid / kTPR;  // (b * Hq + h) * Lq_pad + i
   const int part = static_cast<int>(tid % kTPR);
@@ -279,9 +281,9 @@ cudaError_t run_preprocess(const PreprocessArgs& a, cudaStream_t s) {
   const long threads = n_rows * (D / 8);
   const int blocks = static_cast<int>((threads + 255) / 256);
   KernelTimer kt("bwd_preprocess", s);
-  bwd_preprocess_kernel<T, D><<<blocks, 256, 0, s>>>(static_cast<const T*>(a.o), static_cast<const T*>(a.dout),
-                                                     a.lse, a.delta, a.lse2, a.dq_acc, n_rows, a.Lq, a.Lq_pad, a.Hq);
-  return cudaGetLastError();
+  return launch_overlapping(bwd_preprocess_kernel<T, D>, dim3(blocks), 256, 0, s, static_cast<const T*>(a.o),
+                            static_cast<const T*>(a.dout), a.lse, a.delta, a.lse2, a.dq_acc, n_rows, a.Lq, a.Lq_pad,
+                            a.Hq);
 }
 
 template <typename T, int D>
