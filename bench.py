@@ -818,8 +818,10 @@ def run_sweep(args):
     and not, bf16; fwd and fwd+bwd TFLOP/s (deterministic backward).  One JSON
     line per case, median of 5 repeats with the quartiles.  Also head_dim 32
     (bf16) and fp32 at d=128 for T <= 2048.  Each case is timed twice: as eager
-    calls (host work of every call included: the Python binding, tensor-map
-    encoding and launches) and as replays of a CUDA graph that captured the
+    calls (host work of every call included: the Python binding, tensor
+    allocation, tensor-map encoding and launches), fwd+bwd also as eager calls
+    of the C-name entry points into buffers allocated once
+    (`prealloc_fwd_bwd_ms`), and as replays of a CUDA graph that captured the
     same calls (device time; what a compiled training step sees).  With
     --append FILE each finished case is also appended to FILE, and cases
     already there are skipped, so a killed sweep resumes where it stopped."""
@@ -879,8 +881,19 @@ def run_sweep(args):
             o2, lse2 = ea.forward(q, k, v, causal=c)
             return ea.backward(q, k, v, o2, lse2, do, causal=c)
 
+        # the same step through the C-name calls into buffers allocated once:
+        # no tensor allocation per call
+        o3, lse3 = ea.forward(q, k, v, causal=c)
+        ws3 = torch.empty(ea.attn_bwd_workspace_size(p.B, T, p.Hq, d, True, q.dtype), dtype=torch.uint8, device=dev)
+        g3 = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+
+        def fwd_bwd_prealloc():
+            ea.attn_fwd(q, k, v, o3, lse3, causal=c)
+            ea.attn_bwd(q, k, v, o3, lse3, do, *g3, ws3, causal=c)
+
         qf = timed(fwd_call, n)
         qb = timed(fwd_bwd_call, n)
+        qp = timed(fwd_bwd_prealloc, n)
         gf = graph_timed(fwd_call, n)
         gb = graph_timed(fwd_bwd_call, n)
         F = W.fwd_flops(p)
@@ -889,6 +902,7 @@ def run_sweep(args):
                           "fwd_tflops": round(F / qf[1] / 1e9, 1), "fwd_bwd_ms": round(qb[1], 4),
                           "fwd_bwd_ms_q1_q3": [round(qb[0], 4), round(qb[2], 4)],
                           "fwd_bwd_tflops": round(3.5 * F / qb[1] / 1e9, 1),
+                          "prealloc_fwd_bwd_ms": round(qp[1], 4),
                           "graph_fwd_ms": round(gf[1], 4), "graph_fwd_tflops": round(F / gf[1] / 1e9, 1),
                           "graph_fwd_bwd_ms": round(gb[1], 4),
                           "graph_fwd_bwd_tflops": round(3.5 * F / gb[1] / 1e9, 1)})

@@ -409,7 +409,7 @@ def forward(q, k, v, scale=None, causal=False, kv_lens=None, stream=None, window
     log-sum-exp combine (not with segments)."""
     B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     o = torch.empty_like(q)
-    lse = q.new_empty((B, Hq, Lq), dtype=torch.float32)
+    lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)  # (new_empty costs twice as much)
     if num_splits != 1:
         if segments is not None:
             raise ValueError("num_splits applies to the causal, window and KV-length masks, not to segments")
@@ -437,7 +437,7 @@ def backward(q, k, v, o, lse, dout, scale=None, causal=False, kv_lens=None, dete
     or 2 (single pass, dQ added in key-tile order; reproducible)."""
     B, Lq, Lkv, Hq, Hkv, d = _dims(q, k, v)
     nbytes = attn_bwd_workspace_size(B, Lq, Hq, d, deterministic, q.dtype)
-    ws = q.new_empty(max(nbytes, 256), dtype=torch.uint8)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if segments is not None:
         attn_bwd_segments(q, k, v, o, lse, dout, dq, dk, dv, ws, segments[0], segments[1],
@@ -462,7 +462,7 @@ def decode(q, k_cache, v_cache, scale=None, causal=False, kv_lens=None, num_spli
     lse_part = torch.empty(B, Hq, S, Lq, device=q.device, dtype=torch.float32)
     attn_decode_splitkv(q, k_cache, v_cache, o_part, lse_part, S, scale, causal, kv_lens, stream)
     o = torch.empty_like(q)
-    lse = q.new_empty((B, Hq, Lq), dtype=torch.float32)
+    lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
     attn_decode_combine(o_part, lse_part, o, lse, stream)
     if return_partials:
         return o, lse, o_part, lse_part

@@ -214,12 +214,14 @@ cudaError_t ensure_dynamic_smem(int bytes) {
 // griddepcontrol.wait before it reads anything that kernel may still be
 // writing, and at least one of its CTAs must run it before exiting, so that k
 // still completes after its predecessor and the stream's next operation
-// follows both.  The chain built on this: forward (waits first) ->
-// preprocess (waits first) -> dK/dV pass (waits after its prologue) -> dQ
-// pass (reads only what the preprocess wrote, which is complete once every
-// dK/dV CTA has triggered; its last CTA waits before exiting).  The
-// environment variable EXACT_ATTN_NO_PDL=1 turns the overlap off (plain
-// stream order).
+// follows both.  Forwards, the decode, the combine and the preprocess wait
+// before their first global read; a first backward pass after the
+// preprocess waits after its prologue and only then triggers; a pass that
+// reads nothing its predecessor writes (dQ after dK/dV, dK after dV at
+// head_dim 256) does not wait at its start, since everything it reads was
+// complete before its predecessor's CTAs triggered, and its last CTA waits
+// before exiting.  The environment variable EXACT_ATTN_NO_PDL=1 turns the
+// overlap off (plain stream order).
 bool overlap_launch_enabled();
 template <typename... P, typename... A>
 cudaError_t launch_overlapping(void (*k)(P...), dim3 grid, int block, int smem, cudaStream_t s, A&&... args) {

@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  griddep_launch_dependents();  // the next kernel waits for this grid before it reads anything
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer
@@ -316,6 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
+  // launched to overlap the dK pass (it reads nothing that pass writes): one
+  // CTA waits for it, so this grid completes after it
+  if (blockIdx.x == gridDim.x - 1) griddep_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -405,6 +409,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // The dV pass runs first after the preprocess and waits for it here
+  // (delta and lse2); the dK pass, launched to overlap the dV pass, starts
+  // only once every dV CTA got past that wait, so it reads them at once.
+  if (!kDK) griddep_wait();
+  griddep_launch_dependents();
 
   auto step_head = [&](int t) { return hk * p.G + t / sph; };
   auto step_q0 = [&](int t) { return (i_begin + t % sph) * kStep; };
@@ -616,6 +625,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
+  // launched to overlap the dV pass: one CTA waits for it, so this grid
+  // completes after it
+  if (kDK && blockIdx.x == gridDim.x - 1) griddep_wait();
 }
 
 template <bool kF16, bool kSeg>
@@ -624,8 +636,8 @@ cudaError_t launch_dq256(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   cudaError_t e = ensure_dynamic_smem<dq256_kernel<kF16, kSeg>>(DqCfg256::kSmemBytes);
   if (e != cudaSuccess) return e;
   KernelTimer kt("bwd_dq", stream);
-  dq256_kernel<kF16, kSeg><<<grid, kThreads, DqCfg256::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
-  return cudaGetLastError();
+  return launch_overlapping(dq256_kernel<kF16, kSeg>, grid, kThreads, DqCfg256::kSmemBytes, stream, tq, tk, tv, tdo,
+                            kp);
 }
 
 template <bool kDK, bool kF16, bool kSeg>
@@ -635,8 +647,8 @@ cudaError_t launch_key256(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   cudaError_t e = ensure_dynamic_smem<key256_kernel<kDK, kF16, kSeg>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   KernelTimer kt(kDK ? "bwd_dk" : "bwd_dv", stream);
-  key256_kernel<kDK, kF16, kSeg><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
-  return cudaGetLastError();
+  return launch_overlapping(key256_kernel<kDK, kF16, kSeg>, grid, kThreads, C::kSmemBytes, stream, tq, tk, tv, tdo,
+                            kp);
 }
 
 template <bool kF16, bool kSeg>

@@ -223,6 +223,11 @@ __global__ void __launch_bounds__(512, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // the atomic build is launched to overlap the preprocess: the zeroed dQ
+  // buffer, delta and lse2 are complete from here on (the ordered build
+  // follows a memset and starts after it)
+  griddep_wait();
+  griddep_launch_dependents();
   static_assert(3 * C::kRegsWork + C::kRegsCtl == 4 * 128, "register split must match the launch allocation");
 
   const int linear = kOrdered ? *item_slot : static_cast<int>(blockIdx.x);
@@ -506,6 +511,7 @@ __global__ void __launch_bounds__(512, 1)
 template <bool kF16>
 __global__ void dq_convert_kernel(const float* __restrict__ acc, uint16_t* __restrict__ dq, long n4,
                                   float scale) {
+  griddep_wait();  // launched to overlap the single pass: its adds are complete from here on
   const long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= n4) return;
   const float4 a = reinterpret_cast<const float4*>(acc)[i];
@@ -525,15 +531,18 @@ cudaError_t launch_single_pass_inst(const CUtensorMap& tq, const CUtensorMap& tk
   if (e != cudaSuccess) return e;
   {
     KernelTimer kt(kOrdered ? "bwd_dkdv_ordered" : "bwd_dkdv_atomic", stream);
-    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+    if (kOrdered) {
+      kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+      e = cudaGetLastError();
+    } else {
+      e = launch_overlapping(kern, grid, C::kThreads, C::kSmemBytes, stream, tq, tk, tv, tdo, kp);
+    }
   }
-  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long n4 = n_dq / 4;
   KernelTimer kt("dq_convert", stream);
-  dq_convert_kernel<kF16><<<static_cast<int>((n4 + 255) / 256), 256, 0, stream>>>(
-      kp.dq_acc, static_cast<uint16_t*>(kp.dq), n4, kp.scale);
-  return cudaGetLastError();
+  return launch_overlapping(dq_convert_kernel<kF16>, dim3(static_cast<unsigned>((n4 + 255) / 256)), 256, 0, stream,
+                            static_cast<const float*>(kp.dq_acc), static_cast<uint16_t*>(kp.dq), n4, kp.scale);
 }
 
 // The kernel build for a problem: format x (no left bound | two-sided span |

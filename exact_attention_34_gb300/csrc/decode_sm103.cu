@@ -74,6 +74,9 @@ __global__ void __launch_bounds__(192, 1)
   const int split = blockIdx.x, hkv = blockIdx.y, b = blockIdx.z;
   const int R = p.G * p.Lq;  // real rows
   const int n_active = (R + 31) / 32;
+  // launched to overlap the tail of the kernel before it: nothing in global
+  // memory is read before that grid has completed
+  griddep_wait();
   int kvl = p.Lkv;
   if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
   const int lo = split * p.chunk;
@@ -107,6 +110,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  griddep_launch_dependents();  // the combine waits for this grid before it reads the partials
 
   if (warp == 4) {
     if (lane == 0 && n > 0) {
@@ -321,8 +325,7 @@ cudaError_t launch_decode_inst(const CUtensorMap& tq, const CUtensorMap& tk, con
   cudaError_t e = ensure_dynamic_smem<decode_tc_kernel<D, kF16>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   KernelTimer kt("decode", stream);
-  decode_tc_kernel<D, kF16><<<grid, 192, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
-  return cudaGetLastError();
+  return launch_overlapping(decode_tc_kernel<D, kF16>, grid, 192, C::kSmemBytes, stream, tq, tk, tv, kp);
 }
 
 template <int D>

@@ -88,6 +88,9 @@ __global__ void __launch_bounds__(Cfg256::kThreads, 1)
   const int row0 = qt * kBM;
   const int hq = tc.pair % p.Hq, b = tc.pair / p.Hq;
   const int hkv = hq / p.G;
+  // launched to overlap the tail of the kernel before it: nothing in global
+  // memory is read before that grid has completed
+  griddep_wait();
   int kvl = p.Lkv;
   if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
 
@@ -129,6 +132,7 @@ __global__ void __launch_bounds__(Cfg256::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  griddep_launch_dependents();  // the next kernel waits for this grid before it reads anything
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
@@ -371,8 +375,8 @@ cudaError_t launch_fwd256_inst(const CUtensorMap& tq, const CUtensorMap& tk, con
   cudaError_t e = ensure_dynamic_smem<fwd_d256_kernel<kF16, kSeg>>(Cfg256::kSmemBytes);
   if (e != cudaSuccess) return e;
   KernelTimer kt("fwd", stream);
-  fwd_d256_kernel<kF16, kSeg><<<grid, Cfg256::kThreads, Cfg256::kSmemBytes, stream>>>(tq, tk, tv, kp);
-  return cudaGetLastError();
+  return launch_overlapping(fwd_d256_kernel<kF16, kSeg>, grid, Cfg256::kThreads, Cfg256::kSmemBytes, stream, tq, tk, tv,
+                            kp);
 }
 
 }  // namespace

@@ -148,6 +148,8 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const float* __restrict
   const long warp = (static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long n_rows = static_cast<long>(B) * Hq * Lq;
+  griddep_wait();  // launched to overlap the split kernel: its partials are complete from here on
+  griddep_launch_dependents();
   if (warp * kRows >= n_rows) return;
   long bh[kRows];
   int ri[kRows];
@@ -294,12 +296,13 @@ cudaError_t run_combine(const float* o_part, const float* lse_part, void* o, flo
   if (n_rows >= 16384) {  // four rows a warp
     const long warps = (n_rows + 3) / 4;
     const int blocks = static_cast<int>((warps * 32 + 255) / 256);
-    combine_kernel<T, D, 4><<<blocks, 256, 0, s>>>(o_part, lse_part, static_cast<T*>(o), lse, B, Lq, Hq, S);
+    return launch_overlapping(combine_kernel<T, D, 4>, dim3(blocks), 256, 0, s, o_part, lse_part, static_cast<T*>(o),
+                              lse, B, Lq, Hq, S);
   } else {
     const int blocks = static_cast<int>((n_rows * 32 + 255) / 256);
-    combine_kernel<T, D, 1><<<blocks, 256, 0, s>>>(o_part, lse_part, static_cast<T*>(o), lse, B, Lq, Hq, S);
+    return launch_overlapping(combine_kernel<T, D, 1>, dim3(blocks), 256, 0, s, o_part, lse_part, static_cast<T*>(o),
+                              lse, B, Lq, Hq, S);
   }
-  return cudaGetLastError();
 }
 
 // ---- segment summary -----------------------------------------------------------

@@ -220,6 +220,10 @@ __global__ void __launch_bounds__(288, 1) bwd_split_dkdv_kernel(const BwdKParams
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // launched to overlap the preprocess: delta and lse2 are complete from here
+  // on; the dQ pass reads nothing this kernel writes
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ converters
@@ -493,6 +497,7 @@ __global__ void __launch_bounds__(288, 1) bwd_split_dq_kernel(const BwdKParams p
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  griddep_launch_dependents();  // the next kernel waits for this grid before it reads anything
 
   if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ converters
@@ -673,6 +678,9 @@ __global__ void __launch_bounds__(288, 1) bwd_split_dq_kernel(const BwdKParams p
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
+  // launched to overlap the dK/dV pass: one CTA waits for that grid before it
+  // exits, so this grid completes after it
+  if (blockIdx.x == gridDim.x - 1) griddep_wait();
 }
 
 template <int D, bool kLeftBound>
@@ -690,8 +698,8 @@ cudaError_t run_split_bwd(BwdKParams kp, const BwdArgs& a, cudaStream_t s) {
     kp.n_pairs = pb.B * pb.Hkv;
     kp.pair_group = l2_pair_group(2l * pb.G * pb.Lq * D * 4, kp.n_pairs, 1);
     KernelTimer kt("bwd_dkdv_split_f32", s);
-    bwd_split_dkdv_kernel<D, kLeftBound><<<kp.n_pairs * kp.n_tiles, C::kThreads, C::kSmemBytes, s>>>(kp, q, k, v, dout);
-    e = cudaGetLastError();
+    e = launch_overlapping(bwd_split_dkdv_kernel<D, kLeftBound>, dim3(kp.n_pairs * kp.n_tiles), C::kThreads,
+                           C::kSmemBytes, s, kp, q, k, v, dout);
     if (e != cudaSuccess) return e;
   }
   using C = SplitDqCfg<D>;
@@ -701,8 +709,8 @@ cudaError_t run_split_bwd(BwdKParams kp, const BwdArgs& a, cudaStream_t s) {
   kp.n_pairs = pb.B * pb.Hq;
   kp.pair_group = l2_pair_group(2l * pb.Lkv * D * 4, kp.n_pairs, pb.G);
   KernelTimer kt("bwd_dq_split_f32", s);
-  bwd_split_dq_kernel<D, kLeftBound><<<kp.n_pairs * kp.n_tiles, C::kThreads, C::kSmemBytes, s>>>(kp, q, k, v, dout);
-  return cudaGetLastError();
+  return launch_overlapping(bwd_split_dq_kernel<D, kLeftBound>, dim3(kp.n_pairs * kp.n_tiles), C::kThreads,
+                            C::kSmemBytes, s, kp, q, k, v, dout);
 }
 
 }  // namespace

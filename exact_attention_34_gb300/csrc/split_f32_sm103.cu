@@ -101,6 +101,9 @@ __global__ void __launch_bounds__(288, 1) fwd_split_kernel(const SplitFwdParams 
   const int hq = tc.pair % p.Hq, b = tc.pair / p.Hq;
   const int hkv = hq / p.G;
   const int q0 = qt * kSM;
+  // launched to overlap the tail of the kernel before it: nothing in global
+  // memory is read before that grid has completed
+  griddep_wait();
   int kvl = p.Lkv;
   if (p.kv_lens != nullptr) kvl = min(max(p.kv_lens[b], 0), p.Lkv);
   // 64-key steps [jlo, jlo + n) the tile's rows need (both ends of a row's
@@ -139,6 +142,7 @@ __global__ void __launch_bounds__(288, 1) fwd_split_kernel(const SplitFwdParams 
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  griddep_launch_dependents();  // the next kernel waits for this grid before it reads anything
 
   if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ converters
@@ -350,8 +354,7 @@ cudaError_t launch_split_fwd_inst(const SplitFwdParams& kp, dim3 grid, cudaStrea
   cudaError_t e = ensure_dynamic_smem<fwd_split_kernel<D, kLeftBound>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   KernelTimer kt("fwd_split_f32", stream);
-  fwd_split_kernel<D, kLeftBound><<<grid, C::kThreads, C::kSmemBytes, stream>>>(kp);
-  return cudaGetLastError();
+  return launch_overlapping(fwd_split_kernel<D, kLeftBound>, grid, C::kThreads, C::kSmemBytes, stream, kp);
 }
 
 }  // namespace
