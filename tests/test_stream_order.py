@@ -1,0 +1,116 @@
+"""Stream order under overlapped launches.
+
+The library's kernels start while the kernel before them in the stream is
+still draining (programmatic dependent launch): each one waits for its
+predecessor before it reads what that kernel writes, the dQ pass runs beside
+the dK/dV pass, and the last CTA of every such grid waits before it exits.
+These tests check what that must preserve: an operation queued right after a
+call (no synchronisation in between) sees the call's complete outputs, and
+back-to-back calls that reuse one set of buffers and one workspace give the
+results of the same calls run one at a time."""
+
+import pytest
+import torch
+
+import workloads as W
+from tests._helpers import cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def inputs(p, seed):
+    return cuda(*W.make_inputs(p, seed))
+
+
+CASES = [
+    (W.Problem(2, 700, 900, 4, 2, 128, "bf16", True, None, "so_d128"), True),
+    (W.Problem(2, 700, 900, 4, 2, 64, "fp16", False, None, "so_d64"), True),
+    (W.Problem(1, 600, 600, 2, 2, 256, "bf16", True, None, "so_d256"), True),
+    (W.Problem(2, 300, 500, 2, 2, 128, "fp32", True, None, "so_f32"), True),
+    (W.Problem(2, 700, 900, 4, 2, 128, "bf16", True, None, "so_atomic"), False),
+    (W.Problem(2, 700, 900, 4, 2, 128, "bf16", True, None, "so_ordered"), 2),
+]
+
+
+@pytest.mark.parametrize("p,det", CASES, ids=[c[0].name for c in CASES])
+def test_outputs_complete_for_the_next_operation(p, det):
+    """Copies queued right after forward and backward equal the outputs read
+    after a synchronisation."""
+    import exact_attention_34_gb300 as ea
+
+    q, k, v, do = inputs(p, 1)
+    o, lse = ea.forward(q, k, v, causal=p.causal)
+    o_copy, lse_copy = o.clone(), lse.clone()
+    grads = ea.backward(q, k, v, o, lse, do, causal=p.causal, deterministic=det)
+    copies = [g.clone() for g in grads]
+    torch.cuda.synchronize()
+    assert ea.attn_device_status()[1] == 0
+    assert torch.equal(o_copy, o) and torch.equal(lse_copy, lse)
+    for c, g in zip(copies, grads):
+        assert torch.equal(c, g)
+
+
+@pytest.mark.parametrize("p,det", CASES[:4], ids=[c[0].name for c in CASES[:4]])
+def test_back_to_back_calls_reusing_buffers(p, det):
+    """Three fwd+bwd steps on different inputs into one set of buffers and one
+    workspace, queued without synchronisation, each result copied right after
+    its call: every copy equals the same step run alone."""
+    import exact_attention_34_gb300 as ea
+
+    steps = [inputs(p, s) for s in (2, 3, 4)]
+    B, Lq, Hq, d = p.B, p.Lq, p.Hq, p.d
+    q0, k0, v0, _ = steps[0]
+    o, lse = torch.empty_like(q0), torch.empty((B, Hq, Lq), dtype=torch.float32, device=q0.device)
+    dq, dk, dv = torch.empty_like(q0), torch.empty_like(k0), torch.empty_like(v0)
+    ws = torch.empty(max(ea.attn_bwd_workspace_size(B, Lq, Hq, d, det, q0.dtype), 256), dtype=torch.uint8,
+                     device=q0.device)
+    queued = []
+    for q, k, v, do in steps:
+        ea.attn_fwd(q, k, v, o, lse, causal=p.causal)
+        ea.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, ws, causal=p.causal, deterministic=det)
+        queued.append(tuple(t.clone() for t in (o, lse, dq, dk, dv)))
+    torch.cuda.synchronize()
+    for (q, k, v, do), got in zip(steps, queued):
+        o1, lse1 = ea.forward(q, k, v, causal=p.causal)
+        torch.cuda.synchronize()
+        g1 = ea.backward(q, k, v, o1, lse1, do, causal=p.causal, deterministic=det)
+        torch.cuda.synchronize()
+        for a, b in zip(got, (o1, lse1) + tuple(g1)):
+            assert torch.equal(a, b)
+    assert ea.attn_device_status()[1] == 0
+
+
+def test_backward_twice_on_one_workspace():
+    """Two backward calls in a row on one workspace (the second's preprocess
+    rewrites delta while nothing of the first may still read it)."""
+    import exact_attention_34_gb300 as ea
+
+    p = W.Problem(2, 1030, 1030, 8, 2, 128, "bf16", True, None, "so_twice")
+    q, k, v, do = inputs(p, 5)
+    do2 = torch.randn_like(do)
+    o, lse = ea.forward(q, k, v, causal=True)
+    ws = torch.empty(ea.attn_bwd_workspace_size(p.B, p.Lq, p.Hq, p.d, True, q.dtype), dtype=torch.uint8,
+                     device=q.device)
+    out = []
+    for g in (do, do2):
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ea.attn_bwd(q, k, v, o, lse, g, dq, dk, dv, ws, causal=True)
+        out.append((dq, dk, dv))
+    torch.cuda.synchronize()
+    for g, got in zip((do, do2), out):
+        ref = ea.backward(q, k, v, o, lse, g, causal=True)
+        torch.cuda.synchronize()
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b)
+
+
+def test_decode_then_copy():
+    import exact_attention_34_gb300 as ea
+
+    p = W.Problem(2, 1, 5000, 8, 2, 128, "bf16", False, (5000, 1777), "so_decode")
+    q, k, v, _ = inputs(p, 6)
+    kl = torch.tensor(p.kv_lens, dtype=torch.int32, device=q.device)
+    o, lse = ea.decode(q, k, v, kv_lens=kl)
+    o_copy, lse_copy = o.clone(), lse.clone()
+    torch.cuda.synchronize()
+    assert torch.equal(o_copy, o) and torch.equal(lse_copy, lse)
