@@ -114,3 +114,35 @@ def test_decode_then_copy():
     o_copy, lse_copy = o.clone(), lse.clone()
     torch.cuda.synchronize()
     assert torch.equal(o_copy, o) and torch.equal(lse_copy, lse)
+
+
+def test_plain_stream_order_gives_identical_results(tmp_path):
+    """The same fwd+bwd with the overlapped launches turned off
+    (EXACT_ATTN_NO_PDL=1, in a fresh process) gives the same bits."""
+    import os
+    import subprocess
+    import sys
+
+    import exact_attention_34_gb300 as ea
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    script = (
+        "import sys, torch; sys.path.insert(0, %r)\n"
+        "import exact_attention_34_gb300 as ea, workloads as W\n"
+        "from tests._helpers import cuda\n"
+        "p = W.Problem(2, 900, 1100, 8, 2, 128, 'bf16', True, None, 'so_nopdl')\n"
+        "q, k, v, do = cuda(*W.make_inputs(p, 7))\n"
+        "o, lse = ea.forward(q, k, v, causal=True)\n"
+        "g = ea.backward(q, k, v, o, lse, do, causal=True)\n"
+        "torch.save([t.cpu() for t in (o, lse) + tuple(g)], %r)\n"
+    ) % (root, str(tmp_path / "plain.pt"))
+    env = dict(os.environ, EXACT_ATTN_NO_PDL="1")
+    subprocess.run([sys.executable, "-c", script], check=True, env=env, cwd=root, timeout=600)
+    plain = torch.load(tmp_path / "plain.pt")
+    p = W.Problem(2, 900, 1100, 8, 2, 128, "bf16", True, None, "so_nopdl")
+    q, k, v, do = inputs(p, 7)
+    o, lse = ea.forward(q, k, v, causal=True)
+    g = ea.backward(q, k, v, o, lse, do, causal=True)
+    torch.cuda.synchronize()
+    for a, b in zip((o, lse) + tuple(g), plain):
+        assert torch.equal(a.cpu(), b)
