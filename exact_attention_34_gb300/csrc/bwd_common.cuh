@@ -15,7 +15,7 @@ struct BwdKParams {
   void* dq;
   void* dk;
   void* dv;
-  float* dq_acc;       // single-pass variants: [B, Lq, Hq, dh] fp32, zeroed before the launch
+  float* dq_acc;       // single-pass variants: [B, Lq, Hq, dh] fp32, zeroed by the preprocess (waited for before the first add)
   int* dq_turn;        // ordered single pass: [B, Hq, nq] turn counters, zeroed before the launch
   int* ticket;         // ordered single pass: work-item ticket, zeroed before the launch
   int nq;              // 128-row query tiles per sequence

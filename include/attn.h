@@ -30,6 +30,13 @@
  *     allocates, frees or synchronises.  Calls are asynchronous on `stream`
  *     (NULL = the legacy default stream).  Pointers named here are device
  *     pointers unless stated otherwise.
+ *   - Stream order holds: every output of a call is complete for the next
+ *     operation queued on its stream, and the call reads its inputs only
+ *     after the operations queued before it have completed.  Internally the
+ *     kernels are launched with programmatic stream serialization, so that
+ *     each one starts while the kernel before it drains and waits on the GPU
+ *     before it reads what that kernel writes; setting the environment
+ *     variable EXACT_ATTN_NO_PDL=1 before the first call turns this off.
  *   - Every tensor pointer must be 16-byte aligned and, for bf16, every row
  *     stride (Hq*d, Hkv*d elements) is then a multiple of 16 bytes.
  *   - Arguments are validated on the host before anything is launched; a bad
@@ -45,7 +52,8 @@
  *     At d = 256 the backward is deterministic for either value of
  *     `deterministic`.
  *   - Calls are thread-safe: no mutable global state is shared between calls
- *     (tensor-map descriptors are built per call and passed by value).
+ *     (tensor-map descriptors are passed by value; the small cache that saves
+ *     re-encoding them is per host thread).
  */
 #ifndef GB300_ATTN_H
 #define GB300_ATTN_H

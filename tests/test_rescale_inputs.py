@@ -7,7 +7,7 @@ workload inputs give almost none.  No GPU."""
 import numpy as np
 
 import workloads as W
-from tests.test_parity_rescale import WINDOW_GROWTH, ramped_inputs
+from tests.test_parity_rescale import WINDOW_GROWTHS, ramped_inputs
 
 THRESHOLD = 8.0  # log2 units, as in the forward kernel
 
@@ -51,6 +51,7 @@ def test_plain_inputs_rarely_rescale():
 
 def test_window_inputs_rescale():
     p = W.Problem(2, 700, 700, 4, 2, 128, "bf16", False, None, "rampwin")
-    q, k, _, _ = ramped_inputs(p, 3, WINDOW_GROWTH)
-    for window in ((200, 0), (100, 50)):
-        assert rescale_events(q, k, 2.0 / np.sqrt(128), False, window) >= 300
+    for growth in WINDOW_GROWTHS:
+        q, k, _, _ = ramped_inputs(p, 3, growth)
+        for window in ((200, 0), (100, 50)):
+            assert rescale_events(q, k, 2.0 / np.sqrt(128), False, window) >= 300
