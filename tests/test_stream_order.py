@@ -9,6 +9,7 @@ call (no synchronisation in between) sees the call's complete outputs, and
 back-to-back calls that reuse one set of buffers and one workspace give the
 results of the same calls run one at a time."""
 
+import numpy as np
 import pytest
 import torch
 
@@ -146,3 +147,63 @@ def test_plain_stream_order_gives_identical_results(tmp_path):
     torch.cuda.synchronize()
     for a, b in zip((o, lse) + tuple(g), plain):
         assert torch.equal(a.cpu(), b)
+
+
+def _random_call(rng, ea, dev):
+    """One seeded library call and a function that runs it (returning its
+    outputs, freshly allocated)."""
+    kind = rng.choice(["fwd_bwd", "fwd_bwd", "window", "segments", "split", "decode", "d256", "fp32"])
+    B = int(rng.integers(1, 3))
+    Hkv = int(rng.choice([1, 2]))
+    Hq = Hkv * int(rng.choice([1, 2, 4]))
+    d = 64 if kind == "d256" else int(rng.choice([64, 128]))
+    d = 256 if kind == "d256" else d
+    dtype = "fp32" if kind == "fp32" else str(rng.choice(["bf16", "fp16"]))
+    Lq = 1 if kind == "decode" else int(rng.choice([129, 300, 640]))
+    Lkv = int(rng.choice([129, 300, 640, 1500]))
+    if kind in ("window", "segments"):
+        Lkv = Lq
+    causal = bool(rng.integers(2)) and kind in ("fwd_bwd", "d256", "fp32")
+    p = W.Problem(B, Lq, Lkv, Hq, Hkv, d, dtype, causal, None, f"mix_{kind}")
+    q, k, v, do = inputs(p, int(rng.integers(1 << 30)))
+    det = int(rng.choice([1, 2])) if (kind == "fwd_bwd" and dtype != "fp32" and d <= 128) else 1
+    window = (int(rng.integers(0, 200)), int(rng.integers(0, 50))) if kind == "window" else None
+    segs = None
+    if kind == "segments":
+        ids = torch.tensor(np.sort(rng.integers(0, 4, size=(B, Lq)), axis=1).astype(np.int32), device=dev)
+        segs = (ids, ids)
+    kl = None
+    if kind in ("split", "decode"):
+        kl = torch.tensor([int(rng.integers(0, Lkv + 1)) for _ in range(B)], dtype=torch.int32, device=dev)
+
+    def run():
+        if kind == "decode":
+            return ea.decode(q, k, v, kv_lens=kl)
+        if kind == "split":
+            return ea.forward(q, k, v, kv_lens=kl, num_splits=2)
+        o, lse = ea.forward(q, k, v, causal=causal, window=window, segments=segs)
+        return (o, lse) + tuple(ea.backward(q, k, v, o, lse, do, causal=causal, window=window, segments=segs,
+                                            deterministic=det))
+
+    return run
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_random_mixed_calls_queued_back_to_back(seed):
+    """Twenty seeded calls of every kind (masks, backward variants, head_dim
+    256, fp32, split forward, decode) queued on one stream without
+    synchronisation, each output copied right after its call: every copy
+    equals the same call run alone."""
+    import exact_attention_34_gb300 as ea
+
+    rng = np.random.default_rng(900 + seed)
+    dev = torch.device("cuda")
+    calls = [_random_call(rng, ea, dev) for _ in range(20)]
+    queued = [[t.clone() for t in run()] for run in calls]
+    torch.cuda.synchronize()
+    assert ea.attn_device_status()[1] == 0
+    for run, got in zip(calls, queued):
+        ref = run()
+        torch.cuda.synchronize()
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b)
