@@ -1043,6 +1043,7 @@ PROFILE_CASES = {
     "single_pass": ("B4 H8 T8192 d128 causal", "bf16", False),
     "ordered": ("B4 H8 T8192 d128 causal", "bf16", 2),
     "fp32": ("B4 H8 T2048 d128", "fp32", True),
+    "d64": ("B4 H8 T8192 d64 causal", "bf16", True),
 }
 
 
@@ -1058,7 +1059,8 @@ def run_profile_suite(args):
     eb.build()
     dev = torch.device("cuda", 0)
     _, dt, det = PROFILE_CASES[args.case]
-    p = W.grid(2048, 128, False, "fp32") if dt == "fp32" else W.headline()
+    p = W.grid(2048, 128, False, "fp32") if dt == "fp32" else W.grid(8192, 64, True) if args.case == "d64" else \
+        W.headline()
     g = torch.Generator(device=dev).manual_seed(0)
     q, k, v, do = (torch.randn(p.B, p.Lq, p.Hq, p.d, device=dev, generator=g).to(W.DTYPES[dt]) for _ in range(4))
     for _ in range(args.iters):
