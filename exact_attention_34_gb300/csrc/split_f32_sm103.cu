@@ -156,24 +156,31 @@ __global__ void __launch_bounds__(288, 1) fwd_split_kernel(const SplitFwdParams 
       __syncwarp();
       if (lane == 0) mbar_arrive(q_full);
     }
-    for (int j = 0; j < n && ok; ++j) {
-      const int buf = j & 1, use = j >> 1;
-      const int key0 = (jlo + j) * kSN;
-      uint8_t* kh = smem + C::kOffK + 2 * buf * C::kKVPart;
-      if (use > 0) ok = __all_sync(0xffffffffu, mbar_wait(&empty_k[buf], (use - 1) & 1, abort_flag, p.status, 121));
-      if (!ok) break;
-      convert_tile<D, kSN, kSN>(p.k, b, p.Lkv, p.Hkv, hkv, key0, kvl, kh, kh + C::kKVPart, 0, t);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&full_k[buf]);
-      uint8_t* vh = smem + C::kOffV + 3 * buf * C::kKVPart;
-      if (use > 0) ok = __all_sync(0xffffffffu, mbar_wait(&empty_v[buf], (use - 1) & 1, abort_flag, p.status, 122));
-      if (!ok) break;
-      convert_tile<D, kSN, kSN, true>(p.v, b, p.Lkv, p.Hkv, hkv, key0, kvl, vh, vh + 2 * C::kKVPart, 0, t,
-                                      vh + C::kKVPart);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&full_v[buf]);
+    // K of step u, then V of step u - 1: a K buffer is released when S of
+    // its step has run, a V buffer only after PV, so converting K one step
+    // ahead keeps S(j + 2) from waiting behind V(j + 1), which waits for PV(j - 1).
+    for (int u = 0; u <= n && ok; ++u) {
+      if (u < n) {
+        const int buf = u & 1, use = u >> 1;
+        uint8_t* kh = smem + C::kOffK + 2 * buf * C::kKVPart;
+        if (use > 0) ok = __all_sync(0xffffffffu, mbar_wait(&empty_k[buf], (use - 1) & 1, abort_flag, p.status, 121));
+        if (!ok) break;
+        convert_tile<D, kSN, kSN>(p.k, b, p.Lkv, p.Hkv, hkv, (jlo + u) * kSN, kvl, kh, kh + C::kKVPart, 0, t);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full_k[buf]);
+      }
+      if (u > 0) {
+        const int w = u - 1, buf = w & 1, use = w >> 1;
+        uint8_t* vh = smem + C::kOffV + 3 * buf * C::kKVPart;
+        if (use > 0) ok = __all_sync(0xffffffffu, mbar_wait(&empty_v[buf], (use - 1) & 1, abort_flag, p.status, 122));
+        if (!ok) break;
+        convert_tile<D, kSN, kSN, true>(p.v, b, p.Lkv, p.Hkv, hkv, (jlo + w) * kSN, kvl, vh, vh + 2 * C::kKVPart, 0,
+                                        t, vh + C::kKVPart);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full_v[buf]);
+      }
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------ MMA issuer
