@@ -1,5 +1,6 @@
-"""Tensors past 2^31 elements: every address the kernels form from batch,
-row, head and column indices must be 64-bit.
+"""Query-side tensors past 2^31 elements (the key side is covered by
+test_max_size.py): every address the kernels form from batch, row, head and
+column indices must be 64-bit.
 
 q, o, dO and dQ hold B1 x (2^21 + 300) rows x 8 heads x 128 = 2.15e9
 elements (4.3 GB each in bf16) against 200 keys.  The last 300 rows (all of
