@@ -10,13 +10,26 @@
 namespace attn {
 namespace {
 
+// Eight consecutive elements as loaded (16 bytes of 16-bit values, 32 of
+// float32), converted to float32 only when used, so that several rows' loads
+// can be in flight before the first is needed.
 template <typename T>
-__device__ __forceinline__ void load8(const T* p, float (&f)[8]);
+struct Raw8 {
+  uint4 v[sizeof(T) / 2];
+};
+
+template <typename T>
+__device__ __forceinline__ void raw_load8(const T* p, Raw8<T>& r) {
+#pragma unroll
+  for (int j = 0; j < static_cast<int>(sizeof(T) / 2); ++j) r.v[j] = reinterpret_cast<const uint4*>(p)[j];
+}
+
+template <typename T>
+__device__ __forceinline__ void unpack8(const Raw8<T>& r, float (&f)[8]);
 
 template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&f)[8]) {
-  const uint4 u = *reinterpret_cast<const uint4*>(p);
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+__device__ __forceinline__ void unpack8<__nv_bfloat16>(const Raw8<__nv_bfloat16>& r, float (&f)[8]) {
+  const uint32_t w[4] = {r.v[0].x, r.v[0].y, r.v[0].z, r.v[0].w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     f[2 * i] = __uint_as_float(w[i] << 16);
@@ -25,9 +38,8 @@ __device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, flo
 }
 
 template <>
-__device__ __forceinline__ void load8<__half>(const __half* p, float (&f)[8]) {
-  const uint4 u = *reinterpret_cast<const uint4*>(p);
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+__device__ __forceinline__ void unpack8<__half>(const Raw8<__half>& r, float (&f)[8]) {
+  const uint32_t w[4] = {r.v[0].x, r.v[0].y, r.v[0].z, r.v[0].w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     __half2 h;
@@ -39,11 +51,14 @@ __device__ __forceinline__ void load8<__half>(const __half* p, float (&f)[8]) {
 }
 
 template <>
-__device__ __forceinline__ void load8<float>(const float* p, float (&f)[8]) {
-  const float4 a = *reinterpret_cast<const float4*>(p);
-  const float4 b = *reinterpret_cast<const float4*>(p + 4);
-  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+__device__ __forceinline__ void unpack8<float>(const Raw8<float>& r, float (&f)[8]) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    f[4 * j] = __uint_as_float(r.v[j].x);
+    f[4 * j + 1] = __uint_as_float(r.v[j].y);
+    f[4 * j + 2] = __uint_as_float(r.v[j].z);
+    f[4 * j + 3] = __uint_as_float(r.v[j].w);
+  }
 }
 
 // delta[b, h, i] = sum_c dO[b, i, h, c] * O[b, i, h, c]  (float32 accumulate
@@ -55,8 +70,11 @@ __device__ __forceinline__ void load8<float>(const float* p, float (&f)[8]) {
 // each addition's with Knuth's TwoSum, and the errors are summed beside the
 // result, which is then as accurate as a sum in twice the working precision
 // (float64 arithmetic runs at a small fraction of the float32 rate here).
-// Rows are walked in the padded [B, Hq, Lq_pad] order of the outputs; D/8
-// threads share a row, each reducing 8 consecutive elements.  Optionally it
+// Rows are walked in the padded [B, Hq, Lq_pad] order of the outputs: the
+// grid's (z, y) indices give the (b, h) pair (65535 pairs per z slice), its x
+// index a run of rows, so that no thread divides its index in 64 bits; D/8
+// threads share a row, each reducing 8 consecutive elements, and each thread
+// takes kPreRows rows, whose loads it issues before the first sum.  Optionally it
 // also writes lse2 = lse * log2(e) (+inf where lse = -inf, so that every
 // recomputed probability of such a row is 0), fills the pad rows
 // Lq <= i < Lq_pad with delta = 0 and lse2 = +inf, and zeroes the float32 dQ
@@ -70,28 +88,23 @@ __device__ __forceinline__ void two_sum_add(float& s, float& err, float x) {
   s = t;
 }
 
+// One thread's share of row i of pair bh = b * Hq + h, from its loaded
+// elements of O (ra) and dO (rg).
 template <typename T, int D>
-__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict__ o, const T* __restrict__ dout,
-                                                             const float* __restrict__ lse, float* __restrict__ delta,
-                                                             float* __restrict__ lse2, float* __restrict__ dq_acc,
-                                                             long n_rows_pad, int Lq, int Lq_pad, int Hq) {
-  constexpr int kTPR = D / 8;  // threads per row
-  griddep_wait();  // launched to overlap the forward's tail: O is complete from here on
-  griddep_launch_dependents();
-  const long tid = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long prow = tid / kTPR;  // (b * Hq + h) * Lq_pad + i
-  const int part = static_cast<int>(tid % kTPR);
-  const long bh = prow / Lq_pad;
-  const int i = static_cast<int>(prow % Lq_pad);
-  const long b = bh / Hq, h = bh % Hq;
-  const bool real = prow < n_rows_pad && i < Lq;
+__device__ __forceinline__ void preprocess_row(const Raw8<T>& ra, const Raw8<T>& rg, const float* __restrict__ lse,
+                                               float* __restrict__ delta, float* __restrict__ lse2,
+                                               float* __restrict__ dq_acc, long b, long h, long bh, int i, int part,
+                                               int Lq, int Lq_pad, int Hq) {
+  constexpr int kTPR = D / 8;
+  const long prow = bh * Lq_pad + i;
+  const bool real = i < Lq;
   constexpr bool kComp = std::is_same<T, float>::value;
   float acc = 0.f, err = 0.f;  // err: the compensation of the float32 path
   if (real) {
     const long row = (b * Lq + i) * Hq + h;  // row of the [B, Lq, Hq, D] tensors
     float a[8], g[8];
-    load8<T>(o + row * D + part * 8, a);
-    load8<T>(dout + row * D + part * 8, g);
+    unpack8<T>(ra, a);
+    unpack8<T>(rg, g);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       if (kComp) {
@@ -120,13 +133,53 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict
       acc += other;
     }
   }
-  if (prow < n_rows_pad && part == 0) {
+  if (i < Lq_pad && part == 0) {
     delta[prow] = acc + err;  // 0 on pad rows
     if (lse2 != nullptr) {
       const float l = real ? lse[bh * Lq + i] : -INFINITY;
       lse2[prow] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
     }
   }
+}
+
+constexpr int kPreRows = 2;  // rows per thread in the preprocess (1 and 4 measured slower)
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const T* __restrict__ o, const T* __restrict__ dout,
+                                                             const float* __restrict__ lse, float* __restrict__ delta,
+                                                             float* __restrict__ lse2, float* __restrict__ dq_acc,
+                                                             long n_bh, int Lq, int Lq_pad, int Hq) {
+  constexpr int kTPR = D / 8;  // threads per row
+  griddep_wait();  // launched to overlap the forward's tail: O is complete from here on
+  griddep_launch_dependents();
+  constexpr int kRows = 256 / kTPR;  // rows of one pass of the block
+  const int part = static_cast<int>(threadIdx.x % kTPR);
+  const int i0 = static_cast<int>(blockIdx.x) * kRows * kPreRows + static_cast<int>(threadIdx.x / kTPR);
+  const long bh = static_cast<long>(blockIdx.z) * 65535 + blockIdx.y;
+  if (bh >= n_bh) return;  // whole block: the last z slice is partly empty
+  long b, h;
+  if (n_bh <= 0x7fffffffL) {  // 32-bit division where the pair index fits
+    const unsigned q = static_cast<unsigned>(bh) / static_cast<unsigned>(Hq);
+    b = q;
+    h = static_cast<long>(static_cast<unsigned>(bh) - q * static_cast<unsigned>(Hq));
+  } else {
+    b = bh / Hq;
+    h = bh - b * Hq;
+  }
+  Raw8<T> ra[kPreRows], rg[kPreRows];
+#pragma unroll
+  for (int r = 0; r < kPreRows; ++r) {  // every row's loads in flight before the first sum
+    const int i = i0 + r * kRows;
+    ra[r] = rg[r] = Raw8<T>{};
+    if (i < Lq) {
+      const long row = (b * Lq + i) * Hq + h;
+      raw_load8<T>(o + row * D + part * 8, ra[r]);
+      raw_load8<T>(dout + row * D + part * 8, rg[r]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kPreRows; ++r)
+    preprocess_row<T, D>(ra[r], rg[r], lse, delta, lse2, dq_acc, b, h, bh, i0 + r * kRows, part, Lq, Lq_pad, Hq);
 }
 
 // Log-sum-exp combine of split partials, for output rows (b, h, i):
@@ -279,12 +332,13 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const float* __restrict
 
 template <typename T, int D>
 cudaError_t run_preprocess(const PreprocessArgs& a, cudaStream_t s) {
-  const long n_rows = static_cast<long>(a.B) * a.Hq * a.Lq_pad;
-  const long threads = n_rows * (D / 8);
-  const int blocks = static_cast<int>((threads + 255) / 256);
+  constexpr int kRows = 256 / (D / 8) * kPreRows;  // rows per block
+  const long n_bh = static_cast<long>(a.B) * a.Hq;
+  const dim3 grid((a.Lq_pad + kRows - 1) / kRows, static_cast<unsigned>(n_bh < 65535 ? n_bh : 65535),
+                  static_cast<unsigned>((n_bh + 65534) / 65535));
   KernelTimer kt("bwd_preprocess", s);
-  return launch_overlapping(bwd_preprocess_kernel<T, D>, dim3(blocks), 256, 0, s, static_cast<const T*>(a.o),
-                            static_cast<const T*>(a.dout), a.lse, a.delta, a.lse2, a.dq_acc, n_rows, a.Lq, a.Lq_pad,
+  return launch_overlapping(bwd_preprocess_kernel<T, D>, grid, 256, 0, s, static_cast<const T*>(a.o),
+                            static_cast<const T*>(a.dout), a.lse, a.delta, a.lse2, a.dq_acc, n_bh, a.Lq, a.Lq_pad,
                             a.Hq);
 }
 
