@@ -69,30 +69,6 @@ struct DkdvCfg2 {
   static constexpr int kThreads = 320;
 };
 
-// Store columns [c0, c0 + NC) of one fp32 TMEM row as bf16 (times mul).
-template <int NC, bool kF16>
-__device__ __forceinline__ void store_cols16(uint32_t taddr, uint16_t* dst, float mul, bool do_store,
-                                                bool zero) {
-#pragma unroll
-  for (int c = 0; c < NC / 16; ++c) {
-    uint32_t r[16];
-    if (!zero) {
-      tmem_ld16(taddr + c * 16, r);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) r[i] = 0u;
-    }
-    uint32_t pk[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) pk[i] = pack2<kF16>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
-    if (do_store) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 16);
-      d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-    }
-  }
-}
-
 // TMEM column (relative to the step's S^T / S block) of the packed A operand
 // for query (or key) k-step k of half h, when NWG warpgroups each convert
 // 64 / NWG columns of a half.
@@ -132,7 +108,8 @@ template <int D, bool kLeftBound, bool kF16, bool kSeg>
 __global__ void __launch_bounds__(320, 1)
     bwd_dkdv_kernel2(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                     const BwdKParams p) {
+                     const __grid_constant__ CUtensorMap tm_dk,
+                     const __grid_constant__ CUtensorMap tm_dv, const BwdKParams p) {
   using C = DkdvCfg2<D>;
   constexpr int NQ = C::kQSlots, NO = C::kDOSlots, BM = C::kBM;
   constexpr uint32_t kColS = 256, kColDP = 384;
@@ -382,14 +359,26 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive(ds_ready);
     }
     if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 68));
+    // dK (warpgroup 0, times scale) and dV (warpgroup 1) go through the Q ring,
+    // idle once every MMA has completed, and out with TMA stores, which clip
+    // the rows past Lkv and the columns past the stored head_dim.  (Each thread
+    // storing its own row would put 32 rows, a row stride apart, into every
+    // store instruction: the epilogue took ~2.9 us per CTA that way.)
     if (ok) {
       tc_fence_after();
-      const bool st = j < p.Lkv;
-      const size_t off = ((static_cast<size_t>(b) * p.Lkv + (st ? j : 0)) * p.Hkv + hk) * p.dh;
-      if (w == 0)
-        store_row16<D, kF16>(t_lane + 0, reinterpret_cast<uint16_t*>(p.dk) + off, p.scale, st, T == 0, p.dh);
-      else
-        store_row16<D, kF16>(t_lane + 128, reinterpret_cast<uint16_t*>(p.dv) + off, 1.0f, st, T == 0, p.dh);
+      stage_row16<D, kF16>(t_lane + (w == 0 ? 0 : 128), sQ + w * (D / 64) * C::kBox, r, w == 0 ? p.scale : 1.0f,
+                           T == 0);
+      fence_proxy_async_smem();
+    }
+    named_barrier_sync(1, 256);
+    if (threadIdx.x == 0 && *abort_flag == 0) {
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_store_4d(&tm_dk, sQ + c * C::kBox, c * 64, j0, hk, b);
+        tma_store_4d(&tm_dv, sQ + (D / 64 + c) * C::kBox, c * 64, j0, hk, b);
+      }
+      tma_store_commit();
+      tma_store_wait_read();  // the shared memory is released when the CTA exits
     }
   }
 
@@ -489,6 +478,7 @@ template <int D, bool kLeftBound, bool kF16, bool kSeg>
 __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_dq,
                   const BwdKParams p) {
   using C = DqCfg<D>;
   constexpr int NK = C::kKSlots, NV = C::kVSlots, BN = C::kBN;
@@ -718,14 +708,21 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       }
     }
     if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 38));
+    // dQ goes through the K ring, idle once every MMA has completed, and out
+    // with TMA stores (rows past Lq and columns past the stored head_dim are
+    // clipped); warpgroup w stages head-dim columns [w D / NWG, (w + 1) D / NWG)
     if (ok) {
       tc_fence_after();
-      // warpgroup w stores head-dim columns [w * D / NWG, (w + 1) * D / NWG)
       constexpr int kPer = D / C::kNWG;
-      const bool st = i < p.Lq;
-      uint16_t* dst = reinterpret_cast<uint16_t*>(p.dq) +
-                      ((static_cast<size_t>(b) * p.Lq + (st ? i : 0)) * p.Hq + h) * p.dh + w * kPer;
-      if (w * kPer < p.dh) store_cols16<kPer, kF16>(t_lane + w * kPer, dst, p.scale, st, T == 0);
+      stage_row16<kPer, kF16>(t_lane + w * kPer, sK, r, p.scale, T == 0, w * kPer);
+      fence_proxy_async_smem();
+    }
+    named_barrier_sync(1, 128 * C::kNWG);
+    if (threadIdx.x == 0 && *abort_flag == 0) {
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) tma_store_4d(&tm_dq, sK + c * C::kBox, c * 64, q0, h, b);
+      tma_store_commit();
+      tma_store_wait_read();  // the shared memory is released when the CTA exits
     }
   }
 
@@ -743,24 +740,26 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
 
 template <int D, bool kLeftBound, bool kF16, bool kSeg>
 cudaError_t launch_dkdv_inst(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                             const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, cudaStream_t stream) {
+                             const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                             const BwdKParams& kp, dim3 grid, cudaStream_t stream) {
   using C = DkdvCfg2<D>;
   cudaError_t e = ensure_dynamic_smem<bwd_dkdv_kernel2<D, kLeftBound, kF16, kSeg>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   KernelTimer kt("bwd_dkdv", stream);
   return launch_overlapping(bwd_dkdv_kernel2<D, kLeftBound, kF16, kSeg>, grid, C::kThreads, C::kSmemBytes, stream, tq,
-                            tk, tv, tdo, kp);
+                            tk, tv, tdo, tdk, tdv, kp);
 }
 
 template <int D, bool kLeftBound, bool kF16, bool kSeg>
 cudaError_t launch_dq_inst(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, cudaStream_t stream) {
+                           const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdKParams& kp, dim3 grid,
+                           cudaStream_t stream) {
   using C = DqCfg<D>;
   cudaError_t e = ensure_dynamic_smem<bwd_dq_kernel<D, kLeftBound, kF16, kSeg>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   KernelTimer kt("bwd_dq", stream);
   return launch_overlapping(bwd_dq_kernel<D, kLeftBound, kF16, kSeg>, grid, C::kThreads, C::kSmemBytes, stream, tq, tk,
-                            tv, tdo, kp);
+                            tv, tdo, tdq, kp);
 }
 
 // The kernel build for a problem: format x (no left bound | two-sided span |
@@ -858,7 +857,12 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
       return launch_single_pass<D>(tq128, tk, tv, tdo128, kp, grid, static_cast<long>(pb.B) * pb.Lq * pb.Hq * pb.d,
                                    pb.f16 != 0, a.deterministic == 2, stream);
     }
-    e = dispatch_build<DkdvLaunch, D>(pb, tq128, tk, tv, tdo128, kp, grid, stream);
+    // dK and dV leave through TMA stores of the same 64-column x 128-row boxes
+    CUtensorMap tdk, tdv;
+    if (!make_bshd_tmap(&tdk, a.dk, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, 128) ||
+        !make_bshd_tmap(&tdv, a.dv, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, 128))
+      return cudaErrorInvalidValue;
+    e = dispatch_build<DkdvLaunch, D>(pb, tq128, tk, tv, tdo128, tdk, tdv, kp, grid, stream);
     if (e != cudaSuccess) return e;
   }
   // dQ pass
@@ -867,7 +871,9 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
     kp.n_pairs = pb.B * pb.Hq;
     kp.pair_group = l2_pair_group(2l * pb.Lkv * D * 2, kp.n_pairs, pb.G);
     dim3 grid(kp.n_pairs * kp.n_tiles);
-    return dispatch_build<DqLaunch, D>(pb, tq128, tk, tv, tdo128, kp, grid, stream);
+    CUtensorMap tdq;
+    if (!make_bshd_tmap(&tdq, a.dq, elem, pb.B, pb.Lq, pb.Hq, pb.d, 64, 128)) return cudaErrorInvalidValue;
+    return dispatch_build<DqLaunch, D>(pb, tq128, tk, tv, tdo128, tdq, kp, grid, stream);
   }
 }
 
