@@ -1,6 +1,6 @@
 // Pieces shared by the backward kernels (two-pass dK/dV, dQ, single pass):
-// kernel parameters, the TMEM -> 16-bit row stores (direct, or staged for a
-// TMA store) and the probability half of the dK/dV softmax.
+// kernel parameters, the TMEM -> bf16 row store and the probability half of
+// the dK/dV softmax.
 #pragma once
 #include "attn_internal.h"
 
@@ -55,37 +55,6 @@ __device__ __forceinline__ void store_row16(uint32_t taddr, uint16_t* dst, float
 #pragma unroll
       for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
     }
-  }
-}
-
-// NC fp32 values of one TMEM row from `taddr` on, times `mul`, in the 16-bit
-// format into columns [col0, col0 + NC) (col0 a multiple of 32) of row r of a
-// tile staged for a TMA store: boxes of 64 columns x 128 rows, 128-byte
-// swizzled (16-byte chunk c of row r at chunk c ^ (r & 7)), one box every
-// 16 KB.  With `zero` the row is written as zeros.  Across a warp (32
-// consecutive rows) every 16-byte store touches 8 distinct bank groups, 4
-// lanes each: 4 wavefronts per 512 bytes, the minimum.
-template <int NC, bool kF16>
-__device__ __forceinline__ void stage_row16(uint32_t taddr, uint8_t* tile, int r, float mul, bool zero,
-                                            int col0 = 0) {
-#pragma unroll
-  for (int c = 0; c < NC / 32; ++c) {
-    uint32_t v[32];
-    if (!zero) {
-      tmem_ld32(taddr + c * 32, v);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = 0u;
-    }
-    uint32_t pk[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) pk[i] = pack2<kF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
-    const int g = col0 / 32 + c;  // 32-column group of the tile
-    uint8_t* row = tile + (g >> 1) * (128 * 128) + r * 128;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      *reinterpret_cast<uint4*>(row + ((((g & 1) * 4 + j) ^ (r & 7)) << 4)) =
-          make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
   }
 }
 

@@ -83,7 +83,8 @@ struct FwdKParams {
 template <int D, bool kLeftBound, bool kF16, bool kSeg>
 __global__ void __launch_bounds__(320, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const FwdKParams p) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const FwdKParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -410,19 +411,17 @@ __global__ void __launch_bounds__(320, 1)
       const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
       // a piece of a split stream writes fp32 partials, a whole stream the output
       const size_t prow = ((static_cast<size_t>(b) * p.Hq + hq) * p.n_split + sp) * p.Lq + row;
-      uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
-                            ((static_cast<size_t>(b) * p.Lq + row) * p.Hq + hq) * p.dh;
+      if (split) {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        if (c * 32 >= p.dh) break;
-        uint32_t r[32];
-        if (n_x > 0) {
-          tmem_ld32(o_addr + c * 32, r);
-        } else {
+        for (int c = 0; c < D / 32; ++c) {
+          if (c * 32 >= p.dh) break;
+          uint32_t r[32];
+          if (n_x > 0) {
+            tmem_ld32(o_addr + c * 32, r);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = 0u;
-        }
-        if (split) {
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
           if (row < p.Lq) {
             float4* dst = reinterpret_cast<float4*>(p.o_part + prow * p.dh + c * 32);
 #pragma unroll
@@ -430,17 +429,15 @@ __global__ void __launch_bounds__(320, 1)
               dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
                                    __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
           }
-          continue;
         }
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack2<kF16>(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
-        if (row < p.Lq) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
+      } else {
+        // O goes through this tile's Q buffer, idle once o_full[x] has
+        // completed (every MMA of the tile is done), and out with TMA stores
+        // below, which clip the rows past Lq and the columns past the stored
+        // head_dim (a store of each thread's own row would put 32 rows, a row
+        // stride apart, into every store instruction)
+        stage_row16<D, kF16>(o_addr, sQ + x * C::kQTileBytes, wq * 32 + lane, inv_l, n_x == 0);
+        fence_proxy_async_smem();
       }
       if (row < p.Lq) {
         const float lv = l_sum > 0.f ? (m_used + lg2_approx(l_sum)) * kLn2 : -INFINITY;
@@ -448,6 +445,19 @@ __global__ void __launch_bounds__(320, 1)
           p.lse_part[prow] = lv;
         else
           p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Lq + row] = lv;
+      }
+    }
+    if (!split) {
+      // every thread of this softmax warpgroup reaches this point (a failed
+      // wait only skips work)
+      const int row0 = qb * 2 * kBM + x * kBM;
+      named_barrier_sync(2 + x, kBM);
+      if ((threadIdx.x & (kBM - 1)) == 0 && *abort_flag == 0 && row0 < p.Lq) {
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_store_4d(&tm_o, sQ + x * C::kQTileBytes + c * C::kBoxBytes, c * 64, row0, hq, b);
+        tma_store_commit();
+        tma_store_wait_read();  // the shared memory is released when the CTA exits
       }
     }
     if (split) {
@@ -531,13 +541,13 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int D, bool kLeftBound, bool kF16, bool kSeg = false>
 cudaError_t launch_fwd_inst(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const FwdKParams& kp, dim3 grid, cudaStream_t stream) {
+                            const CUtensorMap& to, const FwdKParams& kp, dim3 grid, cudaStream_t stream) {
   using C = FwdCfg<D>;
   cudaError_t e = ensure_dynamic_smem<fwd_tc_kernel<D, kLeftBound, kF16, kSeg>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   KernelTimer kt("fwd", stream);
   return launch_overlapping(fwd_tc_kernel<D, kLeftBound, kF16, kSeg>, grid, C::kThreads, C::kSmemBytes, stream, tq, tk,
-                            tv, kp);
+                            tv, to, kp);
 }
 
 template <int D>
@@ -548,6 +558,8 @@ cudaError_t launch_fwd_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t stream
   if (!make_bshd_tmap(&tq, a.q, elem, pb.B, pb.Lq, pb.Hq, pb.d, 64, kBM)) return cudaErrorInvalidValue;
   if (!make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, kBN)) return cudaErrorInvalidValue;
   if (!make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, kBN)) return cudaErrorInvalidValue;
+  CUtensorMap to;  // the output leaves through TMA stores of the query tiles' boxes
+  if (!make_bshd_tmap(&to, a.o, elem, pb.B, pb.Lq, pb.Hq, pb.d, 64, kBM)) return cudaErrorInvalidValue;
   FwdKParams kp;
   kp.o = a.o;
   kp.lse = a.lse;
@@ -581,13 +593,13 @@ cudaError_t launch_fwd_d(const FwdArgs& a, DeviceStatus* st, cudaStream_t stream
   // split key ranges run in the left-bounded builds (their streams start anywhere)
   const bool left = pb.wl < kWinInf || kp.n_split > 1;
   if (pb.q_seg != nullptr)  // segment masks run the general (two-sided span) build
-    return pb.f16 ? launch_fwd_inst<D, true, true, true>(tq, tk, tv, kp, grid, stream)
-                  : launch_fwd_inst<D, true, false, true>(tq, tk, tv, kp, grid, stream);
+    return pb.f16 ? launch_fwd_inst<D, true, true, true>(tq, tk, tv, to, kp, grid, stream)
+                  : launch_fwd_inst<D, true, false, true>(tq, tk, tv, to, kp, grid, stream);
   if (pb.f16)
-    return left ? launch_fwd_inst<D, true, true>(tq, tk, tv, kp, grid, stream)
-                : launch_fwd_inst<D, false, true>(tq, tk, tv, kp, grid, stream);
-  return left ? launch_fwd_inst<D, true, false>(tq, tk, tv, kp, grid, stream)
-              : launch_fwd_inst<D, false, false>(tq, tk, tv, kp, grid, stream);
+    return left ? launch_fwd_inst<D, true, true>(tq, tk, tv, to, kp, grid, stream)
+                : launch_fwd_inst<D, false, true>(tq, tk, tv, to, kp, grid, stream);
+  return left ? launch_fwd_inst<D, true, false>(tq, tk, tv, to, kp, grid, stream)
+              : launch_fwd_inst<D, false, false>(tq, tk, tv, to, kp, grid, stream);
 }
 
 }  // namespace
