@@ -115,15 +115,17 @@ __device__ __forceinline__ uint32_t segment_bits32(const int32_t* ids, int col, 
 // sums dQ into kp.dq_acc (grid = KV heads x batch x key tiles), then the dQ
 // convert over n_dq values.  ordered: the sums of each query tile run in
 // key-tile order (bitwise reproducible); otherwise as the adds arrive.  All
-// four tensor maps use boxes of 64 columns x 128 rows.
+// six tensor maps (inputs, and dK/dV for the epilogue's stores) use boxes of
+// 64 columns x 128 rows.
 template <int D>
 cudaError_t launch_single_pass(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, long n_dq, bool f16,
-                               bool ordered, cudaStream_t stream);
+                               const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                               const BwdKParams& kp, dim3 grid, long n_dq, bool f16, bool ordered,
+                               cudaStream_t stream);
 template <int D>
 cudaError_t launch_single_pass_ordered(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                       const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, long n_dq, bool f16,
-                                       cudaStream_t stream);
+                                       const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                                       const BwdKParams& kp, dim3 grid, long n_dq, bool f16, cudaStream_t stream);
 
 }  // namespace bwd
 }  // namespace attn

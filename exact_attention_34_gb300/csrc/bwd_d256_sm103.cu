@@ -55,31 +55,6 @@ __device__ __forceinline__ void issue_accumulate(uint32_t acc_tmem, uint32_t a_t
              (acc || k > 0) ? 1u : 0u);
 }
 
-// Store accumulator columns [128 half, 128 half + 128) of this thread's TMEM
-// lane, times `mul`, into the same columns of a 16-bit row (zeros when `zero`).
-template <bool kF16>
-__device__ __forceinline__ void store_acc_half(uint32_t taddr, uint16_t* dst, int half, float mul, bool do_store,
-                                               bool zero) {
-#pragma unroll 1
-  for (int c = 4 * half; c < 4 * half + 4; ++c) {
-    uint32_t r[32];
-    if (!zero) {
-      tmem_ld32(taddr + c * 32, r);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) r[i] = 0u;
-    }
-    uint32_t pk[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) pk[i] = pack2<kF16>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
-    if (do_store) {
-      uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-    }
-  }
-}
-
 // Pack 32 fp32 values (columns [32 wg, 32 wg + 32) of a step) to 16-bit and
 // write them over the first 16 of the TMEM columns they were read from, so
 // the two warpgroups never write where the other still reads.
@@ -113,7 +88,7 @@ template <bool kF16, bool kSeg>
 __global__ void __launch_bounds__(kThreads, 1)
     dq256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                 const BwdKParams p) {
+                 const __grid_constant__ CUtensorMap tm_out, const BwdKParams p) {
   using C = DqCfg256;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -303,11 +278,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&ds_full[buf]);
     }
     if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 119));
+    // dQ goes through the Q tile, idle once every MMA has completed, and out
+    // with TMA stores that clip the rows past Lq; warpgroup wg stages
+    // columns [128 wg, 128 wg + 128)
     if (ok) {
       tc_fence_after();
-      const bool st = i < p.Lq;
-      uint16_t* dst = reinterpret_cast<uint16_t*>(p.dq) + ((static_cast<size_t>(b) * p.Lq + (st ? i : 0)) * p.Hq + h) * kD;
-      store_acc_half<kF16>(t_lane + 256, dst, wg, p.scale, st, T == 0);
+      stage_row16<128, kF16>(t_lane + 256 + 128 * wg, sQ, wq * 32 + lane, p.scale, T == 0, 128 * wg);
+      fence_proxy_async_smem();
+    }
+    named_barrier_sync(1, 256);  // every P/dS thread gets here (a failed wait only skips work)
+    if (threadIdx.x == 0 && *abort_flag == 0) {
+#pragma unroll
+      for (int c = 0; c < kD / 64; ++c) tma_store_4d(&tm_out, sQ + c * kBigBox, c * 64, q0, h, b);
+      tma_store_commit();
+      tma_store_wait_read();  // the shared memory is released when the CTA exits
     }
   }
 
@@ -351,6 +335,7 @@ template <bool kDK, bool kF16, bool kSeg>
 __global__ void __launch_bounds__(kThreads, 1)
     key256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_out,
                   const BwdKParams p) {
   using C = KeyCfg256<kDK>;
   extern __shared__ uint8_t smem_raw[];
@@ -610,12 +595,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&p_full[buf]);
     }
     if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, 131));
+    // dK or dV goes through the K tile, idle once every MMA has completed,
+    // and out with TMA stores that clip the rows past Lkv; warpgroup wg
+    // stages columns [128 wg, 128 wg + 128)
     if (ok) {
       tc_fence_after();
-      const bool st = j < p.Lkv;
-      uint16_t* dst = reinterpret_cast<uint16_t*>(kDK ? p.dk : p.dv) +
-                      ((static_cast<size_t>(b) * p.Lkv + (st ? j : 0)) * p.Hkv + hk) * kD;
-      store_acc_half<kF16>(t_lane + 256, dst, wg, kDK ? p.scale : 1.0f, st, T == 0);
+      stage_row16<128, kF16>(t_lane + 256 + 128 * wg, sK, wq * 32 + lane, kDK ? p.scale : 1.0f, T == 0, 128 * wg);
+      fence_proxy_async_smem();
+    }
+    named_barrier_sync(1, 256);  // every P/dS thread gets here (a failed wait only skips work)
+    if (threadIdx.x == 0 && *abort_flag == 0) {
+#pragma unroll
+      for (int c = 0; c < kD / 64; ++c) tma_store_4d(&tm_out, sK + c * kBigBox, c * 64, j0, hk, b);
+      tma_store_commit();
+      tma_store_wait_read();  // the shared memory is released when the CTA exits
     }
   }
 
@@ -632,23 +625,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <bool kF16, bool kSeg>
 cudaError_t launch_dq256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                         const BwdKParams& kp, dim3 grid, cudaStream_t stream) {
+                         const CUtensorMap& tout, const BwdKParams& kp, dim3 grid, cudaStream_t stream) {
   cudaError_t e = ensure_dynamic_smem<dq256_kernel<kF16, kSeg>>(DqCfg256::kSmemBytes);
   if (e != cudaSuccess) return e;
   KernelTimer kt("bwd_dq", stream);
   return launch_overlapping(dq256_kernel<kF16, kSeg>, grid, kThreads, DqCfg256::kSmemBytes, stream, tq, tk, tv, tdo,
-                            kp);
+                            tout, kp);
 }
 
 template <bool kDK, bool kF16, bool kSeg>
 cudaError_t launch_key256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                          const BwdKParams& kp, dim3 grid, cudaStream_t stream) {
+                          const CUtensorMap& tout, const BwdKParams& kp, dim3 grid, cudaStream_t stream) {
   using C = KeyCfg256<kDK>;
   cudaError_t e = ensure_dynamic_smem<key256_kernel<kDK, kF16, kSeg>>(C::kSmemBytes);
   if (e != cudaSuccess) return e;
   KernelTimer kt(kDK ? "bwd_dk" : "bwd_dv", stream);
   return launch_overlapping(key256_kernel<kDK, kF16, kSeg>, grid, kThreads, C::kSmemBytes, stream, tq, tk, tv, tdo,
-                            kp);
+                            tout, kp);
 }
 
 template <bool kF16, bool kSeg>
@@ -666,10 +659,15 @@ cudaError_t run_bwd256(const BwdArgs& a, BwdKParams kp, cudaStream_t stream) {
     kp.n_tiles = (pb.Lkv + kRows - 1) / kRows;
     kp.n_pairs = pb.B * pb.Hkv;
     kp.pair_group = l2_pair_group(2l * pb.G * pb.Lq * kD * 2, kp.n_pairs, 1);
+    // dV and dK leave through TMA stores of 64-column x 128-row boxes
+    CUtensorMap tdv, tdk;
+    if (!make_bshd_tmap(&tdv, a.dv, elem, pb.B, pb.Lkv, pb.Hkv, kD, 64, kRows) ||
+        !make_bshd_tmap(&tdk, a.dk, elem, pb.B, pb.Lkv, pb.Hkv, kD, 64, kRows))
+      return cudaErrorInvalidValue;
     const dim3 grid(kp.n_pairs * kp.n_tiles);
-    e = launch_key256<false, kF16, kSeg>(tq, tk, tv, tdo, kp, grid, stream);
+    e = launch_key256<false, kF16, kSeg>(tq, tk, tv, tdo, tdv, kp, grid, stream);
     if (e != cudaSuccess) return e;
-    e = launch_key256<true, kF16, kSeg>(tq, tk, tv, tdo, kp, grid, stream);
+    e = launch_key256<true, kF16, kSeg>(tq, tk, tv, tdo, tdk, kp, grid, stream);
     if (e != cudaSuccess) return e;
   }
   {  // dQ: stationary Q/dO tiles of 128 rows, streamed K/V tiles of 64
@@ -682,8 +680,10 @@ cudaError_t run_bwd256(const BwdArgs& a, BwdKParams kp, cudaStream_t stream) {
     kp.n_tiles = (pb.Lq + kRows - 1) / kRows;
     kp.n_pairs = pb.B * pb.Hq;
     kp.pair_group = l2_pair_group(2l * pb.Lkv * kD * 2, kp.n_pairs, pb.G);
+    CUtensorMap tdq;
+    if (!make_bshd_tmap(&tdq, a.dq, elem, pb.B, pb.Lq, pb.Hq, kD, 64, kRows)) return cudaErrorInvalidValue;
     const dim3 grid(kp.n_pairs * kp.n_tiles);
-    return launch_dq256<kF16, kSeg>(tq, tk, tv, tdo, kp, grid, stream);
+    return launch_dq256<kF16, kSeg>(tq, tk, tv, tdo, tdq, kp, grid, stream);
   }
 }
 

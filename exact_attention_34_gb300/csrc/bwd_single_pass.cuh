@@ -96,6 +96,9 @@ struct DkdvAtomicCfg {
 // parity, "turn granted" and "adds issued", each over the four reduction
 // warps and that parity's turn keeper.
 constexpr int kBarTurn = 1, kBarDone = 3, kBarThreads = 160;
+// Named barrier of the epilogue: the eight softmax warps, before the dK/dV
+// TMA stores.
+constexpr int kBarStore = 5;
 
 // Query tiles [i_begin, i_begin + steps) that see some key of the key tile
 // starting at j0 (of a sequence with kvl valid keys): from the first row that
@@ -164,6 +167,7 @@ template <int D, bool kLeftBound, bool kF16, bool kSeg, bool kOrdered>
 __global__ void __launch_bounds__(512, 1)
     bwd_dkdv_single_pass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                                const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                                 const BwdKParams p) {
   using C = DkdvAtomicCfg<D>;
   constexpr int NS = C::kStages, BM = C::kBM;
@@ -488,14 +492,25 @@ __global__ void __launch_bounds__(512, 1)
       mbar_arrive(ds_ready);
     }
     if (ok && T > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag, p.status, kSite + 12));
+    // dK (warpgroup 0, times scale) and dV (warpgroup 1) go through the Q/dO
+    // stages, idle once every MMA has completed (the reduction warps read
+    // dQ^T from TMEM only), and out with TMA stores that clip the rows past
+    // Lkv and the columns past the stored head_dim
     if (ok) {
       tc_fence_after();
-      const bool st = j < p.Lkv;
-      const size_t off = ((static_cast<size_t>(b) * p.Lkv + (st ? j : 0)) * p.Hkv + hk) * p.dh;
-      if (w == 0)
-        store_row16<D, kF16>(t_lane + 0, reinterpret_cast<uint16_t*>(p.dk) + off, p.scale, st, T == 0, p.dh);
-      else
-        store_row16<D, kF16>(t_lane + 128, reinterpret_cast<uint16_t*>(p.dv) + off, 1.0f, st, T == 0, p.dh);
+      stage_row16<D, kF16>(t_lane + (w == 0 ? 0 : 128), sQ + w * (D / 64) * C::kBox, r, w == 0 ? p.scale : 1.0f,
+                           T == 0);
+      fence_proxy_async_smem();
+    }
+    named_barrier_sync(kBarStore, 256);
+    if (threadIdx.x == 0 && *abort_flag == 0) {
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_store_4d(&tm_dk, sQ + c * C::kBox, c * 64, j0, hk, b);
+        tma_store_4d(&tm_dv, sQ + (D / 64 + c) * C::kBox, c * 64, j0, hk, b);
+      }
+      tma_store_commit();
+      tma_store_wait_read();  // the shared memory is released when the CTA exits
     }
   }
 
@@ -523,8 +538,8 @@ __global__ void dq_convert_kernel(const float* __restrict__ acc, uint16_t* __res
 
 template <int D, bool kLeftBound, bool kF16, bool kSeg, bool kOrdered>
 cudaError_t launch_single_pass_inst(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                    const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, long n_dq,
-                                    cudaStream_t stream) {
+                                    const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                                    const BwdKParams& kp, dim3 grid, long n_dq, cudaStream_t stream) {
   using C = DkdvAtomicCfg<D>;
   constexpr auto kern = bwd_dkdv_single_pass_kernel<D, kLeftBound, kF16, kSeg, kOrdered>;
   cudaError_t e = ensure_dynamic_smem<kern>(C::kSmemBytes);
@@ -532,10 +547,10 @@ cudaError_t launch_single_pass_inst(const CUtensorMap& tq, const CUtensorMap& tk
   {
     KernelTimer kt(kOrdered ? "bwd_dkdv_ordered" : "bwd_dkdv_atomic", stream);
     if (kOrdered) {
-      kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, kp);
+      kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tdo, tdk, tdv, kp);
       e = cudaGetLastError();
     } else {
-      e = launch_overlapping(kern, grid, C::kThreads, C::kSmemBytes, stream, tq, tk, tv, tdo, kp);
+      e = launch_overlapping(kern, grid, C::kThreads, C::kSmemBytes, stream, tq, tk, tv, tdo, tdk, tdv, kp);
     }
   }
   if (e != cudaSuccess) return e;
@@ -547,19 +562,26 @@ cudaError_t launch_single_pass_inst(const CUtensorMap& tq, const CUtensorMap& tk
 
 // The kernel build for a problem: format x (no left bound | two-sided span |
 // two-sided span + segment ids).
+// Compile-time flags of one kernel build: left window bound, fp16, segment ids.
+template <bool L, bool F, bool S>
+struct Build {
+  static constexpr bool kL = L, kF = F, kS = S;
+};
+
 template <int D, bool kOrdered>
 cudaError_t launch_single_pass_build(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                     const CUtensorMap& tdo, const BwdKParams& kp, dim3 grid, long n_dq, bool f16,
-                                     cudaStream_t stream) {
+                                     const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                                     const BwdKParams& kp, dim3 grid, long n_dq, bool f16, cudaStream_t stream) {
   const bool left = kp.wl < kWinInf;
+  // (left bound, fp16, segment ids) of the build
+  auto run = [&](auto build) {
+    return launch_single_pass_inst<D, decltype(build)::kL, decltype(build)::kF, decltype(build)::kS, kOrdered>(
+        tq, tk, tv, tdo, tdk, tdv, kp, grid, n_dq, stream);
+  };
   if (kp.q_seg != nullptr)  // segment masks run the general (two-sided span) build
-    return f16 ? launch_single_pass_inst<D, true, true, true, kOrdered>(tq, tk, tv, tdo, kp, grid, n_dq, stream)
-               : launch_single_pass_inst<D, true, false, true, kOrdered>(tq, tk, tv, tdo, kp, grid, n_dq, stream);
-  if (f16)
-    return left ? launch_single_pass_inst<D, true, true, false, kOrdered>(tq, tk, tv, tdo, kp, grid, n_dq, stream)
-                : launch_single_pass_inst<D, false, true, false, kOrdered>(tq, tk, tv, tdo, kp, grid, n_dq, stream);
-  return left ? launch_single_pass_inst<D, true, false, false, kOrdered>(tq, tk, tv, tdo, kp, grid, n_dq, stream)
-              : launch_single_pass_inst<D, false, false, false, kOrdered>(tq, tk, tv, tdo, kp, grid, n_dq, stream);
+    return f16 ? run(Build<true, true, true>{}) : run(Build<true, false, true>{});
+  if (f16) return left ? run(Build<true, true, false>{}) : run(Build<false, true, false>{});
+  return left ? run(Build<true, false, false>{}) : run(Build<false, false, false>{});
 }
 
 }  // namespace

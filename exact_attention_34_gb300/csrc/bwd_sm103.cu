@@ -849,19 +849,20 @@ cudaError_t launch_bwd_d(const BwdArgs& a, DeviceStatus* st, cudaStream_t stream
     kp.n_pairs = pb.B * pb.Hkv;
     kp.pair_group = l2_pair_group(2l * pb.G * pb.Lq * D * 2, kp.n_pairs, 1);
     dim3 grid(kp.n_pairs * kp.n_tiles);
-    if (a.deterministic != 1) {
-      if (a.deterministic == 2) {  // turn counters and the work-item ticket start at zero
-        e = cudaMemsetAsync(a.dq_turn, 0, a.turn_bytes, stream);
-        if (e != cudaSuccess) return e;
-      }
-      return launch_single_pass<D>(tq128, tk, tv, tdo128, kp, grid, static_cast<long>(pb.B) * pb.Lq * pb.Hq * pb.d,
-                                   pb.f16 != 0, a.deterministic == 2, stream);
-    }
     // dK and dV leave through TMA stores of the same 64-column x 128-row boxes
     CUtensorMap tdk, tdv;
     if (!make_bshd_tmap(&tdk, a.dk, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, 128) ||
         !make_bshd_tmap(&tdv, a.dv, elem, pb.B, pb.Lkv, pb.Hkv, pb.d, 64, 128))
       return cudaErrorInvalidValue;
+    if (a.deterministic != 1) {
+      if (a.deterministic == 2) {  // turn counters and the work-item ticket start at zero
+        e = cudaMemsetAsync(a.dq_turn, 0, a.turn_bytes, stream);
+        if (e != cudaSuccess) return e;
+      }
+      return launch_single_pass<D>(tq128, tk, tv, tdo128, tdk, tdv, kp, grid,
+                                   static_cast<long>(pb.B) * pb.Lq * pb.Hq * pb.d, pb.f16 != 0, a.deterministic == 2,
+                                   stream);
+    }
     e = dispatch_build<DkdvLaunch, D>(pb, tq128, tk, tv, tdo128, tdk, tdv, kp, grid, stream);
     if (e != cudaSuccess) return e;
   }

@@ -60,7 +60,8 @@ struct Fwd256Params {
 template <bool kF16, bool kSeg>
 __global__ void __launch_bounds__(Cfg256::kThreads, 1)
     fwd_d256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const Fwd256Params p) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const Fwd256Params p) {
   using C = Cfg256;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -335,29 +336,22 @@ __global__ void __launch_bounds__(Cfg256::kThreads, 1)
     if (ok) {
       tc_fence_after();
       const float inv_l = l_sum > 0.f ? 1.0f / l_sum : 0.f;
-      uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + ((static_cast<size_t>(b) * p.Lq + row) * p.Hq + hq) * kD;
+      // O goes through the Q buffer, idle once o_final has completed (every
+      // MMA is done), and out with TMA stores that clip the rows past Lq
 #pragma unroll 1
-      for (int c = 0; c < kD / 32; ++c) {
-        uint32_t r[32];
-        if (n > 0) {
-          tmem_ld32(o_addr + c * 32, r);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = 0u;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack2<kF16>(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
-        if (row < p.Lq) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
-      }
+      for (int h = 0; h < kD / 64; ++h)
+        stage_row16<64, kF16>(o_addr + h * 64, sQ, warp * 32 + lane, inv_l, n == 0, h * 64);
+      fence_proxy_async_smem();
       if (row < p.Lq)
         p.lse[(static_cast<size_t>(b) * p.Hq + hq) * p.Lq + row] =
             l_sum > 0.f ? (m_used + lg2_approx(l_sum)) * kLn2 : -INFINITY;
+    }
+    named_barrier_sync(1, kBM);  // every softmax thread gets here (a failed wait only skips work)
+    if (threadIdx.x == 0 && *abort_flag == 0 && row0 < p.Lq) {
+#pragma unroll
+      for (int h = 0; h < kD / 64; ++h) tma_store_4d(&tm_o, sQ + h * C::kQBox, h * 64, row0, hq, b);
+      tma_store_commit();
+      tma_store_wait_read();  // the shared memory is released when the CTA exits
     }
   }
 
@@ -371,12 +365,12 @@ __global__ void __launch_bounds__(Cfg256::kThreads, 1)
 
 template <bool kF16, bool kSeg>
 cudaError_t launch_fwd256_inst(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const Fwd256Params& kp, dim3 grid, cudaStream_t stream) {
+                               const CUtensorMap& to, const Fwd256Params& kp, dim3 grid, cudaStream_t stream) {
   cudaError_t e = ensure_dynamic_smem<fwd_d256_kernel<kF16, kSeg>>(Cfg256::kSmemBytes);
   if (e != cudaSuccess) return e;
   KernelTimer kt("fwd", stream);
   return launch_overlapping(fwd_d256_kernel<kF16, kSeg>, grid, Cfg256::kThreads, Cfg256::kSmemBytes, stream, tq, tk, tv,
-                            kp);
+                            to, kp);
 }
 
 }  // namespace
@@ -388,6 +382,8 @@ cudaError_t launch_fwd_d256(const FwdArgs& a, DeviceStatus* st, cudaStream_t str
   if (!make_bshd_tmap(&tq, a.q, elem, pb.B, pb.Lq, pb.Hq, kD, 64, kBM)) return cudaErrorInvalidValue;
   if (!make_bshd_tmap(&tk, a.k, elem, pb.B, pb.Lkv, pb.Hkv, kD, 64, kBN)) return cudaErrorInvalidValue;
   if (!make_bshd_tmap(&tv, a.v, elem, pb.B, pb.Lkv, pb.Hkv, kD, 64, kBN)) return cudaErrorInvalidValue;
+  CUtensorMap to;  // the output leaves through TMA stores of the query tile's boxes
+  if (!make_bshd_tmap(&to, a.o, elem, pb.B, pb.Lq, pb.Hq, kD, 64, kBM)) return cudaErrorInvalidValue;
   Fwd256Params kp;
   kp.o = a.o;
   kp.lse = a.lse;
@@ -413,10 +409,10 @@ cudaError_t launch_fwd_d256(const FwdArgs& a, DeviceStatus* st, cudaStream_t str
   kp.status = st;
   const dim3 grid(kp.n_pairs * kp.n_qtiles);
   if (pb.q_seg != nullptr)
-    return pb.f16 ? launch_fwd256_inst<true, true>(tq, tk, tv, kp, grid, stream)
-                  : launch_fwd256_inst<false, true>(tq, tk, tv, kp, grid, stream);
-  return pb.f16 ? launch_fwd256_inst<true, false>(tq, tk, tv, kp, grid, stream)
-                : launch_fwd256_inst<false, false>(tq, tk, tv, kp, grid, stream);
+    return pb.f16 ? launch_fwd256_inst<true, true>(tq, tk, tv, to, kp, grid, stream)
+                  : launch_fwd256_inst<false, true>(tq, tk, tv, to, kp, grid, stream);
+  return pb.f16 ? launch_fwd256_inst<true, false>(tq, tk, tv, to, kp, grid, stream)
+                : launch_fwd256_inst<false, false>(tq, tk, tv, to, kp, grid, stream);
 }
 
 }  // namespace attn
